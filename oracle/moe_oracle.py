@@ -1,0 +1,425 @@
+"""Plain CPU oracle for the forward pass of a top-K routed Mixture-of-Experts
+SwiGLU FFN layer with always-on shared experts.
+
+TEST INFRASTRUCTURE ONLY. The product path never imports, calls or runs this
+module; only the tests, the smoke check in ``__graft_entry__`` and the
+``cpu_baseline`` / reference leg of ``bench.py`` use it. It shares no code
+with the CUDA library (no kernels, headers, tables or helpers).
+
+Arithmetic is float64 on the exact input values (BF16 and FP32 inputs convert
+to float64 without rounding), with NumPy's matmul and sort as the only library
+steps. The exception is the quantile bias update, whose page works on FP32
+scores; it is written in FP32 where the page computes in FP32.
+
+Sources, cited as page title + section:
+
+* [APEX-MoE] APEX-1 docs "10 - Mixture of Experts", class ``MoEFFN``: router
+  Linear without bias, expert bias added to the scores, top-K, softmax over
+  the selected scores, per-expert dispatch, shared experts on every token.
+* [APEX-M3] APEX-1 Mathematical Reference Part 3: section 12 (SwiGLU FFN,
+  SiLU), section 13 (MoE output, router, routing weights), section 14
+  (bias-based load balancing).
+* [K3-SLM] kimi_k3 "StableLatentMoE and QuantileBalancer": FP32 sigmoid router,
+  top-(K+1) of bias-corrected scores, weights from uncorrected scores, stable
+  argsort dispatch, latent down/up projections, quantile balancer update.
+* [MoE-FS] "MoE from scratch" tutorial ("A working MoE layer in PyTorch"):
+  ``SwiGLU``, ``MoELayer`` (softmax over all experts, top-K, renormalise,
+  sorted dispatch) and its ``naive_forward`` reference.
+
+Readings where the pages are silent or disagree (each is listed in the design doc):
+ties in top-K go to the lower expert index; slot k holds the k-th largest
+score; in the softmax modes the balance bias is added to the logits before
+the score; the quantile rank is computed in FP32 as the FP32 quantile would;
+the mean in the bias update is a sequential float64 sum rounded once to FP32.
+
+Every function here is pinned by ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+GATE_SOFTMAX_TOPK = "softmax_topk"
+GATE_SOFTMAX_ALL_RENORM = "softmax_all_renorm"
+GATE_SIGMOID = "sigmoid"
+
+
+def f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------
+# SwiGLU expert  [APEX-M3] section 12.2-12.3; [MoE-FS] class SwiGLU
+# --------------------------------------------------------------------------
+
+def sigmoid(a):
+    """sigma(a) = 1 / (1 + e^-a)."""
+    a = f64(a)
+    return 1.0 / (1.0 + np.exp(-a))
+
+
+def silu(a):
+    """SiLU(a) = a * sigma(a) = a / (1 + e^-a)  ([APEX-M3] section 12.3)."""
+    a = f64(a)
+    return a / (1.0 + np.exp(-a))
+
+
+def swiglu_hidden(x, W_gate, W_up):
+    """SiLU(x W_gate) (elementwise *) (x W_up): the gated hidden vector of
+    section 12.2, for one token x [d] or a row block x [n, d]."""
+    x = f64(x)
+    return silu(x @ f64(W_gate)) * (x @ f64(W_up))
+
+
+def swiglu_ffn(x, W_gate, W_up, W_down):
+    """FFN(x) = W_down( SiLU(x W_gate) * (x W_up) )  ([APEX-M3] section 12.2).
+
+    W_gate, W_up are [d, d_ff]; W_down is [d_ff, d]; x is [d] or [n, d].
+    """
+    return swiglu_hidden(x, W_gate, W_up) @ f64(W_down)
+
+
+# --------------------------------------------------------------------------
+# Router  [APEX-MoE] steps 2-3; [APEX-M3] section 13.2 and 13.5;
+#         [MoE-FS] MoELayer.forward; [K3-SLM] "FP32 router and training-only QB update"
+# --------------------------------------------------------------------------
+
+def rank_experts(c):
+    """Expert ids ordered by score descending; among equal scores the lower
+    expert id comes first (the tie-break this build fixes)."""
+    c = f64(c)
+    return np.argsort(-c, axis=-1, kind="stable")
+
+
+def route_from_logits(r, bias, gate, K, renormalize=False, routed_scale=1.0):
+    """Route one token from its router logits r [E].
+
+    Returns a dict with
+      idx [K]        selected experts, slot k = k-th largest selection score
+      w [K]          gate weights
+      margin         c_(K) - c_(K+1): selection score at rank K minus rank K+1
+                     (1-based; +inf when K == E)
+      score [E]      the selection score c the ranking used
+      s [E]          sigmoid scores (sigmoid mode only)
+      top_scores     [K+1] the K+1 largest c, descending (sigmoid mode only)
+
+    Modes:
+      softmax_topk        c = r + b; top-K of c; g = softmax over the K selected
+                          c ([APEX-MoE] step 3, [APEX-M3] section 13.2)
+      softmax_all_renorm  p = softmax over all E of (r + b); top-K of p;
+                          g = p_sel / sum p_sel ([MoE-FS] MoELayer)
+      sigmoid             s = sigma(r); c = s + b; top-(K+1) of c, the first K
+                          used; g = s at the selected experts (uncorrected),
+                          optionally divided by its sum, times routed_scale
+                          ([K3-SLM] "FP32 router ..." and "Flatten routing ...")
+    """
+    r = f64(r)
+    E = r.shape[0]
+    b = np.zeros(E) if bias is None else f64(bias)
+    out = {}
+    if gate == GATE_SOFTMAX_TOPK:
+        c = r + b
+        order = rank_experts(c)
+        idx = order[:K]
+        sel = c[idx]
+        ex = np.exp(sel - sel[0])
+        w = ex / ex.sum()
+    elif gate == GATE_SOFTMAX_ALL_RENORM:
+        z = r + b
+        ez = np.exp(z - z.max())
+        p = ez / ez.sum()
+        c = p
+        order = rank_experts(c)
+        idx = order[:K]
+        w = p[idx] / p[idx].sum()
+    elif gate == GATE_SIGMOID:
+        s = sigmoid(r)
+        c = s + b
+        order = rank_experts(c)
+        top = order[:K + 1]
+        out["top_scores"] = c[top]
+        out["s"] = s
+        idx = top[:K]
+        w = s[idx].copy()
+        if renormalize:
+            w = w / w.sum()
+        w = w * routed_scale
+    else:
+        raise ValueError(f"unknown gate mode {gate!r}")
+    out["idx"] = idx.astype(np.int64)
+    out["w"] = w
+    out["score"] = c
+    out["margin"] = (c[order[K - 1]] - c[order[K]]) if K < E else math.inf
+    return out
+
+
+def router_logits(x, W_router):
+    """r = x W_router, FP32 inputs taken exactly, summed in float64
+    ([APEX-M3] section 13.2; [K3-SLM] F.linear on FP32 copies)."""
+    return f64(x) @ f64(W_router)
+
+
+def route(x, W_router, bias, gate, K, renormalize=False, routed_scale=1.0):
+    """Route every token of x [T, d]. Returns stacked arrays:
+    idx [T, K] int64, w [T, K], margin [T], and for sigmoid mode
+    top_scores [T, K+1] and s [T, E]."""
+    r = router_logits(x, W_router)
+    T = r.shape[0]
+    per = [route_from_logits(r[t], bias, gate, K, renormalize, routed_scale)
+           for t in range(T)]
+    res = {
+        "logits": r,
+        "idx": np.stack([p["idx"] for p in per]) if T else np.zeros((0, K), np.int64),
+        "w": np.stack([p["w"] for p in per]) if T else np.zeros((0, K)),
+        "margin": np.array([p["margin"] for p in per], dtype=np.float64),
+    }
+    if gate == GATE_SIGMOID:
+        res["top_scores"] = np.stack([p["top_scores"] for p in per])
+        res["s"] = np.stack([p["s"] for p in per])
+    return res
+
+
+def gates_for(r, bias, gate, idx, renormalize=False, routed_scale=1.0):
+    """Gate weights of one token for a GIVEN expert selection idx [K] (in slot
+    order). Used when the oracle adopts another router's selection for a
+    near-tie token: the weights follow the same formulas as route_from_logits."""
+    r = f64(r)
+    E = r.shape[0]
+    b = np.zeros(E) if bias is None else f64(bias)
+    idx = np.asarray(idx, dtype=np.int64)
+    if gate == GATE_SOFTMAX_TOPK:
+        sel = (r + b)[idx]
+        ex = np.exp(sel - sel.max())
+        return ex / ex.sum()
+    if gate == GATE_SOFTMAX_ALL_RENORM:
+        z = r + b
+        ez = np.exp(z - z.max())
+        p = ez / ez.sum()
+        return p[idx] / p[idx].sum()
+    if gate == GATE_SIGMOID:
+        w = sigmoid(r)[idx]
+        if renormalize:
+            w = w / w.sum()
+        return w * routed_scale
+    raise ValueError(gate)
+
+
+# --------------------------------------------------------------------------
+# Sorted dispatch  [K3-SLM] "Flatten routing and recover original token order",
+#                  "Dispatch is a stable permutation"; [MoE-FS] MoELayer.forward
+# --------------------------------------------------------------------------
+
+def dispatch(idx, E):
+    """Stable grouping of the T*K assignments by expert id.
+
+    Flat assignment j = t*K + k has expert idx[t, k]. A stable argsort of the
+    flat ids, written as a counting sort over j in ascending order, gives
+    order[pos] = j. Returns
+      counts [E]        assignments per expert (the bincount)
+      offsets [E+1]     exclusive prefix sum of counts (offsets[E] = T*K)
+      order [T*K]       flat index j placed at each sorted position
+      sorted_token [T*K] = order // K
+      sorted_slot [T*K]  = order %  K
+      inv [T, K]        sorted position of assignment (t, k)
+    """
+    idx = np.asarray(idx, dtype=np.int64)
+    T, K = idx.shape
+    flat = idx.reshape(-1)
+    if flat.size and (flat.min() < 0 or flat.max() >= E):
+        raise ValueError("expert id out of range")
+    counts = np.zeros(E, dtype=np.int64)
+    for e in flat:
+        counts[e] += 1
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    for e in range(E):
+        offsets[e + 1] = offsets[e] + counts[e]
+    fill = offsets[:E].copy()
+    order = np.empty(T * K, dtype=np.int64)
+    inv = np.empty(T * K, dtype=np.int64)
+    for j in range(T * K):
+        e = flat[j]
+        order[fill[e]] = j
+        inv[j] = fill[e]
+        fill[e] += 1
+    return {
+        "counts": counts,
+        "offsets": offsets,
+        "order": order,
+        "sorted_token": order // K,
+        "sorted_slot": order % K,
+        "inv": inv.reshape(T, K),
+    }
+
+
+# --------------------------------------------------------------------------
+# Layer forward  [APEX-M3] section 13.2; [APEX-MoE] steps 4-5;
+#                [MoE-FS] naive_forward; [K3-SLM] "Return to model width"
+# --------------------------------------------------------------------------
+
+class _WeightCache:
+    """float64 copies of expert matrices, made on first use."""
+
+    def __init__(self, params):
+        self.p = params
+        self.c = {}
+
+    def get(self, name, i=None):
+        key = (name, i)
+        if key not in self.c:
+            a = self.p[name]
+            a = a if i is None else a[i]
+            if hasattr(a, "detach"):
+                a = a.detach().float().cpu().numpy()
+            self.c[key] = f64(a)
+        return self.c[key]
+
+
+def _to_np(a):
+    if a is None:
+        return None
+    if hasattr(a, "detach"):
+        return a.detach().float().cpu().numpy()
+    return np.asarray(a)
+
+
+def moe_forward_token(xt, idx_t, w_t, params, cache=None):
+    """Output of one token x_t [d] given its selected experts and weights:
+
+        MoE(x) = sum_s Shared_s(x) + sum_k g_k Expert_{e_k}(x)
+
+    ([APEX-M3] section 13.2). In the latent variant the routed experts act on
+    z = x W_down_latent and the routed sum is projected back by W_up_latent
+    before it is added to the shared output ([K3-SLM] "Return to model width").
+    """
+    cache = cache or _WeightCache(params)
+    xt = f64(xt)
+    latent = params.get("W_down_latent") is not None
+    zt = xt @ cache.get("W_down_latent") if latent else xt
+    routed = np.zeros(zt.shape[0])
+    for k in range(len(idx_t)):
+        e = int(idx_t[k])
+        routed = routed + w_t[k] * swiglu_ffn(zt, cache.get("W_gate", e), cache.get("W_up", e),
+                                              cache.get("W_down", e))
+    if latent:
+        routed = routed @ cache.get("W_up_latent")
+    shared = np.zeros(xt.shape[0])
+    if params.get("Ws_gate") is not None:
+        for s in range(params["Ws_gate"].shape[0]):
+            shared = shared + swiglu_ffn(xt, cache.get("Ws_gate", s), cache.get("Ws_up", s),
+                                         cache.get("Ws_down", s))
+    return shared + routed
+
+
+def moe_forward(x, params, gate, K, renormalize=False, routed_scale=1.0,
+                tokens=None, routing=None):
+    """Per-token forward of the whole layer (the naive reference shape).
+
+    x [T, d]; params: dict with W_router, bias, W_gate, W_up, W_down, Ws_*,
+    W_down_latent, W_up_latent (torch tensors or arrays). ``tokens`` restricts
+    the computed rows (others are left NaN). ``routing`` = (idx [T, K], w [T, K])
+    replaces the oracle's own routing (used for near-tie tokens only).
+    Returns (out [T, d] float64, routing dict of the oracle's own route()).
+    """
+    xn = _to_np(x)
+    T = xn.shape[0]
+    rows = range(T) if tokens is None else tokens
+    sub = np.asarray(list(rows), dtype=np.int64)
+    rt = route(xn[sub], _to_np(params["W_router"]), _to_np(params.get("bias")), gate, K,
+               renormalize, routed_scale)
+    idx, w = rt["idx"], rt["w"]
+    if routing is not None:
+        idx = np.asarray(routing[0])[sub]
+        w = np.asarray(routing[1])[sub]
+    cache = _WeightCache(params)
+    out = np.full((T, xn.shape[1]), np.nan)
+    for i, t in enumerate(sub):
+        out[t] = moe_forward_token(xn[t], idx[i], w[i], params, cache)
+    return out, rt
+
+
+def moe_forward_sorted(x, params, gate, K, renormalize=False, routed_scale=1.0):
+    """Second formulation used only to cross-check the per-token one: group the
+    assignments with dispatch(), run each expert once on its contiguous block,
+    weight the rows, and scatter-add them back to their tokens
+    ([MoE-FS] MoELayer.forward; [K3-SLM] grouped execution semantics)."""
+    xn = f64(_to_np(x))
+    T = xn.shape[0]
+    rt = route(xn, _to_np(params["W_router"]), _to_np(params.get("bias")), gate, K,
+               renormalize, routed_scale)
+    E = params["W_gate"].shape[0]
+    dp = dispatch(rt["idx"], E)
+    cache = _WeightCache(params)
+    latent = params.get("W_down_latent") is not None
+    z = xn @ cache.get("W_down_latent") if latent else xn
+    xs = z[dp["sorted_token"]]
+    ws = rt["w"].reshape(-1)[dp["order"]]
+    ys = np.zeros_like(xs)
+    for e in range(E):
+        a, b = dp["offsets"][e], dp["offsets"][e + 1]
+        if b > a:
+            ys[a:b] = swiglu_ffn(xs[a:b], cache.get("W_gate", e), cache.get("W_up", e),
+                                 cache.get("W_down", e))
+    ys = ys * ws[:, None]
+    routed = np.zeros_like(z)
+    np.add.at(routed, dp["sorted_token"], ys)
+    if latent:
+        routed = routed @ cache.get("W_up_latent")
+    shared = np.zeros_like(xn)
+    if params.get("Ws_gate") is not None:
+        for s in range(params["Ws_gate"].shape[0]):
+            shared = shared + swiglu_ffn(xn, cache.get("Ws_gate", s), cache.get("Ws_up", s),
+                                         cache.get("Ws_down", s))
+    return shared + routed
+
+
+# --------------------------------------------------------------------------
+# Balancers
+# --------------------------------------------------------------------------
+
+def quantile_rank(T, E, K):
+    """0-based sorted index that the 'higher' quantile at p = K/E picks from
+    T values: ceil(p * (T - 1)), with p and the product in FP32 as the FP32
+    quantile computes them ([K3-SLM] QuantileBalancer.update)."""
+    p = np.float32(K / E)
+    return int(math.ceil(float(np.float32(p * np.float32(T - 1)))))
+
+
+def quantile_bias_update(top_scores, scores, K):
+    """New balance biases [E] FP32 ([K3-SLM] "QuantileBalancer: persistent
+    biases, no gradient update"):
+
+      thresh_t = top_scores[t, K]          the (K+1)-th corrected score
+      rel[t, j] = thresh_t - s[t, j]       FP32 subtraction
+      b_j = 'higher' quantile p = K/E of rel[:, j] over the T tokens
+      b = b - mean(b)
+
+    The quantile is the value at sorted index quantile_rank(T, E, K). The mean
+    is a sequential float64 sum over j, divided by E and rounded once to FP32;
+    the centring subtraction is FP32.
+    """
+    ts = np.asarray(top_scores, dtype=np.float32)
+    s = np.asarray(scores, dtype=np.float32)
+    T, E = s.shape
+    thresh = ts[:, K]
+    rel = (thresh[:, None] - s).astype(np.float32)
+    q = quantile_rank(T, E, K)
+    b = np.empty(E, dtype=np.float32)
+    for j in range(E):
+        b[j] = np.sort(rel[:, j], kind="stable")[q]
+    acc = 0.0
+    for j in range(E):
+        acc += float(b[j])
+    mean = np.float32(acc / E)
+    return (b - mean).astype(np.float32)
+
+
+def sign_bias_update(counts, N, K, bias, alpha):
+    """Bias-based balancing ([APEX-M3] section 14.3): f_e = c_e / (N K),
+    tau = 1/E, b_e <- clamp(b_e + alpha * sign(tau - f_e), -1, 1)."""
+    c = f64(counts)
+    E = c.shape[0]
+    f = c / (N * K)
+    tau = 1.0 / E
+    b = f64(bias) + alpha * np.sign(tau - f)
+    return np.clip(b, -1.0, 1.0)
