@@ -12,10 +12,7 @@ __all__ = ["api", "workloads"]
 
 
 def __getattr__(name):
-    if name == "api":
-        from . import api
-        return api
-    if name == "workloads":
-        from . import workloads
-        return workloads
+    if name in __all__:
+        import importlib
+        return importlib.import_module(f"{__name__}.{name}")
     raise AttributeError(name)

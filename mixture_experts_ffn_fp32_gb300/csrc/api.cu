@@ -1,0 +1,614 @@
+// C ABI of libmoe (declared in include/moe.h): host-side validation,
+// workspace planning and the forward pipeline that enqueues the kernels of
+// router.cu, dispatch.cu, gemm_tc.cu / gemm_simt.cu and balance.cu.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+#define MOE_API extern "C" __attribute__((visibility("default")))
+
+namespace moe {
+
+static std::atomic<unsigned long long> g_launches{0};
+static std::atomic<long long> g_timeout_ns{1000LL * 1000LL * 1000LL};
+
+void note_launch(int n) { g_launches.fetch_add(static_cast<unsigned long long>(n)); }
+uint64_t wait_timeout_ns() { return static_cast<uint64_t>(g_timeout_ns.load()); }
+
+int num_sms() {
+    static int cache[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return 1;
+    if (cache[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 1;
+    }
+    return cache[dev];
+}
+
+// ---------------------------------------------------------------------------
+// Tensor-map encoding through the driver entry point (no libcuda link).
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encoder() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+bool encode_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                 const uint64_t* strides_bytes, const uint32_t* box) {
+    EncodeTiledFn fn = get_encoder();
+    if (!fn) return false;
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        es[i] = 1;
+    }
+    for (int i = 0; i + 1 < rank; ++i) st[i] = strides_bytes[i];
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+                          const_cast<void*>(base), d, st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// Validation and workspace layout
+// ---------------------------------------------------------------------------
+moe_status validate_config(const moe_config& c) {
+    if (c.T < 1 || c.d < 1 || c.d_ff < 1 || c.E < 1 || c.K < 1) return MOE_ERR_INVALID_ARG;
+    if (c.K > c.E) return MOE_ERR_INVALID_ARG;
+    if (c.gate != MOE_GATE_SOFTMAX_TOPK && c.gate != MOE_GATE_SOFTMAX_ALL_RENORM &&
+        c.gate != MOE_GATE_SIGMOID)
+        return MOE_ERR_INVALID_ARG;
+    if (c.gate == MOE_GATE_SIGMOID && c.K + 1 > c.E) return MOE_ERR_INVALID_ARG;
+    if (c.dtype != MOE_F32 && c.dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (c.n_shared < 0 || (c.n_shared > 0 && c.shared_d_ff < 1)) return MOE_ERR_INVALID_ARG;
+    if (c.latent_dim < 0) return MOE_ERR_INVALID_ARG;
+    if (!(c.routed_scale == c.routed_scale)) return MOE_ERR_INVALID_ARG;
+    if (c.E > 256 || c.K > 16) return MOE_ERR_UNSUPPORTED;
+    // row pitches feed 16-byte vector accesses and TMA strides; tiles store 16 columns at a time
+    if (c.d % 16 || c.d_ff % 16) return MOE_ERR_UNSUPPORTED;
+    if (c.n_shared > 0 && c.shared_d_ff % 16) return MOE_ERR_UNSUPPORTED;
+    if (c.latent_dim > 0 && (c.latent_dim % 16 || c.dtype != MOE_BF16)) return MOE_ERR_UNSUPPORTED;
+    const long long TK = static_cast<long long>(c.T) * c.K;
+    if (TK > (1LL << 30) || static_cast<long long>(c.T) * c.d > (1LL << 40)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+static size_t align_up(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+WsLayout plan_workspace(const moe_config& c) {
+    WsLayout L;
+    memset(&L, 0, sizeof(L));
+    const size_t T = c.T, K = c.K, E = c.E, TK = T * K;
+    const size_t es = (c.dtype == MOE_BF16) ? 2 : 4;
+    const size_t de = c.latent_dim ? c.latent_dim : c.d;
+    L.nchunks = static_cast<int>((TK + DISPATCH_CHUNK - 1) / DISPATCH_CHUNK);
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes);
+        return at;
+    };
+    L.err = take(256);
+    L.topk_idx = take(TK * 4);
+    L.topk_w = take(TK * 4);
+    L.margin = take(T * 4);
+    const bool sig = c.gate == MOE_GATE_SIGMOID;
+    L.top_scores = sig ? take(T * (K + 1) * 4) : 0;
+    L.scores = sig ? take(T * E * 4) : 0;
+    L.chunk_counts = take(static_cast<size_t>(L.nchunks) * E * 4);
+    L.chunk_base = take(static_cast<size_t>(L.nchunks) * E * 4);
+    L.counts = take(E * 4);
+    L.offsets = take((E + 1) * 4);
+    L.mt_prefix = take((E + 1) * 4);
+    L.sorted_token = take(TK * 4);
+    L.sorted_w = take(TK * 4);
+    L.inv = take(TK * 4);
+    const bool bf = c.dtype == MOE_BF16;
+    L.xs = bf ? take(TK * de * es) : 0;
+    L.z = c.latent_dim ? take(T * de * es) : 0;
+    L.h = take(TK * c.d_ff * es);
+    const size_t SF = static_cast<size_t>(c.n_shared) * (c.n_shared ? c.shared_d_ff : 0);
+    L.hs = SF ? take(T * SF * es) : 0;
+    L.ys = take(TK * de * es);
+    L.routed = c.latent_dim ? take(T * de * es) : 0;
+    L.shout = (c.latent_dim && c.n_shared) ? take(T * c.d * 4) : 0;
+    L.xstage = take(T * c.d * es);
+    L.ostage = take(T * c.d * es);
+    L.qb = take(E * 4);
+    L.total = o;
+    return L;
+}
+
+// ---------------------------------------------------------------------------
+// Stage timing (instrumentation)
+// ---------------------------------------------------------------------------
+enum Stage { ST_ROUTE = 0, ST_LATENT_DOWN, ST_DISPATCH, ST_GATHER, ST_GATEUP, ST_DOWN, ST_COMBINE,
+             ST_LATENT_UP, ST_COUNT };
+static const char* kStageNames[ST_COUNT] = {"router", "latent_down", "dispatch", "gather",
+                                            "gate_up", "down", "shared_down_combine", "latent_up"};
+
+struct Timing {
+    std::mutex mu;
+    bool on = false;
+    int max_calls = 0, calls = 0;
+    std::vector<cudaEvent_t> ev;  // [max_calls][ST_COUNT][2]
+    std::vector<char> used;       // [max_calls][ST_COUNT]
+};
+static Timing g_timing;
+
+struct StageRec {
+    int call = -1;
+    cudaStream_t s = nullptr;
+    void begin(int st) {
+        if (call >= 0) cudaEventRecord(g_timing.ev[(call * ST_COUNT + st) * 2], s);
+    }
+    void end(int st) {
+        if (call >= 0) {
+            cudaEventRecord(g_timing.ev[(call * ST_COUNT + st) * 2 + 1], s);
+            g_timing.used[call * ST_COUNT + st] = 1;
+        }
+    }
+};
+
+static StageRec stage_rec(cudaStream_t s) {
+    StageRec r;
+    r.s = s;
+    std::lock_guard<std::mutex> lk(g_timing.mu);
+    if (g_timing.on && g_timing.calls < g_timing.max_calls) r.call = g_timing.calls++;
+    return r;
+}
+
+static moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static moe_status check_weights(const moe_config& c, const moe_weights* w) {
+    if (!w || !w->W_router || !w->W_gate || !w->W_up || !w->W_down) return MOE_ERR_INVALID_ARG;
+    if (c.n_shared > 0 && (!w->Ws_gate || !w->Ws_up || !w->Ws_down)) return MOE_ERR_INVALID_ARG;
+    if (c.latent_dim > 0 && (!w->W_down_latent || !w->W_up_latent)) return MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {w->W_router, w->W_gate, w->W_up, w->W_down, w->Ws_gate, w->Ws_up,
+                          w->Ws_down, w->W_down_latent, w->W_up_latent};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (w->bias && (reinterpret_cast<uintptr_t>(w->bias) & 3u)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+// Enqueue the whole forward on s. x and out are device pointers.
+static moe_status forward_impl(const moe_config& c, const void* x, const moe_weights& w, void* out,
+                               uint8_t* ws, cudaStream_t s) {
+    const WsLayout L = plan_workspace(c);
+    const bool bf = c.dtype == MOE_BF16;
+    const int T = c.T, K = c.K, E = c.E, TK = T * K;
+    const int de = c.latent_dim ? c.latent_dim : c.d;
+    const int S = c.n_shared, Fs = c.shared_d_ff, SF = S * (S ? Fs : 0);
+    const size_t es = bf ? 2 : 4;
+    int* err = reinterpret_cast<int*>(ws + L.err);
+    auto P = [&](size_t off) { return static_cast<void*>(ws + off); };
+    int32_t* idx = static_cast<int32_t*>(P(L.topk_idx));
+    float* tw = static_cast<float*>(P(L.topk_w));
+    int32_t* offsets = static_cast<int32_t*>(P(L.offsets));
+    int32_t* mt_prefix = static_cast<int32_t*>(P(L.mt_prefix));
+    int32_t* sorted_token = static_cast<int32_t*>(P(L.sorted_token));
+    float* sorted_w = static_cast<float*>(P(L.sorted_w));
+    int32_t* inv = static_cast<int32_t*>(P(L.inv));
+    StageRec rec = stage_rec(s);
+    cudaError_t e;
+
+    // 1. router
+    rec.begin(ST_ROUTE);
+    RouterArgs ra{};
+    ra.x = x;
+    ra.x_bf16 = bf;
+    ra.W = w.W_router;
+    ra.bias = w.bias;
+    ra.T = T; ra.d = c.d; ra.E = E; ra.K = K; ra.gate = c.gate; ra.renorm = c.renormalize;
+    ra.scale = c.routed_scale;
+    ra.idx = idx;
+    ra.w = tw;
+    ra.margin = static_cast<float*>(P(L.margin));
+    ra.top_scores = L.top_scores ? static_cast<float*>(P(L.top_scores)) : nullptr;
+    ra.scores = L.scores ? static_cast<float*>(P(L.scores)) : nullptr;
+    if ((e = launch_router(ra, s)) != cudaSuccess) return cuda_status(e);
+    rec.end(ST_ROUTE);
+
+    // 1b. latent compression z = x W_down_latent (once per token)
+    const void* ex_src = x;  // rows the routed experts act on
+    if (c.latent_dim) {
+        rec.begin(ST_LATENT_DOWN);
+        TcGemmArgs g{};
+        g.g[1] = TcGroup{1, x, c.d, T, w.W_down_latent, nullptr, 1, c.latent_dim, P(L.z), c.latent_dim, 0};
+        g.K = c.d;
+        g.err = err;
+        if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
+        ex_src = P(L.z);
+        rec.end(ST_LATENT_DOWN);
+    }
+
+    // 2. dispatch
+    rec.begin(ST_DISPATCH);
+    DispatchArgs da{};
+    da.idx = idx;
+    da.w = tw;
+    da.T = T; da.K = K; da.E = E; da.nchunks = L.nchunks;
+    da.bm = bf ? TC_BM : SIMT_BM;
+    da.chunk_counts = static_cast<int32_t*>(P(L.chunk_counts));
+    da.chunk_base = static_cast<int32_t*>(P(L.chunk_base));
+    da.counts = static_cast<int32_t*>(P(L.counts));
+    da.offsets = offsets;
+    da.mt_prefix = mt_prefix;
+    da.sorted_token = sorted_token;
+    da.sorted_w = sorted_w;
+    da.inv = inv;
+    da.err = err;
+    if ((e = launch_dispatch(da, s, nullptr)) != cudaSuccess) return cuda_status(e);
+    rec.end(ST_DISPATCH);
+
+    if (bf) {
+        // 3. gather the routed rows into expert order
+        rec.begin(ST_GATHER);
+        if ((e = launch_gather_rows(ex_src, sorted_token, TK, de * 2, P(L.xs), s)) != cudaSuccess)
+            return cuda_status(e);
+        rec.end(ST_GATHER);
+
+        // 4. gate/up (+ SiLU * up) for routed and shared experts in one launch
+        rec.begin(ST_GATEUP);
+        if (c.latent_dim && S) {
+            // routed experts (K = L) and the shared FFN (K = d) differ in K: two launches
+            TcGemmArgs g{};
+            g.g[0] = TcGroup{1, P(L.xs), de, TK, w.W_gate, w.W_up, E, c.d_ff, P(L.h), c.d_ff, 0};
+            g.K = de; g.E = E; g.offsets = offsets; g.mt_prefix = mt_prefix; g.swiglu = 1; g.err = err;
+            if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
+            TcGemmArgs g2{};
+            g2.g[1] = TcGroup{1, x, c.d, T, w.Ws_gate, w.Ws_up, S, Fs, P(L.hs), SF, 0};
+            g2.K = c.d; g2.swiglu = 1; g2.err = err;
+            if ((e = launch_tc_gemm(g2, s)) != cudaSuccess) return cuda_status(e);
+        } else {
+            TcGemmArgs g{};
+            g.g[0] = TcGroup{1, P(L.xs), de, TK, w.W_gate, w.W_up, E, c.d_ff, P(L.h), c.d_ff, 0};
+            if (S) g.g[1] = TcGroup{1, x, c.d, T, w.Ws_gate, w.Ws_up, S, Fs, P(L.hs), SF, 0};
+            g.K = de; g.E = E; g.offsets = offsets; g.mt_prefix = mt_prefix; g.swiglu = 1; g.err = err;
+            if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
+        }
+        rec.end(ST_GATEUP);
+
+        // 5. routed down projection, scaled by each assignment's gate weight
+        rec.begin(ST_DOWN);
+        {
+            TcGemmArgs g{};
+            g.g[0] = TcGroup{1, P(L.h), c.d_ff, TK, w.W_down, nullptr, E, de, P(L.ys), de, 0};
+            g.K = c.d_ff; g.E = E; g.offsets = offsets; g.mt_prefix = mt_prefix; g.swiglu = 0;
+            g.rowscale0 = sorted_w; g.err = err;
+            if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
+        }
+        rec.end(ST_DOWN);
+
+        // 6. shared down projection + deterministic combine of the K routed rows
+        rec.begin(ST_COMBINE);
+        if (!c.latent_dim) {
+            if (S) {
+                TcGemmArgs g{};
+                g.g[1] = TcGroup{1, P(L.hs), SF, T, w.Ws_down, nullptr, 1, c.d, out, c.d, 0};
+                g.K = SF; g.swiglu = 0; g.inv = inv; g.ys = P(L.ys); g.ys_ld = de; g.Kr = K;
+                g.err = err;
+                if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
+            } else {
+                if ((e = launch_gather_sum(P(L.ys), 1, inv, T, K, de, out, 1, s)) != cudaSuccess)
+                    return cuda_status(e);
+            }
+            rec.end(ST_COMBINE);
+        } else {
+            // routed sum in latent width, then back to model width plus the shared FFN
+            if ((e = launch_gather_sum(P(L.ys), 1, inv, T, K, de, P(L.routed), 1, s)) != cudaSuccess)
+                return cuda_status(e);
+            if (S) {
+                TcGemmArgs g{};
+                g.g[1] = TcGroup{1, P(L.hs), SF, T, w.Ws_down, nullptr, 1, c.d, P(L.shout), c.d, 1};
+                g.K = SF; g.swiglu = 0; g.err = err;
+                if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
+            }
+            rec.end(ST_COMBINE);
+            rec.begin(ST_LATENT_UP);
+            TcGemmArgs g{};
+            g.g[1] = TcGroup{1, P(L.routed), de, T, w.W_up_latent, nullptr, 1, c.d, out, c.d, 0};
+            g.K = de; g.swiglu = 0; g.err = err;
+            if (S) {
+                g.addend = static_cast<const float*>(P(L.shout));
+                g.add_ld = c.d;
+            }
+            if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
+            rec.end(ST_LATENT_UP);
+        }
+    } else {
+        // FP32 layer on the CUDA cores; routed A rows read through sorted_token
+        const float* xf = static_cast<const float*>(x);
+        rec.begin(ST_GATEUP);
+        {
+            SimtGemmArgs g{};
+            g.g[0] = SimtGroup{1, xf, c.d, sorted_token, TK, static_cast<const float*>(w.W_gate),
+                               static_cast<const float*>(w.W_up), E, c.d_ff,
+                               static_cast<float*>(P(L.h)), c.d_ff};
+            if (S)
+                g.g[1] = SimtGroup{1, xf, c.d, nullptr, T, static_cast<const float*>(w.Ws_gate),
+                                   static_cast<const float*>(w.Ws_up), S, Fs,
+                                   static_cast<float*>(P(L.hs)), SF};
+            g.K = c.d; g.E = E; g.offsets = offsets; g.mt_prefix = mt_prefix; g.swiglu = 1;
+            if ((e = launch_simt_gemm(g, s)) != cudaSuccess) return cuda_status(e);
+        }
+        rec.end(ST_GATEUP);
+        rec.begin(ST_DOWN);
+        {
+            SimtGemmArgs g{};
+            g.g[0] = SimtGroup{1, static_cast<const float*>(P(L.h)), c.d_ff, nullptr, TK,
+                               static_cast<const float*>(w.W_down), nullptr, E, c.d,
+                               static_cast<float*>(P(L.ys)), c.d};
+            g.K = c.d_ff; g.E = E; g.offsets = offsets; g.mt_prefix = mt_prefix; g.swiglu = 0;
+            g.rowscale0 = sorted_w;
+            if ((e = launch_simt_gemm(g, s)) != cudaSuccess) return cuda_status(e);
+        }
+        rec.end(ST_DOWN);
+        rec.begin(ST_COMBINE);
+        if (S) {
+            SimtGemmArgs g{};
+            g.g[1] = SimtGroup{1, static_cast<const float*>(P(L.hs)), SF, nullptr, T,
+                               static_cast<const float*>(w.Ws_down), nullptr, 1, c.d,
+                               static_cast<float*>(out), c.d};
+            g.K = SF; g.swiglu = 0; g.inv = inv; g.ys = static_cast<const float*>(P(L.ys));
+            g.ys_ld = c.d; g.Kr = K;
+            if ((e = launch_simt_gemm(g, s)) != cudaSuccess) return cuda_status(e);
+        } else {
+            if ((e = launch_gather_sum(P(L.ys), 0, inv, T, K, c.d, out, 0, s)) != cudaSuccess)
+                return cuda_status(e);
+        }
+        rec.end(ST_COMBINE);
+    }
+    (void)es;
+    return MOE_OK;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+MOE_API const char* moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+        case MOE_ERR_WORKSPACE: return "workspace too small";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_TIMEOUT: return "device wait timed out";
+        case MOE_ERR_DEVICE_INDEX: return "expert id out of range";
+    }
+    return "unknown status";
+}
+
+MOE_API const char* moe_version(void) { return "0.1.0"; }
+
+MOE_API moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
+    if (!cfg || !bytes) return MOE_ERR_INVALID_ARG;
+    const moe_status v = validate_config(*cfg);
+    if (v != MOE_OK) return v;
+    *bytes = plan_workspace(*cfg).total;
+    return MOE_OK;
+}
+
+MOE_API moe_status moe_get_workspace_views(const moe_config* cfg, void* ws, moe_workspace_views* v) {
+    if (!cfg || !ws || !v) return MOE_ERR_INVALID_ARG;
+    const moe_status st = validate_config(*cfg);
+    if (st != MOE_OK) return st;
+    const WsLayout L = plan_workspace(*cfg);
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    v->topk_idx = reinterpret_cast<int32_t*>(b + L.topk_idx);
+    v->topk_w = reinterpret_cast<float*>(b + L.topk_w);
+    v->margin = reinterpret_cast<float*>(b + L.margin);
+    v->top_scores = L.top_scores ? reinterpret_cast<float*>(b + L.top_scores) : nullptr;
+    v->scores = L.scores ? reinterpret_cast<float*>(b + L.scores) : nullptr;
+    v->counts = reinterpret_cast<int32_t*>(b + L.counts);
+    v->offsets = reinterpret_cast<int32_t*>(b + L.offsets);
+    v->sorted_token = reinterpret_cast<int32_t*>(b + L.sorted_token);
+    v->sorted_w = reinterpret_cast<float*>(b + L.sorted_w);
+    v->inv = reinterpret_cast<int32_t*>(b + L.inv);
+    return MOE_OK;
+}
+
+MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const float* W_router,
+                             const float* bias, int32_t* topk_idx, float* topk_w, float* margin,
+                             float* top_scores, float* scores, void* stream) {
+    if (!cfg || !x || !W_router || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+    const moe_status v = validate_config(*cfg);
+    if (v != MOE_OK) return v;
+    if (!aligned16(x) || !aligned16(W_router)) return MOE_ERR_INVALID_ARG;
+    RouterArgs ra{};
+    ra.x = x;
+    ra.x_bf16 = cfg->dtype == MOE_BF16;
+    ra.W = W_router;
+    ra.bias = bias;
+    ra.T = cfg->T; ra.d = cfg->d; ra.E = cfg->E; ra.K = cfg->K; ra.gate = cfg->gate;
+    ra.renorm = cfg->renormalize; ra.scale = cfg->routed_scale;
+    ra.idx = topk_idx; ra.w = topk_w; ra.margin = margin;
+    ra.top_scores = top_scores;
+    ra.scores = scores;
+    return cuda_status(launch_router(ra, static_cast<cudaStream_t>(stream)));
+}
+
+MOE_API moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const float* topk_w,
+                                int32_t* counts, int32_t* offsets, int32_t* sorted_token,
+                                float* sorted_w, int32_t* inv, void* ws, size_t ws_bytes,
+                                void* stream) {
+    if (!cfg || !topk_idx || !topk_w || !counts || !offsets || !sorted_token || !sorted_w || !inv || !ws)
+        return MOE_ERR_INVALID_ARG;
+    const moe_status v = validate_config(*cfg);
+    if (v != MOE_OK) return v;
+    const WsLayout L = plan_workspace(*cfg);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    DispatchArgs da{};
+    da.idx = topk_idx; da.w = topk_w;
+    da.T = cfg->T; da.K = cfg->K; da.E = cfg->E; da.nchunks = L.nchunks;
+    da.bm = cfg->dtype == MOE_BF16 ? TC_BM : SIMT_BM;
+    da.chunk_counts = reinterpret_cast<int32_t*>(b + L.chunk_counts);
+    da.chunk_base = reinterpret_cast<int32_t*>(b + L.chunk_base);
+    da.counts = counts; da.offsets = offsets;
+    da.mt_prefix = reinterpret_cast<int32_t*>(b + L.mt_prefix);
+    da.sorted_token = sorted_token; da.sorted_w = sorted_w; da.inv = inv;
+    da.err = reinterpret_cast<int*>(b + L.err);
+    return cuda_status(launch_dispatch(da, static_cast<cudaStream_t>(stream), nullptr));
+}
+
+MOE_API moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* w, void* out,
+                               void* ws, size_t ws_bytes, void* stream) {
+    if (!cfg || !x || !out || !ws) return MOE_ERR_INVALID_ARG;
+    moe_status v = validate_config(*cfg);
+    if (v != MOE_OK) return v;
+    if ((v = check_weights(*cfg, w)) != MOE_OK) return v;
+    if (!aligned16(x) || !aligned16(out) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < plan_workspace(*cfg).total) return MOE_ERR_WORKSPACE;
+    return forward_impl(*cfg, x, *w, out, static_cast<uint8_t*>(ws), static_cast<cudaStream_t>(stream));
+}
+
+MOE_API moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const moe_weights* w,
+                                    void* out_host, void* ws, size_t ws_bytes, void* stream) {
+    if (!cfg || !x_host || !out_host || !ws) return MOE_ERR_INVALID_ARG;
+    moe_status v = validate_config(*cfg);
+    if (v != MOE_OK) return v;
+    if ((v = check_weights(*cfg, w)) != MOE_OK) return v;
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = plan_workspace(*cfg);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    const size_t bytes = static_cast<size_t>(cfg->T) * cfg->d * (cfg->dtype == MOE_BF16 ? 2 : 4);
+    if (cudaMemcpyAsync(b + L.xstage, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    v = forward_impl(*cfg, b + L.xstage, *w, b + L.ostage, b, s);
+    if (v != MOE_OK) return v;
+    if (cudaMemcpyAsync(out_host, b + L.ostage, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return cuda_status(cudaStreamSynchronize(s));
+}
+
+MOE_API size_t moe_quantile_workspace_size(int32_t T, int32_t E) {
+    (void)T;
+    return 256 + ((static_cast<size_t>(E > 0 ? E : 0) * 4 + 255) & ~static_cast<size_t>(255));
+}
+
+MOE_API moe_status moe_quantile_bias_update(int32_t T, int32_t E, int32_t K, const float* top_scores,
+                                            const float* scores, float* bias, void* ws,
+                                            size_t ws_bytes, void* stream) {
+    if (T < 1 || E < 2 || K < 1 || K + 1 > E || !top_scores || !scores || !bias || !ws)
+        return MOE_ERR_INVALID_ARG;
+    if (E > 256) return MOE_ERR_UNSUPPORTED;
+    if (ws_bytes < moe_quantile_workspace_size(T, E)) return MOE_ERR_WORKSPACE;
+    // the FP32 pre-centring biases live right after the 256-byte error word
+    float* braw = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + 256);
+    return cuda_status(launch_quantile(T, E, K, top_scores, scores, braw, bias,
+                                       static_cast<cudaStream_t>(stream), nullptr));
+}
+
+MOE_API moe_status moe_sign_bias_update(int32_t E, int32_t N, int32_t K, const int32_t* counts,
+                                        float* bias, float alpha, void* stream) {
+    if (E < 1 || N < 1 || K < 1 || !counts || !bias || !(alpha == alpha)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_sign_bias(E, N, K, counts, bias, alpha, static_cast<cudaStream_t>(stream)));
+}
+
+MOE_API moe_status moe_workspace_status(void* ws, void* stream) {
+    if (!ws) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int h = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemcpy(&h, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (h != 0 && cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+    if (h & ERRBIT_TIMEOUT) return MOE_ERR_TIMEOUT;
+    if (h & ERRBIT_INDEX) return MOE_ERR_DEVICE_INDEX;
+    return MOE_OK;
+}
+
+MOE_API moe_status moe_timing_begin(int32_t max_calls) {
+    if (max_calls < 1) return MOE_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_timing.mu);
+    for (cudaEvent_t e : g_timing.ev) cudaEventDestroy(e);
+    g_timing.ev.assign(static_cast<size_t>(max_calls) * ST_COUNT * 2, nullptr);
+    g_timing.used.assign(static_cast<size_t>(max_calls) * ST_COUNT, 0);
+    for (auto& e : g_timing.ev)
+        if (cudaEventCreate(&e) != cudaSuccess) return MOE_ERR_CUDA;
+    g_timing.max_calls = max_calls;
+    g_timing.calls = 0;
+    g_timing.on = true;
+    return MOE_OK;
+}
+
+MOE_API moe_status moe_timing_end(float* stage_ms, int32_t max_stages, int32_t* n_stages,
+                                  int32_t* n_calls) {
+    std::lock_guard<std::mutex> lk(g_timing.mu);
+    if (!g_timing.on) return MOE_ERR_INVALID_ARG;
+    g_timing.on = false;
+    moe_status st = MOE_OK;
+    std::vector<float> sum(ST_COUNT, 0.0f);
+    for (int c = 0; c < g_timing.calls; ++c)
+        for (int k = 0; k < ST_COUNT; ++k) {
+            if (!g_timing.used[c * ST_COUNT + k]) continue;
+            float ms = 0.0f;
+            cudaEvent_t b = g_timing.ev[(c * ST_COUNT + k) * 2], e = g_timing.ev[(c * ST_COUNT + k) * 2 + 1];
+            if (cudaEventSynchronize(e) != cudaSuccess || cudaEventElapsedTime(&ms, b, e) != cudaSuccess)
+                st = MOE_ERR_CUDA;
+            sum[k] += ms;
+        }
+    if (stage_ms)
+        for (int k = 0; k < ST_COUNT && k < max_stages; ++k) stage_ms[k] = sum[k];
+    if (n_stages) *n_stages = ST_COUNT;
+    if (n_calls) *n_calls = g_timing.calls;
+    for (cudaEvent_t e : g_timing.ev) cudaEventDestroy(e);
+    g_timing.ev.clear();
+    g_timing.used.clear();
+    g_timing.calls = 0;
+    return st;
+}
+
+MOE_API const char* moe_stage_name(int32_t stage) {
+    return (stage >= 0 && stage < ST_COUNT) ? kStageNames[stage] : nullptr;
+}
+
+MOE_API uint64_t moe_launch_count(void) { return g_launches.load(); }
+
+MOE_API moe_status moe_set_wait_timeout_ms(int32_t ms) {
+    if (ms < 1) return MOE_ERR_INVALID_ARG;
+    g_timeout_ns.store(static_cast<long long>(ms) * 1000000LL);
+    return MOE_OK;
+}
+
+MOE_API moe_status moe_selftest_wait_timeout(int32_t ms, void* ws, void* stream) {
+    if (ms < 1 || ms > 10000 || !ws) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (launch_wait_selftest(static_cast<int*>(ws), static_cast<uint64_t>(ms) * 1000000ull, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return moe_workspace_status(ws, stream);
+}

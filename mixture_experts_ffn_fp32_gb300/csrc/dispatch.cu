@@ -1,0 +1,234 @@
+// K2 - sorted dispatch: per-expert histogram, exclusive scan and a stable
+// scatter that lists the T*K assignments expert by expert, plus the row
+// gather that lays the tokens' activations out in that order.
+//
+// Source: kimi_k3 StableLatentMoE, "Flatten routing and recover original
+// token order" and "Dispatch is a stable permutation, not token duplication
+// in model state": the flat ids are sorted with a stable argsort, the sorted
+// assignment at position pos belongs to token order[pos] // K, bincount gives
+// the expert loads and their cumulative sums the expert slices.
+//
+// Here the stable argsort is a counting sort done in three launches with no
+// host synchronisation: (a) each CTA histograms a chunk of 1024 consecutive
+// flat assignments, (b) one CTA turns the chunk histograms into per-expert
+// offsets and per-chunk bases (and the per-expert GEMM m-tile prefix), (c)
+// each CTA ranks its chunk's assignments stably (warp match + per-warp
+// counts) and writes sorted_token / sorted_w / inv. Integer arithmetic only,
+// so the result is bit-exact and independent of scheduling.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+__global__ void __launch_bounds__(256) dispatch_count_kernel(const int32_t* __restrict__ idx,
+                                                             int TK, int E,
+                                                             int32_t* __restrict__ chunk_counts,
+                                                             int* err) {
+    __shared__ int hist[256];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    const int j0 = blockIdx.x * DISPATCH_CHUNK;
+    const int j1 = min(j0 + DISPATCH_CHUNK, TK);
+    bool bad = false;
+    for (int j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
+        const int e = idx[j];
+        if (e >= 0 && e < E)
+            atomicAdd(&hist[e], 1);
+        else
+            bad = true;
+    }
+    if (bad) atomicOr(err, ERRBIT_INDEX);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        chunk_counts[static_cast<size_t>(blockIdx.x) * E + e] = hist[e];
+}
+
+// Exclusive scan of v over the 256 threads of the block (all threads call).
+__device__ int block_exclusive_scan(int v, int* warp_tot) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int t = (lane < 8) ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        if (lane < 8) warp_tot[lane] = t;  // inclusive warp totals
+    }
+    __syncthreads();
+    const int before = (warp > 0) ? warp_tot[warp - 1] : 0;
+    const int excl = before + x - v;
+    __syncthreads();
+    return excl;
+}
+
+__global__ void __launch_bounds__(256) dispatch_scan_kernel(
+    const int32_t* __restrict__ chunk_counts, int nchunks, int E, int TK, int bm,
+    int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ mt_prefix) {
+    __shared__ int warp_tot[8];
+    const int e = threadIdx.x;
+    int running = 0;
+    if (e < E) {
+        for (int b = 0; b < nchunks; ++b) {
+            const int c = chunk_counts[static_cast<size_t>(b) * E + e];
+            chunk_base[static_cast<size_t>(b) * E + e] = running;
+            running += c;
+        }
+    }
+    const int cnt = (e < E) ? running : 0;
+    const int off = block_exclusive_scan(cnt, warp_tot);
+    const int mt = (cnt + bm - 1) / bm;
+    const int mtoff = block_exclusive_scan(mt, warp_tot);
+    if (e < E) {
+        counts[e] = cnt;
+        offsets[e] = off;
+        mt_prefix[e] = mtoff;
+        for (int b = 0; b < nchunks; ++b) chunk_base[static_cast<size_t>(b) * E + e] += off;
+    }
+    if (e == E - 1) {
+        offsets[E] = off + cnt;
+        mt_prefix[E] = mtoff + mt;
+    }
+    (void)TK;
+}
+
+__global__ void __launch_bounds__(DISPATCH_CHUNK) dispatch_scatter_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ w, int TK, int K, int E,
+    const int32_t* __restrict__ chunk_base, int32_t* __restrict__ sorted_token,
+    float* __restrict__ sorted_w, int32_t* __restrict__ inv) {
+    __shared__ int wcnt[32][256];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < 32 * 256; i += blockDim.x) (&wcnt[0][0])[i] = 0;
+    __syncthreads();
+    const int j = blockIdx.x * DISPATCH_CHUNK + threadIdx.x;
+    int e = (j < TK) ? idx[j] : -1;
+    if (e < 0 || e >= E) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (e >= 0 && rank == 0) wcnt[warp][e] = __popc(peers);
+    __syncthreads();
+    for (int x = threadIdx.x; x < E; x += blockDim.x) {
+        int run = 0;
+        for (int ww = 0; ww < 32; ++ww) {
+            const int c = wcnt[ww][x];
+            wcnt[ww][x] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    if (e >= 0) {
+        const int pos = chunk_base[static_cast<size_t>(blockIdx.x) * E + e] + wcnt[warp][e] + rank;
+        sorted_token[pos] = j / K;
+        sorted_w[pos] = w[j];
+        inv[j] = pos;
+    }
+}
+
+// One warp per destination row; 16-byte vectors.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src,
+                                                          const int32_t* __restrict__ rowidx,
+                                                          int rows, int vec_per_row,
+                                                          uint4* __restrict__ dst) {
+    const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (r >= rows) return;
+    const int lane = threadIdx.x & 31;
+    const size_t s = static_cast<size_t>(rowidx[r]) * vec_per_row;
+    const size_t d = static_cast<size_t>(r) * vec_per_row;
+    for (int v = lane; v < vec_per_row; v += 32) dst[d + v] = __ldg(src + s + v);
+}
+
+// out[t, c] = sum_k ys[inv[t, k], c], one warp per token, 8 columns per lane step.
+template <bool YS_BF16, bool OUT_BF16>
+__global__ void __launch_bounds__(256) gather_sum_kernel(const void* __restrict__ ys,
+                                                         const int32_t* __restrict__ inv, int T,
+                                                         int K, int cols, void* __restrict__ out) {
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (t >= T) return;
+    const int lane = threadIdx.x & 31;
+    for (int c0 = lane * 8; c0 < cols; c0 += 32 * 8) {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int k = 0; k < K; ++k) {
+            const size_t row = static_cast<size_t>(inv[static_cast<size_t>(t) * K + k]);
+            if (YS_BF16) {
+                const uint4 v = *reinterpret_cast<const uint4*>(
+                    static_cast<const __nv_bfloat16*>(ys) + row * cols + c0);
+                const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] += bf16_lo(u[i]);
+                    acc[2 * i + 1] += bf16_hi(u[i]);
+                }
+            } else {
+                const float* p = static_cast<const float*>(ys) + row * cols + c0;
+                const float4 a = *reinterpret_cast<const float4*>(p);
+                const float4 b = *reinterpret_cast<const float4*>(p + 4);
+                acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+                acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+            }
+        }
+        const size_t o = static_cast<size_t>(t) * cols + c0;
+        if (OUT_BF16) {
+            uint4 v;
+            v.x = pack_bf16x2(acc[0], acc[1]);
+            v.y = pack_bf16x2(acc[2], acc[3]);
+            v.z = pack_bf16x2(acc[4], acc[5]);
+            v.w = pack_bf16x2(acc[6], acc[7]);
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + o) = v;
+        } else {
+            float* p = static_cast<float*>(out) + o;
+            *reinterpret_cast<float4*>(p) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            *reinterpret_cast<float4*>(p + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s, int* n_launched) {
+    const int TK = a.T * a.K;
+    dispatch_count_kernel<<<a.nchunks, 256, 0, s>>>(a.idx, TK, a.E, a.chunk_counts, a.err);
+    dispatch_scan_kernel<<<1, 256, 0, s>>>(a.chunk_counts, a.nchunks, a.E, TK, a.bm, a.chunk_base,
+                                           a.counts, a.offsets, a.mt_prefix);
+    dispatch_scatter_kernel<<<a.nchunks, DISPATCH_CHUNK, 0, s>>>(
+        a.idx, a.w, TK, a.K, a.E, a.chunk_base, a.sorted_token, a.sorted_w, a.inv);
+    note_launch(3);
+    if (n_launched) *n_launched = 3;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const void* src, const int32_t* rowidx, int rows, int row_bytes,
+                               void* dst, cudaStream_t s) {
+    const int vpr = row_bytes / 16;
+    const int blocks = (rows * 32 + 255) / 256;
+    gather_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(src), rowidx, rows, vpr,
+                                              static_cast<uint4*>(dst));
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_sum(const void* ys, int ys_bf16, const int32_t* inv, int T, int K,
+                              int cols, void* out, int out_bf16, cudaStream_t s) {
+    const int blocks = (T * 32 + 255) / 256;
+    if (ys_bf16 && out_bf16)
+        gather_sum_kernel<true, true><<<blocks, 256, 0, s>>>(ys, inv, T, K, cols, out);
+    else if (ys_bf16)
+        gather_sum_kernel<true, false><<<blocks, 256, 0, s>>>(ys, inv, T, K, cols, out);
+    else if (out_bf16)
+        gather_sum_kernel<false, true><<<blocks, 256, 0, s>>>(ys, inv, T, K, cols, out);
+    else
+        gather_sum_kernel<false, false><<<blocks, 256, 0, s>>>(ys, inv, T, K, cols, out);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,469 @@
+// K3/K4/K7 - grouped GEMM over ragged expert segments on the 5th-generation
+// tensor cores (tcgen05, accumulators in tensor memory), operands fed by TMA.
+//
+// What it computes (APEX-1 Mathematical Reference Part 3, section 12.2,
+// FFN(x) = W_down(SiLU(x W_gate) (.) x W_up), applied per expert to the rows
+// the dispatch grouped for it, as in kimi_k3 StableLatentMoE "The actual
+// grouped GEMM, and the gradient path"):
+//   SwiGLU kernel : h[r, :]  = SiLU(A[r, :] W_gate[z]) * (A[r, :] W_up[z])
+//   plain kernel  : y[r, :]  = rowscale[r] * (A[r, :] B[z])            (routed down x gate)
+//                   out[t, :] = A[t, :] B + sum_k ys[inv[t, k], :] (+ addend[t, :])
+//                                                                (shared down + combine)
+// Two segment groups share one persistent launch: group 0 = the E routed
+// experts over the expert-sorted rows (segment bounds read from device
+// memory, never from the host), group 1 = S dense segments over all token
+// rows (the shared experts, or a single dense projection).
+//
+// Tile: 128 rows x 256 accumulator columns (SwiGLU: 128 gate + 128 up
+// columns of the same output tile), K step 64 (one 128-byte swizzle row),
+// 4-stage TMA ring of 48 KB stages, two 256-column TMEM accumulators so the
+// epilogue of one tile overlaps the main loop of the next. Warp 0 issues TMA,
+// warp 1 issues tcgen05.mma (M=128, N=256, K=16, BF16 in, FP32 accumulate),
+// warps 2-5 drain TMEM, apply the epilogue and store. The weights stay in the
+// caller's [Z, K, N] layout (N contiguous) and are read as an MN-major
+// operand. Every wait is bounded (see common.cuh): on timeout the CTA stops,
+// drains its copies and MMAs, frees TMEM and flags the error word.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = TC_BM;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;        // 16 KB
+constexpr int STRIP_BYTES = BK * 64 * 2;    // 8 KB: 64 k rows x 64 columns
+constexpr int B_BYTES = 4 * STRIP_BYTES;    // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int ACC_COLS = 256;
+constexpr int TMEM_COLS = 512;
+constexpr int THREADS = 192;
+constexpr int MAXE = 256;
+constexpr uint32_t IDESC = idesc_bf16_f32(128, 256, /*b_mn_major=*/1);
+
+constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+constexpr int NBARS = 2 * STAGES + 4 + 1;
+constexpr int MISC_OFF = BAR_OFF + 8 * NBARS;
+constexpr int SCHED_OFF = ((MISC_OFF + 16) + 15) / 16 * 16;
+constexpr int SMEM_BYTES = SCHED_OFF + 2 * (MAXE + 1) * 4 + 1024;
+
+struct TcParams {
+    CUtensorMap mapA[2];
+    CUtensorMap mapB0[2];
+    CUtensorMap mapB1[2];
+    int enabled[2];
+    int rows[2];
+    int N[2];
+    int nt[2];
+    int Z[2];
+    void* out[2];
+    int out_ld[2];
+    int out_f32[2];
+    int kblocks, E, mt1;
+    const int32_t* offsets;
+    const int32_t* mt_prefix;
+    const float* rowscale0;
+    const int32_t* inv;
+    const __nv_bfloat16* ys;
+    int ys_ld, Kr;
+    const float* addend;
+    int add_ld;
+    int* err;
+    unsigned long long timeout_ns;
+};
+
+struct Unit {
+    int g, row0, rows, zb, n0, out_col0;
+};
+
+template <bool SWIGLU>
+MOE_DEV Unit decode_unit(int u, const TcParams& p, int total0, const int* s_mtp, const int* s_off) {
+    constexpr int BNO = SWIGLU ? 128 : 256;
+    Unit t;
+    if (u < total0) {
+        const int nt = p.nt[0];
+        const int mt = u / nt;
+        const int n = u - mt * nt;
+        int lo = 0, hi = p.E;  // s_mtp[lo] <= mt < s_mtp[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_mtp[mid] <= mt)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        const int m = mt - s_mtp[lo];
+        t.g = 0;
+        t.row0 = s_off[lo] + m * BM;
+        t.rows = min(BM, s_off[lo + 1] - t.row0);
+        t.zb = lo;
+        t.n0 = n * BNO;
+        t.out_col0 = t.n0;
+    } else {
+        const int u1 = u - total0;
+        const int nt = p.nt[1];
+        const int per_m = p.Z[1] * nt;
+        const int m = u1 / per_m;
+        const int rem = u1 - m * per_m;
+        const int s = rem / nt;
+        const int n = rem - s * nt;
+        t.g = 1;
+        t.row0 = m * BM;
+        t.rows = min(BM, p.rows[1] - t.row0);
+        t.zb = s;
+        t.n0 = n * BNO;
+        t.out_col0 = s * p.N[1] + t.n0;
+    }
+    return t;
+}
+
+MOE_DEV void store16(void* out, int out_f32, size_t row, int ld, int col, const float (&v)[16],
+                     int limit) {
+    if (out_f32) {
+        float* p = static_cast<float*>(out) + row * static_cast<size_t>(ld) + col;
+        if (limit >= 16) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 4)
+                *reinterpret_cast<float4*>(p + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        } else {
+            for (int i = 0; i < limit; ++i) p[i] = v[i];
+        }
+    } else {
+        __nv_bfloat16* p = static_cast<__nv_bfloat16*>(out) + row * static_cast<size_t>(ld) + col;
+        if (limit >= 16) {
+            uint4 a, b;
+            a.x = pack_bf16x2(v[0], v[1]);
+            a.y = pack_bf16x2(v[2], v[3]);
+            a.z = pack_bf16x2(v[4], v[5]);
+            a.w = pack_bf16x2(v[6], v[7]);
+            b.x = pack_bf16x2(v[8], v[9]);
+            b.y = pack_bf16x2(v[10], v[11]);
+            b.z = pack_bf16x2(v[12], v[13]);
+            b.w = pack_bf16x2(v[14], v[15]);
+            *reinterpret_cast<uint4*>(p) = a;
+            *reinterpret_cast<uint4*>(p + 8) = b;
+        } else {
+            for (int i = 0; i < limit; ++i) p[i] = __float2bfloat16_rn(v[i]);
+        }
+    }
+}
+
+template <bool SWIGLU>
+__global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __grid_constant__ TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + BAR_OFF;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + MISC_OFF);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + MISC_OFF + 4);
+    int* s_mtp = reinterpret_cast<int*>(smem + SCHED_OFF);
+    int* s_off = s_mtp + (MAXE + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 4);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        for (int g = 0; g < 2; ++g) {
+            if (!p.enabled[g]) continue;
+            tma_prefetch_map(&p.mapA[g]);
+            tma_prefetch_map(&p.mapB0[g]);
+            if (SWIGLU) tma_prefetch_map(&p.mapB1[g]);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (p.enabled[0]) {
+        for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
+            s_mtp[i] = p.mt_prefix[i];
+            s_off[i] = p.offsets[i];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total0 = p.enabled[0] ? s_mtp[p.E] * p.nt[0] : 0;
+    const int total = total0 + (p.enabled[1] ? p.mt1 * p.Z[1] * p.nt[1] : 0);
+    const WaitCtx wc{p.err, abort_flag, p.timeout_ns};
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer ----------------
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, last_par = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+                const Unit t = decode_unit<SWIGLU>(u, p, total0, s_mtp, s_off);
+                const CUtensorMap* mA = &p.mapA[t.g];
+                const CUtensorMap* mB0 = &p.mapB0[t.g];
+                const CUtensorMap* mB1 = &p.mapB1[t.g];
+                for (int kb = 0; kb < p.kblocks; ++kb) {
+                    if (!bounded_wait(empty_bar(stage), phase ^ 1u, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sA = sbase + stage * STAGE_BYTES;
+                    const uint32_t sB = sA + A_BYTES;
+                    const uint32_t fb = full_bar(stage);
+                    const int kc = kb * BK;
+                    mbar_expect_tx(fb, STAGE_BYTES);
+                    tma_load_2d(sA, mA, kc, t.row0, fb);
+                    if (SWIGLU) {
+                        tma_load_3d(sB, mB0, t.n0, kc, t.zb, fb);
+                        tma_load_3d(sB + STRIP_BYTES, mB0, t.n0 + 64, kc, t.zb, fb);
+                        tma_load_3d(sB + 2 * STRIP_BYTES, mB1, t.n0, kc, t.zb, fb);
+                        tma_load_3d(sB + 3 * STRIP_BYTES, mB1, t.n0 + 64, kc, t.zb, fb);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            tma_load_3d(sB + j * STRIP_BYTES, mB0, t.n0 + 64 * j, kc, t.zb, fb);
+                    }
+                    issued |= 1u << stage;
+                    last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // every copy this thread issued has landed before the CTA can exit
+            for (int s = 0; s < STAGES; ++s)
+                if ((issued >> s) & 1u)
+                    bounded_drain(full_bar(s), (last_par >> s) & 1u, p.timeout_ns, p.err);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+                if (!bounded_wait(tempty_bar(acc), acc_phase ^ 1u, wc)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
+                for (int kb = 0; kb < p.kblocks; ++kb) {
+                    if (!bounded_wait(full_bar(stage), phase, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sA = sbase + stage * STAGE_BYTES;
+                    const uint32_t sB = sA + A_BYTES;
+#pragma unroll
+                    for (int ks = 0; ks < BK / 16; ++ks) {
+                        const uint64_t ad = smem_desc_sw128(sA + ks * 32, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(sB + ks * 2048, STRIP_BYTES, 1024);
+                        tc_mma_bf16(d_tmem, ad, bd, IDESC, (kb | ks) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(empty_bar(stage));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(tfull_bar(acc));
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            tc_commit(drain_bar);
+            bounded_drain(drain_bar, 0, p.timeout_ns, p.err);
+        }
+    } else {
+        // ---------------- epilogue warps 2..5 ----------------
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int r = q * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int u = blockIdx.x; u < total; u += gridDim.x) {
+            const Unit t = decode_unit<SWIGLU>(u, p, total0, s_mtp, s_off);
+            int ok = 1;
+            if (lane == 0) ok = bounded_wait(tfull_bar(acc), acc_phase, wc) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t tb =
+                tmem_base + static_cast<uint32_t>(acc * ACC_COLS) + (static_cast<uint32_t>(q * 32) << 16);
+            const bool rv = r < t.rows;
+            const size_t orow = static_cast<size_t>(t.row0 + r);
+            const int N = p.N[t.g];
+            void* out = p.out[t.g];
+            const int ld = p.out_ld[t.g];
+            const int of32 = p.out_f32[t.g];
+            if (SWIGLU) {
+#pragma unroll 1
+                for (int c = 0; c < 128; c += 16) {
+                    uint32_t gr[16], ur[16];
+                    tc_ld_32x32b_x16(tb + c, gr);
+                    tc_ld_32x32b_x16(tb + 128 + c, ur);
+                    tc_wait_ld();
+                    const int lim = N - (t.n0 + c);
+                    if (rv && lim > 0) {
+                        float h[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            h[i] = silu_f(__uint_as_float(gr[i])) * __uint_as_float(ur[i]);
+                        store16(out, of32, orow, ld, t.out_col0 + c, h, lim);
+                    }
+                }
+            } else {
+                float rs = 1.0f;
+                if (t.g == 0 && p.rowscale0 != nullptr && rv) rs = p.rowscale0[orow];
+                const bool comb = (t.g == 1 && p.inv != nullptr);
+                const bool add = (t.g == 1 && p.addend != nullptr);
+                int pos[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    pos[k] = (comb && rv && k < p.Kr) ? p.inv[orow * p.Kr + k] : 0;
+#pragma unroll 1
+                for (int c = 0; c < 256; c += 16) {
+                    uint32_t vr[16];
+                    tc_ld_32x32b_x16(tb + c, vr);
+                    tc_wait_ld();
+                    const int lim = N - (t.n0 + c);
+                    if (rv && lim > 0) {
+                        float v[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] = rs * __uint_as_float(vr[i]);
+                        const int col = t.out_col0 + c;
+                        if (comb) {
+                            for (int k = 0; k < p.Kr; ++k) {
+                                const __nv_bfloat16* yp = p.ys + static_cast<size_t>(pos[k]) * p.ys_ld + col;
+                                if (lim >= 16) {
+                                    const uint4 a = *reinterpret_cast<const uint4*>(yp);
+                                    const uint4 b = *reinterpret_cast<const uint4*>(yp + 8);
+                                    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+                                    for (int i = 0; i < 8; ++i) {
+                                        v[2 * i] += bf16_lo(w[i]);
+                                        v[2 * i + 1] += bf16_hi(w[i]);
+                                    }
+                                } else {
+                                    for (int i = 0; i < lim; ++i) v[i] += __bfloat162float(yp[i]);
+                                }
+                            }
+                        }
+                        if (add) {
+                            const float* ap = p.addend + orow * static_cast<size_t>(p.add_ld) + col;
+                            for (int i = 0; i < 16 && i < lim; ++i) v[i] += ap[i];
+                        }
+                        store16(out, of32, orow, ld, col, v, lim);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+bool make_A_map(CUtensorMap* m, const void* A, int rows, int K, int lda) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rows)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(lda) * 2};
+    const uint32_t box[2] = {64, BM};
+    return encode_tmap(m, A, 2, dims, strides, box);
+}
+
+bool make_B_map(CUtensorMap* m, const void* B, int Z, int K, int N) {
+    const uint64_t dims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K),
+                              static_cast<uint64_t>(Z)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(K) * N * 2};
+    const uint32_t box[3] = {64, 64, 1};
+    return encode_tmap(m, B, 3, dims, strides, box);
+}
+
+template <bool SWIGLU>
+cudaError_t launch_tc_t(const TcGemmArgs& a, cudaStream_t s) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(tc_grouped_gemm_kernel<SWIGLU>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    constexpr int BNO = SWIGLU ? 128 : 256;
+    TcParams p;
+    memset(&p, 0, sizeof(p));
+    long long units_bound = 0;
+    for (int g = 0; g < 2; ++g) {
+        const TcGroup& G = a.g[g];
+        p.enabled[g] = G.enabled;
+        if (!G.enabled) continue;
+        if (!make_A_map(&p.mapA[g], G.A, G.rows, a.K, G.lda)) return cudaErrorInvalidValue;
+        if (!make_B_map(&p.mapB0[g], G.B0, G.Z, a.K, G.N)) return cudaErrorInvalidValue;
+        if (SWIGLU && !make_B_map(&p.mapB1[g], G.B1, G.Z, a.K, G.N)) return cudaErrorInvalidValue;
+        p.rows[g] = G.rows;
+        p.N[g] = G.N;
+        p.nt[g] = (G.N + BNO - 1) / BNO;
+        p.Z[g] = G.Z;
+        p.out[g] = G.out;
+        p.out_ld[g] = G.out_ld;
+        p.out_f32[g] = G.out_f32;
+        if (g == 0)
+            units_bound += static_cast<long long>((G.rows + BM - 1) / BM + a.E) * p.nt[0];
+        else
+            units_bound += static_cast<long long>((G.rows + BM - 1) / BM) * G.Z * p.nt[1];
+    }
+    p.kblocks = (a.K + BK - 1) / BK;
+    p.E = a.E;
+    p.mt1 = a.g[1].enabled ? (a.g[1].rows + BM - 1) / BM : 0;
+    p.offsets = a.offsets;
+    p.mt_prefix = a.mt_prefix;
+    p.rowscale0 = a.rowscale0;
+    p.inv = a.inv;
+    p.ys = static_cast<const __nv_bfloat16*>(a.ys);
+    p.ys_ld = a.ys_ld;
+    p.Kr = a.Kr;
+    p.addend = a.addend;
+    p.add_ld = a.add_ld;
+    p.err = a.err;
+    p.timeout_ns = wait_timeout_ns();
+    long long grid = num_sms();
+    if (units_bound < grid) grid = units_bound;
+    if (grid < 1) grid = 1;
+    tc_grouped_gemm_kernel<SWIGLU><<<static_cast<int>(grid), THREADS, SMEM_BYTES, s>>>(p);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t s) {
+    return a.swiglu ? launch_tc_t<true>(a, s) : launch_tc_t<false>(a, s);
+}
+
+}  // namespace moe

@@ -258,21 +258,30 @@ def dispatch(idx, E):
 # --------------------------------------------------------------------------
 
 class _WeightCache:
-    """float64 copies of expert matrices, made on first use."""
+    """float64 copies of expert matrices, made on first use; at most
+    max_entries are kept (least recently used dropped) so that large layers
+    can be sampled token by token with bounded host memory."""
 
-    def __init__(self, params):
+    def __init__(self, params, max_entries=48):
         self.p = params
         self.c = {}
+        self.max_entries = max_entries
 
     def get(self, name, i=None):
         key = (name, i)
-        if key not in self.c:
-            a = self.p[name]
-            a = a if i is None else a[i]
-            if hasattr(a, "detach"):
-                a = a.detach().float().cpu().numpy()
-            self.c[key] = f64(a)
-        return self.c[key]
+        if key in self.c:
+            v = self.c.pop(key)
+            self.c[key] = v
+            return v
+        a = self.p[name]
+        a = a if i is None else a[i]
+        if hasattr(a, "detach"):
+            a = a.detach().float().cpu().numpy()
+        v = f64(a)
+        self.c[key] = v
+        while len(self.c) > self.max_entries:
+            self.c.pop(next(iter(self.c)))
+        return v
 
 
 def _to_np(a):

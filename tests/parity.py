@@ -1,0 +1,154 @@
+"""Glue for the GPU parity tests: run the CUDA path through the C ABI and the
+oracle on the same seeded inputs, and compare.
+
+Tolerances (BASELINE the benchmark spec): routing ids, counts and permutations
+bit-exact wherever the oracle's rank-K / rank-(K+1) score margin exceeds
+1e-5 (near-ties are counted, and for those tokens the oracle adopts the GPU's
+expert selection, with gate weights by its own formulas); layer outputs
+within max-abs 1e-4 for FP32 layers and 2e-2 x RMS(oracle output) for BF16.
+"""
+import math
+
+import numpy as np
+import torch
+
+from mixture_experts_ffn_fp32_gb300 import api
+from mixture_experts_ffn_fp32_gb300 import workloads as W
+from oracle import moe_oracle as O
+
+NEAR_TIE = 1e-5
+F32_ATOL = 1e-4
+BF16_REL = 2e-2
+
+
+def np64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def npi(t):
+    return t.detach().cpu().numpy().astype(np.int64)
+
+
+def spec_of(w: W.Workload) -> api.LayerSpec:
+    return api.LayerSpec.of(w)
+
+
+def oracle_routing(w: W.Workload, inputs, rows=None):
+    x = inputs["x"] if rows is None else inputs["x"][rows]
+    return O.route(np64(x), np64(inputs["W_router"]),
+                   None if inputs["bias"] is None else np64(inputs["bias"]),
+                   w.gate, w.K, w.renormalize, w.routed_scale)
+
+
+def merge_routing(w: W.Workload, inputs, ort, gpu_idx):
+    """Oracle routing with the GPU's selection adopted for near-tie tokens."""
+    near = ort["margin"] <= NEAR_TIE
+    idx = ort["idx"].copy()
+    wts = ort["w"].copy()
+    bias = None if inputs["bias"] is None else np64(inputs["bias"])
+    for t in np.where(near)[0]:
+        idx[t] = gpu_idx[t]
+        wts[t] = O.gates_for(ort["logits"][t], bias, w.gate, gpu_idx[t], w.renormalize,
+                             w.routed_scale)
+    return idx, wts, near
+
+
+def check_routing(w, ort, gpu, near):
+    """Bit-exact ids outside near ties; weights and margins close everywhere."""
+    gi = npi(gpu["idx"])
+    far = ~near
+    mism = np.where((gi[far] != ort["idx"][far]).any(axis=1))[0]
+    assert mism.size == 0, f"{mism.size} tokens routed differently outside near ties"
+    # every GPU selection is K distinct valid ids
+    assert gi.min() >= 0 and gi.max() < w.E
+    srt = np.sort(gi, axis=1)
+    assert w.K == 1 or (np.diff(srt, axis=1) > 0).all()
+    gw = np64(gpu["w"])
+    np.testing.assert_allclose(gw[far], ort["w"][far], atol=2e-6, rtol=1e-5)
+    gm = np64(gpu["margin"])
+    om = ort["margin"]
+    fin = np.isfinite(om)
+    np.testing.assert_allclose(gm[fin], om[fin], atol=2e-5, rtol=1e-4)
+    assert np.all(np.isinf(gm[~fin]))
+    if w.gate == "sigmoid":
+        np.testing.assert_allclose(np64(gpu["top_scores"])[far], ort["top_scores"][far],
+                                   atol=2e-6, rtol=0)
+        np.testing.assert_allclose(np64(gpu["scores"]), ort["s"], atol=2e-6, rtol=0)
+    else:
+        np.testing.assert_allclose(gw.sum(axis=1), 1.0, atol=2e-6)
+
+
+def check_dispatch(w, idx, wts_gpu_flat, gpu):
+    """GPU dispatch results == oracle dispatch of the routing idx, bit for bit."""
+    dp = O.dispatch(idx, w.E)
+    assert np.array_equal(npi(gpu["counts"]), dp["counts"])
+    assert np.array_equal(npi(gpu["offsets"]), dp["offsets"])
+    assert np.array_equal(npi(gpu["sorted_token"]), dp["sorted_token"])
+    assert np.array_equal(npi(gpu["inv"]).reshape(-1), dp["inv"].reshape(-1))
+    sw = gpu["sorted_w"].detach().cpu().numpy()
+    assert np.array_equal(sw, wts_gpu_flat[dp["order"]])
+    assert int(dp["counts"].sum()) == w.T * w.K
+    return dp
+
+
+def check_output(w, out_gpu, ref, rows=None):
+    g = np64(out_gpu)
+    if rows is not None:
+        g, ref = g[rows], ref[rows]
+    assert np.isfinite(g).all(), "non-finite GPU output"
+    err = float(np.abs(g - ref).max())
+    if w.dtype == "f32":
+        assert err <= F32_ATOL, f"max-abs error {err:.3e} > {F32_ATOL}"
+        return err, None
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    assert err <= BF16_REL * rms, f"max-abs error {err:.3e} > {BF16_REL} x RMS {rms:.3e}"
+    return err, rms
+
+
+def run_forward(w: W.Workload, inputs, stream=None):
+    spec = spec_of(w)
+    ws = api.alloc_workspace(spec)
+    out = api.forward(spec, inputs["x"], inputs, ws=ws)
+    st = api.workspace_status(ws)
+    assert st == api.MOE_OK, api.status_string(st)
+    views = api.workspace_views(spec, ws)
+    return out, views, ws
+
+
+def sample_rows(w, gpu_idx, n=12, seed=0):
+    """First, last, random tokens and tokens routed to the rarest used experts."""
+    rng = np.random.default_rng(seed)
+    T = w.T
+    rows = {0, T - 1}
+    rows.update(int(v) for v in rng.choice(T, size=min(T, n // 2), replace=False))
+    counts = np.bincount(gpu_idx.reshape(-1), minlength=w.E)
+    used = np.where(counts > 0)[0]
+    rare = used[np.argsort(counts[used], kind="stable")][: max(1, n // 4)]
+    for e in rare:
+        t = int(np.where((gpu_idx == e).any(axis=1))[0][0])
+        rows.add(t)
+    return sorted(rows)[: n + 4]
+
+
+def full_parity(w: W.Workload, device="cuda", sample=None):
+    """Forward on the GPU, then: routing bit-exact on all tokens (outside near
+    ties), dispatch bit-exact on all assignments, outputs vs the oracle on all
+    rows (sample=None) or a sampled row set."""
+    inputs = W.make_inputs(w, device=device)
+    out, views, ws = run_forward(w, inputs)
+    torch.cuda.synchronize()
+    ort = oracle_routing(w, inputs)
+    gi = npi(views["idx"])
+    idx, wts, near = merge_routing(w, inputs, ort, gi)
+    check_routing(w, ort, views, near)
+    # dispatch of the oracle's routing (GPU selection only at near ties), bit for bit
+    check_dispatch(w, idx, views["w"].detach().cpu().numpy().reshape(-1), views)
+    rows = None if sample is None else sample_rows(w, gi, n=sample)
+    ref, _ = O.moe_forward(inputs["x"], inputs, w.gate, w.K, w.renormalize, w.routed_scale,
+                           tokens=rows, routing=(idx, wts))
+    err, rms = check_output(w, out, ref, rows)
+    res = {"near_ties": int(near.sum()), "max_err": err, "rms": rms,
+           "rows": w.T if rows is None else len(rows)}
+    del inputs, out, views, ws
+    torch.cuda.empty_cache()
+    return res
