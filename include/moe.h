@@ -85,6 +85,9 @@ typedef struct moe_config {
     int32_t gate;         /* moe_gate */
     int32_t renormalize;  /* sigmoid mode: divide the K weights by their sum */
     float routed_scale;   /* sigmoid mode: factor on the routed weights (1.0 = none) */
+    int32_t out_dtype;    /* moe_dtype of out: MOE_F32 (the FP32 accumulation, unrounded) or
+                             MOE_BF16 (rounded once to nearest-even); must be MOE_F32 when
+                             dtype is MOE_F32 */
 } moe_config;
 
 /* Weights, all device pointers. d_e = latent_dim ? latent_dim : d.
@@ -140,17 +143,23 @@ moe_status moe_get_workspace_views(const moe_config* cfg, void* ws, moe_workspac
 
 /* Router: logits r = x W_router in FP32 (x read as FP32 when dtype is BF16,
  * which is exact), the mode's selection score, top-K (top-(K+1) in sigmoid
- * mode) and gate weights. One fused kernel; no workspace.
+ * mode) and gate weights.
  *   x [T, d] (dtype), W_router [d, E] FP32, bias [E] FP32 or NULL.
  *   Outputs (device): topk_idx [T, K] int32, topk_w [T, K] FP32, required;
  *   margin [T] FP32, top_scores [T, K+1] FP32 and scores [T, E] FP32 optional
  *   (NULL = not written); top_scores/scores are only produced in sigmoid mode.
+ *   ws: NULL, or a workspace of moe_workspace_size(cfg) bytes. With a
+ *   workspace, BF16 layers with E > 32, E % 8 == 0 and d % 64 == 0 compute
+ *   the logits on the tensor cores from an exact three-part BF16 split of
+ *   W_router (the same path moe_forward takes); otherwise, and without a
+ *   workspace, one fused FP32 FMA kernel computes them. Both are FP32-accurate
+ *   but sum in different orders, so near-tie tokens may rank differently.
  * Sources: APEX-1 docs "10 - Mixture of Experts" steps 2-3; APEX-1 Math Ref
  * Part 3 sections 13.2 and 13.5; "MoE from scratch" MoELayer.forward;
  * kimi_k3 StableLatentMoE "FP32 router and training-only QB update". */
 moe_status moe_route(const moe_config* cfg, const void* x, const float* W_router,
                      const float* bias, int32_t* topk_idx, float* topk_w, float* margin,
-                     float* top_scores, float* scores, void* stream);
+                     float* top_scores, float* scores, void* ws, size_t ws_bytes, void* stream);
 
 /* Sorted dispatch of the T*K assignments by expert id: a stable counting sort
  * of the flat assignments j = t*K + k (kimi_k3 StableLatentMoE, "Flatten
@@ -171,7 +180,7 @@ moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const fl
 /* Whole layer forward: route -> dispatch -> grouped gate/up GEMM with
  * SiLU(.)*up epilogue -> grouped down GEMM scaled by the gate weight ->
  * shared experts -> deterministic combine (no float atomics).
- *   x [T, d] (dtype, device), out [T, d] (dtype, device).
+ *   x [T, d] (dtype, device), out [T, d] (out_dtype, device).
  *   The routing and dispatch results stay in ws (moe_get_workspace_views).
  *   The balance bias is read, never written (use moe_quantile_bias_update).
  * Sources: APEX-1 Math Ref Part 3 sections 12.2 and 13.2; APEX-1 docs
@@ -181,8 +190,8 @@ moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const fl
 moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* w, void* out,
                        void* ws, size_t ws_bytes, void* stream);
 
-/* moe_forward with HOST input and output: copies x_host [T, d] to the
- * device (inside ws), runs the forward and copies out [T, d] back to
+/* moe_forward with HOST input and output: copies x_host [T, d] (dtype) to the
+ * device (inside ws), runs the forward and copies out [T, d] (out_dtype) back to
  * out_host, all on `stream`, then synchronises the stream before returning.
  * Pinned host memory makes the copies asynchronous DMA; pageable works too. */
 moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const moe_weights* w,
@@ -217,15 +226,19 @@ moe_status moe_sign_bias_update(int32_t E, int32_t N, int32_t K, const int32_t* 
 /* Synchronises `stream`, then reads and clears the device-side error word of
  * the workspace: MOE_OK, MOE_ERR_TIMEOUT (a bounded device wait ran out and
  * its kernel stopped early; outputs of that call are invalid) or
- * MOE_ERR_DEVICE_INDEX. */
+ * MOE_ERR_DEVICE_INDEX. moe_forward and moe_dispatch clear the word when
+ * they start, so the status covers the calls since the last of those. */
 moe_status moe_workspace_status(void* ws, void* stream);
 
 /* Instrumentation. While enabled, each moe_forward records CUDA events
- * around each of its kernel stages on the caller's stream (up to max_calls
- * calls). moe_timing_end synchronises those events and returns, per stage,
- * the summed milliseconds over the recorded calls. Stage names via
- * moe_stage_name. Events are created/destroyed by the library. */
-moe_status moe_timing_begin(int32_t max_calls);
+ * around each of its kernel stages selected by stage_mask (bit i = stage i;
+ * 0xFFFFFFFF = all) on the caller's stream, for up to max_calls calls.
+ * moe_timing_end synchronises those events and returns, per stage, the summed
+ * milliseconds over the recorded calls. Stage names via moe_stage_name.
+ * Events are created/destroyed by the library. Recording an event between
+ * two kernels stops the second from overlapping the first's tail, so time
+ * only the stages you need. */
+moe_status moe_timing_begin(int32_t max_calls, uint32_t stage_mask);
 moe_status moe_timing_end(float* stage_ms, int32_t max_stages, int32_t* n_stages,
                           int32_t* n_calls);
 const char* moe_stage_name(int32_t stage);

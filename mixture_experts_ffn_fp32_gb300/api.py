@@ -36,7 +36,8 @@ class Config(ctypes.Structure):
                 ("E", ctypes.c_int32), ("K", ctypes.c_int32), ("n_shared", ctypes.c_int32),
                 ("shared_d_ff", ctypes.c_int32), ("latent_dim", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("gate", ctypes.c_int32),
-                ("renormalize", ctypes.c_int32), ("routed_scale", ctypes.c_float)]
+                ("renormalize", ctypes.c_int32), ("routed_scale", ctypes.c_float),
+                ("out_dtype", ctypes.c_int32)]
 
 
 class Weights(ctypes.Structure):
@@ -70,7 +71,7 @@ def lib() -> ctypes.CDLL:
             "moe_version": (ctypes.c_char_p, []),
             "moe_workspace_size": (ctypes.c_int, [cfgp, ctypes.POINTER(sz)]),
             "moe_get_workspace_views": (ctypes.c_int, [cfgp, vp, ctypes.POINTER(Views)]),
-            "moe_route": (ctypes.c_int, [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
+            "moe_route": (ctypes.c_int, [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
             "moe_dispatch": (ctypes.c_int, [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
             "moe_forward": (ctypes.c_int, [cfgp, vp, ctypes.POINTER(Weights), vp, vp, sz, vp]),
             "moe_forward_host": (ctypes.c_int, [cfgp, vp, ctypes.POINTER(Weights), vp, vp, sz, vp]),
@@ -78,7 +79,7 @@ def lib() -> ctypes.CDLL:
             "moe_quantile_workspace_size": (sz, [i32, i32]),
             "moe_sign_bias_update": (ctypes.c_int, [i32, i32, i32, vp, vp, ctypes.c_float, vp]),
             "moe_workspace_status": (ctypes.c_int, [vp, vp]),
-            "moe_timing_begin": (ctypes.c_int, [i32]),
+            "moe_timing_begin": (ctypes.c_int, [i32, ctypes.c_uint32]),
             "moe_timing_end": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float), i32,
                                               ctypes.POINTER(i32), ctypes.POINTER(i32)]),
             "moe_stage_name": (ctypes.c_char_p, [i32]),
@@ -135,22 +136,28 @@ class LayerSpec:
     gate: str = "softmax_topk"
     renormalize: bool = False
     routed_scale: float = 1.0
+    out_dtype: str = "f32"
 
     @staticmethod
-    def of(w) -> "LayerSpec":
+    def of(w, out_dtype: str = "f32") -> "LayerSpec":
         """From any object with the Workload attribute names."""
         return LayerSpec(w.T, w.d, w.d_ff, w.E, w.K, w.n_shared, w.shared_d_ff, w.latent_dim,
-                         w.dtype, w.gate, bool(w.renormalize), float(w.routed_scale))
+                         w.dtype, w.gate, bool(w.renormalize), float(w.routed_scale), out_dtype)
 
     def config(self) -> Config:
         return Config(self.T, self.d, self.d_ff, self.E, self.K, self.n_shared,
                       self.shared_d_ff if self.n_shared else 0, self.latent_dim,
                       MOE_F32 if self.dtype == "f32" else MOE_BF16, GATES[self.gate],
-                      int(self.renormalize), float(self.routed_scale))
+                      int(self.renormalize), float(self.routed_scale),
+                      MOE_F32 if self.out_dtype == "f32" else MOE_BF16)
 
     @property
     def torch_dtype(self):
         return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+    @property
+    def torch_out_dtype(self):
+        return torch.float32 if self.out_dtype == "f32" else torch.bfloat16
 
 
 def workspace_size(spec: LayerSpec) -> int:
@@ -201,9 +208,11 @@ def weights_struct(spec: LayerSpec, p: dict) -> Weights:
     return w
 
 
-def route(spec: LayerSpec, x: torch.Tensor, W_router: torch.Tensor, bias=None, stream=None):
+def route(spec: LayerSpec, x: torch.Tensor, W_router: torch.Tensor, bias=None, stream=None,
+          ws: torch.Tensor | None = None):
     """moe_route: returns dict idx [T,K] int32, w [T,K], margin [T] (+ top_scores
-    [T,K+1] and scores [T,E] in sigmoid mode)."""
+    [T,K+1] and scores [T,E] in sigmoid mode). With a workspace the tensor-core
+    router is used where the layer allows it (as in forward)."""
     dev = x.device
     _dev(x, spec.torch_dtype, "x", (spec.T, spec.d))
     _dev(W_router, torch.float32, "W_router", (spec.d, spec.E))
@@ -221,7 +230,8 @@ def route(spec: LayerSpec, x: torch.Tensor, W_router: torch.Tensor, bias=None, s
     _check(lib().moe_route(ctypes.byref(spec.config()), x.data_ptr(), W_router.data_ptr(),
                            _ptr(bias), out["idx"].data_ptr(), out["w"].data_ptr(),
                            out["margin"].data_ptr(), _ptr(out.get("top_scores")),
-                           _ptr(out.get("scores")), _stream(stream)), "moe_route")
+                           _ptr(out.get("scores")), _ptr(ws), 0 if ws is None else ws.numel(),
+                           _stream(stream)), "moe_route")
     return out
 
 
@@ -254,8 +264,9 @@ def forward(spec: LayerSpec, x: torch.Tensor, params: dict, out: torch.Tensor | 
     """moe_forward: the whole layer on device tensors."""
     _dev(x, spec.torch_dtype, "x", (spec.T, spec.d))
     ws = alloc_workspace(spec, x.device) if ws is None else ws
-    out = torch.empty((spec.T, spec.d), dtype=spec.torch_dtype, device=x.device) if out is None else out
-    _dev(out, spec.torch_dtype, "out", (spec.T, spec.d))
+    if out is None:
+        out = torch.empty((spec.T, spec.d), dtype=spec.torch_out_dtype, device=x.device)
+    _dev(out, spec.torch_out_dtype, "out", (spec.T, spec.d))
     w = weights_struct(spec, params)
     _check(lib().moe_forward(ctypes.byref(spec.config()), x.data_ptr(), ctypes.byref(w),
                              out.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)),
@@ -266,9 +277,9 @@ def forward(spec: LayerSpec, x: torch.Tensor, params: dict, out: torch.Tensor | 
 def forward_host(spec: LayerSpec, x_host: torch.Tensor, params: dict, out_host: torch.Tensor,
                  ws: torch.Tensor, stream=None) -> torch.Tensor:
     """moe_forward_host: host x / out (pinned for asynchronous DMA); synchronises."""
-    for n, t in (("x_host", x_host), ("out_host", out_host)):
-        if t.is_cuda or not t.is_contiguous() or t.dtype != spec.torch_dtype:
-            raise ValueError(f"{n} must be a contiguous host tensor of {spec.torch_dtype}")
+    for n, t, dt in (("x_host", x_host, spec.torch_dtype), ("out_host", out_host, spec.torch_out_dtype)):
+        if t.is_cuda or not t.is_contiguous() or t.dtype != dt or t.numel() != spec.T * spec.d:
+            raise ValueError(f"{n} must be a contiguous host tensor of {dt} with T*d elements")
     w = weights_struct(spec, params)
     _check(lib().moe_forward_host(ctypes.byref(spec.config()), x_host.data_ptr(), ctypes.byref(w),
                                   out_host.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)),
@@ -348,11 +359,16 @@ def selftest_wait_timeout(ms: int, ws: torch.Tensor, stream=None) -> int:
     return lib().moe_selftest_wait_timeout(int(ms), ws.data_ptr(), _stream(stream))
 
 
-class StageTimer:
-    """Per-stage CUDA-event timing of moe_forward calls (library-owned events)."""
+STAGES = ["router", "latent_down", "dispatch", "gather", "gate_up", "down", "combine", "latent_up"]
 
-    def __init__(self, max_calls: int):
-        _check(lib().moe_timing_begin(int(max_calls)), "moe_timing_begin")
+
+class StageTimer:
+    """Per-stage CUDA-event timing of moe_forward calls (library-owned events).
+    stages: names to time (None = all)."""
+
+    def __init__(self, max_calls: int, stages=None):
+        mask = 0xFFFFFFFF if stages is None else sum(1 << STAGES.index(n) for n in stages)
+        _check(lib().moe_timing_begin(int(max_calls), mask), "moe_timing_begin")
 
     def finish(self) -> tuple[dict, int]:
         arr = (ctypes.c_float * 32)()

@@ -87,6 +87,8 @@ moe_status validate_config(const moe_config& c) {
         return MOE_ERR_INVALID_ARG;
     if (c.gate == MOE_GATE_SIGMOID && c.K + 1 > c.E) return MOE_ERR_INVALID_ARG;
     if (c.dtype != MOE_F32 && c.dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (c.out_dtype != MOE_F32 && c.out_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (c.dtype == MOE_F32 && c.out_dtype != MOE_F32) return MOE_ERR_UNSUPPORTED;
     if (c.n_shared < 0 || (c.n_shared > 0 && c.shared_d_ff < 1)) return MOE_ERR_INVALID_ARG;
     if (c.latent_dim < 0) return MOE_ERR_INVALID_ARG;
     if (!(c.routed_scale == c.routed_scale)) return MOE_ERR_INVALID_ARG;
@@ -101,6 +103,27 @@ moe_status validate_config(const moe_config& c) {
 }
 
 static size_t align_up(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool router_on_tensor_cores(const moe_config& c) {
+    return c.dtype == MOE_BF16 && c.E > 32 && c.E % 8 == 0 && c.d % ROUTER_CHUNK == 0;
+}
+
+int router_ksplit(int T, int d) {
+    (void)T;
+    return d / ROUTER_CHUNK;
+}
+
+// The router GEMM: x [T, d] against the chunk-interleaved split weights W3
+// [3d, E]; reduction k-block kb reads x k-block (kb / 12) * 4 + kb % 4.
+static TcGroup router_group(const void* x, int T, int d, int E, void* w3, void* rpart) {
+    TcGroup g{1, 3 * d, x, d, T, w3, nullptr, 1, E, rpart, E, 1};
+    g.a_kgroup = ROUTER_CHUNK / 64;
+    g.a_krep = 3;
+    g.ksplit = d / ROUTER_CHUNK;
+    return g;
+}
+
+static int latent_pad(int L) { return (L + 63) / 64 * 64; }
 
 WsLayout plan_workspace(const moe_config& c) {
     WsLayout L;
@@ -136,12 +159,16 @@ WsLayout plan_workspace(const moe_config& c) {
     L.h = take(TK * c.d_ff * es);
     const size_t SF = static_cast<size_t>(c.n_shared) * (c.n_shared ? c.shared_d_ff : 0);
     L.hs = SF ? take(T * SF * es) : 0;
-    L.ys = take(TK * de * es);
-    L.routed = c.latent_dim ? take(T * de * es) : 0;
-    L.shout = (c.latent_dim && c.n_shared) ? take(T * c.d * 4) : 0;
+    L.ys = take(TK * de * 4);  // FP32: the K routed rows are summed before one final rounding
+    // latent routed sum as a BF16 hi/lo pair, each part padded to a multiple of 64 columns
+    L.routed = c.latent_dim ? take(T * 2 * static_cast<size_t>(latent_pad(c.latent_dim)) * 2) : 0;
+    L.shout = c.n_shared ? take(T * c.d * 4) : 0;  // FP32 shared-expert output
     L.xstage = take(T * c.d * es);
-    L.ostage = take(T * c.d * es);
+    L.ostage = take(T * c.d * (c.out_dtype == MOE_BF16 ? 2 : 4));
     L.qb = take(E * 4);
+    const bool tcr = router_on_tensor_cores(c);
+    L.w3 = tcr ? take(3 * static_cast<size_t>(c.d) * E * 2) : 0;
+    L.rpart = tcr ? take(static_cast<size_t>(router_ksplit(c.T, c.d)) * T * E * 4) : 0;
     L.total = o;
     return L;
 }
@@ -152,11 +179,12 @@ WsLayout plan_workspace(const moe_config& c) {
 enum Stage { ST_ROUTE = 0, ST_LATENT_DOWN, ST_DISPATCH, ST_GATHER, ST_GATEUP, ST_DOWN, ST_COMBINE,
              ST_LATENT_UP, ST_COUNT };
 static const char* kStageNames[ST_COUNT] = {"router", "latent_down", "dispatch", "gather",
-                                            "gate_up", "down", "shared_down_combine", "latent_up"};
+                                            "gate_up", "down", "combine", "latent_up"};
 
 struct Timing {
     std::mutex mu;
     bool on = false;
+    uint32_t mask = 0xFFFFFFFFu;
     int max_calls = 0, calls = 0;
     std::vector<cudaEvent_t> ev;  // [max_calls][ST_COUNT][2]
     std::vector<char> used;       // [max_calls][ST_COUNT]
@@ -167,10 +195,11 @@ struct StageRec {
     int call = -1;
     cudaStream_t s = nullptr;
     void begin(int st) {
-        if (call >= 0) cudaEventRecord(g_timing.ev[(call * ST_COUNT + st) * 2], s);
+        if (call >= 0 && ((g_timing.mask >> st) & 1u))
+            cudaEventRecord(g_timing.ev[(call * ST_COUNT + st) * 2], s);
     }
     void end(int st) {
-        if (call >= 0) {
+        if (call >= 0 && ((g_timing.mask >> st) & 1u)) {
             cudaEventRecord(g_timing.ev[(call * ST_COUNT + st) * 2 + 1], s);
             g_timing.used[call * ST_COUNT + st] = 1;
         }
@@ -210,6 +239,7 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
     const int de = c.latent_dim ? c.latent_dim : c.d;
     const int S = c.n_shared, Fs = c.shared_d_ff, SF = S * (S ? Fs : 0);
     const size_t es = bf ? 2 : 4;
+    const int of32 = c.out_dtype == MOE_F32 ? 1 : 0;
     int* err = reinterpret_cast<int*>(ws + L.err);
     auto P = [&](size_t off) { return static_cast<void*>(ws + off); };
     int32_t* idx = static_cast<int32_t*>(P(L.topk_idx));
@@ -236,7 +266,21 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
     ra.margin = static_cast<float*>(P(L.margin));
     ra.top_scores = L.top_scores ? static_cast<float*>(P(L.top_scores)) : nullptr;
     ra.scores = L.scores ? static_cast<float*>(P(L.scores)) : nullptr;
-    if ((e = launch_router(ra, s)) != cudaSuccess) return cuda_status(e);
+    if (router_on_tensor_cores(c)) {
+        if ((e = launch_router_split(w.W_router, c.d, E, P(L.w3), err, s)) != cudaSuccess)
+            return cuda_status(e);
+        const int ks = router_ksplit(T, c.d);
+        TcGemmArgs g{};
+        g.g[1] = router_group(x, T, c.d, E, P(L.w3), P(L.rpart));
+        g.err = err;
+        if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
+        if ((e = launch_route_from_logits(static_cast<const float*>(P(L.rpart)), ks, ra, s)) !=
+            cudaSuccess)
+            return cuda_status(e);
+    } else {
+        ra.err_clear = err;
+        if ((e = launch_router(ra, s)) != cudaSuccess) return cuda_status(e);
+    }
     rec.end(ST_ROUTE);
 
     // 1b. latent compression z = x W_down_latent (once per token)
@@ -244,8 +288,8 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
     if (c.latent_dim) {
         rec.begin(ST_LATENT_DOWN);
         TcGemmArgs g{};
-        g.g[1] = TcGroup{1, x, c.d, T, w.W_down_latent, nullptr, 1, c.latent_dim, P(L.z), c.latent_dim, 0};
-        g.K = c.d;
+        g.g[1] = TcGroup{1, c.d, x, c.d, T, w.W_down_latent, nullptr, 1, c.latent_dim, P(L.z),
+                         c.latent_dim, 0};
         g.err = err;
         if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
         ex_src = P(L.z);
@@ -272,77 +316,62 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
     rec.end(ST_DISPATCH);
 
     if (bf) {
+        float* ys = static_cast<float*>(P(L.ys));
+        float* shout = S ? static_cast<float*>(P(L.shout)) : nullptr;
         // 3. gather the routed rows into expert order
         rec.begin(ST_GATHER);
         if ((e = launch_gather_rows(ex_src, sorted_token, TK, de * 2, P(L.xs), s)) != cudaSuccess)
             return cuda_status(e);
         rec.end(ST_GATHER);
 
-        // 4. gate/up (+ SiLU * up) for routed and shared experts in one launch
+        // 4. gate/up with the SiLU(gate) * up epilogue: routed experts (group 0, on the
+        //    sorted rows) and shared experts (group 1, on x) in one launch
         rec.begin(ST_GATEUP);
-        if (c.latent_dim && S) {
-            // routed experts (K = L) and the shared FFN (K = d) differ in K: two launches
+        {
             TcGemmArgs g{};
-            g.g[0] = TcGroup{1, P(L.xs), de, TK, w.W_gate, w.W_up, E, c.d_ff, P(L.h), c.d_ff, 0};
-            g.K = de; g.E = E; g.offsets = offsets; g.mt_prefix = mt_prefix; g.swiglu = 1; g.err = err;
-            if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
-            TcGemmArgs g2{};
-            g2.g[1] = TcGroup{1, x, c.d, T, w.Ws_gate, w.Ws_up, S, Fs, P(L.hs), SF, 0};
-            g2.K = c.d; g2.swiglu = 1; g2.err = err;
-            if ((e = launch_tc_gemm(g2, s)) != cudaSuccess) return cuda_status(e);
-        } else {
-            TcGemmArgs g{};
-            g.g[0] = TcGroup{1, P(L.xs), de, TK, w.W_gate, w.W_up, E, c.d_ff, P(L.h), c.d_ff, 0};
-            if (S) g.g[1] = TcGroup{1, x, c.d, T, w.Ws_gate, w.Ws_up, S, Fs, P(L.hs), SF, 0};
-            g.K = de; g.E = E; g.offsets = offsets; g.mt_prefix = mt_prefix; g.swiglu = 1; g.err = err;
+            g.g[0] = TcGroup{1, de, P(L.xs), de, TK, w.W_gate, w.W_up, E, c.d_ff, P(L.h), c.d_ff, 0};
+            if (S) g.g[1] = TcGroup{1, c.d, x, c.d, T, w.Ws_gate, w.Ws_up, S, Fs, P(L.hs), SF, 0};
+            g.E = E; g.offsets = offsets; g.mt_prefix = mt_prefix; g.swiglu = 1; g.err = err;
             if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
         }
         rec.end(ST_GATEUP);
 
-        // 5. routed down projection, scaled by each assignment's gate weight
+        // 5. down projections in one launch: routed rows scaled by their gate weight
+        //    (group 0, FP32 ys) and the shared experts summed over their concatenated
+        //    hidden width (group 1, FP32 shared output)
         rec.begin(ST_DOWN);
         {
             TcGemmArgs g{};
-            g.g[0] = TcGroup{1, P(L.h), c.d_ff, TK, w.W_down, nullptr, E, de, P(L.ys), de, 0};
-            g.K = c.d_ff; g.E = E; g.offsets = offsets; g.mt_prefix = mt_prefix; g.swiglu = 0;
+            g.g[0] = TcGroup{1, c.d_ff, P(L.h), c.d_ff, TK, w.W_down, nullptr, E, de, ys, de, 1};
+            if (S) g.g[1] = TcGroup{1, SF, P(L.hs), SF, T, w.Ws_down, nullptr, 1, c.d, shout, c.d, 1};
+            g.E = E; g.offsets = offsets; g.mt_prefix = mt_prefix; g.swiglu = 0;
             g.rowscale0 = sorted_w; g.err = err;
             if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
         }
         rec.end(ST_DOWN);
 
-        // 6. shared down projection + deterministic combine of the K routed rows
+        // 6. deterministic combine of the K routed rows of each token (+ shared)
         rec.begin(ST_COMBINE);
         if (!c.latent_dim) {
-            if (S) {
-                TcGemmArgs g{};
-                g.g[1] = TcGroup{1, P(L.hs), SF, T, w.Ws_down, nullptr, 1, c.d, out, c.d, 0};
-                g.K = SF; g.swiglu = 0; g.inv = inv; g.ys = P(L.ys); g.ys_ld = de; g.Kr = K;
-                g.err = err;
-                if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
-            } else {
-                if ((e = launch_gather_sum(P(L.ys), 1, inv, T, K, de, out, 1, s)) != cudaSuccess)
-                    return cuda_status(e);
-            }
+            if ((e = launch_gather_sum(ys, inv, T, K, de, shout, out, !of32, s)) != cudaSuccess)
+                return cuda_status(e);
             rec.end(ST_COMBINE);
         } else {
-            // routed sum in latent width, then back to model width plus the shared FFN
-            if ((e = launch_gather_sum(P(L.ys), 1, inv, T, K, de, P(L.routed), 1, s)) != cudaSuccess)
+            // routed sum in latent width as a BF16 hi/lo pair: the up projection reads
+            // [hi | lo] against W_up_latent twice, so the sum keeps ~16 bits into it
+            const int Lp = latent_pad(de);
+            if ((e = launch_gather_sum_split(ys, inv, T, K, de, Lp, P(L.routed), s)) != cudaSuccess)
                 return cuda_status(e);
-            if (S) {
-                TcGemmArgs g{};
-                g.g[1] = TcGroup{1, P(L.hs), SF, T, w.Ws_down, nullptr, 1, c.d, P(L.shout), c.d, 1};
-                g.K = SF; g.swiglu = 0; g.err = err;
-                if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
-            }
             rec.end(ST_COMBINE);
             rec.begin(ST_LATENT_UP);
             TcGemmArgs g{};
-            g.g[1] = TcGroup{1, P(L.routed), de, T, w.W_up_latent, nullptr, 1, c.d, out, c.d, 0};
-            g.K = de; g.swiglu = 0; g.err = err;
-            if (S) {
-                g.addend = static_cast<const float*>(P(L.shout));
-                g.add_ld = c.d;
-            }
+            g.g[1] = TcGroup{1, 2 * Lp, P(L.routed), 2 * Lp, T, w.W_up_latent, nullptr, 1, c.d, out,
+                             c.d, of32};
+            g.g[1].b_kmod = Lp;
+            g.g[1].b_rows = de;
+            g.swiglu = 0; g.err = err;
+            g.addend = shout;
+            g.add_ld = c.d;
             if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
             rec.end(ST_LATENT_UP);
         }
@@ -384,7 +413,8 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
             g.ys_ld = c.d; g.Kr = K;
             if ((e = launch_simt_gemm(g, s)) != cudaSuccess) return cuda_status(e);
         } else {
-            if ((e = launch_gather_sum(P(L.ys), 0, inv, T, K, c.d, out, 0, s)) != cudaSuccess)
+            if ((e = launch_gather_sum(static_cast<const float*>(P(L.ys)), inv, T, K, c.d, nullptr,
+                                       out, 0, s)) != cudaSuccess)
                 return cuda_status(e);
         }
         rec.end(ST_COMBINE);
@@ -441,11 +471,15 @@ MOE_API moe_status moe_get_workspace_views(const moe_config* cfg, void* ws, moe_
 
 MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const float* W_router,
                              const float* bias, int32_t* topk_idx, float* topk_w, float* margin,
-                             float* top_scores, float* scores, void* stream) {
+                             float* top_scores, float* scores, void* ws, size_t ws_bytes,
+                             void* stream) {
     if (!cfg || !x || !W_router || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
     const moe_status v = validate_config(*cfg);
     if (v != MOE_OK) return v;
     if (!aligned16(x) || !aligned16(W_router)) return MOE_ERR_INVALID_ARG;
+    if (ws != nullptr && (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = plan_workspace(*cfg);
+    if (ws != nullptr && ws_bytes < L.total) return MOE_ERR_WORKSPACE;
     RouterArgs ra{};
     ra.x = x;
     ra.x_bf16 = cfg->dtype == MOE_BF16;
@@ -456,7 +490,24 @@ MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const float* 
     ra.idx = topk_idx; ra.w = topk_w; ra.margin = margin;
     ra.top_scores = top_scores;
     ra.scores = scores;
-    return cuda_status(launch_router(ra, static_cast<cudaStream_t>(stream)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (ws != nullptr) ra.err_clear = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + L.err);
+    if (ws != nullptr && router_on_tensor_cores(*cfg)) {
+        ra.err_clear = nullptr;
+        uint8_t* b = static_cast<uint8_t*>(ws);
+        int* err = reinterpret_cast<int*>(b + L.err);
+        cudaError_t e;
+        if ((e = launch_router_split(W_router, cfg->d, cfg->E, b + L.w3, err, s)) != cudaSuccess)
+            return cuda_status(e);
+        const int ks = router_ksplit(cfg->T, cfg->d);
+        TcGemmArgs g{};
+        g.g[1] = router_group(x, cfg->T, cfg->d, cfg->E, b + L.w3, b + L.rpart);
+        g.err = err;
+        if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
+        return cuda_status(
+            launch_route_from_logits(reinterpret_cast<const float*>(b + L.rpart), ks, ra, s));
+    }
+    return cuda_status(launch_router(ra, s));
 }
 
 MOE_API moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const float* topk_w,
@@ -480,7 +531,9 @@ MOE_API moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, 
     da.mt_prefix = reinterpret_cast<int32_t*>(b + L.mt_prefix);
     da.sorted_token = sorted_token; da.sorted_w = sorted_w; da.inv = inv;
     da.err = reinterpret_cast<int*>(b + L.err);
-    return cuda_status(launch_dispatch(da, static_cast<cudaStream_t>(stream), nullptr));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(da.err, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
+    return cuda_status(launch_dispatch(da, s, nullptr));
 }
 
 MOE_API moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* w, void* out,
@@ -506,12 +559,13 @@ MOE_API moe_status moe_forward_host(const moe_config* cfg, const void* x_host, c
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* b = static_cast<uint8_t*>(ws);
-    const size_t bytes = static_cast<size_t>(cfg->T) * cfg->d * (cfg->dtype == MOE_BF16 ? 2 : 4);
-    if (cudaMemcpyAsync(b + L.xstage, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    const size_t xbytes = static_cast<size_t>(cfg->T) * cfg->d * (cfg->dtype == MOE_BF16 ? 2 : 4);
+    const size_t obytes = static_cast<size_t>(cfg->T) * cfg->d * (cfg->out_dtype == MOE_BF16 ? 2 : 4);
+    if (cudaMemcpyAsync(b + L.xstage, x_host, xbytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     v = forward_impl(*cfg, b + L.xstage, *w, b + L.ostage, b, s);
     if (v != MOE_OK) return v;
-    if (cudaMemcpyAsync(out_host, b + L.ostage, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    if (cudaMemcpyAsync(out_host, b + L.ostage, obytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     return cuda_status(cudaStreamSynchronize(s));
 }
@@ -552,9 +606,10 @@ MOE_API moe_status moe_workspace_status(void* ws, void* stream) {
     return MOE_OK;
 }
 
-MOE_API moe_status moe_timing_begin(int32_t max_calls) {
+MOE_API moe_status moe_timing_begin(int32_t max_calls, uint32_t stage_mask) {
     if (max_calls < 1) return MOE_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lk(g_timing.mu);
+    g_timing.mask = stage_mask;
     for (cudaEvent_t e : g_timing.ev) cudaEventDestroy(e);
     g_timing.ev.assign(static_cast<size_t>(max_calls) * ST_COUNT * 2, nullptr);
     g_timing.used.assign(static_cast<size_t>(max_calls) * ST_COUNT, 0);

@@ -28,6 +28,15 @@ MOE_DEV uint64_t globaltimer_ns() {
 
 MOE_DEV uint32_t lane_id() { return threadIdx.x & 31u; }
 
+// Programmatic dependent launch: every kernel of the forward is launched with
+// programmatic stream serialisation, so it may start while its predecessor in
+// the stream is still running. pdl_wait() blocks until the predecessor grid
+// has completed and its memory is visible; it must precede any read of the
+// predecessor's outputs (and any write the predecessor might read).
+// pdl_trigger() lets the next kernel in the stream begin launching.
+MOE_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MOE_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------

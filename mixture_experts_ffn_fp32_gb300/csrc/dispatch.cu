@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(256) dispatch_count_kernel(const int32_t* __re
                                                              int TK, int E,
                                                              int32_t* __restrict__ chunk_counts,
                                                              int* err) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int hist[256];
     for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
     __syncthreads();
@@ -75,6 +77,8 @@ __global__ void __launch_bounds__(256) dispatch_scan_kernel(
     const int32_t* __restrict__ chunk_counts, int nchunks, int E, int TK, int bm,
     int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
     int32_t* __restrict__ mt_prefix) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int warp_tot[8];
     const int e = threadIdx.x;
     int running = 0;
@@ -106,6 +110,8 @@ __global__ void __launch_bounds__(DISPATCH_CHUNK) dispatch_scatter_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ w, int TK, int K, int E,
     const int32_t* __restrict__ chunk_base, int32_t* __restrict__ sorted_token,
     float* __restrict__ sorted_w, int32_t* __restrict__ inv) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int wcnt[32][256];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int i = threadIdx.x; i < 32 * 256; i += blockDim.x) (&wcnt[0][0])[i] = 0;
@@ -139,6 +145,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                           const int32_t* __restrict__ rowidx,
                                                           int rows, int vec_per_row,
                                                           uint4* __restrict__ dst) {
+    pdl_wait();
+    pdl_trigger();
     const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (r >= rows) return;
     const int lane = threadIdx.x & 31;
@@ -147,36 +155,45 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
     for (int v = lane; v < vec_per_row; v += 32) dst[d + v] = __ldg(src + s + v);
 }
 
-// out[t, c] = sum_k ys[inv[t, k], c], one warp per token, 8 columns per lane step.
-template <bool YS_BF16, bool OUT_BF16>
-__global__ void __launch_bounds__(256) gather_sum_kernel(const void* __restrict__ ys,
+// K5 - combine: out[t, c] = sum_k ys[inv[t, k], c] (+ addend[t, c]) in FP32, k in
+// ascending slot order, the addend last; one warp per token, 8 columns per
+// lane step. A fixed order and no atomics, so the result is deterministic
+// (APEX-1 Mathematical Reference Part 3 section 13.2: shared output plus the
+// gate-weighted routed outputs; kimi_k3 StableLatentMoE's index_add_ scatter
+// written as a gather through the inverse permutation).
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(256) gather_sum_kernel(const float* __restrict__ ys,
                                                          const int32_t* __restrict__ inv, int T,
-                                                         int K, int cols, void* __restrict__ out) {
+                                                         int K, int cols,
+                                                         const float* __restrict__ addend,
+                                                         void* __restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (t >= T) return;
     const int lane = threadIdx.x & 31;
+    int pos[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) pos[k] = (k < K) ? inv[static_cast<size_t>(t) * K + k] : 0;
+#pragma unroll 4
     for (int c0 = lane * 8; c0 < cols; c0 += 32 * 8) {
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int k = 0; k < K; ++k) {
-            const size_t row = static_cast<size_t>(inv[static_cast<size_t>(t) * K + k]);
-            if (YS_BF16) {
-                const uint4 v = *reinterpret_cast<const uint4*>(
-                    static_cast<const __nv_bfloat16*>(ys) + row * cols + c0);
-                const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    acc[2 * i] += bf16_lo(u[i]);
-                    acc[2 * i + 1] += bf16_hi(u[i]);
-                }
-            } else {
-                const float* p = static_cast<const float*>(ys) + row * cols + c0;
-                const float4 a = *reinterpret_cast<const float4*>(p);
-                const float4 b = *reinterpret_cast<const float4*>(p + 4);
-                acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-                acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
-            }
+        for (int k = 0; k < 16; ++k) {
+            if (k >= K) break;
+            const float* p = ys + static_cast<size_t>(pos[k]) * cols + c0;
+            const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+            const float4 b = __ldg(reinterpret_cast<const float4*>(p + 4));
+            acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+            acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
         }
         const size_t o = static_cast<size_t>(t) * cols + c0;
+        if (addend != nullptr) {
+            const float4 a = __ldg(reinterpret_cast<const float4*>(addend + o));
+            const float4 b = __ldg(reinterpret_cast<const float4*>(addend + o + 4));
+            acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+            acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+        }
         if (OUT_BF16) {
             uint4 v;
             v.x = pack_bf16x2(acc[0], acc[1]);
@@ -192,43 +209,82 @@ __global__ void __launch_bounds__(256) gather_sum_kernel(const void* __restrict_
     }
 }
 
+// gather_sum stored as a BF16 hi/lo pair (see launch_gather_sum_split).
+__global__ void __launch_bounds__(256) gather_sum_split_kernel(const float* __restrict__ ys,
+                                                               const int32_t* __restrict__ inv,
+                                                               int T, int K, int cols, int cols_pad,
+                                                               __nv_bfloat16* __restrict__ out2) {
+    pdl_wait();
+    pdl_trigger();
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (t >= T) return;
+    const int lane = threadIdx.x & 31;
+    __nv_bfloat16* hi = out2 + static_cast<size_t>(t) * 2 * cols_pad;
+    __nv_bfloat16* lo = hi + cols_pad;
+    for (int c0 = lane * 8; c0 < cols; c0 += 32 * 8) {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int k = 0; k < K; ++k) {
+            const float* p = ys + static_cast<size_t>(inv[static_cast<size_t>(t) * K + k]) * cols + c0;
+            const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+            const float4 b = __ldg(reinterpret_cast<const float4*>(p + 4));
+            acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+            acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+        }
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            h[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+            l[i] = pack_bf16x2(acc[2 * i] - bf16_lo(h[i]), acc[2 * i + 1] - bf16_hi(h[i]));
+        }
+        *reinterpret_cast<uint4*>(hi + c0) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(lo + c0) = make_uint4(l[0], l[1], l[2], l[3]);
+    }
+    const __nv_bfloat16 z = __float2bfloat16_rn(0.0f);
+    for (int c = cols + lane; c < cols_pad; c += 32) {
+        hi[c] = z;
+        lo[c] = z;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_gather_sum_split(const float* ys, const int32_t* inv, int T, int K, int cols,
+                                    int cols_pad, void* out2, cudaStream_t s) {
+    const int blocks = (T * 32 + 255) / 256;
+    return launch_pdl(gather_sum_split_kernel, dim3(blocks), dim3(256), 0, s, ys, inv, T, K, cols,
+                      cols_pad, static_cast<__nv_bfloat16*>(out2));
+}
 
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s, int* n_launched) {
     const int TK = a.T * a.K;
-    dispatch_count_kernel<<<a.nchunks, 256, 0, s>>>(a.idx, TK, a.E, a.chunk_counts, a.err);
-    dispatch_scan_kernel<<<1, 256, 0, s>>>(a.chunk_counts, a.nchunks, a.E, TK, a.bm, a.chunk_base,
-                                           a.counts, a.offsets, a.mt_prefix);
-    dispatch_scatter_kernel<<<a.nchunks, DISPATCH_CHUNK, 0, s>>>(
-        a.idx, a.w, TK, a.K, a.E, a.chunk_base, a.sorted_token, a.sorted_w, a.inv);
-    note_launch(3);
+    cudaError_t e = launch_pdl(dispatch_count_kernel, dim3(a.nchunks), dim3(256), 0, s, a.idx, TK,
+                               a.E, a.chunk_counts, a.err);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(256), 0, s, a.chunk_counts, a.nchunks, a.E,
+                   TK, a.bm, a.chunk_base, a.counts, a.offsets, a.mt_prefix);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(dispatch_scatter_kernel, dim3(a.nchunks), dim3(DISPATCH_CHUNK), 0, s, a.idx, a.w,
+                   TK, a.K, a.E, a.chunk_base, a.sorted_token, a.sorted_w, a.inv);
     if (n_launched) *n_launched = 3;
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_gather_rows(const void* src, const int32_t* rowidx, int rows, int row_bytes,
                                void* dst, cudaStream_t s) {
     const int vpr = row_bytes / 16;
     const int blocks = (rows * 32 + 255) / 256;
-    gather_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(src), rowidx, rows, vpr,
-                                              static_cast<uint4*>(dst));
-    note_launch();
-    return cudaGetLastError();
+    return launch_pdl(gather_rows_kernel, dim3(blocks), dim3(256), 0, s,
+                      static_cast<const uint4*>(src), rowidx, rows, vpr, static_cast<uint4*>(dst));
 }
 
-cudaError_t launch_gather_sum(const void* ys, int ys_bf16, const int32_t* inv, int T, int K,
-                              int cols, void* out, int out_bf16, cudaStream_t s) {
+cudaError_t launch_gather_sum(const float* ys, const int32_t* inv, int T, int K, int cols,
+                              const float* addend, void* out, int out_bf16, cudaStream_t s) {
     const int blocks = (T * 32 + 255) / 256;
-    if (ys_bf16 && out_bf16)
-        gather_sum_kernel<true, true><<<blocks, 256, 0, s>>>(ys, inv, T, K, cols, out);
-    else if (ys_bf16)
-        gather_sum_kernel<true, false><<<blocks, 256, 0, s>>>(ys, inv, T, K, cols, out);
-    else if (out_bf16)
-        gather_sum_kernel<false, true><<<blocks, 256, 0, s>>>(ys, inv, T, K, cols, out);
-    else
-        gather_sum_kernel<false, false><<<blocks, 256, 0, s>>>(ys, inv, T, K, cols, out);
-    note_launch();
-    return cudaGetLastError();
+    if (out_bf16)
+        return launch_pdl(gather_sum_kernel<true>, dim3(blocks), dim3(256), 0, s, ys, inv, T, K,
+                          cols, addend, out);
+    return launch_pdl(gather_sum_kernel<false>, dim3(blocks), dim3(256), 0, s, ys, inv, T, K, cols,
+                      addend, out);
 }
 
 }  // namespace moe

@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(256) simt_grouped_gemm_kernel(SimtParams p) {
     constexpr int NB = SWIGLU ? 2 : 1;
     __shared__ float As[BK][BM + 4];
     __shared__ float Bs[NB][BK][BN + 4];
+    pdl_wait();
+    pdl_trigger();
 
     const int total0 = p.g[0].enabled ? p.mt_prefix[p.E] * p.nt0 : 0;
     const int total = total0 + (p.g[1].enabled ? p.mt1 * p.g[1].Z * p.nt1 : 0);
@@ -177,9 +179,8 @@ cudaError_t launch_simt_t(const SimtGemmArgs& a, cudaStream_t s) {
     if (a.g[0].enabled) bound += static_cast<long long>((a.g[0].rows + BM - 1) / BM + a.E) * p.nt0;
     if (a.g[1].enabled) bound += static_cast<long long>(p.mt1) * a.g[1].Z * p.nt1;
     if (bound < 1) bound = 1;
-    simt_grouped_gemm_kernel<SWIGLU><<<static_cast<unsigned>(bound), 256, 0, s>>>(p);
-    note_launch();
-    return cudaGetLastError();
+    return launch_pdl(simt_grouped_gemm_kernel<SWIGLU>, dim3(static_cast<unsigned>(bound)), dim3(256),
+                      0, s, p);
 }
 
 }  // namespace

@@ -6,20 +6,21 @@
 // the dispatch grouped for it, as in kimi_k3 StableLatentMoE "The actual
 // grouped GEMM, and the gradient path"):
 //   SwiGLU kernel : h[r, :]  = SiLU(A[r, :] W_gate[z]) * (A[r, :] W_up[z])
-//   plain kernel  : y[r, :]  = rowscale[r] * (A[r, :] B[z])            (routed down x gate)
-//                   out[t, :] = A[t, :] B + sum_k ys[inv[t, k], :] (+ addend[t, :])
-//                                                                (shared down + combine)
-// Two segment groups share one persistent launch: group 0 = the E routed
-// experts over the expert-sorted rows (segment bounds read from device
-// memory, never from the host), group 1 = S dense segments over all token
-// rows (the shared experts, or a single dense projection).
+//   plain kernel  : y[r, :]  = rowscale[r] * (A[r, :] B[z])   (routed down x gate weight)
+//                   y[t, :]  = A[t, :] B (+ addend[t, :])       (shared down, projections)
+// Two segment groups share one persistent launch, each with its own
+// reduction length: group 0 = the E routed experts over the expert-sorted
+// rows (segment bounds read from device memory, never from the host),
+// group 1 = S dense segments over all token rows (the shared experts, or a
+// single dense projection).
 //
 // Tile: 128 rows x 256 accumulator columns (SwiGLU: 128 gate + 128 up
 // columns of the same output tile), K step 64 (one 128-byte swizzle row),
 // 4-stage TMA ring of 48 KB stages, two 256-column TMEM accumulators so the
 // epilogue of one tile overlaps the main loop of the next. Warp 0 issues TMA,
 // warp 1 issues tcgen05.mma (M=128, N=256, K=16, BF16 in, FP32 accumulate),
-// warps 2-5 drain TMEM, apply the epilogue and store. The weights stay in the
+// warps 2-9 drain TMEM (two warps per 32-lane quarter, each taking half of
+// the columns), apply the epilogue and store. The weights stay in the
 // caller's [Z, K, N] layout (N contiguous) and are read as an MN-major
 // operand. Every wait is bounded (see common.cuh): on timeout the CTA stops,
 // drains its copies and MMAs, frees TMEM and flags the error word.
@@ -38,9 +39,9 @@ constexpr int B_BYTES = 4 * STRIP_BYTES;    // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 512;
-constexpr int THREADS = 192;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int MAXE = 256;
-constexpr uint32_t IDESC = idesc_bf16_f32(128, 256, /*b_mn_major=*/1);
 
 constexpr int BAR_OFF = STAGES * STAGE_BYTES;
 constexpr int NBARS = 2 * STAGES + 4 + 1;
@@ -60,13 +61,16 @@ struct TcParams {
     void* out[2];
     int out_ld[2];
     int out_f32[2];
-    int kblocks, E, mt1;
+    int kblocks[2];
+    int a_kmod[2], b_kmod[2], a_kgroup[2], a_krep[2];
+    int nstrip;          // plain kernel: 64-column B strips per tile (MMA N = 64 * nstrip)
+    int bno;             // output columns per tile
+    uint32_t idesc;      // instruction descriptor (M = 128, N = 64 * nstrip)
+    int ksplit1, kbs1;   // group 1 split-K: slices and k-blocks per slice
+    int E, mt1;
     const int32_t* offsets;
     const int32_t* mt_prefix;
     const float* rowscale0;
-    const int32_t* inv;
-    const __nv_bfloat16* ys;
-    int ys_ld, Kr;
     const float* addend;
     int add_ld;
     int* err;
@@ -74,12 +78,12 @@ struct TcParams {
 };
 
 struct Unit {
-    int g, row0, rows, zb, n0, out_col0;
+    int g, row0, rows, zb, n0, out_row0, out_col0, kb0, kb1;
 };
 
 template <bool SWIGLU>
 MOE_DEV Unit decode_unit(int u, const TcParams& p, int total0, const int* s_mtp, const int* s_off) {
-    constexpr int BNO = SWIGLU ? 128 : 256;
+    const int BNO = p.bno;
     Unit t;
     if (u < total0) {
         const int nt = p.nt[0];
@@ -99,11 +103,15 @@ MOE_DEV Unit decode_unit(int u, const TcParams& p, int total0, const int* s_mtp,
         t.rows = min(BM, s_off[lo + 1] - t.row0);
         t.zb = lo;
         t.n0 = n * BNO;
+        t.out_row0 = t.row0;
         t.out_col0 = t.n0;
+        t.kb0 = 0;
+        t.kb1 = p.kblocks[0];
     } else {
         const int u1 = u - total0;
         const int nt = p.nt[1];
-        const int per_m = p.Z[1] * nt;
+        const int nseg = p.ksplit1 > 1 ? p.ksplit1 : p.Z[1];
+        const int per_m = nseg * nt;
         const int m = u1 / per_m;
         const int rem = u1 - m * per_m;
         const int s = rem / nt;
@@ -111,9 +119,20 @@ MOE_DEV Unit decode_unit(int u, const TcParams& p, int total0, const int* s_mtp,
         t.g = 1;
         t.row0 = m * BM;
         t.rows = min(BM, p.rows[1] - t.row0);
-        t.zb = s;
         t.n0 = n * BNO;
-        t.out_col0 = s * p.N[1] + t.n0;
+        if (p.ksplit1 > 1) {
+            t.zb = 0;
+            t.kb0 = s * p.kbs1;
+            t.kb1 = min(t.kb0 + p.kbs1, p.kblocks[1]);
+            t.out_row0 = s * p.rows[1] + t.row0;
+            t.out_col0 = t.n0;
+        } else {
+            t.zb = s;
+            t.kb0 = 0;
+            t.kb1 = p.kblocks[1];
+            t.out_row0 = t.row0;
+            t.out_col0 = s * p.N[1] + t.n0;
+        }
     }
     return t;
 }
@@ -176,7 +195,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 4);
+            mbar_init(tempty_bar(a), EPI_WARPS);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -194,6 +213,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
         tmem_relinquish();
     }
+    // everything above overlaps the previous kernel; its outputs are read below
+    pdl_wait();
+    pdl_trigger();
     if (p.enabled[0]) {
         for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
             s_mtp[i] = p.mt_prefix[i];
@@ -205,7 +227,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int total0 = p.enabled[0] ? s_mtp[p.E] * p.nt[0] : 0;
-    const int total = total0 + (p.enabled[1] ? p.mt1 * p.Z[1] * p.nt[1] : 0);
+    const int total =
+        total0 + (p.enabled[1] ? p.mt1 * (p.ksplit1 > 1 ? p.ksplit1 : p.Z[1]) * p.nt[1] : 0);
     const WaitCtx wc{p.err, abort_flag, p.timeout_ns};
 
     if (warp == 0) {
@@ -219,7 +242,11 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
                 const CUtensorMap* mA = &p.mapA[t.g];
                 const CUtensorMap* mB0 = &p.mapB0[t.g];
                 const CUtensorMap* mB1 = &p.mapB1[t.g];
-                for (int kb = 0; kb < p.kblocks; ++kb) {
+                const int akm = p.a_kmod[t.g], bkm = p.b_kmod[t.g];
+                const int akg = p.a_kgroup[t.g], akr = p.a_krep[t.g];
+                const int nstrip = SWIGLU ? 4 : p.nstrip;
+                const uint32_t stage_bytes = A_BYTES + nstrip * STRIP_BYTES;
+                for (int kb = t.kb0; kb < t.kb1; ++kb) {
                     if (!bounded_wait(empty_bar(stage), phase ^ 1u, wc)) {
                         ok = false;
                         break;
@@ -228,17 +255,19 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
                     const uint32_t sB = sA + A_BYTES;
                     const uint32_t fb = full_bar(stage);
                     const int kc = kb * BK;
-                    mbar_expect_tx(fb, STAGE_BYTES);
-                    tma_load_2d(sA, mA, kc, t.row0, fb);
+                    int kca = akm ? kc % akm : kc;
+                    if (akg) kca = ((kb / (akg * akr)) * akg + kb % akg) * BK;
+                    const int kcb = bkm ? kc % bkm : kc;
+                    mbar_expect_tx(fb, stage_bytes);
+                    tma_load_2d(sA, mA, kca, t.row0, fb);
                     if (SWIGLU) {
-                        tma_load_3d(sB, mB0, t.n0, kc, t.zb, fb);
-                        tma_load_3d(sB + STRIP_BYTES, mB0, t.n0 + 64, kc, t.zb, fb);
-                        tma_load_3d(sB + 2 * STRIP_BYTES, mB1, t.n0, kc, t.zb, fb);
-                        tma_load_3d(sB + 3 * STRIP_BYTES, mB1, t.n0 + 64, kc, t.zb, fb);
+                        tma_load_3d(sB, mB0, t.n0, kcb, t.zb, fb);
+                        tma_load_3d(sB + STRIP_BYTES, mB0, t.n0 + 64, kcb, t.zb, fb);
+                        tma_load_3d(sB + 2 * STRIP_BYTES, mB1, t.n0, kcb, t.zb, fb);
+                        tma_load_3d(sB + 3 * STRIP_BYTES, mB1, t.n0 + 64, kcb, t.zb, fb);
                     } else {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            tma_load_3d(sB + j * STRIP_BYTES, mB0, t.n0 + 64 * j, kc, t.zb, fb);
+                        for (int j = 0; j < nstrip; ++j)
+                            tma_load_3d(sB + j * STRIP_BYTES, mB0, t.n0 + 64 * j, kcb, t.zb, fb);
                     }
                     issued |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
@@ -260,10 +289,11 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+                const Unit t = decode_unit<SWIGLU>(u, p, total0, s_mtp, s_off);
                 if (!bounded_wait(tempty_bar(acc), acc_phase ^ 1u, wc)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
-                for (int kb = 0; kb < p.kblocks; ++kb) {
+                for (int kb = t.kb0; kb < t.kb1; ++kb) {
                     if (!bounded_wait(full_bar(stage), phase, wc)) {
                         ok = false;
                         break;
@@ -275,7 +305,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
                     for (int ks = 0; ks < BK / 16; ++ks) {
                         const uint64_t ad = smem_desc_sw128(sA + ks * 32, 16, 1024);
                         const uint64_t bd = smem_desc_sw128(sB + ks * 2048, STRIP_BYTES, 1024);
-                        tc_mma_bf16(d_tmem, ad, bd, IDESC, (kb | ks) != 0 ? 1u : 0u);
+                        tc_mma_bf16(d_tmem, ad, bd, p.idesc, (kb != t.kb0 || ks != 0) ? 1u : 0u);
                     }
                     tc_commit(empty_bar(stage));
                     if (++stage == STAGES) {
@@ -292,8 +322,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
             bounded_drain(drain_bar, 0, p.timeout_ns, p.err);
         }
     } else {
-        // ---------------- epilogue warps 2..5 ----------------
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        // ---------------- epilogue warps 2..9 ----------------
+        const int q = warp & 3;          // TMEM lane quarter this warp may access
+        const int half = (warp - 2) >> 2;  // which half of the tile's columns
         const int r = q * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -307,14 +338,14 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
             const uint32_t tb =
                 tmem_base + static_cast<uint32_t>(acc * ACC_COLS) + (static_cast<uint32_t>(q * 32) << 16);
             const bool rv = r < t.rows;
-            const size_t orow = static_cast<size_t>(t.row0 + r);
+            const size_t orow = static_cast<size_t>(t.out_row0 + r);
             const int N = p.N[t.g];
             void* out = p.out[t.g];
             const int ld = p.out_ld[t.g];
             const int of32 = p.out_f32[t.g];
             if (SWIGLU) {
 #pragma unroll 1
-                for (int c = 0; c < 128; c += 16) {
+                for (int c = half * 64; c < half * 64 + 64; c += 16) {
                     uint32_t gr[16], ur[16];
                     tc_ld_32x32b_x16(tb + c, gr);
                     tc_ld_32x32b_x16(tb + 128 + c, ur);
@@ -323,22 +354,20 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
                     if (rv && lim > 0) {
                         float h[16];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            h[i] = silu_f(__uint_as_float(gr[i])) * __uint_as_float(ur[i]);
+                        for (int i = 0; i < 16; ++i) {
+                            const float g = __uint_as_float(gr[i]);
+                            h[i] = __fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(ur[i]);
+                        }
                         store16(out, of32, orow, ld, t.out_col0 + c, h, lim);
                     }
                 }
             } else {
                 float rs = 1.0f;
                 if (t.g == 0 && p.rowscale0 != nullptr && rv) rs = p.rowscale0[orow];
-                const bool comb = (t.g == 1 && p.inv != nullptr);
                 const bool add = (t.g == 1 && p.addend != nullptr);
-                int pos[16];
-#pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    pos[k] = (comb && rv && k < p.Kr) ? p.inv[orow * p.Kr + k] : 0;
+                const int span = 32 * p.nstrip;  // this warp's columns: [half * span, +span)
 #pragma unroll 1
-                for (int c = 0; c < 256; c += 16) {
+                for (int c = half * span; c < half * span + span; c += 16) {
                     uint32_t vr[16];
                     tc_ld_32x32b_x16(tb + c, vr);
                     tc_wait_ld();
@@ -348,26 +377,20 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
 #pragma unroll
                         for (int i = 0; i < 16; ++i) v[i] = rs * __uint_as_float(vr[i]);
                         const int col = t.out_col0 + c;
-                        if (comb) {
-                            for (int k = 0; k < p.Kr; ++k) {
-                                const __nv_bfloat16* yp = p.ys + static_cast<size_t>(pos[k]) * p.ys_ld + col;
-                                if (lim >= 16) {
-                                    const uint4 a = *reinterpret_cast<const uint4*>(yp);
-                                    const uint4 b = *reinterpret_cast<const uint4*>(yp + 8);
-                                    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-                                    for (int i = 0; i < 8; ++i) {
-                                        v[2 * i] += bf16_lo(w[i]);
-                                        v[2 * i + 1] += bf16_hi(w[i]);
-                                    }
-                                } else {
-                                    for (int i = 0; i < lim; ++i) v[i] += __bfloat162float(yp[i]);
-                                }
-                            }
-                        }
                         if (add) {
                             const float* ap = p.addend + orow * static_cast<size_t>(p.add_ld) + col;
-                            for (int i = 0; i < 16 && i < lim; ++i) v[i] += ap[i];
+                            if (lim >= 16) {
+#pragma unroll
+                                for (int i = 0; i < 16; i += 4) {
+                                    const float4 a4 = *reinterpret_cast<const float4*>(ap + i);
+                                    v[i] += a4.x;
+                                    v[i + 1] += a4.y;
+                                    v[i + 2] += a4.z;
+                                    v[i + 3] += a4.w;
+                                }
+                            } else {
+                                for (int i = 0; i < lim; ++i) v[i] += ap[i];
+                            }
                         }
                         store16(out, of32, orow, ld, col, v, lim);
                     }
@@ -390,6 +413,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
 }
 
 bool make_A_map(CUtensorMap* m, const void* A, int rows, int K, int lda) {
+    // K: the columns of A the reduction reads
     const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rows)};
     const uint64_t strides[1] = {static_cast<uint64_t>(lda) * 2};
     const uint32_t box[2] = {64, BM};
@@ -415,17 +439,37 @@ cudaError_t launch_tc_t(const TcGemmArgs& a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    constexpr int BNO = SWIGLU ? 128 : 256;
     TcParams p;
     memset(&p, 0, sizeof(p));
+    int nmax = 0;
+    for (int g = 0; g < 2; ++g)
+        if (a.g[g].enabled && a.g[g].N > nmax) nmax = a.g[g].N;
+    p.nstrip = SWIGLU ? 4 : (nmax >= 256 ? 4 : (nmax + 63) / 64);
+    p.bno = SWIGLU ? 128 : 64 * p.nstrip;
+    p.idesc = idesc_bf16_f32(128, 64 * p.nstrip, /*b_mn_major=*/1);
+    const int BNO = p.bno;
     long long units_bound = 0;
     for (int g = 0; g < 2; ++g) {
         const TcGroup& G = a.g[g];
         p.enabled[g] = G.enabled;
         if (!G.enabled) continue;
-        if (!make_A_map(&p.mapA[g], G.A, G.rows, a.K, G.lda)) return cudaErrorInvalidValue;
-        if (!make_B_map(&p.mapB0[g], G.B0, G.Z, a.K, G.N)) return cudaErrorInvalidValue;
-        if (SWIGLU && !make_B_map(&p.mapB1[g], G.B1, G.Z, a.K, G.N)) return cudaErrorInvalidValue;
+        const int KA = G.a_kmod ? G.a_kmod : (G.a_kgroup ? G.K / (G.a_krep > 0 ? G.a_krep : 1) : G.K);
+        const int KB = G.b_rows ? G.b_rows : (G.b_kmod ? G.b_kmod : G.K);
+        if ((G.a_kmod && G.a_kmod % BK) || (G.b_kmod && G.b_kmod % BK)) return cudaErrorInvalidValue;
+        if (G.ksplit > 1 && (g != 1 || G.Z != 1)) return cudaErrorInvalidValue;
+        if (!make_A_map(&p.mapA[g], G.A, G.rows, KA, G.lda)) return cudaErrorInvalidValue;
+        if (!make_B_map(&p.mapB0[g], G.B0, G.Z, KB, G.N)) return cudaErrorInvalidValue;
+        if (SWIGLU && !make_B_map(&p.mapB1[g], G.B1, G.Z, KB, G.N)) return cudaErrorInvalidValue;
+        p.kblocks[g] = (G.K + BK - 1) / BK;
+        p.a_kmod[g] = G.a_kmod;
+        p.b_kmod[g] = G.b_kmod;
+        p.a_kgroup[g] = G.a_kgroup;
+        p.a_krep[g] = G.a_krep > 0 ? G.a_krep : 1;
+        if (g == 1) {
+            const int ks = G.ksplit > 1 ? G.ksplit : 1;
+            p.kbs1 = (p.kblocks[1] + ks - 1) / ks;
+            p.ksplit1 = ks > 1 ? (p.kblocks[1] + p.kbs1 - 1) / p.kbs1 : 1;
+        }
         p.rows[g] = G.rows;
         p.N[g] = G.N;
         p.nt[g] = (G.N + BNO - 1) / BNO;
@@ -436,18 +480,14 @@ cudaError_t launch_tc_t(const TcGemmArgs& a, cudaStream_t s) {
         if (g == 0)
             units_bound += static_cast<long long>((G.rows + BM - 1) / BM + a.E) * p.nt[0];
         else
-            units_bound += static_cast<long long>((G.rows + BM - 1) / BM) * G.Z * p.nt[1];
+            units_bound += static_cast<long long>((G.rows + BM - 1) / BM) *
+                           (p.ksplit1 > 1 ? p.ksplit1 : G.Z) * p.nt[1];
     }
-    p.kblocks = (a.K + BK - 1) / BK;
     p.E = a.E;
     p.mt1 = a.g[1].enabled ? (a.g[1].rows + BM - 1) / BM : 0;
     p.offsets = a.offsets;
     p.mt_prefix = a.mt_prefix;
     p.rowscale0 = a.rowscale0;
-    p.inv = a.inv;
-    p.ys = static_cast<const __nv_bfloat16*>(a.ys);
-    p.ys_ld = a.ys_ld;
-    p.Kr = a.Kr;
     p.addend = a.addend;
     p.add_ld = a.add_ld;
     p.err = a.err;
@@ -455,9 +495,8 @@ cudaError_t launch_tc_t(const TcGemmArgs& a, cudaStream_t s) {
     long long grid = num_sms();
     if (units_bound < grid) grid = units_bound;
     if (grid < 1) grid = 1;
-    tc_grouped_gemm_kernel<SWIGLU><<<static_cast<int>(grid), THREADS, SMEM_BYTES, s>>>(p);
-    note_launch();
-    return cudaGetLastError();
+    return launch_pdl(tc_grouped_gemm_kernel<SWIGLU>, dim3(static_cast<unsigned>(grid)),
+                      dim3(THREADS), SMEM_BYTES, s, p);
 }
 
 }  // namespace

@@ -7,12 +7,32 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/moe.h"
 
 namespace moe {
 
 // Count of kernels launched by the library (moe_launch_count).
 void note_launch(int n = 1);
+
+// Launch with programmatic stream serialisation (see pdl_wait in common.cuh).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    note_launch();
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 // Wait limit of device-side bounded waits, in ns.
 uint64_t wait_timeout_ns();
 // Number of SMs of the current device (cached per device).
@@ -24,12 +44,13 @@ int num_sms();
 constexpr int DISPATCH_CHUNK = 1024;   // assignments per dispatch CTA
 constexpr int TC_BM = 128;             // rows per tcgen05 GEMM tile
 constexpr int SIMT_BM = 64;            // rows per FP32 SIMT GEMM tile
+constexpr int ROUTER_CHUNK = 256;      // tensor-core router: reduction chunk per split-K slice
 
 struct WsLayout {
     size_t err, topk_idx, topk_w, margin, top_scores, scores;
     size_t chunk_counts, chunk_base, counts, offsets, mt_prefix;
     size_t sorted_token, sorted_w, inv;
-    size_t xs, z, h, hs, ys, routed, shout, xstage, ostage, qb;
+    size_t xs, z, h, hs, ys, routed, shout, xstage, ostage, qb, w3, rpart;
     size_t total;
     int nchunks;
 };
@@ -52,8 +73,19 @@ struct RouterArgs {
     float* margin;
     float* top_scores;
     float* scores;
+    int* err_clear;   // if set, block 0 zeroes this error word (first kernel of a forward)
 };
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
+// Tensor-core router pieces: W3 [3, d, E] BF16 = exact split of W [d, E];
+// routing from logits summed over nsplit partial slices part [nsplit, T, E].
+cudaError_t launch_router_split(const float* W, int d, int E, void* W3, int* err_clear,
+                                cudaStream_t s);
+cudaError_t launch_route_from_logits(const float* part, int nsplit, const RouterArgs& a,
+                                     cudaStream_t s);
+// Tensor-core router used when x is BF16, E > 32, E % 8 == 0 and d % ROUTER_CHUNK == 0.
+bool router_on_tensor_cores(const moe_config& c);
+// Split-K slices of the tensor-core router GEMM (one per chunk of d).
+int router_ksplit(int T, int d);
 
 struct DispatchArgs {
     const int32_t* idx;
@@ -75,9 +107,15 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s, int* n_launch
 cudaError_t launch_gather_rows(const void* src, const int32_t* rowidx, int rows, int row_bytes,
                                void* dst, cudaStream_t s);
 
-// out[t, :] = sum_k ys[inv[t, k], :] (+ addend[t, :]) in FP32, stored BF16 or FP32.
-cudaError_t launch_gather_sum(const void* ys, int ys_bf16, const int32_t* inv, int T, int K,
-                              int cols, void* out, int out_bf16, cudaStream_t s);
+// out[t, :] = sum_k ys[inv[t, k], :] (+ addend[t, :]) in FP32 (k ascending, addend
+// last), stored BF16 or FP32. ys and addend are FP32; addend may be NULL.
+cudaError_t launch_gather_sum(const float* ys, const int32_t* inv, int T, int K, int cols,
+                              const float* addend, void* out, int out_bf16, cudaStream_t s);
+// Same sum, stored as two BF16 parts hi = bf16(v), lo = bf16(v - hi) in
+// out2 [T, 2*cols_pad]: hi in columns [0, cols), lo in [cols_pad, cols_pad + cols),
+// zeros elsewhere (hi + lo carries ~16 significant bits of v).
+cudaError_t launch_gather_sum_split(const float* ys, const int32_t* inv, int T, int K, int cols,
+                                    int cols_pad, void* out2, cudaStream_t s);
 
 // ---- tcgen05 grouped GEMM -------------------------------------------------
 // A segment group: rows of A multiplied by a per-segment B matrix.
@@ -87,7 +125,8 @@ cudaError_t launch_gather_sum(const void* ys, int ys_bf16, const int32_t* inv, i
 //     output columns [s*N1, (s+1)*N1).
 struct TcGroup {
     int enabled;
-    const void* A;      // [rows, K] BF16, row pitch lda elements
+    int K;              // reduction length of this group
+    const void* A;      // [rows, K] BF16, row pitch lda elements (see a_kmod)
     int lda;
     int rows;           // group 0: T*K (rows of A), group 1: rows1
     const void* B0;     // [Z, K, N] BF16 (gate / down / plain)
@@ -97,19 +136,22 @@ struct TcGroup {
     void* out;          // [rows, out_ld] BF16 or FP32
     int out_ld;
     int out_f32;
+    int a_kmod = 0;     // > 0: A is [rows, a_kmod] and reduction index k reads A column k % a_kmod
+    int a_kgroup = 0;   // > 0 (k-blocks of 64): reduction k-block kb reads A k-block
+    int a_krep = 1;     //   (kb / (a_kgroup * a_krep)) * a_kgroup + kb % a_kgroup
+    int b_kmod = 0;     // > 0: reduction index k reads B row k % b_kmod
+    int b_rows = 0;     // > 0: B has b_rows rows per matrix (rows beyond read as zero)
+    int ksplit = 1;     // group 1 only: split K into ksplit slices; slice s writes the partial
+                        // product to out rows [s*rows, (s+1)*rows) (needs Z == 1)
 };
 
 struct TcGemmArgs {
     TcGroup g[2];
-    int K;                       // reduction length
     int E;                       // group 0 segment count
     const int32_t* offsets;      // group 0 [E+1]
     const int32_t* mt_prefix;    // group 0 [E+1], m-tiles of TC_BM rows
     int swiglu;                  // 1: h = SiLU(A B0) * (A B1); 0: single product
     const float* rowscale0;      // group 0: multiply row r by rowscale0[r]
-    const int32_t* inv;          // group 1: add sum_k ys[inv[r*Kr + k]]
-    const void* ys;              // BF16 [*, ys_ld]
-    int ys_ld, Kr;
     const float* addend;         // group 1: add addend[r, col] (FP32 [rows1, add_ld])
     int add_ld;
     int* err;

@@ -150,43 +150,69 @@ MOE_DEV void route_token_warp(const float (&r)[J], int t, const RouterArgs& a) {
     if (a.margin != nullptr && lane == 0) a.margin[t] = (K < E) ? (vK1 - vK) : INFINITY;
 }
 
-// E <= 32: one warp per token; lanes split d, then a butterfly leaves every
-// expert's full sum on every lane.
+// E <= 32: one warp per token. Lane l takes the d-index pair k0 + 2l, k0 + 2l + 1,
+// so a warp's x loads and its W_router row loads are both contiguous; a
+// butterfly then leaves every expert's full sum on every lane.
 template <int EP, bool BF16>
 __global__ void __launch_bounds__(256) router_small_kernel(RouterArgs a) {
+    pdl_wait();
+    pdl_trigger();
+    if (a.err_clear != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *a.err_clear = 0;
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (t >= a.T) return;
     const int lane = static_cast<int>(lane_id());
     const int E = a.E, d = a.d;
+    const bool vec = (E == EP) && (EP % 4 == 0);
+    // U d-index pairs per lane per step, all loads issued before the FMAs
+    constexpr int U = EP <= 8 ? 4 : (EP <= 16 ? 2 : 1);
     float acc[EP];
 #pragma unroll
     for (int e = 0; e < EP; ++e) acc[e] = 0.0f;
-    // chunks of 8 consecutive x elements
-    for (int k0 = lane * 8; k0 < d; k0 += 32 * 8) {
-        float xv[8];
-        if (BF16) {
-            const uint4 v = *reinterpret_cast<const uint4*>(
-                static_cast<const __nv_bfloat16*>(a.x) + static_cast<size_t>(t) * d + k0);
-            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    for (int k0 = 2 * lane; k0 < d; k0 += 64 * U) {
+        float x0[U], x1[U];
+        float w0[U][EP], w1[U][EP];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                xv[2 * i] = bf16_lo(u[i]);
-                xv[2 * i + 1] = bf16_hi(u[i]);
+        for (int u = 0; u < U; ++u) {
+            const int k = k0 + 64 * u;
+            x0[u] = x1[u] = 0.0f;
+#pragma unroll
+            for (int e = 0; e < EP; ++e) w0[u][e] = w1[u][e] = 0.0f;
+            if (k < d) {
+                if (BF16) {
+                    const uint32_t v = *reinterpret_cast<const uint32_t*>(
+                        static_cast<const __nv_bfloat16*>(a.x) + static_cast<size_t>(t) * d + k);
+                    x0[u] = bf16_lo(v);
+                    x1[u] = bf16_hi(v);
+                } else {
+                    const float2 v = *reinterpret_cast<const float2*>(
+                        static_cast<const float*>(a.x) + static_cast<size_t>(t) * d + k);
+                    x0[u] = v.x;
+                    x1[u] = v.y;
+                }
+                const float* r0 = a.W + static_cast<size_t>(k) * E;
+                const float* r1 = r0 + E;
+                if (vec) {
+#pragma unroll
+                    for (int e = 0; e < EP; e += 4) {
+                        const float4 p = __ldg(reinterpret_cast<const float4*>(r0 + e));
+                        const float4 q = __ldg(reinterpret_cast<const float4*>(r1 + e));
+                        w0[u][e] = p.x; w0[u][e + 1] = p.y; w0[u][e + 2] = p.z; w0[u][e + 3] = p.w;
+                        w1[u][e] = q.x; w1[u][e + 1] = q.y; w1[u][e + 2] = q.z; w1[u][e + 3] = q.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < EP; ++e)
+                        if (e < E) {
+                            w0[u][e] = __ldg(r0 + e);
+                            w1[u][e] = __ldg(r1 + e);
+                        }
+                }
             }
-        } else {
-            const float* xp = static_cast<const float*>(a.x) + static_cast<size_t>(t) * d + k0;
-            const float4 p0 = *reinterpret_cast<const float4*>(xp);
-            const float4 p1 = *reinterpret_cast<const float4*>(xp + 4);
-            xv[0] = p0.x; xv[1] = p0.y; xv[2] = p0.z; xv[3] = p0.w;
-            xv[4] = p1.x; xv[5] = p1.y; xv[6] = p1.z; xv[7] = p1.w;
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float* wr = a.W + static_cast<size_t>(k0 + i) * E;
+        for (int u = 0; u < U; ++u)
 #pragma unroll
-            for (int e = 0; e < EP; ++e)
-                if (e < E) acc[e] = fmaf(xv[i], __ldg(wr + e), acc[e]);
-        }
+            for (int e = 0; e < EP; ++e) acc[e] = fmaf(x1[u], w1[u][e], fmaf(x0[u], w0[u][e], acc[e]));
     }
 #pragma unroll
     for (int e = 0; e < EP; ++e) acc[e] = warp_sum(acc[e]);
@@ -204,6 +230,8 @@ constexpr int RT_DK = 32;
 
 template <int J, bool BF16>
 __global__ void __launch_bounds__(256) router_tiled_kernel(RouterArgs a) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int EPAD = 32 * J;        // 64, 128 or 256
     constexpr int EI = EPAD / 64;       // experts per thread
     __shared__ float xs[RT_BT * RT_DK];
@@ -211,6 +239,7 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(RouterArgs a) {
     static_assert(RT_BT * EPAD <= RT_DK * EPAD, "logit tile must fit the W chunk buffer");
 
     const int tid = threadIdx.x;
+    if (a.err_clear != nullptr && blockIdx.x == 0 && tid == 0) *a.err_clear = 0;
     const int tg = tid >> 6;   // token group: tokens tg*8 .. tg*8+7
     const int el = tid & 63;   // experts el + 64 i
     const int t0 = blockIdx.x * RT_BT;
@@ -282,35 +311,114 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(RouterArgs a) {
     }
 }
 
+// Exact three-term BF16 split of the FP32 router weights for the tensor-core
+// router: W = hi + mid + lo with hi = bf16(W), mid = bf16(W - hi),
+// lo = bf16(W - hi - mid). Both subtractions are exact in FP32 and the last
+// remainder has at most 8 significant bits, so hi + mid + lo == W exactly.
+// x is BF16, so every product x * part is exact in FP32. The tensor core's
+// FP32 accumulation loses precision over long chains, so the reduction is cut
+// into chunks of ROUTER_CHUNK rows of W: rows are stored chunk by chunk, and
+// within a chunk as lo, mid, hi (small parts first). The GEMM accumulates one
+// chunk per split-K slice and the slices are summed in FP32 afterwards.
+__global__ void __launch_bounds__(256) router_split_kernel(const float* __restrict__ W, int d, int E,
+                                                           __nv_bfloat16* __restrict__ W3,
+                                                           int* err_clear) {
+    pdl_wait();
+    pdl_trigger();
+    if (err_clear != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *err_clear = 0;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= d * E) return;
+    const int k = i / E, e = i - k * E;
+    const int c = k / ROUTER_CHUNK, j = k - c * ROUTER_CHUNK;
+    const float w = W[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const float r1 = __fsub_rn(w, __bfloat162float(hi));
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = __fsub_rn(r1, __bfloat162float(mid));
+    const size_t base = (static_cast<size_t>(c) * 3 * ROUTER_CHUNK + j) * E + e;
+    const size_t part = static_cast<size_t>(ROUTER_CHUNK) * E;
+    W3[base] = __float2bfloat16_rn(r2);
+    W3[base + part] = mid;
+    W3[base + 2 * part] = hi;
+}
+
+// Routing from precomputed logits: r[t, e] = sum over the split-K slices of
+// part[s, t, e], summed in slice order; one warp per token.
+template <int J>
+__global__ void __launch_bounds__(256) route_from_logits_kernel(const float* __restrict__ part,
+                                                                int nsplit, RouterArgs a) {
+    pdl_wait();
+    pdl_trigger();
+    if (a.err_clear != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *a.err_clear = 0;
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (t >= a.T) return;
+    const int lane = static_cast<int>(lane_id());
+    const size_t slice = static_cast<size_t>(a.T) * a.E;
+    float r[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int e = lane + 32 * j;
+        float v = 0.0f;
+        if (e < a.E) {
+            const float* p = part + static_cast<size_t>(t) * a.E + e;
+            for (int s = 0; s < nsplit; ++s) v += p[s * slice];
+        }
+        r[j] = v;
+    }
+    route_token_warp<J>(r, t, a);
+}
+
 template <bool BF16>
 cudaError_t launch_router_t(const RouterArgs& a, cudaStream_t s) {
+    cudaError_t e = cudaSuccess;
     if (a.E <= 32) {
         const int blocks = (a.T * 32 + 255) / 256;
         if (a.E <= 4)
-            router_small_kernel<4, BF16><<<blocks, 256, 0, s>>>(a);
+            e = launch_pdl(router_small_kernel<4, BF16>, dim3(blocks), dim3(256), 0, s, a);
         else if (a.E <= 8)
-            router_small_kernel<8, BF16><<<blocks, 256, 0, s>>>(a);
+            e = launch_pdl(router_small_kernel<8, BF16>, dim3(blocks), dim3(256), 0, s, a);
         else if (a.E <= 16)
-            router_small_kernel<16, BF16><<<blocks, 256, 0, s>>>(a);
+            e = launch_pdl(router_small_kernel<16, BF16>, dim3(blocks), dim3(256), 0, s, a);
         else
-            router_small_kernel<32, BF16><<<blocks, 256, 0, s>>>(a);
+            e = launch_pdl(router_small_kernel<32, BF16>, dim3(blocks), dim3(256), 0, s, a);
     } else {
         const int blocks = (a.T + RT_BT - 1) / RT_BT;
         if (a.E <= 64)
-            router_tiled_kernel<2, BF16><<<blocks, 256, 0, s>>>(a);
+            e = launch_pdl(router_tiled_kernel<2, BF16>, dim3(blocks), dim3(256), 0, s, a);
         else if (a.E <= 128)
-            router_tiled_kernel<4, BF16><<<blocks, 256, 0, s>>>(a);
+            e = launch_pdl(router_tiled_kernel<4, BF16>, dim3(blocks), dim3(256), 0, s, a);
         else
-            router_tiled_kernel<8, BF16><<<blocks, 256, 0, s>>>(a);
+            e = launch_pdl(router_tiled_kernel<8, BF16>, dim3(blocks), dim3(256), 0, s, a);
     }
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace
 
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s) {
-    note_launch();
     return a.x_bf16 ? launch_router_t<true>(a, s) : launch_router_t<false>(a, s);
+}
+
+cudaError_t launch_router_split(const float* W, int d, int E, void* W3, int* err_clear,
+                                cudaStream_t s) {
+    const int n = d * E;
+    return launch_pdl(router_split_kernel, dim3((n + 255) / 256), dim3(256), 0, s, W, d, E,
+                      static_cast<__nv_bfloat16*>(W3), err_clear);
+}
+
+cudaError_t launch_route_from_logits(const float* part, int nsplit, const RouterArgs& a,
+                                     cudaStream_t s) {
+    const int blocks = (a.T * 32 + 255) / 256;
+    cudaError_t e;
+    if (a.E <= 32)
+        e = launch_pdl(route_from_logits_kernel<1>, dim3(blocks), dim3(256), 0, s, part, nsplit, a);
+    else if (a.E <= 64)
+        e = launch_pdl(route_from_logits_kernel<2>, dim3(blocks), dim3(256), 0, s, part, nsplit, a);
+    else if (a.E <= 128)
+        e = launch_pdl(route_from_logits_kernel<4>, dim3(blocks), dim3(256), 0, s, part, nsplit, a);
+    else
+        e = launch_pdl(route_from_logits_kernel<8>, dim3(blocks), dim3(256), 0, s, part, nsplit, a);
+    return e;
 }
 
 }  // namespace moe

@@ -100,6 +100,9 @@ def route_from_logits(r, bias, gate, K, renormalize=False, routed_scale=1.0):
       w [K]          gate weights
       margin         c_(K) - c_(K+1): selection score at rank K minus rank K+1
                      (1-based; +inf when K == E)
+      min_gap        smallest gap between consecutive ranked scores among the
+                     first min(K+1, E): how close the selection or the slot
+                     order came to a tie
       score [E]      the selection score c the ranking used
       s [E]          sigmoid scores (sigmoid mode only)
       top_scores     [K+1] the K+1 largest c, descending (sigmoid mode only)
@@ -151,6 +154,8 @@ def route_from_logits(r, bias, gate, K, renormalize=False, routed_scale=1.0):
     out["w"] = w
     out["score"] = c
     out["margin"] = (c[order[K - 1]] - c[order[K]]) if K < E else math.inf
+    top = c[order[:min(K + 1, E)]]
+    out["min_gap"] = float(np.min(top[:-1] - top[1:])) if top.shape[0] > 1 else math.inf
     return out
 
 
@@ -173,6 +178,7 @@ def route(x, W_router, bias, gate, K, renormalize=False, routed_scale=1.0):
         "idx": np.stack([p["idx"] for p in per]) if T else np.zeros((0, K), np.int64),
         "w": np.stack([p["w"] for p in per]) if T else np.zeros((0, K)),
         "margin": np.array([p["margin"] for p in per], dtype=np.float64),
+        "min_gap": np.array([p["min_gap"] for p in per], dtype=np.float64),
     }
     if gate == GATE_SIGMOID:
         res["top_scores"] = np.stack([p["top_scores"] for p in per])

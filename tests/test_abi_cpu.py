@@ -91,8 +91,10 @@ def test_host_side_rejections_do_not_touch_the_gpu(api):
         api.MOE_ERR_INVALID_ARG
     # invalid config through every entry point
     bad = _spec(api, K=9).config()
-    assert L.moe_route(ctypes.byref(bad), fake, fake, None, fake, fake, None, None, None, None) == \
-        api.MOE_ERR_INVALID_ARG
+    assert L.moe_route(ctypes.byref(bad), fake, fake, None, fake, fake, None, None, None, None, 0,
+                       None) == api.MOE_ERR_INVALID_ARG
+    assert L.moe_route(ctypes.byref(cfg), fake, fake, None, fake, fake, None, None, None, fake, 8,
+                       None) == api.MOE_ERR_WORKSPACE
     assert L.moe_dispatch(ctypes.byref(bad), fake, fake, fake, fake, fake, fake, fake, fake, 1 << 30,
                           None) == api.MOE_ERR_INVALID_ARG
     assert L.moe_dispatch(ctypes.byref(cfg), fake, fake, fake, fake, fake, fake, fake, fake, 8,

@@ -102,17 +102,24 @@ def test_full_size_sampled_rows(name):
                                       ("softmax_all_renorm", 100, 7), ("sigmoid", 128, 8),
                                       ("sigmoid", 9, 8), ("softmax_topk", 33, 16),
                                       ("sigmoid", 20, 1)])
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_route(gate, E, K, dtype):
+@pytest.mark.parametrize("dtype,d,with_ws", [("bf16", 272, False), ("f32", 272, False),
+                                             ("bf16", 256, True), ("bf16", 1024, True)])
+def test_route(gate, E, K, dtype, d, with_ws):
+    """Both router paths: the fused FP32 FMA kernel, and (BF16, E > 32, E % 8 == 0,
+    d % 64 == 0, with a workspace) the tensor-core split-weight router."""
     A = api()
-    w = W.Workload("r", T=517, d=272, d_ff=16, E=E, K=K, n_shared=0, shared_d_ff=0, dtype=dtype,
+    w = W.Workload("r", T=517, d=d, d_ff=16, E=E, K=K, n_shared=0, shared_d_ff=0, dtype=dtype,
                    gate=gate, bias_std=0.02, skew=0.5 if gate != "sigmoid" else 0.0)
     inp = W.make_inputs(w, device="cuda")
     if gate == "sigmoid":
         inp["bias"] = (torch.randn(E, generator=torch.Generator().manual_seed(5)) * 0.05).cuda()
-    g = A.route(A.LayerSpec.of(w), inp["x"], inp["W_router"], inp["bias"])
+    spec = A.LayerSpec.of(w)
+    ws = A.alloc_workspace(spec) if with_ws else None
+    g = A.route(spec, inp["x"], inp["W_router"], inp["bias"], ws=ws)
+    if ws is not None:
+        assert A.workspace_status(ws) == A.MOE_OK
     ort = P.oracle_routing(w, inp)
-    near = ort["margin"] <= P.NEAR_TIE
+    near = ort["min_gap"] <= P.NEAR_TIE
     P.check_routing(w, ort, g, near)
 
 
@@ -223,12 +230,17 @@ def test_forward_deterministic_and_host_variant():
     ws = A.alloc_workspace(spec)
     o1 = A.forward(spec, inp["x"], inp, ws=ws).clone()
     o2 = A.forward(spec, inp["x"], inp, ws=ws).clone()
-    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(o1.view(torch.int32), o2.view(torch.int32))
     xh = inp["x"].cpu().pin_memory()
-    oh = torch.empty_like(xh).pin_memory()
+    oh = torch.empty((w.T, w.d), dtype=torch.float32).pin_memory()
     A.forward_host(spec, xh, inp, oh, ws)
-    assert torch.equal(oh.view(torch.int16), o1.cpu().view(torch.int16))
+    assert torch.equal(oh.view(torch.int32), o1.cpu().view(torch.int32))
     assert A.workspace_status(ws) == A.MOE_OK
+    # BF16 output: the same FP32 result rounded once to nearest-even
+    sb = A.LayerSpec.of(w, out_dtype="bf16")
+    ob = A.forward(sb, inp["x"], inp, ws=ws)
+    assert ob.dtype == torch.bfloat16
+    assert torch.equal(ob.view(torch.int16), o1.to(torch.bfloat16).view(torch.int16))
 
 
 def test_launch_count_grows():
