@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
 // (APEX-1 Mathematical Reference Part 3 section 13.2: shared output plus the
 // gate-weighted routed outputs; kimi_k3 StableLatentMoE's index_add_ scatter
 // written as a gather through the inverse permutation).
-template <bool OUT_BF16>
+template <bool OUT_BF16, int KMAX, int NB>
 __global__ void __launch_bounds__(256) gather_sum_kernel(const float* __restrict__ ys,
                                                          const int32_t* __restrict__ inv, int T,
                                                          int K, int cols,
@@ -172,39 +172,61 @@ __global__ void __launch_bounds__(256) gather_sum_kernel(const float* __restrict
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (t >= T) return;
     const int lane = threadIdx.x & 31;
-    int pos[16];
+    int pos[KMAX];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) pos[k] = (k < K) ? inv[static_cast<size_t>(t) * K + k] : 0;
-#pragma unroll 4
-    for (int c0 = lane * 8; c0 < cols; c0 += 32 * 8) {
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int k = 0; k < KMAX; ++k) pos[k] = (k < K) ? inv[static_cast<size_t>(t) * K + k] : 0;
+    // NB column blocks of 256 per batch, every load of the batch issued before the sums
+    for (int cb = 0; cb < cols; cb += 256 * NB) {
+        float4 y[NB][KMAX][2];
+        float4 ad[NB][2];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            if (k >= K) break;
-            const float* p = ys + static_cast<size_t>(pos[k]) * cols + c0;
-            const float4 a = __ldg(reinterpret_cast<const float4*>(p));
-            const float4 b = __ldg(reinterpret_cast<const float4*>(p + 4));
-            acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-            acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+        for (int b = 0; b < NB; ++b) {
+            const int c0 = cb + 256 * b + lane * 8;
+            if (c0 < cols) {
+#pragma unroll
+                for (int k = 0; k < KMAX; ++k) {
+                    if (k < K) {
+                        const float* p = ys + static_cast<size_t>(pos[k]) * cols + c0;
+                        y[b][k][0] = __ldg(reinterpret_cast<const float4*>(p));
+                        y[b][k][1] = __ldg(reinterpret_cast<const float4*>(p + 4));
+                    }
+                }
+                if (addend != nullptr) {
+                    const float* p = addend + static_cast<size_t>(t) * cols + c0;
+                    ad[b][0] = __ldg(reinterpret_cast<const float4*>(p));
+                    ad[b][1] = __ldg(reinterpret_cast<const float4*>(p + 4));
+                }
+            }
         }
-        const size_t o = static_cast<size_t>(t) * cols + c0;
-        if (addend != nullptr) {
-            const float4 a = __ldg(reinterpret_cast<const float4*>(addend + o));
-            const float4 b = __ldg(reinterpret_cast<const float4*>(addend + o + 4));
-            acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-            acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
-        }
-        if (OUT_BF16) {
-            uint4 v;
-            v.x = pack_bf16x2(acc[0], acc[1]);
-            v.y = pack_bf16x2(acc[2], acc[3]);
-            v.z = pack_bf16x2(acc[4], acc[5]);
-            v.w = pack_bf16x2(acc[6], acc[7]);
-            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + o) = v;
-        } else {
-            float* p = static_cast<float*>(out) + o;
-            *reinterpret_cast<float4*>(p) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            *reinterpret_cast<float4*>(p + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const int c0 = cb + 256 * b + lane * 8;
+            if (c0 >= cols) continue;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < KMAX; ++k) {
+                if (k < K) {
+                    acc[0] += y[b][k][0].x; acc[1] += y[b][k][0].y; acc[2] += y[b][k][0].z; acc[3] += y[b][k][0].w;
+                    acc[4] += y[b][k][1].x; acc[5] += y[b][k][1].y; acc[6] += y[b][k][1].z; acc[7] += y[b][k][1].w;
+                }
+            }
+            if (addend != nullptr) {
+                acc[0] += ad[b][0].x; acc[1] += ad[b][0].y; acc[2] += ad[b][0].z; acc[3] += ad[b][0].w;
+                acc[4] += ad[b][1].x; acc[5] += ad[b][1].y; acc[6] += ad[b][1].z; acc[7] += ad[b][1].w;
+            }
+            const size_t o = static_cast<size_t>(t) * cols + c0;
+            if (OUT_BF16) {
+                uint4 v;
+                v.x = pack_bf16x2(acc[0], acc[1]);
+                v.y = pack_bf16x2(acc[2], acc[3]);
+                v.z = pack_bf16x2(acc[4], acc[5]);
+                v.w = pack_bf16x2(acc[6], acc[7]);
+                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + o) = v;
+            } else {
+                float* q = static_cast<float*>(out) + o;
+                *reinterpret_cast<float4*>(q) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                *reinterpret_cast<float4*>(q + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            }
         }
     }
 }
@@ -280,11 +302,17 @@ cudaError_t launch_gather_rows(const void* src, const int32_t* rowidx, int rows,
 cudaError_t launch_gather_sum(const float* ys, const int32_t* inv, int T, int K, int cols,
                               const float* addend, void* out, int out_bf16, cudaStream_t s) {
     const int blocks = (T * 32 + 255) / 256;
-    if (out_bf16)
-        return launch_pdl(gather_sum_kernel<true>, dim3(blocks), dim3(256), 0, s, ys, inv, T, K,
-                          cols, addend, out);
-    return launch_pdl(gather_sum_kernel<false>, dim3(blocks), dim3(256), 0, s, ys, inv, T, K, cols,
-                      addend, out);
+    // about 16 float4 loads in flight per lane per batch
+#define MOE_GS(KM, NB)                                                                            \
+    return out_bf16 ? launch_pdl(gather_sum_kernel<true, KM, NB>, dim3(blocks), dim3(256), 0, s, ys, \
+                                 inv, T, K, cols, addend, out)                                   \
+                    : launch_pdl(gather_sum_kernel<false, KM, NB>, dim3(blocks), dim3(256), 0, s, ys, \
+                                 inv, T, K, cols, addend, out)
+    if (K <= 2) MOE_GS(2, 4);
+    if (K <= 4) MOE_GS(4, 2);
+    if (K <= 8) MOE_GS(8, 1);
+    MOE_GS(16, 1);
+#undef MOE_GS
 }
 
 }  // namespace moe

@@ -47,7 +47,9 @@ constexpr int BAR_OFF = STAGES * STAGE_BYTES;
 constexpr int NBARS = 2 * STAGES + 4 + 1;
 constexpr int MISC_OFF = BAR_OFF + 8 * NBARS;
 constexpr int SCHED_OFF = ((MISC_OFF + 16) + 15) / 16 * 16;
-constexpr int SMEM_BYTES = SCHED_OFF + 2 * (MAXE + 1) * 4 + 1024;
+constexpr int STG_BYTES = 32 * 64;  // per epilogue warp: 32 rows x 64 bytes
+constexpr int STG_OFF = (SCHED_OFF + 2 * (MAXE + 1) * 4 + 127) / 128 * 128;
+constexpr int SMEM_BYTES = STG_OFF + EPI_WARPS * STG_BYTES + 1024;
 
 struct TcParams {
     CUtensorMap mapA[2];
@@ -137,35 +139,26 @@ MOE_DEV Unit decode_unit(int u, const TcParams& p, int total0, const int* s_mtp,
     return t;
 }
 
-MOE_DEV void store16(void* out, int out_f32, size_t row, int ld, int col, const float (&v)[16],
-                     int limit) {
-    if (out_f32) {
-        float* p = static_cast<float*>(out) + row * static_cast<size_t>(ld) + col;
-        if (limit >= 16) {
+// Stores a 32-row x 64-byte block whose row `lane` this lane holds in v[0..3]:
+// through the warp's staging buffer (16-byte chunks XOR-swizzled by row, so
+// both the row-wise writes and the column-wise reads are bank-conflict free),
+// then 4 rows x 64 bytes per store instruction. Rows >= valid_rows and
+// 16-byte chunks >= valid_chunks are not written.
+MOE_DEV void warp_store_block(uint4* stg, const uint4 (&v)[4], int lane, char* row0,
+                              size_t pitch, int valid_rows, int valid_chunks) {
+    const int sw = (lane >> 1) & 3;
 #pragma unroll
-            for (int i = 0; i < 16; i += 4)
-                *reinterpret_cast<float4*>(p + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-        } else {
-            for (int i = 0; i < limit; ++i) p[i] = v[i];
-        }
-    } else {
-        __nv_bfloat16* p = static_cast<__nv_bfloat16*>(out) + row * static_cast<size_t>(ld) + col;
-        if (limit >= 16) {
-            uint4 a, b;
-            a.x = pack_bf16x2(v[0], v[1]);
-            a.y = pack_bf16x2(v[2], v[3]);
-            a.z = pack_bf16x2(v[4], v[5]);
-            a.w = pack_bf16x2(v[6], v[7]);
-            b.x = pack_bf16x2(v[8], v[9]);
-            b.y = pack_bf16x2(v[10], v[11]);
-            b.z = pack_bf16x2(v[12], v[13]);
-            b.w = pack_bf16x2(v[14], v[15]);
-            *reinterpret_cast<uint4*>(p) = a;
-            *reinterpret_cast<uint4*>(p + 8) = b;
-        } else {
-            for (int i = 0; i < limit; ++i) p[i] = __float2bfloat16_rn(v[i]);
-        }
+    for (int c = 0; c < 4; ++c) stg[lane * 4 + (c ^ sw)] = v[c];
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int row = 8 * i + (lane >> 2);
+        const int ch = lane & 3;
+        const uint4 w = stg[row * 4 + (ch ^ ((row >> 1) & 3))];
+        if (row < valid_rows && ch < valid_chunks)
+            *reinterpret_cast<uint4*>(row0 + row * pitch + ch * 16) = w;
     }
+    __syncwarp();
 }
 
 template <bool SWIGLU>
@@ -325,7 +318,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
         // ---------------- epilogue warps 2..9 ----------------
         const int q = warp & 3;          // TMEM lane quarter this warp may access
         const int half = (warp - 2) >> 2;  // which half of the tile's columns
-        const int r = q * 32 + lane;
+        uint4* stg = reinterpret_cast<uint4*>(smem + STG_OFF + (warp - 2) * STG_BYTES);
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int u = blockIdx.x; u < total; u += gridDim.x) {
@@ -337,63 +330,95 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
             tc_fence_after();
             const uint32_t tb =
                 tmem_base + static_cast<uint32_t>(acc * ACC_COLS) + (static_cast<uint32_t>(q * 32) << 16);
-            const bool rv = r < t.rows;
-            const size_t orow = static_cast<size_t>(t.out_row0 + r);
+            const int valid_rows = t.rows - q * 32;  // rows of this warp's 32 that exist
+            const size_t orow = static_cast<size_t>(t.out_row0 + q * 32 + lane);
             const int N = p.N[t.g];
-            void* out = p.out[t.g];
             const int ld = p.out_ld[t.g];
             const int of32 = p.out_f32[t.g];
+            const size_t es = of32 ? 4 : 2;
+            const size_t pitch = static_cast<size_t>(ld) * es;
+            char* out_rows = static_cast<char*>(p.out[t.g]) +
+                             static_cast<size_t>(t.out_row0 + q * 32) * pitch;
             if (SWIGLU) {
+                // 2 blocks of 32 BF16 columns per warp
 #pragma unroll 1
-                for (int c = half * 64; c < half * 64 + 64; c += 16) {
-                    uint32_t gr[16], ur[16];
-                    tc_ld_32x32b_x16(tb + c, gr);
-                    tc_ld_32x32b_x16(tb + 128 + c, ur);
+                for (int c = half * 64; c < half * 64 + 64; c += 32) {
+                    uint32_t g0[16], g1[16], u0[16], u1[16];
+                    tc_ld_32x32b_x16(tb + c, g0);
+                    tc_ld_32x32b_x16(tb + c + 16, g1);
+                    tc_ld_32x32b_x16(tb + 128 + c, u0);
+                    tc_ld_32x32b_x16(tb + 128 + c + 16, u1);
                     tc_wait_ld();
-                    const int lim = N - (t.n0 + c);
-                    if (rv && lim > 0) {
-                        float h[16];
+                    uint32_t pk[16];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float g = __uint_as_float(gr[i]);
-                            h[i] = __fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(ur[i]);
-                        }
-                        store16(out, of32, orow, ld, t.out_col0 + c, h, lim);
+                    for (int i = 0; i < 8; ++i) {
+                        float ga = __uint_as_float(g0[2 * i]), gb = __uint_as_float(g0[2 * i + 1]);
+                        pk[i] = pack_bf16x2(__fdividef(ga, 1.0f + __expf(-ga)) * __uint_as_float(u0[2 * i]),
+                                            __fdividef(gb, 1.0f + __expf(-gb)) * __uint_as_float(u0[2 * i + 1]));
+                        ga = __uint_as_float(g1[2 * i]);
+                        gb = __uint_as_float(g1[2 * i + 1]);
+                        pk[8 + i] = pack_bf16x2(__fdividef(ga, 1.0f + __expf(-ga)) * __uint_as_float(u1[2 * i]),
+                                                __fdividef(gb, 1.0f + __expf(-gb)) * __uint_as_float(u1[2 * i + 1]));
                     }
+                    const uint4 v[4] = {make_uint4(pk[0], pk[1], pk[2], pk[3]), make_uint4(pk[4], pk[5], pk[6], pk[7]),
+                                        make_uint4(pk[8], pk[9], pk[10], pk[11]),
+                                        make_uint4(pk[12], pk[13], pk[14], pk[15])};
+                    const int vch = (N - (t.n0 + c)) / 8;  // valid 16-byte chunks (8 BF16 each)
+                    warp_store_block(stg, v, lane, out_rows + static_cast<size_t>(t.out_col0 + c) * 2,
+                                     pitch, valid_rows, vch);
                 }
             } else {
                 float rs = 1.0f;
-                if (t.g == 0 && p.rowscale0 != nullptr && rv) rs = p.rowscale0[orow];
-                const bool add = (t.g == 1 && p.addend != nullptr);
+                if (t.g == 0 && p.rowscale0 != nullptr && lane < valid_rows) rs = p.rowscale0[orow];
+                const float* arow = (t.g == 1 && p.addend != nullptr && lane < valid_rows)
+                                        ? p.addend + orow * static_cast<size_t>(p.add_ld)
+                                        : nullptr;
                 const int span = 32 * p.nstrip;  // this warp's columns: [half * span, +span)
+                // blocks of 64 bytes per row: 16 FP32 or 32 BF16 columns
+                const int bc = of32 ? 16 : 32;
 #pragma unroll 1
-                for (int c = half * span; c < half * span + span; c += 16) {
-                    uint32_t vr[16];
-                    tc_ld_32x32b_x16(tb + c, vr);
+                for (int c = half * span; c < half * span + span; c += bc) {
+                    float v[32];
+                    uint32_t r0[16], r1[16];
+                    tc_ld_32x32b_x16(tb + c, r0);
+                    if (!of32) tc_ld_32x32b_x16(tb + c + 16, r1);
                     tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        v[i] = rs * __uint_as_float(r0[i]);
+                        v[16 + i] = of32 ? 0.0f : rs * __uint_as_float(r1[i]);
+                    }
                     const int lim = N - (t.n0 + c);
-                    if (rv && lim > 0) {
-                        float v[16];
+                    if (arow != nullptr && lim > 0) {
+                        const float* ap = arow + t.out_col0 + c;
+                        const int n = lim < bc ? lim : bc;
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] = rs * __uint_as_float(vr[i]);
-                        const int col = t.out_col0 + c;
-                        if (add) {
-                            const float* ap = p.addend + orow * static_cast<size_t>(p.add_ld) + col;
-                            if (lim >= 16) {
-#pragma unroll
-                                for (int i = 0; i < 16; i += 4) {
-                                    const float4 a4 = *reinterpret_cast<const float4*>(ap + i);
-                                    v[i] += a4.x;
-                                    v[i + 1] += a4.y;
-                                    v[i + 2] += a4.z;
-                                    v[i + 3] += a4.w;
-                                }
-                            } else {
-                                for (int i = 0; i < lim; ++i) v[i] += ap[i];
+                        for (int i = 0; i < 32; i += 4) {
+                            if (i < n) {
+                                const float4 a4 = *reinterpret_cast<const float4*>(ap + i);
+                                v[i] += a4.x;
+                                v[i + 1] += a4.y;
+                                v[i + 2] += a4.z;
+                                v[i + 3] += a4.w;
                             }
                         }
-                        store16(out, of32, orow, ld, col, v, lim);
                     }
+                    uint4 blk[4];
+                    if (of32) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            blk[j] = make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                                                __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            blk[j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                                                pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                                                pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+                    }
+                    const int vch = lim > 0 ? static_cast<int>(lim * es / 16) : 0;
+                    warp_store_block(stg, blk, lane, out_rows + static_cast<size_t>(t.out_col0 + c) * es,
+                                     pitch, valid_rows, vch);
                 }
             }
             tc_fence_before();

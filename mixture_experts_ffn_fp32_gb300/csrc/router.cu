@@ -150,20 +150,33 @@ MOE_DEV void route_token_warp(const float (&r)[J], int t, const RouterArgs& a) {
     if (a.margin != nullptr && lane == 0) a.margin[t] = (K < E) ? (vK1 - vK) : INFINITY;
 }
 
-// E <= 32: one warp per token. Lane l takes the d-index pair k0 + 2l, k0 + 2l + 1,
-// so a warp's x loads and its W_router row loads are both contiguous; a
-// butterfly then leaves every expert's full sum on every lane.
+// E <= 32: one warp per token, 8 tokens per CTA. The CTA first copies its 8
+// x rows into shared memory with all its loads in flight at once (one memory
+// round trip), then lane l of a warp takes the d-index pairs k0 + 2l, k0 + 2l + 1,
+// so the W_router row loads of a warp are contiguous; a butterfly then leaves
+// every expert's full sum on every lane.
 template <int EP, bool BF16>
 __global__ void __launch_bounds__(256) router_small_kernel(RouterArgs a) {
+    extern __shared__ __align__(16) uint8_t xsm[];
     pdl_wait();
     pdl_trigger();
     if (a.err_clear != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *a.err_clear = 0;
-    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (t >= a.T) return;
-    const int lane = static_cast<int>(lane_id());
     const int E = a.E, d = a.d;
+    const int t0 = blockIdx.x * 8;
+    const int ntok = min(8, a.T - t0);
+    {
+        const size_t row_bytes = static_cast<size_t>(d) * (BF16 ? 2 : 4);
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.x) + t0 * row_bytes);
+        uint4* dst = reinterpret_cast<uint4*>(xsm);
+        const int nvec = static_cast<int>(ntok * row_bytes / 16);
+        for (int i = threadIdx.x; i < nvec; i += blockDim.x) dst[i] = __ldg(src + i);
+    }
+    __syncthreads();
+    const int wt = threadIdx.x >> 5;
+    if (wt >= ntok) return;
+    const int t = t0 + wt;
+    const int lane = static_cast<int>(lane_id());
     const bool vec = (E == EP) && (EP % 4 == 0);
-    // U d-index pairs per lane per step, all loads issued before the FMAs
     constexpr int U = EP <= 8 ? 4 : (EP <= 16 ? 2 : 1);
     float acc[EP];
 #pragma unroll
@@ -179,13 +192,11 @@ __global__ void __launch_bounds__(256) router_small_kernel(RouterArgs a) {
             for (int e = 0; e < EP; ++e) w0[u][e] = w1[u][e] = 0.0f;
             if (k < d) {
                 if (BF16) {
-                    const uint32_t v = *reinterpret_cast<const uint32_t*>(
-                        static_cast<const __nv_bfloat16*>(a.x) + static_cast<size_t>(t) * d + k);
+                    const uint32_t v = reinterpret_cast<const uint32_t*>(xsm)[(wt * d + k) >> 1];
                     x0[u] = bf16_lo(v);
                     x1[u] = bf16_hi(v);
                 } else {
-                    const float2 v = *reinterpret_cast<const float2*>(
-                        static_cast<const float*>(a.x) + static_cast<size_t>(t) * d + k);
+                    const float2 v = reinterpret_cast<const float2*>(xsm)[(wt * d + k) >> 1];
                     x0[u] = v.x;
                     x1[u] = v.y;
                 }
@@ -372,15 +383,26 @@ template <bool BF16>
 cudaError_t launch_router_t(const RouterArgs& a, cudaStream_t s) {
     cudaError_t e = cudaSuccess;
     if (a.E <= 32) {
-        const int blocks = (a.T * 32 + 255) / 256;
+        const int blocks = (a.T + 7) / 8;
+        const size_t smem = static_cast<size_t>(8) * a.d * (BF16 ? 2 : 4);
+        if (smem > 48 * 1024) {
+            static bool set = false;
+            if (!set) {
+                cudaFuncSetAttribute(router_small_kernel<4, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+                cudaFuncSetAttribute(router_small_kernel<8, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+                cudaFuncSetAttribute(router_small_kernel<16, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+                cudaFuncSetAttribute(router_small_kernel<32, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+                set = true;
+            }
+        }
         if (a.E <= 4)
-            e = launch_pdl(router_small_kernel<4, BF16>, dim3(blocks), dim3(256), 0, s, a);
+            e = launch_pdl(router_small_kernel<4, BF16>, dim3(blocks), dim3(256), smem, s, a);
         else if (a.E <= 8)
-            e = launch_pdl(router_small_kernel<8, BF16>, dim3(blocks), dim3(256), 0, s, a);
+            e = launch_pdl(router_small_kernel<8, BF16>, dim3(blocks), dim3(256), smem, s, a);
         else if (a.E <= 16)
-            e = launch_pdl(router_small_kernel<16, BF16>, dim3(blocks), dim3(256), 0, s, a);
+            e = launch_pdl(router_small_kernel<16, BF16>, dim3(blocks), dim3(256), smem, s, a);
         else
-            e = launch_pdl(router_small_kernel<32, BF16>, dim3(blocks), dim3(256), 0, s, a);
+            e = launch_pdl(router_small_kernel<32, BF16>, dim3(blocks), dim3(256), smem, s, a);
     } else {
         const int blocks = (a.T + RT_BT - 1) / RT_BT;
         if (a.E <= 64)
