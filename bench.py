@@ -59,6 +59,23 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(value: float, device="cpu") -> float:
+    """Slowest rank's value (replicas run independently; the job takes as long
+    as its slowest rank). Identity without an initialised process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, step_ms: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's step."""
+    return world * tokens_per_rank / (step_ms / 1e3)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -108,16 +125,20 @@ def kernel_source_hash() -> str:
 
 def profiled_traffic(workload: str):
     """DRAM bytes per launch of the gate/up kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", "gate_up_traffic.json")
+    summary (profiles/gate_up_traffic.txt), if it was taken on the current
+    kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "gate_up_traffic.txt")
     if not os.path.exists(path):
         return None
+    src = kernel_source_hash()
     with open(path) as f:
-        d = json.load(f)
-    e = d.get(workload)
-    if not e or e.get("kernel_source") != kernel_source_hash():
-        return None
-    return e.get("dram_bytes_per_launch")
+        for ln in f:
+            if ln.startswith("#") or "=" not in ln:
+                continue
+            kv = dict(p.split("=", 1) for p in ln.split())
+            if kv.get("workload") == workload and kv.get("kernel_source") == src:
+                return int(kv["dram_bytes_per_launch"])
+    return None
 
 
 # ---------------------------------------------------------------------------
@@ -326,7 +347,7 @@ def run_ours(args, name):
     if st != api.MOE_OK:
         raise RuntimeError(f"device status after the timed steps: {api.status_string(st)}")
     per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = sum(per) / len(per)
+    ms = max_over_ranks(sum(per) / len(per), dev)
     # per-stage breakdown from a separate instrumented pass (events between every stage)
     n_inst = min(args.steps, 20)
     timer2 = api.StageTimer(n_inst)
@@ -334,10 +355,6 @@ def run_ours(args, name):
         flush.fill_(i & 0xFF)
         step()
     breakdown, nb = timer2.finish()
-    if world > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
 
     # end to end through the host-buffer entry point (copies inside the timed region)
     e2e = None
@@ -356,12 +373,8 @@ def run_ours(args, name):
             b.record(stream)
             b.synchronize()
             e_ms.append(a.elapsed_time(b))
-        em = sum(e_ms) / len(e_ms)
-        if world > 1:
-            t = torch.tensor([em], device=dev, dtype=torch.float64)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            em = float(t.item())
-        e2e = {"value": world * w.T / (em / 1e3), "unit": "tokens/s",
+        em = max_over_ranks(sum(e_ms) / len(e_ms), dev)
+        e2e = {"value": job_tokens_per_s(w.T, world, em), "unit": "tokens/s",
                "h2d_bytes_per_step": xh.numel() * xh.element_size(),
                "d2h_bytes_per_step": oh.numel() * oh.element_size(), "ms_per_step": em}
 
@@ -380,7 +393,7 @@ def run_ours(args, name):
     t_flop = flops / (pk["bf16_tflops"] * 1e12)
     t_hbm = layer_bytes(w, counts) / (pk["hbm_gbs"] * 1e9)
     line = {
-        "metric": METRIC, "value": world * w.T / (ms / 1e3), "unit": "tokens/s",
+        "metric": METRIC, "value": job_tokens_per_s(w.T, world, ms), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
