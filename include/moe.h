@@ -177,6 +177,26 @@ moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const fl
                         float* sorted_w, int32_t* inv, void* ws, size_t ws_bytes,
                         void* stream);
 
+/* moe_dispatch for callers that cannot allocate device memory: for example a
+ * runtime that owns all device memory and only hands out the tensors it
+ * manages, or code that must not call cudaMalloc after start-up because an
+ * allocation can synchronise the device or fail under memory pressure.
+ * The pages have no counterpart of this call; it exists for such callers.
+ * Same inputs, outputs and results as moe_dispatch, but no workspace: its
+ * scratch is a fixed array in the library's own device memory, sized for
+ * T*K <= 65536 and E <= 256 (about 130 KB, held by every GPU that loads the
+ * library until the process exits); larger calls return MOE_ERR_UNSUPPORTED.
+ * The first call on each device looks up the array's device address with
+ * that device current; make that first call before any stream capture.
+ * Every call reuses the same array, so calls that overlap on the GPU (for
+ * example on two streams with no ordering between them) race and corrupt
+ * each other's results; order such calls on one stream. Expert ids outside
+ * [0, E) are skipped and not reported. Calls no allocating function. */
+moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* topk_idx,
+                                const float* topk_w, int32_t* counts, int32_t* offsets,
+                                int32_t* sorted_token, float* sorted_w, int32_t* inv,
+                                void* stream);
+
 /* Whole layer forward: route -> dispatch -> grouped gate/up GEMM with
  * SiLU(.)*up epilogue -> grouped down GEMM scaled by the gate weight ->
  * shared experts -> deterministic combine (no float atomics).

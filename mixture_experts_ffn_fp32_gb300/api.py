@@ -73,6 +73,7 @@ def lib() -> ctypes.CDLL:
             "moe_get_workspace_views": (ctypes.c_int, [cfgp, vp, ctypes.POINTER(Views)]),
             "moe_route": (ctypes.c_int, [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
             "moe_dispatch": (ctypes.c_int, [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "moe_dispatch_noalloc": (ctypes.c_int, [cfgp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "moe_forward": (ctypes.c_int, [cfgp, vp, ctypes.POINTER(Weights), vp, vp, sz, vp]),
             "moe_forward_host": (ctypes.c_int, [cfgp, vp, ctypes.POINTER(Weights), vp, vp, sz, vp]),
             "moe_quantile_bias_update": (ctypes.c_int, [i32, i32, i32, vp, vp, vp, vp, sz, vp]),
@@ -256,6 +257,32 @@ def dispatch(spec: LayerSpec, idx: torch.Tensor, w: torch.Tensor, ws: torch.Tens
                               out["inv"].data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)),
            "moe_dispatch")
     out["ws"] = ws
+    return out
+
+
+def dispatch_noalloc(spec: LayerSpec, idx: torch.Tensor, w: torch.Tensor, out: dict | None = None,
+                     stream=None):
+    """moe_dispatch_noalloc: moe_dispatch without a workspace, for callers that
+    cannot allocate device memory (the library keeps the scratch in a fixed
+    device array; T*K <= 65536, E <= 256). ``out`` may hold preallocated
+    counts, offsets, sorted_token, sorted_w and inv tensors."""
+    dev = idx.device
+    _dev(idx, torch.int32, "topk_idx", (spec.T, spec.K))
+    _dev(w, torch.float32, "topk_w", (spec.T, spec.K))
+    TK = spec.T * spec.K
+    if out is None:
+        out = {
+            "counts": torch.empty((spec.E,), dtype=torch.int32, device=dev),
+            "offsets": torch.empty((spec.E + 1,), dtype=torch.int32, device=dev),
+            "sorted_token": torch.empty((TK,), dtype=torch.int32, device=dev),
+            "sorted_w": torch.empty((TK,), dtype=torch.float32, device=dev),
+            "inv": torch.empty((spec.T, spec.K), dtype=torch.int32, device=dev),
+        }
+    _check(lib().moe_dispatch_noalloc(ctypes.byref(spec.config()), idx.data_ptr(), w.data_ptr(),
+                                      out["counts"].data_ptr(), out["offsets"].data_ptr(),
+                                      out["sorted_token"].data_ptr(), out["sorted_w"].data_ptr(),
+                                      out["inv"].data_ptr(), _stream(stream)),
+           "moe_dispatch_noalloc")
     return out
 
 
