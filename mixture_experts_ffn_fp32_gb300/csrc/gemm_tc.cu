@@ -65,6 +65,7 @@ struct TcParams {
     int out_f32[2];
     int kblocks[2];
     int a_kmod[2], b_kmod[2], a_kgroup[2], a_krep[2];
+    int b_wide[2];       // B maps are 4-D strip maps: one copy fetches all strips of a tile
     int nstrip;          // plain kernel: 64-column B strips per tile (MMA N = 64 * nstrip)
     int bno;             // output columns per tile
     uint32_t idesc;      // instruction descriptor (M = 128, N = 64 * nstrip)
@@ -253,7 +254,11 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
                     const int kcb = bkm ? kc % bkm : kc;
                     mbar_expect_tx(fb, stage_bytes);
                     tma_load_2d(sA, mA, kca, t.row0, fb);
-                    if (SWIGLU) {
+                    if (p.b_wide[t.g]) {
+                        const int sn = t.n0 >> 6;
+                        tma_load_4d(sB, mB0, 0, kcb, sn, t.zb, fb);
+                        if (SWIGLU) tma_load_4d(sB + 2 * STRIP_BYTES, mB1, 0, kcb, sn, t.zb, fb);
+                    } else if (SWIGLU) {
                         tma_load_3d(sB, mB0, t.n0, kcb, t.zb, fb);
                         tma_load_3d(sB + STRIP_BYTES, mB0, t.n0 + 64, kcb, t.zb, fb);
                         tma_load_3d(sB + 2 * STRIP_BYTES, mB1, t.n0, kcb, t.zb, fb);
@@ -445,6 +450,18 @@ bool make_A_map(CUtensorMap* m, const void* A, int rows, int K, int lda) {
     return encode_tmap(m, A, 2, dims, strides, box);
 }
 
+// B [Z, K, N] seen as [Z, N/64 strips, K, 64]: one box of `strips` strips lands
+// in shared memory strip after strip (8 KB each), the layout the MMA reads.
+// Needs N % 64 == 0 so that no strip runs past the end of a row.
+bool make_B_strip_map(CUtensorMap* m, const void* B, int Z, int K, int N, int strips) {
+    const uint64_t dims[4] = {64, static_cast<uint64_t>(K), static_cast<uint64_t>(N / 64),
+                              static_cast<uint64_t>(Z)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(N) * 2, 128,
+                                 static_cast<uint64_t>(K) * N * 2};
+    const uint32_t box[4] = {64, 64, static_cast<uint32_t>(strips), 1};
+    return encode_tmap(m, B, 4, dims, strides, box);
+}
+
 bool make_B_map(CUtensorMap* m, const void* B, int Z, int K, int N) {
     const uint64_t dims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K),
                               static_cast<uint64_t>(Z)};
@@ -483,8 +500,13 @@ cudaError_t launch_tc_t(const TcGemmArgs& a, cudaStream_t s) {
         if ((G.a_kmod && G.a_kmod % BK) || (G.b_kmod && G.b_kmod % BK)) return cudaErrorInvalidValue;
         if (G.ksplit > 1 && (g != 1 || G.Z != 1)) return cudaErrorInvalidValue;
         if (!make_A_map(&p.mapA[g], G.A, G.rows, KA, G.lda)) return cudaErrorInvalidValue;
-        if (!make_B_map(&p.mapB0[g], G.B0, G.Z, KB, G.N)) return cudaErrorInvalidValue;
-        if (SWIGLU && !make_B_map(&p.mapB1[g], G.B1, G.Z, KB, G.N)) return cudaErrorInvalidValue;
+        const int strips = SWIGLU ? 2 : p.nstrip;
+        p.b_wide[g] = G.N % 64 == 0 && make_B_strip_map(&p.mapB0[g], G.B0, G.Z, KB, G.N, strips) &&
+                      (!SWIGLU || make_B_strip_map(&p.mapB1[g], G.B1, G.Z, KB, G.N, strips));
+        if (!p.b_wide[g]) {
+            if (!make_B_map(&p.mapB0[g], G.B0, G.Z, KB, G.N)) return cudaErrorInvalidValue;
+            if (SWIGLU && !make_B_map(&p.mapB1[g], G.B1, G.Z, KB, G.N)) return cudaErrorInvalidValue;
+        }
         p.kblocks[g] = (G.K + BK - 1) / BK;
         p.a_kmod[g] = G.a_kmod;
         p.b_kmod[g] = G.b_kmod;
