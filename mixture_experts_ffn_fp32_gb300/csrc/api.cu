@@ -149,7 +149,7 @@ WsLayout plan_workspace(const moe_config& c) {
     L.chunk_base = take(static_cast<size_t>(L.nchunks) * E * 4);
     L.counts = take(E * 4);
     L.offsets = take((E + 1) * 4);
-    L.mt_prefix = take((E + 1) * 4);
+    L.mt_prefix = take(2 * (E + 1) * 4);  // tiles of bm and of 2 bm rows
     L.sorted_token = take(TK * 4);
     L.sorted_w = take(TK * 4);
     L.inv = take(TK * 4);

@@ -91,17 +91,22 @@ __global__ void __launch_bounds__(256) dispatch_scan_kernel(
     }
     const int cnt = (e < E) ? running : 0;
     const int off = block_exclusive_scan(cnt, warp_tot);
+    // tiles of bm rows per expert (mt_prefix[0..E]) and of 2 bm rows (mt_prefix[E+1..2E+1])
     const int mt = (cnt + bm - 1) / bm;
     const int mtoff = block_exclusive_scan(mt, warp_tot);
+    const int mt2 = (cnt + 2 * bm - 1) / (2 * bm);
+    const int mtoff2 = block_exclusive_scan(mt2, warp_tot);
     if (e < E) {
         counts[e] = cnt;
         offsets[e] = off;
         mt_prefix[e] = mtoff;
+        mt_prefix[E + 1 + e] = mtoff2;
         for (int b = 0; b < nchunks; ++b) chunk_base[static_cast<size_t>(b) * E + e] += off;
     }
     if (e == E - 1) {
         offsets[E] = off + cnt;
         mt_prefix[E] = mtoff + mt;
+        mt_prefix[2 * E + 1] = mtoff2 + mt2;
     }
     (void)TK;
 }

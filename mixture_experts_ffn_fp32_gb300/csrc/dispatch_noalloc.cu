@@ -28,9 +28,9 @@ constexpr int NOALLOC_MAX_E = 256;
 constexpr int NOALLOC_CHUNKS = NOALLOC_MAX_TK / DISPATCH_CHUNK;
 
 // [0, 64): error word (cleared at the start of every call)
-// then chunk_counts and chunk_base [NOALLOC_CHUNKS * E], then mt_prefix [E + 1]
+// then chunk_counts and chunk_base [NOALLOC_CHUNKS * E], then mt_prefix [2 (E + 1)]
 constexpr size_t NOALLOC_WORDS =
-    64 + 2 * static_cast<size_t>(NOALLOC_CHUNKS) * NOALLOC_MAX_E + (NOALLOC_MAX_E + 1);
+    64 + 2 * static_cast<size_t>(NOALLOC_CHUNKS) * NOALLOC_MAX_E + 2 * (NOALLOC_MAX_E + 1);
 
 static __device__ __align__(256) int32_t g_dispatch_scratch[NOALLOC_WORDS];
 

@@ -14,42 +14,60 @@
 // group 1 = S dense segments over all token rows (the shared experts, or a
 // single dense projection).
 //
-// Tile: 128 rows x 256 accumulator columns (SwiGLU: 128 gate + 128 up
-// columns of the same output tile), K step 64 (one 128-byte swizzle row),
-// 4-stage TMA ring of 48 KB stages, two 256-column TMEM accumulators so the
-// epilogue of one tile overlaps the main loop of the next. Warp 0 issues TMA,
-// warp 1 issues tcgen05.mma (M=128, N=256, K=16, BF16 in, FP32 accumulate),
-// warps 2-9 drain TMEM (two warps per 32-lane quarter, each taking half of
-// the columns), apply the epilogue and store. The weights stay in the
-// caller's [Z, K, N] layout (N contiguous) and are read as an MN-major
-// operand. Every wait is bounded (see common.cuh): on timeout the CTA stops,
-// drains its copies and MMAs, frees TMEM and flags the error word.
+// Tile: 128 rows x 256 accumulator columns per CTA (SwiGLU: 128 gate + 128
+// up columns of the same output tile), K step 64 (one 128-byte swizzle row),
+// a ring of TMA stages, two 256-column TMEM accumulators so the epilogue of
+// one tile overlaps the main loop of the next. Warp 0 issues TMA, warp 1
+// issues tcgen05.mma (BF16 in, FP32 accumulate), warps 2-9 drain TMEM (two
+// warps per 32-lane quarter, each taking half of the columns), apply the
+// epilogue and store. The weights stay in the caller's [Z, K, N] layout (N
+// contiguous) and are read as an MN-major operand.
+//
+// Two forms. CTA pair (the usual one, MMA N = 128 or 256): a cluster of two
+// CTAs on neighbouring SMs computes a 256-row tile with cta_group::2 MMAs
+// (M = 256) issued by the even CTA; each CTA loads its own 128 rows of A and
+// one half of B's columns, so every SM brings in 32 KB per K step instead of
+// 48 KB for the same tensor work. Both CTAs' copies complete on the even
+// CTA's stage barrier; the MMA commits arrive on both CTAs' barriers. A pair
+// stage holds two k-blocks, as handing a stage over between the two SMs
+// costs more than within one. Single CTA: M = 128 (any MMA N).
+//
+// Every wait is bounded (see common.cuh): on timeout the CTA stops, drains
+// its copies and MMAs, frees TMEM and flags the error word.
 #include "common.cuh"
 #include "internal.h"
 
 namespace moe {
 namespace {
 
-constexpr int BM = TC_BM;
-constexpr int BK = 64;
-constexpr int STAGES = 4;
+constexpr int BM = TC_BM;          // rows per CTA
+constexpr int BK = 64;             // one k-block: a 128-byte swizzle row of BF16
 constexpr int A_BYTES = BM * BK * 2;        // 16 KB
 constexpr int STRIP_BYTES = BK * 64 * 2;    // 8 KB: 64 k rows x 64 columns
-constexpr int B_BYTES = 4 * STRIP_BYTES;    // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 512;
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int MAXE = 256;
-
-constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-constexpr int NBARS = 2 * STAGES + 4 + 1;
-constexpr int MISC_OFF = BAR_OFF + 8 * NBARS;
-constexpr int SCHED_OFF = ((MISC_OFF + 16) + 15) / 16 * 16;
 constexpr int STG_BYTES = 32 * 64;  // per epilogue warp: 32 rows x 64 bytes
-constexpr int STG_OFF = (SCHED_OFF + 2 * (MAXE + 1) * 4 + 127) / 128 * 128;
-constexpr int SMEM_BYTES = STG_OFF + EPI_WARPS * STG_BYTES + 1024;
+
+// Shared-memory plan: a 192 KB ring of stages, barriers, the segment tables
+// and the epilogue staging buffers. Single CTA: 4 stages of one k-block (16 KB
+// A + 32 KB B). Pair: 3 stages of two k-blocks (2 x (16 KB A + 16 KB B half)):
+// a pair stage costs more to hand over than a single one, so it carries more.
+template <bool PAIR>
+struct Geo {
+    static constexpr int STAGES = PAIR ? 3 : 4;
+    static constexpr int KPS = PAIR ? 2 : 1;  // k-blocks per stage
+    static constexpr int SUB_BYTES = A_BYTES + (PAIR ? 2 : 4) * STRIP_BYTES;
+    static constexpr int STAGE_BYTES = KPS * SUB_BYTES;
+    static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+    static constexpr int NBARS = 2 * STAGES + 4 + 1;
+    static constexpr int MISC_OFF = BAR_OFF + 8 * NBARS;
+    static constexpr int SCHED_OFF = ((MISC_OFF + 16) + 15) / 16 * 16;
+    static constexpr int STG_OFF = (SCHED_OFF + 2 * (MAXE + 1) * 4 + 127) / 128 * 128;
+    static constexpr int SMEM_BYTES = STG_OFF + EPI_WARPS * STG_BYTES + 1024;
+};
 
 struct TcParams {
     CUtensorMap mapA[2];
@@ -65,14 +83,14 @@ struct TcParams {
     int out_f32[2];
     int kblocks[2];
     int a_kmod[2], b_kmod[2], a_kgroup[2], a_krep[2];
-    int b_wide[2];       // B maps are 4-D strip maps: one copy fetches all strips of a tile
+    int b_wide[2];       // B maps are 4-D strip maps: one copy fetches all strips a CTA needs
     int nstrip;          // plain kernel: 64-column B strips per tile (MMA N = 64 * nstrip)
     int bno;             // output columns per tile
-    uint32_t idesc;      // instruction descriptor (M = 128, N = 64 * nstrip)
+    uint32_t idesc;      // instruction descriptor (M = 128 or 256, N = 64 * nstrip)
     int ksplit1, kbs1;   // group 1 split-K: slices and k-blocks per slice
     int E, mt1;
     const int32_t* offsets;
-    const int32_t* mt_prefix;
+    const int32_t* mt_prefix;  // group 0 tiles of this kernel's rows (128, pair 256) per segment
     const float* rowscale0;
     const float* addend;
     int add_ld;
@@ -80,12 +98,18 @@ struct TcParams {
     unsigned long long timeout_ns;
 };
 
+// One work unit: `rows` (> 0) rows from row0 (at most 128; pair: 256, the
+// even CTA the first 128) by one tile of output columns, reduction k-blocks
+// [kb0, kb1).
 struct Unit {
     int g, row0, rows, zb, n0, out_row0, out_col0, kb0, kb1;
 };
 
-template <bool SWIGLU>
+// Group 0 units tile each expert's segment (mt_prefix counts the tiles),
+// group 1 units the dense rows; tiles of 128 rows, or 256 for a pair.
+template <bool PAIR>
 MOE_DEV Unit decode_unit(int u, const TcParams& p, int total0, const int* s_mtp, const int* s_off) {
+    constexpr int UROWS = PAIR ? 2 * BM : BM;
     const int BNO = p.bno;
     Unit t;
     if (u < total0) {
@@ -102,8 +126,8 @@ MOE_DEV Unit decode_unit(int u, const TcParams& p, int total0, const int* s_mtp,
         }
         const int m = mt - s_mtp[lo];
         t.g = 0;
-        t.row0 = s_off[lo] + m * BM;
-        t.rows = min(BM, s_off[lo + 1] - t.row0);
+        t.row0 = s_off[lo] + m * UROWS;
+        t.rows = min(UROWS, s_off[lo + 1] - t.row0);
         t.zb = lo;
         t.n0 = n * BNO;
         t.out_row0 = t.row0;
@@ -120,8 +144,8 @@ MOE_DEV Unit decode_unit(int u, const TcParams& p, int total0, const int* s_mtp,
         const int s = rem / nt;
         const int n = rem - s * nt;
         t.g = 1;
-        t.row0 = m * BM;
-        t.rows = min(BM, p.rows[1] - t.row0);
+        t.row0 = m * UROWS;
+        t.rows = min(UROWS, p.rows[1] - t.row0);
         t.n0 = n * BNO;
         if (p.ksplit1 > 1) {
             t.zb = 0;
@@ -162,25 +186,91 @@ MOE_DEV void warp_store_block(uint4* stg, const uint4 (&v)[4], int lane, char* r
     __syncwarp();
 }
 
-template <bool SWIGLU>
+// The copies one CTA makes for unit t, prepared once per unit: for each
+// k-block, its A rows and its B strips into sA / sB, completing on `bar`
+// (pair: the even CTA's barrier, a shared::cluster address).
+template <bool SWIGLU, bool PAIR>
+struct UnitCopies {
+    const CUtensorMap* mA;
+    const CUtensorMap* mB0;   // pair: this CTA's B (SwiGLU: gate for the even CTA, up for the odd)
+    const CUtensorMap* mB1;
+    int akm, bkm, akg, akr;   // k-block remaps (0: none)
+    int arow, nb, zb, bstrips;
+    bool loadA, wide;
+
+    MOE_DEV UnitCopies(const TcParams& p, const Unit& t, int rank, int bstrips_) {
+        mA = &p.mapA[t.g];
+        mB0 = (PAIR && SWIGLU && rank) ? &p.mapB1[t.g] : &p.mapB0[t.g];
+        mB1 = &p.mapB1[t.g];
+        akm = p.a_kmod[t.g];
+        bkm = p.b_kmod[t.g];
+        akg = p.a_kgroup[t.g];
+        akr = p.a_krep[t.g];
+        arow = t.row0 + rank * BM;
+        loadA = t.rows > rank * BM;  // pair: the odd CTA of a short unit has no rows
+        bstrips = bstrips_;
+        // pair, plain: each CTA one half of the tile's strips
+        nb = (PAIR && !SWIGLU) ? t.n0 + 64 * bstrips * rank : t.n0;
+        zb = t.zb;
+        wide = p.b_wide[t.g] != 0;
+    }
+
+    MOE_DEV void issue(int kb, uint32_t sA, uint32_t sB, uint32_t bar) const {
+        const int kc = kb * BK;
+        int kca = akm ? kc % akm : kc;
+        if (akg) kca = ((kb / (akg * akr)) * akg + kb % akg) * BK;
+        const int kcb = bkm ? kc % bkm : kc;
+        if (PAIR) {
+            if (loadA) tma_load_2d_pair(sA, mA, kca, arow, bar);
+            if (wide) {
+                tma_load_4d_pair(sB, mB0, 0, kcb, nb >> 6, zb, bar);
+            } else {
+                for (int j = 0; j < bstrips; ++j)
+                    tma_load_3d_pair(sB + j * STRIP_BYTES, mB0, nb + 64 * j, kcb, zb, bar);
+            }
+        } else {
+            tma_load_2d(sA, mA, kca, arow, bar);
+            if (wide) {
+                tma_load_4d(sB, mB0, 0, kcb, nb >> 6, zb, bar);
+                if (SWIGLU) tma_load_4d(sB + 2 * STRIP_BYTES, mB1, 0, kcb, nb >> 6, zb, bar);
+            } else if (SWIGLU) {
+                tma_load_3d(sB, mB0, nb, kcb, zb, bar);
+                tma_load_3d(sB + STRIP_BYTES, mB0, nb + 64, kcb, zb, bar);
+                tma_load_3d(sB + 2 * STRIP_BYTES, mB1, nb, kcb, zb, bar);
+                tma_load_3d(sB + 3 * STRIP_BYTES, mB1, nb + 64, kcb, zb, bar);
+            } else {
+                for (int j = 0; j < bstrips; ++j)
+                    tma_load_3d(sB + j * STRIP_BYTES, mB0, nb + 64 * j, kcb, zb, bar);
+            }
+        }
+    }
+};
+
+template <bool SWIGLU, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __grid_constant__ TcParams p) {
+    using G = Geo<PAIR>;
+    constexpr int STAGES = G::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t bar0 = sbase + BAR_OFF;
+    const uint32_t bar0 = sbase + G::BAR_OFF;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
     const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + MISC_OFF);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + MISC_OFF + 4);
-    int* s_mtp = reinterpret_cast<int*>(smem + SCHED_OFF);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::MISC_OFF);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + G::MISC_OFF + 4);
+    int* s_mtp = reinterpret_cast<int*>(smem + G::SCHED_OFF);
     int* s_off = s_mtp + (MAXE + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // pair: rank 0 issues the MMAs; work is distributed per cluster
+    const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+    const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int ustep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -189,7 +279,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), EPI_WARPS);
+            mbar_init(tempty_bar(a), PAIR ? 2 * EPI_WARPS : EPI_WARPS);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -204,8 +294,13 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
         }
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     // everything above overlaps the previous kernel; its outputs are read below
     pdl_wait();
@@ -216,14 +311,20 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
             s_off[i] = p.offsets[i];
         }
     }
+    __syncwarp();
     tc_fence_before();
-    __syncthreads();
+    if (PAIR)
+        cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int total0 = p.enabled[0] ? s_mtp[p.E] * p.nt[0] : 0;
     const int total =
         total0 + (p.enabled[1] ? p.mt1 * (p.ksplit1 > 1 ? p.ksplit1 : p.Z[1]) * p.nt[1] : 0);
     const WaitCtx wc{p.err, abort_flag, p.timeout_ns};
+    const int nstrip = SWIGLU ? 4 : p.nstrip;
+    const int bstrips = PAIR ? (SWIGLU ? 2 : nstrip / 2) : nstrip;  // strips this CTA loads
 
     if (warp == 0) {
         if (lane == 0) {
@@ -231,41 +332,25 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
             int stage = 0;
             uint32_t phase = 0, issued = 0, last_par = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-                const Unit t = decode_unit<SWIGLU>(u, p, total0, s_mtp, s_off);
-                const CUtensorMap* mA = &p.mapA[t.g];
-                const CUtensorMap* mB0 = &p.mapB0[t.g];
-                const CUtensorMap* mB1 = &p.mapB1[t.g];
-                const int akm = p.a_kmod[t.g], bkm = p.b_kmod[t.g];
-                const int akg = p.a_kgroup[t.g], akr = p.a_krep[t.g];
-                const int nstrip = SWIGLU ? 4 : p.nstrip;
-                const uint32_t stage_bytes = A_BYTES + nstrip * STRIP_BYTES;
-                for (int kb = t.kb0; kb < t.kb1; ++kb) {
+            for (int u = unit0; u < total && ok; u += ustep) {
+                const Unit t = decode_unit<PAIR>(u, p, total0, s_mtp, s_off);
+                const UnitCopies<SWIGLU, PAIR> cp(p, t, rank, bstrips);
+                // pair: the even CTA's barrier counts both CTAs' bytes
+                const uint32_t own = (cp.loadA ? A_BYTES : 0) + bstrips * STRIP_BYTES;
+                const uint32_t peer = (t.rows > BM ? A_BYTES : 0) + bstrips * STRIP_BYTES;
+                const uint32_t sub_bytes = PAIR ? own + peer : own;
+                for (int kb = t.kb0; kb < t.kb1; kb += G::KPS) {
+                    const int nk = min(G::KPS, t.kb1 - kb);
                     if (!bounded_wait(empty_bar(stage), phase ^ 1u, wc)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t sA = sbase + stage * STAGE_BYTES;
-                    const uint32_t sB = sA + A_BYTES;
-                    const uint32_t fb = full_bar(stage);
-                    const int kc = kb * BK;
-                    int kca = akm ? kc % akm : kc;
-                    if (akg) kca = ((kb / (akg * akr)) * akg + kb % akg) * BK;
-                    const int kcb = bkm ? kc % bkm : kc;
-                    mbar_expect_tx(fb, stage_bytes);
-                    tma_load_2d(sA, mA, kca, t.row0, fb);
-                    if (p.b_wide[t.g]) {
-                        const int sn = t.n0 >> 6;
-                        tma_load_4d(sB, mB0, 0, kcb, sn, t.zb, fb);
-                        if (SWIGLU) tma_load_4d(sB + 2 * STRIP_BYTES, mB1, 0, kcb, sn, t.zb, fb);
-                    } else if (SWIGLU) {
-                        tma_load_3d(sB, mB0, t.n0, kcb, t.zb, fb);
-                        tma_load_3d(sB + STRIP_BYTES, mB0, t.n0 + 64, kcb, t.zb, fb);
-                        tma_load_3d(sB + 2 * STRIP_BYTES, mB1, t.n0, kcb, t.zb, fb);
-                        tma_load_3d(sB + 3 * STRIP_BYTES, mB1, t.n0 + 64, kcb, t.zb, fb);
-                    } else {
-                        for (int j = 0; j < nstrip; ++j)
-                            tma_load_3d(sB + j * STRIP_BYTES, mB0, t.n0 + 64 * j, kcb, t.zb, fb);
+                    const uint32_t sS = sbase + stage * G::STAGE_BYTES;
+                    const uint32_t fb = PAIR ? map_shared_rank(full_bar(stage), 0) : full_bar(stage);
+                    if (rank == 0) mbar_expect_tx(full_bar(stage), nk * sub_bytes);
+                    for (int j = 0; j < nk; ++j) {
+                        const uint32_t sA = sS + j * G::SUB_BYTES;
+                        cp.issue(kb + j, sA, sA + A_BYTES, fb);
                     }
                     issued |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
@@ -275,59 +360,80 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
                     }
                 }
             }
-            // every copy this thread issued has landed before the CTA can exit
+            // every copy this thread issued has landed before the CTA can exit:
+            // its stage was filled (even CTA: the barrier counts both CTAs'
+            // bytes) or, in the odd CTA, consumed by the pair's MMAs
             for (int s = 0; s < STAGES; ++s)
                 if ((issued >> s) & 1u)
-                    bounded_drain(full_bar(s), (last_par >> s) & 1u, p.timeout_ns, p.err);
+                    bounded_drain(rank == 0 ? full_bar(s) : empty_bar(s), (last_par >> s) & 1u,
+                                  p.timeout_ns, p.err);
         }
+    } else if (warp == 1 && PAIR && rank == 1) {
+        // the odd CTA of a pair issues no MMAs
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer ----------------
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-                const Unit t = decode_unit<SWIGLU>(u, p, total0, s_mtp, s_off);
-                if (!bounded_wait(tempty_bar(acc), acc_phase ^ 1u, wc)) break;
+            for (int u = unit0; u < total && ok; u += ustep) {
+                const Unit t = decode_unit<PAIR>(u, p, total0, s_mtp, s_off);
+                if (!bounded_wait(tempty_bar(acc), acc_phase ^ 1u, wc, PAIR)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
-                for (int kb = t.kb0; kb < t.kb1; ++kb) {
-                    if (!bounded_wait(full_bar(stage), phase, wc)) {
+                for (int kb = t.kb0; kb < t.kb1; kb += G::KPS) {
+                    const int nk = min(G::KPS, t.kb1 - kb);
+                    if (!bounded_wait(full_bar(stage), phase, wc, PAIR)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sA = sbase + stage * STAGE_BYTES;
-                    const uint32_t sB = sA + A_BYTES;
+                    for (int j = 0; j < nk; ++j) {
+                        const uint32_t sA = sbase + stage * G::STAGE_BYTES + j * G::SUB_BYTES;
+                        const uint32_t sB = sA + A_BYTES;
 #pragma unroll
-                    for (int ks = 0; ks < BK / 16; ++ks) {
-                        const uint64_t ad = smem_desc_sw128(sA + ks * 32, 16, 1024);
-                        const uint64_t bd = smem_desc_sw128(sB + ks * 2048, STRIP_BYTES, 1024);
-                        tc_mma_bf16(d_tmem, ad, bd, p.idesc, (kb != t.kb0 || ks != 0) ? 1u : 0u);
+                        for (int ks = 0; ks < BK / 16; ++ks) {
+                            const uint64_t ad = smem_desc_sw128(sA + ks * 32, 16, 1024);
+                            const uint64_t bd = smem_desc_sw128(sB + ks * 2048, STRIP_BYTES, 1024);
+                            const uint32_t accum = (kb != t.kb0 || j != 0 || ks != 0) ? 1u : 0u;
+                            if (PAIR)
+                                tc_mma_bf16_pair(d_tmem, ad, bd, p.idesc, accum);
+                            else
+                                tc_mma_bf16(d_tmem, ad, bd, p.idesc, accum);
+                        }
                     }
-                    tc_commit(empty_bar(stage));
+                    if (PAIR)
+                        tc_commit_pair_mc(empty_bar(stage), 3);
+                    else
+                        tc_commit(empty_bar(stage));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit(tfull_bar(acc));
+                if (PAIR)
+                    tc_commit_pair_mc(tfull_bar(acc), 3);
+                else
+                    tc_commit(tfull_bar(acc));
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             }
-            tc_commit(drain_bar);
+            if (PAIR)
+                tc_commit_pair(drain_bar);
+            else
+                tc_commit(drain_bar);
             bounded_drain(drain_bar, 0, p.timeout_ns, p.err);
         }
     } else {
         // ---------------- epilogue warps 2..9 ----------------
         const int q = warp & 3;          // TMEM lane quarter this warp may access
         const int half = (warp - 2) >> 2;  // which half of the tile's columns
-        uint4* stg = reinterpret_cast<uint4*>(smem + STG_OFF + (warp - 2) * STG_BYTES);
+        uint4* stg = reinterpret_cast<uint4*>(smem + G::STG_OFF + (warp - 2) * STG_BYTES);
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int u = blockIdx.x; u < total; u += gridDim.x) {
-            const Unit t = decode_unit<SWIGLU>(u, p, total0, s_mtp, s_off);
+        for (int u = unit0; u < total; u += ustep) {
+            const Unit t = decode_unit<PAIR>(u, p, total0, s_mtp, s_off);
             int ok = 1;
             if (lane == 0) ok = bounded_wait(tfull_bar(acc), acc_phase, wc) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -335,16 +441,21 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
             tc_fence_after();
             const uint32_t tb =
                 tmem_base + static_cast<uint32_t>(acc * ACC_COLS) + (static_cast<uint32_t>(q * 32) << 16);
-            const int valid_rows = t.rows - q * 32;  // rows of this warp's 32 that exist
-            const size_t orow = static_cast<size_t>(t.out_row0 + q * 32 + lane);
+            // this CTA's rows of the unit, then this warp's 32 of them
+            const int my_rows = min(BM, t.rows - rank * BM);
+            const int valid_rows = my_rows - q * 32;
+            const int my_out0 = t.out_row0 + rank * BM;
+            const size_t orow = static_cast<size_t>(my_out0 + q * 32 + lane);
             const int N = p.N[t.g];
             const int ld = p.out_ld[t.g];
             const int of32 = p.out_f32[t.g];
             const size_t es = of32 ? 4 : 2;
             const size_t pitch = static_cast<size_t>(ld) * es;
             char* out_rows = static_cast<char*>(p.out[t.g]) +
-                             static_cast<size_t>(t.out_row0 + q * 32) * pitch;
-            if (SWIGLU) {
+                             static_cast<size_t>(my_out0 + q * 32) * pitch;
+            if (valid_rows <= 0) {
+                // none of this warp's 32 rows exist (the odd CTA of a short pair unit)
+            } else if (SWIGLU) {
                 // 2 blocks of 32 BF16 columns per warp
 #pragma unroll 1
                 for (int c = half * 64; c < half * 64 + 64; c += 32) {
@@ -428,17 +539,35 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (lane == 0) {
+                if (PAIR && rank == 1)
+                    mbar_arrive_remote(map_shared_rank(tempty_bar(acc), 0));
+                else
+                    mbar_arrive(tempty_bar(acc));
+            }
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
     }
 
-    __syncthreads();
-    if (warp == 1) {
+    if (PAIR) {
+        // no CTA of the pair leaves while the other may still touch its
+        // shared memory, barriers or tensor memory
         __syncwarp();
-        tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        tc_fence_before();
+        cluster_sync();
+        if (warp == 1) {
+            __syncwarp();
+            tc_fence_after();
+            tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        }
+    } else {
+        __syncthreads();
+        if (warp == 1) {
+            __syncwarp();
+            tc_fence_after();
+            tmem_dealloc(tmem_base, TMEM_COLS);
+        }
     }
 }
 
@@ -470,26 +599,64 @@ bool make_B_map(CUtensorMap* m, const void* B, int Z, int K, int N) {
     return encode_tmap(m, B, 3, dims, strides, box);
 }
 
-template <bool SWIGLU>
-cudaError_t launch_tc_t(const TcGemmArgs& a, cudaStream_t s) {
+template <bool SWIGLU, bool PAIR>
+bool prepare_kernel(int dev) {
     static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(tc_grouped_gemm_kernel<SWIGLU>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return false;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(tc_grouped_gemm_kernel<SWIGLU, PAIR>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Geo<PAIR>::SMEM_BYTES) != cudaSuccess)
+            return false;
         attr_set[dev] = true;
     }
+    return true;
+}
+
+// How many CTA pairs of the pair kernel fit on the device at once (0: none,
+// or the query failed; the single-CTA form is used then).
+template <bool SWIGLU>
+int pair_slots(int dev) {
+    static int cache[64] = {};
+    if (dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int n = -1;
+        if (prepare_kernel<SWIGLU, true>(dev)) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2 * static_cast<unsigned>(num_sms()));
+            cfg.blockDim = dim3(THREADS);
+            cfg.dynamicSmemBytes = Geo<true>::SMEM_BYTES;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int c = 0;
+            if (cudaOccupancyMaxActiveClusters(&c, tc_grouped_gemm_kernel<SWIGLU, true>, &cfg) ==
+                    cudaSuccess &&
+                c > 0)
+                n = c;
+            else
+                cudaGetLastError();  // clear a failed query
+        }
+        cache[dev] = n;
+    }
+    return cache[dev] > 0 ? cache[dev] : 0;
+}
+
+template <bool SWIGLU, bool PAIR>
+cudaError_t launch_tc_t(const TcGemmArgs& a, int nstrip, int slots, cudaStream_t s) {
+    constexpr int UROWS = PAIR ? 2 * BM : BM;
     TcParams p;
     memset(&p, 0, sizeof(p));
-    int nmax = 0;
-    for (int g = 0; g < 2; ++g)
-        if (a.g[g].enabled && a.g[g].N > nmax) nmax = a.g[g].N;
-    p.nstrip = SWIGLU ? 4 : (nmax >= 256 ? 4 : (nmax + 63) / 64);
+    p.nstrip = nstrip;
     p.bno = SWIGLU ? 128 : 64 * p.nstrip;
-    p.idesc = idesc_bf16_f32(128, 64 * p.nstrip, /*b_mn_major=*/1);
+    p.idesc = idesc_bf16_f32(PAIR ? 2 * BM : BM, 64 * p.nstrip, /*b_mn_major=*/1);
     const int BNO = p.bno;
+    // strips of B one CTA loads per stage
+    const int strips = PAIR ? (SWIGLU ? 2 : nstrip / 2) : (SWIGLU ? 2 : nstrip);
     long long units_bound = 0;
     for (int g = 0; g < 2; ++g) {
         const TcGroup& G = a.g[g];
@@ -500,7 +667,6 @@ cudaError_t launch_tc_t(const TcGemmArgs& a, cudaStream_t s) {
         if ((G.a_kmod && G.a_kmod % BK) || (G.b_kmod && G.b_kmod % BK)) return cudaErrorInvalidValue;
         if (G.ksplit > 1 && (g != 1 || G.Z != 1)) return cudaErrorInvalidValue;
         if (!make_A_map(&p.mapA[g], G.A, G.rows, KA, G.lda)) return cudaErrorInvalidValue;
-        const int strips = SWIGLU ? 2 : p.nstrip;
         p.b_wide[g] = G.N % 64 == 0 && make_B_strip_map(&p.mapB0[g], G.B0, G.Z, KB, G.N, strips) &&
                       (!SWIGLU || make_B_strip_map(&p.mapB1[g], G.B1, G.Z, KB, G.N, strips));
         if (!p.b_wide[g]) {
@@ -525,31 +691,55 @@ cudaError_t launch_tc_t(const TcGemmArgs& a, cudaStream_t s) {
         p.out_ld[g] = G.out_ld;
         p.out_f32[g] = G.out_f32;
         if (g == 0)
-            units_bound += static_cast<long long>((G.rows + BM - 1) / BM + a.E) * p.nt[0];
+            units_bound += static_cast<long long>((G.rows + UROWS - 1) / UROWS + a.E) * p.nt[0];
         else
-            units_bound += static_cast<long long>((G.rows + BM - 1) / BM) *
+            units_bound += static_cast<long long>((G.rows + UROWS - 1) / UROWS) *
                            (p.ksplit1 > 1 ? p.ksplit1 : G.Z) * p.nt[1];
     }
     p.E = a.E;
-    p.mt1 = a.g[1].enabled ? (a.g[1].rows + BM - 1) / BM : 0;
+    p.mt1 = a.g[1].enabled ? (a.g[1].rows + UROWS - 1) / UROWS : 0;
     p.offsets = a.offsets;
-    p.mt_prefix = a.mt_prefix;
+    p.mt_prefix = a.mt_prefix ? a.mt_prefix + (PAIR ? a.E + 1 : 0) : nullptr;
     p.rowscale0 = a.rowscale0;
     p.addend = a.addend;
     p.add_ld = a.add_ld;
     p.err = a.err;
     p.timeout_ns = wait_timeout_ns();
-    long long grid = num_sms();
+    long long grid = slots;  // persistent: one CTA (pair) per slot, at most one per unit
     if (units_bound < grid) grid = units_bound;
     if (grid < 1) grid = 1;
-    return launch_pdl(tc_grouped_gemm_kernel<SWIGLU>, dim3(static_cast<unsigned>(grid)),
-                      dim3(THREADS), SMEM_BYTES, s, p);
+    if (PAIR)
+        return launch_pdl_cluster(tc_grouped_gemm_kernel<SWIGLU, true>,
+                                  dim3(2 * static_cast<unsigned>(grid)), dim3(THREADS),
+                                  Geo<true>::SMEM_BYTES, s, 2, p);
+    return launch_pdl(tc_grouped_gemm_kernel<SWIGLU, false>, dim3(static_cast<unsigned>(grid)),
+                      dim3(THREADS), Geo<false>::SMEM_BYTES, s, p);
+}
+
+template <bool SWIGLU>
+cudaError_t launch_tc_s(const TcGemmArgs& a, cudaStream_t s) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int nmax = 0;
+    for (int g = 0; g < 2; ++g)
+        if (a.g[g].enabled && a.g[g].N > nmax) nmax = a.g[g].N;
+    const int nstrip = SWIGLU ? 4 : (nmax >= 256 ? 4 : (nmax + 63) / 64);
+    // The pair form splits B's strips between the two CTAs (an even count).
+    // Its routed tiles are 256 rows, so a segment wastes 128 padded rows on
+    // average instead of 64: it is used when segments average >= 512 rows.
+    const bool even = SWIGLU || nstrip % 2 == 0;
+    const bool long_segments =
+        !a.g[0].enabled || static_cast<long long>(a.g[0].rows) >= 512LL * (a.E > 0 ? a.E : 1);
+    const int slots = (even && long_segments) ? pair_slots<SWIGLU>(dev) : 0;
+    if (slots > 0) return launch_tc_t<SWIGLU, true>(a, nstrip, slots, s);
+    if (!prepare_kernel<SWIGLU, false>(dev)) return cudaErrorInvalidValue;
+    return launch_tc_t<SWIGLU, false>(a, nstrip, num_sms(), s);
 }
 
 }  // namespace
 
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t s) {
-    return a.swiglu ? launch_tc_t<true>(a, s) : launch_tc_t<false>(a, s);
+    return a.swiglu ? launch_tc_s<true>(a, s) : launch_tc_s<false>(a, s);
 }
 
 }  // namespace moe

@@ -33,6 +33,27 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     note_launch();
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
+// The same with thread-block clusters of `cluster_x` CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                               cudaStream_t s, int cluster_x, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    note_launch();
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 // Wait limit of device-side bounded waits, in ns.
 uint64_t wait_timeout_ns();
 // Number of SMs of the current device (cached per device).
@@ -42,7 +63,7 @@ int num_sms();
 // Workspace layout. Every region is 256-byte aligned; offsets in bytes.
 // ---------------------------------------------------------------------------
 constexpr int DISPATCH_CHUNK = 1024;   // assignments per dispatch CTA
-constexpr int TC_BM = 128;             // rows per tcgen05 GEMM tile
+constexpr int TC_BM = 128;             // rows per tcgen05 GEMM tile of one CTA (a pair: 2 TC_BM)
 constexpr int SIMT_BM = 64;            // rows per FP32 SIMT GEMM tile
 constexpr int ROUTER_CHUNK = 256;      // tensor-core router: reduction chunk per split-K slice
 
@@ -149,7 +170,7 @@ struct TcGemmArgs {
     TcGroup g[2];
     int E;                       // group 0 segment count
     const int32_t* offsets;      // group 0 [E+1]
-    const int32_t* mt_prefix;    // group 0 [E+1], m-tiles of TC_BM rows
+    const int32_t* mt_prefix;    // group 0 [2(E+1)]: tiles of TC_BM rows, then of 2 TC_BM rows
     int swiglu;                  // 1: h = SiLU(A B0) * (A B1); 0: single product
     const float* rowscale0;      // group 0: multiply row r by rowscale0[r]
     const float* addend;         // group 1: add addend[r, col] (FP32 [rows1, add_ld])
