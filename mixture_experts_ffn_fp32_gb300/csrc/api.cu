@@ -312,6 +312,7 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
     da.sorted_w = sorted_w;
     da.inv = inv;
     da.err = err;
+    da.ticket = err + 1;
     if ((e = launch_dispatch(da, s, nullptr)) != cudaSuccess) return cuda_status(e);
     rec.end(ST_DISPATCH);
 
@@ -531,8 +532,10 @@ MOE_API moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, 
     da.mt_prefix = reinterpret_cast<int32_t*>(b + L.mt_prefix);
     da.sorted_token = sorted_token; da.sorted_w = sorted_w; da.inv = inv;
     da.err = reinterpret_cast<int*>(b + L.err);
+    da.ticket = da.err + 1;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(da.err, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
+    // the error word and the dispatch ticket start at zero
+    if (cudaMemsetAsync(da.err, 0, 2 * sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
     return cuda_status(launch_dispatch(da, s, nullptr));
 }
 

@@ -8,43 +8,19 @@
 // assignment at position pos belongs to token order[pos] // K, bincount gives
 // the expert loads and their cumulative sums the expert slices.
 //
-// Here the stable argsort is a counting sort done in three launches with no
+// Here the stable argsort is a counting sort done in two launches with no
 // host synchronisation: (a) each CTA histograms a chunk of 1024 consecutive
-// flat assignments, (b) one CTA turns the chunk histograms into per-expert
-// offsets and per-chunk bases (and the per-expert GEMM m-tile prefix), (c)
-// each CTA ranks its chunk's assignments stably (warp match + per-warp
-// counts) and writes sorted_token / sorted_w / inv. Integer arithmetic only,
-// so the result is bit-exact and independent of scheduling.
+// flat assignments, and the CTA that finishes last (a ticket counter) turns
+// the chunk histograms into per-expert offsets and per-chunk bases (and the
+// per-expert GEMM tile prefixes), (b) each CTA ranks its chunk's assignments
+// stably (warp match + per-warp counts) and writes sorted_token / sorted_w /
+// inv. Integer arithmetic only, so the result is bit-exact and independent of
+// scheduling.
 #include "common.cuh"
 #include "internal.h"
 
 namespace moe {
 namespace {
-
-__global__ void __launch_bounds__(256) dispatch_count_kernel(const int32_t* __restrict__ idx,
-                                                             int TK, int E,
-                                                             int32_t* __restrict__ chunk_counts,
-                                                             int* err) {
-    pdl_wait();
-    pdl_trigger();
-    __shared__ int hist[256];
-    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
-    __syncthreads();
-    const int j0 = blockIdx.x * DISPATCH_CHUNK;
-    const int j1 = min(j0 + DISPATCH_CHUNK, TK);
-    bool bad = false;
-    for (int j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
-        const int e = idx[j];
-        if (e >= 0 && e < E)
-            atomicAdd(&hist[e], 1);
-        else
-            bad = true;
-    }
-    if (bad) atomicOr(err, ERRBIT_INDEX);
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-        chunk_counts[static_cast<size_t>(blockIdx.x) * E + e] = hist[e];
-}
 
 // Exclusive scan of v over the 256 threads of the block (all threads call).
 __device__ int block_exclusive_scan(int v, int* warp_tot) {
@@ -73,20 +49,27 @@ __device__ int block_exclusive_scan(int v, int* warp_tot) {
     return excl;
 }
 
-__global__ void __launch_bounds__(256) dispatch_scan_kernel(
-    const int32_t* __restrict__ chunk_counts, int nchunks, int E, int TK, int bm,
-    int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-    int32_t* __restrict__ mt_prefix) {
-    pdl_wait();
-    pdl_trigger();
+// Per-expert offsets, per-chunk bases and GEMM tile prefixes from the chunk
+// histograms (one CTA of 256 threads, thread e = expert e). The histograms
+// were written by other CTAs of the same grid: read through L2 (ld.cg).
+__device__ void dispatch_scan(const int32_t* chunk_counts, int nchunks, int E, int bm,
+                              int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts,
+                              int32_t* __restrict__ offsets, int32_t* __restrict__ mt_prefix) {
     __shared__ int warp_tot[8];
     const int e = threadIdx.x;
+    // 8 histogram loads in flight per step rather than one round trip per chunk
+    auto load8 = [&](int b0, int (&c)[8]) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            c[i] = (b0 + i < nchunks) ? __ldcg(chunk_counts + static_cast<size_t>(b0 + i) * E + e) : 0;
+    };
     int running = 0;
     if (e < E) {
-        for (int b = 0; b < nchunks; ++b) {
-            const int c = chunk_counts[static_cast<size_t>(b) * E + e];
-            chunk_base[static_cast<size_t>(b) * E + e] = running;
-            running += c;
+        for (int b0 = 0; b0 < nchunks; b0 += 8) {
+            int c[8];
+            load8(b0, c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) running += c[i];
         }
     }
     const int cnt = (e < E) ? running : 0;
@@ -101,14 +84,61 @@ __global__ void __launch_bounds__(256) dispatch_scan_kernel(
         offsets[e] = off;
         mt_prefix[e] = mtoff;
         mt_prefix[E + 1 + e] = mtoff2;
-        for (int b = 0; b < nchunks; ++b) chunk_base[static_cast<size_t>(b) * E + e] += off;
+        // chunk b of expert e starts after the expert's earlier chunks
+        int base = off;
+        for (int b0 = 0; b0 < nchunks; b0 += 8) {
+            int c[8];
+            load8(b0, c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (b0 + i < nchunks) chunk_base[static_cast<size_t>(b0 + i) * E + e] = base;
+                base += c[i];
+            }
+        }
     }
     if (e == E - 1) {
         offsets[E] = off + cnt;
         mt_prefix[E] = mtoff + mt;
         mt_prefix[2 * E + 1] = mtoff2 + mt2;
     }
-    (void)TK;
+}
+
+// (a): histogram of one chunk; the last CTA to finish then runs the scan and
+// re-arms the ticket (zero) for the next dispatch.
+__global__ void __launch_bounds__(256) dispatch_count_kernel(
+    const int32_t* __restrict__ idx, int TK, int E, int nchunks, int bm,
+    int32_t* __restrict__ chunk_counts, int32_t* __restrict__ chunk_base,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ mt_prefix,
+    int* ticket, int* err) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ int hist[256];
+    __shared__ int is_last;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    const int j0 = blockIdx.x * DISPATCH_CHUNK;
+    const int j1 = min(j0 + DISPATCH_CHUNK, TK);
+    bool bad = false;
+    for (int j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
+        const int e = idx[j];
+        if (e >= 0 && e < E)
+            atomicAdd(&hist[e], 1);
+        else
+            bad = true;
+    }
+    if (bad) atomicOr(err, ERRBIT_INDEX);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        chunk_counts[static_cast<size_t>(blockIdx.x) * E + e] = hist[e];
+    // publish this chunk's histogram, then take a ticket
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) is_last = atomicAdd(ticket, 1) == nchunks - 1;
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    if (threadIdx.x == 0) *ticket = 0;
+    dispatch_scan(chunk_counts, nchunks, E, bm, chunk_base, counts, offsets, mt_prefix);
 }
 
 __global__ void __launch_bounds__(DISPATCH_CHUNK) dispatch_scatter_kernel(
@@ -157,7 +187,16 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
     const int lane = threadIdx.x & 31;
     const size_t s = static_cast<size_t>(rowidx[r]) * vec_per_row;
     const size_t d = static_cast<size_t>(r) * vec_per_row;
-    for (int v = lane; v < vec_per_row; v += 32) dst[d + v] = __ldg(src + s + v);
+    // 4 loads per lane in flight before their stores
+    for (int v0 = lane; v0 < vec_per_row; v0 += 128) {
+        uint4 buf[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (v0 + 32 * i < vec_per_row) buf[i] = __ldg(src + s + v0 + 32 * i);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (v0 + 32 * i < vec_per_row) dst[d + v0 + 32 * i] = buf[i];
+    }
 }
 
 // K5 - combine: out[t, c] = sum_k ys[inv[t, k], c] (+ addend[t, c]) in FP32, k in
@@ -285,14 +324,12 @@ cudaError_t launch_gather_sum_split(const float* ys, const int32_t* inv, int T, 
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s, int* n_launched) {
     const int TK = a.T * a.K;
     cudaError_t e = launch_pdl(dispatch_count_kernel, dim3(a.nchunks), dim3(256), 0, s, a.idx, TK,
-                               a.E, a.chunk_counts, a.err);
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(256), 0, s, a.chunk_counts, a.nchunks, a.E,
-                   TK, a.bm, a.chunk_base, a.counts, a.offsets, a.mt_prefix);
+                               a.E, a.nchunks, a.bm, a.chunk_counts, a.chunk_base, a.counts,
+                               a.offsets, a.mt_prefix, a.ticket, a.err);
     if (e != cudaSuccess) return e;
     e = launch_pdl(dispatch_scatter_kernel, dim3(a.nchunks), dim3(DISPATCH_CHUNK), 0, s, a.idx, a.w,
                    TK, a.K, a.E, a.chunk_base, a.sorted_token, a.sorted_w, a.inv);
-    if (n_launched) *n_launched = 3;
+    if (n_launched) *n_launched = 2;
     return e;
 }
 

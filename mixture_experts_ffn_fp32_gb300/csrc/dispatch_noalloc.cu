@@ -27,7 +27,7 @@ constexpr int NOALLOC_MAX_TK = 65536;
 constexpr int NOALLOC_MAX_E = 256;
 constexpr int NOALLOC_CHUNKS = NOALLOC_MAX_TK / DISPATCH_CHUNK;
 
-// [0, 64): error word (cleared at the start of every call)
+// [0, 64): error word and dispatch ticket (cleared at the start of every call)
 // then chunk_counts and chunk_base [NOALLOC_CHUNKS * E], then mt_prefix [2 (E + 1)]
 constexpr size_t NOALLOC_WORDS =
     64 + 2 * static_cast<size_t>(NOALLOC_CHUNKS) * NOALLOC_MAX_E + 2 * (NOALLOC_MAX_E + 1);
@@ -75,8 +75,9 @@ MOE_API moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* to
     int32_t* base = scratch_address(&e);
     if (base == nullptr) return MOE_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the error word must start at zero; everything else is fully rewritten
-    if (cudaMemsetAsync(base, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+    // the error word and the dispatch ticket must start at zero; everything
+    // else is fully rewritten
+    if (cudaMemsetAsync(base, 0, 2 * sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
     const int nchunks = static_cast<int>((TK + DISPATCH_CHUNK - 1) / DISPATCH_CHUNK);
     DispatchArgs da{};
     da.idx = topk_idx;
@@ -95,5 +96,6 @@ MOE_API moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* to
     da.sorted_w = sorted_w;
     da.inv = inv;
     da.err = base;
+    da.ticket = base + 1;
     return launch_dispatch(da, s, nullptr) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

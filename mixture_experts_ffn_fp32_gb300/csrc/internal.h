@@ -94,7 +94,8 @@ struct RouterArgs {
     float* margin;
     float* top_scores;
     float* scores;
-    int* err_clear;   // if set, block 0 zeroes this error word (first kernel of a forward)
+    int* err_clear;   // if set, block 0 zeroes this error word and the dispatch ticket after
+                      // it (first kernel of a forward)
 };
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
 // Tensor-core router pieces: W3 [3, d, E] BF16 = exact split of W [d, E];
@@ -121,6 +122,7 @@ struct DispatchArgs {
     float* sorted_w;
     int32_t* inv;
     int* err;
+    int* ticket;   // zero when no dispatch is running; the word after *err in a workspace
 };
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s, int* n_launched);
 

@@ -20,6 +20,12 @@ namespace moe {
 namespace {
 
 
+// The error word and the dispatch ticket that follows it start every forward at zero.
+MOE_DEV void clear_status(int* w) {
+    w[0] = 0;
+    w[1] = 0;
+}
+
 MOE_DEV float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -160,7 +166,7 @@ __global__ void __launch_bounds__(256) router_small_kernel(RouterArgs a) {
     extern __shared__ __align__(16) uint8_t xsm[];
     pdl_wait();
     pdl_trigger();
-    if (a.err_clear != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *a.err_clear = 0;
+    if (a.err_clear != nullptr && blockIdx.x == 0 && threadIdx.x == 0) clear_status(a.err_clear);
     const int E = a.E, d = a.d;
     const int t0 = blockIdx.x * 8;
     const int ntok = min(8, a.T - t0);
@@ -250,7 +256,7 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(RouterArgs a) {
     static_assert(RT_BT * EPAD <= RT_DK * EPAD, "logit tile must fit the W chunk buffer");
 
     const int tid = threadIdx.x;
-    if (a.err_clear != nullptr && blockIdx.x == 0 && tid == 0) *a.err_clear = 0;
+    if (a.err_clear != nullptr && blockIdx.x == 0 && tid == 0) clear_status(a.err_clear);
     const int tg = tid >> 6;   // token group: tokens tg*8 .. tg*8+7
     const int el = tid & 63;   // experts el + 64 i
     const int t0 = blockIdx.x * RT_BT;
@@ -336,7 +342,7 @@ __global__ void __launch_bounds__(256) router_split_kernel(const float* __restri
                                                            int* err_clear) {
     pdl_wait();
     pdl_trigger();
-    if (err_clear != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *err_clear = 0;
+    if (err_clear != nullptr && blockIdx.x == 0 && threadIdx.x == 0) clear_status(err_clear);
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= d * E) return;
     const int k = i / E, e = i - k * E;
@@ -360,7 +366,7 @@ __global__ void __launch_bounds__(256) route_from_logits_kernel(const float* __r
                                                                 int nsplit, RouterArgs a) {
     pdl_wait();
     pdl_trigger();
-    if (a.err_clear != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *a.err_clear = 0;
+    if (a.err_clear != nullptr && blockIdx.x == 0 && threadIdx.x == 0) clear_status(a.err_clear);
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (t >= a.T) return;
     const int lane = static_cast<int>(lane_id());

@@ -101,7 +101,8 @@ def test_full_size_sampled_rows(name):
                                       ("softmax_topk", 256, 8), ("softmax_all_renorm", 8, 2),
                                       ("softmax_all_renorm", 100, 7), ("sigmoid", 128, 8),
                                       ("sigmoid", 9, 8), ("softmax_topk", 33, 16),
-                                      ("sigmoid", 20, 1)])
+                                      ("sigmoid", 20, 1), ("sigmoid", 8, 3), ("softmax_topk", 5, 5),
+                                      ("softmax_all_renorm", 3, 1)])
 @pytest.mark.parametrize("dtype,d,with_ws", [("bf16", 272, False), ("f32", 272, False),
                                              ("bf16", 256, True), ("bf16", 1024, True)])
 def test_route(gate, E, K, dtype, d, with_ws):
