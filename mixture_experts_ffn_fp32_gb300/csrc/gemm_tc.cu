@@ -376,6 +376,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
+            // Descriptors of stage 0, k-block 0, k-step 0; the others differ only in
+            // the start-address field (16-byte units, no carry out of it below 256 KB).
+            const uint64_t adesc0 = smem_desc_sw128(sbase, 16, 1024);
+            const uint64_t bdesc0 = smem_desc_sw128(sbase + A_BYTES, STRIP_BYTES, 1024);
             for (int u = unit0; u < total && ok; u += ustep) {
                 const Unit t = decode_unit<PAIR>(u, p, total0, s_mtp, s_off);
                 if (!bounded_wait(tempty_bar(acc), acc_phase ^ 1u, wc, PAIR)) break;
@@ -388,18 +392,21 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
                         break;
                     }
                     tc_fence_after();
-                    for (int j = 0; j < nk; ++j) {
-                        const uint32_t sA = sbase + stage * G::STAGE_BYTES + j * G::SUB_BYTES;
-                        const uint32_t sB = sA + A_BYTES;
+                    const uint64_t soff = static_cast<uint64_t>(stage * G::STAGE_BYTES) >> 4;
+                    const uint32_t first = kb == t.kb0 ? 0u : 1u;  // 0: overwrite the accumulator
 #pragma unroll
-                        for (int ks = 0; ks < BK / 16; ++ks) {
-                            const uint64_t ad = smem_desc_sw128(sA + ks * 32, 16, 1024);
-                            const uint64_t bd = smem_desc_sw128(sB + ks * 2048, STRIP_BYTES, 1024);
-                            const uint32_t accum = (kb != t.kb0 || j != 0 || ks != 0) ? 1u : 0u;
-                            if (PAIR)
-                                tc_mma_bf16_pair(d_tmem, ad, bd, p.idesc, accum);
-                            else
-                                tc_mma_bf16(d_tmem, ad, bd, p.idesc, accum);
+                    for (int j = 0; j < G::KPS; ++j) {
+                        if (j < nk) {
+#pragma unroll
+                            for (int ks = 0; ks < BK / 16; ++ks) {
+                                const uint64_t ad = adesc0 + soff + (j * G::SUB_BYTES + ks * 32) / 16;
+                                const uint64_t bd = bdesc0 + soff + (j * G::SUB_BYTES + ks * 2048) / 16;
+                                const uint32_t accum = (j != 0 || ks != 0) ? 1u : first;
+                                if (PAIR)
+                                    tc_mma_bf16_pair(d_tmem, ad, bd, p.idesc, accum);
+                                else
+                                    tc_mma_bf16(d_tmem, ad, bd, p.idesc, accum);
+                            }
                         }
                     }
                     if (PAIR)
