@@ -156,6 +156,118 @@ MOE_DEV void route_token_warp(const float (&r)[J], int t, const RouterArgs& a) {
     if (a.margin != nullptr && lane == 0) a.margin[t] = (K < E) ? (vK1 - vK) : INFINITY;
 }
 
+// Routes token t in one thread from all E logits in r[0..E-1] (E <= EP <= 8):
+// the same selection, ranking and weights as route_token_warp, for small E
+// where one lane is cheaper than the warp-wide search.
+template <int EP>
+MOE_DEV void route_token_seq(const float (&r)[EP], int t, const RouterArgs& a) {
+    const int E = a.E, K = a.K;
+    float c[EP], sg[EP];
+#pragma unroll
+    for (int e = 0; e < EP; ++e) {
+        sg[e] = 0.0f;
+        c[e] = -INFINITY;
+        if (e < E) {
+            const float b = a.bias != nullptr ? a.bias[e] : 0.0f;
+            if (a.gate == MOE_GATE_SIGMOID) {
+                sg[e] = 1.0f / (1.0f + expf(-r[e]));
+                c[e] = sg[e] + b;
+            } else {
+                c[e] = r[e] + b;
+            }
+        }
+    }
+    if (a.gate == MOE_GATE_SOFTMAX_ALL_RENORM) {
+        float m = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < EP; ++e)
+            if (e < E) m = fmaxf(m, c[e]);
+        float sum = 0.0f;
+#pragma unroll
+        for (int e = 0; e < EP; ++e) {
+            c[e] = e < E ? expf(c[e] - m) : 0.0f;
+            sum += c[e];
+        }
+#pragma unroll
+        for (int e = 0; e < EP; ++e)
+            if (e < E) c[e] = c[e] / sum;
+    }
+    if (a.gate == MOE_GATE_SIGMOID && a.scores != nullptr) {
+#pragma unroll
+        for (int e = 0; e < EP; ++e)
+            if (e < E) a.scores[static_cast<size_t>(t) * E + e] = sg[e];
+    }
+#pragma unroll
+    for (int e = 0; e < EP; ++e)
+        if (!(c[e] == c[e])) c[e] = -INFINITY;
+    // rank of each expert: how many beat it (higher value, or equal value and
+    // lower id); slot k of the top-(K+1) holds the expert of rank k
+    int rank[EP];
+#pragma unroll
+    for (int e = 0; e < EP; ++e) {
+        rank[e] = EP;
+        if (e < E) {
+            int n = 0;
+#pragma unroll
+            for (int f = 0; f < EP; ++f)
+                if (f < E && (c[f] > c[e] || (c[f] == c[e] && f < e))) ++n;
+            rank[e] = n;
+        }
+    }
+    auto slot = [&](int k, float& v, int& id, float& sgv) {
+        v = 0.0f;
+        id = 0;
+        sgv = 0.0f;
+#pragma unroll
+        for (int e = 0; e < EP; ++e)
+            if (rank[e] == k) {
+                v = c[e];
+                id = e;
+                sgv = sg[e];
+            }
+    };
+    float v0, sg0;
+    int id0;
+    slot(0, v0, id0, sg0);
+    float sum = 0.0f;
+#pragma unroll
+    for (int k = 0; k < EP; ++k) {
+        if (k < K) {
+            float v, sgv;
+            int id;
+            slot(k, v, id, sgv);
+            sum += a.gate == MOE_GATE_SOFTMAX_TOPK ? expf(v - v0)
+                   : a.gate == MOE_GATE_SOFTMAX_ALL_RENORM ? v : sgv;
+        }
+    }
+    const bool normalise = a.gate != MOE_GATE_SIGMOID || a.renorm;
+#pragma unroll
+    for (int k = 0; k < EP + 1; ++k) {
+        if (k <= K && k < E) {
+            float v, sgv;
+            int id;
+            slot(k, v, id, sgv);
+            if (k < K) {
+                float wk = a.gate == MOE_GATE_SOFTMAX_TOPK ? expf(v - v0)
+                           : a.gate == MOE_GATE_SOFTMAX_ALL_RENORM ? v : sgv;
+                if (normalise) wk = wk / sum;
+                if (a.gate == MOE_GATE_SIGMOID) wk *= a.scale;
+                a.idx[static_cast<size_t>(t) * K + k] = id;
+                a.w[static_cast<size_t>(t) * K + k] = wk;
+            }
+            if (a.top_scores != nullptr && a.gate == MOE_GATE_SIGMOID)
+                a.top_scores[static_cast<size_t>(t) * (K + 1) + k] = v;
+        }
+    }
+    if (a.margin != nullptr) {
+        float vK1, vK, sgv;
+        int id;
+        slot(K - 1, vK1, id, sgv);
+        slot(K, vK, id, sgv);
+        a.margin[t] = (K < E) ? (vK1 - vK) : INFINITY;
+    }
+}
+
 // E <= 32: one warp per token, 8 tokens per CTA. The CTA first copies its 8
 // x rows into shared memory with all its loads in flight at once (one memory
 // round trip), then lane l of a warp takes the d-index pairs k0 + 2l, k0 + 2l + 1,
@@ -232,7 +344,12 @@ __global__ void __launch_bounds__(256) router_small_kernel(RouterArgs a) {
             for (int e = 0; e < EP; ++e) acc[e] = fmaf(x1[u], w1[u][e], fmaf(x0[u], w0[u][e], acc[e]));
     }
 #pragma unroll
-    for (int e = 0; e < EP; ++e) acc[e] = warp_sum(acc[e]);
+    for (int e = 0; e < EP; ++e) acc[e] = warp_sum(acc[e]);  // every lane: all E sums
+    if (EP <= 8) {
+        if (lane == 0) route_token_seq<(EP <= 8 ? EP : 8)>(
+            reinterpret_cast<const float(&)[(EP <= 8 ? EP : 8)]>(acc), t, a);
+        return;
+    }
     float r[1] = {0.0f};
 #pragma unroll
     for (int e = 0; e < EP; ++e)
