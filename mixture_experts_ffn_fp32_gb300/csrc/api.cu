@@ -108,6 +108,11 @@ bool router_on_tensor_cores(const moe_config& c) {
     return c.dtype == MOE_BF16 && c.E > 32 && c.E % 8 == 0 && c.d % ROUTER_CHUNK == 0;
 }
 
+// Up to 512 tokens and 128 experts the chunked FP32 router (two launches, no
+// split weights written) is as fast as the tensor-core router (three); with
+// more experts each of its threads walks a whole 256-long slice and it loses.
+bool router_chunked(const moe_config& c) { return c.E > 32 && c.E <= 128 && c.T <= 512; }
+
 int router_ksplit(int T, int d) {
     (void)T;
     return d / ROUTER_CHUNK;
@@ -166,9 +171,11 @@ WsLayout plan_workspace(const moe_config& c) {
     L.xstage = take(T * c.d * es);
     L.ostage = take(T * c.d * (c.out_dtype == MOE_BF16 ? 2 : 4));
     L.qb = take(E * 4);
-    const bool tcr = router_on_tensor_cores(c);
+    const bool chk = router_chunked(c);
+    const bool tcr = router_on_tensor_cores(c) && !chk;
     L.w3 = tcr ? take(3 * static_cast<size_t>(c.d) * E * 2) : 0;
-    L.rpart = tcr ? take(static_cast<size_t>(router_ksplit(c.T, c.d)) * T * E * 4) : 0;
+    const size_t nsplit = chk ? (c.d + ROUTER_CHUNK - 1) / ROUTER_CHUNK : router_ksplit(c.T, c.d);
+    L.rpart = (tcr || chk) ? take(nsplit * T * E * 4) : 0;
     L.total = o;
     return L;
 }
@@ -266,7 +273,11 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
     ra.margin = static_cast<float*>(P(L.margin));
     ra.top_scores = L.top_scores ? static_cast<float*>(P(L.top_scores)) : nullptr;
     ra.scores = L.scores ? static_cast<float*>(P(L.scores)) : nullptr;
-    if (router_on_tensor_cores(c)) {
+    if (router_chunked(c)) {
+        ra.err_clear = err;
+        if ((e = launch_router_chunked(ra, static_cast<float*>(P(L.rpart)), s)) != cudaSuccess)
+            return cuda_status(e);
+    } else if (router_on_tensor_cores(c)) {
         if ((e = launch_router_split(w.W_router, c.d, E, P(L.w3), err, s)) != cudaSuccess)
             return cuda_status(e);
         const int ks = router_ksplit(T, c.d);
@@ -493,6 +504,9 @@ MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const float* 
     ra.scores = scores;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (ws != nullptr) ra.err_clear = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + L.err);
+    if (ws != nullptr && router_chunked(*cfg))
+        return cuda_status(launch_router_chunked(
+            ra, reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.rpart), s));
     if (ws != nullptr && router_on_tensor_cores(*cfg)) {
         ra.err_clear = nullptr;
         uint8_t* b = static_cast<uint8_t*>(ws);

@@ -220,7 +220,8 @@ __global__ void __launch_bounds__(256) gather_sum_kernel(const float* __restrict
 #pragma unroll
     for (int k = 0; k < KMAX; ++k) pos[k] = (k < K) ? inv[static_cast<size_t>(t) * K + k] : 0;
     // NB column blocks of 256 per batch, every load of the batch issued before the sums
-    for (int cb = 0; cb < cols; cb += 256 * NB) {
+    // column batches; few tokens: the batches of a token spread over gridDim.y CTAs
+    for (int cb = blockIdx.y * 256 * NB; cb < cols; cb += gridDim.y * 256 * NB) {
         float4 y[NB][KMAX][2];
         float4 ad[NB][2];
 #pragma unroll
@@ -344,11 +345,17 @@ cudaError_t launch_gather_rows(const void* src, const int32_t* rowidx, int rows,
 cudaError_t launch_gather_sum(const float* ys, const int32_t* inv, int T, int K, int cols,
                               const float* addend, void* out, int out_bf16, cudaStream_t s) {
     const int blocks = (T * 32 + 255) / 256;
-    // about 16 float4 loads in flight per lane per batch
+    // about 16 float4 loads in flight per lane per batch; with few tokens the
+    // column batches go to separate CTAs so that at least ~2 CTAs per SM work
+    auto ysplit = [&](int nb) {
+        const int batches = (cols + 256 * nb - 1) / (256 * nb);
+        const int want = (2 * num_sms() + blocks - 1) / blocks;
+        return dim3(blocks, static_cast<unsigned>(batches < want ? batches : (want > 0 ? want : 1)));
+    };
 #define MOE_GS(KM, NB)                                                                            \
-    return out_bf16 ? launch_pdl(gather_sum_kernel<true, KM, NB>, dim3(blocks), dim3(256), 0, s, ys, \
+    return out_bf16 ? launch_pdl(gather_sum_kernel<true, KM, NB>, ysplit(NB), dim3(256), 0, s, ys, \
                                  inv, T, K, cols, addend, out)                                   \
-                    : launch_pdl(gather_sum_kernel<false, KM, NB>, dim3(blocks), dim3(256), 0, s, ys, \
+                    : launch_pdl(gather_sum_kernel<false, KM, NB>, ysplit(NB), dim3(256), 0, s, ys, \
                                  inv, T, K, cols, addend, out)
     if (K <= 2) MOE_GS(2, 4);
     if (K <= 4) MOE_GS(4, 2);

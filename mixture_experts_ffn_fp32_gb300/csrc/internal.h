@@ -106,6 +106,10 @@ cudaError_t launch_route_from_logits(const float* part, int nsplit, const Router
                                      cudaStream_t s);
 // Tensor-core router used when x is BF16, E > 32, E % 8 == 0 and d % ROUTER_CHUNK == 0.
 bool router_on_tensor_cores(const moe_config& c);
+// Few tokens and E > 32: FP32 partial logits per 256-long slice of d on many
+// CTAs, summed and routed by route_from_logits (needs a workspace's rpart).
+bool router_chunked(const moe_config& c);
+cudaError_t launch_router_chunked(const RouterArgs& a, float* part, cudaStream_t s);
 // Split-K slices of the tensor-core router GEMM (one per chunk of d).
 int router_ksplit(int T, int d);
 

@@ -502,6 +502,77 @@ __global__ void __launch_bounds__(256) route_from_logits_kernel(const float* __r
     route_token_warp<J>(r, t, a);
 }
 
+// Few tokens, E > 32: partial logits over 256-long slices of d, one CTA per
+// (8 tokens, slice) so that even a decode batch spreads over many SMs. The
+// CTA's threads are (expert e, part r): R = 256 / EP parts each take a
+// contiguous 256 / R run of the slice (W_router rows read coalesced across e,
+// 8 rows in flight), the 8 tokens' x slices sit in shared memory, and part 0
+// adds the R partial sums in order. route_from_logits_kernel sums the slices
+// in FP32 (as for the tensor-core router) and routes.
+template <bool BF16, int EP>
+__global__ void __launch_bounds__(256) router_chunk_kernel(RouterArgs a, float* __restrict__ part) {
+    constexpr int R = 256 / EP;            // parts per expert
+    constexpr int RUN = ROUTER_CHUNK / R;  // k values per part
+    pdl_wait();
+    pdl_trigger();
+    if (a.err_clear != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+        clear_status(a.err_clear);
+    __shared__ float xs[8][ROUTER_CHUNK];
+    __shared__ float red[R > 1 ? R - 1 : 1][8][EP];
+    const int t0 = blockIdx.x * 8, k0 = blockIdx.y * ROUTER_CHUNK;
+    const int kn = min(ROUTER_CHUNK, a.d - k0);
+    for (int i = threadIdx.x; i < 8 * ROUTER_CHUNK; i += blockDim.x) {
+        const int tt = i / ROUTER_CHUNK, k = i - tt * ROUTER_CHUNK;
+        float v = 0.0f;
+        if (t0 + tt < a.T && k < kn) {
+            const size_t off = static_cast<size_t>(t0 + tt) * a.d + k0 + k;
+            v = BF16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(a.x)[off])
+                     : static_cast<const float*>(a.x)[off];
+        }
+        xs[tt][k] = v;
+    }
+    __syncthreads();
+    const int e = threadIdx.x % EP, r = threadIdx.x / EP;
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    if (e < a.E) {
+        const int kb = r * RUN;
+        const int ke = min(kb + RUN, kn);
+        const float* w = a.W + static_cast<size_t>(k0) * a.E + e;
+        int k = kb;
+        for (; k + 8 <= ke; k += 8) {
+            float wv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) wv[i] = __ldg(w + static_cast<size_t>(k + i) * a.E);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] = fmaf(xs[j][k + i], wv[i], acc[j]);
+        }
+        for (; k < ke; ++k) {
+            const float wv = __ldg(w + static_cast<size_t>(k) * a.E);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = fmaf(xs[j][k], wv, acc[j]);
+        }
+    }
+    if (R > 1) {
+        if (r > 0)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) red[r - 1][j][e] = acc[j];
+        __syncthreads();
+        if (r == 0)
+            for (int q = 0; q < R - 1; ++q)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] += red[q][j][e];
+    }
+    if (r != 0 || e >= a.E) return;
+    float* dst = part + (static_cast<size_t>(blockIdx.y) * a.T + t0) * a.E + e;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        if (t0 + j < a.T) dst[static_cast<size_t>(j) * a.E] = acc[j];
+}
+
 template <bool BF16>
 cudaError_t launch_router_t(const RouterArgs& a, cudaStream_t s) {
     cudaError_t e = cudaSuccess;
@@ -549,6 +620,26 @@ cudaError_t launch_router_split(const float* W, int d, int E, void* W3, int* err
     const int n = d * E;
     return launch_pdl(router_split_kernel, dim3((n + 255) / 256), dim3(256), 0, s, W, d, E,
                       static_cast<__nv_bfloat16*>(W3), err_clear);
+}
+
+cudaError_t launch_router_chunked(const RouterArgs& a, float* part, cudaStream_t s) {
+    const int nsplit = (a.d + ROUTER_CHUNK - 1) / ROUTER_CHUNK;
+    const dim3 grid((a.T + 7) / 8, nsplit);
+    cudaError_t e;
+#define MOE_RC(EPV)                                                                                \
+    e = a.x_bf16 ? launch_pdl(router_chunk_kernel<true, EPV>, grid, dim3(256), 0, s, a, part)      \
+                 : launch_pdl(router_chunk_kernel<false, EPV>, grid, dim3(256), 0, s, a, part)
+    if (a.E <= 64)
+        MOE_RC(64);
+    else if (a.E <= 128)
+        MOE_RC(128);
+    else
+        MOE_RC(256);
+#undef MOE_RC
+    if (e != cudaSuccess) return e;
+    RouterArgs b = a;
+    b.err_clear = nullptr;  // cleared by the partial kernel; later bits must survive
+    return launch_route_from_logits(part, nsplit, b, s);
 }
 
 cudaError_t launch_route_from_logits(const float* part, int nsplit, const RouterArgs& a,

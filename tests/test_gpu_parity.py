@@ -124,6 +124,30 @@ def test_route(gate, E, K, dtype, d, with_ws):
     P.check_routing(w, ort, g, near)
 
 
+@pytest.mark.parametrize("gate,E,K", [("softmax_topk", 64, 8), ("softmax_topk", 256, 8),
+                                      ("sigmoid", 128, 8), ("softmax_all_renorm", 100, 7),
+                                      ("softmax_topk", 33, 16), ("sigmoid", 120, 4)])
+@pytest.mark.parametrize("dtype,d,T", [("bf16", 272, 200), ("f32", 1024, 64), ("bf16", 4096, 1)])
+def test_route_few_tokens(gate, E, K, dtype, d, T):
+    """Up to 512 tokens with 32 < E <= 128 and a workspace: the chunked FP32
+    router (partial logits per 256-long slice of d, summed in FP32), including
+    a ragged last slice (d = 272) and a single token; E = 256 takes the other
+    paths."""
+    A = api()
+    w = W.Workload("r", T=T, d=d, d_ff=16, E=E, K=K, n_shared=0, shared_d_ff=0, dtype=dtype,
+                   gate=gate, bias_std=0.02, skew=0.5 if gate != "sigmoid" else 0.0)
+    inp = W.make_inputs(w, device="cuda")
+    if gate == "sigmoid":
+        inp["bias"] = (torch.randn(E, generator=torch.Generator().manual_seed(6)) * 0.05).cuda()
+    spec = A.LayerSpec.of(w)
+    ws = A.alloc_workspace(spec)
+    g = A.route(spec, inp["x"], inp["W_router"], inp["bias"], ws=ws)
+    assert A.workspace_status(ws) == A.MOE_OK
+    ort = P.oracle_routing(w, inp)
+    near = ort["min_gap"] <= P.NEAR_TIE
+    P.check_routing(w, ort, g, near)
+
+
 @pytest.mark.parametrize("T,E,K,skew", [(1, 1, 1, 0.0), (3, 3, 2, 0.0), (1000, 8, 2, 0.0),
                                         (1500, 64, 8, 1.1), (4096, 256, 8, 1.2),
                                         (777, 256, 16, 0.0), (20000, 7, 3, 0.5),
