@@ -24,7 +24,10 @@ Sources, cited as page title + section:
   argsort dispatch, latent down/up projections, quantile balancer update.
 * [MoE-FS] "MoE from scratch" tutorial ("A working MoE layer in PyTorch"):
   ``SwiGLU``, ``MoELayer`` (softmax over all experts, top-K, renormalise,
-  sorted dispatch) and its ``naive_forward`` reference.
+  sorted dispatch, Switch load-balancing loss) and its ``naive_forward``
+  reference.
+* [BOOK-MoE] book-ai "Mixture of Experts" chapter, class ``MoELoss``:
+  ``router_z_loss`` (ST-MoE z-loss).
 
 Readings where the pages are silent or disagree (each is listed in the design doc):
 ties in top-K go to the lower expert index; slot k holds the k-th largest
@@ -438,3 +441,31 @@ def sign_bias_update(counts, N, K, bias, alpha):
     tau = 1.0 / E
     b = f64(bias) + alpha * np.sign(tau - f)
     return np.clip(b, -1.0, 1.0)
+
+
+# --------------------------------------------------------------------------
+# Routing diagnostics  [MoE-FS] MoELayer.forward (Switch load-balancing loss);
+#                      [BOOK-MoE] MoELoss.router_z_loss
+# --------------------------------------------------------------------------
+
+def routing_stats(r, idx, E):
+    """Diagnostics of one batch's routing from the raw router logits r [T, E]
+    (x W_router, no balance bias) and the selected experts idx [T, K]:
+
+      P_e  = (1/T) sum_t softmax(r_t)_e         mean router probability
+      f_e  = #{(t, k): idx[t, k] = e} / (T K)    share of the assignments
+      aux  = E * sum_e f_e P_e                   Switch loss before its alpha
+      z    = (1/T) sum_t (log sum_e exp r_te)^2  z-loss before its weight
+
+    Returns dict(aux, z, P, f)."""
+    r = f64(r)
+    idx = np.asarray(idx)
+    T = r.shape[0]
+    K = idx.shape[1]
+    m = r.max(axis=1, keepdims=True)
+    ex = np.exp(r - m)
+    p = ex / ex.sum(axis=1, keepdims=True)
+    lse = m[:, 0] + np.log(ex.sum(axis=1))
+    P = p.mean(axis=0)
+    f = np.bincount(idx.reshape(-1), minlength=E).astype(np.float64) / (T * K)
+    return {"aux": float(E * np.sum(f * P)), "z": float(np.mean(lse ** 2)), "P": P, "f": f}

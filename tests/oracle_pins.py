@@ -343,8 +343,49 @@ def pin_sign_bias_example(o):
     np.testing.assert_allclose(nb, [-1.0, 1.0, 0.1, 0.1], atol=1e-15)
 
 
+def pin_routing_stats(o):
+    """Switch loss and z-loss ([MoE-FS] MoELayer.forward, [BOOK-MoE]
+    router_z_loss) on cases fixed by the definitions: a zero router gives
+    P_e = 1/E, so aux = E * sum_e f_e / E = 1 for any routing and z = (ln E)^2;
+    all assignments on one expert with one-hot-like logits give aux -> E;
+    a 2-token, 2-expert hand example; shifting a token's logits by c leaves P
+    unchanged and moves its log-sum-exp by c."""
+    T, E, K = 6, 4, 2
+    idx = np.array([[0, 1], [0, 2], [3, 0], [1, 0], [2, 3], [0, 1]])
+    st = o.routing_stats(np.zeros((T, E)), idx, E)
+    assert abs(st["aux"] - 1.0) < 1e-15
+    assert abs(st["z"] - math.log(E) ** 2) < 1e-14
+    assert np.allclose(st["P"], 1.0 / E) and abs(st["f"].sum() - 1.0) < 1e-15
+    assert np.allclose(st["f"], np.array([5, 3, 2, 2]) / 12.0)
+    # everything on expert 0, router certain of it: aux -> E * 1 * 1 = E
+    big = np.zeros((5, E))
+    big[:, 0] = 60.0
+    st = o.routing_stats(big, np.zeros((5, 1), dtype=int), E)
+    assert abs(st["aux"] - E) < 1e-12
+    # hand example: r = [[ln 3, 0], [0, 0]], idx = [[0], [1]]
+    # softmax rows [3/4, 1/4] and [1/2, 1/2] -> P = [5/8, 3/8]; f = [1/2, 1/2]
+    # aux = 2 (5/16 + 3/16) = 1; lse = [ln 4, ln 2] -> z = ((ln 4)^2 + (ln 2)^2) / 2
+    st = o.routing_stats(np.array([[math.log(3.0), 0.0], [0.0, 0.0]]), np.array([[0], [1]]), 2)
+    assert np.allclose(st["P"], [5 / 8, 3 / 8], rtol=0, atol=1e-15)
+    assert abs(st["aux"] - 1.0) < 1e-15
+    assert abs(st["z"] - (math.log(4.0) ** 2 + math.log(2.0) ** 2) / 2) < 1e-14
+    # second hand example, unequal shares: r = [[ln 3, 0], [ln 3, 0]], idx = [[0], [0]]
+    # P = [3/4, 1/4], f = [1, 0] -> aux = 2 * 3/4 = 3/2
+    st = o.routing_stats(np.array([[math.log(3.0), 0.0]] * 2), np.array([[0], [0]]), 2)
+    assert abs(st["aux"] - 1.5) < 1e-15
+    # shift invariance of P; lse moves by the shift
+    rng = np.random.default_rng(9)
+    r = rng.normal(size=(7, 5))
+    a = o.routing_stats(r, np.zeros((7, 1), dtype=int), 5)
+    b = o.routing_stats(r + 2.5, np.zeros((7, 1), dtype=int), 5)
+    assert np.allclose(a["P"], b["P"], atol=1e-15)
+    lse = np.log(np.exp(r).sum(axis=1))
+    assert abs(a["z"] - np.mean(lse ** 2)) < 1e-12
+    assert abs(b["z"] - np.mean((lse + 2.5) ** 2)) < 1e-12
+
+
 ALL_PINS = [pin_silu_table, pin_swiglu_example, pin_ffn_down_projection, pin_router_example,
             pin_tie_break, pin_gate_formulas, pin_sigmoid_example, pin_stable_dispatch_example,
             pin_dispatch_vs_library, pin_counts_sum, pin_output_composition,
             pin_sorted_equals_naive, pin_shared_concat_identity, pin_latent_reduces_to_plain,
-            pin_quantile, pin_sign_bias_example]
+            pin_quantile, pin_sign_bias_example, pin_routing_stats]

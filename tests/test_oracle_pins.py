@@ -132,10 +132,33 @@ def _mut_sign_bias_flipped(m):
     m.sign_bias_update = lambda c, N, K, b, a: orig(c, N, K, b, -a)
 
 
+def _mut_aux_share_over_tokens(m):
+    orig = m.routing_stats
+
+    def stats(r, idx, E):
+        st = orig(r, idx, E)
+        K = np.asarray(idx).shape[1]
+        st["aux"] = st["aux"] * K  # f normalised by T instead of T*K
+        return st
+    m.routing_stats = stats
+
+
+def _mut_z_not_squared(m):
+    orig = m.routing_stats
+
+    def stats(r, idx, E):
+        st = orig(r, idx, E)
+        rr = np.asarray(r, float)
+        st["z"] = float(np.mean(np.log(np.exp(rr).sum(axis=1))))
+        return st
+    m.routing_stats = stats
+
+
 MUTANTS = [_mut_silu_sign, _mut_gate_up_swapped, _mut_down_transposed, _mut_softmax_over_all,
            _mut_tie_to_higher, _mut_dispatch_unstable, _mut_drop_shared,
            _mut_sigmoid_corrected_weights, _mut_quantile_lower, _mut_quantile_no_centre,
-           _mut_latent_no_up, _mut_sign_bias_flipped]
+           _mut_latent_no_up, _mut_sign_bias_flipped, _mut_aux_share_over_tokens,
+           _mut_z_not_squared]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)
