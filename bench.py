@@ -356,6 +356,29 @@ def run_ours(args, name):
         step()
     breakdown, nb = timer2.finish()
 
+    # routing diagnostics (Switch loss, z-loss; moe_routing_stats): their own
+    # pass, outside the timed forward region
+    diag = None
+    if world == 1:
+        dws = api.alloc_workspace(spec)
+        api.routing_stats(spec, inp["x"], inp["W_router"], inp["bias"], ws=dws, stream=stream)
+        d_ms = []
+        for i in range(min(args.steps, 10)):
+            flush.fill_(i & 0xFF)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            api.routing_stats(spec, inp["x"], inp["W_router"], inp["bias"], ws=dws,
+                              stream=stream, read=False)
+            b.record(stream)
+            torch.cuda.synchronize()
+            d_ms.append(a.elapsed_time(b))
+        g = api.routing_stats(spec, inp["x"], inp["W_router"], inp["bias"], ws=dws, stream=stream)
+        diag = {"ms": sum(d_ms) / len(d_ms), "aux": g["aux"], "z": g["z"],
+                "note": "moe_routing_stats (router + diagnostics reduction) timed alone with "
+                        "CUDA events, L2 flushed before each call"}
+        del dws
+
     # end to end through the host-buffer entry point (copies inside the timed region)
     e2e = None
     if not args.no_e2e:
@@ -414,6 +437,7 @@ def run_ours(args, name):
                      "avg_launch_ms": gu_ms, "flops_per_launch": gu_flops},
         "stage_ms": {k: v / max(1, nb) for k, v in breakdown.items() if v > 0},
         "stage_ms_note": "separate instrumented pass (an event between every stage)",
+        "routing_diagnostics": diag,
         "gpu_launches": int(launches),
         "wall_s_timed": t_wall,
         "clocks": clk,

@@ -235,6 +235,25 @@ moe_status moe_quantile_bias_update(int32_t T, int32_t E, int32_t K, const float
 /* Workspace bytes moe_quantile_bias_update needs on its own. */
 size_t moe_quantile_workspace_size(int32_t T, int32_t E);
 
+/* Routing diagnostics of one batch: runs the router of cfg on x (as
+ * moe_route with a workspace; its selection and logits stay in ws) and
+ * writes to out (device, FP32, 2 + E values):
+ *     out[0] = aux = E * sum_e f_e P_e      Switch load-balancing loss before
+ *                                           its alpha ("MoE from scratch",
+ *                                           MoELayer.forward)
+ *     out[1] = z = (1/T) sum_t (log sum_e exp r_te)^2   router z-loss before
+ *                                           its weight (book-ai MoE chapter,
+ *                                           MoELoss.router_z_loss)
+ *     out[2 + e] = P_e = (1/T) sum_t softmax(r_t)_e
+ * with r = x W_router the raw FP32 logits (no balance bias) and f_e the share
+ * of the T*K selected (token, slot) pairs on expert e (the selection uses the
+ * bias, as the forward's does). Sums run in a fixed order: the result is
+ * reproducible bit for bit. ws: required, at least moe_workspace_size(cfg)
+ * bytes, 256-byte aligned; x and W_router 16-byte aligned. */
+moe_status moe_routing_stats(const moe_config* cfg, const void* x, const float* W_router,
+                             const float* bias, float* out, void* ws, size_t ws_bytes,
+                             void* stream);
+
 /* Sign-bias balancing (APEX-1 Math Ref Part 3, section 14.3): with
  * f_e = counts[e] / (N K) and tau = 1/E,
  *     bias[e] <- clamp(bias[e] + alpha * sign(tau - f_e), -1, 1)

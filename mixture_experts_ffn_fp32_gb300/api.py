@@ -79,6 +79,7 @@ def lib() -> ctypes.CDLL:
             "moe_quantile_bias_update": (ctypes.c_int, [i32, i32, i32, vp, vp, vp, vp, sz, vp]),
             "moe_quantile_workspace_size": (sz, [i32, i32]),
             "moe_sign_bias_update": (ctypes.c_int, [i32, i32, i32, vp, vp, ctypes.c_float, vp]),
+            "moe_routing_stats": (ctypes.c_int, [cfgp, vp, vp, vp, vp, vp, sz, vp]),
             "moe_workspace_status": (ctypes.c_int, [vp, vp]),
             "moe_timing_begin": (ctypes.c_int, [i32, ctypes.c_uint32]),
             "moe_timing_end": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float), i32,
@@ -357,6 +358,25 @@ def quantile_bias_update(top_scores: torch.Tensor, scores: torch.Tensor, K: int,
                                           bias.data_ptr(), ws.data_ptr(), ws.numel(),
                                           _stream(stream)), "moe_quantile_bias_update")
     return bias
+
+
+def routing_stats(spec: LayerSpec, x: torch.Tensor, W_router: torch.Tensor, bias=None,
+                  ws: torch.Tensor | None = None, stream=None, read: bool = True) -> dict:
+    """Switch load-balancing loss (before alpha), router z-loss (before its
+    weight) and mean router probabilities of one batch (moe_routing_stats).
+    Returns dict(out [2+E] device tensor, ws) and, with read=True (waits for
+    the stream), aux, z and P [E] on the host."""
+    ws = alloc_workspace(spec, x.device) if ws is None else ws
+    out = torch.empty(2 + spec.E, dtype=torch.float32, device=x.device)
+    _check(lib().moe_routing_stats(ctypes.byref(spec.config()), _ptr(x), _ptr(W_router),
+                                   _ptr(bias), _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_routing_stats")
+    res = {"out": out, "ws": ws}
+    if read:
+        (stream if stream is not None else torch.cuda.current_stream()).synchronize()
+        vals = out.cpu()
+        res.update(aux=float(vals[0]), z=float(vals[1]), P=vals[2:])
+    return res
 
 
 def sign_bias_update(counts: torch.Tensor, N: int, K: int, bias: torch.Tensor, alpha: float,

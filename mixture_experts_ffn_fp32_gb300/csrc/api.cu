@@ -176,6 +176,8 @@ WsLayout plan_workspace(const moe_config& c) {
     L.w3 = tcr ? take(3 * static_cast<size_t>(c.d) * E * 2) : 0;
     const size_t nsplit = chk ? (c.d + ROUTER_CHUNK - 1) / ROUTER_CHUNK : router_ksplit(c.T, c.d);
     L.rpart = (tcr || chk) ? take(nsplit * T * E * 4) : 0;
+    L.logits = take(T * E * 4);
+    L.stats_part = take(((T + STATS_TOKENS - 1) / STATS_TOKENS) * (2 * E + 1) * 4);
     L.total = o;
     return L;
 }
@@ -481,6 +483,42 @@ MOE_API moe_status moe_get_workspace_views(const moe_config* cfg, void* ws, moe_
     return MOE_OK;
 }
 
+// The router of cfg on x into ra's outputs (ws optional: with it, the
+// workspace error word is cleared and the chunked or tensor-core paths may run).
+static moe_status run_router(const moe_config& c, RouterArgs ra, const float* W_router,
+                             const void* x, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
+    if (ws != nullptr) ra.err_clear = reinterpret_cast<int*>(ws + L.err);
+    if (ws != nullptr && router_chunked(c))
+        return cuda_status(launch_router_chunked(ra, reinterpret_cast<float*>(ws + L.rpart), s));
+    if (ws != nullptr && router_on_tensor_cores(c)) {
+        ra.err_clear = nullptr;
+        int* err = reinterpret_cast<int*>(ws + L.err);
+        cudaError_t e;
+        if ((e = launch_router_split(W_router, c.d, c.E, ws + L.w3, err, s)) != cudaSuccess)
+            return cuda_status(e);
+        const int ks = router_ksplit(c.T, c.d);
+        TcGemmArgs g{};
+        g.g[1] = router_group(x, c.T, c.d, c.E, ws + L.w3, ws + L.rpart);
+        g.err = err;
+        if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
+        return cuda_status(
+            launch_route_from_logits(reinterpret_cast<const float*>(ws + L.rpart), ks, ra, s));
+    }
+    return cuda_status(launch_router(ra, s));
+}
+
+static RouterArgs router_args(const moe_config& c, const void* x, const float* W_router,
+                              const float* bias) {
+    RouterArgs ra{};
+    ra.x = x;
+    ra.x_bf16 = c.dtype == MOE_BF16;
+    ra.W = W_router;
+    ra.bias = bias;
+    ra.T = c.T; ra.d = c.d; ra.E = c.E; ra.K = c.K; ra.gate = c.gate;
+    ra.renorm = c.renormalize; ra.scale = c.routed_scale;
+    return ra;
+}
+
 MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const float* W_router,
                              const float* bias, int32_t* topk_idx, float* topk_w, float* margin,
                              float* top_scores, float* scores, void* ws, size_t ws_bytes,
@@ -492,37 +530,37 @@ MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const float* 
     if (ws != nullptr && (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOE_ERR_INVALID_ARG;
     const WsLayout L = plan_workspace(*cfg);
     if (ws != nullptr && ws_bytes < L.total) return MOE_ERR_WORKSPACE;
-    RouterArgs ra{};
-    ra.x = x;
-    ra.x_bf16 = cfg->dtype == MOE_BF16;
-    ra.W = W_router;
-    ra.bias = bias;
-    ra.T = cfg->T; ra.d = cfg->d; ra.E = cfg->E; ra.K = cfg->K; ra.gate = cfg->gate;
-    ra.renorm = cfg->renormalize; ra.scale = cfg->routed_scale;
+    RouterArgs ra = router_args(*cfg, x, W_router, bias);
     ra.idx = topk_idx; ra.w = topk_w; ra.margin = margin;
     ra.top_scores = top_scores;
     ra.scores = scores;
+    return run_router(*cfg, ra, W_router, x, static_cast<uint8_t*>(ws), L,
+                      static_cast<cudaStream_t>(stream));
+}
+
+MOE_API moe_status moe_routing_stats(const moe_config* cfg, const void* x, const float* W_router,
+                                     const float* bias, float* out, void* ws, size_t ws_bytes,
+                                     void* stream) {
+    if (!cfg || !x || !W_router || !out || !ws) return MOE_ERR_INVALID_ARG;
+    const moe_status v = validate_config(*cfg);
+    if (v != MOE_OK) return v;
+    if (!aligned16(x) || !aligned16(W_router) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return MOE_ERR_INVALID_ARG;
+    const WsLayout L = plan_workspace(*cfg);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    RouterArgs ra = router_args(*cfg, x, W_router, bias);
+    ra.idx = reinterpret_cast<int32_t*>(b + L.topk_idx);
+    ra.w = reinterpret_cast<float*>(b + L.topk_w);
+    ra.margin = reinterpret_cast<float*>(b + L.margin);
+    ra.top_scores = L.top_scores ? reinterpret_cast<float*>(b + L.top_scores) : nullptr;
+    ra.scores = L.scores ? reinterpret_cast<float*>(b + L.scores) : nullptr;
+    ra.logits = reinterpret_cast<float*>(b + L.logits);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (ws != nullptr) ra.err_clear = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + L.err);
-    if (ws != nullptr && router_chunked(*cfg))
-        return cuda_status(launch_router_chunked(
-            ra, reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.rpart), s));
-    if (ws != nullptr && router_on_tensor_cores(*cfg)) {
-        ra.err_clear = nullptr;
-        uint8_t* b = static_cast<uint8_t*>(ws);
-        int* err = reinterpret_cast<int*>(b + L.err);
-        cudaError_t e;
-        if ((e = launch_router_split(W_router, cfg->d, cfg->E, b + L.w3, err, s)) != cudaSuccess)
-            return cuda_status(e);
-        const int ks = router_ksplit(cfg->T, cfg->d);
-        TcGemmArgs g{};
-        g.g[1] = router_group(x, cfg->T, cfg->d, cfg->E, b + L.w3, b + L.rpart);
-        g.err = err;
-        if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
-        return cuda_status(
-            launch_route_from_logits(reinterpret_cast<const float*>(b + L.rpart), ks, ra, s));
-    }
-    return cuda_status(launch_router(ra, s));
+    const moe_status st = run_router(*cfg, ra, W_router, x, b, L, s);
+    if (st != MOE_OK) return st;
+    return cuda_status(launch_routing_stats(ra.logits, ra.idx, cfg->T, cfg->E, cfg->K,
+                                            reinterpret_cast<float*>(b + L.stats_part), out, s));
 }
 
 MOE_API moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const float* topk_w,

@@ -13,6 +13,16 @@
 //
 // Sign-bias balancer (APEX-1 Mathematical Reference Part 3, section 14.3):
 // f_e = c_e / (N K), tau = 1/E, b_e <- clamp(b_e + alpha sign(tau - f_e), -1, 1).
+//
+// Routing diagnostics: the Switch load-balancing loss of "MoE from scratch"
+// (MoELayer.forward: f_e = share of the T*K assignments on expert e, P_e =
+// mean softmax router probability, aux = E sum_e f_e P_e before its alpha) and
+// the router z-loss of the book-ai MoE chapter (MoELoss.router_z_loss: mean
+// over tokens of the squared log-sum-exp of the logits, before its weight),
+// from the raw FP32 logits the router wrote. Two fixed-order passes, so the
+// result does not depend on scheduling: per CTA of STATS_TOKENS tokens the
+// probability sums, expert counts and squared log-sum-exps; then one CTA adds
+// the partials in CTA order.
 #include <math.h>
 
 #include "common.cuh"
@@ -127,6 +137,115 @@ __global__ void wait_selftest_kernel(int* err, unsigned long long timeout_ns) {
     __syncthreads();
 }
 
+MOE_DEV float stats_warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+MOE_DEV float stats_warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Partial sums of one CTA: 8 warps x STATS_TOKENS / 8 consecutive tokens each,
+// lane l holds experts l + 32 j. part row: [P sums (E), counts (E), sum lse^2].
+template <int J>
+__global__ void __launch_bounds__(256) stats_partial_kernel(const float* __restrict__ logits,
+                                                            const int32_t* __restrict__ idx, int T,
+                                                            int E, int K, float* __restrict__ part) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ float wsum[8][32 * J];
+    __shared__ float wz[8];
+    __shared__ int cnt[32 * J];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int e = threadIdx.x; e < 32 * J; e += blockDim.x) cnt[e] = 0;
+    __syncthreads();
+    float ps[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) ps[j] = 0.0f;
+    float zs = 0.0f;
+    constexpr int PER_WARP = STATS_TOKENS / 8;
+    const int tw = blockIdx.x * STATS_TOKENS + warp * PER_WARP;
+    for (int i = 0; i < PER_WARP; ++i) {
+        const int t = tw + i;
+        if (t >= T) break;
+        float r[J], m = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const int e = lane + 32 * j;
+            r[j] = e < E ? logits[static_cast<size_t>(t) * E + e] : -INFINITY;
+            m = fmaxf(m, r[j]);
+        }
+        m = stats_warp_max(m);
+        float ex[J], sum = 0.0f;
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            ex[j] = lane + 32 * j < E ? expf(r[j] - m) : 0.0f;
+            sum += ex[j];
+        }
+        sum = stats_warp_sum(sum);
+#pragma unroll
+        for (int j = 0; j < J; ++j) ps[j] += ex[j] / sum;
+        const float lse = m + logf(sum);
+        zs += lse * lse;
+        if (lane < K) {
+            const int e = idx[static_cast<size_t>(t) * K + lane];
+            if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j) wsum[warp][lane + 32 * j] = ps[j];
+    if (lane == 0) wz[warp] = zs;
+    __syncthreads();
+    float* row = part + static_cast<size_t>(blockIdx.x) * (2 * E + 1);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        float acc = 0.0f;
+        for (int w = 0; w < 8; ++w) acc += wsum[w][e];
+        row[e] = acc;
+        row[E + e] = static_cast<float>(cnt[e]);
+    }
+    if (threadIdx.x == 0) {
+        float z = 0.0f;
+        for (int w = 0; w < 8; ++w) z += wz[w];
+        row[2 * E] = z;
+    }
+}
+
+// out = [aux, z, P_0 .. P_{E-1}] from the partial rows, added in CTA order.
+__global__ void __launch_bounds__(256) stats_final_kernel(const float* __restrict__ part, int nblk,
+                                                          int T, int E, int K, float* __restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ float red[8];
+    const int e = threadIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const size_t stride = 2 * static_cast<size_t>(E) + 1;
+    float P = 0.0f, fP = 0.0f;
+    if (e < E) {
+        long long c = 0;
+        for (int b = 0; b < nblk; ++b) {
+            P += part[b * stride + e];
+            c += static_cast<long long>(part[b * stride + E + e]);
+        }
+        P /= static_cast<float>(T);
+        const float f = static_cast<float>(static_cast<double>(c) / (static_cast<double>(T) * K));
+        fP = f * P;
+        out[2 + e] = P;
+    }
+    fP = stats_warp_sum(fP);
+    if (lane == 0) red[warp] = fP;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float a = 0.0f;
+        for (int w = 0; w < 8; ++w) a += red[w];
+        out[0] = static_cast<float>(E) * a;
+        float z = 0.0f;
+        for (int b = 0; b < nblk; ++b) z += part[b * stride + 2 * E];
+        out[1] = z / static_cast<float>(T);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_quantile(int T, int E, int K, const float* top_scores, const float* scores,
@@ -149,6 +268,22 @@ cudaError_t launch_sign_bias(int E, int N, int K, const int32_t* counts, float* 
     sign_bias_kernel<<<(E + 255) / 256, 256, 0, s>>>(E, N, K, counts, bias, alpha);
     note_launch();
     return cudaGetLastError();
+}
+
+cudaError_t launch_routing_stats(const float* logits, const int32_t* idx, int T, int E, int K,
+                                 float* part, float* out, cudaStream_t s) {
+    const int nblk = (T + STATS_TOKENS - 1) / STATS_TOKENS;
+    cudaError_t e;
+    if (E <= 32)
+        e = launch_pdl(stats_partial_kernel<1>, dim3(nblk), dim3(256), 0, s, logits, idx, T, E, K, part);
+    else if (E <= 64)
+        e = launch_pdl(stats_partial_kernel<2>, dim3(nblk), dim3(256), 0, s, logits, idx, T, E, K, part);
+    else if (E <= 128)
+        e = launch_pdl(stats_partial_kernel<4>, dim3(nblk), dim3(256), 0, s, logits, idx, T, E, K, part);
+    else
+        e = launch_pdl(stats_partial_kernel<8>, dim3(nblk), dim3(256), 0, s, logits, idx, T, E, K, part);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(stats_final_kernel, dim3(1), dim3(256), 0, s, part, nblk, T, E, K, out);
 }
 
 cudaError_t launch_wait_selftest(int* err, uint64_t timeout_ns, cudaStream_t s) {

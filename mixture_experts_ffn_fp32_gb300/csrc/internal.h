@@ -72,6 +72,7 @@ struct WsLayout {
     size_t chunk_counts, chunk_base, counts, offsets, mt_prefix;
     size_t sorted_token, sorted_w, inv;
     size_t xs, z, h, hs, ys, routed, shout, xstage, ostage, qb, w3, rpart;
+    size_t logits, stats_part;  // routing diagnostics: r [T, E], per-CTA partial sums
     size_t total;
     int nchunks;
 };
@@ -96,6 +97,7 @@ struct RouterArgs {
     float* scores;
     int* err_clear;   // if set, block 0 zeroes this error word and the dispatch ticket after
                       // it (first kernel of a forward)
+    float* logits;    // if set: the raw FP32 logits r [T, E] (routing diagnostics)
 };
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
 // Tensor-core router pieces: W3 [3, d, E] BF16 = exact split of W [d, E];
@@ -210,6 +212,11 @@ struct SimtGemmArgs {
     int ys_ld, Kr;
 };
 cudaError_t launch_simt_gemm(const SimtGemmArgs& a, cudaStream_t s);
+
+// ---- routing diagnostics -----------------------------------------------------
+constexpr int STATS_TOKENS = 64;  // tokens per CTA of the partial-sum kernel
+cudaError_t launch_routing_stats(const float* logits, const int32_t* idx, int T, int E, int K,
+                                 float* part, float* out, cudaStream_t s);
 
 // ---- balancers --------------------------------------------------------------
 cudaError_t launch_quantile(int T, int E, int K, const float* top_scores, const float* scores,

@@ -42,6 +42,11 @@ template <int J>
 MOE_DEV void route_token_warp(const float (&r)[J], int t, const RouterArgs& a) {
     const int lane = static_cast<int>(lane_id());
     const int E = a.E, K = a.K;
+    if (a.logits != nullptr) {
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+            if (lane + 32 * j < E) a.logits[static_cast<size_t>(t) * E + lane + 32 * j] = r[j];
+    }
     float c[J], s[J];
 #pragma unroll
     for (int j = 0; j < J; ++j) {
@@ -162,6 +167,11 @@ MOE_DEV void route_token_warp(const float (&r)[J], int t, const RouterArgs& a) {
 template <int EP>
 MOE_DEV void route_token_seq(const float (&r)[EP], int t, const RouterArgs& a) {
     const int E = a.E, K = a.K;
+    if (a.logits != nullptr) {
+#pragma unroll
+        for (int e = 0; e < EP; ++e)
+            if (e < E) a.logits[static_cast<size_t>(t) * E + e] = r[e];
+    }
     float c[EP], sg[EP];
 #pragma unroll
     for (int e = 0; e < EP; ++e) {

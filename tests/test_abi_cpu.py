@@ -104,6 +104,15 @@ def test_host_side_rejections_do_not_touch_the_gpu(api):
     assert L.moe_quantile_bias_update(8, 16, 2, fake, fake, fake, fake, 4, None) == \
         api.MOE_ERR_WORKSPACE
     assert L.moe_sign_bias_update(0, 8, 2, fake, fake, 0.1, None) == api.MOE_ERR_INVALID_ARG
+    # routing diagnostics: workspace and output are required, sizes checked
+    assert L.moe_routing_stats(ctypes.byref(cfg), fake, fake, None, None, fake, 1 << 30, None) == \
+        api.MOE_ERR_INVALID_ARG
+    assert L.moe_routing_stats(ctypes.byref(cfg), fake, fake, None, fake, None, 0, None) == \
+        api.MOE_ERR_INVALID_ARG
+    assert L.moe_routing_stats(ctypes.byref(cfg), fake, fake, None, fake, fake, 8, None) == \
+        api.MOE_ERR_WORKSPACE
+    assert L.moe_routing_stats(ctypes.byref(bad), fake, fake, None, fake, fake, 1 << 30, None) == \
+        api.MOE_ERR_INVALID_ARG
     assert L.moe_timing_end(None, 0, None, None) == api.MOE_ERR_INVALID_ARG
     assert api.launch_count() == 0
 

@@ -148,6 +148,37 @@ def test_route_few_tokens(gate, E, K, dtype, d, T):
     P.check_routing(w, ort, g, near)
 
 
+@pytest.mark.parametrize("gate,E,K,T,d,dtype", [
+    ("softmax_topk", 4, 2, 4096, 768, "bf16"),       # the 4096-token layer's router
+    ("softmax_all_renorm", 8, 2, 300, 96, "f32"),
+    ("softmax_topk", 64, 8, 200, 272, "bf16"),       # chunked router
+    ("softmax_topk", 256, 8, 1030, 512, "bf16"),     # tensor-core router, ragged CTA tail
+    ("sigmoid", 128, 8, 777, 256, "bf16"),
+    ("softmax_topk", 16, 4, 1, 64, "f32")])
+def test_routing_stats(gate, E, K, T, d, dtype):
+    """Switch loss, z-loss and mean probabilities against the oracle's
+    routing_stats on the GPU's own selection (f is a count of it), and
+    reproducible bit for bit."""
+    A = api()
+    w = W.Workload("s", T=T, d=d, d_ff=16, E=E, K=K, n_shared=0, shared_d_ff=0, dtype=dtype,
+                   gate=gate, bias_std=0.02, skew=0.5 if gate != "sigmoid" else 0.0)
+    inp = W.make_inputs(w, device="cuda")
+    spec = A.LayerSpec.of(w)
+    g = A.routing_stats(spec, inp["x"], inp["W_router"], inp["bias"])
+    assert A.workspace_status(g["ws"]) == A.MOE_OK
+    gidx = P.npi(A.workspace_views(spec, g["ws"])["idx"])
+    # the selection itself matches the oracle's outside near ties
+    ort = P.oracle_routing(w, inp)
+    near = ort["min_gap"] <= P.NEAR_TIE
+    assert (gidx[~near] == ort["idx"][~near]).all()
+    ref = O.routing_stats(ort["logits"], gidx, E)
+    assert abs(g["aux"] - ref["aux"]) <= 2e-5 * max(1.0, abs(ref["aux"]))
+    assert abs(g["z"] - ref["z"]) <= 2e-5 * max(1.0, abs(ref["z"]))
+    np.testing.assert_allclose(P.np64(g["P"]), ref["P"], atol=2e-6, rtol=2e-5)
+    g2 = A.routing_stats(spec, inp["x"], inp["W_router"], inp["bias"], ws=g["ws"])
+    assert torch.equal(g["out"], g2["out"])
+
+
 @pytest.mark.parametrize("T,E,K,skew", [(1, 1, 1, 0.0), (3, 3, 2, 0.0), (1000, 8, 2, 0.0),
                                         (1500, 64, 8, 1.1), (4096, 256, 8, 1.2),
                                         (777, 256, 16, 0.0), (20000, 7, 3, 0.5),
