@@ -68,6 +68,20 @@ SMALL = {
     "bf16_e256": W.Workload("t_b11", T=96, d=128, d_ff=128, E=256, K=8, n_shared=1,
                             shared_d_ff=128, dtype="bf16", gate="softmax_topk", bias_std=0.01,
                             skew=1.2),
+    # Segments averaging >= 512 rows: the grouped GEMMs run as CTA pairs (256-row
+    # tiles). Skew leaves some experts with fewer than 128 rows (the odd CTA of
+    # a pair has no rows), widths that are not multiples of 64 take the per-strip
+    # copies, and reduction lengths of 3.25 / 2.75 k-blocks end on a half-full
+    # two-k-block stage.
+    "pair_skew": W.Workload("t_p1", T=1200, d=256, d_ff=384, E=4, K=2, n_shared=1,
+                            shared_d_ff=256, dtype="bf16", gate="softmax_topk", bias_std=0.01,
+                            skew=1.5),
+    "pair_ragged_widths": W.Workload("t_p2", T=1100, d=208, d_ff=176, E=2, K=1, n_shared=1,
+                                     shared_d_ff=144, dtype="bf16", gate="softmax_topk",
+                                     bias_std=0.01),
+    "pair_latent_sigmoid": W.Workload("t_p3", T=1024, d=256, d_ff=192, E=4, K=2, n_shared=1,
+                                      shared_d_ff=256, dtype="bf16", gate="sigmoid",
+                                      latent_dim=128),
 }
 
 
