@@ -109,8 +109,9 @@ bool router_on_tensor_cores(const moe_config& c) {
 }
 
 // Up to 512 tokens and 128 experts the chunked FP32 router (two launches, no
-// split weights written) is as fast as the tensor-core router (three); with
-// more experts each of its threads walks a whole 256-long slice and it loses.
+// split weights written, many CTAs even for a decode batch) is as fast as the
+// tensor-core router (three launches). With 256 experts its logit-sum kernel,
+// one warp per token over 8 experts x d/64 slices per lane, is the slower one.
 bool router_chunked(const moe_config& c) { return c.E > 32 && c.E <= 128 && c.T <= 512; }
 
 int router_ksplit(int T, int d) {
@@ -174,7 +175,7 @@ WsLayout plan_workspace(const moe_config& c) {
     const bool chk = router_chunked(c);
     const bool tcr = router_on_tensor_cores(c) && !chk;
     L.w3 = tcr ? take(3 * static_cast<size_t>(c.d) * E * 2) : 0;
-    const size_t nsplit = chk ? (c.d + ROUTER_CHUNK - 1) / ROUTER_CHUNK : router_ksplit(c.T, c.d);
+    const size_t nsplit = chk ? router_chunked_nsplit(c.d, c.E) : router_ksplit(c.T, c.d);
     L.rpart = (tcr || chk) ? take(nsplit * T * E * 4) : 0;
     L.logits = take(T * E * 4);
     L.stats_part = take(((T + STATS_TOKENS - 1) / STATS_TOKENS) * (2 * E + 1) * 4);

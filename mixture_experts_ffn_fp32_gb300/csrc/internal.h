@@ -112,6 +112,7 @@ bool router_on_tensor_cores(const moe_config& c);
 // CTAs, summed and routed by route_from_logits (needs a workspace's rpart).
 bool router_chunked(const moe_config& c);
 cudaError_t launch_router_chunked(const RouterArgs& a, float* part, cudaStream_t s);
+int router_chunked_nsplit(int d, int E);  // slices of the chunked router
 // Split-K slices of the tensor-core router GEMM (one per chunk of d).
 int router_ksplit(int T, int d);
 

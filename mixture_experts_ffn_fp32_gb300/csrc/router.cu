@@ -504,35 +504,46 @@ __global__ void __launch_bounds__(256) route_from_logits_kernel(const float* __r
         const int e = lane + 32 * j;
         float v = 0.0f;
         if (e < a.E) {
+            // slices in order, 8 loads in flight per step
             const float* p = part + static_cast<size_t>(t) * a.E + e;
-            for (int s = 0; s < nsplit; ++s) v += p[s * slice];
+            for (int s0 = 0; s0 < nsplit; s0 += 8) {
+                float q[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) q[i] = s0 + i < nsplit ? p[(s0 + i) * slice] : 0.0f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (s0 + i < nsplit) v += q[i];
+            }
         }
         r[j] = v;
     }
     route_token_warp<J>(r, t, a);
 }
 
-// Few tokens, E > 32: partial logits over 256-long slices of d, one CTA per
-// (8 tokens, slice) so that even a decode batch spreads over many SMs. The
-// CTA's threads are (expert e, part r): R = 256 / EP parts each take a
-// contiguous 256 / R run of the slice (W_router rows read coalesced across e,
-// 8 rows in flight), the 8 tokens' x slices sit in shared memory, and part 0
-// adds the R partial sums in order. route_from_logits_kernel sums the slices
-// in FP32 (as for the tensor-core router) and routes.
+// Few tokens, E > 32: partial logits over slices of d, one CTA per (8 tokens,
+// slice) so that even a decode batch spreads over many SMs. The CTA's threads
+// are (expert e, part r): R = 256 / EP parts each take a contiguous run of 64
+// of the slice's CHUNK_LEN(EP) = 64 R values (W_router rows read coalesced
+// across e, 8 rows in flight), the 8 tokens' x slices sit in shared memory,
+// and part 0 adds the R partial sums in order. route_from_logits_kernel sums
+// the slices in FP32 and routes.
+__host__ __device__ constexpr int router_chunk_len(int EP) { return 64 * (256 / EP); }
+
 template <bool BF16, int EP>
 __global__ void __launch_bounds__(256) router_chunk_kernel(RouterArgs a, float* __restrict__ part) {
     constexpr int R = 256 / EP;            // parts per expert
-    constexpr int RUN = ROUTER_CHUNK / R;  // k values per part
+    constexpr int LEN = router_chunk_len(EP);
+    constexpr int RUN = LEN / R;           // k values per part (64)
     pdl_wait();
     pdl_trigger();
     if (a.err_clear != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
         clear_status(a.err_clear);
-    __shared__ float xs[8][ROUTER_CHUNK];
+    __shared__ float xs[8][LEN];
     __shared__ float red[R > 1 ? R - 1 : 1][8][EP];
-    const int t0 = blockIdx.x * 8, k0 = blockIdx.y * ROUTER_CHUNK;
-    const int kn = min(ROUTER_CHUNK, a.d - k0);
-    for (int i = threadIdx.x; i < 8 * ROUTER_CHUNK; i += blockDim.x) {
-        const int tt = i / ROUTER_CHUNK, k = i - tt * ROUTER_CHUNK;
+    const int t0 = blockIdx.x * 8, k0 = blockIdx.y * LEN;
+    const int kn = min(LEN, a.d - k0);
+    for (int i = threadIdx.x; i < 8 * LEN; i += blockDim.x) {
+        const int tt = i / LEN, k = i - tt * LEN;
         float v = 0.0f;
         if (t0 + tt < a.T && k < kn) {
             const size_t off = static_cast<size_t>(t0 + tt) * a.d + k0 + k;
@@ -632,8 +643,13 @@ cudaError_t launch_router_split(const float* W, int d, int E, void* W3, int* err
                       static_cast<__nv_bfloat16*>(W3), err_clear);
 }
 
+int router_chunked_nsplit(int d, int E) {
+    const int len = router_chunk_len(E <= 64 ? 64 : (E <= 128 ? 128 : 256));
+    return (d + len - 1) / len;
+}
+
 cudaError_t launch_router_chunked(const RouterArgs& a, float* part, cudaStream_t s) {
-    const int nsplit = (a.d + ROUTER_CHUNK - 1) / ROUTER_CHUNK;
+    const int nsplit = router_chunked_nsplit(a.d, a.E);
     const dim3 grid((a.T + 7) / 8, nsplit);
     cudaError_t e;
 #define MOE_RC(EPV)                                                                                \

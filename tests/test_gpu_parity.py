@@ -144,9 +144,9 @@ def test_route(gate, E, K, dtype, d, with_ws):
 @pytest.mark.parametrize("dtype,d,T", [("bf16", 272, 200), ("f32", 1024, 64), ("bf16", 4096, 1)])
 def test_route_few_tokens(gate, E, K, dtype, d, T):
     """Up to 512 tokens with 32 < E <= 128 and a workspace: the chunked FP32
-    router (partial logits per 256-long slice of d, summed in FP32), including
-    a ragged last slice (d = 272) and a single token; E = 256 takes the other
-    paths."""
+    router (partial logits per slice of d, 256 long for E <= 64 and 128 long for
+    E <= 128, summed in FP32), including ragged last slices and a single token;
+    E = 256 takes the tensor-core or tiled router."""
     A = api()
     w = W.Workload("r", T=T, d=d, d_ff=16, E=E, K=K, n_shared=0, shared_d_ff=0, dtype=dtype,
                    gate=gate, bias_std=0.02, skew=0.5 if gate != "sigmoid" else 0.0)
