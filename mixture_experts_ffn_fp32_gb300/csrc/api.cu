@@ -240,6 +240,42 @@ static moe_status check_weights(const moe_config& c, const moe_weights* w) {
     return MOE_OK;
 }
 
+// The router of cfg on x into ra's outputs (ws optional: with it, the
+// workspace error word is cleared and the chunked or tensor-core paths may run).
+static moe_status run_router(const moe_config& c, RouterArgs ra, const float* W_router,
+                             const void* x, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
+    if (ws != nullptr) ra.err_clear = reinterpret_cast<int*>(ws + L.err);
+    if (ws != nullptr && router_chunked(c))
+        return cuda_status(launch_router_chunked(ra, reinterpret_cast<float*>(ws + L.rpart), s));
+    if (ws != nullptr && router_on_tensor_cores(c)) {
+        ra.err_clear = nullptr;
+        int* err = reinterpret_cast<int*>(ws + L.err);
+        cudaError_t e;
+        if ((e = launch_router_split(W_router, c.d, c.E, ws + L.w3, err, s)) != cudaSuccess)
+            return cuda_status(e);
+        const int ks = router_ksplit(c.T, c.d);
+        TcGemmArgs g{};
+        g.g[1] = router_group(x, c.T, c.d, c.E, ws + L.w3, ws + L.rpart);
+        g.err = err;
+        if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
+        return cuda_status(
+            launch_route_from_logits(reinterpret_cast<const float*>(ws + L.rpart), ks, ra, s));
+    }
+    return cuda_status(launch_router(ra, s));
+}
+
+static RouterArgs router_args(const moe_config& c, const void* x, const float* W_router,
+                              const float* bias) {
+    RouterArgs ra{};
+    ra.x = x;
+    ra.x_bf16 = c.dtype == MOE_BF16;
+    ra.W = W_router;
+    ra.bias = bias;
+    ra.T = c.T; ra.d = c.d; ra.E = c.E; ra.K = c.K; ra.gate = c.gate;
+    ra.renorm = c.renormalize; ra.scale = c.routed_scale;
+    return ra;
+}
+
 // Enqueue the whole forward on s. x and out are device pointers.
 static moe_status forward_impl(const moe_config& c, const void* x, const moe_weights& w, void* out,
                                uint8_t* ws, cudaStream_t s) {
@@ -264,36 +300,16 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
 
     // 1. router
     rec.begin(ST_ROUTE);
-    RouterArgs ra{};
-    ra.x = x;
-    ra.x_bf16 = bf;
-    ra.W = w.W_router;
-    ra.bias = w.bias;
-    ra.T = T; ra.d = c.d; ra.E = E; ra.K = K; ra.gate = c.gate; ra.renorm = c.renormalize;
-    ra.scale = c.routed_scale;
+    RouterArgs ra = router_args(c, x, static_cast<const float*>(w.W_router),
+                                static_cast<const float*>(w.bias));
     ra.idx = idx;
     ra.w = tw;
     ra.margin = static_cast<float*>(P(L.margin));
     ra.top_scores = L.top_scores ? static_cast<float*>(P(L.top_scores)) : nullptr;
     ra.scores = L.scores ? static_cast<float*>(P(L.scores)) : nullptr;
-    if (router_chunked(c)) {
-        ra.err_clear = err;
-        if ((e = launch_router_chunked(ra, static_cast<float*>(P(L.rpart)), s)) != cudaSuccess)
-            return cuda_status(e);
-    } else if (router_on_tensor_cores(c)) {
-        if ((e = launch_router_split(w.W_router, c.d, E, P(L.w3), err, s)) != cudaSuccess)
-            return cuda_status(e);
-        const int ks = router_ksplit(T, c.d);
-        TcGemmArgs g{};
-        g.g[1] = router_group(x, T, c.d, E, P(L.w3), P(L.rpart));
-        g.err = err;
-        if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
-        if ((e = launch_route_from_logits(static_cast<const float*>(P(L.rpart)), ks, ra, s)) !=
-            cudaSuccess)
-            return cuda_status(e);
-    } else {
-        ra.err_clear = err;
-        if ((e = launch_router(ra, s)) != cudaSuccess) return cuda_status(e);
+    {
+        const moe_status rs = run_router(c, ra, static_cast<const float*>(w.W_router), x, ws, L, s);
+        if (rs != MOE_OK) return rs;
     }
     rec.end(ST_ROUTE);
 
@@ -482,42 +498,6 @@ MOE_API moe_status moe_get_workspace_views(const moe_config* cfg, void* ws, moe_
     v->sorted_w = reinterpret_cast<float*>(b + L.sorted_w);
     v->inv = reinterpret_cast<int32_t*>(b + L.inv);
     return MOE_OK;
-}
-
-// The router of cfg on x into ra's outputs (ws optional: with it, the
-// workspace error word is cleared and the chunked or tensor-core paths may run).
-static moe_status run_router(const moe_config& c, RouterArgs ra, const float* W_router,
-                             const void* x, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
-    if (ws != nullptr) ra.err_clear = reinterpret_cast<int*>(ws + L.err);
-    if (ws != nullptr && router_chunked(c))
-        return cuda_status(launch_router_chunked(ra, reinterpret_cast<float*>(ws + L.rpart), s));
-    if (ws != nullptr && router_on_tensor_cores(c)) {
-        ra.err_clear = nullptr;
-        int* err = reinterpret_cast<int*>(ws + L.err);
-        cudaError_t e;
-        if ((e = launch_router_split(W_router, c.d, c.E, ws + L.w3, err, s)) != cudaSuccess)
-            return cuda_status(e);
-        const int ks = router_ksplit(c.T, c.d);
-        TcGemmArgs g{};
-        g.g[1] = router_group(x, c.T, c.d, c.E, ws + L.w3, ws + L.rpart);
-        g.err = err;
-        if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
-        return cuda_status(
-            launch_route_from_logits(reinterpret_cast<const float*>(ws + L.rpart), ks, ra, s));
-    }
-    return cuda_status(launch_router(ra, s));
-}
-
-static RouterArgs router_args(const moe_config& c, const void* x, const float* W_router,
-                              const float* bias) {
-    RouterArgs ra{};
-    ra.x = x;
-    ra.x_bf16 = c.dtype == MOE_BF16;
-    ra.W = W_router;
-    ra.bias = bias;
-    ra.T = c.T; ra.d = c.d; ra.E = c.E; ra.K = c.K; ra.gate = c.gate;
-    ra.renorm = c.renormalize; ra.scale = c.routed_scale;
-    return ra;
 }
 
 MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const float* W_router,

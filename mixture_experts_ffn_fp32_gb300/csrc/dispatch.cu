@@ -175,6 +175,95 @@ __global__ void __launch_bounds__(DISPATCH_CHUNK) dispatch_scatter_kernel(
     }
 }
 
+// All of the dispatch for at most DISPATCH_CHUNK assignments (a decode batch)
+// in one CTA: the scatter kernel's warp ranking, the per-expert totals, their
+// exclusive scan (one warp, 8 experts per lane) and the positions - the same
+// integer results as the two-launch path, one launch.
+__global__ void __launch_bounds__(DISPATCH_CHUNK) dispatch_single_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ w, int TK, int K, int E, int bm,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ mt_prefix,
+    int32_t* __restrict__ sorted_token, float* __restrict__ sorted_w, int32_t* __restrict__ inv,
+    int* err) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ int wcnt[32][256];
+    __shared__ int off[256];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < 32 * 256; i += blockDim.x) (&wcnt[0][0])[i] = 0;
+    __syncthreads();
+    const int j = threadIdx.x;
+    int e = (j < TK) ? idx[j] : -1;
+    if (j < TK && (e < 0 || e >= E)) atomicOr(err, ERRBIT_INDEX);
+    if (e < 0 || e >= E) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (e >= 0 && rank == 0) wcnt[warp][e] = __popc(peers);
+    __syncthreads();
+    // per-warp exclusive prefixes and the expert totals
+    for (int x = threadIdx.x; x < 256; x += blockDim.x) {
+        int run = 0;
+        for (int ww = 0; ww < 32; ++ww) {
+            const int c = wcnt[ww][x];
+            wcnt[ww][x] = run;
+            run += c;
+        }
+        off[x] = x < E ? run : 0;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // exclusive scan of the totals (and of the tile counts of both heights)
+        int c[8], m1[8], m2[8], s = 0, s1 = 0, s2 = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            c[i] = off[8 * lane + i];
+            m1[i] = (c[i] + bm - 1) / bm;
+            m2[i] = (c[i] + 2 * bm - 1) / (2 * bm);
+            s += c[i];
+            s1 += m1[i];
+            s2 += m2[i];
+        }
+        int x = s, x1 = s1, x2 = s2;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            const int y1 = __shfl_up_sync(0xffffffffu, x1, o);
+            const int y2 = __shfl_up_sync(0xffffffffu, x2, o);
+            if (lane >= o) {
+                x += y;
+                x1 += y1;
+                x2 += y2;
+            }
+        }
+        int b = x - s, b1 = x1 - s1, b2 = x2 - s2;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int ex = 8 * lane + i;
+            if (ex < E) {
+                counts[ex] = c[i];
+                offsets[ex] = b;
+                mt_prefix[ex] = b1;
+                mt_prefix[E + 1 + ex] = b2;
+            }
+            if (ex == E - 1) {
+                offsets[E] = b + c[i];
+                mt_prefix[E] = b1 + m1[i];
+                mt_prefix[2 * E + 1] = b2 + m2[i];
+            }
+            off[ex] = b;
+            b += c[i];
+            b1 += m1[i];
+            b2 += m2[i];
+        }
+    }
+    __syncthreads();
+    if (e >= 0) {
+        const int pos = off[e] + wcnt[warp][e] + rank;
+        sorted_token[pos] = j / K;
+        sorted_w[pos] = w[j];
+        inv[j] = pos;
+    }
+}
+
 // One warp per destination row; 16-byte vectors.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src,
                                                           const int32_t* __restrict__ rowidx,
@@ -324,6 +413,12 @@ cudaError_t launch_gather_sum_split(const float* ys, const int32_t* inv, int T, 
 
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s, int* n_launched) {
     const int TK = a.T * a.K;
+    if (a.nchunks == 1) {
+        if (n_launched) *n_launched = 1;
+        return launch_pdl(dispatch_single_kernel, dim3(1), dim3(DISPATCH_CHUNK), 0, s, a.idx, a.w,
+                          TK, a.K, a.E, a.bm, a.counts, a.offsets, a.mt_prefix, a.sorted_token,
+                          a.sorted_w, a.inv, a.err);
+    }
     cudaError_t e = launch_pdl(dispatch_count_kernel, dim3(a.nchunks), dim3(256), 0, s, a.idx, TK,
                                a.E, a.nchunks, a.bm, a.chunk_counts, a.chunk_base, a.counts,
                                a.offsets, a.mt_prefix, a.ticket, a.err);

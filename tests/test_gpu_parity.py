@@ -193,7 +193,8 @@ def test_routing_stats(gate, E, K, T, d, dtype):
     assert torch.equal(g["out"], g2["out"])
 
 
-@pytest.mark.parametrize("T,E,K,skew", [(1, 1, 1, 0.0), (3, 3, 2, 0.0), (1000, 8, 2, 0.0),
+@pytest.mark.parametrize("T,E,K,skew", [(1, 1, 1, 0.0), (3, 3, 2, 0.0), (128, 256, 8, 0.0),
+                                        (125, 64, 8, 1.1), (512, 5, 2, 0.8), (1000, 8, 2, 0.0),
                                         (1500, 64, 8, 1.1), (4096, 256, 8, 1.2),
                                         (777, 256, 16, 0.0), (20000, 7, 3, 0.5),
                                         (16384, 64, 8, 1.1)])
@@ -320,7 +321,9 @@ def test_launch_count_grows():
     n0 = A.launch_count()
     A.forward(A.LayerSpec.of(w), inp["x"], inp)
     torch.cuda.synchronize()
-    assert A.launch_count() - n0 >= 6
+    # router, single-CTA dispatch (T*K = 256 assignments), gate/up, routed down,
+    # shared down fused with the combine
+    assert A.launch_count() - n0 == 5
 
 
 def test_bounded_wait_gives_up_and_context_survives():
