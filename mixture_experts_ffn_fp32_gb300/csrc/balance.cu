@@ -224,9 +224,19 @@ __global__ void __launch_bounds__(256) stats_final_kernel(const float* __restric
     float P = 0.0f, fP = 0.0f;
     if (e < E) {
         long long c = 0;
-        for (int b = 0; b < nblk; ++b) {
-            P += part[b * stride + e];
-            c += static_cast<long long>(part[b * stride + E + e]);
+        // CTA order, 8 partial rows' loads in flight per step
+        for (int b0 = 0; b0 < nblk; b0 += 8) {
+            float pv[8], cv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                pv[i] = b0 + i < nblk ? part[(b0 + i) * stride + e] : 0.0f;
+                cv[i] = b0 + i < nblk ? part[(b0 + i) * stride + E + e] : 0.0f;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (b0 + i < nblk) P += pv[i];
+                c += static_cast<long long>(cv[i]);
+            }
         }
         P /= static_cast<float>(T);
         const float f = static_cast<float>(static_cast<double>(c) / (static_cast<double>(T) * K));
@@ -241,7 +251,14 @@ __global__ void __launch_bounds__(256) stats_final_kernel(const float* __restric
         for (int w = 0; w < 8; ++w) a += red[w];
         out[0] = static_cast<float>(E) * a;
         float z = 0.0f;
-        for (int b = 0; b < nblk; ++b) z += part[b * stride + 2 * E];
+        for (int b0 = 0; b0 < nblk; b0 += 8) {
+            float zv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) zv[i] = b0 + i < nblk ? part[(b0 + i) * stride + 2 * E] : 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (b0 + i < nblk) z += zv[i];
+        }
         out[1] = z / static_cast<float>(T);
     }
 }
