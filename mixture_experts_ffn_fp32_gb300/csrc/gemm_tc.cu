@@ -23,7 +23,8 @@
 // epilogue and store. The weights stay in the caller's [Z, K, N] layout (N
 // contiguous) and are read as an MN-major operand.
 //
-// Two forms. CTA pair (the usual one, MMA N = 128 or 256): a cluster of two
+// Two forms. CTA pair (MMA N = 128 or 256; for routed segments of 512 rows on
+// average or more, and for dense groups): a cluster of two
 // CTAs on neighbouring SMs computes a 256-row tile with cta_group::2 MMAs
 // (M = 256) issued by the even CTA; each CTA loads its own 128 rows of A and
 // one half of B's columns, so every SM brings in 32 KB per K step instead of
