@@ -76,15 +76,22 @@ def job_tokens_per_s(tokens_per_rank: int, world: int, step_ms: float) -> float:
     return world * tokens_per_rank / (step_ms / 1e3)
 
 
+# FP32 FFMA peak of the CUDA cores: 152 SMs x 128 FP32 lanes x 2 FLOP x the
+# maximum SM clock (2070 MHz, or MEASURED_PEAKS.json's sm_max_mhz).
+def fp32_alu_tflops(sm_mhz: float = 2070.0) -> float:
+    return 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
         return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
-                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured",
+                "fp32_tflops": fp32_alu_tflops(d.get("sm_max_mhz", 2070.0))}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
-            "source": "fallback"}
+            "source": "fallback", "fp32_tflops": fp32_alu_tflops()}
 
 
 # ---------------------------------------------------------------------------
@@ -98,6 +105,20 @@ def gate_up_flops(w) -> float:
     if not w.latent_dim:
         f += 4.0 * w.T * w.d * w.shared_d_ff * w.n_shared
     return f
+
+
+def gate_up_bytes(w, counts=None) -> float:
+    """Algorithmic HBM bytes of the grouped gate/up launch: gate and up weights
+    of the experts that get tokens and of the shared experts, the BF16 operand
+    rows read once, the BF16 hidden rows written once."""
+    es = 4 if w.dtype == "f32" else 2
+    de = w.latent_dim or w.d
+    used = w.E if counts is None else int(sum(1 for c in counts if c > 0))
+    b = used * 2 * de * w.d_ff * es + w.T * w.K * de * es + w.T * w.K * w.d_ff * es
+    if not w.latent_dim:
+        b += w.n_shared * 2 * w.d * w.shared_d_ff * es
+        b += w.T * w.d * es + w.T * w.n_shared * w.shared_d_ff * es
+    return float(b)
 
 
 def layer_bytes(w, counts=None) -> float:
@@ -411,10 +432,33 @@ def run_ours(args, name):
     tflops = flops / (ms / 1e3) / 1e12
     gu_ms = stages.get("gate_up", 0.0) / max(1, ncalls)
     gu_flops = gate_up_flops(w)
-    achieved = gu_flops / (gu_ms / 1e3) / 1e12 if gu_ms > 0 else None
+    gu_bytes = gate_up_bytes(w, counts)
     traffic = profiled_traffic(name)
     t_flop = flops / (pk["bf16_tflops"] * 1e12)
     t_hbm = layer_bytes(w, counts) / (pk["hbm_gbs"] * 1e9)
+    # the gate/up launch is tensor-bound on prefill and weight-streaming
+    # (HBM-bound) on decode: report it against the roof that bounds it
+    f32 = w.dtype == "f32"
+    flop_peak = pk["fp32_tflops"] if f32 else pk["bf16_tflops"]
+    gu_hbm = gu_bytes / (pk["hbm_gbs"] * 1e9) > gu_flops / (flop_peak * 1e12)
+    if f32:
+        # the FP32 layer's grouped GEMMs run on the CUDA cores (FFMA)
+        achieved = gu_flops / (gu_ms / 1e3) / 1e12 if gu_ms > 0 else None
+        roof = {"bound": "alu", "achieved": achieved, "peak": flop_peak, "unit": "TFLOP/s",
+                "peak_source": "FP32 FFMA: 152 SMs x 128 lanes x 2 FLOP x max SM clock",
+                "flops_per_launch": gu_flops}
+    elif gu_hbm:
+        achieved = gu_bytes / (gu_ms / 1e3) / 1e9 if gu_ms > 0 else None
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "peak_source": f"{pk['source']} HBM copy", "bytes_per_launch": gu_bytes}
+    else:
+        achieved = gu_flops / (gu_ms / 1e3) / 1e12 if gu_ms > 0 else None
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "peak_source": f"{pk['source']} bf16 burst",
+                "flops_per_launch": gu_flops}
+    roof["frac"] = (achieved / roof["peak"]) if achieved else None
+    roof["traffic"] = traffic
+    roof["avg_launch_ms"] = gu_ms
     line = {
         "metric": METRIC, "value": job_tokens_per_s(w.T, world, ms), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -430,11 +474,8 @@ def run_ours(args, name):
                            "bound": "tensor" if t_flop >= t_hbm else "hbm",
                            "frac": max(t_flop, t_hbm) * 1e3 / ms,
                            "peak_source": pk["source"]},
-        "roofline": {"kernel": "tc_grouped_gemm_kernel<SwiGLU> (gate_up)", "bound": "tensor",
-                     "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": (achieved / pk["bf16_tflops"]) if achieved else None,
-                     "traffic": traffic, "peak_source": f"{pk['source']} bf16 burst",
-                     "avg_launch_ms": gu_ms, "flops_per_launch": gu_flops},
+        "roofline": {"kernel": ("simt_grouped_gemm_kernel (gate_up)" if f32 else
+                                "tc_grouped_gemm_kernel<SwiGLU> (gate_up)"), **roof},
         "stage_ms": {k: v / max(1, nb) for k, v in breakdown.items() if v > 0},
         "stage_ms_note": "separate instrumented pass (an event between every stage)",
         "routing_diagnostics": diag,

@@ -3,6 +3,7 @@
 // router.cu, dispatch.cu, gemm_tc.cu / gemm_simt.cu and balance.cu.
 #include <math.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <atomic>
@@ -298,7 +299,23 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
     StageRec rec = stage_rec(s);
     cudaError_t e;
 
-    // 1. router
+    DispatchArgs da{};
+    da.idx = idx;
+    da.w = tw;
+    da.T = T; da.K = K; da.E = E; da.nchunks = L.nchunks;
+    da.bm = bf ? TC_BM : SIMT_BM;
+    da.chunk_counts = static_cast<int32_t*>(P(L.chunk_counts));
+    da.chunk_base = static_cast<int32_t*>(P(L.chunk_base));
+    da.counts = static_cast<int32_t*>(P(L.counts));
+    da.offsets = offsets;
+    da.mt_prefix = mt_prefix;
+    da.sorted_token = sorted_token;
+    da.sorted_w = sorted_w;
+    da.inv = inv;
+    da.err = err;
+    da.ticket = err + 1;
+
+    // 1. router (with the dispatch, for a decode batch)
     rec.begin(ST_ROUTE);
     RouterArgs ra = router_args(c, x, static_cast<const float*>(w.W_router),
                                 static_cast<const float*>(w.bias));
@@ -326,24 +343,15 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
         rec.end(ST_LATENT_DOWN);
     }
 
-    // 2. dispatch
+    // 2. dispatch (a BF16 decode batch: with the row gather, one launch)
     rec.begin(ST_DISPATCH);
-    DispatchArgs da{};
-    da.idx = idx;
-    da.w = tw;
-    da.T = T; da.K = K; da.E = E; da.nchunks = L.nchunks;
-    da.bm = bf ? TC_BM : SIMT_BM;
-    da.chunk_counts = static_cast<int32_t*>(P(L.chunk_counts));
-    da.chunk_base = static_cast<int32_t*>(P(L.chunk_base));
-    da.counts = static_cast<int32_t*>(P(L.counts));
-    da.offsets = offsets;
-    da.mt_prefix = mt_prefix;
-    da.sorted_token = sorted_token;
-    da.sorted_w = sorted_w;
-    da.inv = inv;
-    da.err = err;
-    da.ticket = err + 1;
-    if ((e = launch_dispatch(da, s, nullptr)) != cudaSuccess) return cuda_status(e);
+    const bool dg = bf && L.nchunks == 1;
+    if (dg) {
+        if ((e = launch_dispatch_gather(da, ex_src, de * 2, P(L.xs), s)) != cudaSuccess)
+            return cuda_status(e);
+    } else if ((e = launch_dispatch(da, s, nullptr)) != cudaSuccess) {
+        return cuda_status(e);
+    }
     rec.end(ST_DISPATCH);
 
     if (bf) {
@@ -351,7 +359,7 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
         float* shout = S ? static_cast<float*>(P(L.shout)) : nullptr;
         // 3. gather the routed rows into expert order
         rec.begin(ST_GATHER);
-        if ((e = launch_gather_rows(ex_src, sorted_token, TK, de * 2, P(L.xs), s)) != cudaSuccess)
+        if (!dg && (e = launch_gather_rows(ex_src, sorted_token, TK, de * 2, P(L.xs), s)) != cudaSuccess)
             return cuda_status(e);
         rec.end(ST_GATHER);
 

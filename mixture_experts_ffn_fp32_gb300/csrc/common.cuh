@@ -100,6 +100,17 @@ MOE_DEV uint32_t map_shared_rank(uint32_t saddr, uint32_t rank) {
     return r;
 }
 
+// The two halves of cluster_sync, for work between the arrival and the wait.
+MOE_DEV void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+MOE_DEV void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+
+// FP32 load from the shared memory of a CTA of the cluster (shared::cluster address).
+MOE_DEV float ld_shared_cluster_f32(uint32_t cluster_addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
 // Arrive on an mbarrier of another CTA of the cluster (shared::cluster address).
 MOE_DEV void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
@@ -151,6 +162,17 @@ MOE_DEV bool bounded_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns, i
             return false;
         }
     }
+}
+
+// ---------------------------------------------------------------------------
+// Untiled bulk copy global -> shared of `bytes` bytes, completing on an
+// mbarrier: both addresses 16-byte aligned, bytes a multiple of 16.
+// ---------------------------------------------------------------------------
+MOE_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
 }
 
 // ---------------------------------------------------------------------------

@@ -16,7 +16,10 @@
 // stably (warp match + per-warp counts) and writes sorted_token / sorted_w /
 // inv. Integer arithmetic only, so the result is bit-exact and independent of
 // scheduling.
+#include <algorithm>
+
 #include "common.cuh"
+#include "dispatch_dev.cuh"
 #include "internal.h"
 
 namespace moe {
@@ -176,9 +179,8 @@ __global__ void __launch_bounds__(DISPATCH_CHUNK) dispatch_scatter_kernel(
 }
 
 // All of the dispatch for at most DISPATCH_CHUNK assignments (a decode batch)
-// in one CTA: the scatter kernel's warp ranking, the per-expert totals, their
-// exclusive scan (one warp, 8 experts per lane) and the positions - the same
-// integer results as the two-launch path, one launch.
+// in one CTA of 1024 threads (dispatch_block): the same integer results as
+// the two-launch path, one launch.
 __global__ void __launch_bounds__(DISPATCH_CHUNK) dispatch_single_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ w, int TK, int K, int E, int bm,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ mt_prefix,
@@ -186,81 +188,44 @@ __global__ void __launch_bounds__(DISPATCH_CHUNK) dispatch_single_kernel(
     int* err) {
     pdl_wait();
     pdl_trigger();
-    __shared__ int wcnt[32][256];
-    __shared__ int off[256];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int i = threadIdx.x; i < 32 * 256; i += blockDim.x) (&wcnt[0][0])[i] = 0;
+    dispatch_block<DISPATCH_CHUNK, 256>(idx, w, TK, K, E, bm, true, counts, offsets, mt_prefix,
+                                        sorted_token, sorted_w, inv, err);
+}
+
+// Dispatch and row gather of a decode batch (at most DISPATCH_CHUNK
+// assignments) in one launch: every CTA runs the whole dispatch on its own
+// (dispatch_block: the same integer results in each) and CTA 0 writes it out;
+// each CTA then copies its rows of the gathered operand from the positions it
+// computed itself, so nothing passes between CTAs. One warp per row, rows
+// blockIdx.x * 8 + warp with a stride of 8 gridDim.x.
+template <int EMAX>
+__global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a,
+                                                              const uint4* __restrict__ src,
+                                                              int vec_per_row,
+                                                              uint4* __restrict__ dst) {
+    __shared__ int32_t tok[DISPATCH_CHUNK];
+    // every row index defined even if an id were invalid (its row then copies token 0)
+    for (int i = threadIdx.x; i < DISPATCH_CHUNK; i += blockDim.x) tok[i] = 0;
+    pdl_wait();
+    pdl_trigger();
+    const int TK = a.T * a.K;
+    dispatch_block<256, EMAX>(a.idx, a.w, TK, a.K, a.E, a.bm, blockIdx.x == 0, a.counts,
+                              a.offsets, a.mt_prefix, a.sorted_token, a.sorted_w, a.inv, a.err,
+                              tok);
     __syncthreads();
-    const int j = threadIdx.x;
-    int e = (j < TK) ? idx[j] : -1;
-    if (j < TK && (e < 0 || e >= E)) atomicOr(err, ERRBIT_INDEX);
-    if (e < 0 || e >= E) e = -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    if (e >= 0 && rank == 0) wcnt[warp][e] = __popc(peers);
-    __syncthreads();
-    // per-warp exclusive prefixes and the expert totals
-    for (int x = threadIdx.x; x < 256; x += blockDim.x) {
-        int run = 0;
-        for (int ww = 0; ww < 32; ++ww) {
-            const int c = wcnt[ww][x];
-            wcnt[ww][x] = run;
-            run += c;
-        }
-        off[x] = x < E ? run : 0;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        // exclusive scan of the totals (and of the tile counts of both heights)
-        int c[8], m1[8], m2[8], s = 0, s1 = 0, s2 = 0;
+    const int lane = threadIdx.x & 31;
+    for (int r = blockIdx.x * 8 + (threadIdx.x >> 5); r < TK; r += gridDim.x * 8) {
+        const size_t so = static_cast<size_t>(tok[r]) * vec_per_row;
+        const size_t d = static_cast<size_t>(r) * vec_per_row;
+        for (int v0 = lane; v0 < vec_per_row; v0 += 128) {
+            uint4 buf[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            c[i] = off[8 * lane + i];
-            m1[i] = (c[i] + bm - 1) / bm;
-            m2[i] = (c[i] + 2 * bm - 1) / (2 * bm);
-            s += c[i];
-            s1 += m1[i];
-            s2 += m2[i];
-        }
-        int x = s, x1 = s1, x2 = s2;
+            for (int i = 0; i < 4; ++i)
+                if (v0 + 32 * i < vec_per_row) buf[i] = __ldg(src + so + v0 + 32 * i);
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
-            const int y1 = __shfl_up_sync(0xffffffffu, x1, o);
-            const int y2 = __shfl_up_sync(0xffffffffu, x2, o);
-            if (lane >= o) {
-                x += y;
-                x1 += y1;
-                x2 += y2;
-            }
+            for (int i = 0; i < 4; ++i)
+                if (v0 + 32 * i < vec_per_row) dst[d + v0 + 32 * i] = buf[i];
         }
-        int b = x - s, b1 = x1 - s1, b2 = x2 - s2;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int ex = 8 * lane + i;
-            if (ex < E) {
-                counts[ex] = c[i];
-                offsets[ex] = b;
-                mt_prefix[ex] = b1;
-                mt_prefix[E + 1 + ex] = b2;
-            }
-            if (ex == E - 1) {
-                offsets[E] = b + c[i];
-                mt_prefix[E] = b1 + m1[i];
-                mt_prefix[2 * E + 1] = b2 + m2[i];
-            }
-            off[ex] = b;
-            b += c[i];
-            b1 += m1[i];
-            b2 += m2[i];
-        }
-    }
-    __syncthreads();
-    if (e >= 0) {
-        const int pos = off[e] + wcnt[warp][e] + rank;
-        sorted_token[pos] = j / K;
-        sorted_w[pos] = w[j];
-        inv[j] = pos;
     }
 }
 
@@ -427,6 +392,21 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s, int* n_launch
                    TK, a.K, a.E, a.chunk_base, a.sorted_token, a.sorted_w, a.inv);
     if (n_launched) *n_launched = 2;
     return e;
+}
+
+cudaError_t launch_dispatch_gather(const DispatchArgs& a, const void* src, int row_bytes, void* dst,
+                                   cudaStream_t s) {
+    const int TK = a.T * a.K;
+    if (TK > DISPATCH_CHUNK || a.E > 256) return cudaErrorInvalidValue;
+    const int blocks = std::max(1, std::min((TK + 7) / 8, num_sms()));
+    const uint4* sv = static_cast<const uint4*>(src);
+    uint4* dv = static_cast<uint4*>(dst);
+    const int vpr = row_bytes / 16;
+    if (a.E <= 64)
+        return launch_pdl(dispatch_gather_kernel<64>, dim3(blocks), dim3(256), 0, s, a, sv, vpr, dv);
+    if (a.E <= 128)
+        return launch_pdl(dispatch_gather_kernel<128>, dim3(blocks), dim3(256), 0, s, a, sv, vpr, dv);
+    return launch_pdl(dispatch_gather_kernel<256>, dim3(blocks), dim3(256), 0, s, a, sv, vpr, dv);
 }
 
 cudaError_t launch_gather_rows(const void* src, const int32_t* rowidx, int rows, int row_bytes,

@@ -132,6 +132,10 @@ struct DispatchArgs {
     int* ticket;   // zero when no dispatch is running; the word after *err in a workspace
 };
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s, int* n_launched);
+// Dispatch + gather of the routed rows (row_bytes each, from src into dst in
+// expert order) in one launch, for T*K <= DISPATCH_CHUNK.
+cudaError_t launch_dispatch_gather(const DispatchArgs& a, const void* src, int row_bytes, void* dst,
+                                   cudaStream_t s);
 
 // dst[r, :] = src[rowidx[r], :] for r < rows, row_bytes a multiple of 16.
 cudaError_t launch_gather_rows(const void* src, const int32_t* rowidx, int rows, int row_bytes,

@@ -13,270 +13,15 @@
 // score ranks as -inf so the selected ids are always valid.
 #include <math.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
+#include "route_dev.cuh"
 
 namespace moe {
 namespace {
 
-
-// The error word and the dispatch ticket that follows it start every forward at zero.
-MOE_DEV void clear_status(int* w) {
-    w[0] = 0;
-    w[1] = 0;
-}
-
-MOE_DEV float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-MOE_DEV float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
-// Routes token t. Lane l holds the logits of experts l + 32 j in r[j].
-template <int J>
-MOE_DEV void route_token_warp(const float (&r)[J], int t, const RouterArgs& a) {
-    const int lane = static_cast<int>(lane_id());
-    const int E = a.E, K = a.K;
-    if (a.logits != nullptr) {
-#pragma unroll
-        for (int j = 0; j < J; ++j)
-            if (lane + 32 * j < E) a.logits[static_cast<size_t>(t) * E + lane + 32 * j] = r[j];
-    }
-    float c[J], s[J];
-#pragma unroll
-    for (int j = 0; j < J; ++j) {
-        const int e = lane + 32 * j;
-        const float b = (a.bias != nullptr && e < E) ? a.bias[e] : 0.0f;
-        s[j] = 0.0f;
-        if (a.gate == MOE_GATE_SIGMOID) {
-            s[j] = 1.0f / (1.0f + expf(-r[j]));
-            c[j] = s[j] + b;
-        } else {
-            c[j] = r[j] + b;
-        }
-    }
-    if (a.gate == MOE_GATE_SOFTMAX_ALL_RENORM) {
-        float m = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < J; ++j)
-            if (lane + 32 * j < E) m = fmaxf(m, c[j]);
-        m = warp_max(m);
-        float z[J], sum = 0.0f;
-#pragma unroll
-        for (int j = 0; j < J; ++j) {
-            z[j] = (lane + 32 * j < E) ? expf(c[j] - m) : 0.0f;
-            sum += z[j];
-        }
-        sum = warp_sum(sum);
-#pragma unroll
-        for (int j = 0; j < J; ++j) c[j] = z[j] / sum;
-    }
-    if (a.gate == MOE_GATE_SIGMOID && a.scores != nullptr) {
-#pragma unroll
-        for (int j = 0; j < J; ++j) {
-            const int e = lane + 32 * j;
-            if (e < E) a.scores[static_cast<size_t>(t) * E + e] = s[j];
-        }
-    }
-#pragma unroll
-    for (int j = 0; j < J; ++j)
-        if (!(c[j] == c[j])) c[j] = -INFINITY;
-
-    const int nsel = (K < E) ? K + 1 : K;
-    uint32_t taken = 0;
-    float my_val = 0.0f;
-    int my_idx = 0;
-    for (int it = 0; it < nsel; ++it) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < J; ++j) {
-            const int e = lane + 32 * j;
-            if (e < E && !((taken >> j) & 1u)) {
-                if (c[j] > bv || (c[j] == bv && e < bi)) {
-                    bv = c[j];
-                    bi = e;
-                }
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        if (lane == (bi & 31)) taken |= 1u << (bi >> 5);
-        if (lane == it) {
-            my_val = bv;
-            my_idx = bi;
-        }
-    }
-
-    float w = 0.0f;
-    if (a.gate == MOE_GATE_SOFTMAX_TOPK) {
-        const float m = __shfl_sync(0xffffffffu, my_val, 0);
-        const float ex = (lane < K) ? expf(my_val - m) : 0.0f;
-        const float sum = warp_sum(ex);
-        w = ex / sum;
-    } else if (a.gate == MOE_GATE_SOFTMAX_ALL_RENORM) {
-        const float p = (lane < K) ? my_val : 0.0f;
-        const float sum = warp_sum(p);
-        w = p / sum;
-    } else {
-        float my_s = 0.0f;
-        for (int k = 0; k < K; ++k) {
-            const int e = __shfl_sync(0xffffffffu, my_idx, k);
-            const int jj = e >> 5;
-            float sv = 0.0f;
-#pragma unroll
-            for (int j = 0; j < J; ++j)
-                if (j == jj) sv = s[j];
-            sv = __shfl_sync(0xffffffffu, sv, e & 31);
-            if (lane == k) my_s = sv;
-        }
-        w = my_s;
-        if (a.renorm) {
-            const float sum = warp_sum(lane < K ? my_s : 0.0f);
-            w = my_s / sum;
-        }
-        w *= a.scale;
-    }
-
-    const float vK1 = __shfl_sync(0xffffffffu, my_val, K - 1);
-    const float vK = __shfl_sync(0xffffffffu, my_val, (K < E) ? K : K - 1);
-    if (lane < K) {
-        a.idx[static_cast<size_t>(t) * K + lane] = my_idx;
-        a.w[static_cast<size_t>(t) * K + lane] = w;
-    }
-    if (a.top_scores != nullptr && a.gate == MOE_GATE_SIGMOID && lane <= K)
-        a.top_scores[static_cast<size_t>(t) * (K + 1) + lane] = my_val;
-    if (a.margin != nullptr && lane == 0) a.margin[t] = (K < E) ? (vK1 - vK) : INFINITY;
-}
-
-// Routes token t in one thread from all E logits in r[0..E-1] (E <= EP <= 8):
-// the same selection, ranking and weights as route_token_warp, for small E
-// where one lane is cheaper than the warp-wide search.
-template <int EP>
-MOE_DEV void route_token_seq(const float (&r)[EP], int t, const RouterArgs& a) {
-    const int E = a.E, K = a.K;
-    if (a.logits != nullptr) {
-#pragma unroll
-        for (int e = 0; e < EP; ++e)
-            if (e < E) a.logits[static_cast<size_t>(t) * E + e] = r[e];
-    }
-    float c[EP], sg[EP];
-#pragma unroll
-    for (int e = 0; e < EP; ++e) {
-        sg[e] = 0.0f;
-        c[e] = -INFINITY;
-        if (e < E) {
-            const float b = a.bias != nullptr ? a.bias[e] : 0.0f;
-            if (a.gate == MOE_GATE_SIGMOID) {
-                sg[e] = 1.0f / (1.0f + expf(-r[e]));
-                c[e] = sg[e] + b;
-            } else {
-                c[e] = r[e] + b;
-            }
-        }
-    }
-    if (a.gate == MOE_GATE_SOFTMAX_ALL_RENORM) {
-        float m = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < EP; ++e)
-            if (e < E) m = fmaxf(m, c[e]);
-        float sum = 0.0f;
-#pragma unroll
-        for (int e = 0; e < EP; ++e) {
-            c[e] = e < E ? expf(c[e] - m) : 0.0f;
-            sum += c[e];
-        }
-#pragma unroll
-        for (int e = 0; e < EP; ++e)
-            if (e < E) c[e] = c[e] / sum;
-    }
-    if (a.gate == MOE_GATE_SIGMOID && a.scores != nullptr) {
-#pragma unroll
-        for (int e = 0; e < EP; ++e)
-            if (e < E) a.scores[static_cast<size_t>(t) * E + e] = sg[e];
-    }
-#pragma unroll
-    for (int e = 0; e < EP; ++e)
-        if (!(c[e] == c[e])) c[e] = -INFINITY;
-    // rank of each expert: how many beat it (higher value, or equal value and
-    // lower id); slot k of the top-(K+1) holds the expert of rank k
-    int rank[EP];
-#pragma unroll
-    for (int e = 0; e < EP; ++e) {
-        rank[e] = EP;
-        if (e < E) {
-            int n = 0;
-#pragma unroll
-            for (int f = 0; f < EP; ++f)
-                if (f < E && (c[f] > c[e] || (c[f] == c[e] && f < e))) ++n;
-            rank[e] = n;
-        }
-    }
-    auto slot = [&](int k, float& v, int& id, float& sgv) {
-        v = 0.0f;
-        id = 0;
-        sgv = 0.0f;
-#pragma unroll
-        for (int e = 0; e < EP; ++e)
-            if (rank[e] == k) {
-                v = c[e];
-                id = e;
-                sgv = sg[e];
-            }
-    };
-    float v0, sg0;
-    int id0;
-    slot(0, v0, id0, sg0);
-    float sum = 0.0f;
-#pragma unroll
-    for (int k = 0; k < EP; ++k) {
-        if (k < K) {
-            float v, sgv;
-            int id;
-            slot(k, v, id, sgv);
-            sum += a.gate == MOE_GATE_SOFTMAX_TOPK ? expf(v - v0)
-                   : a.gate == MOE_GATE_SOFTMAX_ALL_RENORM ? v : sgv;
-        }
-    }
-    const bool normalise = a.gate != MOE_GATE_SIGMOID || a.renorm;
-#pragma unroll
-    for (int k = 0; k < EP + 1; ++k) {
-        if (k <= K && k < E) {
-            float v, sgv;
-            int id;
-            slot(k, v, id, sgv);
-            if (k < K) {
-                float wk = a.gate == MOE_GATE_SOFTMAX_TOPK ? expf(v - v0)
-                           : a.gate == MOE_GATE_SOFTMAX_ALL_RENORM ? v : sgv;
-                if (normalise) wk = wk / sum;
-                if (a.gate == MOE_GATE_SIGMOID) wk *= a.scale;
-                a.idx[static_cast<size_t>(t) * K + k] = id;
-                a.w[static_cast<size_t>(t) * K + k] = wk;
-            }
-            if (a.top_scores != nullptr && a.gate == MOE_GATE_SIGMOID)
-                a.top_scores[static_cast<size_t>(t) * (K + 1) + k] = v;
-        }
-    }
-    if (a.margin != nullptr) {
-        float vK1, vK, sgv;
-        int id;
-        slot(K - 1, vK1, id, sgv);
-        slot(K, vK, id, sgv);
-        a.margin[t] = (K < E) ? (vK1 - vK) : INFINITY;
-    }
-}
 
 // E <= 32: one warp per token, 8 tokens per CTA. The CTA first copies its 8
 // x rows into shared memory with all its loads in flight at once (one memory
@@ -496,103 +241,174 @@ __global__ void __launch_bounds__(256) route_from_logits_kernel(const float* __r
     if (a.err_clear != nullptr && blockIdx.x == 0 && threadIdx.x == 0) clear_status(a.err_clear);
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (t >= a.T) return;
-    const int lane = static_cast<int>(lane_id());
-    const size_t slice = static_cast<size_t>(a.T) * a.E;
     float r[J];
-#pragma unroll
-    for (int j = 0; j < J; ++j) {
-        const int e = lane + 32 * j;
-        float v = 0.0f;
-        if (e < a.E) {
-            // slices in order, 8 loads in flight per step
-            const float* p = part + static_cast<size_t>(t) * a.E + e;
-            for (int s0 = 0; s0 < nsplit; s0 += 8) {
-                float q[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) q[i] = s0 + i < nsplit ? p[(s0 + i) * slice] : 0.0f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if (s0 + i < nsplit) v += q[i];
-            }
-        }
-        r[j] = v;
-    }
+    sum_slices<J>(part, nsplit, t, a.T, a.E, r);
     route_token_warp<J>(r, t, a);
 }
 
-// Few tokens, E > 32: partial logits over slices of d, one CTA per (8 tokens,
-// slice) so that even a decode batch spreads over many SMs. The CTA's threads
-// are (expert e, part r): R = 256 / EP parts each take a contiguous run of 64
-// of the slice's CHUNK_LEN(EP) = 64 R values (W_router rows read coalesced
-// across e, 8 rows in flight), the 8 tokens' x slices sit in shared memory,
-// and part 0 adds the R partial sums in order. route_from_logits_kernel sums
-// the slices in FP32 and routes.
-__host__ __device__ constexpr int router_chunk_len(int EP) { return 64 * (256 / EP); }
-
+// Few tokens, E > 32: partial logits over slices of d (chunk_partials), one
+// CTA per (8 tokens, slice); route_from_logits_kernel sums the slices.
 template <bool BF16, int EP>
 __global__ void __launch_bounds__(256) router_chunk_kernel(RouterArgs a, float* __restrict__ part) {
-    constexpr int R = 256 / EP;            // parts per expert
-    constexpr int LEN = router_chunk_len(EP);
-    constexpr int RUN = LEN / R;           // k values per part (64)
     pdl_wait();
     pdl_trigger();
     if (a.err_clear != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
         clear_status(a.err_clear);
-    __shared__ float xs[8][LEN];
-    __shared__ float red[R > 1 ? R - 1 : 1][8][EP];
-    const int t0 = blockIdx.x * 8, k0 = blockIdx.y * LEN;
-    const int kn = min(LEN, a.d - k0);
-    for (int i = threadIdx.x; i < 8 * LEN; i += blockDim.x) {
-        const int tt = i / LEN, k = i - tt * LEN;
-        float v = 0.0f;
-        if (t0 + tt < a.T && k < kn) {
-            const size_t off = static_cast<size_t>(t0 + tt) * a.d + k0 + k;
-            v = BF16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(a.x)[off])
-                     : static_cast<const float*>(a.x)[off];
+    chunk_partials<BF16, EP>(a, part, blockIdx.x, blockIdx.y);
+}
+
+// Few tokens, E > 32, as one launch without any memory-based synchronisation:
+// a thread-block cluster per block of 8 tokens, one CTA per slice of d (at
+// most 8 slices). Each CTA brings its W_router rows and the 8 tokens' x
+// slices into shared memory with bulk copies (one round trip), computes the
+// partial logits of the slice there, and after a cluster barrier the CTAs
+// sum the slices of their tokens in slice order straight from the peers'
+// shared memory and route them (token c + ns w in warp w of the CTA of
+// cluster rank c).
+struct ClusterRouterShape {
+    int ns, lenc;
+    size_t smem;
+};
+
+template <bool BF16, int EP>
+__global__ void __launch_bounds__(256) router_cluster_kernel(RouterArgs a, int lenc, uint64_t timeout_ns) {
+    extern __shared__ __align__(128) uint8_t sm[];
+    constexpr int R = 256 / EP;  // parts per expert
+    constexpr int J = EP / 32;
+    constexpr int XES = BF16 ? 2 : 4;
+    const int E = a.E, d = a.d;
+    const int ns = static_cast<int>(gridDim.x);  // cluster = the token block's slices
+    const int c = static_cast<int>(cluster_ctarank());
+    const int t0 = blockIdx.y * 8, k0 = c * lenc;
+    const int kn = max(0, min(lenc, d - k0));
+    const int ntok = min(8, a.T - t0);
+    const int xstage_bytes = (8 * lenc * XES + 15) / 16 * 16;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm);
+    uint8_t* xstage = sm + 16;
+    float* xt = reinterpret_cast<float*>(xstage + xstage_bytes);  // [lenc][8]
+    float* ws = xt + 8 * lenc;                                    // [lenc][E]
+    float* part = ws + static_cast<size_t>(lenc) * E;             // [8][EP]
+    float* red = part + 8 * EP;                                   // [R-1][8][EP]
+    __shared__ int abort_flag;
+    const uint32_t b = smem_u32(bar);
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(b, 1);
+        fence_mbarrier_init();
+    }
+    pdl_wait();
+    pdl_trigger();
+    if (a.err_clear != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+        clear_status(a.err_clear);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint32_t wbytes = static_cast<uint32_t>(kn) * E * 4;
+        const uint32_t xbytes = static_cast<uint32_t>(kn) * XES;
+        mbar_expect_tx(b, wbytes + xbytes * ntok);
+        if (kn > 0) {
+            bulk_load(smem_u32(ws), a.W + static_cast<size_t>(k0) * E, wbytes, b);
+            for (int tt = 0; tt < ntok; ++tt)
+                bulk_load(smem_u32(xstage + static_cast<size_t>(tt) * lenc * XES),
+                          static_cast<const uint8_t*>(a.x) +
+                              (static_cast<size_t>(t0 + tt) * d + k0) * XES,
+                          xbytes, b);
         }
-        xs[tt][k] = v;
+    }
+    // the routing warps' bias values, loaded while the copies are in flight
+    float bj[J];
+    load_bias_lanes<J>(a, bj);
+    const WaitCtx wc{a.err_clear, &abort_flag, timeout_ns};
+    const bool ok = bounded_wait(b, 0, wc);
+    // x slices as FP32, transposed to [k][token] (zero for missing tokens)
+    for (int i = threadIdx.x; i < 8 * kn; i += blockDim.x) {
+        const int tt = i / kn, k = i - tt * kn;
+        float v = 0.0f;
+        if (ok && tt < ntok) {
+            v = BF16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(xstage)[tt * lenc + k])
+                     : reinterpret_cast<const float*>(xstage)[tt * lenc + k];
+        }
+        xt[k * 8 + tt] = v;
     }
     __syncthreads();
     const int e = threadIdx.x % EP, r = threadIdx.x / EP;
+    const int run = (kn + R - 1) / R;
+    const int kb = r * run, ke = min(kb + run, kn);
     float acc[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-    if (e < a.E) {
-        const int kb = r * RUN;
-        const int ke = min(kb + RUN, kn);
-        const float* w = a.W + static_cast<size_t>(k0) * a.E + e;
-        int k = kb;
-        for (; k + 8 <= ke; k += 8) {
-            float wv[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) wv[i] = __ldg(w + static_cast<size_t>(k + i) * a.E);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) acc[j] = fmaf(xs[j][k + i], wv[i], acc[j]);
-        }
-        for (; k < ke; ++k) {
-            const float wv = __ldg(w + static_cast<size_t>(k) * a.E);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] = fmaf(xs[j][k], wv, acc[j]);
+    if (ok && e < E) {
+        for (int k = kb; k < ke; ++k) {
+            const float wv = ws[static_cast<size_t>(k) * E + e];
+            const float4 x0 = *reinterpret_cast<const float4*>(xt + k * 8);
+            const float4 x1 = *reinterpret_cast<const float4*>(xt + k * 8 + 4);
+            acc[0] = fmaf(x0.x, wv, acc[0]);
+            acc[1] = fmaf(x0.y, wv, acc[1]);
+            acc[2] = fmaf(x0.z, wv, acc[2]);
+            acc[3] = fmaf(x0.w, wv, acc[3]);
+            acc[4] = fmaf(x1.x, wv, acc[4]);
+            acc[5] = fmaf(x1.y, wv, acc[5]);
+            acc[6] = fmaf(x1.z, wv, acc[6]);
+            acc[7] = fmaf(x1.w, wv, acc[7]);
         }
     }
     if (R > 1) {
         if (r > 0)
 #pragma unroll
-            for (int j = 0; j < 8; ++j) red[r - 1][j][e] = acc[j];
+            for (int j = 0; j < 8; ++j) red[((r - 1) * 8 + j) * EP + e] = acc[j];
         __syncthreads();
         if (r == 0)
             for (int q = 0; q < R - 1; ++q)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[j] += red[q][j][e];
+                for (int j = 0; j < 8; ++j) acc[j] += red[(q * 8 + j) * EP + e];
     }
-    if (r != 0 || e >= a.E) return;
-    float* dst = part + (static_cast<size_t>(blockIdx.y) * a.T + t0) * a.E + e;
+    if (r == 0)
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-        if (t0 + j < a.T) dst[static_cast<size_t>(j) * a.E] = acc[j];
+        for (int j = 0; j < 8; ++j) part[j * EP + e] = acc[j];
+    // every slice's partials are in its CTA's shared memory
+    cluster_sync();
+
+    const int lane = static_cast<int>(lane_id()), w = threadIdx.x >> 5;
+    const int tt = c + ns * w;
+    const bool mine = tt < ntok;
+    float rl[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) rl[j] = 0.0f;
+    if (mine) {
+        float q[8][J];
+#pragma unroll
+        for (int sl = 0; sl < 8; ++sl) {
+            const uint32_t src = map_shared_rank(smem_u32(part + tt * EP), static_cast<uint32_t>(sl < ns ? sl : 0));
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+                q[sl][j] = (sl < ns) ? ld_shared_cluster_f32(src + 4u * (lane + 32 * j)) : 0.0f;
+        }
+#pragma unroll
+        for (int sl = 0; sl < 8; ++sl)
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+                if (sl < ns) rl[j] += q[sl][j];
+    }
+    // the peers' partials are read: a CTA may leave once every CTA got here
+    cluster_arrive();
+    if (mine) route_token_warp<J>(rl, bj, t0 + tt, a);
+    if (!ok) bounded_drain(b, 0, timeout_ns, a.err_clear);
+    cluster_wait();
 }
+
+ClusterRouterShape cluster_router_shape(int d, int E, int x_bf16) {
+    ClusterRouterShape sh{};
+    const int ns0 = std::min(8, (d + 127) / 128);
+    sh.lenc = ((d + ns0 - 1) / ns0 + 15) / 16 * 16;
+    sh.ns = (d + sh.lenc - 1) / sh.lenc;
+    const int EP = E <= 64 ? 64 : 128;
+    const int R = 256 / EP;
+    const size_t xes = x_bf16 ? 2 : 4;
+    sh.smem = 16 + (8 * sh.lenc * xes + 15) / 16 * 16 + 8 * static_cast<size_t>(sh.lenc) * 4 +
+              static_cast<size_t>(sh.lenc) * E * 4 + 8 * EP * 4 + (R - 1) * 8 * EP * 4;
+    return sh;
+}
+
+constexpr size_t CLUSTER_ROUTER_SMEM_MAX = 200 * 1024;
 
 template <bool BF16>
 cudaError_t launch_router_t(const RouterArgs& a, cudaStream_t s) {
@@ -649,6 +465,32 @@ int router_chunked_nsplit(int d, int E) {
 }
 
 cudaError_t launch_router_chunked(const RouterArgs& a, float* part, cudaStream_t s) {
+    const ClusterRouterShape sh = cluster_router_shape(a.d, a.E, a.x_bf16);
+    if (a.err_clear != nullptr && sh.smem <= CLUSTER_ROUTER_SMEM_MAX) {
+        const dim3 grid(sh.ns, (a.T + 7) / 8);
+        const uint64_t to = wait_timeout_ns();
+#define MOE_RCL(B, EPV)                                                                            \
+    {                                                                                              \
+        static bool set = false;                                                                   \
+        if (!set) {                                                                                \
+            cudaFuncSetAttribute(router_cluster_kernel<B, EPV>,                                    \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,                      \
+                                 static_cast<int>(CLUSTER_ROUTER_SMEM_MAX));                       \
+            set = true;                                                                            \
+        }                                                                                          \
+        return launch_pdl_cluster(router_cluster_kernel<B, EPV>, grid, dim3(256), sh.smem, s,      \
+                                  sh.ns, a, sh.lenc, to);                                          \
+    }
+        if (a.x_bf16) {
+            if (a.E <= 64) MOE_RCL(true, 64)
+            MOE_RCL(true, 128)
+        } else {
+            if (a.E <= 64) MOE_RCL(false, 64)
+            MOE_RCL(false, 128)
+        }
+#undef MOE_RCL
+    }
+    // wide slices that do not fit shared memory: partials through global memory
     const int nsplit = router_chunked_nsplit(a.d, a.E);
     const dim3 grid((a.T + 7) / 8, nsplit);
     cudaError_t e;

@@ -82,6 +82,22 @@ SMALL = {
     "pair_latent_sigmoid": W.Workload("t_p3", T=1024, d=256, d_ff=192, E=4, K=2, n_shared=1,
                                       shared_d_ff=256, dtype="bf16", gate="sigmoid",
                                       latent_dim=128),
+    # Decode batches (32 < E <= 128, T*K <= 1024): the cluster router and the
+    # one-launch dispatch + gather. Ragged last token block and last slice of d,
+    # both expert widths of the router (64 and 128 lanes), FP32 and BF16, the
+    # sigmoid gate (top_scores/scores) on latent rows, exactly 1024 assignments.
+    "decode_e64_ragged": W.Workload("t_d1", T=100, d=720, d_ff=128, E=64, K=8, n_shared=1,
+                                   shared_d_ff=128, dtype="bf16", gate="softmax_topk",
+                                   bias_std=0.01, skew=1.1),
+    "decode_f32_e96": W.Workload("t_d2", T=37, d=208, d_ff=96, E=96, K=5, n_shared=1,
+                                shared_d_ff=64, dtype="f32", gate="softmax_all_renorm",
+                                has_bias=False),
+    "decode_sigmoid_latent": W.Workload("t_d3", T=60, d=256, d_ff=64, E=48, K=4, n_shared=1,
+                                       shared_d_ff=128, dtype="bf16", gate="sigmoid",
+                                       latent_dim=64),
+    "decode_max_assignments": W.Workload("t_d4", T=128, d=384, d_ff=64, E=128, K=8, n_shared=0,
+                                        shared_d_ff=0, dtype="bf16", gate="softmax_topk",
+                                        bias_std=0.01),
 }
 
 
@@ -143,10 +159,11 @@ def test_route(gate, E, K, dtype, d, with_ws):
                                       ("softmax_topk", 33, 16), ("sigmoid", 120, 4)])
 @pytest.mark.parametrize("dtype,d,T", [("bf16", 272, 200), ("f32", 1024, 64), ("bf16", 4096, 1)])
 def test_route_few_tokens(gate, E, K, dtype, d, T):
-    """Up to 512 tokens with 32 < E <= 128 and a workspace: the chunked FP32
-    router (partial logits per slice of d, 256 long for E <= 64 and 128 long for
-    E <= 128, summed in FP32), including ragged last slices and a single token;
-    E = 256 takes the tensor-core or tiled router."""
+    """Up to 512 tokens with 32 < E <= 128 and a workspace: the FP32 cluster
+    router (partial logits per slice of d, at most 8 slices, summed in slice
+    order through distributed shared memory), including ragged last slices and
+    a single token; slices too wide for shared memory (E = 128, d = 4096) take
+    the two-launch chunked router; E = 256 takes the tensor-core or tiled router."""
     A = api()
     w = W.Workload("r", T=T, d=d, d_ff=16, E=E, K=K, n_shared=0, shared_d_ff=0, dtype=dtype,
                    gate=gate, bias_std=0.02, skew=0.5 if gate != "sigmoid" else 0.0)
@@ -324,6 +341,29 @@ def test_launch_count_grows():
     # router, single-CTA dispatch (T*K = 256 assignments), gate/up, routed down,
     # shared down fused with the combine
     assert A.launch_count() - n0 == 5
+
+
+def test_decode_launches_and_dirty_workspace():
+    """A decode batch routes in one cluster launch and dispatches and gathers in
+    one more; nothing in the workspace carries over between forwards, so a
+    workspace full of garbage gives the same result, bit for bit."""
+    A = api()
+    w = W.WORKLOADS["medium_decode"].resized(T=64, d=512, d_ff=128)
+    inp = W.make_inputs(w, device="cuda")
+    spec = A.LayerSpec.of(w)
+    ws = A.alloc_workspace(spec)
+    torch.cuda.synchronize()
+    n0 = A.launch_count()
+    o1 = A.forward(spec, inp["x"], inp, ws=ws).clone()
+    torch.cuda.synchronize()
+    # router, dispatch + gather, gate/up, down, combine
+    assert A.launch_count() - n0 == 5
+    ws.fill_(0xFF)
+    o2 = A.forward(spec, inp["x"], inp, ws=ws).clone()
+    assert A.workspace_status(ws) == A.MOE_OK
+    assert torch.equal(o1.view(torch.int32), o2.view(torch.int32))
+    o3 = A.forward(spec, inp["x"], inp, ws=ws)
+    assert torch.equal(o1.view(torch.int32), o3.view(torch.int32))
 
 
 def test_bounded_wait_gives_up_and_context_survives():
