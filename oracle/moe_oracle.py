@@ -469,3 +469,165 @@ def routing_stats(r, idx, E):
     P = p.mean(axis=0)
     f = np.bincount(idx.reshape(-1), minlength=E).astype(np.float64) / (T * K)
     return {"aux": float(E * np.sum(f * P)), "z": float(np.mean(lse ** 2)), "P": P, "f": f}
+
+
+# --------------------------------------------------------------------------
+# Backward pass  [K3-SLM] "The actual grouped GEMM, and the gradient path",
+#                "Grouped expert execution and sparse gradients";
+#                [APEX-M3] sections 12.2-12.3 and 13.2 (the forward it differentiates)
+# --------------------------------------------------------------------------
+
+def silu_grad(a):
+    """d SiLU(a) / da = sigma(a) (1 + a (1 - sigma(a)))."""
+    a = f64(a)
+    s = sigmoid(a)
+    return s * (1.0 + a * (1.0 - s))
+
+
+def gate_logit_grad(r, bias, gate, idx, dw, renormalize=False, routed_scale=1.0):
+    """dL/dr [E] of one token from dL/dg [K], the selection idx held fixed
+    (top-K indices carry no gradient; [K3-SLM] "The actual grouped GEMM, and
+    the gradient path"). The chain rule through each mode's own formula:
+
+      softmax_topk        g = softmax over the selected c = r + b
+      softmax_all_renorm  p = softmax over all E of r + b, g = p_sel / sum p_sel
+      sigmoid             s = sigma(r), g = scale * s_sel (/ sum s_sel)
+    The balance bias is a buffer without gradient."""
+    r = f64(r)
+    E = r.shape[0]
+    b = np.zeros(E) if bias is None else f64(bias)
+    idx = np.asarray(idx, dtype=np.int64)
+    dw = f64(dw)
+    dr = np.zeros(E)
+    if gate == GATE_SOFTMAX_TOPK:
+        sel = (r + b)[idx]
+        ex = np.exp(sel - sel.max())
+        g = ex / ex.sum()
+        dr[idx] += g * (dw - np.dot(g, dw))
+    elif gate == GATE_SOFTMAX_ALL_RENORM:
+        z = r + b
+        ez = np.exp(z - z.max())
+        p = ez / ez.sum()
+        P = p[idx].sum()
+        g = p[idx] / P
+        dp = np.zeros(E)
+        dp[idx] = (dw - np.dot(dw, g)) / P
+        dr = p * (dp - np.dot(p, dp))
+    elif gate == GATE_SIGMOID:
+        s = sigmoid(r)
+        ds = np.zeros(E)
+        if renormalize:
+            S = s[idx].sum()
+            ds[idx] = routed_scale * (dw - np.dot(dw, s[idx]) / S) / S
+        else:
+            ds[idx] = routed_scale * dw
+        dr = ds * s * (1.0 - s)
+    else:
+        raise ValueError(gate)
+    return dr
+
+
+def moe_backward(x, params, dout, gate, K, renormalize=False, routed_scale=1.0, routing=None):
+    """Gradients of L = sum(dout * out) for the layer of moe_forward, the
+    routing (selection) held fixed. Per token and per selected expert, the
+    chain rule of
+
+        a = z W_gate[e], u = z W_up[e], h = SiLU(a) * u, y = h W_down[e]
+        out = sum_k g_k y_k (latent: projected by W_up_latent) + shared(x)
+
+    with z = x (latent: x W_down_latent) and g from the router logits
+    x W_router (gate_logit_grad). ``routing`` = (idx [T, K]) replaces the
+    oracle's own selection (near ties); the weights are recomputed from the
+    logits either way.
+
+    Experts that no token selects get no gradient ([K3-SLM] "Grouped expert
+    execution and sparse gradients": inactive experts stay outside autograd):
+    their entries of dW_gate / dW_up / dW_down are zero and ``active`` [E] is
+    False for them. Returns a dict of float64 arrays: dx, dW_router, dW_gate,
+    dW_up, dW_down, dWs_gate, dWs_up, dWs_down (or None), dW_down_latent,
+    dW_up_latent (or None), active, dw [T, K] (dL/dg)."""
+    xn = f64(_to_np(x))
+    g_out = f64(_to_np(dout))
+    T, d = xn.shape
+    Wr = f64(_to_np(params["W_router"]))
+    bias = _to_np(params.get("bias"))
+    bias = None if bias is None else f64(bias)
+    cache = _WeightCache(params, max_entries=10 ** 6)
+    E = params["W_gate"].shape[0]
+    r = xn @ Wr
+    idx = route(xn, Wr, bias, gate, K, renormalize, routed_scale)["idx"] if routing is None \
+        else np.asarray(routing, dtype=np.int64)
+    latent = params.get("W_down_latent") is not None
+    Wdl = cache.get("W_down_latent") if latent else None
+    Wul = cache.get("W_up_latent") if latent else None
+    de = Wdl.shape[1] if latent else d
+    F = params["W_gate"].shape[2]
+    out = {
+        "dx": np.zeros((T, d)), "dW_router": np.zeros_like(Wr),
+        "dW_gate": np.zeros((E, de, F)), "dW_up": np.zeros((E, de, F)),
+        "dW_down": np.zeros((E, F, de)), "active": np.zeros(E, dtype=bool),
+        "dw": np.zeros((T, K)),
+    }
+    shared = params.get("Ws_gate") is not None
+    if shared:
+        S, _, Fs = params["Ws_gate"].shape
+        out["dWs_gate"] = np.zeros((S, d, Fs))
+        out["dWs_up"] = np.zeros((S, d, Fs))
+        out["dWs_down"] = np.zeros((S, Fs, d))
+    else:
+        out["dWs_gate"] = out["dWs_up"] = out["dWs_down"] = None
+    out["dW_down_latent"] = np.zeros_like(Wdl) if latent else None
+    out["dW_up_latent"] = np.zeros_like(Wul) if latent else None
+
+    def ffn_backward(zt, gy, Wg, Wu, Wd):
+        """(y, dWg, dWu, dWd, dz) of one SwiGLU expert at one row, upstream gy."""
+        a = zt @ Wg
+        u = zt @ Wu
+        h = silu(a) * u
+        y = h @ Wd
+        dh = gy @ Wd.T
+        da = dh * u * silu_grad(a)
+        du = dh * silu(a)
+        return y, np.outer(zt, da), np.outer(zt, du), np.outer(h, gy), da @ Wg.T + du @ Wu.T
+
+    for t in range(T):
+        xt = xn[t]
+        zt = xt @ Wdl if latent else xt
+        w_t = gates_for(r[t], bias, gate, idx[t], renormalize, routed_scale)
+        gt = g_out[t]
+        g_lat = gt @ Wul.T if latent else gt
+        dz = np.zeros(de)
+        routed = np.zeros(de)
+        dw = np.zeros(K)
+        for k in range(K):
+            e = int(idx[t, k])
+            out["active"][e] = True
+            y, dWg, dWu, dWd, dzk = ffn_backward(zt, w_t[k] * g_lat, cache.get("W_gate", e),
+                                                 cache.get("W_up", e), cache.get("W_down", e))
+            # y here is the expert output for upstream w_k * g: the unweighted output
+            # is the same y (it does not depend on the upstream gradient)
+            routed = routed + w_t[k] * y
+            dw[k] = np.dot(g_lat, y)
+            out["dW_gate"][e] += dWg
+            out["dW_up"][e] += dWu
+            out["dW_down"][e] += dWd
+            dz = dz + dzk
+        out["dw"][t] = dw
+        if latent:
+            out["dW_up_latent"] += np.outer(routed, gt)
+            out["dW_down_latent"] += np.outer(xt, dz)
+            dxt = dz @ Wdl.T
+        else:
+            dxt = dz
+        if shared:
+            for s in range(S):
+                _, dWg, dWu, dWd, dzs = ffn_backward(xt, gt, cache.get("Ws_gate", s),
+                                                     cache.get("Ws_up", s), cache.get("Ws_down", s))
+                out["dWs_gate"][s] += dWg
+                out["dWs_up"][s] += dWu
+                out["dWs_down"][s] += dWd
+                dxt = dxt + dzs
+        dr = gate_logit_grad(r[t], bias, gate, idx[t], dw, renormalize, routed_scale)
+        out["dW_router"] += np.outer(xt, dr)
+        out["dx"][t] = dxt + dr @ Wr.T
+    return out

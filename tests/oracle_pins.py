@@ -384,8 +384,84 @@ def pin_routing_stats(o):
     assert abs(b["z"] - np.mean((lse + 2.5) ** 2)) < 1e-12
 
 
+# -- Backward -------------------------------------------------------------------
+
+def _fd_loss(o, x, p, dout, gate, K, idx, renorm, scale):
+    """L = sum(dout * out) of the layer with the selection idx held fixed and
+    the gate weights recomputed from the (perturbed) router logits: built from
+    the oracle's forward pieces only."""
+    xn = np.asarray(x, float)
+    r = o.router_logits(xn, p["W_router"])
+    L = 0.0
+    for t in range(xn.shape[0]):
+        w_t = o.gates_for(r[t], p.get("bias"), gate, idx[t], renorm, scale)
+        L += float(np.dot(dout[t], o.moe_forward_token(xn[t], idx[t], w_t, p, None)))
+    return L
+
+
+def pin_backward_finite_differences(o):
+    """Every gradient of moe_backward against central differences of the
+    forward (L = sum(dout * out), selection fixed), for each gate mode, with
+    shared experts, renormalised and scaled sigmoid gates and the latent
+    variant; experts nobody selects get no gradient (kimi_k3 StableLatentMoE,
+    'Grouped expert execution and sparse gradients')."""
+    rng = np.random.default_rng(11)
+    eps = 1e-5
+    cases = [(o.GATE_SOFTMAX_TOPK, 0, False, 1.0, 2), (o.GATE_SOFTMAX_ALL_RENORM, 0, False, 1.0, 1),
+             (o.GATE_SIGMOID, 0, True, 2.5, 2), (o.GATE_SIGMOID, 5, False, 1.0, 0)]
+    for gate, L, renorm, scale, S in cases:
+        T, d, F, E, K, Fs = 5, 7, 6, 6, 2, 4
+        p = tiny_params(rng, d, F, E, S, Fs, latent=L)
+        p["bias"] = rng.normal(scale=0.01, size=E)
+        p["bias"][E - 1] = -50.0  # expert E-1 is never selected
+        x = rng.normal(size=(T, d))
+        dout = rng.normal(size=(T, d))
+        idx = o.route(x, p["W_router"], p["bias"], gate, K, renorm, scale)["idx"]
+        assert not (idx == E - 1).any()
+        g = o.moe_backward(x, p, dout, gate, K, renorm, scale)
+        assert not g["active"][E - 1] and g["active"][np.unique(idx)].all()
+        for name in ("dW_gate", "dW_up", "dW_down"):
+            assert not g[name][E - 1].any(), name
+
+        def check(name, arr_key, grad, picks):
+            for ii in picks:
+                base = (p[arr_key] if arr_key != "x" else x)
+                a = np.array(base, dtype=float, copy=True)
+                q = dict(p)
+                orig = a[ii]
+                a[ii] = orig + eps
+                if arr_key == "x":
+                    lp = _fd_loss(o, a, q, dout, gate, K, idx, renorm, scale)
+                else:
+                    q[arr_key] = a
+                    lp = _fd_loss(o, x, q, dout, gate, K, idx, renorm, scale)
+                a[ii] = orig - eps
+                if arr_key == "x":
+                    lm = _fd_loss(o, a, q, dout, gate, K, idx, renorm, scale)
+                else:
+                    q[arr_key] = a
+                    lm = _fd_loss(o, x, q, dout, gate, K, idx, renorm, scale)
+                fd = (lp - lm) / (2 * eps)
+                assert abs(grad[ii] - fd) <= 1e-7 * (1.0 + abs(fd)), (gate, name, ii, grad[ii], fd)
+
+        def picks(shape, n):
+            return [tuple(int(rng.integers(0, s)) for s in shape) for _ in range(n)]
+
+        check("dx", "x", g["dx"], [(t, j) for t in range(T) for j in range(d)])
+        check("dW_router", "W_router", g["dW_router"], [(i, j) for i in range(d) for j in range(E)])
+        for name, key in (("dW_gate", "W_gate"), ("dW_up", "W_up"), ("dW_down", "W_down")):
+            check(name, key, g[name], picks(p[key].shape, 10))
+        if S:
+            for name, key in (("dWs_gate", "Ws_gate"), ("dWs_up", "Ws_up"), ("dWs_down", "Ws_down")):
+                check(name, key, g[name], picks(p[key].shape, 8))
+        if L:
+            for name, key in (("dW_down_latent", "W_down_latent"), ("dW_up_latent", "W_up_latent")):
+                check(name, key, g[name], picks(p[key].shape, 8))
+
+
 ALL_PINS = [pin_silu_table, pin_swiglu_example, pin_ffn_down_projection, pin_router_example,
             pin_tie_break, pin_gate_formulas, pin_sigmoid_example, pin_stable_dispatch_example,
             pin_dispatch_vs_library, pin_counts_sum, pin_output_composition,
             pin_sorted_equals_naive, pin_shared_concat_identity, pin_latent_reduces_to_plain,
-            pin_quantile, pin_sign_bias_example, pin_routing_stats]
+            pin_quantile, pin_sign_bias_example, pin_routing_stats,
+            pin_backward_finite_differences]

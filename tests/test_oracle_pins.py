@@ -154,11 +154,43 @@ def _mut_z_not_squared(m):
     m.routing_stats = stats
 
 
+def _mut_bwd_silu_grad_short(m):
+    m.silu_grad = lambda a: m.sigmoid(a)
+
+
+def _mut_bwd_gate_grad_sign(m):
+    orig = m.gate_logit_grad
+    m.gate_logit_grad = lambda *a, **k: -orig(*a, **k)
+
+
+def _mut_bwd_no_router_grad(m):
+    m.gate_logit_grad = lambda r, *a, **k: np.zeros_like(np.asarray(r, float))
+
+
+def _mut_bwd_gate_up_swapped(m):
+    orig = m.moe_backward
+
+    def bwd(*a, **k):
+        g = orig(*a, **k)
+        g["dW_gate"], g["dW_up"] = g["dW_up"], g["dW_gate"]
+        return g
+    m.moe_backward = bwd
+
+
+def _mut_bwd_renorm_ignored(m):
+    orig = m.gate_logit_grad
+
+    def ggrad(r, bias, gate, idx, dw, renormalize=False, routed_scale=1.0):
+        return orig(r, bias, gate, idx, dw, False, routed_scale)
+    m.gate_logit_grad = ggrad
+
+
 MUTANTS = [_mut_silu_sign, _mut_gate_up_swapped, _mut_down_transposed, _mut_softmax_over_all,
            _mut_tie_to_higher, _mut_dispatch_unstable, _mut_drop_shared,
            _mut_sigmoid_corrected_weights, _mut_quantile_lower, _mut_quantile_no_centre,
            _mut_latent_no_up, _mut_sign_bias_flipped, _mut_aux_share_over_tokens,
-           _mut_z_not_squared]
+           _mut_z_not_squared, _mut_bwd_silu_grad_short, _mut_bwd_gate_grad_sign,
+           _mut_bwd_no_router_grad, _mut_bwd_gate_up_swapped, _mut_bwd_renorm_ignored]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)
