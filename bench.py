@@ -50,6 +50,7 @@ def parse():
     p.add_argument("--workload", default=None)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-backward", action="store_true", help="skip the timed backward pass")
     p.add_argument("--out-dtype", choices=["f32", "bf16"], default="f32")
     return p.parse_args()
 
@@ -119,6 +120,19 @@ def gate_up_bytes(w, counts=None) -> float:
         b += w.n_shared * 2 * w.d * w.shared_d_ff * es
         b += w.T * w.d * es + w.T * w.n_shared * w.shared_d_ff * es
     return float(b)
+
+
+def backward_flops(w) -> float:
+    """Algorithmic FLOPs of the backward: twice the forward's expert GEMMs
+    (input and weight gradients), the router's two, the latent projections'
+    four; the recomputation of the gate/up products is not counted."""
+    de = w.latent_dim or w.d
+    f = 12.0 * w.T * w.K * de * w.d_ff
+    f += 12.0 * w.T * w.d * w.shared_d_ff * w.n_shared
+    f += 4.0 * w.T * w.d * w.E
+    if w.latent_dim:
+        f += 8.0 * w.T * w.d * w.latent_dim
+    return f
 
 
 def layer_bytes(w, counts=None) -> float:
@@ -400,6 +414,42 @@ def run_ours(args, name):
                         "CUDA events, L2 flushed before each call"}
         del dws
 
+    # backward (moe_backward after the forward on ws): its own pass, outside the
+    # timed forward region
+    bwd = None
+    if world == 1 and not args.no_backward:
+        torch.manual_seed(1)
+        dout = torch.randn(w.T, w.d, device=dev, dtype=torch.float32)
+        bws = torch.empty(api.backward_workspace_size(spec), dtype=torch.uint8, device=dev)
+        grads = {n: torch.empty(s, dtype=torch.float32, device=dev)
+                 for n, s in api.grad_shapes(spec).items()}
+        n_bw = max(1, min(args.steps, 5))
+        b_ms = []
+        for i in range(n_bw + 2):
+            flush.fill_(i & 0xFF)
+            step()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            api.backward(spec, inp["x"], inp, dout, ws, grads=grads, bws=bws, stream=stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= 2:
+                b_ms.append(a.elapsed_time(b))
+        st = api.workspace_status(ws, stream)
+        if st != api.MOE_OK:
+            raise RuntimeError(f"device status after the backward: {api.status_string(st)}")
+        bms = sum(b_ms) / len(b_ms)
+        bfl = backward_flops(w)
+        pk0 = peaks()
+        bwd = {"ms": bms, "tflops": bfl / (bms / 1e3) / 1e12, "flops_per_step": bfl,
+               "bound": "alu", "peak": pk0["fp32_tflops"], "unit": "TFLOP/s",
+               "frac": bfl / (bms / 1e3) / 1e12 / pk0["fp32_tflops"],
+               "note": "moe_backward (all gradients) after a forward on the same workspace, "
+                       "FP32 FFMA grouped GEMMs; L2 flushed before each forward; "
+                       "CUDA events around the backward alone"}
+        del bws, grads, dout
+
     # end to end through the host-buffer entry point (copies inside the timed region)
     e2e = None
     if not args.no_e2e:
@@ -479,6 +529,7 @@ def run_ours(args, name):
         "stage_ms": {k: v / max(1, nb) for k, v in breakdown.items() if v > 0},
         "stage_ms_note": "separate instrumented pass (an event between every stage)",
         "routing_diagnostics": diag,
+        "backward": bwd,
         "gpu_launches": int(launches),
         "wall_s_timed": t_wall,
         "clocks": clk,

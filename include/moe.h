@@ -1,6 +1,7 @@
 /*
- * moe.h - C ABI of the GB300 (sm_103a) forward pass of a top-K routed
- * Mixture-of-Experts SwiGLU FFN layer with always-on shared experts.
+ * moe.h - C ABI of the GB300 (sm_103a) forward (and backward) pass of a
+ * top-K routed Mixture-of-Experts SwiGLU FFN layer with always-on shared
+ * experts.
  *
  * The layer (APEX-1 Mathematical Reference Part 3, section 13.2):
  *
@@ -261,6 +262,46 @@ moe_status moe_routing_stats(const moe_config* cfg, const void* x, const float* 
  * N = T tokens), bias [E] FP32 device, updated in place. */
 moe_status moe_sign_bias_update(int32_t E, int32_t N, int32_t K, const int32_t* counts,
                                 float* bias, float alpha, void* stream);
+
+/* Gradients written by moe_backward: FP32 device arrays, row-major. dx is
+ * required; any other pointer may be NULL (that gradient is not computed). */
+typedef struct moe_grads {
+    float* dx;              /* [T, d] */
+    float* dW_router;       /* [d, E] */
+    float* dW_gate;         /* [E, d_e, d_ff]  d_e = latent_dim ? latent_dim : d */
+    float* dW_up;           /* [E, d_e, d_ff] */
+    float* dW_down;         /* [E, d_ff, d_e] */
+    float* dWs_gate;        /* [S, d, shared_d_ff] */
+    float* dWs_up;          /* [S, d, shared_d_ff] */
+    float* dWs_down;        /* [S, shared_d_ff, d] */
+    float* dW_down_latent;  /* [d, latent_dim] */
+    float* dW_up_latent;    /* [latent_dim, d] */
+} moe_grads;
+
+/* Bytes of the backward's own scratch workspace (bws of moe_backward). */
+moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Backward pass: the gradients of L = sum(dout * out) of the forward that
+ * last ran on `ws` (moe_forward with the same cfg, x and weights; its routing
+ * and dispatch, and for the latent variant z and the routed rows, are read
+ * from ws), with that forward's expert selection held fixed - the top-K
+ * indices carry no gradient (kimi_k3 StableLatentMoE, "The actual grouped
+ * GEMM, and the gradient path"):
+ *     gate weights g -> router logits r -> W_router and x, through the gate
+ *     rule's formula (the balance bias is a buffer without gradient);
+ *     the routed and shared SwiGLU experts, their weights and their input;
+ *     the latent projections.
+ * Experts that no token selected get no gradient: their slices of dW_gate,
+ * dW_up and dW_down are NOT written (kimi_k3 StableLatentMoE, "Grouped
+ * expert execution and sparse gradients"); the workspace's counts tell which.
+ * Every other requested gradient is overwritten. Sums run in a fixed order:
+ * bit-reproducible. Arithmetic: FP32 (BF16 inputs converted exactly).
+ *   x [T, d] (dtype), dout [T, d] FP32 device, 16-byte aligned.
+ *   ws: the forward's workspace (moe_workspace_size bytes, 256-byte aligned).
+ *   bws: moe_backward_workspace_size bytes, 256-byte aligned. */
+moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights* w,
+                        const float* dout, const moe_grads* grads, void* ws, size_t ws_bytes,
+                        void* bws, size_t bws_bytes, void* stream);
 
 /* Synchronises `stream`, then reads and clears the device-side error word of
  * the workspace: MOE_OK, MOE_ERR_TIMEOUT (a bounded device wait ran out and

@@ -46,6 +46,14 @@ class Weights(ctypes.Structure):
                  "W_down_latent", "W_up_latent")]
 
 
+GRAD_NAMES = ("dx", "dW_router", "dW_gate", "dW_up", "dW_down", "dWs_gate", "dWs_up",
+              "dWs_down", "dW_down_latent", "dW_up_latent")
+
+
+class Grads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in GRAD_NAMES]
+
+
 class Views(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("topk_idx", "topk_w", "margin", "top_scores", "scores", "counts", "offsets",
@@ -81,6 +89,9 @@ def lib() -> ctypes.CDLL:
             "moe_sign_bias_update": (ctypes.c_int, [i32, i32, i32, vp, vp, ctypes.c_float, vp]),
             "moe_routing_stats": (ctypes.c_int, [cfgp, vp, vp, vp, vp, vp, sz, vp]),
             "moe_workspace_status": (ctypes.c_int, [vp, vp]),
+            "moe_backward_workspace_size": (ctypes.c_int, [cfgp, ctypes.POINTER(sz)]),
+            "moe_backward": (ctypes.c_int, [cfgp, vp, ctypes.POINTER(Weights), vp,
+                                            ctypes.POINTER(Grads), vp, sz, vp, sz, vp]),
             "moe_timing_begin": (ctypes.c_int, [i32, ctypes.c_uint32]),
             "moe_timing_end": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float), i32,
                                               ctypes.POINTER(i32), ctypes.POINTER(i32)]),
@@ -299,6 +310,58 @@ def forward(spec: LayerSpec, x: torch.Tensor, params: dict, out: torch.Tensor | 
     _check(lib().moe_forward(ctypes.byref(spec.config()), x.data_ptr(), ctypes.byref(w),
                              out.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)),
            "moe_forward")
+    return out
+
+
+def backward_workspace_size(spec: LayerSpec) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_backward_workspace_size(ctypes.byref(spec.config()), ctypes.byref(n)),
+           "moe_backward_workspace_size")
+    return int(n.value)
+
+
+def grad_shapes(spec: LayerSpec) -> dict:
+    de = spec.latent_dim or spec.d
+    S, Fs, L = spec.n_shared, spec.shared_d_ff, spec.latent_dim
+    sh = {"dx": (spec.T, spec.d), "dW_router": (spec.d, spec.E),
+          "dW_gate": (spec.E, de, spec.d_ff), "dW_up": (spec.E, de, spec.d_ff),
+          "dW_down": (spec.E, spec.d_ff, de)}
+    if S:
+        sh.update(dWs_gate=(S, spec.d, Fs), dWs_up=(S, spec.d, Fs), dWs_down=(S, Fs, spec.d))
+    if L:
+        sh.update(dW_down_latent=(spec.d, L), dW_up_latent=(L, spec.d))
+    return sh
+
+
+def backward(spec: LayerSpec, x: torch.Tensor, params: dict, dout: torch.Tensor, ws: torch.Tensor,
+             grads: dict | None = None, bws: torch.Tensor | None = None, stream=None) -> dict:
+    """moe_backward after a moe_forward on ws: FP32 gradients of sum(dout * out).
+    ``grads`` maps names of GRAD_NAMES to preallocated FP32 tensors (absent
+    names are allocated, zero-filled: an expert slice that gets no gradient
+    stays as given); a name mapped to None is not computed."""
+    _dev(x, spec.torch_dtype, "x", (spec.T, spec.d))
+    _dev(dout, torch.float32, "dout", (spec.T, spec.d))
+    shapes = grad_shapes(spec)
+    out = {}
+    given = grads or {}
+    for n, shp in shapes.items():
+        if n in given:
+            if given[n] is not None:
+                out[n] = _dev(given[n], torch.float32, n, shp)
+        else:
+            out[n] = torch.zeros(shp, dtype=torch.float32, device=x.device)
+    if "dx" not in out:
+        raise ValueError("dx is required")
+    g = Grads()
+    for n in GRAD_NAMES:
+        setattr(g, n, out[n].data_ptr() if n in out else None)
+    if bws is None:
+        bws = torch.empty(backward_workspace_size(spec), dtype=torch.uint8, device=x.device)
+    w = weights_struct(spec, params)
+    _check(lib().moe_backward(ctypes.byref(spec.config()), x.data_ptr(), ctypes.byref(w),
+                              dout.data_ptr(), ctypes.byref(g), ws.data_ptr(), ws.numel(),
+                              bws.data_ptr(), bws.numel(), _stream(stream)),
+           "moe_backward")
     return out
 
 

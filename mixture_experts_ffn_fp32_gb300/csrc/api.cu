@@ -592,6 +592,39 @@ MOE_API moe_status moe_forward(const moe_config* cfg, const void* x, const moe_w
     return forward_impl(*cfg, x, *w, out, static_cast<uint8_t*>(ws), static_cast<cudaStream_t>(stream));
 }
 
+MOE_API moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes) {
+    if (!cfg || !bytes) return MOE_ERR_INVALID_ARG;
+    const moe_status v = validate_config(*cfg);
+    if (v != MOE_OK) return v;
+    *bytes = plan_backward(*cfg).total;
+    return MOE_OK;
+}
+
+MOE_API moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights* w,
+                                const float* dout, const moe_grads* grads, void* ws,
+                                size_t ws_bytes, void* bws, size_t bws_bytes, void* stream) {
+    if (!cfg || !x || !dout || !grads || !grads->dx || !ws || !bws) return MOE_ERR_INVALID_ARG;
+    moe_status v = validate_config(*cfg);
+    if (v != MOE_OK) return v;
+    if ((v = check_weights(*cfg, w)) != MOE_OK) return v;
+    if (!aligned16(x) || !aligned16(dout) || (reinterpret_cast<uintptr_t>(ws) & 255u) ||
+        (reinterpret_cast<uintptr_t>(bws) & 255u))
+        return MOE_ERR_INVALID_ARG;
+    const float* outs[] = {grads->dx, grads->dW_router, grads->dW_gate, grads->dW_up,
+                           grads->dW_down, grads->dWs_gate, grads->dWs_up, grads->dWs_down,
+                           grads->dW_down_latent, grads->dW_up_latent};
+    for (const float* p : outs)
+        if (p && (reinterpret_cast<uintptr_t>(p) & 3u)) return MOE_ERR_INVALID_ARG;
+    if ((grads->dWs_gate || grads->dWs_up || grads->dWs_down) && cfg->n_shared == 0)
+        return MOE_ERR_INVALID_ARG;
+    if ((grads->dW_down_latent || grads->dW_up_latent) && cfg->latent_dim == 0)
+        return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < plan_workspace(*cfg).total || bws_bytes < plan_backward(*cfg).total)
+        return MOE_ERR_WORKSPACE;
+    return backward_impl(*cfg, x, *w, dout, *grads, static_cast<uint8_t*>(ws),
+                         static_cast<uint8_t*>(bws), static_cast<cudaStream_t>(stream));
+}
+
 MOE_API moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const moe_weights* w,
                                     void* out_host, void* ws, size_t ws_bytes, void* stream) {
     if (!cfg || !x_host || !out_host || !ws) return MOE_ERR_INVALID_ARG;

@@ -1,0 +1,336 @@
+// Backward pass of the layer: gradients of L = sum(dout * out) with the
+// routing of the forward held fixed (the top-K selection carries no
+// gradient). Source: kimi_k3 StableLatentMoE, "The actual grouped GEMM, and
+// the gradient path" (backpropagation through the scatter, both grouped GEMMs
+// and the gate weights to the selected router scores) and "Grouped expert
+// execution and sparse gradients" (experts without rows get no gradient); the
+// forward it differentiates is APEX-1 Mathematical Reference Part 3, sections
+// 12.2 and 13.2.
+//
+// Per routed assignment at sorted position pos (token t, expert e, gate g)
+// with upstream gy = dout[t] (latent: dout[t] W_up_latent^T):
+//   dh' = gy W_down[e]^T                          (G1, unweighted)
+//   a, u = z W_gate[e], z W_up[e] (recomputed), h = SiLU(a) u
+//   da = g dh' u SiLU'(a), du = g dh' SiLU(a)     (SwiGLU backward epilogue)
+//   dg = sum dh' h  (= gy . y)                    (gate weight gradient)
+//   dz = da W_gate[e]^T + du W_up[e]^T            (G3)
+//   dW_down[e] += (g h)^T gy, dW_gate[e] += z^T da, dW_up[e] += z^T du
+// The shared experts the same with g = 1 on every token; the router logits
+// get dr from dg through the gate mode's formula, dW_router = x^T dr and
+// dx += dr W_router^T; the latent projections their two GEMMs. All sums are
+// plain stores and accumulations in a fixed order: the result is
+// reproducible bit for bit. This first form runs every contraction on the
+// CUDA cores in FP32 (gemm_gen.cu), BF16 operands converted exactly.
+#include <string.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+// dr[t, :] from the gate-weight gradients of token t, one warp per token.
+// dg of slot k is the fixed-order sum of the SwiGLU epilogue's column-tile
+// partials of its sorted position. Softmax modes (both select on and weight
+// by a softmax over the selected logits): dr_e(k) = g_k (dg_k - sum_j g_j dg_j).
+// Sigmoid: ds_k = scale dg_k, renormalised: scale (dg_k - sum_j dg_j s_j / S) / S
+// with S = sum_j s_j; dr = ds s (1 - s). Unselected experts: 0.
+__global__ void __launch_bounds__(256) router_bwd_kernel(const float* __restrict__ dwpart, int ntf,
+                                                         const int32_t* __restrict__ inv,
+                                                         const int32_t* __restrict__ idx,
+                                                         const float* __restrict__ w,
+                                                         const float* __restrict__ scores, int T,
+                                                         int K, int E, int gate, int renorm,
+                                                         float scale, float* __restrict__ dr,
+                                                         float* __restrict__ dg_out) {
+    pdl_wait();
+    pdl_trigger();
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (t >= T) return;
+    const int lane = threadIdx.x & 31;
+    float dg = 0.0f, gk = 0.0f, sk = 0.0f;
+    int ek = 0;
+    if (lane < K) {
+        const int pos = inv[static_cast<size_t>(t) * K + lane];
+        const float* pp = dwpart + static_cast<size_t>(pos) * ntf;
+        for (int i = 0; i < ntf; ++i) dg += pp[i];
+        ek = idx[static_cast<size_t>(t) * K + lane];
+        gk = w[static_cast<size_t>(t) * K + lane];
+        if (gate == MOE_GATE_SIGMOID) sk = scores[static_cast<size_t>(t) * E + ek];
+        if (dg_out != nullptr) dg_out[static_cast<size_t>(t) * K + lane] = dg;
+    }
+    float drk;
+    if (gate == MOE_GATE_SIGMOID) {
+        float ds;
+        if (renorm) {
+            float S = lane < K ? sk : 0.0f, sd = lane < K ? dg * sk : 0.0f;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                S += __shfl_xor_sync(0xffffffffu, S, o);
+                sd += __shfl_xor_sync(0xffffffffu, sd, o);
+            }
+            ds = scale * (dg - sd / S) / S;
+        } else {
+            ds = scale * dg;
+        }
+        drk = ds * sk * (1.0f - sk);
+    } else {
+        float sgd = lane < K ? gk * dg : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sgd += __shfl_xor_sync(0xffffffffu, sgd, o);
+        drk = gk * (dg - sgd);
+    }
+    float* row = dr + static_cast<size_t>(t) * E;
+    for (int e = lane; e < E; e += 32) row[e] = 0.0f;
+    __syncwarp();
+    if (lane < K) row[ek] = drk;
+}
+
+GenOp op(const void* p, int bf16, long long s0, long long s1, long long zs = 0,
+         const int32_t* idx0 = nullptr, const int32_t* idx1 = nullptr) {
+    GenOp o;
+    o.p = p;
+    o.bf16 = bf16;
+    o.s0 = s0;
+    o.s1 = s1;
+    o.zs = zs;
+    o.idx0 = idx0;
+    o.idx1 = idx1;
+    return o;
+}
+
+GenGemm gemm(int mode, int M, int N, int K, int Z, GenOp A, int a_m_contig, GenOp B,
+             int b_n_contig, float* C, long long ldc, long long c_zs = 0,
+             const int32_t* offsets = nullptr) {
+    GenGemm g;
+    memset(&g, 0, sizeof(g));
+    g.mode = mode;
+    g.offsets = offsets;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.Z = Z;
+    g.A = A;
+    g.B0 = B;
+    g.B1 = B;
+    g.a_m_contig = a_m_contig;
+    g.b_n_contig = b_n_contig;
+    g.C = C;
+    g.ldc = ldc;
+    g.c_zs = c_zs;
+    return g;
+}
+
+const void* offset_elems(const void* p, long long n, int bf16) {
+    return static_cast<const uint8_t*>(p) + n * (bf16 ? 2 : 4);
+}
+
+}  // namespace
+
+BwdLayout plan_backward(const moe_config& c) {
+    BwdLayout B;
+    memset(&B, 0, sizeof(B));
+    const size_t T = c.T, TK = T * c.K, F = c.d_ff;
+    const size_t de = c.latent_dim ? c.latent_dim : c.d;
+    const size_t SF = static_cast<size_t>(c.n_shared) * (c.n_shared ? c.shared_d_ff : 0);
+    const size_t L = c.latent_dim;
+    const size_t ntf = gen_gemm_ntiles(c.d_ff);
+    size_t o = 0;
+    auto take = [&](size_t floats) {
+        const size_t at = o;
+        o = (o + floats * 4 + 255) & ~static_cast<size_t>(255);
+        return at;
+    };
+    B.dhp = take(TK * F);
+    B.da = take(TK * F);
+    B.du = take(TK * F);
+    B.hw = take(TK * F);
+    B.dwpart = take(TK * ntf);
+    B.dxs = take(TK * de);
+    B.dhs = SF ? take(T * SF) : 0;
+    B.das = SF ? take(T * SF) : 0;
+    B.dus = SF ? take(T * SF) : 0;
+    B.hs = SF ? take(T * SF) : 0;
+    B.dr = take(T * c.E);
+    B.dg = take(TK);
+    B.glat = L ? take(T * L) : 0;
+    B.routed = L ? take(T * L) : 0;
+    B.dz = L ? take(T * L) : 0;
+    B.total = o;
+    return B;
+}
+
+moe_status backward_impl(const moe_config& c, const void* x, const moe_weights& w, const float* dout,
+                         const moe_grads& gr, uint8_t* ws, uint8_t* bws, cudaStream_t s) {
+    const WsLayout L = plan_workspace(c);
+    const BwdLayout BL = plan_backward(c);
+    const int bf = c.dtype == MOE_BF16 ? 1 : 0;
+    const int T = c.T, K = c.K, E = c.E, TK = T * K, F = c.d_ff, d = c.d;
+    const int lat = c.latent_dim, de = lat ? lat : d;
+    const int S = c.n_shared, Fs = S ? c.shared_d_ff : 0, SF = S * Fs;
+    auto WP = [&](size_t off) { return static_cast<void*>(ws + off); };
+    auto BP = [&](size_t off) { return reinterpret_cast<float*>(bws + off); };
+    const int32_t* stok = static_cast<const int32_t*>(WP(L.sorted_token));
+    const float* sw = static_cast<const float*>(WP(L.sorted_w));
+    const int32_t* inv = static_cast<const int32_t*>(WP(L.inv));
+    const int32_t* offsets = static_cast<const int32_t*>(WP(L.offsets));
+    const int32_t* tidx = static_cast<const int32_t*>(WP(L.topk_idx));
+    const float* tw = static_cast<const float*>(WP(L.topk_w));
+    const float* scores = L.scores ? static_cast<const float*>(WP(L.scores)) : nullptr;
+    float *dhp = BP(BL.dhp), *da = BP(BL.da), *du = BP(BL.du), *hw = BP(BL.hw);
+    float *dwpart = BP(BL.dwpart), *dxs = BP(BL.dxs), *dr = BP(BL.dr), *dg = BP(BL.dg);
+    const int ntf = gen_gemm_ntiles(F);
+    cudaError_t e;
+#define RUN(G, EPI)                                                      \
+    do {                                                                 \
+        if ((e = launch_gen_gemm((G), (EPI), s)) != cudaSuccess) return MOE_ERR_CUDA; \
+    } while (0)
+
+    // upstream gradient of the routed sum, and the rows the experts act on
+    const float* gy = dout;
+    long long ld_gy = d;
+    const void* zsrc = x;
+    long long ld_z = d;
+    int z_bf = bf;
+    if (lat) {
+        float* glat = BP(BL.glat);
+        float* routed = BP(BL.routed);
+        // gy = dout W_up_latent^T
+        RUN(gemm(GEN_DENSE, T, lat, d, 1, op(dout, 0, d, 1), 0, op(w.W_up_latent, bf, 1, d), 0,
+                 glat, lat),
+            GEN_EPI_STORE);
+        if (gr.dW_up_latent) {
+            // routed sum of the forward (latent width), then dW_up_latent = routed^T dout
+            if ((e = launch_gather_sum(static_cast<const float*>(WP(L.ys)), inv, T, K, lat, nullptr,
+                                       routed, 0, s)) != cudaSuccess)
+                return MOE_ERR_CUDA;
+            RUN(gemm(GEN_DENSE, lat, d, T, 1, op(routed, 0, 1, lat), 1, op(dout, 0, d, 1), 1,
+                     gr.dW_up_latent, d),
+                GEN_EPI_STORE);
+        }
+        gy = glat;
+        ld_gy = lat;
+        zsrc = WP(L.z);
+        ld_z = lat;
+        z_bf = 1;
+    }
+
+    // routed experts
+    // G1: dh' = gy[tok] W_down[e]^T
+    RUN(gemm(GEN_MSEG, TK, F, de, E, op(gy, 0, ld_gy, 1, 0, stok), 0,
+             op(w.W_down, bf, 1, de, static_cast<long long>(F) * de), 0, dhp, F, 0, offsets),
+        GEN_EPI_STORE);
+    // a, u recomputed; SwiGLU backward with the gate weights
+    {
+        GenGemm g = gemm(GEN_MSEG, TK, F, de, E, op(zsrc, z_bf, ld_z, 1, 0, stok), 0,
+                         op(w.W_gate, bf, F, 1, static_cast<long long>(de) * F), 1, nullptr, F);
+        g.B1 = op(w.W_up, bf, F, 1, static_cast<long long>(de) * F);
+        g.offsets = offsets;
+        g.rowscale = sw;
+        g.dh = dhp;
+        g.da = da;
+        g.du = du;
+        g.hw = hw;
+        g.dwpart = dwpart;
+        RUN(g, GEN_EPI_SWIGLU_BWD);
+    }
+    // G3: dz rows = da W_gate[e]^T + du W_up[e]^T
+    {
+        GenGemm g = gemm(GEN_MSEG, TK, de, F, E, op(da, 0, F, 1), 0,
+                         op(w.W_gate, bf, 1, F, static_cast<long long>(de) * F), 0, dxs, de);
+        g.offsets = offsets;
+        RUN(g, GEN_EPI_STORE);
+        g.A = op(du, 0, F, 1);
+        g.B0 = op(w.W_up, bf, 1, F, static_cast<long long>(de) * F);
+        RUN(g, GEN_EPI_ACCUM);
+    }
+    // expert weight gradients, reduced over each expert's rows
+    if (gr.dW_down) {
+        GenGemm g = gemm(GEN_KSEG, F, de, TK, E, op(hw, 0, 1, F), 1,
+                         op(gy, 0, ld_gy, 1, 0, stok), 1, gr.dW_down, de,
+                         static_cast<long long>(F) * de);
+        g.offsets = offsets;
+        RUN(g, GEN_EPI_STORE);
+    }
+    if (gr.dW_gate || gr.dW_up) {
+        GenGemm g = gemm(GEN_KSEG, de, F, TK, E, op(zsrc, z_bf, 1, ld_z, 0, nullptr, stok), 1,
+                         op(da, 0, F, 1), 1, gr.dW_gate, F, static_cast<long long>(de) * F);
+        g.offsets = offsets;
+        if (gr.dW_gate) RUN(g, GEN_EPI_STORE);
+        g.B0 = op(du, 0, F, 1);
+        g.C = gr.dW_up;
+        if (gr.dW_up) RUN(g, GEN_EPI_STORE);
+    }
+
+    // dx from the routed experts (latent: through dz and W_down_latent)
+    if (!lat) {
+        if ((e = launch_gather_sum(dxs, inv, T, K, d, nullptr, gr.dx, 0, s)) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    } else {
+        float* dz = BP(BL.dz);
+        if ((e = launch_gather_sum(dxs, inv, T, K, lat, nullptr, dz, 0, s)) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (gr.dW_down_latent)
+            RUN(gemm(GEN_DENSE, d, lat, T, 1, op(x, bf, 1, d), 1, op(dz, 0, lat, 1), 1,
+                     gr.dW_down_latent, lat),
+                GEN_EPI_STORE);
+        RUN(gemm(GEN_DENSE, T, d, lat, 1, op(dz, 0, lat, 1), 0, op(w.W_down_latent, bf, 1, lat), 0,
+                 gr.dx, d),
+            GEN_EPI_STORE);
+    }
+
+    // shared experts (g = 1 on every token)
+    if (S) {
+        float *dhs = BP(BL.dhs), *das = BP(BL.das), *dus = BP(BL.dus), *hs = BP(BL.hs);
+        RUN(gemm(GEN_DENSE, T, Fs, d, S, op(dout, 0, d, 1), 0,
+                 op(w.Ws_down, bf, 1, d, static_cast<long long>(Fs) * d), 0, dhs, SF, Fs),
+            GEN_EPI_STORE);
+        {
+            GenGemm g = gemm(GEN_DENSE, T, Fs, d, S, op(x, bf, d, 1), 0,
+                             op(w.Ws_gate, bf, Fs, 1, static_cast<long long>(d) * Fs), 1, nullptr,
+                             SF, Fs);
+            g.B1 = op(w.Ws_up, bf, Fs, 1, static_cast<long long>(d) * Fs);
+            g.dh = dhs;
+            g.da = das;
+            g.du = dus;
+            g.hw = hs;
+            RUN(g, GEN_EPI_SWIGLU_BWD);
+        }
+        for (int z = 0; z < S; ++z) {
+            const long long wz = static_cast<long long>(z) * d * Fs;
+            RUN(gemm(GEN_DENSE, T, d, Fs, 1, op(das + z * Fs, 0, SF, 1), 0,
+                     op(offset_elems(w.Ws_gate, wz, bf), bf, 1, Fs), 0, gr.dx, d),
+                GEN_EPI_ACCUM);
+            RUN(gemm(GEN_DENSE, T, d, Fs, 1, op(dus + z * Fs, 0, SF, 1), 0,
+                     op(offset_elems(w.Ws_up, wz, bf), bf, 1, Fs), 0, gr.dx, d),
+                GEN_EPI_ACCUM);
+        }
+        if (gr.dWs_down)
+            RUN(gemm(GEN_DENSE, Fs, d, T, S, op(hs, 0, 1, SF, Fs), 1, op(dout, 0, d, 1), 1,
+                     gr.dWs_down, d, static_cast<long long>(Fs) * d),
+                GEN_EPI_STORE);
+        if (gr.dWs_gate)
+            RUN(gemm(GEN_DENSE, d, Fs, T, S, op(x, bf, 1, d), 1, op(das, 0, SF, 1, Fs), 1,
+                     gr.dWs_gate, Fs, static_cast<long long>(d) * Fs),
+                GEN_EPI_STORE);
+        if (gr.dWs_up)
+            RUN(gemm(GEN_DENSE, d, Fs, T, S, op(x, bf, 1, d), 1, op(dus, 0, SF, 1, Fs), 1,
+                     gr.dWs_up, Fs, static_cast<long long>(d) * Fs),
+                GEN_EPI_STORE);
+    }
+
+    // router: dg -> dr -> dW_router and dx
+    if ((e = launch_pdl(router_bwd_kernel, dim3((T * 32 + 255) / 256), dim3(256), 0, s, dwpart, ntf,
+                        inv, tidx, tw, scores, T, K, E, c.gate, c.renormalize, c.routed_scale, dr,
+                        dg)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (gr.dW_router)
+        RUN(gemm(GEN_DENSE, d, E, T, 1, op(x, bf, 1, d), 1, op(dr, 0, E, 1), 1, gr.dW_router, E),
+            GEN_EPI_STORE);
+    RUN(gemm(GEN_DENSE, T, d, E, 1, op(dr, 0, E, 1), 0, op(w.W_router, 0, 1, E), 0, gr.dx, d),
+        GEN_EPI_ACCUM);
+#undef RUN
+    return MOE_OK;
+}
+
+}  // namespace moe

@@ -236,4 +236,45 @@ cudaError_t launch_wait_selftest(int* err, uint64_t timeout_ns, cudaStream_t s);
 bool encode_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
                  const uint64_t* strides_bytes, const uint32_t* box);
 
+
+// ---------------------------------------------------------------------------
+// Backward pass (gemm_gen.cu, backward.cu)
+// ---------------------------------------------------------------------------
+// One operand of gen_gemm: element (i, j) at p + zoff + I(i) s0 + J(j) s1,
+// I / J the optional index lists idx0 / idx1; dimension 0 is m for A and k
+// for B. zs advances the base per problem (GEN_DENSE; B of GEN_MSEG).
+struct GenOp {
+    const void* p;
+    int bf16;
+    long long s0, s1, zs;
+    const int32_t* idx0;
+    const int32_t* idx1;
+};
+enum { GEN_DENSE = 0, GEN_MSEG = 1, GEN_KSEG = 2 };
+enum { GEN_EPI_STORE = 0, GEN_EPI_ACCUM = 1, GEN_EPI_SWIGLU_BWD = 2 };
+constexpr int MAXSEG = 256;
+struct GenGemm {
+    int mode, M, N, K, Z;
+    const int32_t* offsets;  // [Z+1] device: GEN_MSEG rows / GEN_KSEG reduction ranges
+    GenOp A, B0, B1;         // B1: the up operand of the SwiGLU backward
+    float* C;                // output (store / accumulate), element (m, n) at C + z c_zs + m ldc + n
+    long long ldc, c_zs;
+    int a_m_contig, b_n_contig;  // which index of A / B is the contiguous one
+    const float* rowscale;   // optional per-row factor (gate weight)
+    const float* dh;         // SwiGLU backward: upstream gradient of h, same layout as C
+    float *da, *du, *hw;     // SwiGLU backward outputs, same layout as C
+    float* dwpart;           // optional [rows, column tiles] partials of sum dh h
+};
+cudaError_t launch_gen_gemm(const GenGemm& p, int epi, cudaStream_t s);
+int gen_gemm_ntiles(int N);  // column tiles of a gen_gemm output of width N
+
+// Backward scratch (FP32 arrays, byte offsets into the backward workspace).
+struct BwdLayout {
+    size_t dhp, da, du, hw, dwpart, dxs, dhs, das, dus, hs, dr, dg, glat, routed, dz, total;
+};
+BwdLayout plan_backward(const moe_config& c);
+// Enqueue the backward on s; ws holds the forward's routing and dispatch.
+moe_status backward_impl(const moe_config& c, const void* x, const moe_weights& w, const float* dout,
+                         const moe_grads& g, uint8_t* ws, uint8_t* bws, cudaStream_t s);
+
 }  // namespace moe

@@ -527,7 +527,18 @@ def gate_logit_grad(r, bias, gate, idx, dw, renormalize=False, routed_scale=1.0)
     return dr
 
 
-def moe_backward(x, params, dout, gate, K, renormalize=False, routed_scale=1.0, routing=None):
+def round_bf16(a):
+    """Rounds to FP32 (nearest-even), then to BF16 (nearest-even on the FP32
+    bits: add 0x7FFF plus the kept lsb, drop the low 16 bits), returned as
+    float64. Finite inputs."""
+    f = np.asarray(a, dtype=np.float64).astype(np.float32)
+    bits = f.view(np.uint32).astype(np.uint64)
+    bits = (bits + 0x7FFF + ((bits >> 16) & 1)) & 0xFFFF0000
+    return bits.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def moe_backward(x, params, dout, gate, K, renormalize=False, routed_scale=1.0, routing=None,
+                 latent_rows_bf16=False):
     """Gradients of L = sum(dout * out) for the layer of moe_forward, the
     routing (selection) held fixed. Per token and per selected expert, the
     chain rule of
@@ -545,7 +556,11 @@ def moe_backward(x, params, dout, gate, K, renormalize=False, routed_scale=1.0, 
     their entries of dW_gate / dW_up / dW_down are zero and ``active`` [E] is
     False for them. Returns a dict of float64 arrays: dx, dW_router, dW_gate,
     dW_up, dW_down, dWs_gate, dWs_up, dWs_down (or None), dW_down_latent,
-    dW_up_latent (or None), active, dw [T, K] (dL/dg)."""
+    dW_up_latent (or None), active, dw [T, K] (dL/dg).
+
+    latent_rows_bf16: the latent rows z are rounded to BF16 (round_bf16)
+    before the experts use them, as a BF16 layer stores its activations; the
+    derivative of that rounding is taken as 1."""
     xn = f64(_to_np(x))
     g_out = f64(_to_np(dout))
     T, d = xn.shape
@@ -593,6 +608,8 @@ def moe_backward(x, params, dout, gate, K, renormalize=False, routed_scale=1.0, 
     for t in range(T):
         xt = xn[t]
         zt = xt @ Wdl if latent else xt
+        if latent and latent_rows_bf16:
+            zt = round_bf16(zt)
         w_t = gates_for(r[t], bias, gate, idx[t], renormalize, routed_scale)
         gt = g_out[t]
         g_lat = gt @ Wul.T if latent else gt

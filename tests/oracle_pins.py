@@ -459,9 +459,21 @@ def pin_backward_finite_differences(o):
                 check(name, key, g[name], picks(p[key].shape, 8))
 
 
+def pin_round_bf16(o):
+    """round_bf16 equals PyTorch's FP32 -> BF16 conversion (nearest-even) on
+    random values and on exact ties."""
+    import torch
+    rng = np.random.default_rng(12)
+    v = np.concatenate([rng.normal(size=2000) * 10.0 ** rng.integers(-6, 6, size=2000),
+                        [1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8), 0.0]])
+    ref = torch.tensor(v.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(o.round_bf16(v), ref)
+    assert o.round_bf16(1.0 + 2.0 ** -8) == 1.0 and o.round_bf16(1.0 + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6
+
+
 ALL_PINS = [pin_silu_table, pin_swiglu_example, pin_ffn_down_projection, pin_router_example,
             pin_tie_break, pin_gate_formulas, pin_sigmoid_example, pin_stable_dispatch_example,
             pin_dispatch_vs_library, pin_counts_sum, pin_output_composition,
             pin_sorted_equals_naive, pin_shared_concat_identity, pin_latent_reduces_to_plain,
             pin_quantile, pin_sign_bias_example, pin_routing_stats,
-            pin_backward_finite_differences]
+            pin_backward_finite_differences, pin_round_bf16]

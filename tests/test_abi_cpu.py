@@ -114,6 +114,29 @@ def test_host_side_rejections_do_not_touch_the_gpu(api):
     assert L.moe_routing_stats(ctypes.byref(bad), fake, fake, None, fake, fake, 1 << 30, None) == \
         api.MOE_ERR_INVALID_ARG
     assert L.moe_timing_end(None, 0, None, None) == api.MOE_ERR_INVALID_ARG
+    # backward: dout and dx required, gradients only for parts the layer has,
+    # both workspaces checked
+    g = api.Grads()
+    g.dx = 1 << 20
+    big = 1 << 40
+    assert L.moe_backward(ctypes.byref(cfg), fake, ctypes.byref(w), None, ctypes.byref(g), fake,
+                          big, fake, big, None) == api.MOE_ERR_INVALID_ARG
+    g0 = api.Grads()
+    assert L.moe_backward(ctypes.byref(cfg), fake, ctypes.byref(w), fake, ctypes.byref(g0), fake,
+                          big, fake, big, None) == api.MOE_ERR_INVALID_ARG
+    gl = api.Grads()
+    gl.dx = gl.dW_up_latent = 1 << 20
+    assert L.moe_backward(ctypes.byref(cfg), fake, ctypes.byref(w), fake, ctypes.byref(gl), fake,
+                          big, fake, big, None) == api.MOE_ERR_INVALID_ARG
+    assert L.moe_backward(ctypes.byref(cfg), fake, ctypes.byref(w), fake, ctypes.byref(g), fake,
+                          big, fake, 16, None) == api.MOE_ERR_WORKSPACE
+    assert L.moe_backward(ctypes.byref(cfg), fake, ctypes.byref(w), ctypes.c_void_p((1 << 20) + 4),
+                          ctypes.byref(g), fake, big, fake, big, None) == api.MOE_ERR_INVALID_ARG
+    assert L.moe_backward(ctypes.byref(bad), fake, ctypes.byref(w), fake, ctypes.byref(g), fake,
+                          big, fake, big, None) == api.MOE_ERR_INVALID_ARG
+    n = ctypes.c_size_t(0)
+    assert L.moe_backward_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == api.MOE_OK
+    assert n.value > 0
     assert api.launch_count() == 0
 
 

@@ -1,0 +1,111 @@
+"""Backward pass on the GPU (moe_backward through the C ABI) against the
+oracle's float64 backward, on the GPU forward's own expert selection (the
+selection carries no gradient, so both sides differentiate the same
+piecewise-smooth function).
+
+Tolerances: the backward computes in FP32 from the exact inputs, so its
+gradients of non-latent layers stay within 1e-4 x RMS of the oracle's (FP32
+sums of at most a few hundred terms of unit scale: ~1e-6 relative). The latent
+variant's experts act on the forward's latent rows z, which a BF16 layer
+stores in BF16; the oracle rounds its z the same way (latent_rows_bf16; with
+exact z the rounding alone moves expert weight gradients by up to ~4% of
+their RMS on this layer), and the remaining differences - an FP32 sum that
+rounds to the other BF16 neighbour, and the forward's BF16 hidden rows inside
+the routed sum dW_up_latent reads - stay within the forward's 2e-2 x RMS.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_ffn_fp32_gb300 import api as A
+from mixture_experts_ffn_fp32_gb300 import workloads as W
+from oracle import moe_oracle as O
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+LAYERS = {
+    "f32_softmax_all": W.Workload("g_f1", T=60, d=64, d_ff=96, E=8, K=2, n_shared=1,
+                                  shared_d_ff=64, dtype="f32", gate="softmax_all_renorm",
+                                  has_bias=False),
+    "bf16_topk_shared2": W.Workload("g_b1", T=70, d=128, d_ff=96, E=12, K=3, n_shared=2,
+                                    shared_d_ff=64, dtype="bf16", gate="softmax_topk",
+                                    bias_std=0.01, skew=1.2),
+    "bf16_sigmoid_renorm": W.Workload("g_b2", T=50, d=96, d_ff=64, E=16, K=3, n_shared=1,
+                                      shared_d_ff=32, dtype="bf16", gate="sigmoid",
+                                      renormalize=True, routed_scale=2.5),
+    "bf16_sparse_experts": W.Workload("g_b3", T=30, d=64, d_ff=48, E=40, K=2, n_shared=0,
+                                      shared_d_ff=0, dtype="bf16", gate="softmax_topk",
+                                      bias_std=0.01, skew=1.2),
+    "bf16_latent_sigmoid": W.Workload("g_b4", T=40, d=128, d_ff=64, E=10, K=2, n_shared=1,
+                                      shared_d_ff=64, dtype="bf16", gate="sigmoid",
+                                      latent_dim=64),
+}
+
+
+def _dout(w, seed=7):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(w.T, w.d, generator=g, dtype=torch.float32).cuda()
+
+
+def run(w):
+    spec = A.LayerSpec.of(w)
+    inp = W.make_inputs(w, device="cuda")
+    ws = A.alloc_workspace(spec)
+    A.forward(spec, inp["x"], inp, ws=ws)
+    views = A.workspace_views(spec, ws)
+    gidx = P.npi(views["idx"])
+    counts = P.npi(views["counts"])
+    dout = _dout(w)
+    # expert gradients pre-filled with NaN: slices of experts without rows must stay NaN
+    shapes = A.grad_shapes(spec)
+    grads = {n: torch.full(shapes[n], float("nan"), device="cuda")
+             for n in ("dW_gate", "dW_up", "dW_down")}
+    g = A.backward(spec, inp["x"], inp, dout, ws, grads=grads)
+    torch.cuda.synchronize()
+    assert A.workspace_status(ws) == A.MOE_OK
+    return spec, inp, ws, gidx, counts, dout, g
+
+
+@pytest.mark.parametrize("name", list(LAYERS))
+def test_backward_matches_oracle(name):
+    w = LAYERS[name]
+    spec, inp, ws, gidx, counts, dout, g = run(w)
+    ref = O.moe_backward(inp["x"], inp, dout, w.gate, w.K, w.renormalize, w.routed_scale,
+                         routing=gidx, latent_rows_bf16=bool(w.latent_dim))
+    assert np.array_equal(ref["active"], counts > 0)
+    rel = 2e-2 if w.latent_dim else 1e-4
+    for n, gt in g.items():
+        r = ref[n]
+        got = gt.detach().cpu().numpy().astype(np.float64)
+        if n in ("dW_gate", "dW_up", "dW_down"):
+            act = ref["active"]
+            assert np.isnan(got[~act]).all(), f"{n}: an expert without rows got a gradient"
+            got, r = got[act], r[act]
+        assert np.isfinite(got).all(), n
+        rms = float(np.sqrt(np.mean(r ** 2))) or 1.0
+        err = float(np.abs(got - r).max())
+        assert err <= rel * rms, f"{name} {n}: max-abs error {err:.3e} > {rel} x RMS {rms:.3e}"
+
+
+def test_backward_sparse_case_has_empty_experts():
+    counts = run(LAYERS["bf16_sparse_experts"])[4]
+    assert (counts == 0).any() and (counts > 0).any()
+
+
+def test_backward_reproducible_and_optional_outputs():
+    w = LAYERS["bf16_topk_shared2"]
+    spec, inp, ws, gidx, counts, dout, g1 = run(w)
+    g2 = A.backward(spec, inp["x"], inp, dout, ws,
+                    grads={n: torch.full(A.grad_shapes(spec)[n], float("nan"), device="cuda")
+                           for n in ("dW_gate", "dW_up", "dW_down")})
+    for n in g1:
+        assert torch.equal(torch.nan_to_num(g1[n], nan=7.0).view(torch.int32),
+                           torch.nan_to_num(g2[n], nan=7.0).view(torch.int32)), n
+    # only dx requested: the same dx
+    g3 = A.backward(spec, inp["x"], inp, dout, ws,
+                    grads={n: None for n in A.GRAD_NAMES if n != "dx"})
+    assert set(g3) == {"dx"}
+    assert torch.equal(g3["dx"].view(torch.int32), g1["dx"].view(torch.int32))
