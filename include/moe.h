@@ -295,8 +295,13 @@ moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes);
  * dW_up and dW_down are NOT written (kimi_k3 StableLatentMoE, "Grouped
  * expert execution and sparse gradients"); the workspace's counts tell which.
  * Every other requested gradient is overwritten. Sums run in a fixed order:
- * bit-reproducible. Arithmetic: FP32 (BF16 inputs converted exactly).
- *   x [T, d] (dtype), dout [T, d] FP32 device, 16-byte aligned.
+ * bit-reproducible.
+ *   x [T, d] (dtype), dout [T, d] FP32 device; x, dout and every gradient
+ *   16-byte aligned.
+ * BF16 layers whose d, d_ff, latent_dim and shared_d_ff are multiples of 64
+ * run the expert contractions on the tensor cores with BF16 operands (the
+ * upstream and activation gradients rounded to BF16, FP32 sums); the others
+ * on the CUDA cores in FP32.
  *   ws: the forward's workspace (moe_workspace_size bytes, 256-byte aligned).
  *   bws: moe_backward_workspace_size bytes, 256-byte aligned. */
 moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights* w,

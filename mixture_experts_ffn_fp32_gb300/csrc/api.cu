@@ -614,7 +614,7 @@ MOE_API moe_status moe_backward(const moe_config* cfg, const void* x, const moe_
                            grads->dW_down, grads->dWs_gate, grads->dWs_up, grads->dWs_down,
                            grads->dW_down_latent, grads->dW_up_latent};
     for (const float* p : outs)
-        if (p && (reinterpret_cast<uintptr_t>(p) & 3u)) return MOE_ERR_INVALID_ARG;
+        if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
     if ((grads->dWs_gate || grads->dWs_up || grads->dWs_down) && cfg->n_shared == 0)
         return MOE_ERR_INVALID_ARG;
     if ((grads->dW_down_latent || grads->dW_up_latent) && cfg->latent_dim == 0)

@@ -127,43 +127,89 @@ const void* offset_elems(const void* p, long long n, int bf16) {
 
 }  // namespace
 
+bool bwd_on_tensor_cores(const moe_config& c) {
+    const int de = c.latent_dim ? c.latent_dim : c.d;
+    return c.dtype == MOE_BF16 && c.d % 64 == 0 && c.d_ff % 64 == 0 && de % 64 == 0 &&
+           (c.n_shared == 0 || c.shared_d_ff % 64 == 0);
+}
+
 BwdLayout plan_backward(const moe_config& c) {
     BwdLayout B;
     memset(&B, 0, sizeof(B));
-    const size_t T = c.T, TK = T * c.K, F = c.d_ff;
+    const size_t T = c.T, TK = T * c.K, F = c.d_ff, E = c.E;
     const size_t de = c.latent_dim ? c.latent_dim : c.d;
     const size_t SF = static_cast<size_t>(c.n_shared) * (c.n_shared ? c.shared_d_ff : 0);
     const size_t L = c.latent_dim;
     const size_t ntf = gen_gemm_ntiles(c.d_ff);
+    B.tc = bwd_on_tensor_cores(c) ? 1 : 0;
     size_t o = 0;
-    auto take = [&](size_t floats) {
+    auto take = [&](size_t bytes) {
         const size_t at = o;
-        o = (o + floats * 4 + 255) & ~static_cast<size_t>(255);
+        o = (o + bytes + 255) & ~static_cast<size_t>(255);
         return at;
     };
-    B.dhp = take(TK * F);
-    B.da = take(TK * F);
-    B.du = take(TK * F);
-    B.hw = take(TK * F);
-    B.dwpart = take(TK * ntf);
-    B.dxs = take(TK * de);
-    B.dhs = SF ? take(T * SF) : 0;
-    B.das = SF ? take(T * SF) : 0;
-    B.dus = SF ? take(T * SF) : 0;
-    B.hs = SF ? take(T * SF) : 0;
-    B.dr = take(T * c.E);
-    B.dg = take(TK);
-    B.glat = L ? take(T * L) : 0;
-    B.routed = L ? take(T * L) : 0;
-    B.dz = L ? take(T * L) : 0;
+    B.dxs = take(TK * de * 4);
+    B.dr = take(T * E * 4);
+    B.dg = take(TK * 4);
+    B.glat = L ? take(T * L * 4) : 0;
+    B.routed = L ? take(T * L * 4) : 0;
+    B.dz = L ? take(T * L * 4) : 0;
+    if (!B.tc) {
+        B.dhp = take(TK * F * 4);
+        B.da = take(TK * F * 4);
+        B.du = take(TK * F * 4);
+        B.hw = take(TK * F * 4);
+        B.dwpart = take(TK * ntf * 4);
+        B.dhs = SF ? take(T * SF * 4) : 0;
+        B.das = SF ? take(T * SF * 4) : 0;
+        B.dus = SF ? take(T * SF * 4) : 0;
+        B.hs = SF ? take(T * SF * 4) : 0;
+    } else {
+        B.tkpad = static_cast<long long>((TK + 63) / 64 * 64 + 64 * E);  // >= padded total
+        B.tpad = static_cast<long long>((T + 63) / 64 * 64);
+        const size_t kp = static_cast<size_t>(B.tkpad), tp = static_cast<size_t>(B.tpad);
+        B.poff = take((E + 1) * 4);
+        B.gys = take(TK * de * 2);
+        B.gysT = take(de * kp * 2);
+        B.zsT = take(de * kp * 2);
+        B.a = take(TK * F * 4);
+        B.u = take(TK * F * 4);
+        B.dhp = take(TK * F * 4);
+        B.dab = take(TK * F * 2);
+        B.dub = take(TK * F * 2);
+        B.hwb = take(TK * F * 2);
+        B.daT = take(F * kp * 2);
+        B.duT = take(F * kp * 2);
+        B.hwT = take(F * kp * 2);
+        B.dwrow = take(TK * 4);
+        if (SF) {
+            B.doutb = take(T * c.d * 2);
+            B.doutT = take(c.d * tp * 2);
+            B.xT = take(c.d * tp * 2);
+            B.as = take(T * SF * 4);
+            B.us = take(T * SF * 4);
+            B.dhs = take(T * SF * 4);
+            B.dasb = take(T * SF * 2);
+            B.dusb = take(T * SF * 2);
+            B.hsb = take(T * SF * 2);
+            B.dasT = take(SF * tp * 2);
+            B.dusT = take(SF * tp * 2);
+            B.hsT = take(SF * tp * 2);
+        }
+    }
     B.total = o;
     return B;
 }
+
+static moe_status backward_tc(const moe_config& c, const void* x, const moe_weights& w,
+                              const float* dout, const moe_grads& gr, uint8_t* ws, uint8_t* bws,
+                              cudaStream_t s);
 
 moe_status backward_impl(const moe_config& c, const void* x, const moe_weights& w, const float* dout,
                          const moe_grads& gr, uint8_t* ws, uint8_t* bws, cudaStream_t s) {
     const WsLayout L = plan_workspace(c);
     const BwdLayout BL = plan_backward(c);
+    if (BL.tc) return backward_tc(c, x, w, dout, gr, ws, bws, s);
     const int bf = c.dtype == MOE_BF16 ? 1 : 0;
     const int T = c.T, K = c.K, E = c.E, TK = T * K, F = c.d_ff, d = c.d;
     const int lat = c.latent_dim, de = lat ? lat : d;
@@ -330,6 +376,250 @@ moe_status backward_impl(const moe_config& c, const void* x, const moe_weights& 
     RUN(gemm(GEN_DENSE, T, d, E, 1, op(dr, 0, E, 1), 0, op(w.W_router, 0, 1, E), 0, gr.dx, d),
         GEN_EPI_ACCUM);
 #undef RUN
+    return MOE_OK;
+}
+
+// The tensor-core form (BF16 layers, widths multiples of 64): the gate and up
+// products recomputed by the forward's grouped GEMM (plain epilogue, FP32
+// out), every other expert contraction by the NT kernel on BF16 operands
+// laid out for it; the SwiGLU backward per row in between. Upstream
+// gradients and activation gradients enter the tensor cores rounded to BF16;
+// every sum is FP32.
+static moe_status backward_tc(const moe_config& c, const void* x, const moe_weights& w,
+                              const float* dout, const moe_grads& gr, uint8_t* ws, uint8_t* bws,
+                              cudaStream_t s) {
+    const WsLayout L = plan_workspace(c);
+    const BwdLayout BL = plan_backward(c);
+    const int T = c.T, K = c.K, E = c.E, TK = T * K, F = c.d_ff, d = c.d;
+    const int lat = c.latent_dim, de = lat ? lat : d;
+    const int S = c.n_shared, Fs = S ? c.shared_d_ff : 0, SF = S * Fs;
+    const long long kp = BL.tkpad, tp = BL.tpad;
+    int* err = reinterpret_cast<int*>(ws + L.err);
+    auto WP = [&](size_t off) { return static_cast<void*>(ws + off); };
+    auto BF = [&](size_t off) { return reinterpret_cast<float*>(bws + off); };
+    auto BH = [&](size_t off) { return reinterpret_cast<__nv_bfloat16*>(bws + off); };
+    const int32_t* stok = static_cast<const int32_t*>(WP(L.sorted_token));
+    const float* sw = static_cast<const float*>(WP(L.sorted_w));
+    const int32_t* inv = static_cast<const int32_t*>(WP(L.inv));
+    const int32_t* offsets = static_cast<const int32_t*>(WP(L.offsets));
+    const int32_t* tidx = static_cast<const int32_t*>(WP(L.topk_idx));
+    const float* tw = static_cast<const float*>(WP(L.topk_w));
+    const float* scores = L.scores ? static_cast<const float*>(WP(L.scores)) : nullptr;
+    int32_t* poff = reinterpret_cast<int32_t*>(bws + BL.poff);
+    float *dxs = BF(BL.dxs), *dr = BF(BL.dr), *dg = BF(BL.dg);
+    cudaError_t e;
+#define CK(call)                                     \
+    do {                                             \
+        if ((e = (call)) != cudaSuccess) return MOE_ERR_CUDA; \
+    } while (0)
+    auto nt_op = [](const void* p, long long rows, long long K_, long long ld, long long Z = 1,
+                    long long zstride = 0) {
+        NtOperand o;
+        o.p = p;
+        o.rows = rows;
+        o.K = K_;
+        o.ld = ld;
+        o.Z = Z;
+        o.zstride = zstride;
+        return o;
+    };
+    auto nt = [&](int mode, int M, int N, int K_, int Z, NtOperand A, NtOperand B, float* C,
+                  long long ldc, long long c_zs = 0, const int32_t* offs = nullptr) {
+        NtGemm g;
+        memset(&g, 0, sizeof(g));
+        g.mode = mode;
+        g.M = M;
+        g.N = N;
+        g.K = K_;
+        g.Z = Z;
+        g.nph = 1;
+        g.A[0] = A;
+        g.B[0] = B;
+        g.offsets = offs;
+        g.C = C;
+        g.ldc = ldc;
+        g.c_zs = c_zs;
+        g.err = err;
+        return g;
+    };
+
+    // upstream gradient of the routed sum (FP32) and the rows the experts act on
+    const float* gy = dout;
+    long long ld_gy = d;
+    const void* zsrc = x;
+    long long ld_z = d;
+    if (lat) {
+        float* glat = BF(BL.glat);
+        CK(launch_gen_gemm(gemm(GEN_DENSE, T, lat, d, 1, op(dout, 0, d, 1), 0,
+                                op(w.W_up_latent, 1, 1, d), 0, glat, lat),
+                           GEN_EPI_STORE, s));
+        if (gr.dW_up_latent) {
+            float* routed = BF(BL.routed);
+            CK(launch_gather_sum(static_cast<const float*>(WP(L.ys)), inv, T, K, lat, nullptr,
+                                 routed, 0, s));
+            CK(launch_gen_gemm(gemm(GEN_DENSE, lat, d, T, 1, op(routed, 0, 1, lat), 1,
+                                    op(dout, 0, d, 1), 1, gr.dW_up_latent, d),
+                               GEN_EPI_STORE, s));
+        }
+        gy = glat;
+        ld_gy = lat;
+        zsrc = WP(L.z);
+        ld_z = lat;
+    }
+
+    // ---- operand copies: expert-padded columns, gathered rows ----
+    CK(launch_pad_offsets(offsets, E, poff, s));
+    __nv_bfloat16 *gys = BH(BL.gys), *gysT = BH(BL.gysT), *zsT = BH(BL.zsT);
+    CK(launch_gather_bf16(gy, 0, ld_gy, stok, TK, de, gys, s));
+    CK(launch_transpose_pad(gy, 0, ld_gy, stok, TK, de, poff, offsets, E, static_cast<int>(kp), gysT, s));
+    CK(launch_transpose_pad(zsrc, 1, ld_z, stok, TK, de, poff, offsets, E, static_cast<int>(kp), zsT, s));
+
+    // ---- recomputed gate and up products (the forward's GEMM, FP32 out) ----
+    float *a = BF(BL.a), *u = BF(BL.u);
+    float *as = S ? BF(BL.as) : nullptr, *us = S ? BF(BL.us) : nullptr;
+    for (int which = 0; which < 2; ++which) {
+        TcGemmArgs g{};
+        g.g[0] = TcGroup{1, de, WP(L.xs), de, TK, which ? w.W_up : w.W_gate, nullptr, E, F,
+                         which ? u : a, F, 1};
+        if (S)
+            g.g[1] = TcGroup{1, d, x, d, T, which ? w.Ws_up : w.Ws_gate, nullptr, S, Fs,
+                             which ? us : as, SF, 1};
+        g.E = E;
+        g.offsets = offsets;
+        g.mt_prefix = static_cast<const int32_t*>(WP(L.mt_prefix));
+        g.swiglu = 0;
+        g.err = err;
+        CK(launch_tc_gemm(g, s));
+    }
+
+    // ---- G1: dh' = gy W_down^T (routed, per expert), dout Ws_down^T (shared) ----
+    float* dhp = BF(BL.dhp);
+    CK(launch_nt_gemm(nt(NT_MSEG, TK, F, de, E, nt_op(gys, TK, de, de),
+                         nt_op(w.W_down, F, de, de, E, static_cast<long long>(F) * de), dhp, F, 0,
+                         offsets),
+                      s));
+    __nv_bfloat16 *doutb = nullptr, *doutT = nullptr, *xT = nullptr;
+    float* dhs = nullptr;
+    if (S) {
+        doutb = BH(BL.doutb);
+        doutT = BH(BL.doutT);
+        xT = BH(BL.xT);
+        dhs = BF(BL.dhs);
+        CK(launch_gather_bf16(dout, 0, d, nullptr, T, d, doutb, s));
+        CK(launch_transpose_pad(dout, 0, d, nullptr, T, d, nullptr, nullptr, 0, static_cast<int>(tp), doutT, s));
+        CK(launch_transpose_pad(x, 1, d, nullptr, T, d, nullptr, nullptr, 0, static_cast<int>(tp), xT, s));
+        NtGemm g = nt(NT_DENSE, T, Fs, d, S, nt_op(doutb, T, d, d),
+                      nt_op(w.Ws_down, Fs, d, d, S, static_cast<long long>(Fs) * d), dhs, SF, Fs);
+        g.b_z3 = 1;
+        CK(launch_nt_gemm(g, s));
+    }
+
+    // ---- SwiGLU backward per row; transposed, padded copies ----
+    __nv_bfloat16 *dab = BH(BL.dab), *dub = BH(BL.dub), *hwb = BH(BL.hwb);
+    __nv_bfloat16 *daT = BH(BL.daT), *duT = BH(BL.duT), *hwT = BH(BL.hwT);
+    float* dwrow = BF(BL.dwrow);
+    CK(launch_swiglu_bwd(a, u, dhp, F, TK, F, sw, dab, dub, hwb, dwrow, s));
+    CK(launch_transpose_pad(dab, 1, F, nullptr, TK, F, poff, offsets, E, static_cast<int>(kp), daT, s));
+    CK(launch_transpose_pad(dub, 1, F, nullptr, TK, F, poff, offsets, E, static_cast<int>(kp), duT, s));
+    CK(launch_transpose_pad(hwb, 1, F, nullptr, TK, F, poff, offsets, E, static_cast<int>(kp), hwT, s));
+    __nv_bfloat16 *dasb = nullptr, *dusb = nullptr, *hsb = nullptr;
+    __nv_bfloat16 *dasT = nullptr, *dusT = nullptr, *hsT = nullptr;
+    if (S) {
+        dasb = BH(BL.dasb);
+        dusb = BH(BL.dusb);
+        hsb = BH(BL.hsb);
+        dasT = BH(BL.dasT);
+        dusT = BH(BL.dusT);
+        hsT = BH(BL.hsT);
+        CK(launch_swiglu_bwd(as, us, dhs, SF, T, SF, nullptr, dasb, dusb, hsb, nullptr, s));
+        CK(launch_transpose_pad(dasb, 1, SF, nullptr, T, SF, nullptr, nullptr, 0, static_cast<int>(tp), dasT, s));
+        CK(launch_transpose_pad(dusb, 1, SF, nullptr, T, SF, nullptr, nullptr, 0, static_cast<int>(tp), dusT, s));
+        CK(launch_transpose_pad(hsb, 1, SF, nullptr, T, SF, nullptr, nullptr, 0, static_cast<int>(tp), hsT, s));
+    }
+
+    // ---- G3: dz rows = da W_gate^T + du W_up^T (two phases) ----
+    {
+        NtGemm g = nt(NT_MSEG, TK, de, F, E, nt_op(dab, TK, F, F),
+                      nt_op(w.W_gate, de, F, F, E, static_cast<long long>(de) * F), dxs, de, 0,
+                      offsets);
+        g.nph = 2;
+        g.A[1] = nt_op(dub, TK, F, F);
+        g.B[1] = nt_op(w.W_up, de, F, F, E, static_cast<long long>(de) * F);
+        CK(launch_nt_gemm(g, s));
+    }
+    // ---- expert weight gradients over each expert's padded columns ----
+    if (gr.dW_down)
+        CK(launch_nt_gemm(nt(NT_KSEG, F, de, static_cast<int>(kp), E, nt_op(hwT, F, kp, kp),
+                             nt_op(gysT, de, kp, kp), gr.dW_down, de, static_cast<long long>(F) * de,
+                             poff),
+                          s));
+    if (gr.dW_gate)
+        CK(launch_nt_gemm(nt(NT_KSEG, de, F, static_cast<int>(kp), E, nt_op(zsT, de, kp, kp),
+                             nt_op(daT, F, kp, kp), gr.dW_gate, F, static_cast<long long>(de) * F,
+                             poff),
+                          s));
+    if (gr.dW_up)
+        CK(launch_nt_gemm(nt(NT_KSEG, de, F, static_cast<int>(kp), E, nt_op(zsT, de, kp, kp),
+                             nt_op(duT, F, kp, kp), gr.dW_up, F, static_cast<long long>(de) * F,
+                             poff),
+                          s));
+
+    // ---- dx from the routed experts (latent: through dz and W_down_latent) ----
+    if (!lat) {
+        CK(launch_gather_sum(dxs, inv, T, K, d, nullptr, gr.dx, 0, s));
+    } else {
+        float* dz = BF(BL.dz);
+        CK(launch_gather_sum(dxs, inv, T, K, lat, nullptr, dz, 0, s));
+        if (gr.dW_down_latent)
+            CK(launch_gen_gemm(gemm(GEN_DENSE, d, lat, T, 1, op(x, 1, 1, d), 1, op(dz, 0, lat, 1), 1,
+                                    gr.dW_down_latent, lat),
+                               GEN_EPI_STORE, s));
+        CK(launch_gen_gemm(gemm(GEN_DENSE, T, d, lat, 1, op(dz, 0, lat, 1), 0,
+                                op(w.W_down_latent, 1, 1, lat), 0, gr.dx, d),
+                           GEN_EPI_STORE, s));
+    }
+
+    // ---- shared experts: dx, weight gradients ----
+    if (S) {
+        for (int z = 0; z < S; ++z) {
+            NtGemm g = nt(NT_DENSE, T, d, Fs, 1, nt_op(dasb, T, SF, SF),
+                          nt_op(w.Ws_gate, d, Fs, Fs, S, static_cast<long long>(d) * Fs), gr.dx, d);
+            g.nph = 2;
+            g.A[1] = nt_op(dusb, T, SF, SF);
+            g.B[1] = nt_op(w.Ws_up, d, Fs, Fs, S, static_cast<long long>(d) * Fs);
+            g.a_kofs[0] = g.a_kofs[1] = z * Fs;
+            g.b_zc[0] = g.b_zc[1] = z;
+            g.accumulate = 1;
+            CK(launch_nt_gemm(g, s));
+        }
+        if (gr.dWs_down) {
+            NtGemm g = nt(NT_DENSE, Fs, d, static_cast<int>(tp), S, nt_op(hsT, SF, tp, tp),
+                          nt_op(doutT, d, tp, tp), gr.dWs_down, d, static_cast<long long>(Fs) * d);
+            g.a_zrow = Fs;
+            CK(launch_nt_gemm(g, s));
+        }
+        for (int which = 0; which < 2; ++which) {
+            float* C = which ? gr.dWs_up : gr.dWs_gate;
+            if (!C) continue;
+            NtGemm g = nt(NT_DENSE, d, Fs, static_cast<int>(tp), S, nt_op(xT, d, tp, tp),
+                          nt_op(which ? dusT : dasT, SF, tp, tp), C, Fs, static_cast<long long>(d) * Fs);
+            g.b_zrow = Fs;
+            CK(launch_nt_gemm(g, s));
+        }
+    }
+
+    // ---- router: dg -> dr -> dW_router and dx ----
+    CK(launch_pdl(router_bwd_kernel, dim3((T * 32 + 255) / 256), dim3(256), 0, s,
+                  static_cast<const float*>(dwrow), 1, inv, tidx, tw, scores, T, K, E, c.gate,
+                  c.renormalize, c.routed_scale, dr, dg));
+    if (gr.dW_router)
+        CK(launch_gen_gemm(gemm(GEN_DENSE, d, E, T, 1, op(x, 1, 1, d), 1, op(dr, 0, E, 1), 1,
+                                gr.dW_router, E),
+                           GEN_EPI_STORE, s));
+    CK(launch_gen_gemm(gemm(GEN_DENSE, T, d, E, 1, op(dr, 0, E, 1), 0, op(w.W_router, 0, 1, E), 0,
+                            gr.dx, d),
+                       GEN_EPI_ACCUM, s));
+#undef CK
     return MOE_OK;
 }
 

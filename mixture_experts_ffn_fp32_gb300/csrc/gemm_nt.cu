@@ -1,0 +1,379 @@
+// Grouped "NT" GEMM on the 5th-generation tensor cores for the backward pass:
+//   C[m, n] (+)= sum_k A[m, k] B[n, k]
+// with BOTH operands K-major BF16 (rows of K contiguous) - the layout every
+// backward contraction has once its operands are laid out for it: the
+// transposed weight products dh = gy W_down^T and dz = da W_gate^T + du W_up^T
+// read the caller's weights as they are ([E, F, d_e] and [E, d_e, F] rows),
+// and the weight gradients read transposed, expert-padded copies of the
+// activations that the backward writes for them. FP32 accumulation in tensor
+// memory, FP32 output (stored or accumulated).
+//
+// Ways to cut the work (the forward's grouping, extended to the reduction):
+//   NT_MSEG  : the rows of segment z are offsets[z] .. offsets[z+1] (routed
+//              rows in expert order); B is the 3-D map's slice z
+//   NT_KSEG  : the reduction of segment z runs over columns koff[z] ..
+//              koff[z+1] (each a multiple of 64: every expert's rows padded
+//              with zero columns); C advanced by z c_zs; an empty segment
+//              writes nothing (no gradient for an expert without rows)
+//   NT_DENSE : Z problems of one shape; A rows, B rows and B's slice advanced
+//              by z a_zrow, z b_zrow, z b_z3; C by z c_zs
+// A unit accumulates one or two phases (e.g. da W_gate^T then du W_up^T),
+// each with its own pair of tensor maps and coordinate offsets.
+//
+// Tile 128 x 128, K step 64 (a 128-byte swizzle row), 6 TMA stages of 32 KB,
+// two 128-column TMEM accumulators. Warp 0 issues TMA, warp 1 the MMAs
+// (tcgen05.mma kind::f16, M = 128, N = 128, both operands K-major), warps
+// 2-5 drain one TMEM lane quarter each and write FP32 rows. Every wait is
+// bounded; on timeout the CTA stops, drains and flags the error word.
+// Shapes: every K, N and row count the maps see is handled by TMA bounds and
+// masks, but each phase's K must be a multiple of 64 (the caller's choice).
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int NBM = 128, NBN = 128, NBK = 64;
+constexpr int NT_STAGES = 6;
+constexpr int NT_TILE_BYTES = NBM * NBK * 2;  // 16 KB, A and B alike
+constexpr int NT_STAGE_BYTES = 2 * NT_TILE_BYTES;
+constexpr int NT_ACC_COLS = 128;
+constexpr int NT_TMEM_COLS = 256;
+constexpr int NT_THREADS = 192;
+constexpr int NT_BAR_OFF = NT_STAGES * NT_STAGE_BYTES;
+constexpr int NT_NBARS = 2 * NT_STAGES + 4 + 1;
+constexpr int NT_MISC_OFF = NT_BAR_OFF + 8 * NT_NBARS;
+constexpr int NT_SCHED_OFF = (NT_MISC_OFF + 16 + 15) / 16 * 16;
+constexpr int NT_SMEM_BYTES = NT_SCHED_OFF + 2 * (MAXSEG + 1) * 4 + 1024;
+
+struct NtParams {
+    CUtensorMap mapA[2];
+    CUtensorMap mapB[2];
+    int nph;
+    int a_kofs[2], b_zc[2];
+    int mode, M, N, Z, kblocks;
+    int a_zrow, b_zrow, b_z3;
+    const int32_t* offsets;
+    float* C;
+    long long ldc, c_zs;
+    int accumulate;
+    uint32_t idesc;
+    int* err;
+    unsigned long long timeout_ns;
+};
+
+struct NtUnit {
+    int z, arow, rows, m0, n0, kb0, nkb;
+    bool skip;
+};
+
+// s_tp: m-tile prefix per segment (NT_MSEG), s_off: offsets (NT_MSEG, NT_KSEG)
+MOE_DEV NtUnit nt_unit(int u, const NtParams& p, int nt, int mt, const int* s_tp, const int* s_off) {
+    NtUnit t;
+    t.skip = false;
+    if (p.mode == NT_MSEG) {
+        const int m = u / nt;
+        t.n0 = (u - m * nt) * NBN;
+        int lo = 0, hi = p.Z;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_tp[mid] <= m)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        t.z = lo;
+        t.arow = s_off[lo] + (m - s_tp[lo]) * NBM;
+        t.rows = min(NBM, s_off[lo + 1] - t.arow);
+        t.m0 = t.arow;
+        t.kb0 = 0;
+        t.nkb = p.kblocks;
+    } else {
+        const int per = mt * nt;
+        t.z = u / per;
+        const int rem = u - t.z * per;
+        const int m = rem / nt;
+        t.m0 = m * NBM;
+        t.n0 = (rem - m * nt) * NBN;
+        t.rows = min(NBM, p.M - t.m0);
+        t.arow = t.m0 + t.z * p.a_zrow;
+        if (p.mode == NT_KSEG) {
+            t.kb0 = s_off[t.z] / NBK;
+            t.nkb = (s_off[t.z + 1] - s_off[t.z]) / NBK;
+            t.skip = t.nkb <= 0;
+        } else {
+            t.kb0 = 0;
+            t.nkb = p.kblocks;
+        }
+    }
+    return t;
+}
+
+__global__ void __launch_bounds__(NT_THREADS, 1) nt_gemm_kernel(const __grid_constant__ NtParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + NT_BAR_OFF;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (NT_STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * NT_STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * NT_STAGES + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * NT_STAGES + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + NT_MISC_OFF);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + NT_MISC_OFF + 4);
+    int* s_tp = reinterpret_cast<int*>(smem + NT_SCHED_OFF);
+    int* s_off = s_tp + (MAXSEG + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NT_STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 4);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0)
+        for (int ph = 0; ph < p.nph; ++ph) {
+            tma_prefetch_map(&p.mapA[ph]);
+            tma_prefetch_map(&p.mapB[ph]);
+        }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), NT_TMEM_COLS);
+        tmem_relinquish();
+    }
+    pdl_wait();
+    pdl_trigger();
+    if (p.mode != NT_DENSE) {
+        for (int i = threadIdx.x; i <= p.Z; i += blockDim.x) s_off[i] = p.offsets[i];
+    }
+    __syncthreads();
+    if (p.mode == NT_MSEG && threadIdx.x == 0) {
+        int acc = 0;
+        for (int z = 0; z < p.Z; ++z) {
+            s_tp[z] = acc;
+            acc += (s_off[z + 1] - s_off[z] + NBM - 1) / NBM;
+        }
+        s_tp[p.Z] = acc;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int nt = (p.N + NBN - 1) / NBN;
+    const int mt = (p.M + NBM - 1) / NBM;
+    const int total = p.mode == NT_MSEG ? s_tp[p.Z] * nt : p.Z * mt * nt;
+    const WaitCtx wc{p.err, abort_flag, p.timeout_ns};
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer ----------------
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, last_par = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+                const NtUnit t = nt_unit(u, p, nt, mt, s_tp, s_off);
+                if (t.skip) continue;
+                const int brow = t.n0 + t.z * p.b_zrow;
+                for (int ph = 0; ph < p.nph && ok; ++ph) {
+                    const int bz = p.b_zc[ph] + (p.mode == NT_MSEG ? t.z : t.z * p.b_z3);
+                    for (int kb = t.kb0; kb < t.kb0 + t.nkb; ++kb) {
+                        if (!bounded_wait(empty_bar(stage), phase ^ 1u, wc)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t sA = sbase + stage * NT_STAGE_BYTES;
+                        mbar_expect_tx(full_bar(stage), NT_STAGE_BYTES);
+                        tma_load_2d(sA, &p.mapA[ph], kb * NBK + p.a_kofs[ph], t.arow, full_bar(stage));
+                        tma_load_3d(sA + NT_TILE_BYTES, &p.mapB[ph], kb * NBK, brow, bz, full_bar(stage));
+                        issued |= 1u << stage;
+                        last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                        if (++stage == NT_STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+            }
+            for (int s = 0; s < NT_STAGES; ++s)
+                if ((issued >> s) & 1u) bounded_drain(full_bar(s), (last_par >> s) & 1u, p.timeout_ns, p.err);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            const uint64_t adesc0 = smem_desc_sw128(sbase, 16, 1024);
+            const uint64_t bdesc0 = smem_desc_sw128(sbase + NT_TILE_BYTES, 16, 1024);
+            for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+                const NtUnit t = nt_unit(u, p, nt, mt, s_tp, s_off);
+                if (t.skip) continue;
+                if (!bounded_wait(tempty_bar(acc), acc_phase ^ 1u, wc)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * NT_ACC_COLS);
+                const int nkb = t.nkb * p.nph;
+                for (int i = 0; i < nkb; ++i) {
+                    if (!bounded_wait(full_bar(stage), phase, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t soff = static_cast<uint64_t>(stage * NT_STAGE_BYTES) >> 4;
+#pragma unroll
+                    for (int ks = 0; ks < NBK / 16; ++ks) {
+                        const uint32_t accum = (i != 0 || ks != 0) ? 1u : 0u;
+                        tc_mma_bf16(d_tmem, adesc0 + soff + ks * 2, bdesc0 + soff + ks * 2, p.idesc, accum);
+                    }
+                    tc_commit(empty_bar(stage));
+                    if (++stage == NT_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(tfull_bar(acc));
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            tc_commit(drain_bar);
+            bounded_drain(drain_bar, 0, p.timeout_ns, p.err);
+        }
+    } else {
+        // ---------------- epilogue warps 2..5 ----------------
+        const int q = warp & 3;  // TMEM lane quarter of this warp
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int u = blockIdx.x; u < total; u += gridDim.x) {
+            const NtUnit t = nt_unit(u, p, nt, mt, s_tp, s_off);
+            if (t.skip) continue;
+            int ok = 1;
+            if (lane == 0) ok = bounded_wait(tfull_bar(acc), acc_phase, wc) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * NT_ACC_COLS) +
+                                (static_cast<uint32_t>(q * 32) << 16);
+            const int r = q * 32 + lane;
+            const bool row_ok = r < t.rows;
+            float* crow = p.C + (p.mode == NT_MSEG ? 0 : t.z * p.c_zs) +
+                          static_cast<long long>(t.m0 + r) * p.ldc + t.n0;
+#pragma unroll 1
+            for (int c = 0; c < NBN; c += 16) {
+                uint32_t v[16];
+                tc_ld_32x32b_x16(tb + c, v);
+                tc_wait_ld();
+                if (row_ok && t.n0 + c < p.N) {
+                    float4* dst = reinterpret_cast<float4*>(crow + c);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        float4 o = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                               __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                        if (p.accumulate) {
+                            const float4 a = dst[j];
+                            o.x += a.x;
+                            o.y += a.y;
+                            o.z += a.z;
+                            o.w += a.w;
+                        }
+                        dst[j] = o;
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, NT_TMEM_COLS);
+    }
+}
+
+// A: rows x K_total, row pitch lda elements (K-major), box 64 x 128
+bool make_nt_A(CUtensorMap* m, const void* A, long long rows, long long K, long long lda) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rows)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(lda) * 2};
+    const uint32_t box[2] = {NBK, NBM};
+    return encode_tmap(m, A, 2, dims, strides, box);
+}
+
+// B: Z slices of rows x K (K-major), row pitch ldb, slice pitch zstride elements
+bool make_nt_B(CUtensorMap* m, const void* B, long long Z, long long rows, long long K, long long ldb,
+               long long zstride) {
+    const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rows),
+                              static_cast<uint64_t>(Z)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(ldb) * 2, static_cast<uint64_t>(zstride) * 2};
+    const uint32_t box[3] = {NBK, NBN, 1};
+    return encode_tmap(m, B, 3, dims, strides, box);
+}
+
+}  // namespace
+
+cudaError_t launch_nt_gemm(const NtGemm& g, cudaStream_t s) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidValue;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(nt_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 NT_SMEM_BYTES) != cudaSuccess)
+            return cudaErrorInvalidValue;
+        attr_set[dev] = true;
+    }
+    if (g.nph < 1 || g.nph > 2 || g.Z < 1 || (g.mode != NT_DENSE && g.Z > MAXSEG))
+        return cudaErrorInvalidValue;
+    if (g.N % 16 || g.K % NBK) return cudaErrorInvalidValue;
+    NtParams p;
+    memset(&p, 0, sizeof(p));
+    for (int ph = 0; ph < g.nph; ++ph) {
+        const NtOperand& a = g.A[ph];
+        const NtOperand& b = g.B[ph];
+        if (!make_nt_A(&p.mapA[ph], a.p, a.rows, a.K, a.ld)) return cudaErrorInvalidValue;
+        if (!make_nt_B(&p.mapB[ph], b.p, b.Z > 0 ? b.Z : 1, b.rows, b.K, b.ld, b.zstride))
+            return cudaErrorInvalidValue;
+        p.a_kofs[ph] = g.a_kofs[ph];
+        p.b_zc[ph] = g.b_zc[ph];
+    }
+    p.nph = g.nph;
+    p.mode = g.mode;
+    p.M = g.M;
+    p.N = g.N;
+    p.Z = g.Z;
+    p.kblocks = g.K / NBK;
+    p.a_zrow = g.a_zrow;
+    p.b_zrow = g.b_zrow;
+    p.b_z3 = g.b_z3;
+    p.offsets = g.offsets;
+    p.C = g.C;
+    p.ldc = g.ldc;
+    p.c_zs = g.c_zs;
+    p.accumulate = g.accumulate;
+    p.idesc = idesc_bf16_f32(NBM, NBN, /*b_mn_major=*/0);
+    p.err = g.err;
+    p.timeout_ns = wait_timeout_ns();
+    const long long nt = (g.N + NBN - 1) / NBN;
+    long long units;
+    if (g.mode == NT_MSEG)
+        units = ((g.M + NBM - 1) / NBM + g.Z) * nt;
+    else
+        units = static_cast<long long>(g.Z) * ((g.M + NBM - 1) / NBM) * nt;
+    long long grid = num_sms();
+    if (units < grid) grid = units;
+    if (grid < 1) grid = 1;
+    return launch_pdl(nt_gemm_kernel, dim3(static_cast<unsigned>(grid)), dim3(NT_THREADS),
+                      NT_SMEM_BYTES, s, p);
+}
+
+}  // namespace moe

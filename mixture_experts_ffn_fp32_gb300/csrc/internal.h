@@ -268,10 +268,60 @@ struct GenGemm {
 cudaError_t launch_gen_gemm(const GenGemm& p, int epi, cudaStream_t s);
 int gen_gemm_ntiles(int N);  // column tiles of a gen_gemm output of width N
 
+// NT grouped GEMM on the tensor cores (gemm_nt.cu): C (+)= A B^T, both
+// operands K-major BF16. A: rows x K (pitch ld); B: Z slices of rows x K.
+enum { NT_DENSE = 0, NT_MSEG = 1, NT_KSEG = 2 };
+struct NtOperand {
+    const void* p;
+    long long rows, K, ld, Z, zstride;
+};
+struct NtGemm {
+    int mode, M, N, K, Z, nph;  // K: per-phase reduction (multiple of 64); NT_KSEG: offsets
+    NtOperand A[2], B[2];
+    int a_kofs[2], b_zc[2];     // per phase: A column offset, B slice offset
+    int a_zrow, b_zrow, b_z3;   // NT_DENSE: per-problem A row, B row and B slice steps
+    const int32_t* offsets;     // [Z+1] device: NT_MSEG rows / NT_KSEG reduction columns
+    float* C;
+    long long ldc, c_zs;
+    int accumulate;
+    int* err;
+};
+cudaError_t launch_nt_gemm(const NtGemm& g, cudaStream_t s);
+
+// Backward operand preparation (bwd_prep.cu).
+// poff[z] = sum over z' < z of cnt_z' rounded up to 64 (cnt from offsets), z <= E.
+cudaError_t launch_pad_offsets(const int32_t* offsets, int E, int32_t* poff, cudaStream_t s);
+// dst[r, :cols] = BF16(src[idx ? idx[r] : r, :cols]) for r < rows; src FP32 or BF16.
+cudaError_t launch_gather_bf16(const void* src, int src_bf16, long long ld, const int32_t* idx,
+                               int rows, int cols, __nv_bfloat16* dst, cudaStream_t s);
+// Transposed, padded copy: dst[c, j] (pitch kpad) = BF16(src[row(j), c]) for
+// c < cols, j < kpad, with row(j) = j (j < nrows) when poff is null, else the
+// j-th padded column of the expert layout (poff/offsets: segment z's columns
+// poff[z] .. poff[z] + cnt_z map to rows offsets[z] ..), zero elsewhere;
+// src rows read through idx when given.
+cudaError_t launch_transpose_pad(const void* src, int src_bf16, long long ld, const int32_t* idx,
+                                 int nrows, int cols, const int32_t* poff, const int32_t* offsets,
+                                 int E, int kpad, __nv_bfloat16* dst, cudaStream_t s);
+// SwiGLU backward per row from FP32 a, u, dh [rows, F] (pitch ld) and the
+// row's gate weight (rowscale, or 1): da, du, hw = g h as BF16 [rows, F], and
+// dg[r] = sum_f dh h (optional).
+cudaError_t launch_swiglu_bwd(const float* a, const float* u, const float* dh, long long ld, int rows,
+                              int F, const float* rowscale, __nv_bfloat16* da, __nv_bfloat16* du,
+                              __nv_bfloat16* hw, float* dg, cudaStream_t s);
+
 // Backward scratch (FP32 arrays, byte offsets into the backward workspace).
 struct BwdLayout {
-    size_t dhp, da, du, hw, dwpart, dxs, dhs, das, dus, hs, dr, dg, glat, routed, dz, total;
+    int tc;  // the tensor-core form (bwd_on_tensor_cores)
+    size_t dhp, da, du, hw, dwpart, dxs, dhs, das, dus, hs, dr, dg, glat, routed, dz;
+    // tensor-core form only: BF16 operand copies, recomputed products, padding
+    size_t poff, gys, gysT, zsT, a, u, dab, dub, hwb, daT, duT, hwT, dwrow;
+    size_t doutb, doutT, xT, as, us, dasb, dusb, hsb, dasT, dusT, hsT;
+    long long tkpad, tpad;
+    size_t total;
 };
+// BF16 layers whose widths are multiples of 64 run the backward's expert
+// contractions on the tensor cores (gemm_nt.cu); the others on gemm_gen.cu.
+bool bwd_on_tensor_cores(const moe_config& c);
 BwdLayout plan_backward(const moe_config& c);
 // Enqueue the backward on s; ws holds the forward's routing and dispatch.
 moe_status backward_impl(const moe_config& c, const void* x, const moe_weights& w, const float* dout,
