@@ -23,6 +23,8 @@
 // CUDA cores in FP32 (gemm_gen.cu), BF16 operands converted exactly.
 #include <string.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -121,6 +123,14 @@ GenGemm gemm(int mode, int M, int N, int K, int Z, GenOp A, int a_m_contig, GenO
     return g;
 }
 
+// A dense CUDA-core product whose reduction runs over the tokens (weight
+// gradients of the router and the latent projections): split-K into `part`.
+cudaError_t run_splitk(GenGemm g, int epi, float* part, size_t part_floats, cudaStream_t s) {
+    g.ksplit = gen_gemm_ksplit(g, part_floats);
+    g.part = part;
+    return launch_gen_gemm(g, epi, s);
+}
+
 const void* offset_elems(const void* p, long long n, int bf16) {
     return static_cast<const uint8_t*>(p) + n * (bf16 ? 2 : 4);
 }
@@ -149,6 +159,11 @@ BwdLayout plan_backward(const moe_config& c) {
         return at;
     };
     B.dxs = take(TK * de * 4);
+    {
+        const size_t plane = std::max(static_cast<size_t>(c.d) * E, static_cast<size_t>(c.d) * L);
+        B.kpart_floats = std::min<size_t>(size_t(4) << 20, 64 * plane);
+        B.kpart = take(B.kpart_floats * 4);
+    }
     B.dr = take(T * E * 4);
     B.dg = take(TK * 4);
     B.glat = L ? take(T * L * 4) : 0;
@@ -250,9 +265,10 @@ moe_status backward_impl(const moe_config& c, const void* x, const moe_weights& 
             if ((e = launch_gather_sum(static_cast<const float*>(WP(L.ys)), inv, T, K, lat, nullptr,
                                        routed, 0, s)) != cudaSuccess)
                 return MOE_ERR_CUDA;
-            RUN(gemm(GEN_DENSE, lat, d, T, 1, op(routed, 0, 1, lat), 1, op(dout, 0, d, 1), 1,
-                     gr.dW_up_latent, d),
-                GEN_EPI_STORE);
+            if ((e = run_splitk(gemm(GEN_DENSE, lat, d, T, 1, op(routed, 0, 1, lat), 1,
+                                     op(dout, 0, d, 1), 1, gr.dW_up_latent, d),
+                                GEN_EPI_STORE, BP(BL.kpart), BL.kpart_floats, s)) != cudaSuccess)
+                return MOE_ERR_CUDA;
         }
         gy = glat;
         ld_gy = lat;
@@ -316,10 +332,11 @@ moe_status backward_impl(const moe_config& c, const void* x, const moe_weights& 
         float* dz = BP(BL.dz);
         if ((e = launch_gather_sum(dxs, inv, T, K, lat, nullptr, dz, 0, s)) != cudaSuccess)
             return MOE_ERR_CUDA;
-        if (gr.dW_down_latent)
-            RUN(gemm(GEN_DENSE, d, lat, T, 1, op(x, bf, 1, d), 1, op(dz, 0, lat, 1), 1,
-                     gr.dW_down_latent, lat),
-                GEN_EPI_STORE);
+        if (gr.dW_down_latent &&
+            (e = run_splitk(gemm(GEN_DENSE, d, lat, T, 1, op(x, bf, 1, d), 1, op(dz, 0, lat, 1), 1,
+                                 gr.dW_down_latent, lat),
+                            GEN_EPI_STORE, BP(BL.kpart), BL.kpart_floats, s)) != cudaSuccess)
+            return MOE_ERR_CUDA;
         RUN(gemm(GEN_DENSE, T, d, lat, 1, op(dz, 0, lat, 1), 0, op(w.W_down_latent, bf, 1, lat), 0,
                  gr.dx, d),
             GEN_EPI_STORE);
@@ -370,9 +387,11 @@ moe_status backward_impl(const moe_config& c, const void* x, const moe_weights& 
                         inv, tidx, tw, scores, T, K, E, c.gate, c.renormalize, c.routed_scale, dr,
                         dg)) != cudaSuccess)
         return MOE_ERR_CUDA;
-    if (gr.dW_router)
-        RUN(gemm(GEN_DENSE, d, E, T, 1, op(x, bf, 1, d), 1, op(dr, 0, E, 1), 1, gr.dW_router, E),
-            GEN_EPI_STORE);
+    if (gr.dW_router &&
+        (e = run_splitk(gemm(GEN_DENSE, d, E, T, 1, op(x, bf, 1, d), 1, op(dr, 0, E, 1), 1,
+                             gr.dW_router, E),
+                        GEN_EPI_STORE, BP(BL.kpart), BL.kpart_floats, s)) != cudaSuccess)
+        return MOE_ERR_CUDA;
     RUN(gemm(GEN_DENSE, T, d, E, 1, op(dr, 0, E, 1), 0, op(w.W_router, 0, 1, E), 0, gr.dx, d),
         GEN_EPI_ACCUM);
 #undef RUN
@@ -457,9 +476,9 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
             float* routed = BF(BL.routed);
             CK(launch_gather_sum(static_cast<const float*>(WP(L.ys)), inv, T, K, lat, nullptr,
                                  routed, 0, s));
-            CK(launch_gen_gemm(gemm(GEN_DENSE, lat, d, T, 1, op(routed, 0, 1, lat), 1,
-                                    op(dout, 0, d, 1), 1, gr.dW_up_latent, d),
-                               GEN_EPI_STORE, s));
+            CK(run_splitk(gemm(GEN_DENSE, lat, d, T, 1, op(routed, 0, 1, lat), 1,
+                               op(dout, 0, d, 1), 1, gr.dW_up_latent, d),
+                          GEN_EPI_STORE, BF(BL.kpart), BL.kpart_floats, s));
         }
         gy = glat;
         ld_gy = lat;
@@ -571,9 +590,9 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
         float* dz = BF(BL.dz);
         CK(launch_gather_sum(dxs, inv, T, K, lat, nullptr, dz, 0, s));
         if (gr.dW_down_latent)
-            CK(launch_gen_gemm(gemm(GEN_DENSE, d, lat, T, 1, op(x, 1, 1, d), 1, op(dz, 0, lat, 1), 1,
-                                    gr.dW_down_latent, lat),
-                               GEN_EPI_STORE, s));
+            CK(run_splitk(gemm(GEN_DENSE, d, lat, T, 1, op(x, 1, 1, d), 1, op(dz, 0, lat, 1), 1,
+                               gr.dW_down_latent, lat),
+                          GEN_EPI_STORE, BF(BL.kpart), BL.kpart_floats, s));
         CK(launch_gen_gemm(gemm(GEN_DENSE, T, d, lat, 1, op(dz, 0, lat, 1), 0,
                                 op(w.W_down_latent, 1, 1, lat), 0, gr.dx, d),
                            GEN_EPI_STORE, s));
@@ -613,9 +632,9 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
                   static_cast<const float*>(dwrow), 1, inv, tidx, tw, scores, T, K, E, c.gate,
                   c.renormalize, c.routed_scale, dr, dg));
     if (gr.dW_router)
-        CK(launch_gen_gemm(gemm(GEN_DENSE, d, E, T, 1, op(x, 1, 1, d), 1, op(dr, 0, E, 1), 1,
-                                gr.dW_router, E),
-                           GEN_EPI_STORE, s));
+        CK(run_splitk(gemm(GEN_DENSE, d, E, T, 1, op(x, 1, 1, d), 1, op(dr, 0, E, 1), 1,
+                           gr.dW_router, E),
+                      GEN_EPI_STORE, BF(BL.kpart), BL.kpart_floats, s));
     CK(launch_gen_gemm(gemm(GEN_DENSE, T, d, E, 1, op(dr, 0, E, 1), 0, op(w.W_router, 0, 1, E), 0,
                             gr.dx, d),
                        GEN_EPI_ACCUM, s));

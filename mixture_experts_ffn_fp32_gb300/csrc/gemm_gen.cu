@@ -76,6 +76,12 @@ __global__ void __launch_bounds__(256) gen_gemm_kernel(GenGemm p) {
 
     int z, m0, rows, n0, k0 = 0, k1 = p.K;
     long long a_z = 0, b_z = 0, c_z = 0;
+    if (p.ksplit > 1) {
+        // split-K: this CTA's slice of the reduction, into its own partial plane
+        const int kc = (p.K + p.ksplit - 1) / p.ksplit;
+        k0 = blockIdx.y * kc;
+        k1 = min(p.K, k0 + kc);
+    }
     if (p.mode == GEN_MSEG) {
         const int mt = u / nt;
         n0 = (u - mt * nt) * GBN;
@@ -226,8 +232,12 @@ __global__ void __launch_bounds__(256) gen_gemm_kernel(GenGemm p) {
             for (int j = 0; j < 4; ++j) {
                 const int n = n0 + tx * 4 + j;
                 if (n >= p.N) continue;
-                float* c = p.C + c_z + row * p.ldc + n;
                 const float v = g * acc[0][i][j];
+                if (p.ksplit > 1) {
+                    p.part[((static_cast<long long>(blockIdx.y) * p.Z + z) * p.M + row) * p.N + n] = v;
+                    continue;
+                }
+                float* c = p.C + c_z + row * p.ldc + n;
                 if (EPI == GEN_EPI_ACCUM)
                     *c += v;
                 else
@@ -237,7 +247,38 @@ __global__ void __launch_bounds__(256) gen_gemm_kernel(GenGemm p) {
     }
 }
 
+// C (=|+=) sum over the ksplit partial planes, in plane order.
+__global__ void __launch_bounds__(256) gen_reduce_kernel(const float* __restrict__ part, int ksplit,
+                                                         int Z, int M, int N, float* __restrict__ C,
+                                                         long long ldc, long long c_zs, int accumulate) {
+    pdl_wait();
+    pdl_trigger();
+    const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long plane = static_cast<long long>(Z) * M * N;
+    if (i >= plane) return;
+    float v = 0.0f;
+    for (int k = 0; k < ksplit; ++k) v += part[k * plane + i];
+    const long long z = i / (static_cast<long long>(M) * N);
+    const long long rem = i - z * M * N;
+    const long long m = rem / N, n = rem - m * N;
+    float* c = C + z * c_zs + m * ldc + n;
+    if (accumulate)
+        *c += v;
+    else
+        *c = v;
+}
+
 }  // namespace
+
+int gen_gemm_ksplit(const GenGemm& p, size_t part_floats) {
+    if (p.mode != GEN_DENSE) return 1;
+    const long long tiles = static_cast<long long>(p.Z) * ((p.M + GBM - 1) / GBM) * ((p.N + GBN - 1) / GBN);
+    const long long plane = static_cast<long long>(p.Z) * p.M * p.N;
+    long long ks = (2LL * num_sms() + tiles - 1) / tiles;      // about two CTAs per SM
+    ks = std::min<long long>(ks, (p.K + 255) / 256);           // at least 256 k per slice
+    ks = std::min<long long>(ks, plane > 0 ? static_cast<long long>(part_floats) / plane : 1);
+    return ks > 1 ? static_cast<int>(std::min<long long>(ks, 1024)) : 1;
+}
 
 cudaError_t launch_gen_gemm(const GenGemm& p, int epi, cudaStream_t s) {
     if (p.mode == GEN_MSEG && p.Z > MAXSEG) return cudaErrorInvalidValue;
@@ -248,6 +289,17 @@ cudaError_t launch_gen_gemm(const GenGemm& p, int epi, cudaStream_t s) {
     else
         tiles = static_cast<long long>(p.Z) * ((p.M + GBM - 1) / GBM) * nt;
     if (tiles < 1) return cudaSuccess;
+    if (p.ksplit > 1) {
+        if (p.mode != GEN_DENSE || epi == GEN_EPI_SWIGLU_BWD || p.part == nullptr)
+            return cudaErrorInvalidValue;
+        const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(p.ksplit));
+        cudaError_t e = launch_pdl(gen_gemm_kernel<GEN_EPI_STORE>, grid, dim3(256), 0, s, p);
+        if (e != cudaSuccess) return e;
+        const long long plane = static_cast<long long>(p.Z) * p.M * p.N;
+        return launch_pdl(gen_reduce_kernel, dim3(static_cast<unsigned>((plane + 255) / 256)), dim3(256), 0,
+                          s, static_cast<const float*>(p.part), p.ksplit, p.Z, p.M, p.N, p.C, p.ldc,
+                          p.c_zs, epi == GEN_EPI_ACCUM ? 1 : 0);
+    }
     const dim3 grid(static_cast<unsigned>(tiles));
     if (epi == GEN_EPI_SWIGLU_BWD) return launch_pdl(gen_gemm_kernel<GEN_EPI_SWIGLU_BWD>, grid, dim3(256), 0, s, p);
     if (epi == GEN_EPI_ACCUM) return launch_pdl(gen_gemm_kernel<GEN_EPI_ACCUM>, grid, dim3(256), 0, s, p);

@@ -264,8 +264,12 @@ struct GenGemm {
     const float* dh;         // SwiGLU backward: upstream gradient of h, same layout as C
     float *da, *du, *hw;     // SwiGLU backward outputs, same layout as C
     float* dwpart;           // optional [rows, column tiles] partials of sum dh h
+    int ksplit;              // GEN_DENSE store/accumulate: > 1 splits the reduction
+    float* part;             // ksplit x Z x M x N FP32 partials (ksplit > 1)
 };
 cudaError_t launch_gen_gemm(const GenGemm& p, int epi, cudaStream_t s);
+// ksplit a GEN_DENSE product should use with `part_floats` of scratch (1: none).
+int gen_gemm_ksplit(const GenGemm& p, size_t part_floats);
 int gen_gemm_ntiles(int N);  // column tiles of a gen_gemm output of width N
 
 // NT grouped GEMM on the tensor cores (gemm_nt.cu): C (+)= A B^T, both
@@ -317,6 +321,7 @@ struct BwdLayout {
     size_t poff, gys, gysT, zsT, a, u, dab, dub, hwb, daT, duT, hwT, dwrow;
     size_t doutb, doutT, xT, as, us, dasb, dusb, hsb, dasT, dusT, hsT;
     long long tkpad, tpad;
+    size_t kpart, kpart_floats;  // split-K partials of the long-reduction CUDA-core products
     size_t total;
 };
 // BF16 layers whose widths are multiples of 64 run the backward's expert
