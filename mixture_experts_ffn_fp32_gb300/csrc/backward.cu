@@ -192,21 +192,26 @@ BwdLayout plan_backward(const moe_config& c) {
         B.dhp = take(TK * F * 4);
         B.dab = take(TK * F * 2);
         B.dub = take(TK * F * 2);
-        B.hwb = take(TK * F * 2);
         B.daT = take(F * kp * 2);
         B.duT = take(F * kp * 2);
         B.hwT = take(F * kp * 2);
-        B.dwrow = take(TK * 4);
-        if (SF) {
+        B.dwrow = take(TK * ((F + 63) / 64) * 4);  // per-row partials of dg, one per 64 columns
+        if (SF || L) {
             B.doutb = take(T * c.d * 2);
             B.doutT = take(c.d * tp * 2);
             B.xT = take(c.d * tp * 2);
+        }
+        if (L) {
+            B.routedT = take(L * tp * 2);
+            B.dzT = take(L * tp * 2);
+            B.dzb = take(T * L * 2);
+        }
+        if (SF) {
             B.as = take(T * SF * 4);
             B.us = take(T * SF * 4);
             B.dhs = take(T * SF * 4);
             B.dasb = take(T * SF * 2);
             B.dusb = take(T * SF * 2);
-            B.hsb = take(T * SF * 2);
             B.dasT = take(SF * tp * 2);
             B.dusT = take(SF * tp * 2);
             B.hsT = take(SF * tp * 2);
@@ -462,6 +467,18 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
         return g;
     };
 
+    // BF16 copies of dout (and its transpose) and of x transposed: the shared
+    // experts' and the latent projections' operands
+    __nv_bfloat16 *doutb = nullptr, *doutT = nullptr, *xT = nullptr;
+    if (S || lat) {
+        doutb = BH(BL.doutb);
+        doutT = BH(BL.doutT);
+        xT = BH(BL.xT);
+        CK(launch_gather_bf16(dout, 0, d, nullptr, T, d, doutb, s));
+        CK(launch_transpose_pad(dout, 0, d, nullptr, T, d, nullptr, nullptr, 0, static_cast<int>(tp), doutT, s));
+        CK(launch_transpose_pad(x, 1, d, nullptr, T, d, nullptr, nullptr, 0, static_cast<int>(tp), xT, s));
+    }
+
     // upstream gradient of the routed sum (FP32) and the rows the experts act on
     const float* gy = dout;
     long long ld_gy = d;
@@ -469,16 +486,20 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
     long long ld_z = d;
     if (lat) {
         float* glat = BF(BL.glat);
-        CK(launch_gen_gemm(gemm(GEN_DENSE, T, lat, d, 1, op(dout, 0, d, 1), 0,
-                                op(w.W_up_latent, 1, 1, d), 0, glat, lat),
-                           GEN_EPI_STORE, s));
+        // gy = dout W_up_latent^T: W_up_latent [L, d] rows are K-major for this product
+        CK(launch_nt_gemm(nt(NT_DENSE, T, lat, d, 1, nt_op(doutb, T, d, d), nt_op(w.W_up_latent, lat, d, d),
+                             glat, lat),
+                          s));
         if (gr.dW_up_latent) {
+            // routed sum of the forward (latent width), then dW_up_latent = routed^T dout
             float* routed = BF(BL.routed);
+            __nv_bfloat16* routedT = BH(BL.routedT);
             CK(launch_gather_sum(static_cast<const float*>(WP(L.ys)), inv, T, K, lat, nullptr,
                                  routed, 0, s));
-            CK(run_splitk(gemm(GEN_DENSE, lat, d, T, 1, op(routed, 0, 1, lat), 1,
-                               op(dout, 0, d, 1), 1, gr.dW_up_latent, d),
-                          GEN_EPI_STORE, BF(BL.kpart), BL.kpart_floats, s));
+            CK(launch_transpose_pad(routed, 0, lat, nullptr, T, lat, nullptr, nullptr, 0, static_cast<int>(tp), routedT, s));
+            CK(launch_nt_gemm(nt(NT_DENSE, lat, d, static_cast<int>(tp), 1, nt_op(routedT, lat, tp, tp),
+                                 nt_op(doutT, d, tp, tp), gr.dW_up_latent, d),
+                              s));
         }
         gy = glat;
         ld_gy = lat;
@@ -517,43 +538,31 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
                          nt_op(w.W_down, F, de, de, E, static_cast<long long>(F) * de), dhp, F, 0,
                          offsets),
                       s));
-    __nv_bfloat16 *doutb = nullptr, *doutT = nullptr, *xT = nullptr;
     float* dhs = nullptr;
     if (S) {
-        doutb = BH(BL.doutb);
-        doutT = BH(BL.doutT);
-        xT = BH(BL.xT);
         dhs = BF(BL.dhs);
-        CK(launch_gather_bf16(dout, 0, d, nullptr, T, d, doutb, s));
-        CK(launch_transpose_pad(dout, 0, d, nullptr, T, d, nullptr, nullptr, 0, static_cast<int>(tp), doutT, s));
-        CK(launch_transpose_pad(x, 1, d, nullptr, T, d, nullptr, nullptr, 0, static_cast<int>(tp), xT, s));
         NtGemm g = nt(NT_DENSE, T, Fs, d, S, nt_op(doutb, T, d, d),
                       nt_op(w.Ws_down, Fs, d, d, S, static_cast<long long>(Fs) * d), dhs, SF, Fs);
         g.b_z3 = 1;
         CK(launch_nt_gemm(g, s));
     }
 
-    // ---- SwiGLU backward per row; transposed, padded copies ----
-    __nv_bfloat16 *dab = BH(BL.dab), *dub = BH(BL.dub), *hwb = BH(BL.hwb);
+    // ---- SwiGLU backward per row, with the transposed, padded copies ----
+    __nv_bfloat16 *dab = BH(BL.dab), *dub = BH(BL.dub);
     __nv_bfloat16 *daT = BH(BL.daT), *duT = BH(BL.duT), *hwT = BH(BL.hwT);
-    float* dwrow = BF(BL.dwrow);
-    CK(launch_swiglu_bwd(a, u, dhp, F, TK, F, sw, dab, dub, hwb, dwrow, s));
-    CK(launch_transpose_pad(dab, 1, F, nullptr, TK, F, poff, offsets, E, static_cast<int>(kp), daT, s));
-    CK(launch_transpose_pad(dub, 1, F, nullptr, TK, F, poff, offsets, E, static_cast<int>(kp), duT, s));
-    CK(launch_transpose_pad(hwb, 1, F, nullptr, TK, F, poff, offsets, E, static_cast<int>(kp), hwT, s));
-    __nv_bfloat16 *dasb = nullptr, *dusb = nullptr, *hsb = nullptr;
+    float* dgpart = BF(BL.dwrow);
+    CK(launch_swiglu_bwd_t(a, u, dhp, F, TK, F, sw, poff, offsets, E, static_cast<int>(kp), dab, dub,
+                           daT, duT, hwT, dgpart, s));
+    __nv_bfloat16 *dasb = nullptr, *dusb = nullptr;
     __nv_bfloat16 *dasT = nullptr, *dusT = nullptr, *hsT = nullptr;
     if (S) {
         dasb = BH(BL.dasb);
         dusb = BH(BL.dusb);
-        hsb = BH(BL.hsb);
         dasT = BH(BL.dasT);
         dusT = BH(BL.dusT);
         hsT = BH(BL.hsT);
-        CK(launch_swiglu_bwd(as, us, dhs, SF, T, SF, nullptr, dasb, dusb, hsb, nullptr, s));
-        CK(launch_transpose_pad(dasb, 1, SF, nullptr, T, SF, nullptr, nullptr, 0, static_cast<int>(tp), dasT, s));
-        CK(launch_transpose_pad(dusb, 1, SF, nullptr, T, SF, nullptr, nullptr, 0, static_cast<int>(tp), dusT, s));
-        CK(launch_transpose_pad(hsb, 1, SF, nullptr, T, SF, nullptr, nullptr, 0, static_cast<int>(tp), hsT, s));
+        CK(launch_swiglu_bwd_t(as, us, dhs, SF, T, SF, nullptr, nullptr, nullptr, 0,
+                               static_cast<int>(tp), dasb, dusb, dasT, dusT, hsT, nullptr, s));
     }
 
     // ---- G3: dz rows = da W_gate^T + du W_up^T (two phases) ----
@@ -588,14 +597,20 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
         CK(launch_gather_sum(dxs, inv, T, K, d, nullptr, gr.dx, 0, s));
     } else {
         float* dz = BF(BL.dz);
+        __nv_bfloat16 *dzb = BH(BL.dzb), *dzT = BH(BL.dzT);
         CK(launch_gather_sum(dxs, inv, T, K, lat, nullptr, dz, 0, s));
-        if (gr.dW_down_latent)
-            CK(run_splitk(gemm(GEN_DENSE, d, lat, T, 1, op(x, 1, 1, d), 1, op(dz, 0, lat, 1), 1,
-                               gr.dW_down_latent, lat),
-                          GEN_EPI_STORE, BF(BL.kpart), BL.kpart_floats, s));
-        CK(launch_gen_gemm(gemm(GEN_DENSE, T, d, lat, 1, op(dz, 0, lat, 1), 0,
-                                op(w.W_down_latent, 1, 1, lat), 0, gr.dx, d),
-                           GEN_EPI_STORE, s));
+        CK(launch_gather_bf16(dz, 0, lat, nullptr, T, lat, dzb, s));
+        if (gr.dW_down_latent) {
+            // dW_down_latent = x^T dz
+            CK(launch_transpose_pad(dz, 0, lat, nullptr, T, lat, nullptr, nullptr, 0, static_cast<int>(tp), dzT, s));
+            CK(launch_nt_gemm(nt(NT_DENSE, d, lat, static_cast<int>(tp), 1, nt_op(xT, d, tp, tp),
+                                 nt_op(dzT, lat, tp, tp), gr.dW_down_latent, lat),
+                              s));
+        }
+        // dx = dz W_down_latent^T: W_down_latent [d, L] rows are K-major for this product
+        CK(launch_nt_gemm(nt(NT_DENSE, T, d, lat, 1, nt_op(dzb, T, lat, lat),
+                             nt_op(w.W_down_latent, d, lat, lat), gr.dx, d),
+                          s));
     }
 
     // ---- shared experts: dx, weight gradients ----
@@ -629,8 +644,8 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
 
     // ---- router: dg -> dr -> dW_router and dx ----
     CK(launch_pdl(router_bwd_kernel, dim3((T * 32 + 255) / 256), dim3(256), 0, s,
-                  static_cast<const float*>(dwrow), 1, inv, tidx, tw, scores, T, K, E, c.gate,
-                  c.renormalize, c.routed_scale, dr, dg));
+                  static_cast<const float*>(dgpart), (F + 63) / 64, inv, tidx, tw, scores, T, K, E,
+                  c.gate, c.renormalize, c.routed_scale, dr, dg));
     if (gr.dW_router)
         CK(run_splitk(gemm(GEN_DENSE, d, E, T, 1, op(x, 1, 1, d), 1, op(dr, 0, E, 1), 1,
                            gr.dW_router, E),

@@ -274,8 +274,9 @@ int gen_gemm_ksplit(const GenGemm& p, size_t part_floats) {
     if (p.mode != GEN_DENSE) return 1;
     const long long tiles = static_cast<long long>(p.Z) * ((p.M + GBM - 1) / GBM) * ((p.N + GBN - 1) / GBN);
     const long long plane = static_cast<long long>(p.Z) * p.M * p.N;
-    long long ks = (2LL * num_sms() + tiles - 1) / tiles;      // about two CTAs per SM
-    ks = std::min<long long>(ks, (p.K + 255) / 256);           // at least 256 k per slice
+    long long ks = (4LL * num_sms() + tiles - 1) / tiles;      // about four CTAs per SM
+    ks = std::min<long long>(ks, (p.K + 63) / 64);             // at least 64 k per slice
+    ks = std::max<long long>(ks, (p.K + 1023) / 1024);         // and at most 1024 k per slice: its k-steps are not pipelined
     ks = std::min<long long>(ks, plane > 0 ? static_cast<long long>(part_floats) / plane : 1);
     return ks > 1 ? static_cast<int>(std::min<long long>(ks, 1024)) : 1;
 }

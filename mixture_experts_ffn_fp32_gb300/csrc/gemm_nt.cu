@@ -20,11 +20,13 @@
 // A unit accumulates one or two phases (e.g. da W_gate^T then du W_up^T),
 // each with its own pair of tensor maps and coordinate offsets.
 //
-// Tile 128 x 128, K step 64 (a 128-byte swizzle row), 6 TMA stages of 32 KB,
-// two 128-column TMEM accumulators. Warp 0 issues TMA, warp 1 the MMAs
-// (tcgen05.mma kind::f16, M = 128, N = 128, both operands K-major), warps
-// 2-5 drain one TMEM lane quarter each and write FP32 rows. Every wait is
-// bounded; on timeout the CTA stops, drains and flags the error word.
+// Tile 128 x BN (BN = 256 when N >= 256, else 128), K step 64 (a 128-byte
+// swizzle row), a 192 KB ring of TMA stages (4 of 48 KB, or 6 of 32 KB), two
+// BN-column TMEM accumulators. Warp 0 issues TMA, warp 1 the MMAs
+// (tcgen05.mma kind::f16, M = 128, N = BN, both operands K-major), warps 2-9
+// drain TMEM (two warps per lane quarter, each half of the columns) and
+// write FP32 rows. Every wait is bounded; on timeout the CTA stops, drains
+// and flags the error word.
 // Shapes: every K, N and row count the maps see is handled by TMA bounds and
 // masks, but each phase's K must be a multiple of 64 (the caller's choice).
 #include "common.cuh"
@@ -33,18 +35,24 @@
 namespace moe {
 namespace {
 
-constexpr int NBM = 128, NBN = 128, NBK = 64;
-constexpr int NT_STAGES = 6;
-constexpr int NT_TILE_BYTES = NBM * NBK * 2;  // 16 KB, A and B alike
-constexpr int NT_STAGE_BYTES = 2 * NT_TILE_BYTES;
-constexpr int NT_ACC_COLS = 128;
-constexpr int NT_TMEM_COLS = 256;
-constexpr int NT_THREADS = 192;
-constexpr int NT_BAR_OFF = NT_STAGES * NT_STAGE_BYTES;
-constexpr int NT_NBARS = 2 * NT_STAGES + 4 + 1;
-constexpr int NT_MISC_OFF = NT_BAR_OFF + 8 * NT_NBARS;
-constexpr int NT_SCHED_OFF = (NT_MISC_OFF + 16 + 15) / 16 * 16;
-constexpr int NT_SMEM_BYTES = NT_SCHED_OFF + 2 * (MAXSEG + 1) * 4 + 1024;
+constexpr int NBM = 128, NBK = 64;
+constexpr int NT_A_BYTES = NBM * NBK * 2;  // 16 KB
+constexpr int NT_THREADS = 320;
+constexpr int NT_EPI_WARPS = 8;
+
+template <int BN>
+struct NtGeo {
+    static constexpr int B_BYTES = BN * NBK * 2;
+    static constexpr int STAGE_BYTES = NT_A_BYTES + B_BYTES;
+    static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;
+    static constexpr int ACC_COLS = BN;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+    static constexpr int NBARS = 2 * STAGES + 4 + 1;
+    static constexpr int MISC_OFF = BAR_OFF + 8 * NBARS;
+    static constexpr int SCHED_OFF = (MISC_OFF + 16 + 15) / 16 * 16;
+    static constexpr int SMEM_BYTES = SCHED_OFF + 2 * (MAXSEG + 1) * 4 + 1024;
+};
 
 struct NtParams {
     CUtensorMap mapA[2];
@@ -68,6 +76,7 @@ struct NtUnit {
 };
 
 // s_tp: m-tile prefix per segment (NT_MSEG), s_off: offsets (NT_MSEG, NT_KSEG)
+template <int NBN>
 MOE_DEV NtUnit nt_unit(int u, const NtParams& p, int nt, int mt, const int* s_tp, const int* s_off) {
     NtUnit t;
     t.skip = false;
@@ -109,7 +118,16 @@ MOE_DEV NtUnit nt_unit(int u, const NtParams& p, int nt, int mt, const int* s_tp
     return t;
 }
 
+template <int NBN>
 __global__ void __launch_bounds__(NT_THREADS, 1) nt_gemm_kernel(const __grid_constant__ NtParams p) {
+    using G = NtGeo<NBN>;
+    constexpr int NT_STAGES = G::STAGES;
+    constexpr int NT_STAGE_BYTES = G::STAGE_BYTES;
+    constexpr int NT_ACC_COLS = G::ACC_COLS;
+    constexpr int NT_TMEM_COLS = G::TMEM_COLS;
+    constexpr int NT_BAR_OFF = G::BAR_OFF;
+    constexpr int NT_MISC_OFF = G::MISC_OFF;
+    constexpr int NT_SCHED_OFF = G::SCHED_OFF;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -133,7 +151,7 @@ __global__ void __launch_bounds__(NT_THREADS, 1) nt_gemm_kernel(const __grid_con
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 4);
+            mbar_init(tempty_bar(a), NT_EPI_WARPS);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -178,7 +196,7 @@ __global__ void __launch_bounds__(NT_THREADS, 1) nt_gemm_kernel(const __grid_con
             uint32_t phase = 0, issued = 0, last_par = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-                const NtUnit t = nt_unit(u, p, nt, mt, s_tp, s_off);
+                const NtUnit t = nt_unit<NBN>(u, p, nt, mt, s_tp, s_off);
                 if (t.skip) continue;
                 const int brow = t.n0 + t.z * p.b_zrow;
                 for (int ph = 0; ph < p.nph && ok; ++ph) {
@@ -191,7 +209,7 @@ __global__ void __launch_bounds__(NT_THREADS, 1) nt_gemm_kernel(const __grid_con
                         const uint32_t sA = sbase + stage * NT_STAGE_BYTES;
                         mbar_expect_tx(full_bar(stage), NT_STAGE_BYTES);
                         tma_load_2d(sA, &p.mapA[ph], kb * NBK + p.a_kofs[ph], t.arow, full_bar(stage));
-                        tma_load_3d(sA + NT_TILE_BYTES, &p.mapB[ph], kb * NBK, brow, bz, full_bar(stage));
+                        tma_load_3d(sA + NT_A_BYTES, &p.mapB[ph], kb * NBK, brow, bz, full_bar(stage));
                         issued |= 1u << stage;
                         last_par = (last_par & ~(1u << stage)) | (phase << stage);
                         if (++stage == NT_STAGES) {
@@ -211,9 +229,9 @@ __global__ void __launch_bounds__(NT_THREADS, 1) nt_gemm_kernel(const __grid_con
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             const uint64_t adesc0 = smem_desc_sw128(sbase, 16, 1024);
-            const uint64_t bdesc0 = smem_desc_sw128(sbase + NT_TILE_BYTES, 16, 1024);
+            const uint64_t bdesc0 = smem_desc_sw128(sbase + NT_A_BYTES, 16, 1024);
             for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-                const NtUnit t = nt_unit(u, p, nt, mt, s_tp, s_off);
+                const NtUnit t = nt_unit<NBN>(u, p, nt, mt, s_tp, s_off);
                 if (t.skip) continue;
                 if (!bounded_wait(tempty_bar(acc), acc_phase ^ 1u, wc)) break;
                 tc_fence_after();
@@ -246,12 +264,13 @@ __global__ void __launch_bounds__(NT_THREADS, 1) nt_gemm_kernel(const __grid_con
             bounded_drain(drain_bar, 0, p.timeout_ns, p.err);
         }
     } else {
-        // ---------------- epilogue warps 2..5 ----------------
-        const int q = warp & 3;  // TMEM lane quarter of this warp
+        // ---------------- epilogue warps 2..9 ----------------
+        const int q = warp & 3;            // TMEM lane quarter of this warp
+        const int half = (warp - 2) >> 2;  // which half of the tile's columns
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int u = blockIdx.x; u < total; u += gridDim.x) {
-            const NtUnit t = nt_unit(u, p, nt, mt, s_tp, s_off);
+            const NtUnit t = nt_unit<NBN>(u, p, nt, mt, s_tp, s_off);
             if (t.skip) continue;
             int ok = 1;
             if (lane == 0) ok = bounded_wait(tfull_bar(acc), acc_phase, wc) ? 1 : 0;
@@ -265,7 +284,7 @@ __global__ void __launch_bounds__(NT_THREADS, 1) nt_gemm_kernel(const __grid_con
             float* crow = p.C + (p.mode == NT_MSEG ? 0 : t.z * p.c_zs) +
                           static_cast<long long>(t.m0 + r) * p.ldc + t.n0;
 #pragma unroll 1
-            for (int c = 0; c < NBN; c += 16) {
+            for (int c = half * (NBN / 2); c < (half + 1) * (NBN / 2); c += 16) {
                 uint32_t v[16];
                 tc_ld_32x32b_x16(tb + c, v);
                 tc_wait_ld();
@@ -301,7 +320,7 @@ __global__ void __launch_bounds__(NT_THREADS, 1) nt_gemm_kernel(const __grid_con
     }
 }
 
-// A: rows x K_total, row pitch lda elements (K-major), box 64 x 128
+// A: rows x K_total, row pitch lda elements (K-major), box 64 x 128 rows
 bool make_nt_A(CUtensorMap* m, const void* A, long long rows, long long K, long long lda) {
     const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rows)};
     const uint64_t strides[1] = {static_cast<uint64_t>(lda) * 2};
@@ -309,39 +328,36 @@ bool make_nt_A(CUtensorMap* m, const void* A, long long rows, long long K, long 
     return encode_tmap(m, A, 2, dims, strides, box);
 }
 
-// B: Z slices of rows x K (K-major), row pitch ldb, slice pitch zstride elements
+// B: Z slices of rows x K (K-major), row pitch ldb, slice pitch zstride elements; box 64 x bn rows
 bool make_nt_B(CUtensorMap* m, const void* B, long long Z, long long rows, long long K, long long ldb,
-               long long zstride) {
+               long long zstride, int bn) {
     const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rows),
                               static_cast<uint64_t>(Z)};
     const uint64_t strides[2] = {static_cast<uint64_t>(ldb) * 2, static_cast<uint64_t>(zstride) * 2};
-    const uint32_t box[3] = {NBK, NBN, 1};
+    const uint32_t box[3] = {NBK, static_cast<uint32_t>(bn), 1};
     return encode_tmap(m, B, 3, dims, strides, box);
 }
 
-}  // namespace
 
-cudaError_t launch_nt_gemm(const NtGemm& g, cudaStream_t s) {
+template <int NBN>
+cudaError_t launch_nt_t(const NtGemm& g, cudaStream_t s) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidValue;
     if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(nt_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 NT_SMEM_BYTES) != cudaSuccess)
+        if (cudaFuncSetAttribute(nt_gemm_kernel<NBN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 NtGeo<NBN>::SMEM_BYTES) != cudaSuccess)
             return cudaErrorInvalidValue;
         attr_set[dev] = true;
     }
-    if (g.nph < 1 || g.nph > 2 || g.Z < 1 || (g.mode != NT_DENSE && g.Z > MAXSEG))
-        return cudaErrorInvalidValue;
-    if (g.N % 16 || g.K % NBK) return cudaErrorInvalidValue;
     NtParams p;
     memset(&p, 0, sizeof(p));
     for (int ph = 0; ph < g.nph; ++ph) {
         const NtOperand& a = g.A[ph];
         const NtOperand& b = g.B[ph];
         if (!make_nt_A(&p.mapA[ph], a.p, a.rows, a.K, a.ld)) return cudaErrorInvalidValue;
-        if (!make_nt_B(&p.mapB[ph], b.p, b.Z > 0 ? b.Z : 1, b.rows, b.K, b.ld, b.zstride))
+        if (!make_nt_B(&p.mapB[ph], b.p, b.Z > 0 ? b.Z : 1, b.rows, b.K, b.ld, b.zstride, NBN))
             return cudaErrorInvalidValue;
         p.a_kofs[ph] = g.a_kofs[ph];
         p.b_zc[ph] = g.b_zc[ph];
@@ -372,8 +388,30 @@ cudaError_t launch_nt_gemm(const NtGemm& g, cudaStream_t s) {
     long long grid = num_sms();
     if (units < grid) grid = units;
     if (grid < 1) grid = 1;
-    return launch_pdl(nt_gemm_kernel, dim3(static_cast<unsigned>(grid)), dim3(NT_THREADS),
-                      NT_SMEM_BYTES, s, p);
+    return launch_pdl(nt_gemm_kernel<NBN>, dim3(static_cast<unsigned>(grid)), dim3(NT_THREADS),
+                      NtGeo<NBN>::SMEM_BYTES, s, p);
+}
+
+}  // namespace
+
+cudaError_t launch_nt_gemm(const NtGemm& g, cudaStream_t s) {
+    if (g.nph < 1 || g.nph > 2 || g.Z < 1 || (g.mode != NT_DENSE && g.Z > MAXSEG))
+        return cudaErrorInvalidValue;
+    if (g.N % 16 || g.K % NBK) return cudaErrorInvalidValue;
+    // 128 x 256 tiles halve the A re-reads, but only while they still give
+    // every SM a unit, and (grouped by expert) while the segments average 256
+    // rows or more: short segments stream weights or store FP32 gradients,
+    // which narrower tiles spread over more SMs
+    bool wide = g.N >= 256;
+    if (g.mode == NT_MSEG) {
+        wide = wide && static_cast<long long>(g.M) >= 256LL * g.Z;
+    } else if (g.mode == NT_KSEG && static_cast<long long>(g.K) < 256LL * g.Z) {
+        wide = false;  // short reductions: the tiles' FP32 stores dominate; spread them
+    } else {
+        const long long units256 = static_cast<long long>(g.Z) * ((g.M + NBM - 1) / NBM) * ((g.N + 255) / 256);
+        wide = wide && units256 >= num_sms();
+    }
+    return wide ? launch_nt_t<256>(g, s) : launch_nt_t<128>(g, s);
 }
 
 }  // namespace moe

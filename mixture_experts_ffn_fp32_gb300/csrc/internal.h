@@ -306,20 +306,25 @@ cudaError_t launch_gather_bf16(const void* src, int src_bf16, long long ld, cons
 cudaError_t launch_transpose_pad(const void* src, int src_bf16, long long ld, const int32_t* idx,
                                  int nrows, int cols, const int32_t* poff, const int32_t* offsets,
                                  int E, int kpad, __nv_bfloat16* dst, cudaStream_t s);
-// SwiGLU backward per row from FP32 a, u, dh [rows, F] (pitch ld) and the
-// row's gate weight (rowscale, or 1): da, du, hw = g h as BF16 [rows, F], and
-// dg[r] = sum_f dh h (optional).
-cudaError_t launch_swiglu_bwd(const float* a, const float* u, const float* dh, long long ld, int rows,
-                              int F, const float* rowscale, __nv_bfloat16* da, __nv_bfloat16* du,
-                              __nv_bfloat16* hw, float* dg, cudaStream_t s);
+// SwiGLU backward from FP32 a, u, dh [rows, F] (pitch ld) and each row's
+// gate weight (rowscale, or 1), fused with the padded transposes (F, kpad
+// multiples of 64): da, du row-major BF16, daT, duT and (g h)T [F, kpad] BF16
+// in the padded layout of transpose_pad, dgpart [rows, F/64] = per 64
+// columns sum dh h (optional).
+cudaError_t launch_swiglu_bwd_t(const float* a, const float* u, const float* dh, long long ld,
+                                int nrows, int F, const float* rowscale, const int32_t* poff,
+                                const int32_t* offsets, int E, int kpad, __nv_bfloat16* da,
+                                __nv_bfloat16* du, __nv_bfloat16* daT, __nv_bfloat16* duT,
+                                __nv_bfloat16* hwT, float* dgpart, cudaStream_t s);
 
 // Backward scratch (FP32 arrays, byte offsets into the backward workspace).
 struct BwdLayout {
     int tc;  // the tensor-core form (bwd_on_tensor_cores)
     size_t dhp, da, du, hw, dwpart, dxs, dhs, das, dus, hs, dr, dg, glat, routed, dz;
     // tensor-core form only: BF16 operand copies, recomputed products, padding
-    size_t poff, gys, gysT, zsT, a, u, dab, dub, hwb, daT, duT, hwT, dwrow;
-    size_t doutb, doutT, xT, as, us, dasb, dusb, hsb, dasT, dusT, hsT;
+    size_t poff, gys, gysT, zsT, a, u, dab, dub, daT, duT, hwT, dwrow;
+    size_t doutb, doutT, xT, as, us, dasb, dusb, dasT, dusT, hsT;
+    size_t routedT, dzT, dzb;  // latent projections' BF16 operands
     long long tkpad, tpad;
     size_t kpart, kpart_floats;  // split-K partials of the long-reduction CUDA-core products
     size_t total;

@@ -68,6 +68,11 @@ TC_LAYERS = {
     "tc_renorm_all": W.Workload("g_t5", T=64, d=64, d_ff=64, E=8, K=2, n_shared=1,
                                 shared_d_ff=64, dtype="bf16", gate="softmax_all_renorm",
                                 has_bias=False),
+    # outputs 256 and more columns wide: the 128 x 256 tile form, ragged in N
+    "tc_wide": W.Workload("g_t6", T=200, d=256, d_ff=320, E=5, K=2, n_shared=1,
+                          shared_d_ff=256, dtype="bf16", gate="softmax_topk", bias_std=0.01),
+    "tc_wide_latent": W.Workload("g_t7", T=120, d=320, d_ff=256, E=6, K=2, n_shared=1,
+                                 shared_d_ff=64, dtype="bf16", gate="sigmoid", latent_dim=256),
 }
 
 
