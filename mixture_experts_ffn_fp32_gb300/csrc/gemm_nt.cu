@@ -25,7 +25,8 @@
 // BN-column TMEM accumulators. Warp 0 issues TMA, warp 1 the MMAs
 // (tcgen05.mma kind::f16, M = 128, N = BN, both operands K-major), warps 2-9
 // drain TMEM (two warps per lane quarter, each half of the columns) and
-// write FP32 rows. Every wait is bounded; on timeout the CTA stops, drains
+// write FP32 rows through a per-warp staging buffer, 8 rows x 64 contiguous
+// bytes per store. Every wait is bounded; on timeout the CTA stops, drains
 // and flags the error word.
 // Shapes: every K, N and row count the maps see is handled by TMA bounds and
 // masks, but each phase's K must be a multiple of 64 (the caller's choice).
@@ -51,7 +52,9 @@ struct NtGeo {
     static constexpr int NBARS = 2 * STAGES + 4 + 1;
     static constexpr int MISC_OFF = BAR_OFF + 8 * NBARS;
     static constexpr int SCHED_OFF = (MISC_OFF + 16 + 15) / 16 * 16;
-    static constexpr int SMEM_BYTES = SCHED_OFF + 2 * (MAXSEG + 1) * 4 + 1024;
+    static constexpr int STG_OFF = (SCHED_OFF + 2 * (MAXSEG + 1) * 4 + 127) / 128 * 128;
+    static constexpr int STG_BYTES = 32 * 16 * 4;  // per epilogue warp: 32 rows x 16 FP32
+    static constexpr int SMEM_BYTES = STG_OFF + NT_EPI_WARPS * STG_BYTES + 1024;
 };
 
 struct NtParams {
@@ -267,6 +270,10 @@ __global__ void __launch_bounds__(NT_THREADS, 1) nt_gemm_kernel(const __grid_con
         // ---------------- epilogue warps 2..9 ----------------
         const int q = warp & 3;            // TMEM lane quarter of this warp
         const int half = (warp - 2) >> 2;  // which half of the tile's columns
+        // staging: a row's 16 values in, then 8 rows x 64 contiguous bytes per
+        // store instruction out (16-byte slots XOR-swizzled by row: both
+        // directions bank-conflict free)
+        float4* stg = reinterpret_cast<float4*>(smem + G::STG_OFF + (warp - 2) * G::STG_BYTES);
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int u = blockIdx.x; u < total; u += gridDim.x) {
@@ -279,31 +286,40 @@ __global__ void __launch_bounds__(NT_THREADS, 1) nt_gemm_kernel(const __grid_con
             tc_fence_after();
             const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * NT_ACC_COLS) +
                                 (static_cast<uint32_t>(q * 32) << 16);
-            const int r = q * 32 + lane;
-            const bool row_ok = r < t.rows;
-            float* crow = p.C + (p.mode == NT_MSEG ? 0 : t.z * p.c_zs) +
-                          static_cast<long long>(t.m0 + r) * p.ldc + t.n0;
+            float* cbase = p.C + (p.mode == NT_MSEG ? 0 : t.z * p.c_zs);
 #pragma unroll 1
             for (int c = half * (NBN / 2); c < (half + 1) * (NBN / 2); c += 16) {
                 uint32_t v[16];
                 tc_ld_32x32b_x16(tb + c, v);
                 tc_wait_ld();
-                if (row_ok && t.n0 + c < p.N) {
-                    float4* dst = reinterpret_cast<float4*>(crow + c);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        float4 o = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                               __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-                        if (p.accumulate) {
-                            const float4 a = dst[j];
-                            o.x += a.x;
-                            o.y += a.y;
-                            o.z += a.z;
-                            o.w += a.w;
+                for (int j = 0; j < 4; ++j)
+                    stg[lane * 4 + (j ^ ((lane >> 1) & 3))] =
+                        make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                    __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                __syncwarp();
+                if (t.n0 + c < p.N) {
+#pragma unroll
+                    for (int it = 0; it < 4; ++it) {
+                        const int rr = it * 8 + (lane >> 2), qq = lane & 3;
+                        const int r = q * 32 + rr;
+                        if (r < t.rows) {
+                            float4 o = stg[rr * 4 + (qq ^ ((rr >> 1) & 3))];
+                            float4* dst = reinterpret_cast<float4*>(
+                                              cbase + static_cast<long long>(t.m0 + r) * p.ldc + t.n0 + c) +
+                                          qq;
+                            if (p.accumulate) {
+                                const float4 a = *dst;
+                                o.x += a.x;
+                                o.y += a.y;
+                                o.z += a.z;
+                                o.w += a.w;
+                            }
+                            *dst = o;
                         }
-                        dst[j] = o;
                     }
                 }
+                __syncwarp();
             }
             tc_fence_before();
             __syncwarp();
