@@ -187,15 +187,13 @@ BwdLayout plan_backward(const moe_config& c) {
         B.gys = take(TK * de * 2);
         B.gysT = take(de * kp * 2);
         B.zsT = take(de * kp * 2);
-        B.a = take(TK * F * 4);
-        B.u = take(TK * F * 4);
         B.dhp = take(TK * F * 4);
         B.dab = take(TK * F * 2);
         B.dub = take(TK * F * 2);
         B.daT = take(F * kp * 2);
         B.duT = take(F * kp * 2);
         B.hwT = take(F * kp * 2);
-        B.dwrow = take(TK * ((F + 63) / 64) * 4);  // per-row partials of dg, one per 64 columns
+        B.dwrow = take(TK * 2 * ((F + 127) / 128) * 4);  // per-row partials of dg, one per 64 columns
         if (SF || L) {
             B.doutb = take(T * c.d * 2);
             B.doutT = take(c.d * tp * 2);
@@ -207,8 +205,6 @@ BwdLayout plan_backward(const moe_config& c) {
             B.dzb = take(T * L * 2);
         }
         if (SF) {
-            B.as = take(T * SF * 4);
-            B.us = take(T * SF * 4);
             B.dhs = take(T * SF * 4);
             B.dasb = take(T * SF * 2);
             B.dusb = take(T * SF * 2);
@@ -514,24 +510,6 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
     CK(launch_transpose_pad(gy, 0, ld_gy, stok, TK, de, poff, offsets, E, static_cast<int>(kp), gysT, s));
     CK(launch_transpose_pad(zsrc, 1, ld_z, stok, TK, de, poff, offsets, E, static_cast<int>(kp), zsT, s));
 
-    // ---- recomputed gate and up products (the forward's GEMM, FP32 out) ----
-    float *a = BF(BL.a), *u = BF(BL.u);
-    float *as = S ? BF(BL.as) : nullptr, *us = S ? BF(BL.us) : nullptr;
-    for (int which = 0; which < 2; ++which) {
-        TcGemmArgs g{};
-        g.g[0] = TcGroup{1, de, WP(L.xs), de, TK, which ? w.W_up : w.W_gate, nullptr, E, F,
-                         which ? u : a, F, 1};
-        if (S)
-            g.g[1] = TcGroup{1, d, x, d, T, which ? w.Ws_up : w.Ws_gate, nullptr, S, Fs,
-                             which ? us : as, SF, 1};
-        g.E = E;
-        g.offsets = offsets;
-        g.mt_prefix = static_cast<const int32_t*>(WP(L.mt_prefix));
-        g.swiglu = 0;
-        g.err = err;
-        CK(launch_tc_gemm(g, s));
-    }
-
     // ---- G1: dh' = gy W_down^T (routed, per expert), dout Ws_down^T (shared) ----
     float* dhp = BF(BL.dhp);
     CK(launch_nt_gemm(nt(NT_MSEG, TK, F, de, E, nt_op(gys, TK, de, de),
@@ -547,22 +525,50 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
         CK(launch_nt_gemm(g, s));
     }
 
-    // ---- SwiGLU backward per row, with the transposed, padded copies ----
+    // ---- gate and up products recomputed by the forward's GEMM, whose SwiGLU
+    //      backward epilogue writes da, du (row-major and padded-transposed),
+    //      g h (padded-transposed) and the gate-gradient partials ----
     __nv_bfloat16 *dab = BH(BL.dab), *dub = BH(BL.dub);
     __nv_bfloat16 *daT = BH(BL.daT), *duT = BH(BL.duT), *hwT = BH(BL.hwT);
     float* dgpart = BF(BL.dwrow);
-    CK(launch_swiglu_bwd_t(a, u, dhp, F, TK, F, sw, poff, offsets, E, static_cast<int>(kp), dab, dub,
-                           daT, duT, hwT, dgpart, s));
     __nv_bfloat16 *dasb = nullptr, *dusb = nullptr;
     __nv_bfloat16 *dasT = nullptr, *dusT = nullptr, *hsT = nullptr;
-    if (S) {
-        dasb = BH(BL.dasb);
-        dusb = BH(BL.dusb);
-        dasT = BH(BL.dasT);
-        dusT = BH(BL.dusT);
-        hsT = BH(BL.hsT);
-        CK(launch_swiglu_bwd_t(as, us, dhs, SF, T, SF, nullptr, nullptr, nullptr, 0,
-                               static_cast<int>(tp), dasb, dusb, dasT, dusT, hsT, nullptr, s));
+    {
+        TcGemmArgs g{};
+        g.g[0] = TcGroup{1, de, WP(L.xs), de, TK, w.W_gate, w.W_up, E, F, nullptr, F, 0};
+        g.g[0].dh = dhp;
+        g.g[0].dh_ld = F;
+        g.g[0].da = dab;
+        g.g[0].du = dub;
+        g.g[0].daT = daT;
+        g.g[0].duT = duT;
+        g.g[0].hwT = hwT;
+        g.g[0].kpad = kp;
+        g.g[0].dgpart = dgpart;
+        if (S) {
+            dasb = BH(BL.dasb);
+            dusb = BH(BL.dusb);
+            dasT = BH(BL.dasT);
+            dusT = BH(BL.dusT);
+            hsT = BH(BL.hsT);
+            g.g[1] = TcGroup{1, d, x, d, T, w.Ws_gate, w.Ws_up, S, Fs, nullptr, SF, 0};
+            g.g[1].dh = dhs;
+            g.g[1].dh_ld = SF;
+            g.g[1].da = dasb;
+            g.g[1].du = dusb;
+            g.g[1].daT = dasT;
+            g.g[1].duT = dusT;
+            g.g[1].hwT = hsT;
+            g.g[1].kpad = tp;
+        }
+        g.E = E;
+        g.offsets = offsets;
+        g.mt_prefix = static_cast<const int32_t*>(WP(L.mt_prefix));
+        g.swiglu = TC_SWIGLU_BWD;
+        g.rowscale0 = sw;
+        g.poff = poff;
+        g.err = err;
+        CK(launch_tc_gemm(g, s));
     }
 
     // ---- G3: dz rows = da W_gate^T + du W_up^T (two phases) ----
@@ -644,7 +650,7 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
 
     // ---- router: dg -> dr -> dW_router and dx ----
     CK(launch_pdl(router_bwd_kernel, dim3((T * 32 + 255) / 256), dim3(256), 0, s,
-                  static_cast<const float*>(dgpart), (F + 63) / 64, inv, tidx, tw, scores, T, K, E,
+                  static_cast<const float*>(dgpart), 2 * ((F + 127) / 128), inv, tidx, tw, scores, T, K, E,
                   c.gate, c.renormalize, c.routed_scale, dr, dg));
     if (gr.dW_router)
         CK(run_splitk(gemm(GEN_DENSE, d, E, T, 1, op(x, 1, 1, d), 1, op(dr, 0, E, 1), 1,

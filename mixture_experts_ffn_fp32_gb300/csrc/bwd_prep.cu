@@ -2,9 +2,8 @@
 // operands K-major): BF16 copies of gathered rows, transposed copies laid out
 // per expert with each expert's rows padded to a multiple of 64 columns
 // (zero columns between experts, so an expert's weight-gradient reduction
-// covers whole k-blocks of its own rows only), and the SwiGLU backward of
-// each row. Sources: the chain rule of APEX-1 Mathematical Reference Part 3,
-// section 12.2 (SwiGLU) and 12.3 (SiLU), as in backward.cu.
+// covers whole k-blocks of its own rows only). The SwiGLU backward itself
+// runs in the epilogue of the recomputing gate/up GEMM (gemm_tc.cu).
 #include "common.cuh"
 #include "internal.h"
 
@@ -131,91 +130,6 @@ __global__ void __launch_bounds__(256) transpose_pad_kernel(
     }
 }
 
-// The SwiGLU backward of a 64 x 64 block (64 padded columns j of the
-// expert layout, i.e. 64 rows, by 64 hidden columns c): da, du row-major BF16
-// for the rows that exist, and da, du, g h transposed into the padded layout
-// (zero columns for padding), plus dgpart[row, c / 64] = sum over the block's
-// c of dh h. One pass over a, u, dh instead of a row pass and three
-// transposes.
-__global__ void __launch_bounds__(256) swiglu_bwd_t_kernel(
-    const float* __restrict__ a, const float* __restrict__ u, const float* __restrict__ dh,
-    long long ld, int nrows, int F, const float* __restrict__ rowscale,
-    const int32_t* __restrict__ poff, const int32_t* __restrict__ offsets, int E, int kpad,
-    __nv_bfloat16* __restrict__ da, __nv_bfloat16* __restrict__ du, __nv_bfloat16* __restrict__ daT,
-    __nv_bfloat16* __restrict__ duT, __nv_bfloat16* __restrict__ hwT, float* __restrict__ dgpart) {
-    __shared__ __nv_bfloat16 t_da[64][66], t_du[64][66], t_hw[64][66];  // [row j][c]
-    __shared__ float s_part[64][17];
-    __shared__ long long srow[64];
-    pdl_wait();
-    pdl_trigger();
-    const int j0 = blockIdx.x * 64, c0 = blockIdx.y * 64;
-    if (threadIdx.x < 64) srow[threadIdx.x] = pad_row(j0 + threadIdx.x, nrows, kpad, poff, offsets, E);
-    __syncthreads();
-    // 64 rows x 16 chunks of 4 columns: four chunks per thread
-    for (int i = threadIdx.x; i < 64 * 16; i += 256) {
-        const int jj = i >> 4, ch = i & 15;
-        const int c = c0 + ch * 4;
-        const long long r = srow[jj];
-        float o_da[4] = {0.f, 0.f, 0.f, 0.f}, o_du[4] = {0.f, 0.f, 0.f, 0.f}, o_hw[4] = {0.f, 0.f, 0.f, 0.f};
-        float part = 0.0f;
-        if (r >= 0 && c < F) {
-            const float g = rowscale ? rowscale[r] : 1.0f;
-            const float4 av = *reinterpret_cast<const float4*>(a + r * ld + c);
-            const float4 uv = *reinterpret_cast<const float4*>(u + r * ld + c);
-            const float4 dv = *reinterpret_cast<const float4*>(dh + r * ld + c);
-            const float aa[4] = {av.x, av.y, av.z, av.w}, uu[4] = {uv.x, uv.y, uv.z, uv.w};
-            const float dd[4] = {dv.x, dv.y, dv.z, dv.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float sg = 1.0f / (1.0f + expf(-aa[q]));
-                const float si = aa[q] * sg;
-                const float h = si * uu[q];
-                o_da[q] = g * dd[q] * uu[q] * (sg * (1.0f + aa[q] * (1.0f - sg)));
-                o_du[q] = g * dd[q] * si;
-                o_hw[q] = g * h;
-                part += dd[q] * h;
-            }
-            const long long o = r * F + c;
-            *reinterpret_cast<uint2*>(da + o) = make_uint2(pack_bf16x2(o_da[0], o_da[1]), pack_bf16x2(o_da[2], o_da[3]));
-            *reinterpret_cast<uint2*>(du + o) = make_uint2(pack_bf16x2(o_du[0], o_du[1]), pack_bf16x2(o_du[2], o_du[3]));
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            t_da[jj][ch * 4 + q] = __float2bfloat16_rn(o_da[q]);
-            t_du[jj][ch * 4 + q] = __float2bfloat16_rn(o_du[q]);
-            t_hw[jj][ch * 4 + q] = __float2bfloat16_rn(o_hw[q]);
-        }
-        s_part[jj][ch] = part;
-    }
-    __syncthreads();
-    if (dgpart != nullptr && threadIdx.x < 64 && srow[threadIdx.x] >= 0) {
-        float v = 0.0f;
-        for (int ch = 0; ch < 16; ++ch) v += s_part[threadIdx.x][ch];
-        dgpart[srow[threadIdx.x] * ((F + 63) / 64) + blockIdx.y] = v;
-    }
-    // transposed: 64 destination rows (c) x 8 chunks of 8 padded columns (j)
-    for (int i = threadIdx.x; i < 64 * 8; i += 256) {
-        const int cc = i >> 3, ch = i & 7;
-        const int c = c0 + cc, j = j0 + ch * 8;
-        if (c >= F || j >= kpad) continue;
-        uint32_t p0[4], p1[4], p2[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const int r0 = ch * 8 + 2 * t;
-            p0[t] = static_cast<uint32_t>(__bfloat16_as_ushort(t_da[r0][cc])) |
-                    (static_cast<uint32_t>(__bfloat16_as_ushort(t_da[r0 + 1][cc])) << 16);
-            p1[t] = static_cast<uint32_t>(__bfloat16_as_ushort(t_du[r0][cc])) |
-                    (static_cast<uint32_t>(__bfloat16_as_ushort(t_du[r0 + 1][cc])) << 16);
-            p2[t] = static_cast<uint32_t>(__bfloat16_as_ushort(t_hw[r0][cc])) |
-                    (static_cast<uint32_t>(__bfloat16_as_ushort(t_hw[r0 + 1][cc])) << 16);
-        }
-        const long long o = static_cast<long long>(c) * kpad + j;
-        *reinterpret_cast<uint4*>(daT + o) = make_uint4(p0[0], p0[1], p0[2], p0[3]);
-        *reinterpret_cast<uint4*>(duT + o) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
-        *reinterpret_cast<uint4*>(hwT + o) = make_uint4(p2[0], p2[1], p2[2], p2[3]);
-    }
-}
-
 }  // namespace
 
 cudaError_t launch_pad_offsets(const int32_t* offsets, int E, int32_t* poff, cudaStream_t s) {
@@ -239,17 +153,6 @@ cudaError_t launch_transpose_pad(const void* src, int src_bf16, long long ld, co
                           poff, offsets, E, kpad, dst);
     return launch_pdl(transpose_pad_kernel<false>, grid, dim3(256), 0, s, src, ld, idx, nrows, cols,
                       poff, offsets, E, kpad, dst);
-}
-
-cudaError_t launch_swiglu_bwd_t(const float* a, const float* u, const float* dh, long long ld,
-                                int nrows, int F, const float* rowscale, const int32_t* poff,
-                                const int32_t* offsets, int E, int kpad, __nv_bfloat16* da,
-                                __nv_bfloat16* du, __nv_bfloat16* daT, __nv_bfloat16* duT,
-                                __nv_bfloat16* hwT, float* dgpart, cudaStream_t s) {
-    if (F % 64 || ld % 4 || kpad % 64) return cudaErrorInvalidValue;
-    const dim3 grid(kpad / 64, F / 64);
-    return launch_pdl(swiglu_bwd_t_kernel, grid, dim3(256), 0, s, a, u, dh, ld, nrows, F, rowscale,
-                      poff, offsets, E, kpad, da, du, daT, duT, hwT, dgpart);
 }
 
 }  // namespace moe

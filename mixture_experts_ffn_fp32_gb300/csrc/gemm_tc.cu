@@ -6,6 +6,8 @@
 // the dispatch grouped for it, as in kimi_k3 StableLatentMoE "The actual
 // grouped GEMM, and the gradient path"):
 //   SwiGLU kernel : h[r, :]  = SiLU(A[r, :] W_gate[z]) * (A[r, :] W_up[z])
+//   its backward  : from a = A W_gate[z], u = A W_up[z] and the upstream dh:
+//                   da = g dh u SiLU'(a), du = g dh SiLU(a), g h (backward pass)
 //   plain kernel  : y[r, :]  = rowscale[r] * (A[r, :] B[z])   (routed down x gate weight)
 //                   y[t, :]  = A[t, :] B (+ addend[t, :])       (shared down, projections)
 // Two segment groups share one persistent launch, each with its own
@@ -95,6 +97,17 @@ struct TcParams {
     const float* rowscale0;
     const float* addend;
     int add_ld;
+    // TC_SWIGLU_BWD (see TcGroup)
+    const float* dh[2];
+    int dh_ld[2];
+    __nv_bfloat16* da[2];
+    __nv_bfloat16* du[2];
+    __nv_bfloat16* daT[2];
+    __nv_bfloat16* duT[2];
+    __nv_bfloat16* hwT[2];
+    long long kpad[2];
+    float* dgpart;
+    const int32_t* poff;
     int* err;
     unsigned long long timeout_ns;
 };
@@ -247,8 +260,9 @@ struct UnitCopies {
     }
 };
 
-template <bool SWIGLU, bool PAIR>
+template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __grid_constant__ TcParams p) {
+    constexpr bool SWIGLU = MODE != TC_PLAIN;
     using G = Geo<PAIR>;
     constexpr int STAGES = G::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -461,7 +475,96 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
             const size_t pitch = static_cast<size_t>(ld) * es;
             char* out_rows = static_cast<char*>(p.out[t.g]) +
                              static_cast<size_t>(my_out0 + q * 32) * pitch;
-            if (valid_rows <= 0) {
+            if (MODE == TC_SWIGLU_BWD) {
+                // padded column of this lane's row: the row's own, or a padding
+                // column of the segment (zeroed), or none
+                long long jrow = -1;
+                if (t.g == 0) {
+                    const long long jj = p.poff[t.zb] + (static_cast<long long>(orow) - s_off[t.zb]);
+                    if (jj < p.poff[t.zb + 1]) jrow = jj;
+                } else if (static_cast<long long>(orow) < p.kpad[1]) {
+                    jrow = static_cast<long long>(orow);
+                }
+                const bool row_valid = lane < valid_rows;
+                const float g = (t.g == 0 && p.rowscale0 != nullptr && row_valid) ? p.rowscale0[orow] : 1.0f;
+                const size_t bpitch = static_cast<size_t>(ld) * 2;
+                char* da_rows = reinterpret_cast<char*>(p.da[t.g]) + static_cast<size_t>(my_out0 + q * 32) * bpitch;
+                char* du_rows = reinterpret_cast<char*>(p.du[t.g]) + static_cast<size_t>(my_out0 + q * 32) * bpitch;
+                const long long kp = p.kpad[t.g];
+                float part = 0.0f;
+#pragma unroll 1
+                for (int c = half * 64; c < half * 64 + 64; c += 32) {
+                    uint32_t pda[16], pdu[16], phw[16];
+#pragma unroll
+                    for (int hc = 0; hc < 32; hc += 16) {
+                        uint32_t gv[16], uv[16];
+                        tc_ld_32x32b_x16(tb + c + hc, gv);
+                        tc_ld_32x32b_x16(tb + 128 + c + hc, uv);
+                        tc_wait_ld();
+                        const int lim = N - (t.n0 + c + hc);
+                        float dh[16];
+#pragma unroll
+                        for (int i = 0; i < 16; i += 4) {
+                            float4 d4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (row_valid && i < lim)
+                                d4 = *reinterpret_cast<const float4*>(
+                                    p.dh[t.g] + orow * static_cast<size_t>(p.dh_ld[t.g]) + t.out_col0 + c + hc + i);
+                            dh[i] = d4.x;
+                            dh[i + 1] = d4.y;
+                            dh[i + 2] = d4.z;
+                            dh[i + 3] = d4.w;
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; i += 2) {
+                            float o_da[2], o_du[2], o_hw[2];
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const float a = __uint_as_float(gv[i + e]), uu = __uint_as_float(uv[i + e]);
+                                const float sg = 1.0f / (1.0f + expf(-a));
+                                const float si = a * sg;
+                                const float h = si * uu;
+                                const float dv = row_valid ? dh[i + e] : 0.0f;
+                                o_da[e] = row_valid ? g * dv * uu * (sg * (1.0f + a * (1.0f - sg))) : 0.0f;
+                                o_du[e] = row_valid ? g * dv * si : 0.0f;
+                                o_hw[e] = row_valid ? g * h : 0.0f;
+                                part += row_valid ? dv * h : 0.0f;
+                            }
+                            pda[(hc + i) / 2] = pack_bf16x2(o_da[0], o_da[1]);
+                            pdu[(hc + i) / 2] = pack_bf16x2(o_du[0], o_du[1]);
+                            phw[(hc + i) / 2] = pack_bf16x2(o_hw[0], o_hw[1]);
+                        }
+                    }
+                    // row-major da, du: 32 BF16 of each row through the staging buffer
+                    const int vch = (N - (t.n0 + c)) / 8;
+                    const uint4 va[4] = {make_uint4(pda[0], pda[1], pda[2], pda[3]), make_uint4(pda[4], pda[5], pda[6], pda[7]),
+                                         make_uint4(pda[8], pda[9], pda[10], pda[11]), make_uint4(pda[12], pda[13], pda[14], pda[15])};
+                    warp_store_block(stg, va, lane, da_rows + static_cast<size_t>(t.out_col0 + c) * 2, bpitch,
+                                     valid_rows, vch);
+                    const uint4 vu[4] = {make_uint4(pdu[0], pdu[1], pdu[2], pdu[3]), make_uint4(pdu[4], pdu[5], pdu[6], pdu[7]),
+                                         make_uint4(pdu[8], pdu[9], pdu[10], pdu[11]), make_uint4(pdu[12], pdu[13], pdu[14], pdu[15])};
+                    warp_store_block(stg, vu, lane, du_rows + static_cast<size_t>(t.out_col0 + c) * 2, bpitch,
+                                     valid_rows, vch);
+                    // transposed: column f of the hidden layout, padded column jrow; the
+                    // lanes' consecutive rows make each store 64 contiguous bytes
+                    if (jrow >= 0) {
+                        uint16_t* dT = reinterpret_cast<uint16_t*>(p.daT[t.g]);
+                        uint16_t* uT = reinterpret_cast<uint16_t*>(p.duT[t.g]);
+                        uint16_t* hT = reinterpret_cast<uint16_t*>(p.hwT[t.g]);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            if (t.n0 + c + i < N) {
+                                const long long o = static_cast<long long>(t.out_col0 + c + i) * kp + jrow;
+                                const int sh = (i & 1) * 16;
+                                dT[o] = static_cast<uint16_t>(pda[i / 2] >> sh);
+                                uT[o] = static_cast<uint16_t>(pdu[i / 2] >> sh);
+                                hT[o] = static_cast<uint16_t>(phw[i / 2] >> sh);
+                            }
+                        }
+                    }
+                }
+                if (t.g == 0 && p.dgpart != nullptr && row_valid)
+                    p.dgpart[orow * static_cast<size_t>(2 * p.nt[0]) + 2 * (t.n0 / 128) + half] = part;
+            } else if (valid_rows <= 0) {
                 // none of this warp's 32 rows exist (the odd CTA of a short pair unit)
             } else if (SWIGLU) {
                 // 2 blocks of 32 BF16 columns per warp
@@ -607,12 +710,12 @@ bool make_B_map(CUtensorMap* m, const void* B, int Z, int K, int N) {
     return encode_tmap(m, B, 3, dims, strides, box);
 }
 
-template <bool SWIGLU, bool PAIR>
+template <int MODE, bool PAIR>
 bool prepare_kernel(int dev) {
     static bool attr_set[64] = {};
     if (dev < 0 || dev >= 64) return false;
     if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(tc_grouped_gemm_kernel<SWIGLU, PAIR>,
+        if (cudaFuncSetAttribute(tc_grouped_gemm_kernel<MODE, PAIR>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Geo<PAIR>::SMEM_BYTES) != cudaSuccess)
             return false;
@@ -623,13 +726,13 @@ bool prepare_kernel(int dev) {
 
 // How many CTA pairs of the pair kernel fit on the device at once (0: none,
 // or the query failed; the single-CTA form is used then).
-template <bool SWIGLU>
+template <int MODE>
 int pair_slots(int dev) {
     static int cache[64] = {};
     if (dev < 0 || dev >= 64) return 0;
     if (cache[dev] == 0) {
         int n = -1;
-        if (prepare_kernel<SWIGLU, true>(dev)) {
+        if (prepare_kernel<MODE, true>(dev)) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2 * static_cast<unsigned>(num_sms()));
             cfg.blockDim = dim3(THREADS);
@@ -642,7 +745,7 @@ int pair_slots(int dev) {
             cfg.attrs = attr;
             cfg.numAttrs = 1;
             int c = 0;
-            if (cudaOccupancyMaxActiveClusters(&c, tc_grouped_gemm_kernel<SWIGLU, true>, &cfg) ==
+            if (cudaOccupancyMaxActiveClusters(&c, tc_grouped_gemm_kernel<MODE, true>, &cfg) ==
                     cudaSuccess &&
                 c > 0)
                 n = c;
@@ -654,8 +757,9 @@ int pair_slots(int dev) {
     return cache[dev] > 0 ? cache[dev] : 0;
 }
 
-template <bool SWIGLU, bool PAIR>
+template <int MODE, bool PAIR>
 cudaError_t launch_tc_t(const TcGemmArgs& a, int nstrip, int slots, cudaStream_t s) {
+    constexpr bool SWIGLU = MODE != TC_PLAIN;
     constexpr int UROWS = PAIR ? 2 * BM : BM;
     TcParams p;
     memset(&p, 0, sizeof(p));
@@ -698,6 +802,17 @@ cudaError_t launch_tc_t(const TcGemmArgs& a, int nstrip, int slots, cudaStream_t
         p.out[g] = G.out;
         p.out_ld[g] = G.out_ld;
         p.out_f32[g] = G.out_f32;
+        p.dh[g] = G.dh;
+        p.dh_ld[g] = G.dh_ld;
+        p.da[g] = static_cast<__nv_bfloat16*>(G.da);
+        p.du[g] = static_cast<__nv_bfloat16*>(G.du);
+        p.daT[g] = static_cast<__nv_bfloat16*>(G.daT);
+        p.duT[g] = static_cast<__nv_bfloat16*>(G.duT);
+        p.hwT[g] = static_cast<__nv_bfloat16*>(G.hwT);
+        p.kpad[g] = G.kpad;
+        if (MODE == TC_SWIGLU_BWD && (!G.dh || !G.da || !G.du || !G.daT || !G.duT || !G.hwT ||
+                                      G.kpad <= 0 || G.dh_ld % 4))
+            return cudaErrorInvalidValue;
         if (g == 0)
             units_bound += static_cast<long long>((G.rows + UROWS - 1) / UROWS + a.E) * p.nt[0];
         else
@@ -711,21 +826,25 @@ cudaError_t launch_tc_t(const TcGemmArgs& a, int nstrip, int slots, cudaStream_t
     p.rowscale0 = a.rowscale0;
     p.addend = a.addend;
     p.add_ld = a.add_ld;
+    p.poff = a.poff;
+    p.dgpart = a.g[0].dgpart;
+    if (MODE == TC_SWIGLU_BWD && a.g[0].enabled && a.poff == nullptr) return cudaErrorInvalidValue;
     p.err = a.err;
     p.timeout_ns = wait_timeout_ns();
     long long grid = slots;  // persistent: one CTA (pair) per slot, at most one per unit
     if (units_bound < grid) grid = units_bound;
     if (grid < 1) grid = 1;
     if (PAIR)
-        return launch_pdl_cluster(tc_grouped_gemm_kernel<SWIGLU, true>,
+        return launch_pdl_cluster(tc_grouped_gemm_kernel<MODE, true>,
                                   dim3(2 * static_cast<unsigned>(grid)), dim3(THREADS),
                                   Geo<true>::SMEM_BYTES, s, 2, p);
-    return launch_pdl(tc_grouped_gemm_kernel<SWIGLU, false>, dim3(static_cast<unsigned>(grid)),
+    return launch_pdl(tc_grouped_gemm_kernel<MODE, false>, dim3(static_cast<unsigned>(grid)),
                       dim3(THREADS), Geo<false>::SMEM_BYTES, s, p);
 }
 
-template <bool SWIGLU>
+template <int MODE>
 cudaError_t launch_tc_s(const TcGemmArgs& a, cudaStream_t s) {
+    constexpr bool SWIGLU = MODE != TC_PLAIN;
     int dev = 0;
     cudaGetDevice(&dev);
     int nmax = 0;
@@ -738,16 +857,17 @@ cudaError_t launch_tc_s(const TcGemmArgs& a, cudaStream_t s) {
     const bool even = SWIGLU || nstrip % 2 == 0;
     const bool long_segments =
         !a.g[0].enabled || static_cast<long long>(a.g[0].rows) >= 512LL * (a.E > 0 ? a.E : 1);
-    const int slots = (even && long_segments) ? pair_slots<SWIGLU>(dev) : 0;
-    if (slots > 0) return launch_tc_t<SWIGLU, true>(a, nstrip, slots, s);
-    if (!prepare_kernel<SWIGLU, false>(dev)) return cudaErrorInvalidValue;
-    return launch_tc_t<SWIGLU, false>(a, nstrip, num_sms(), s);
+    const int slots = (even && long_segments) ? pair_slots<MODE>(dev) : 0;
+    if (slots > 0) return launch_tc_t<MODE, true>(a, nstrip, slots, s);
+    if (!prepare_kernel<MODE, false>(dev)) return cudaErrorInvalidValue;
+    return launch_tc_t<MODE, false>(a, nstrip, num_sms(), s);
 }
 
 }  // namespace
 
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t s) {
-    return a.swiglu ? launch_tc_s<true>(a, s) : launch_tc_s<false>(a, s);
+    if (a.swiglu == TC_SWIGLU_BWD) return launch_tc_s<TC_SWIGLU_BWD>(a, s);
+    return a.swiglu ? launch_tc_s<TC_SWIGLU>(a, s) : launch_tc_s<TC_PLAIN>(a, s);
 }
 
 }  // namespace moe

@@ -157,6 +157,8 @@ cudaError_t launch_gather_sum_split(const float* ys, const int32_t* inv, int T, 
 //     B = expert e's matrix; output rows = the same A rows.
 //   Group 1 ("dense"): S segments all over A rows [0, rows1), B = matrix s;
 //     output columns [s*N1, (s+1)*N1).
+// tc_grouped_gemm epilogues (TcGemmArgs::swiglu)
+enum { TC_PLAIN = 0, TC_SWIGLU = 1, TC_SWIGLU_BWD = 2 };
 struct TcGroup {
     int enabled;
     int K;              // reduction length of this group
@@ -177,6 +179,23 @@ struct TcGroup {
     int b_rows = 0;     // > 0: B has b_rows rows per matrix (rows beyond read as zero)
     int ksplit = 1;     // group 1 only: split K into ksplit slices; slice s writes the partial
                         // product to out rows [s*rows, (s+1)*rows) (needs Z == 1)
+    // TC_SWIGLU_BWD: with a, u the gate and up products of row r, column c (the
+    // SwiGLU layout of `out`, pitch out_ld), the upstream gradient dh of h
+    // (FP32, same layout, pitch dh_ld) and the row's gate weight g (group 0:
+    // rowscale0, group 1: 1): da = g dh u SiLU'(a), du = g dh SiLU(a) as BF16
+    // in da / du (pitch out_ld), and da, du, g h transposed as BF16 [cols, kpad]
+    // at column j(r) of the padded layout (group 0: poff / offsets; group 1:
+    // j = r), the padding columns zeroed; group 0 also dgpart[r, 2 tile + half]
+    // = sum of dh h over each 64 of the tile's columns.
+    const float* dh = nullptr;
+    int dh_ld = 0;
+    void* da = nullptr;
+    void* du = nullptr;
+    void* daT = nullptr;
+    void* duT = nullptr;
+    void* hwT = nullptr;
+    long long kpad = 0;
+    float* dgpart = nullptr;
 };
 
 struct TcGemmArgs {
@@ -184,7 +203,9 @@ struct TcGemmArgs {
     int E;                       // group 0 segment count
     const int32_t* offsets;      // group 0 [E+1]
     const int32_t* mt_prefix;    // group 0 [2(E+1)]: tiles of TC_BM rows, then of 2 TC_BM rows
-    int swiglu;                  // 1: h = SiLU(A B0) * (A B1); 0: single product
+    int swiglu;                  // TC_SWIGLU: h = SiLU(A B0) * (A B1); TC_PLAIN: single product;
+                                 // TC_SWIGLU_BWD: the SwiGLU backward epilogue (TcGroup)
+    const int32_t* poff;         // TC_SWIGLU_BWD group 0: padded column offsets [E+1]
     const float* rowscale0;      // group 0: multiply row r by rowscale0[r]
     const float* addend;         // group 1: add addend[r, col] (FP32 [rows1, add_ld])
     int add_ld;
@@ -306,24 +327,13 @@ cudaError_t launch_gather_bf16(const void* src, int src_bf16, long long ld, cons
 cudaError_t launch_transpose_pad(const void* src, int src_bf16, long long ld, const int32_t* idx,
                                  int nrows, int cols, const int32_t* poff, const int32_t* offsets,
                                  int E, int kpad, __nv_bfloat16* dst, cudaStream_t s);
-// SwiGLU backward from FP32 a, u, dh [rows, F] (pitch ld) and each row's
-// gate weight (rowscale, or 1), fused with the padded transposes (F, kpad
-// multiples of 64): da, du row-major BF16, daT, duT and (g h)T [F, kpad] BF16
-// in the padded layout of transpose_pad, dgpart [rows, F/64] = per 64
-// columns sum dh h (optional).
-cudaError_t launch_swiglu_bwd_t(const float* a, const float* u, const float* dh, long long ld,
-                                int nrows, int F, const float* rowscale, const int32_t* poff,
-                                const int32_t* offsets, int E, int kpad, __nv_bfloat16* da,
-                                __nv_bfloat16* du, __nv_bfloat16* daT, __nv_bfloat16* duT,
-                                __nv_bfloat16* hwT, float* dgpart, cudaStream_t s);
-
 // Backward scratch (FP32 arrays, byte offsets into the backward workspace).
 struct BwdLayout {
     int tc;  // the tensor-core form (bwd_on_tensor_cores)
     size_t dhp, da, du, hw, dwpart, dxs, dhs, das, dus, hs, dr, dg, glat, routed, dz;
     // tensor-core form only: BF16 operand copies, recomputed products, padding
-    size_t poff, gys, gysT, zsT, a, u, dab, dub, daT, duT, hwT, dwrow;
-    size_t doutb, doutT, xT, as, us, dasb, dusb, dasT, dusT, hsT;
+    size_t poff, gys, gysT, zsT, dab, dub, daT, duT, hwT, dwrow;
+    size_t doutb, doutT, xT, dasb, dusb, dasT, dusT, hsT;
     size_t routedT, dzT, dzb;  // latent projections' BF16 operands
     long long tkpad, tpad;
     size_t kpart, kpart_floats;  // split-K partials of the long-reduction CUDA-core products
