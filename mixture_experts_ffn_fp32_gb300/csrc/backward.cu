@@ -180,37 +180,30 @@ BwdLayout plan_backward(const moe_config& c) {
         B.dus = SF ? take(T * SF * 4) : 0;
         B.hs = SF ? take(T * SF * 4) : 0;
     } else {
+        // expert-padded row layout: each expert's rows, then zero rows up to a multiple of 64
         B.tkpad = static_cast<long long>((TK + 63) / 64 * 64 + 64 * E);  // >= padded total
         B.tpad = static_cast<long long>((T + 63) / 64 * 64);
-        const size_t kp = static_cast<size_t>(B.tkpad), tp = static_cast<size_t>(B.tpad);
+        const size_t kp = static_cast<size_t>(B.tkpad);
         B.poff = take((E + 1) * 4);
-        B.gys = take(TK * de * 2);
-        B.gysT = take(de * kp * 2);
-        B.zsT = take(de * kp * 2);
-        B.dhp = take(TK * F * 4);
-        B.dab = take(TK * F * 2);
-        B.dub = take(TK * F * 2);
-        B.daT = take(F * kp * 2);
-        B.duT = take(F * kp * 2);
-        B.hwT = take(F * kp * 2);
+        B.invp = take(TK * 4);
+        B.gys = take(kp * de * 2);
+        B.zs = take(kp * de * 2);
+        B.dhp = take(kp * F * 4);
+        B.dab = take(kp * F * 2);
+        B.dub = take(kp * F * 2);
+        B.hwb = take(kp * F * 2);
         B.dwrow = take(TK * 2 * ((F + 127) / 128) * 4);  // per-row partials of dg, one per 64 columns
-        if (SF || L) {
-            B.doutb = take(T * c.d * 2);
-            B.doutT = take(c.d * tp * 2);
-            B.xT = take(c.d * tp * 2);
-        }
+        B.dxsp = take(kp * de * 4);
+        if (SF || L) B.doutb = take(T * c.d * 2);
         if (L) {
-            B.routedT = take(L * tp * 2);
-            B.dzT = take(L * tp * 2);
+            B.routedb = take(T * L * 2);
             B.dzb = take(T * L * 2);
         }
         if (SF) {
             B.dhs = take(T * SF * 4);
             B.dasb = take(T * SF * 2);
             B.dusb = take(T * SF * 2);
-            B.dasT = take(SF * tp * 2);
-            B.dusT = take(SF * tp * 2);
-            B.hsT = take(SF * tp * 2);
+            B.hsb = take(T * SF * 2);
         }
     }
     B.total = o;
@@ -399,21 +392,25 @@ moe_status backward_impl(const moe_config& c, const void* x, const moe_weights& 
     return MOE_OK;
 }
 
-// The tensor-core form (BF16 layers, widths multiples of 64): the gate and up
-// products recomputed by the forward's grouped GEMM (plain epilogue, FP32
-// out), every other expert contraction by the NT kernel on BF16 operands
-// laid out for it; the SwiGLU backward per row in between. Upstream
-// gradients and activation gradients enter the tensor cores rounded to BF16;
-// every sum is FP32.
+// The tensor-core form (BF16 layers, widths multiples of 64). The routed
+// rows live in the expert-padded row layout (each expert's rows, then zero
+// rows up to a multiple of 64), so every per-expert reduction covers whole
+// 64-row k-blocks of its own rows. dh = gy W_down^T and dz = da W_gate^T +
+// du W_up^T run on the NT kernel (both operands K-major: the weights as they
+// are); the gate and up products are recomputed by the forward's grouped
+// GEMM, whose backward epilogue writes da, du and g h; the weight gradients
+// run on the NT kernel with both operands MN-major (the row-major
+// activations as they are, C = A^T B over the rows). Upstream and activation
+// gradients enter the tensor cores rounded to BF16; every sum is FP32.
 static moe_status backward_tc(const moe_config& c, const void* x, const moe_weights& w,
                               const float* dout, const moe_grads& gr, uint8_t* ws, uint8_t* bws,
                               cudaStream_t s) {
     const WsLayout L = plan_workspace(c);
     const BwdLayout BL = plan_backward(c);
-    const int T = c.T, K = c.K, E = c.E, TK = T * K, F = c.d_ff, d = c.d;
+    const int T = c.T, K = c.K, E = c.E, TK = T * c.K, F = c.d_ff, d = c.d;
     const int lat = c.latent_dim, de = lat ? lat : d;
     const int S = c.n_shared, Fs = S ? c.shared_d_ff : 0, SF = S * Fs;
-    const long long kp = BL.tkpad, tp = BL.tpad;
+    const int kp = static_cast<int>(BL.tkpad), tp = static_cast<int>(BL.tpad);
     int* err = reinterpret_cast<int*>(ws + L.err);
     auto WP = [&](size_t off) { return static_cast<void*>(ws + off); };
     auto BF = [&](size_t off) { return reinterpret_cast<float*>(bws + off); };
@@ -426,14 +423,17 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
     const float* tw = static_cast<const float*>(WP(L.topk_w));
     const float* scores = L.scores ? static_cast<const float*>(WP(L.scores)) : nullptr;
     int32_t* poff = reinterpret_cast<int32_t*>(bws + BL.poff);
-    float *dxs = BF(BL.dxs), *dr = BF(BL.dr), *dg = BF(BL.dg);
+    int32_t* invp = reinterpret_cast<int32_t*>(bws + BL.invp);
+    float *dr = BF(BL.dr), *dg = BF(BL.dg);
     cudaError_t e;
-#define CK(call)                                     \
-    do {                                             \
-        if ((e = (call)) != cudaSuccess) return MOE_ERR_CUDA; \
+#define CK(call)                                                  \
+    do {                                                          \
+        if ((e = (call)) != cudaSuccess) return MOE_ERR_CUDA;     \
     } while (0)
-    auto nt_op = [](const void* p, long long rows, long long K_, long long ld, long long Z = 1,
-                    long long zstride = 0) {
+    // K-major operand: rows x K (pitch ld), optionally Z slices; MN-major:
+    // K rows of `rows` columns (pitch ld)
+    auto opnd = [](const void* p, long long rows, long long K_, long long ld, long long Z = 1,
+                   long long zstride = 0) {
         NtOperand o;
         o.p = p;
         o.rows = rows;
@@ -462,17 +462,19 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
         g.err = err;
         return g;
     };
+    auto tn = [&](int mode, int M, int N, int K_, int Z, NtOperand A, NtOperand B, float* C,
+                  long long ldc, long long c_zs = 0, const int32_t* offs = nullptr) {
+        NtGemm g = nt(mode, M, N, K_, Z, A, B, C, ldc, c_zs, offs);
+        g.a_mn = 1;
+        g.b_mn = 1;
+        return g;
+    };
 
-    // BF16 copies of dout (and its transpose) and of x transposed: the shared
-    // experts' and the latent projections' operands
-    __nv_bfloat16 *doutb = nullptr, *doutT = nullptr, *xT = nullptr;
+    // BF16 copy of dout: the shared experts' and the latent projections' operand
+    __nv_bfloat16* doutb = nullptr;
     if (S || lat) {
         doutb = BH(BL.doutb);
-        doutT = BH(BL.doutT);
-        xT = BH(BL.xT);
         CK(launch_gather_bf16(dout, 0, d, nullptr, T, d, doutb, s));
-        CK(launch_transpose_pad(dout, 0, d, nullptr, T, d, nullptr, nullptr, 0, static_cast<int>(tp), doutT, s));
-        CK(launch_transpose_pad(x, 1, d, nullptr, T, d, nullptr, nullptr, 0, static_cast<int>(tp), xT, s));
     }
 
     // upstream gradient of the routed sum (FP32) and the rows the experts act on
@@ -483,18 +485,18 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
     if (lat) {
         float* glat = BF(BL.glat);
         // gy = dout W_up_latent^T: W_up_latent [L, d] rows are K-major for this product
-        CK(launch_nt_gemm(nt(NT_DENSE, T, lat, d, 1, nt_op(doutb, T, d, d), nt_op(w.W_up_latent, lat, d, d),
+        CK(launch_nt_gemm(nt(NT_DENSE, T, lat, d, 1, opnd(doutb, T, d, d), opnd(w.W_up_latent, lat, d, d),
                              glat, lat),
                           s));
         if (gr.dW_up_latent) {
             // routed sum of the forward (latent width), then dW_up_latent = routed^T dout
             float* routed = BF(BL.routed);
-            __nv_bfloat16* routedT = BH(BL.routedT);
+            __nv_bfloat16* routedb = BH(BL.routedb);
             CK(launch_gather_sum(static_cast<const float*>(WP(L.ys)), inv, T, K, lat, nullptr,
                                  routed, 0, s));
-            CK(launch_transpose_pad(routed, 0, lat, nullptr, T, lat, nullptr, nullptr, 0, static_cast<int>(tp), routedT, s));
-            CK(launch_nt_gemm(nt(NT_DENSE, lat, d, static_cast<int>(tp), 1, nt_op(routedT, lat, tp, tp),
-                                 nt_op(doutT, d, tp, tp), gr.dW_up_latent, d),
+            CK(launch_gather_bf16(routed, 0, lat, nullptr, T, lat, routedb, s));
+            CK(launch_nt_gemm(tn(NT_DENSE, lat, d, tp, 1, opnd(routedb, lat, T, lat), opnd(doutb, d, T, d),
+                                 gr.dW_up_latent, d),
                               s));
         }
         gy = glat;
@@ -503,36 +505,32 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
         ld_z = lat;
     }
 
-    // ---- operand copies: expert-padded columns, gathered rows ----
+    // ---- the expert-padded row layout: offsets, positions, gathered rows ----
     CK(launch_pad_offsets(offsets, E, poff, s));
-    __nv_bfloat16 *gys = BH(BL.gys), *gysT = BH(BL.gysT), *zsT = BH(BL.zsT);
-    CK(launch_gather_bf16(gy, 0, ld_gy, stok, TK, de, gys, s));
-    CK(launch_transpose_pad(gy, 0, ld_gy, stok, TK, de, poff, offsets, E, static_cast<int>(kp), gysT, s));
-    CK(launch_transpose_pad(zsrc, 1, ld_z, stok, TK, de, poff, offsets, E, static_cast<int>(kp), zsT, s));
+    CK(launch_pad_inverse(inv, tidx, TK, poff, offsets, invp, s));
+    __nv_bfloat16 *gys = BH(BL.gys), *zs = BH(BL.zs);
+    CK(launch_gather_pad_bf16(gy, 0, ld_gy, stok, TK, de, poff, offsets, E, kp, gys, s));
+    CK(launch_gather_pad_bf16(zsrc, 1, ld_z, stok, TK, de, poff, offsets, E, kp, zs, s));
 
-    // ---- G1: dh' = gy W_down^T (routed, per expert), dout Ws_down^T (shared) ----
+    // ---- dh = gy W_down^T per expert (padded rows), dout Ws_down^T (shared) ----
     float* dhp = BF(BL.dhp);
-    CK(launch_nt_gemm(nt(NT_MSEG, TK, F, de, E, nt_op(gys, TK, de, de),
-                         nt_op(w.W_down, F, de, de, E, static_cast<long long>(F) * de), dhp, F, 0,
-                         offsets),
+    CK(launch_nt_gemm(nt(NT_MSEG, kp, F, de, E, opnd(gys, kp, de, de),
+                         opnd(w.W_down, F, de, de, E, static_cast<long long>(F) * de), dhp, F, 0, poff),
                       s));
     float* dhs = nullptr;
     if (S) {
         dhs = BF(BL.dhs);
-        NtGemm g = nt(NT_DENSE, T, Fs, d, S, nt_op(doutb, T, d, d),
-                      nt_op(w.Ws_down, Fs, d, d, S, static_cast<long long>(Fs) * d), dhs, SF, Fs);
+        NtGemm g = nt(NT_DENSE, T, Fs, d, S, opnd(doutb, T, d, d),
+                      opnd(w.Ws_down, Fs, d, d, S, static_cast<long long>(Fs) * d), dhs, SF, Fs);
         g.b_z3 = 1;
         CK(launch_nt_gemm(g, s));
     }
 
-    // ---- gate and up products recomputed by the forward's GEMM, whose SwiGLU
-    //      backward epilogue writes da, du (row-major and padded-transposed),
-    //      g h (padded-transposed) and the gate-gradient partials ----
-    __nv_bfloat16 *dab = BH(BL.dab), *dub = BH(BL.dub);
-    __nv_bfloat16 *daT = BH(BL.daT), *duT = BH(BL.duT), *hwT = BH(BL.hwT);
+    // ---- gate and up products recomputed by the forward's GEMM; its SwiGLU
+    //      backward epilogue writes da, du, g h and the gate-gradient partials ----
+    __nv_bfloat16 *dab = BH(BL.dab), *dub = BH(BL.dub), *hwb = BH(BL.hwb);
     float* dgpart = BF(BL.dwrow);
-    __nv_bfloat16 *dasb = nullptr, *dusb = nullptr;
-    __nv_bfloat16 *dasT = nullptr, *dusT = nullptr, *hsT = nullptr;
+    __nv_bfloat16 *dasb = nullptr, *dusb = nullptr, *hsb = nullptr;
     {
         TcGemmArgs g{};
         g.g[0] = TcGroup{1, de, WP(L.xs), de, TK, w.W_gate, w.W_up, E, F, nullptr, F, 0};
@@ -540,26 +538,18 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
         g.g[0].dh_ld = F;
         g.g[0].da = dab;
         g.g[0].du = dub;
-        g.g[0].daT = daT;
-        g.g[0].duT = duT;
-        g.g[0].hwT = hwT;
-        g.g[0].kpad = kp;
+        g.g[0].hw = hwb;
         g.g[0].dgpart = dgpart;
         if (S) {
             dasb = BH(BL.dasb);
             dusb = BH(BL.dusb);
-            dasT = BH(BL.dasT);
-            dusT = BH(BL.dusT);
-            hsT = BH(BL.hsT);
+            hsb = BH(BL.hsb);
             g.g[1] = TcGroup{1, d, x, d, T, w.Ws_gate, w.Ws_up, S, Fs, nullptr, SF, 0};
             g.g[1].dh = dhs;
             g.g[1].dh_ld = SF;
             g.g[1].da = dasb;
             g.g[1].du = dusb;
-            g.g[1].daT = dasT;
-            g.g[1].duT = dusT;
-            g.g[1].hwT = hsT;
-            g.g[1].kpad = tp;
+            g.g[1].hw = hsb;
         }
         g.E = E;
         g.offsets = offsets;
@@ -571,78 +561,73 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
         CK(launch_tc_gemm(g, s));
     }
 
-    // ---- G3: dz rows = da W_gate^T + du W_up^T (two phases) ----
+    // ---- dz rows = da W_gate^T + du W_up^T (padded rows, two phases) ----
+    float* dxsp = BF(BL.dxsp);
     {
-        NtGemm g = nt(NT_MSEG, TK, de, F, E, nt_op(dab, TK, F, F),
-                      nt_op(w.W_gate, de, F, F, E, static_cast<long long>(de) * F), dxs, de, 0,
-                      offsets);
+        NtGemm g = nt(NT_MSEG, kp, de, F, E, opnd(dab, kp, F, F),
+                      opnd(w.W_gate, de, F, F, E, static_cast<long long>(de) * F), dxsp, de, 0, poff);
         g.nph = 2;
-        g.A[1] = nt_op(dub, TK, F, F);
-        g.B[1] = nt_op(w.W_up, de, F, F, E, static_cast<long long>(de) * F);
+        g.A[1] = opnd(dub, kp, F, F);
+        g.B[1] = opnd(w.W_up, de, F, F, E, static_cast<long long>(de) * F);
         CK(launch_nt_gemm(g, s));
     }
-    // ---- expert weight gradients over each expert's padded columns ----
+    // ---- expert weight gradients: sums over each expert's padded rows of the
+    //      row-major operands (both MN-major) ----
     if (gr.dW_down)
-        CK(launch_nt_gemm(nt(NT_KSEG, F, de, static_cast<int>(kp), E, nt_op(hwT, F, kp, kp),
-                             nt_op(gysT, de, kp, kp), gr.dW_down, de, static_cast<long long>(F) * de,
-                             poff),
+        CK(launch_nt_gemm(tn(NT_KSEG, F, de, kp, E, opnd(hwb, F, kp, F), opnd(gys, de, kp, de), gr.dW_down,
+                             de, static_cast<long long>(F) * de, poff),
                           s));
     if (gr.dW_gate)
-        CK(launch_nt_gemm(nt(NT_KSEG, de, F, static_cast<int>(kp), E, nt_op(zsT, de, kp, kp),
-                             nt_op(daT, F, kp, kp), gr.dW_gate, F, static_cast<long long>(de) * F,
-                             poff),
+        CK(launch_nt_gemm(tn(NT_KSEG, de, F, kp, E, opnd(zs, de, kp, de), opnd(dab, F, kp, F), gr.dW_gate, F,
+                             static_cast<long long>(de) * F, poff),
                           s));
     if (gr.dW_up)
-        CK(launch_nt_gemm(nt(NT_KSEG, de, F, static_cast<int>(kp), E, nt_op(zsT, de, kp, kp),
-                             nt_op(duT, F, kp, kp), gr.dW_up, F, static_cast<long long>(de) * F,
-                             poff),
+        CK(launch_nt_gemm(tn(NT_KSEG, de, F, kp, E, opnd(zs, de, kp, de), opnd(dub, F, kp, F), gr.dW_up, F,
+                             static_cast<long long>(de) * F, poff),
                           s));
 
     // ---- dx from the routed experts (latent: through dz and W_down_latent) ----
     if (!lat) {
-        CK(launch_gather_sum(dxs, inv, T, K, d, nullptr, gr.dx, 0, s));
+        CK(launch_gather_sum(dxsp, invp, T, K, d, nullptr, gr.dx, 0, s));
     } else {
         float* dz = BF(BL.dz);
-        __nv_bfloat16 *dzb = BH(BL.dzb), *dzT = BH(BL.dzT);
-        CK(launch_gather_sum(dxs, inv, T, K, lat, nullptr, dz, 0, s));
+        __nv_bfloat16* dzb = BH(BL.dzb);
+        CK(launch_gather_sum(dxsp, invp, T, K, lat, nullptr, dz, 0, s));
         CK(launch_gather_bf16(dz, 0, lat, nullptr, T, lat, dzb, s));
-        if (gr.dW_down_latent) {
-            // dW_down_latent = x^T dz
-            CK(launch_transpose_pad(dz, 0, lat, nullptr, T, lat, nullptr, nullptr, 0, static_cast<int>(tp), dzT, s));
-            CK(launch_nt_gemm(nt(NT_DENSE, d, lat, static_cast<int>(tp), 1, nt_op(xT, d, tp, tp),
-                                 nt_op(dzT, lat, tp, tp), gr.dW_down_latent, lat),
+        if (gr.dW_down_latent)  // dW_down_latent = x^T dz
+            CK(launch_nt_gemm(tn(NT_DENSE, d, lat, tp, 1, opnd(x, d, T, d), opnd(dzb, lat, T, lat),
+                                 gr.dW_down_latent, lat),
                               s));
-        }
         // dx = dz W_down_latent^T: W_down_latent [d, L] rows are K-major for this product
-        CK(launch_nt_gemm(nt(NT_DENSE, T, d, lat, 1, nt_op(dzb, T, lat, lat),
-                             nt_op(w.W_down_latent, d, lat, lat), gr.dx, d),
+        CK(launch_nt_gemm(nt(NT_DENSE, T, d, lat, 1, opnd(dzb, T, lat, lat),
+                             opnd(w.W_down_latent, d, lat, lat), gr.dx, d),
                           s));
     }
 
     // ---- shared experts: dx, weight gradients ----
     if (S) {
         for (int z = 0; z < S; ++z) {
-            NtGemm g = nt(NT_DENSE, T, d, Fs, 1, nt_op(dasb, T, SF, SF),
-                          nt_op(w.Ws_gate, d, Fs, Fs, S, static_cast<long long>(d) * Fs), gr.dx, d);
+            NtGemm g = nt(NT_DENSE, T, d, Fs, 1, opnd(dasb, T, SF, SF),
+                          opnd(w.Ws_gate, d, Fs, Fs, S, static_cast<long long>(d) * Fs), gr.dx, d);
             g.nph = 2;
-            g.A[1] = nt_op(dusb, T, SF, SF);
-            g.B[1] = nt_op(w.Ws_up, d, Fs, Fs, S, static_cast<long long>(d) * Fs);
+            g.A[1] = opnd(dusb, T, SF, SF);
+            g.B[1] = opnd(w.Ws_up, d, Fs, Fs, S, static_cast<long long>(d) * Fs);
             g.a_kofs[0] = g.a_kofs[1] = z * Fs;
             g.b_zc[0] = g.b_zc[1] = z;
             g.accumulate = 1;
             CK(launch_nt_gemm(g, s));
         }
-        if (gr.dWs_down) {
-            NtGemm g = nt(NT_DENSE, Fs, d, static_cast<int>(tp), S, nt_op(hsT, SF, tp, tp),
-                          nt_op(doutT, d, tp, tp), gr.dWs_down, d, static_cast<long long>(Fs) * d);
+        if (gr.dWs_down) {  // dWs_down[s] = hs_s^T dout
+            NtGemm g = tn(NT_DENSE, Fs, d, tp, S, opnd(hsb, SF, T, SF), opnd(doutb, d, T, d), gr.dWs_down, d,
+                          static_cast<long long>(Fs) * d);
             g.a_zrow = Fs;
             CK(launch_nt_gemm(g, s));
         }
-        for (int which = 0; which < 2; ++which) {
+        for (int which = 0; which < 2; ++which) {  // dWs_gate[s] = x^T das_s, dWs_up[s] = x^T dus_s
             float* C = which ? gr.dWs_up : gr.dWs_gate;
             if (!C) continue;
-            NtGemm g = nt(NT_DENSE, d, Fs, static_cast<int>(tp), S, nt_op(xT, d, tp, tp),
-                          nt_op(which ? dusT : dasT, SF, tp, tp), C, Fs, static_cast<long long>(d) * Fs);
+            NtGemm g = tn(NT_DENSE, d, Fs, tp, S, opnd(x, d, T, d), opnd(which ? dusb : dasb, SF, T, SF), C, Fs,
+                          static_cast<long long>(d) * Fs);
             g.b_zrow = Fs;
             CK(launch_nt_gemm(g, s));
         }
@@ -653,11 +638,9 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
                   static_cast<const float*>(dgpart), 2 * ((F + 127) / 128), inv, tidx, tw, scores, T, K, E,
                   c.gate, c.renormalize, c.routed_scale, dr, dg));
     if (gr.dW_router)
-        CK(run_splitk(gemm(GEN_DENSE, d, E, T, 1, op(x, 1, 1, d), 1, op(dr, 0, E, 1), 1,
-                           gr.dW_router, E),
+        CK(run_splitk(gemm(GEN_DENSE, d, E, T, 1, op(x, 1, 1, d), 1, op(dr, 0, E, 1), 1, gr.dW_router, E),
                       GEN_EPI_STORE, BF(BL.kpart), BL.kpart_floats, s));
-    CK(launch_gen_gemm(gemm(GEN_DENSE, T, d, E, 1, op(dr, 0, E, 1), 0, op(w.W_router, 0, 1, E), 0,
-                            gr.dx, d),
+    CK(launch_gen_gemm(gemm(GEN_DENSE, T, d, E, 1, op(dr, 0, E, 1), 0, op(w.W_router, 0, 1, E), 0, gr.dx, d),
                        GEN_EPI_ACCUM, s));
 #undef CK
     return MOE_OK;

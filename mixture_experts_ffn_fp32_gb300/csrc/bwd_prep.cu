@@ -1,9 +1,9 @@
-// Operand preparation for the tensor-core backward (gemm_nt.cu reads both
-// operands K-major): BF16 copies of gathered rows, transposed copies laid out
-// per expert with each expert's rows padded to a multiple of 64 columns
-// (zero columns between experts, so an expert's weight-gradient reduction
-// covers whole k-blocks of its own rows only). The SwiGLU backward itself
-// runs in the epilogue of the recomputing gate/up GEMM (gemm_tc.cu).
+// Operand preparation for the tensor-core backward: BF16 copies of rows, and
+// the expert-padded row layout (each expert's rows, then zero rows up to a
+// multiple of 64, so an expert's weight-gradient reduction covers whole
+// 64-row k-blocks of its own rows only): padded offsets, padded positions of
+// the assignments, rows gathered into it. The SwiGLU backward itself runs in
+// the epilogue of the recomputing gate/up GEMM (gemm_tc.cu).
 #include "common.cuh"
 #include "internal.h"
 
@@ -67,67 +67,45 @@ MOE_DEV long long pad_row(int j, int nrows, int kpad, const int32_t* poff, const
     return k < offsets[lo + 1] - offsets[lo] ? offsets[lo] + k : -1;
 }
 
-// 64 x 64 tiles through shared memory, 16-byte accesses on both sides:
-// 8 BF16 (or 4 FP32) consecutive source columns per load, 8 consecutive
-// destination columns per store. blockIdx.x: 64-block of j, blockIdx.y: of c.
-// cols is a multiple of 8.
-template <bool SRC_BF16>
-__global__ void __launch_bounds__(256) transpose_pad_kernel(
-    const void* __restrict__ src, long long ld, const int32_t* __restrict__ idx, int nrows, int cols,
-    const int32_t* __restrict__ poff, const int32_t* __restrict__ offsets, int E, int kpad,
-    __nv_bfloat16* __restrict__ dst) {
-    __shared__ float tile[64][65];
-    __shared__ long long srow[64];
+// Row gather into the expert-padded row layout: dst row j (of kpad) =
+// BF16(src[idx[pos(j)], :cols]) for the rows of the experts, zero for the
+// padding rows. One warp per row, 8 columns per lane step.
+__global__ void __launch_bounds__(256) gather_pad_bf16_kernel(
+    const void* __restrict__ src, int src_bf16, long long ld, const int32_t* __restrict__ idx,
+    int nrows, int cols, const int32_t* __restrict__ poff, const int32_t* __restrict__ offsets, int E,
+    int kpad, __nv_bfloat16* __restrict__ dst) {
     pdl_wait();
     pdl_trigger();
-    const int j0 = blockIdx.x * 64, c0 = blockIdx.y * 64;
-    if (threadIdx.x < 64) {
-        const long long r = pad_row(j0 + threadIdx.x, nrows, kpad, poff, offsets, E);
-        srow[threadIdx.x] = r < 0 ? -1 : (idx ? idx[r] : r);
-    }
-    __syncthreads();
-    if (SRC_BF16) {
-        // 64 rows x 8 chunks of 8 BF16: two chunks per thread
-        for (int i = threadIdx.x; i < 64 * 8; i += 256) {
-            const int jj = i >> 3, ch = i & 7;
-            const int c = c0 + ch * 8;
-            float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (srow[jj] >= 0 && c < cols) {
-                const uint4 q = *reinterpret_cast<const uint4*>(
-                    static_cast<const __nv_bfloat16*>(src) + srow[jj] * ld + c);
-                v[0] = bf16_lo(q.x); v[1] = bf16_hi(q.x); v[2] = bf16_lo(q.y); v[3] = bf16_hi(q.y);
-                v[4] = bf16_lo(q.z); v[5] = bf16_hi(q.z); v[6] = bf16_lo(q.w); v[7] = bf16_hi(q.w);
-            }
+    const int j = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (j >= kpad) return;
+    const int lane = threadIdx.x & 31;
+    const long long r = pad_row(j, nrows, kpad, poff, offsets, E);
+    const long long sr = r < 0 ? -1 : (idx ? idx[r] : r);
+    for (int c = lane * 8; c < cols; c += 256) {
+        uint32_t pk[4] = {0u, 0u, 0u, 0u};
+        if (sr >= 0) {
 #pragma unroll
-            for (int t = 0; t < 8; ++t) tile[jj][ch * 8 + t] = v[t];
+            for (int i = 0; i < 4; ++i)
+                pk[i] = pack_bf16x2(ld_any(src, src_bf16, sr * ld + c + 2 * i),
+                                    ld_any(src, src_bf16, sr * ld + c + 2 * i + 1));
         }
-    } else {
-        // 64 rows x 16 chunks of 4 FP32: four chunks per thread
-        for (int i = threadIdx.x; i < 64 * 16; i += 256) {
-            const int jj = i >> 4, ch = i & 15;
-            const int c = c0 + ch * 4;
-            float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (srow[jj] >= 0 && c < cols)
-                q = *reinterpret_cast<const float4*>(static_cast<const float*>(src) + srow[jj] * ld + c);
-            tile[jj][ch * 4] = q.x;
-            tile[jj][ch * 4 + 1] = q.y;
-            tile[jj][ch * 4 + 2] = q.z;
-            tile[jj][ch * 4 + 3] = q.w;
-        }
-    }
-    __syncthreads();
-    // 64 destination rows (c) x 8 chunks of 8 BF16 (j)
-    for (int i = threadIdx.x; i < 64 * 8; i += 256) {
-        const int cc = i >> 3, ch = i & 7;
-        const int c = c0 + cc, j = j0 + ch * 8;
-        if (c >= cols || j >= kpad) continue;
-        uint32_t pk[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-            pk[t] = pack_bf16x2(tile[ch * 8 + 2 * t][cc], tile[ch * 8 + 2 * t + 1][cc]);
-        *reinterpret_cast<uint4*>(dst + static_cast<long long>(c) * kpad + j) =
+        *reinterpret_cast<uint4*>(dst + static_cast<long long>(j) * cols + c) =
             make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
+}
+
+// Padded position of every assignment: inv_pad = poff[e] + inv - offsets[e].
+__global__ void __launch_bounds__(256) pad_inverse_kernel(const int32_t* __restrict__ inv,
+                                                          const int32_t* __restrict__ idx, int TK,
+                                                          const int32_t* __restrict__ poff,
+                                                          const int32_t* __restrict__ offsets,
+                                                          int32_t* __restrict__ inv_pad) {
+    pdl_wait();
+    pdl_trigger();
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= TK) return;
+    const int e = idx[i];
+    inv_pad[i] = poff[e] + inv[i] - offsets[e];
 }
 
 }  // namespace
@@ -143,16 +121,18 @@ cudaError_t launch_gather_bf16(const void* src, int src_bf16, long long ld, cons
                       src_bf16, ld, idx, rows, cols, dst);
 }
 
-cudaError_t launch_transpose_pad(const void* src, int src_bf16, long long ld, const int32_t* idx,
-                                 int nrows, int cols, const int32_t* poff, const int32_t* offsets,
-                                 int E, int kpad, __nv_bfloat16* dst, cudaStream_t s) {
-    if (cols % 8 || kpad % 8 || ld % 8) return cudaErrorInvalidValue;
-    const dim3 grid((kpad + 63) / 64, (cols + 63) / 64);
-    if (src_bf16)
-        return launch_pdl(transpose_pad_kernel<true>, grid, dim3(256), 0, s, src, ld, idx, nrows, cols,
-                          poff, offsets, E, kpad, dst);
-    return launch_pdl(transpose_pad_kernel<false>, grid, dim3(256), 0, s, src, ld, idx, nrows, cols,
-                      poff, offsets, E, kpad, dst);
+cudaError_t launch_gather_pad_bf16(const void* src, int src_bf16, long long ld, const int32_t* idx,
+                                   int nrows, int cols, const int32_t* poff, const int32_t* offsets,
+                                   int E, int kpad, __nv_bfloat16* dst, cudaStream_t s) {
+    if (cols % 8) return cudaErrorInvalidValue;
+    return launch_pdl(gather_pad_bf16_kernel, dim3((kpad * 32 + 255) / 256), dim3(256), 0, s, src,
+                      src_bf16, ld, idx, nrows, cols, poff, offsets, E, kpad, dst);
+}
+
+cudaError_t launch_pad_inverse(const int32_t* inv, const int32_t* idx, int TK, const int32_t* poff,
+                               const int32_t* offsets, int32_t* inv_pad, cudaStream_t s) {
+    return launch_pdl(pad_inverse_kernel, dim3((TK + 255) / 256), dim3(256), 0, s, inv, idx, TK, poff,
+                      offsets, inv_pad);
 }
 
 }  // namespace moe

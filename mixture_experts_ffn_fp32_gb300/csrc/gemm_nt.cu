@@ -19,6 +19,9 @@
 //              by z a_zrow, z b_zrow, z b_z3; C by z c_zs
 // A unit accumulates one or two phases (e.g. da W_gate^T then du W_up^T),
 // each with its own pair of tensor maps and coordinate offsets.
+// Either operand may instead be stored MN-major (K rows of its M or N
+// columns, a_mn / b_mn): the weight gradients then read the row-major
+// activations as they are, C = A^T B over the rows (no transposed copies).
 //
 // Tile 128 x BN (BN = 256 when N >= 256, else 128), K step 64 (a 128-byte
 // swizzle row), a 192 KB ring of TMA stages (4 of 48 KB, or 6 of 32 KB), two
@@ -64,6 +67,7 @@ struct NtParams {
     int a_kofs[2], b_zc[2];
     int mode, M, N, Z, kblocks;
     int a_zrow, b_zrow, b_z3;
+    int a_mn, b_mn;  // operand stored MN-major: K rows of its M (N) columns
     const int32_t* offsets;
     float* C;
     long long ldc, c_zs;
@@ -211,8 +215,14 @@ __global__ void __launch_bounds__(NT_THREADS, 1) nt_gemm_kernel(const __grid_con
                         }
                         const uint32_t sA = sbase + stage * NT_STAGE_BYTES;
                         mbar_expect_tx(full_bar(stage), NT_STAGE_BYTES);
-                        tma_load_2d(sA, &p.mapA[ph], kb * NBK + p.a_kofs[ph], t.arow, full_bar(stage));
-                        tma_load_3d(sA + NT_A_BYTES, &p.mapB[ph], kb * NBK, brow, bz, full_bar(stage));
+                        if (p.a_mn)  // two 64-column strips of 64 k rows
+                            tma_load_3d(sA, &p.mapA[ph], 0, kb * NBK + p.a_kofs[ph], t.arow / 64, full_bar(stage));
+                        else
+                            tma_load_2d(sA, &p.mapA[ph], kb * NBK + p.a_kofs[ph], t.arow, full_bar(stage));
+                        if (p.b_mn)  // NBN / 64 strips
+                            tma_load_3d(sA + NT_A_BYTES, &p.mapB[ph], 0, kb * NBK, brow / 64, full_bar(stage));
+                        else
+                            tma_load_3d(sA + NT_A_BYTES, &p.mapB[ph], kb * NBK, brow, bz, full_bar(stage));
                         issued |= 1u << stage;
                         last_par = (last_par & ~(1u << stage)) | (phase << stage);
                         if (++stage == NT_STAGES) {
@@ -231,8 +241,12 @@ __global__ void __launch_bounds__(NT_THREADS, 1) nt_gemm_kernel(const __grid_con
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            const uint64_t adesc0 = smem_desc_sw128(sbase, 16, 1024);
-            const uint64_t bdesc0 = smem_desc_sw128(sbase + NT_A_BYTES, 16, 1024);
+            // K-major tiles: rows of 64 k (lbo unused), a 16-deep k-step is 32 bytes;
+            // MN-major tiles: 8 KB strips of 64 columns x 64 k rows (lbo = the strip
+            // pitch), a 16-deep k-step is 16 rows = 2048 bytes
+            const uint64_t adesc0 = smem_desc_sw128(sbase, p.a_mn ? 8192 : 16, 1024);
+            const uint64_t bdesc0 = smem_desc_sw128(sbase + NT_A_BYTES, p.b_mn ? 8192 : 16, 1024);
+            const uint32_t a_ks = p.a_mn ? 128 : 2, b_ks = p.b_mn ? 128 : 2;  // 16-byte units
             for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
                 const NtUnit t = nt_unit<NBN>(u, p, nt, mt, s_tp, s_off);
                 if (t.skip) continue;
@@ -250,7 +264,8 @@ __global__ void __launch_bounds__(NT_THREADS, 1) nt_gemm_kernel(const __grid_con
 #pragma unroll
                     for (int ks = 0; ks < NBK / 16; ++ks) {
                         const uint32_t accum = (i != 0 || ks != 0) ? 1u : 0u;
-                        tc_mma_bf16(d_tmem, adesc0 + soff + ks * 2, bdesc0 + soff + ks * 2, p.idesc, accum);
+                        tc_mma_bf16(d_tmem, adesc0 + soff + ks * a_ks, bdesc0 + soff + ks * b_ks, p.idesc,
+                                    accum);
                     }
                     tc_commit(empty_bar(stage));
                     if (++stage == NT_STAGES) {
@@ -336,6 +351,16 @@ __global__ void __launch_bounds__(NT_THREADS, 1) nt_gemm_kernel(const __grid_con
     }
 }
 
+// MN-major operand: K rows of `cols` columns (pitch ld), seen as
+// [cols/64 strips, K, 64]; a box is `strips` strips of 64 k rows (8 KB each),
+// the layout the MMA reads as an MN-major tile.
+bool make_nt_strips(CUtensorMap* m, const void* X, long long cols, long long K, long long ld, int strips) {
+    const uint64_t dims[3] = {64, static_cast<uint64_t>(K), static_cast<uint64_t>(cols / 64)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(ld) * 2, 128};
+    const uint32_t box[3] = {64, NBK, static_cast<uint32_t>(strips)};
+    return encode_tmap(m, X, 3, dims, strides, box);
+}
+
 // A: rows x K_total, row pitch lda elements (K-major), box 64 x 128 rows
 bool make_nt_A(CUtensorMap* m, const void* A, long long rows, long long K, long long lda) {
     const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rows)};
@@ -372,8 +397,11 @@ cudaError_t launch_nt_t(const NtGemm& g, cudaStream_t s) {
     for (int ph = 0; ph < g.nph; ++ph) {
         const NtOperand& a = g.A[ph];
         const NtOperand& b = g.B[ph];
-        if (!make_nt_A(&p.mapA[ph], a.p, a.rows, a.K, a.ld)) return cudaErrorInvalidValue;
-        if (!make_nt_B(&p.mapB[ph], b.p, b.Z > 0 ? b.Z : 1, b.rows, b.K, b.ld, b.zstride, NBN))
+        if (g.a_mn ? !make_nt_strips(&p.mapA[ph], a.p, a.rows, a.K, a.ld, NBM / 64)
+                   : !make_nt_A(&p.mapA[ph], a.p, a.rows, a.K, a.ld))
+            return cudaErrorInvalidValue;
+        if (g.b_mn ? !make_nt_strips(&p.mapB[ph], b.p, b.rows, b.K, b.ld, NBN / 64)
+                   : !make_nt_B(&p.mapB[ph], b.p, b.Z > 0 ? b.Z : 1, b.rows, b.K, b.ld, b.zstride, NBN))
             return cudaErrorInvalidValue;
         p.a_kofs[ph] = g.a_kofs[ph];
         p.b_zc[ph] = g.b_zc[ph];
@@ -387,12 +415,14 @@ cudaError_t launch_nt_t(const NtGemm& g, cudaStream_t s) {
     p.a_zrow = g.a_zrow;
     p.b_zrow = g.b_zrow;
     p.b_z3 = g.b_z3;
+    p.a_mn = g.a_mn;
+    p.b_mn = g.b_mn;
     p.offsets = g.offsets;
     p.C = g.C;
     p.ldc = g.ldc;
     p.c_zs = g.c_zs;
     p.accumulate = g.accumulate;
-    p.idesc = idesc_bf16_f32(NBM, NBN, /*b_mn_major=*/0);
+    p.idesc = idesc_bf16_f32(NBM, NBN, g.b_mn ? 1 : 0) | (g.a_mn ? (1u << 15) : 0u);  // bit 15: A MN-major
     p.err = g.err;
     p.timeout_ns = wait_timeout_ns();
     const long long nt = (g.N + NBN - 1) / NBN;
@@ -414,6 +444,14 @@ cudaError_t launch_nt_gemm(const NtGemm& g, cudaStream_t s) {
     if (g.nph < 1 || g.nph > 2 || g.Z < 1 || (g.mode != NT_DENSE && g.Z > MAXSEG))
         return cudaErrorInvalidValue;
     if (g.N % 16 || g.K % NBK) return cudaErrorInvalidValue;
+    // MN-major operands: whole 64-column strips, no row segments, no B slices
+    for (int ph = 0; ph < g.nph; ++ph) {
+        if (g.a_mn && (g.mode == NT_MSEG || g.A[ph].rows % 64 || g.A[ph].ld % 8 || g.a_zrow % 64))
+            return cudaErrorInvalidValue;
+        if (g.b_mn && (g.B[ph].rows % 64 || g.B[ph].ld % 8 || g.b_zrow % 64 || g.b_z3 || g.b_zc[ph] ||
+                       g.mode == NT_MSEG))
+            return cudaErrorInvalidValue;
+    }
     // 128 x 256 tiles halve the A re-reads, but only while they still give
     // every SM a unit, and (grouped by expert) while the segments average 256
     // rows or more: short segments stream weights or store FP32 gradients,

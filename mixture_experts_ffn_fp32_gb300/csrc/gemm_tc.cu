@@ -102,10 +102,7 @@ struct TcParams {
     int dh_ld[2];
     __nv_bfloat16* da[2];
     __nv_bfloat16* du[2];
-    __nv_bfloat16* daT[2];
-    __nv_bfloat16* duT[2];
-    __nv_bfloat16* hwT[2];
-    long long kpad[2];
+    __nv_bfloat16* hw[2];
     float* dgpart;
     const int32_t* poff;
     int* err;
@@ -476,21 +473,26 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
             char* out_rows = static_cast<char*>(p.out[t.g]) +
                              static_cast<size_t>(my_out0 + q * 32) * pitch;
             if (MODE == TC_SWIGLU_BWD) {
-                // padded column of this lane's row: the row's own, or a padding
-                // column of the segment (zeroed), or none
-                long long jrow = -1;
+                // Output rows of this warp: group 0 in the expert-padded row layout
+                // (the segment's rows, then its padding rows, written as zeros),
+                // group 1 the token rows. dh is read in the same layout.
+                long long rbase;
+                int nrow;
                 if (t.g == 0) {
-                    const long long jj = p.poff[t.zb] + (static_cast<long long>(orow) - s_off[t.zb]);
-                    if (jj < p.poff[t.zb + 1]) jrow = jj;
-                } else if (static_cast<long long>(orow) < p.kpad[1]) {
-                    jrow = static_cast<long long>(orow);
+                    rbase = p.poff[t.zb] + (static_cast<long long>(my_out0 + q * 32) - s_off[t.zb]);
+                    const long long left = p.poff[t.zb + 1] - rbase;
+                    nrow = left < 32 ? static_cast<int>(left) : 32;
+                } else {
+                    rbase = my_out0 + q * 32;
+                    nrow = valid_rows;
                 }
                 const bool row_valid = lane < valid_rows;
+                const long long drow = rbase + lane;
                 const float g = (t.g == 0 && p.rowscale0 != nullptr && row_valid) ? p.rowscale0[orow] : 1.0f;
                 const size_t bpitch = static_cast<size_t>(ld) * 2;
-                char* da_rows = reinterpret_cast<char*>(p.da[t.g]) + static_cast<size_t>(my_out0 + q * 32) * bpitch;
-                char* du_rows = reinterpret_cast<char*>(p.du[t.g]) + static_cast<size_t>(my_out0 + q * 32) * bpitch;
-                const long long kp = p.kpad[t.g];
+                char* da_rows = reinterpret_cast<char*>(p.da[t.g]) + static_cast<size_t>(rbase) * bpitch;
+                char* du_rows = reinterpret_cast<char*>(p.du[t.g]) + static_cast<size_t>(rbase) * bpitch;
+                char* hw_rows = reinterpret_cast<char*>(p.hw[t.g]) + static_cast<size_t>(rbase) * bpitch;
                 float part = 0.0f;
 #pragma unroll 1
                 for (int c = half * 64; c < half * 64 + 64; c += 32) {
@@ -508,7 +510,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
                             float4 d4 = make_float4(0.f, 0.f, 0.f, 0.f);
                             if (row_valid && i < lim)
                                 d4 = *reinterpret_cast<const float4*>(
-                                    p.dh[t.g] + orow * static_cast<size_t>(p.dh_ld[t.g]) + t.out_col0 + c + hc + i);
+                                    p.dh[t.g] + drow * p.dh_ld[t.g] + t.out_col0 + c + hc + i);
                             dh[i] = d4.x;
                             dh[i + 1] = d4.y;
                             dh[i + 2] = d4.z;
@@ -523,7 +525,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
                                 const float sg = 1.0f / (1.0f + expf(-a));
                                 const float si = a * sg;
                                 const float h = si * uu;
-                                const float dv = row_valid ? dh[i + e] : 0.0f;
+                                const float dv = dh[i + e];
                                 o_da[e] = row_valid ? g * dv * uu * (sg * (1.0f + a * (1.0f - sg))) : 0.0f;
                                 o_du[e] = row_valid ? g * dv * si : 0.0f;
                                 o_hw[e] = row_valid ? g * h : 0.0f;
@@ -534,33 +536,18 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
                             phw[(hc + i) / 2] = pack_bf16x2(o_hw[0], o_hw[1]);
                         }
                     }
-                    // row-major da, du: 32 BF16 of each row through the staging buffer
+                    // 32 BF16 of each row through the staging buffer, padding rows included
                     const int vch = (N - (t.n0 + c)) / 8;
+                    const size_t col = static_cast<size_t>(t.out_col0 + c) * 2;
                     const uint4 va[4] = {make_uint4(pda[0], pda[1], pda[2], pda[3]), make_uint4(pda[4], pda[5], pda[6], pda[7]),
                                          make_uint4(pda[8], pda[9], pda[10], pda[11]), make_uint4(pda[12], pda[13], pda[14], pda[15])};
-                    warp_store_block(stg, va, lane, da_rows + static_cast<size_t>(t.out_col0 + c) * 2, bpitch,
-                                     valid_rows, vch);
+                    warp_store_block(stg, va, lane, da_rows + col, bpitch, nrow, vch);
                     const uint4 vu[4] = {make_uint4(pdu[0], pdu[1], pdu[2], pdu[3]), make_uint4(pdu[4], pdu[5], pdu[6], pdu[7]),
                                          make_uint4(pdu[8], pdu[9], pdu[10], pdu[11]), make_uint4(pdu[12], pdu[13], pdu[14], pdu[15])};
-                    warp_store_block(stg, vu, lane, du_rows + static_cast<size_t>(t.out_col0 + c) * 2, bpitch,
-                                     valid_rows, vch);
-                    // transposed: column f of the hidden layout, padded column jrow; the
-                    // lanes' consecutive rows make each store 64 contiguous bytes
-                    if (jrow >= 0) {
-                        uint16_t* dT = reinterpret_cast<uint16_t*>(p.daT[t.g]);
-                        uint16_t* uT = reinterpret_cast<uint16_t*>(p.duT[t.g]);
-                        uint16_t* hT = reinterpret_cast<uint16_t*>(p.hwT[t.g]);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            if (t.n0 + c + i < N) {
-                                const long long o = static_cast<long long>(t.out_col0 + c + i) * kp + jrow;
-                                const int sh = (i & 1) * 16;
-                                dT[o] = static_cast<uint16_t>(pda[i / 2] >> sh);
-                                uT[o] = static_cast<uint16_t>(pdu[i / 2] >> sh);
-                                hT[o] = static_cast<uint16_t>(phw[i / 2] >> sh);
-                            }
-                        }
-                    }
+                    warp_store_block(stg, vu, lane, du_rows + col, bpitch, nrow, vch);
+                    const uint4 vh[4] = {make_uint4(phw[0], phw[1], phw[2], phw[3]), make_uint4(phw[4], phw[5], phw[6], phw[7]),
+                                         make_uint4(phw[8], phw[9], phw[10], phw[11]), make_uint4(phw[12], phw[13], phw[14], phw[15])};
+                    warp_store_block(stg, vh, lane, hw_rows + col, bpitch, nrow, vch);
                 }
                 if (t.g == 0 && p.dgpart != nullptr && row_valid)
                     p.dgpart[orow * static_cast<size_t>(2 * p.nt[0]) + 2 * (t.n0 / 128) + half] = part;
@@ -806,12 +793,8 @@ cudaError_t launch_tc_t(const TcGemmArgs& a, int nstrip, int slots, cudaStream_t
         p.dh_ld[g] = G.dh_ld;
         p.da[g] = static_cast<__nv_bfloat16*>(G.da);
         p.du[g] = static_cast<__nv_bfloat16*>(G.du);
-        p.daT[g] = static_cast<__nv_bfloat16*>(G.daT);
-        p.duT[g] = static_cast<__nv_bfloat16*>(G.duT);
-        p.hwT[g] = static_cast<__nv_bfloat16*>(G.hwT);
-        p.kpad[g] = G.kpad;
-        if (MODE == TC_SWIGLU_BWD && (!G.dh || !G.da || !G.du || !G.daT || !G.duT || !G.hwT ||
-                                      G.kpad <= 0 || G.dh_ld % 4))
+        p.hw[g] = static_cast<__nv_bfloat16*>(G.hw);
+        if (MODE == TC_SWIGLU_BWD && (!G.dh || !G.da || !G.du || !G.hw || G.dh_ld % 4))
             return cudaErrorInvalidValue;
         if (g == 0)
             units_bound += static_cast<long long>((G.rows + UROWS - 1) / UROWS + a.E) * p.nt[0];

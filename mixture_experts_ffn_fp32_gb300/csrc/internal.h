@@ -181,20 +181,17 @@ struct TcGroup {
                         // product to out rows [s*rows, (s+1)*rows) (needs Z == 1)
     // TC_SWIGLU_BWD: with a, u the gate and up products of row r, column c (the
     // SwiGLU layout of `out`, pitch out_ld), the upstream gradient dh of h
-    // (FP32, same layout, pitch dh_ld) and the row's gate weight g (group 0:
-    // rowscale0, group 1: 1): da = g dh u SiLU'(a), du = g dh SiLU(a) as BF16
-    // in da / du (pitch out_ld), and da, du, g h transposed as BF16 [cols, kpad]
-    // at column j(r) of the padded layout (group 0: poff / offsets; group 1:
-    // j = r), the padding columns zeroed; group 0 also dgpart[r, 2 tile + half]
-    // = sum of dh h over each 64 of the tile's columns.
+    // (FP32, pitch dh_ld) and the row's gate weight g (group 0: rowscale0,
+    // group 1: 1): da = g dh u SiLU'(a), du = g dh SiLU(a) and g h as BF16
+    // rows of da / du / hw (pitch out_ld). Group 0 reads dh and writes in the
+    // expert-padded row layout (TcGemmArgs::poff; padding rows zeroed), group 1
+    // in token rows; group 0 also dgpart[r, 2 tile + half] = sum of dh h over
+    // each 64 of the tile's columns (r the unpadded row).
     const float* dh = nullptr;
     int dh_ld = 0;
     void* da = nullptr;
     void* du = nullptr;
-    void* daT = nullptr;
-    void* duT = nullptr;
-    void* hwT = nullptr;
-    long long kpad = 0;
+    void* hw = nullptr;
     float* dgpart = nullptr;
 };
 
@@ -305,6 +302,8 @@ struct NtGemm {
     NtOperand A[2], B[2];
     int a_kofs[2], b_zc[2];     // per phase: A column offset, B slice offset
     int a_zrow, b_zrow, b_z3;   // NT_DENSE: per-problem A row, B row and B slice steps
+    int a_mn = 0, b_mn = 0;     // operand stored MN-major: K rows of its rows-many columns
+                                // (pitch ld; rows a multiple of 64; not with NT_MSEG)
     const int32_t* offsets;     // [Z+1] device: NT_MSEG rows / NT_KSEG reduction columns
     float* C;
     long long ldc, c_zs;
@@ -319,22 +318,25 @@ cudaError_t launch_pad_offsets(const int32_t* offsets, int E, int32_t* poff, cud
 // dst[r, :cols] = BF16(src[idx ? idx[r] : r, :cols]) for r < rows; src FP32 or BF16.
 cudaError_t launch_gather_bf16(const void* src, int src_bf16, long long ld, const int32_t* idx,
                                int rows, int cols, __nv_bfloat16* dst, cudaStream_t s);
-// Transposed, padded copy: dst[c, j] (pitch kpad) = BF16(src[row(j), c]) for
-// c < cols, j < kpad, with row(j) = j (j < nrows) when poff is null, else the
-// j-th padded column of the expert layout (poff/offsets: segment z's columns
-// poff[z] .. poff[z] + cnt_z map to rows offsets[z] ..), zero elsewhere;
-// src rows read through idx when given.
-cudaError_t launch_transpose_pad(const void* src, int src_bf16, long long ld, const int32_t* idx,
-                                 int nrows, int cols, const int32_t* poff, const int32_t* offsets,
-                                 int E, int kpad, __nv_bfloat16* dst, cudaStream_t s);
+// Rows gathered into the expert-padded row layout: dst [kpad, cols] BF16,
+// row j = poff[z] + i holds src row idx[offsets[z] + i] for i < cnt_z (the
+// rows of segment z), zero rows up to poff[z + 1]; without poff, row j = j
+// for j < nrows.
+cudaError_t launch_gather_pad_bf16(const void* src, int src_bf16, long long ld, const int32_t* idx,
+                                   int nrows, int cols, const int32_t* poff, const int32_t* offsets,
+                                   int E, int kpad, __nv_bfloat16* dst, cudaStream_t s);
+// inv_pad[i] = poff[idx[i]] + inv[i] - offsets[idx[i]] for i < TK.
+cudaError_t launch_pad_inverse(const int32_t* inv, const int32_t* idx, int TK, const int32_t* poff,
+                               const int32_t* offsets, int32_t* inv_pad, cudaStream_t s);
+
 // Backward scratch (FP32 arrays, byte offsets into the backward workspace).
 struct BwdLayout {
     int tc;  // the tensor-core form (bwd_on_tensor_cores)
     size_t dhp, da, du, hw, dwpart, dxs, dhs, das, dus, hs, dr, dg, glat, routed, dz;
-    // tensor-core form only: BF16 operand copies, recomputed products, padding
-    size_t poff, gys, gysT, zsT, dab, dub, daT, duT, hwT, dwrow;
-    size_t doutb, doutT, xT, dasb, dusb, dasT, dusT, hsT;
-    size_t routedT, dzT, dzb;  // latent projections' BF16 operands
+    // tensor-core form only, in the expert-padded row layout where routed: BF16
+    // operand copies, the SwiGLU backward's outputs, padded positions
+    size_t poff, invp, gys, zs, dab, dub, hwb, dwrow, dxsp;
+    size_t doutb, dasb, dusb, hsb, routedb, dzb;
     long long tkpad, tpad;
     size_t kpart, kpart_floats;  // split-K partials of the long-reduction CUDA-core products
     size_t total;
