@@ -44,7 +44,11 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(const float* __restrict
                                                          const float* __restrict__ scores, int T,
                                                          int K, int E, int gate, int renorm,
                                                          float scale, float* __restrict__ dr,
-                                                         float* __restrict__ dg_out) {
+                                                         float* __restrict__ dg_out,
+                                                         float* __restrict__ cp,
+                                                         const int32_t* __restrict__ invp,
+                                                         const float* __restrict__ WrT, int d,
+                                                         float* __restrict__ dx) {
     pdl_wait();
     pdl_trigger();
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -86,6 +90,72 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(const float* __restrict
     for (int e = lane; e < E; e += 32) row[e] = 0.0f;
     __syncwarp();
     if (lane < K) row[ek] = drk;
+    // the router's coefficient of each assignment at its expert-padded row
+    if (cp != nullptr && lane < K) cp[invp[static_cast<size_t>(t) * K + lane]] = drk;
+    // dx[t, :] += sum_k dr_k W_router[:, e_k] (slot order), from W_router^T rows
+    if (WrT != nullptr) {
+        float* xr = dx + static_cast<size_t>(t) * d;
+        for (int j = lane; j < d; j += 32) {
+            float acc = 0.0f;
+            for (int k = 0; k < K; ++k) {
+                const float dk = __shfl_sync(0xffffffffu, drk, k);
+                const int e = __shfl_sync(0xffffffffu, ek, k);
+                acc = fmaf(dk, WrT[static_cast<size_t>(e) * d + j], acc);
+            }
+            xr[j] += acc;
+        }
+    }
+}
+
+// Partial router weight gradients over 64 expert-padded rows (all of one
+// expert): part[chunk, j] = sum over the chunk's rows k (in order) of
+// rows[k, j] cp[k]; cp is zero on padding rows.
+__global__ void __launch_bounds__(256) router_wgrad_part_kernel(const __nv_bfloat16* __restrict__ rows,
+                                                                const float* __restrict__ cp, int d,
+                                                                float* __restrict__ part) {
+    pdl_wait();
+    pdl_trigger();
+    const int j = blockIdx.y * 256 + threadIdx.x;
+    const int k0 = blockIdx.x * 64;
+    __shared__ float c[64];
+    if (threadIdx.x < 64) c[threadIdx.x] = cp[k0 + threadIdx.x];
+    __syncthreads();
+    if (j >= d) return;
+    float acc = 0.0f;
+#pragma unroll 8
+    for (int k = 0; k < 64; ++k)
+        acc = fmaf(__bfloat162float(rows[static_cast<size_t>(k0 + k) * d + j]), c[k], acc);
+    part[static_cast<size_t>(blockIdx.x) * d + j] = acc;
+}
+
+// dW_router[j, e] = sum over expert e's chunks (in order) of part[chunk, j].
+__global__ void __launch_bounds__(256) router_wgrad_reduce_kernel(const float* __restrict__ part,
+                                                                  const int32_t* __restrict__ poff,
+                                                                  int d, int E,
+                                                                  float* __restrict__ dW) {
+    pdl_wait();
+    pdl_trigger();
+    const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= static_cast<long long>(d) * E) return;
+    const int j = static_cast<int>(i / E), e = static_cast<int>(i - static_cast<long long>(j) * E);
+    float v = 0.0f;
+    for (int ch = poff[e] / 64; ch < poff[e + 1] / 64; ++ch) v += part[static_cast<size_t>(ch) * d + j];
+    dW[i] = v;
+}
+
+// out [cols, rows] = in [rows, cols]^T, FP32, 32 x 32 tiles.
+__global__ void __launch_bounds__(256) transpose_f32_kernel(const float* __restrict__ in, int rows,
+                                                            int cols, float* __restrict__ out) {
+    __shared__ float tile[32][33];
+    pdl_wait();
+    pdl_trigger();
+    const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    for (int r = ty; r < 32; r += 8)
+        if (r0 + r < rows && c0 + tx < cols) tile[r][tx] = in[static_cast<size_t>(r0 + r) * cols + c0 + tx];
+    __syncthreads();
+    for (int c = ty; c < 32; c += 8)
+        if (c0 + c < cols && r0 + tx < rows) out[static_cast<size_t>(c0 + c) * rows + r0 + tx] = tile[tx][c];
 }
 
 GenOp op(const void* p, int bf16, long long s0, long long s1, long long zs = 0,
@@ -194,6 +264,9 @@ BwdLayout plan_backward(const moe_config& c) {
         B.hwb = take(kp * F * 2);
         B.dwrow = take(TK * 2 * ((F + 127) / 128) * 4);  // per-row partials of dg, one per 64 columns
         B.dxsp = take(kp * de * 4);
+        B.wrt = take(static_cast<size_t>(c.d) * E * 4);
+        B.cp = take(kp * 4);
+        B.rpart = take(kp / 64 * c.d * 4);
         if (SF || L) B.doutb = take(T * c.d * 2);
         if (L) {
             B.routedb = take(T * L * 2);
@@ -379,7 +452,8 @@ moe_status backward_impl(const moe_config& c, const void* x, const moe_weights& 
     // router: dg -> dr -> dW_router and dx
     if ((e = launch_pdl(router_bwd_kernel, dim3((T * 32 + 255) / 256), dim3(256), 0, s, dwpart, ntf,
                         inv, tidx, tw, scores, T, K, E, c.gate, c.renormalize, c.routed_scale, dr,
-                        dg)) != cudaSuccess)
+                        dg, static_cast<float*>(nullptr), static_cast<const int32_t*>(nullptr),
+                        static_cast<const float*>(nullptr), 0, static_cast<float*>(nullptr))) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (gr.dW_router &&
         (e = run_splitk(gemm(GEN_DENSE, d, E, T, 1, op(x, bf, 1, d), 1, op(dr, 0, E, 1), 1,
@@ -633,15 +707,31 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
         }
     }
 
-    // ---- router: dg -> dr -> dW_router and dx ----
+    // ---- router: dg -> dr; dx += dr W_router^T (K nonzeros per token, read
+    //      from W_router^T rows); dW_router over each expert's padded rows of
+    //      x (the latent variant: a split-K product over the tokens) ----
+    float* wrt = BF(BL.wrt);
+    float* cp = lat ? nullptr : BF(BL.cp);
+    if (cp != nullptr) CK(cudaMemsetAsync(cp, 0, static_cast<size_t>(kp) * sizeof(float), s));
+    CK(launch_pdl(transpose_f32_kernel, dim3((E + 31) / 32, (d + 31) / 32), dim3(256), 0, s,
+                  static_cast<const float*>(w.W_router), d, E, wrt));
     CK(launch_pdl(router_bwd_kernel, dim3((T * 32 + 255) / 256), dim3(256), 0, s,
                   static_cast<const float*>(dgpart), 2 * ((F + 127) / 128), inv, tidx, tw, scores, T, K, E,
-                  c.gate, c.renormalize, c.routed_scale, dr, dg));
-    if (gr.dW_router)
-        CK(run_splitk(gemm(GEN_DENSE, d, E, T, 1, op(x, 1, 1, d), 1, op(dr, 0, E, 1), 1, gr.dW_router, E),
-                      GEN_EPI_STORE, BF(BL.kpart), BL.kpart_floats, s));
-    CK(launch_gen_gemm(gemm(GEN_DENSE, T, d, E, 1, op(dr, 0, E, 1), 0, op(w.W_router, 0, 1, E), 0, gr.dx, d),
-                       GEN_EPI_ACCUM, s));
+                  c.gate, c.renormalize, c.routed_scale, dr, dg, cp, static_cast<const int32_t*>(invp),
+                  static_cast<const float*>(wrt), d, gr.dx));
+    if (gr.dW_router) {
+        if (!lat) {
+            float* rp = BF(BL.rpart);
+            CK(launch_pdl(router_wgrad_part_kernel, dim3(kp / 64, (d + 255) / 256), dim3(256), 0, s,
+                          static_cast<const __nv_bfloat16*>(zs), static_cast<const float*>(cp), d, rp));
+            CK(launch_pdl(router_wgrad_reduce_kernel, dim3((d * E + 255) / 256), dim3(256), 0, s,
+                          static_cast<const float*>(rp), static_cast<const int32_t*>(poff), d, E,
+                          gr.dW_router));
+        } else {
+            CK(run_splitk(gemm(GEN_DENSE, d, E, T, 1, op(x, 1, 1, d), 1, op(dr, 0, E, 1), 1, gr.dW_router, E),
+                          GEN_EPI_STORE, BF(BL.kpart), BL.kpart_floats, s));
+        }
+    }
 #undef CK
     return MOE_OK;
 }

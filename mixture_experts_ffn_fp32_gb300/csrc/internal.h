@@ -337,6 +337,7 @@ struct BwdLayout {
     // operand copies, the SwiGLU backward's outputs, padded positions
     size_t poff, invp, gys, zs, dab, dub, hwb, dwrow, dxsp;
     size_t doutb, dasb, dusb, hsb, routedb, dzb;
+    size_t wrt, cp, rpart;  // W_router^T; router coefficient per padded row; per-64-row partials
     long long tkpad, tpad;
     size_t kpart, kpart_floats;  // split-K partials of the long-reduction CUDA-core products
     size_t total;
