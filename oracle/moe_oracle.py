@@ -538,7 +538,7 @@ def round_bf16(a):
 
 
 def moe_backward(x, params, dout, gate, K, renormalize=False, routed_scale=1.0, routing=None,
-                 latent_rows_bf16=False):
+                 latent_rows_bf16=False, tokens=None):
     """Gradients of L = sum(dout * out) for the layer of moe_forward, the
     routing (selection) held fixed. Per token and per selected expert, the
     chain rule of
@@ -560,18 +560,29 @@ def moe_backward(x, params, dout, gate, K, renormalize=False, routed_scale=1.0, 
 
     latent_rows_bf16: the latent rows z are rounded to BF16 (round_bf16)
     before the experts use them, as a BF16 layer stores its activations; the
-    derivative of that rounding is taken as 1."""
+    derivative of that rounding is taken as 1.
+
+    tokens: only these tokens are processed (large layers sampled token by
+    token): their rows of dx and dw are complete, the other rows are zero,
+    and the weight gradients hold only these tokens' terms."""
     xn = f64(_to_np(x))
     g_out = f64(_to_np(dout))
     T, d = xn.shape
     Wr = f64(_to_np(params["W_router"]))
     bias = _to_np(params.get("bias"))
     bias = None if bias is None else f64(bias)
-    cache = _WeightCache(params, max_entries=10 ** 6)
+    cache = _WeightCache(params, max_entries=10 ** 6 if tokens is None else 48)
     E = params["W_gate"].shape[0]
-    r = xn @ Wr
-    idx = route(xn, Wr, bias, gate, K, renormalize, routed_scale)["idx"] if routing is None \
-        else np.asarray(routing, dtype=np.int64)
+    rows = range(T) if tokens is None else [int(t) for t in tokens]
+    r = np.zeros((T, Wr.shape[1]))
+    for t in rows:
+        r[t] = xn[t] @ Wr
+    if routing is None:
+        idx = np.zeros((T, K), dtype=np.int64)
+        for t in rows:
+            idx[t] = route_from_logits(r[t], bias, gate, K, renormalize, routed_scale)["idx"]
+    else:
+        idx = np.asarray(routing, dtype=np.int64)
     latent = params.get("W_down_latent") is not None
     Wdl = cache.get("W_down_latent") if latent else None
     Wul = cache.get("W_up_latent") if latent else None
@@ -605,7 +616,7 @@ def moe_backward(x, params, dout, gate, K, renormalize=False, routed_scale=1.0, 
         du = dh * silu(a)
         return y, np.outer(zt, da), np.outer(zt, du), np.outer(h, gy), da @ Wg.T + du @ Wu.T
 
-    for t in range(T):
+    for t in rows:
         xt = xn[t]
         zt = xt @ Wdl if latent else xt
         if latent and latent_rows_bf16:

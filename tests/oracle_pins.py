@@ -420,6 +420,10 @@ def pin_backward_finite_differences(o):
         assert not (idx == E - 1).any()
         g = o.moe_backward(x, p, dout, gate, K, renorm, scale)
         assert not g["active"][E - 1] and g["active"][np.unique(idx)].all()
+        # a token subset gives those tokens' dx rows exactly and zero elsewhere
+        gs = o.moe_backward(x, p, dout, gate, K, renorm, scale, tokens=[1, 3])
+        assert np.array_equal(gs["dx"][[1, 3]], g["dx"][[1, 3]])
+        assert not gs["dx"][[0, 2, 4]].any()
         for name in ("dW_gate", "dW_up", "dW_down"):
             assert not g[name][E - 1].any(), name
 

@@ -153,3 +153,39 @@ def test_backward_reproducible_and_optional_outputs():
                     grads={n: None for n in A.GRAD_NAMES if n != "dx"})
     assert set(g3) == {"dx"}
     assert torch.equal(g3["dx"].view(torch.int32), g1["dx"].view(torch.int32))
+
+
+FULL = ["small", "medium_prefill", "medium_decode", "large_prefill", "large_prefill_zipf",
+        "large_decode", "large_decode_zipf", "latent"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_backward_sampled_rows(name):
+    """The benchmark layers at full size: dx on sampled tokens (first, last,
+    random, tokens of the rarest experts) against the oracle's backward of
+    just those tokens, on the GPU's selection; expert slices of experts
+    without rows stay as given; a second backward gives the same bits."""
+    w = W.WORKLOADS[name]
+    assert _tc(w)
+    spec, inp, ws, gidx, counts, dout, g = run(w)
+    rows = P.sample_rows(w, gidx, n=8)
+    ref = O.moe_backward(inp["x"], inp, dout, w.gate, w.K, w.renormalize, w.routed_scale,
+                         routing=gidx, latent_rows_bf16=bool(w.latent_dim), tokens=rows)
+    got = g["dx"][rows].detach().cpu().numpy().astype(np.float64)
+    r = ref["dx"][rows]
+    assert np.isfinite(got).all()
+    rms = float(np.sqrt(np.mean(r ** 2)))
+    err = float(np.abs(got - r).max())
+    fr = float(np.linalg.norm(got - r) / np.linalg.norm(r))
+    assert fr <= 1e-2, f"{name}: dx relative Frobenius error {fr:.3e} on sampled rows"
+    assert err <= 1e-1 * rms, f"{name}: dx max-abs error {err:.3e} > 0.1 x RMS {rms:.3e}"
+    empty = np.where(counts == 0)[0]
+    for n in ("dW_gate", "dW_up", "dW_down"):
+        if empty.size:
+            assert torch.isnan(g[n][torch.as_tensor(empty, device=g[n].device)]).all(), n
+        assert torch.isfinite(g[n][torch.as_tensor(np.where(counts > 0)[0], device=g[n].device)]).all(), n
+    g2 = A.backward(spec, inp["x"], inp, dout, ws, grads={n: None for n in A.GRAD_NAMES if n != "dx"})
+    assert torch.equal(g2["dx"].view(torch.int32), g["dx"].view(torch.int32))
+    print(name, {"rows": len(rows), "frob": fr, "max_err_over_rms": err / rms, "empty_experts": int(empty.size)})
+    del g, g2, ws, inp
+    torch.cuda.empty_cache()
