@@ -343,11 +343,17 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
         rec.end(ST_LATENT_DOWN);
     }
 
-    // 2. dispatch (a BF16 decode batch: with the row gather, one launch)
+    // 2. dispatch (BF16 batches of up to DISPATCH_WIDE_MAX assignments: with the row
+    //    gather, one launch)
     rec.begin(ST_DISPATCH);
-    const bool dg = bf && L.nchunks == 1;
-    if (dg) {
+    const bool dg1 = bf && L.nchunks == 1;
+    const bool dgw = bf && !dg1 && TK <= DISPATCH_WIDE_MAX;
+    const bool dg = dg1 || dgw;
+    if (dg1) {
         if ((e = launch_dispatch_gather(da, ex_src, de * 2, P(L.xs), s)) != cudaSuccess)
+            return cuda_status(e);
+    } else if (dgw) {
+        if ((e = launch_dispatch_gather_wide(da, ex_src, de * 2, P(L.xs), s)) != cudaSuccess)
             return cuda_status(e);
     } else if ((e = launch_dispatch(da, s, nullptr)) != cudaSuccess) {
         return cuda_status(e);

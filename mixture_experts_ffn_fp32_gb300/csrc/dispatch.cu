@@ -229,6 +229,225 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a,
     }
 }
 
+// Dispatch and row gather of up to DISPATCH_WIDE_MAX assignments in one
+// launch over many CTAs, with nothing passed between them: every CTA counts
+// all assignments per expert itself (the totals, and the counts before its
+// own range of per_cta consecutive assignments, a multiple of 32), which
+// places each assignment of its range in the stable expert order; CTA 0
+// writes the counts, offsets and tile prefixes; each CTA writes sorted_token
+// / sorted_w / inv of its range and copies the range's rows (one warp per
+// row, several rows of a warp in flight). The same integer results as the
+// two-launch dispatch. E <= 8: 1024 threads, per-thread counters packed as
+// 16-bit fields of two 64-bit words; otherwise 256 threads and per-warp
+// counters in shared memory.
+template <int EMAX, int NT>
+__global__ void __launch_bounds__(NT) dispatch_gather_wide_kernel(DispatchArgs a, int per_cta,
+                                                                  const uint4* __restrict__ src,
+                                                                  int vpr, uint4* __restrict__ dst) {
+    constexpr int NW = NT / 32;
+    constexpr bool REG = EMAX <= 8;
+    constexpr int RB = NT >= 1024 ? 2 : 4;  // rows of a warp in flight in the gather
+    static_assert(DISPATCH_WIDE_MAX < 65536 && EMAX <= 256 && (REG || NT == 256), "wide dispatch shape");
+    __shared__ int s_all[NW][EMAX];
+    __shared__ int s_pre[NW][EMAX];
+    __shared__ int s_rank[8][EMAX];
+    __shared__ int s_tot[EMAX];
+    __shared__ int s_base[EMAX];
+    __shared__ int s_pos[256];
+    __shared__ int s_tok[256];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < NW * EMAX; i += NT) {
+        (&s_all[0][0])[i] = 0;
+        (&s_pre[0][0])[i] = 0;
+    }
+    for (int i = threadIdx.x; i < 8 * EMAX; i += NT) (&s_rank[0][0])[i] = 0;
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+    const int TK = a.T * a.K, E = a.E;
+    const int j0 = blockIdx.x * per_cta;
+    const int j1 = min(j0 + per_cta, TK);
+    bool bad = false;
+
+    // 1. counts of all assignments per expert, and of those before j0 (packed
+    //    fields: a CTA sees at most DISPATCH_WIDE_MAX ids, no field overflows)
+    {
+        unsigned long long all0 = 0, all1 = 0, pre0 = 0, pre1 = 0;
+        auto count = [&](int j, int e) {
+            if (e < 0 || e >= E) {
+                bad = true;
+                return;
+            }
+            if (REG) {
+                const unsigned long long inc = 1ull << (16 * (e & 3));
+                const bool hi = e >= 4, before = j < j0;
+                all0 += hi ? 0ull : inc;
+                all1 += hi ? inc : 0ull;
+                pre0 += (before && !hi) ? inc : 0ull;
+                pre1 += (before && hi) ? inc : 0ull;
+            } else {
+                atomicAdd(&s_all[warp][e], 1);
+                if (j < j0) atomicAdd(&s_pre[warp][e], 1);
+            }
+        };
+        const int nv = TK / 4;  // ids four at a time, up to four loads in flight per thread
+        const int4* iv = reinterpret_cast<const int4*>(a.idx);
+        for (int i0 = threadIdx.x; i0 < nv; i0 += 4 * NT) {
+            int4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * NT;
+                v[u] = i < nv ? __ldcg(iv + i) : make_int4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * NT;
+                if (i < nv) {
+                    count(4 * i, v[u].x);
+                    count(4 * i + 1, v[u].y);
+                    count(4 * i + 2, v[u].z);
+                    count(4 * i + 3, v[u].w);
+                }
+            }
+        }
+        for (int j = 4 * nv + threadIdx.x; j < TK; j += NT) count(j, __ldcg(a.idx + j));
+        if (REG) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                all0 += __shfl_xor_sync(0xffffffffu, all0, o);
+                all1 += __shfl_xor_sync(0xffffffffu, all1, o);
+                pre0 += __shfl_xor_sync(0xffffffffu, pre0, o);
+                pre1 += __shfl_xor_sync(0xffffffffu, pre1, o);
+            }
+            if (lane < EMAX) {
+                const unsigned long long wa = lane < 4 ? all0 : all1, wp = lane < 4 ? pre0 : pre1;
+                s_all[warp][lane] = static_cast<int>((wa >> (16 * (lane & 3))) & 0xFFFFull);
+                s_pre[warp][lane] = static_cast<int>((wp >> (16 * (lane & 3))) & 0xFFFFull);
+            }
+        }
+    }
+    if (bad && blockIdx.x == 0) atomicOr(a.err, ERRBIT_INDEX);
+    __syncthreads();
+
+    // 2. per-expert totals; warp 0 scans them (and in CTA 0 writes the outputs)
+    for (int e = threadIdx.x; e < EMAX; e += NT) {
+        int tot = 0, pre = 0;
+        if (e < E) {
+#pragma unroll 8
+            for (int w = 0; w < NW; ++w) {
+                tot += s_all[w][e];
+                pre += s_pre[w][e];
+            }
+        }
+        s_tot[e] = tot;
+        s_base[e] = pre;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        constexpr int EPL = EMAX >= 32 ? EMAX / 32 : 1;  // experts per lane
+        const int bm = a.bm;
+        int c[EPL], m1[EPL], m2[EPL], sc = 0, s1 = 0, s2 = 0;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int ex = EPL * lane + i;
+            c[i] = ex < E && ex < EMAX ? s_tot[ex] : 0;
+            m1[i] = (c[i] + bm - 1) / bm;
+            m2[i] = (c[i] + 2 * bm - 1) / (2 * bm);
+            sc += c[i];
+            s1 += m1[i];
+            s2 += m2[i];
+        }
+        int x = sc, x1 = s1, x2 = s2;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            const int y1 = __shfl_up_sync(0xffffffffu, x1, o);
+            const int y2 = __shfl_up_sync(0xffffffffu, x2, o);
+            if (lane >= o) {
+                x += y;
+                x1 += y1;
+                x2 += y2;
+            }
+        }
+        int b = x - sc, b1 = x1 - s1, b2 = x2 - s2;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int ex = EPL * lane + i;
+            if (ex < E && ex < EMAX) {
+                s_base[ex] += b;
+                if (blockIdx.x == 0) {
+                    a.counts[ex] = c[i];
+                    a.offsets[ex] = b;
+                    a.mt_prefix[ex] = b1;
+                    a.mt_prefix[E + 1 + ex] = b2;
+                    if (ex == E - 1) {
+                        a.offsets[E] = b + c[i];
+                        a.mt_prefix[E] = b1 + m1[i];
+                        a.mt_prefix[2 * E + 1] = b2 + m2[i];
+                    }
+                }
+            }
+            b += c[i];
+            b1 += m1[i];
+            b2 += m2[i];
+        }
+    }
+    __syncthreads();
+
+    // 3. stable ranks within the range: warp w < 8 takes assignments j0 + 32 w + lane
+    {
+        const bool mine = warp < 8 && 32 * warp < per_cta;
+        const int j = j0 + 32 * warp + lane;
+        int e = (mine && j < j1) ? __ldcg(a.idx + j) : -1;
+        if (e < 0 || e >= E) e = -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        if (e >= 0 && rank == 0) s_rank[warp][e] = __popc(peers);
+        __syncthreads();
+        if (mine && j < j1) {
+            int pos = -1;
+            if (e >= 0) {
+                pos = s_base[e] + rank;
+                for (int w = 0; w < warp; ++w) pos += s_rank[w][e];
+                a.sorted_token[pos] = j / a.K;
+                a.sorted_w[pos] = __ldcg(a.w + j);
+                a.inv[j] = pos;
+            }
+            s_pos[j - j0] = pos;
+            s_tok[j - j0] = j / a.K;
+        }
+    }
+    __syncthreads();
+
+    // 4. the range's rows: RB rows of a warp in flight, 4 vectors per lane each
+    const int n = j1 - j0;
+    for (int r0 = RB * warp; r0 < n; r0 += RB * NW) {
+        for (int v0 = lane; v0 < vpr; v0 += 128) {
+            uint4 buf[RB][4];
+#pragma unroll
+            for (int q = 0; q < RB; ++q) {
+                const int r = r0 + q;
+                if (r < n && s_pos[r] >= 0) {
+                    const size_t so = static_cast<size_t>(s_tok[r]) * vpr;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (v0 + 32 * i < vpr) buf[q][i] = __ldg(src + so + v0 + 32 * i);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < RB; ++q) {
+                const int r = r0 + q;
+                if (r < n && s_pos[r] >= 0) {
+                    const size_t d = static_cast<size_t>(s_pos[r]) * vpr;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (v0 + 32 * i < vpr) dst[d + v0 + 32 * i] = buf[q][i];
+                }
+            }
+        }
+    }
+}
+
 // One warp per destination row; 16-byte vectors.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src,
                                                           const int32_t* __restrict__ rowidx,
@@ -407,6 +626,29 @@ cudaError_t launch_dispatch_gather(const DispatchArgs& a, const void* src, int r
     if (a.E <= 128)
         return launch_pdl(dispatch_gather_kernel<128>, dim3(blocks), dim3(256), 0, s, a, sv, vpr, dv);
     return launch_pdl(dispatch_gather_kernel<256>, dim3(blocks), dim3(256), 0, s, a, sv, vpr, dv);
+}
+
+cudaError_t launch_dispatch_gather_wide(const DispatchArgs& a, const void* src, int row_bytes,
+                                        void* dst, cudaStream_t s) {
+    const int TK = a.T * a.K;
+    if (TK > DISPATCH_WIDE_MAX || a.E > 256 || a.E < 1 || row_bytes % 16 ||
+        (reinterpret_cast<uintptr_t>(a.idx) & 15u))
+        return cudaErrorInvalidValue;
+    // ranges of a multiple of 32 assignments, about one CTA per SM (each CTA
+    // counts every assignment, so more CTAs cost more than their rows save)
+    const int want = num_sms();
+    int per_cta = (TK + want - 1) / want;
+    per_cta = std::min(256, std::max(32, (per_cta + 31) / 32 * 32));
+    const int blocks = (TK + per_cta - 1) / per_cta;
+    const uint4* sv = static_cast<const uint4*>(src);
+    uint4* dv = static_cast<uint4*>(dst);
+    const int vpr = row_bytes / 16;
+#define MOE_DGW(EM, NT) \
+    return launch_pdl(dispatch_gather_wide_kernel<EM, NT>, dim3(blocks), dim3(NT), 0, s, a, per_cta, sv, vpr, dv)
+    if (a.E <= 8) MOE_DGW(8, 1024);
+    if (a.E <= 64) MOE_DGW(64, 256);
+    MOE_DGW(256, 256);
+#undef MOE_DGW
 }
 
 cudaError_t launch_gather_rows(const void* src, const int32_t* rowidx, int rows, int row_bytes,

@@ -137,6 +137,12 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s, int* n_launch
 cudaError_t launch_dispatch_gather(const DispatchArgs& a, const void* src, int row_bytes, void* dst,
                                    cudaStream_t s);
 
+// The same for T*K <= DISPATCH_WIDE_MAX, over many CTAs (each counts all
+// assignments itself and places its own range of them).
+constexpr int DISPATCH_WIDE_MAX = 16384;
+cudaError_t launch_dispatch_gather_wide(const DispatchArgs& a, const void* src, int row_bytes,
+                                        void* dst, cudaStream_t s);
+
 // dst[r, :] = src[rowidx[r], :] for r < rows, row_bytes a multiple of 16.
 cudaError_t launch_gather_rows(const void* src, const int32_t* rowidx, int rows, int row_bytes,
                                void* dst, cudaStream_t s);

@@ -98,6 +98,22 @@ SMALL = {
     "decode_max_assignments": W.Workload("t_d4", T=128, d=384, d_ff=64, E=128, K=8, n_shared=0,
                                         shared_d_ff=0, dtype="bf16", gate="softmax_topk",
                                         bias_std=0.01),
+    # Batches of 1025..16384 assignments: dispatch and gather in one launch over
+    # many CTAs (each counts every assignment itself). A flat-id count that is
+    # not a multiple of four (the scalar tail of the id loads) with more than 64
+    # experts (per-warp shared counters), and exactly 16384 assignments with
+    # 16 experts.
+    "wide_e96_tail": W.Workload("t_w1", T=701, d=192, d_ff=128, E=96, K=6, n_shared=1,
+                                shared_d_ff=128, dtype="bf16", gate="softmax_topk",
+                                bias_std=0.01, skew=1.2),
+    "wide_max_assignments": W.Workload("t_w2", T=2048, d=128, d_ff=64, E=16, K=8, n_shared=0,
+                                       shared_d_ff=0, dtype="bf16", gate="softmax_topk",
+                                       bias_std=0.01),
+    # 16800 assignments: the two-launch dispatch (chunk histograms, then the scatter)
+    # and the separate row gather
+    "two_launch_dispatch": W.Workload("t_w3", T=4200, d=64, d_ff=64, E=12, K=4, n_shared=1,
+                                      shared_d_ff=64, dtype="bf16", gate="softmax_topk",
+                                      bias_std=0.01, skew=0.8),
 }
 
 
@@ -224,6 +240,24 @@ def test_dispatch_bit_exact(T, E, K, skew):
                    gate="softmax_topk")
     P.check_dispatch(w, P.npi(idx), wts.cpu().numpy().reshape(-1), g)
     assert A.workspace_status(g["ws"]) == A.MOE_OK
+
+
+@pytest.mark.parametrize("name", ["wide_e96_tail", "wide_max_assignments", "bf16_topk",
+                                  "pair_skew", "decode_e64_ragged", "bf16_e256",
+                                  "two_launch_dispatch"])
+def test_forward_dispatch_bit_exact(name):
+    """The dispatch a forward leaves in its workspace (one-launch single-CTA,
+    one-launch many-CTA or two-launch form) is the oracle's stable dispatch of
+    the forward's own routing, bit for bit."""
+    A = api()
+    w = SMALL[name]
+    inp = W.make_inputs(w, device="cuda")
+    spec = A.LayerSpec.of(w)
+    ws = A.alloc_workspace(spec)
+    A.forward(spec, inp["x"], inp, ws=ws)
+    v = A.workspace_views(spec, ws)
+    P.check_dispatch(w, P.npi(v["idx"]), v["w"].cpu().numpy().reshape(-1), v)
+    assert A.workspace_status(ws) == A.MOE_OK
 
 
 def test_dispatch_worked_example():
