@@ -837,10 +837,14 @@ cudaError_t launch_tc_s(const TcGemmArgs& a, cudaStream_t s) {
     // The pair form splits B's strips between the two CTAs (an even count).
     // Its routed tiles are 256 rows, so a segment wastes 128 padded rows on
     // average instead of 64: it is used when segments average >= 512 rows.
+    // Dense projections alone (no routed group, single product: the latent
+    // down and up projections, the router) measured faster in the single-CTA
+    // form (latent up projection 69 -> 60 us).
     const bool even = SWIGLU || nstrip % 2 == 0;
     const bool long_segments =
         !a.g[0].enabled || static_cast<long long>(a.g[0].rows) >= 512LL * (a.E > 0 ? a.E : 1);
-    const int slots = (even && long_segments) ? pair_slots<MODE>(dev) : 0;
+    const bool dense_plain = MODE == TC_PLAIN && !a.g[0].enabled;
+    const int slots = (even && long_segments && !dense_plain) ? pair_slots<MODE>(dev) : 0;
     if (slots > 0) return launch_tc_t<MODE, true>(a, nstrip, slots, s);
     if (!prepare_kernel<MODE, false>(dev)) return cudaErrorInvalidValue;
     return launch_tc_t<MODE, false>(a, nstrip, num_sms(), s);
