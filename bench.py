@@ -152,7 +152,7 @@ def layer_bytes(w, counts=None) -> float:
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("gemm_tc.cu", "common.cuh"):
+    for f in ("gemm_tc.cu", "common.cuh", "warp_stage.cuh"):
         with open(os.path.join(ROOT, "mixture_experts_ffn_fp32_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -420,42 +420,62 @@ def run_ours(args, name):
     if world == 1 and not args.no_backward:
         torch.manual_seed(1)
         dout = torch.randn(w.T, w.d, device=dev, dtype=torch.float32)
-        bws = torch.empty(api.backward_workspace_size(spec), dtype=torch.uint8, device=dev)
-        grads = {n: torch.empty(s, dtype=torch.float32, device=dev)
-                 for n, s in api.grad_shapes(spec).items()}
-        n_bw = max(1, min(args.steps, 5))
-        b_ms = []
-        for i in range(n_bw + 2):
-            flush.fill_(i & 0xFF)
-            step()
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            api.backward(spec, inp["x"], inp, dout, ws, grads=grads, bws=bws, stream=stream)
-            b.record(stream)
-            torch.cuda.synchronize()
-            if i >= 2:
-                b_ms.append(a.elapsed_time(b))
-        st = api.workspace_status(ws, stream)
-        if st != api.MOE_OK:
-            raise RuntimeError(f"device status after the backward: {api.status_string(st)}")
-        bms = sum(b_ms) / len(b_ms)
-        bfl = backward_flops(w)
-        pk0 = peaks()
         de = w.latent_dim or w.d
         tc = (w.dtype == "bf16" and w.d % 64 == 0 and w.d_ff % 64 == 0 and de % 64 == 0
               and (w.n_shared == 0 or w.shared_d_ff % 64 == 0))
+        n_bw = max(1, min(args.steps, 5))
+
+        def time_backward(bspec):
+            """Forward then backward on one workspace, each timed with CUDA events
+            (L2 flushed before each forward); averages over n_bw steps after 2."""
+            bws_ = torch.empty(api.backward_workspace_size(bspec), dtype=torch.uint8, device=dev)
+            fws = ws if bspec is spec else torch.empty(api.workspace_size(bspec), dtype=torch.uint8,
+                                                       device=dev)
+            grads = {n: torch.empty(s_, dtype=torch.float32, device=dev)
+                     for n, s_ in api.grad_shapes(bspec).items()}
+            f_ms, b_ms = [], []
+            for i in range(n_bw + 2):
+                flush.fill_(i & 0xFF)
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                ev[0].record(stream)
+                api.forward(bspec, inp["x"], inp, out=out, ws=fws, stream=stream)
+                ev[1].record(stream)
+                api.backward(bspec, inp["x"], inp, dout, fws, grads=grads, bws=bws_, stream=stream)
+                ev[2].record(stream)
+                torch.cuda.synchronize()
+                if i >= 2:
+                    f_ms.append(ev[0].elapsed_time(ev[1]))
+                    b_ms.append(ev[1].elapsed_time(ev[2]))
+            st_ = api.workspace_status(fws, stream)
+            if st_ != api.MOE_OK:
+                raise RuntimeError(f"device status after the backward: {api.status_string(st_)}")
+            del bws_, grads
+            return sum(f_ms) / len(f_ms), sum(b_ms) / len(b_ms)
+
+        f_re, b_re = time_backward(spec)
+        bfl = backward_flops(w)
+        pk0 = peaks()
         bpk = pk0["bf16_tflops"] if tc else pk0["fp32_tflops"]
+        if tc:
+            # training form: the forward keeps its gate/up products, the backward reads them
+            tspec = api.LayerSpec.of(w, save_gate_up=True)
+            f_sv, bms = time_backward(tspec)
+        else:
+            f_sv, bms = f_re, b_re
         bwd = {"ms": bms, "tflops": bfl / (bms / 1e3) / 1e12, "flops_per_step": bfl,
                "bound": "tensor" if tc else "alu", "peak": bpk, "unit": "TFLOP/s",
                "frac": bfl / (bms / 1e3) / 1e12 / bpk,
+               "forward_ms": f_sv, "training_step_ms": f_sv + bms,
+               "recompute": {"ms": b_re, "forward_ms": f_re, "training_step_ms": f_re + b_re},
                "note": ("moe_backward (all gradients) after a forward on the same workspace; "
-                        + ("expert contractions on tcgen05 (BF16 operands, FP32 sums), "
-                           "peak = measured BF16 burst; " if tc else
+                        + ("the forward keeps its BF16 gate/up products (save_gate_up) and the "
+                           "backward reads them ('recompute': the backward recomputes them "
+                           "instead); expert contractions on tcgen05 (BF16 operands, FP32 "
+                           "sums), peak = measured BF16 burst; " if tc else
                            "FP32 FFMA grouped GEMMs, peak = FP32 FFMA; ")
-                        + "L2 flushed before each forward; CUDA events around the backward "
-                          "alone; FLOPs exclude the recomputed gate/up products")}
-        del bws, grads, dout
+                        + "L2 flushed before each forward; CUDA events around the forward "
+                          "and the backward separately; FLOPs exclude recomputed products")}
+        del dout
 
     # end to end through the host-buffer entry point (copies inside the timed region)
     e2e = None

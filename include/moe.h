@@ -89,6 +89,14 @@ typedef struct moe_config {
     int32_t out_dtype;    /* moe_dtype of out: MOE_F32 (the FP32 accumulation, unrounded) or
                              MOE_BF16 (rounded once to nearest-even); must be MOE_F32 when
                              dtype is MOE_F32 */
+    int32_t save_gate_up; /* 0 or 1. 1, for a layer whose moe_backward runs on the tensor
+                             cores (BF16, widths multiples of 64): moe_forward also keeps
+                             the gate and up products a = z W_gate, u = z W_up of every
+                             routed row and shared expert (BF16) in the workspace, and
+                             moe_backward reads them instead of recomputing them (the
+                             workspace grows by 4 (T K d_ff + T n_shared shared_d_ff)
+                             bytes). The forward and the backward of one step must use the
+                             same value. Ignored by other layers. */
 } moe_config;
 
 /* Weights, all device pointers. d_e = latent_dim ? latent_dim : d.

@@ -37,7 +37,7 @@ class Config(ctypes.Structure):
                 ("shared_d_ff", ctypes.c_int32), ("latent_dim", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("gate", ctypes.c_int32),
                 ("renormalize", ctypes.c_int32), ("routed_scale", ctypes.c_float),
-                ("out_dtype", ctypes.c_int32)]
+                ("out_dtype", ctypes.c_int32), ("save_gate_up", ctypes.c_int32)]
 
 
 class Weights(ctypes.Structure):
@@ -150,19 +150,21 @@ class LayerSpec:
     renormalize: bool = False
     routed_scale: float = 1.0
     out_dtype: str = "f32"
+    save_gate_up: bool = False  # forward keeps the gate/up products for the backward
 
     @staticmethod
-    def of(w, out_dtype: str = "f32") -> "LayerSpec":
+    def of(w, out_dtype: str = "f32", save_gate_up: bool = False) -> "LayerSpec":
         """From any object with the Workload attribute names."""
         return LayerSpec(w.T, w.d, w.d_ff, w.E, w.K, w.n_shared, w.shared_d_ff, w.latent_dim,
-                         w.dtype, w.gate, bool(w.renormalize), float(w.routed_scale), out_dtype)
+                         w.dtype, w.gate, bool(w.renormalize), float(w.routed_scale), out_dtype,
+                         bool(save_gate_up))
 
     def config(self) -> Config:
         return Config(self.T, self.d, self.d_ff, self.E, self.K, self.n_shared,
                       self.shared_d_ff if self.n_shared else 0, self.latent_dim,
                       MOE_F32 if self.dtype == "f32" else MOE_BF16, GATES[self.gate],
                       int(self.renormalize), float(self.routed_scale),
-                      MOE_F32 if self.out_dtype == "f32" else MOE_BF16)
+                      MOE_F32 if self.out_dtype == "f32" else MOE_BF16, int(self.save_gate_up))
 
     @property
     def torch_dtype(self):

@@ -93,6 +93,7 @@ moe_status validate_config(const moe_config& c) {
     if (c.n_shared < 0 || (c.n_shared > 0 && c.shared_d_ff < 1)) return MOE_ERR_INVALID_ARG;
     if (c.latent_dim < 0) return MOE_ERR_INVALID_ARG;
     if (!(c.routed_scale == c.routed_scale)) return MOE_ERR_INVALID_ARG;
+    if (c.save_gate_up != 0 && c.save_gate_up != 1) return MOE_ERR_INVALID_ARG;
     if (c.E > 256 || c.K > 16) return MOE_ERR_UNSUPPORTED;
     // row pitches feed 16-byte vector accesses and TMA strides; tiles store 16 columns at a time
     if (c.d % 16 || c.d_ff % 16) return MOE_ERR_UNSUPPORTED;
@@ -166,6 +167,12 @@ WsLayout plan_workspace(const moe_config& c) {
     L.h = take(TK * c.d_ff * es);
     const size_t SF = static_cast<size_t>(c.n_shared) * (c.n_shared ? c.shared_d_ff : 0);
     L.hs = SF ? take(T * SF * es) : 0;
+    // the gate and up products, kept for a backward pass on the tensor cores
+    const bool sv = bf && c.save_gate_up && bwd_on_tensor_cores(c);
+    L.ga = sv ? take(TK * c.d_ff * 2) : 0;
+    L.gu = sv ? take(TK * c.d_ff * 2) : 0;
+    L.gas = (sv && SF) ? take(T * SF * 2) : 0;
+    L.gus = (sv && SF) ? take(T * SF * 2) : 0;
     L.ys = take(TK * de * 4);  // FP32: the K routed rows are summed before one final rounding
     // latent routed sum as a BF16 hi/lo pair, each part padded to a multiple of 64 columns
     L.routed = c.latent_dim ? take(T * 2 * static_cast<size_t>(latent_pad(c.latent_dim)) * 2) : 0;
@@ -376,6 +383,14 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
             TcGemmArgs g{};
             g.g[0] = TcGroup{1, de, P(L.xs), de, TK, w.W_gate, w.W_up, E, c.d_ff, P(L.h), c.d_ff, 0};
             if (S) g.g[1] = TcGroup{1, c.d, x, c.d, T, w.Ws_gate, w.Ws_up, S, Fs, P(L.hs), SF, 0};
+            if (L.ga) {
+                g.g[0].a_out = P(L.ga);
+                g.g[0].u_out = P(L.gu);
+                if (S) {
+                    g.g[1].a_out = P(L.gas);
+                    g.g[1].u_out = P(L.gus);
+                }
+            }
             g.E = E; g.offsets = offsets; g.mt_prefix = mt_prefix; g.swiglu = 1; g.err = err;
             if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
         }

@@ -258,11 +258,13 @@ BwdLayout plan_backward(const moe_config& c) {
         B.invp = take(TK * 4);
         B.gys = take(kp * de * 2);
         B.zs = take(kp * de * 2);
-        B.dhp = take(kp * F * 4);
+        B.saved = c.save_gate_up != 0;  // the forward kept the gate / up products
+        B.dhp = B.saved ? 0 : take(kp * F * 4);
         B.dab = take(kp * F * 2);
         B.dub = take(kp * F * 2);
         B.hwb = take(kp * F * 2);
         B.dwrow = take(TK * 2 * ((F + 127) / 128) * 4);  // per-row partials of dg, one per 64 columns
+                                                           // (>= F / 64 of them)
         B.dxsp = take(kp * de * 4);
         B.wrt = take(static_cast<size_t>(c.d) * E * 4);
         B.cp = take(kp * 4);
@@ -273,7 +275,7 @@ BwdLayout plan_backward(const moe_config& c) {
             B.dzb = take(T * L * 2);
         }
         if (SF) {
-            B.dhs = take(T * SF * 4);
+            B.dhs = B.saved ? 0 : take(T * SF * 4);
             B.dasb = take(T * SF * 2);
             B.dusb = take(T * SF * 2);
             B.hsb = take(T * SF * 2);
@@ -586,26 +588,56 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
     CK(launch_gather_pad_bf16(gy, 0, ld_gy, stok, TK, de, poff, offsets, E, kp, gys, s));
     CK(launch_gather_pad_bf16(zsrc, 1, ld_z, stok, TK, de, poff, offsets, E, kp, zs, s));
 
-    // ---- dh = gy W_down^T per expert (padded rows), dout Ws_down^T (shared) ----
-    float* dhp = BF(BL.dhp);
-    CK(launch_nt_gemm(nt(NT_MSEG, kp, F, de, E, opnd(gys, kp, de, de),
-                         opnd(w.W_down, F, de, de, E, static_cast<long long>(F) * de), dhp, F, 0, poff),
-                      s));
-    float* dhs = nullptr;
-    if (S) {
-        dhs = BF(BL.dhs);
-        NtGemm g = nt(NT_DENSE, T, Fs, d, S, opnd(doutb, T, d, d),
-                      opnd(w.Ws_down, Fs, d, d, S, static_cast<long long>(Fs) * d), dhs, SF, Fs);
-        g.b_z3 = 1;
-        CK(launch_nt_gemm(g, s));
-    }
-
-    // ---- gate and up products recomputed by the forward's GEMM; its SwiGLU
-    //      backward epilogue writes da, du, g h and the gate-gradient partials ----
+    // ---- dh = gy W_down^T per expert (padded rows), dout Ws_down^T (shared),
+    //      then the SwiGLU backward: da, du, g h and the gate-gradient partials ----
     __nv_bfloat16 *dab = BH(BL.dab), *dub = BH(BL.dub), *hwb = BH(BL.hwb);
     float* dgpart = BF(BL.dwrow);
-    __nv_bfloat16 *dasb = nullptr, *dusb = nullptr, *hsb = nullptr;
-    {
+    __nv_bfloat16 *dasb = S ? BH(BL.dasb) : nullptr, *dusb = S ? BH(BL.dusb) : nullptr,
+                  *hsb = S ? BH(BL.hsb) : nullptr;
+    int npart;  // gate-gradient partials per row
+    if (BL.saved) {
+        // the forward kept the gate and up products: the SwiGLU backward runs in
+        // the epilogue of the dh products, nothing is recomputed
+        NtGemm g = nt(NT_MSEG, kp, F, de, E, opnd(gys, kp, de, de),
+                      opnd(w.W_down, F, de, de, E, static_cast<long long>(F) * de), nullptr, F, 0, poff);
+        g.sg_a = static_cast<const __nv_bfloat16*>(WP(L.ga));
+        g.sg_u = static_cast<const __nv_bfloat16*>(WP(L.gu));
+        g.sg_off = offsets;
+        g.sg_ld = F;
+        g.sg_g = sw;
+        g.sg_da = dab;
+        g.sg_du = dub;
+        g.sg_hw = hwb;
+        g.sg_part = dgpart;
+        g.sg_npart = F / 64;
+        CK(launch_nt_gemm(g, s));
+        if (S) {
+            NtGemm g2 = nt(NT_DENSE, T, Fs, d, S, opnd(doutb, T, d, d),
+                           opnd(w.Ws_down, Fs, d, d, S, static_cast<long long>(Fs) * d), nullptr, SF, Fs);
+            g2.b_z3 = 1;
+            g2.sg_a = static_cast<const __nv_bfloat16*>(WP(L.gas));
+            g2.sg_u = static_cast<const __nv_bfloat16*>(WP(L.gus));
+            g2.sg_da = dasb;
+            g2.sg_du = dusb;
+            g2.sg_hw = hsb;
+            CK(launch_nt_gemm(g2, s));
+        }
+        npart = F / 64;
+    } else {
+        float* dhp = BF(BL.dhp);
+        CK(launch_nt_gemm(nt(NT_MSEG, kp, F, de, E, opnd(gys, kp, de, de),
+                             opnd(w.W_down, F, de, de, E, static_cast<long long>(F) * de), dhp, F, 0, poff),
+                          s));
+        float* dhs = nullptr;
+        if (S) {
+            dhs = BF(BL.dhs);
+            NtGemm g = nt(NT_DENSE, T, Fs, d, S, opnd(doutb, T, d, d),
+                          opnd(w.Ws_down, Fs, d, d, S, static_cast<long long>(Fs) * d), dhs, SF, Fs);
+            g.b_z3 = 1;
+            CK(launch_nt_gemm(g, s));
+        }
+        // the gate and up products recomputed by the forward's GEMM; its SwiGLU
+        // backward epilogue writes da, du, g h and the gate-gradient partials
         TcGemmArgs g{};
         g.g[0] = TcGroup{1, de, WP(L.xs), de, TK, w.W_gate, w.W_up, E, F, nullptr, F, 0};
         g.g[0].dh = dhp;
@@ -615,9 +647,6 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
         g.g[0].hw = hwb;
         g.g[0].dgpart = dgpart;
         if (S) {
-            dasb = BH(BL.dasb);
-            dusb = BH(BL.dusb);
-            hsb = BH(BL.hsb);
             g.g[1] = TcGroup{1, d, x, d, T, w.Ws_gate, w.Ws_up, S, Fs, nullptr, SF, 0};
             g.g[1].dh = dhs;
             g.g[1].dh_ld = SF;
@@ -633,6 +662,7 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
         g.poff = poff;
         g.err = err;
         CK(launch_tc_gemm(g, s));
+        npart = 2 * ((F + 127) / 128);
     }
 
     // ---- dz rows = da W_gate^T + du W_up^T (padded rows, two phases) ----
@@ -716,7 +746,7 @@ static moe_status backward_tc(const moe_config& c, const void* x, const moe_weig
     CK(launch_pdl(transpose_f32_kernel, dim3((E + 31) / 32, (d + 31) / 32), dim3(256), 0, s,
                   static_cast<const float*>(w.W_router), d, E, wrt));
     CK(launch_pdl(router_bwd_kernel, dim3((T * 32 + 255) / 256), dim3(256), 0, s,
-                  static_cast<const float*>(dgpart), 2 * ((F + 127) / 128), inv, tidx, tw, scores, T, K, E,
+                  static_cast<const float*>(dgpart), npart, inv, tidx, tw, scores, T, K, E,
                   c.gate, c.renormalize, c.routed_scale, dr, dg, cp, static_cast<const int32_t*>(invp),
                   static_cast<const float*>(wrt), d, gr.dx));
     if (gr.dW_router) {

@@ -35,6 +35,7 @@
 // masks, but each phase's K must be a multiple of 64 (the caller's choice).
 #include "common.cuh"
 #include "internal.h"
+#include "warp_stage.cuh"
 
 namespace moe {
 namespace {
@@ -72,6 +73,17 @@ struct NtParams {
     float* C;
     long long ldc, c_zs;
     int accumulate;
+    // SwiGLU-backward epilogue (NtGemm)
+    const __nv_bfloat16* sg_a;
+    const __nv_bfloat16* sg_u;
+    const int32_t* sg_off;
+    long long sg_ld;
+    const float* sg_g;
+    __nv_bfloat16* sg_da;
+    __nv_bfloat16* sg_du;
+    __nv_bfloat16* sg_hw;
+    float* sg_part;
+    int sg_npart;
     uint32_t idesc;
     int* err;
     unsigned long long timeout_ns;
@@ -301,6 +313,94 @@ __global__ void __launch_bounds__(NT_THREADS, 1) nt_gemm_kernel(const __grid_con
             tc_fence_after();
             const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * NT_ACC_COLS) +
                                 (static_cast<uint32_t>(q * 32) << 16);
+            if (p.sg_a != nullptr) {
+                // SwiGLU backward, 32 columns at a time: a and u of the warp's 32 rows
+                // come in and da, du, g h go out as row-major 64-byte row segments
+                // through the warp's staging buffer; lane = row in between
+                uint4* stg4 = reinterpret_cast<uint4*>(stg);
+                const int wr0 = t.m0 + q * 32;                        // the warp's first row
+                const int tile_rows = max(0, min(32, t.rows - q * 32));  // rows written
+                int real_rows = tile_rows;                            // rows with a and u
+                long long arow0 = wr0;
+                if (p.mode == NT_MSEG) {
+                    const int i0 = wr0 - s_off[t.z];
+                    real_rows = max(0, min(tile_rows, p.sg_off[t.z + 1] - p.sg_off[t.z] - i0));
+                    arow0 = p.sg_off[t.z] + i0;
+                }
+                const bool real = lane < real_rows;
+                const float g = (real && p.sg_g != nullptr) ? p.sg_g[arow0 + lane] : 1.0f;
+                const long long obase = (p.mode == NT_MSEG ? 0 : t.z * p.c_zs) + static_cast<long long>(wr0) * p.ldc + t.n0;
+                const long long abase = p.mode == NT_MSEG ? arow0 * p.sg_ld + t.n0 : obase;
+                const size_t apitch = static_cast<size_t>(p.mode == NT_MSEG ? p.sg_ld : p.ldc) * 2;
+                const size_t opitch = static_cast<size_t>(p.ldc) * 2;
+                float part = 0.0f;
+                const int c_beg = half * (NBN / 2), c_end = (half + 1) * (NBN / 2);
+                // a and u of a 32-column block: both arrays' loads in flight together
+                // (N is a multiple of 64: a block is wholly inside or outside it)
+                const char* a_row0 = reinterpret_cast<const char*>(p.sg_a + abase);
+                const char* u_row0 = reinterpret_cast<const char*>(p.sg_u + abase);
+#pragma unroll 1
+                for (int c = c_beg; c < c_end; c += 32) {
+                    const bool col_ok = t.n0 + c < p.N;
+                    uint32_t v0[16], v1[16];
+                    tc_ld_32x32b_x16(tb + c, v0);
+                    tc_ld_32x32b_x16(tb + c + 16, v1);
+                    uint4 av[4], uv[4];
+                    {
+                        uint4 wa[4], wu[4];
+                        warp_load_issue(wa, lane, a_row0 + 2 * c, apitch, col_ok ? real_rows : 0);
+                        warp_load_issue(wu, lane, u_row0 + 2 * c, apitch, col_ok ? real_rows : 0);
+                        warp_load_finish(stg4, wa, av, lane);
+                        warp_load_finish(stg4, wu, uv, lane);
+                    }
+                    tc_wait_ld();
+                    const uint32_t* aw = reinterpret_cast<const uint32_t*>(av);
+                    const uint32_t* uw = reinterpret_cast<const uint32_t*>(uv);
+                    uint32_t pda[16], pdu[16], phw[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        float o_da[2], o_du[2], o_hw[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const float a = e ? bf16_hi(aw[j]) : bf16_lo(aw[j]);
+                            const float uu = e ? bf16_hi(uw[j]) : bf16_lo(uw[j]);
+                            const float dv = __uint_as_float(j < 8 ? v0[2 * j + e] : v1[2 * j - 16 + e]);
+                            const float sg = 1.0f / (1.0f + expf(-a));
+                            const float si = a * sg;
+                            const float h = si * uu;
+                            o_da[e] = real ? g * dv * uu * (sg * (1.0f + a * (1.0f - sg))) : 0.0f;
+                            o_du[e] = real ? g * dv * si : 0.0f;
+                            o_hw[e] = real ? g * h : 0.0f;
+                            part += real ? dv * h : 0.0f;
+                        }
+                        pda[j] = pack_bf16x2(o_da[0], o_da[1]);
+                        pdu[j] = pack_bf16x2(o_du[0], o_du[1]);
+                        phw[j] = pack_bf16x2(o_hw[0], o_hw[1]);
+                    }
+                    const int wrows = col_ok ? tile_rows : 0;
+                    const uint4 vd[4] = {make_uint4(pda[0], pda[1], pda[2], pda[3]), make_uint4(pda[4], pda[5], pda[6], pda[7]),
+                                         make_uint4(pda[8], pda[9], pda[10], pda[11]), make_uint4(pda[12], pda[13], pda[14], pda[15])};
+                    warp_store_block(stg4, vd, lane, reinterpret_cast<char*>(p.sg_da + obase + c), opitch, wrows, 4);
+                    const uint4 vu[4] = {make_uint4(pdu[0], pdu[1], pdu[2], pdu[3]), make_uint4(pdu[4], pdu[5], pdu[6], pdu[7]),
+                                         make_uint4(pdu[8], pdu[9], pdu[10], pdu[11]), make_uint4(pdu[12], pdu[13], pdu[14], pdu[15])};
+                    warp_store_block(stg4, vu, lane, reinterpret_cast<char*>(p.sg_du + obase + c), opitch, wrows, 4);
+                    const uint4 vh[4] = {make_uint4(phw[0], phw[1], phw[2], phw[3]), make_uint4(phw[4], phw[5], phw[6], phw[7]),
+                                         make_uint4(phw[8], phw[9], phw[10], phw[11]), make_uint4(phw[12], phw[13], phw[14], phw[15])};
+                    warp_store_block(stg4, vh, lane, reinterpret_cast<char*>(p.sg_hw + obase + c), opitch, wrows, 4);
+                    if (((t.n0 + c + 32) & 63) == 0) {
+                        // a 64-column group is complete
+                        if (real && col_ok && p.sg_part != nullptr)
+                            p.sg_part[(arow0 + lane) * p.sg_npart + (t.n0 + c) / 64] = part;
+                        part = 0.0f;
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(acc));
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+                continue;
+            }
             float* cbase = p.C + (p.mode == NT_MSEG ? 0 : t.z * p.c_zs);
 #pragma unroll 1
             for (int c = half * (NBN / 2); c < (half + 1) * (NBN / 2); c += 16) {
@@ -422,6 +522,16 @@ cudaError_t launch_nt_t(const NtGemm& g, cudaStream_t s) {
     p.ldc = g.ldc;
     p.c_zs = g.c_zs;
     p.accumulate = g.accumulate;
+    p.sg_a = g.sg_a;
+    p.sg_u = g.sg_u;
+    p.sg_off = g.sg_off;
+    p.sg_ld = g.sg_ld;
+    p.sg_g = g.sg_g;
+    p.sg_da = g.sg_da;
+    p.sg_du = g.sg_du;
+    p.sg_hw = g.sg_hw;
+    p.sg_part = g.sg_part;
+    p.sg_npart = g.sg_npart;
     p.idesc = idesc_bf16_f32(NBM, NBN, g.b_mn ? 1 : 0) | (g.a_mn ? (1u << 15) : 0u);  // bit 15: A MN-major
     p.err = g.err;
     p.timeout_ns = wait_timeout_ns();
@@ -444,6 +554,13 @@ cudaError_t launch_nt_gemm(const NtGemm& g, cudaStream_t s) {
     if (g.nph < 1 || g.nph > 2 || g.Z < 1 || (g.mode != NT_DENSE && g.Z > MAXSEG))
         return cudaErrorInvalidValue;
     if (g.N % 16 || g.K % NBK) return cudaErrorInvalidValue;
+    if (g.sg_a != nullptr) {
+        // SwiGLU-backward epilogue: BF16 rows of 16-byte aligned 16-column blocks
+        if (!g.sg_u || !g.sg_da || !g.sg_du || !g.sg_hw || g.N % 64 || g.ldc % 8 || g.c_zs % 8 ||
+            g.mode == NT_KSEG || (g.mode == NT_MSEG && (!g.sg_off || g.sg_ld % 8)) ||
+            (g.sg_part != nullptr && g.sg_npart < (g.N + 63) / 64))
+            return cudaErrorInvalidValue;
+    }
     // MN-major operands: whole 64-column strips, no row segments, no B slices
     for (int ph = 0; ph < g.nph; ++ph) {
         if (g.a_mn && (g.mode == NT_MSEG || g.A[ph].rows % 64 || g.A[ph].ld % 8 || g.a_zrow % 64))

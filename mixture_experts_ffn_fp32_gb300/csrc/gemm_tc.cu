@@ -39,6 +39,7 @@
 // its copies and MMAs, frees TMEM and flags the error word.
 #include "common.cuh"
 #include "internal.h"
+#include "warp_stage.cuh"
 
 namespace moe {
 namespace {
@@ -97,6 +98,9 @@ struct TcParams {
     const float* rowscale0;
     const float* addend;
     int add_ld;
+    // TC_SWIGLU: also the gate and up products, BF16 in out's layout (TcGroup)
+    __nv_bfloat16* a_out[2];
+    __nv_bfloat16* u_out[2];
     // TC_SWIGLU_BWD (see TcGroup)
     const float* dh[2];
     int dh_ld[2];
@@ -173,28 +177,6 @@ MOE_DEV Unit decode_unit(int u, const TcParams& p, int total0, const int* s_mtp,
         }
     }
     return t;
-}
-
-// Stores a 32-row x 64-byte block whose row `lane` this lane holds in v[0..3]:
-// through the warp's staging buffer (16-byte chunks XOR-swizzled by row, so
-// both the row-wise writes and the column-wise reads are bank-conflict free),
-// then 4 rows x 64 bytes per store instruction. Rows >= valid_rows and
-// 16-byte chunks >= valid_chunks are not written.
-MOE_DEV void warp_store_block(uint4* stg, const uint4 (&v)[4], int lane, char* row0,
-                              size_t pitch, int valid_rows, int valid_chunks) {
-    const int sw = (lane >> 1) & 3;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) stg[lane * 4 + (c ^ sw)] = v[c];
-    __syncwarp();
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int row = 8 * i + (lane >> 2);
-        const int ch = lane & 3;
-        const uint4 w = stg[row * 4 + (ch ^ ((row >> 1) & 3))];
-        if (row < valid_rows && ch < valid_chunks)
-            *reinterpret_cast<uint4*>(row0 + row * pitch + ch * 16) = w;
-    }
-    __syncwarp();
 }
 
 // The copies one CTA makes for unit t, prepared once per unit: for each
@@ -580,6 +562,29 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
                     const int vch = (N - (t.n0 + c)) / 8;  // valid 16-byte chunks (8 BF16 each)
                     warp_store_block(stg, v, lane, out_rows + static_cast<size_t>(t.out_col0 + c) * 2,
                                      pitch, valid_rows, vch);
+                    if (p.a_out[t.g] != nullptr) {
+                        // the products themselves, kept for the backward pass
+                        const size_t ro = static_cast<size_t>(my_out0 + q * 32) * pitch +
+                                          static_cast<size_t>(t.out_col0 + c) * 2;
+                        uint32_t pa[16], pu[16];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            pa[i] = pack_bf16x2(__uint_as_float(g0[2 * i]), __uint_as_float(g0[2 * i + 1]));
+                            pa[8 + i] = pack_bf16x2(__uint_as_float(g1[2 * i]), __uint_as_float(g1[2 * i + 1]));
+                            pu[i] = pack_bf16x2(__uint_as_float(u0[2 * i]), __uint_as_float(u0[2 * i + 1]));
+                            pu[8 + i] = pack_bf16x2(__uint_as_float(u1[2 * i]), __uint_as_float(u1[2 * i + 1]));
+                        }
+                        const uint4 va[4] = {make_uint4(pa[0], pa[1], pa[2], pa[3]), make_uint4(pa[4], pa[5], pa[6], pa[7]),
+                                             make_uint4(pa[8], pa[9], pa[10], pa[11]),
+                                             make_uint4(pa[12], pa[13], pa[14], pa[15])};
+                        warp_store_block(stg, va, lane, reinterpret_cast<char*>(p.a_out[t.g]) + ro, pitch,
+                                         valid_rows, vch);
+                        const uint4 vu[4] = {make_uint4(pu[0], pu[1], pu[2], pu[3]), make_uint4(pu[4], pu[5], pu[6], pu[7]),
+                                             make_uint4(pu[8], pu[9], pu[10], pu[11]),
+                                             make_uint4(pu[12], pu[13], pu[14], pu[15])};
+                        warp_store_block(stg, vu, lane, reinterpret_cast<char*>(p.u_out[t.g]) + ro, pitch,
+                                         valid_rows, vch);
+                    }
                 }
             } else {
                 float rs = 1.0f;
@@ -789,6 +794,10 @@ cudaError_t launch_tc_t(const TcGemmArgs& a, int nstrip, int slots, cudaStream_t
         p.out[g] = G.out;
         p.out_ld[g] = G.out_ld;
         p.out_f32[g] = G.out_f32;
+        p.a_out[g] = static_cast<__nv_bfloat16*>(G.a_out);
+        p.u_out[g] = static_cast<__nv_bfloat16*>(G.u_out);
+        if ((G.a_out != nullptr) != (G.u_out != nullptr) || (G.a_out && (MODE != TC_SWIGLU || G.out_f32)))
+            return cudaErrorInvalidValue;
         p.dh[g] = G.dh;
         p.dh_ld[g] = G.dh_ld;
         p.da[g] = static_cast<__nv_bfloat16*>(G.da);

@@ -72,6 +72,7 @@ struct WsLayout {
     size_t chunk_counts, chunk_base, counts, offsets, mt_prefix;
     size_t sorted_token, sorted_w, inv;
     size_t xs, z, h, hs, ys, routed, shout, xstage, ostage, qb, w3, rpart;
+    size_t ga, gu, gas, gus;  // saved gate / up products (save_gate_up): routed rows, shared
     size_t logits, stats_part;  // routing diagnostics: r [T, E], per-CTA partial sums
     size_t total;
     int nchunks;
@@ -185,6 +186,10 @@ struct TcGroup {
     int b_rows = 0;     // > 0: B has b_rows rows per matrix (rows beyond read as zero)
     int ksplit = 1;     // group 1 only: split K into ksplit slices; slice s writes the partial
                         // product to out rows [s*rows, (s+1)*rows) (needs Z == 1)
+    // TC_SWIGLU: a_out / u_out (optional, both or neither, BF16 like out): the gate
+    // and up products a = A B0, u = A B1 themselves, in out's rows, columns and pitch.
+    void* a_out = nullptr;
+    void* u_out = nullptr;
     // TC_SWIGLU_BWD: with a, u the gate and up products of row r, column c (the
     // SwiGLU layout of `out`, pitch out_ld), the upstream gradient dh of h
     // (FP32, pitch dh_ld) and the row's gate weight g (group 0: rowscale0,
@@ -315,6 +320,25 @@ struct NtGemm {
     long long ldc, c_zs;
     int accumulate;
     int* err;
+    // SwiGLU-backward epilogue (sg_a set; C unused): the accumulator at output row r,
+    // column c is dh, the gradient of h = SiLU(a) u. With a = sg_a, u = sg_u (BF16
+    // gate and up products; NT_MSEG: row i of segment z read at row sg_off[z] + i
+    // of pitch sg_ld, the segment's rows past sg_off[z+1] - sg_off[z] are padding;
+    // otherwise at the output's own index, pitch ldc) and g = sg_g[that row] (NULL:
+    // 1), writes BF16 da = g dh u SiLU'(a), du = g dh SiLU(a), g h at the output
+    // index (pitch ldc, NT_DENSE slices c_zs apart; zeros on padding rows), and
+    // sg_part[row * sg_npart + c / 64] = the sum of dh h over each 64 columns
+    // (NULL: not written). N a multiple of 64.
+    const __nv_bfloat16* sg_a = nullptr;
+    const __nv_bfloat16* sg_u = nullptr;
+    const int32_t* sg_off = nullptr;
+    long long sg_ld = 0;
+    const float* sg_g = nullptr;
+    __nv_bfloat16* sg_da = nullptr;
+    __nv_bfloat16* sg_du = nullptr;
+    __nv_bfloat16* sg_hw = nullptr;
+    float* sg_part = nullptr;
+    int sg_npart = 0;
 };
 cudaError_t launch_nt_gemm(const NtGemm& g, cudaStream_t s);
 
@@ -346,6 +370,7 @@ struct BwdLayout {
     size_t wrt, cp, rpart;  // W_router^T; router coefficient per padded row; per-64-row partials
     long long tkpad, tpad;
     size_t kpart, kpart_floats;  // split-K partials of the long-reduction CUDA-core products
+    bool saved = false;          // tensor-core form on the forward's saved gate / up products
     size_t total;
 };
 // BF16 layers whose widths are multiples of 64 run the backward's expert

@@ -81,8 +81,8 @@ def _dout(w, seed=7):
     return torch.randn(w.T, w.d, generator=g, dtype=torch.float32).cuda()
 
 
-def run(w):
-    spec = A.LayerSpec.of(w)
+def run(w, save_gate_up=False):
+    spec = A.LayerSpec.of(w, save_gate_up=save_gate_up)
     inp = W.make_inputs(w, device="cuda")
     ws = A.alloc_workspace(spec)
     A.forward(spec, inp["x"], inp, ws=ws)
@@ -106,11 +106,17 @@ def _tc(w):
             and (w.n_shared == 0 or w.shared_d_ff % 64 == 0))
 
 
-@pytest.mark.parametrize("name", list(LAYERS) + list(TC_LAYERS))
-def test_backward_matches_oracle(name):
+CASES = [(n, False) for n in list(LAYERS) + list(TC_LAYERS)] + [(n, True) for n in TC_LAYERS]
+
+
+@pytest.mark.parametrize("name,saved", CASES)
+def test_backward_matches_oracle(name, saved):
+    """saved: the forward kept its BF16 gate and up products (save_gate_up) and
+    the SwiGLU backward runs in the epilogue of the dh products on them; the
+    tensor-core form's bounds hold for it unchanged."""
     w = {**LAYERS, **TC_LAYERS}[name]
     assert _tc(w) == (name in TC_LAYERS)
-    spec, inp, ws, gidx, counts, dout, g = run(w)
+    spec, inp, ws, gidx, counts, dout, g = run(w, save_gate_up=saved)
     ref = O.moe_backward(inp["x"], inp, dout, w.gate, w.K, w.renormalize, w.routed_scale,
                          routing=gidx, latent_rows_bf16=bool(w.latent_dim))
     assert np.array_equal(ref["active"], counts > 0)
@@ -132,6 +138,29 @@ def test_backward_matches_oracle(name):
         if frob is not None:
             fr = float(np.linalg.norm(got - r) / (np.linalg.norm(r) or 1.0))
             assert fr <= frob, f"{name} {n}: relative Frobenius error {fr:.3e} > {frob}"
+
+
+@pytest.mark.parametrize("name", ["tc_topk_shared", "tc_sigmoid_renorm_s2", "tc_latent", "tc_sparse"])
+def test_saved_gate_up_forward_unchanged_and_gradients_agree(name):
+    """Keeping the gate/up products changes no bit of the forward's output; the
+    gradients from the saved BF16 products and from the recomputed FP32 ones
+    agree to well within the bound either keeps against the oracle."""
+    w = TC_LAYERS[name]
+    inp = W.make_inputs(w, device="cuda")
+    dout = _dout(w)
+    outs, grads = [], []
+    for saved in (False, True):
+        spec = A.LayerSpec.of(w, save_gate_up=saved)
+        ws = A.alloc_workspace(spec)
+        outs.append(A.forward(spec, inp["x"], inp, ws=ws).clone())
+        grads.append(A.backward(spec, inp["x"], inp, dout, ws))
+        assert A.workspace_status(ws) == A.MOE_OK
+    assert torch.equal(outs[0].view(torch.int32), outs[1].view(torch.int32))
+    for n in grads[0]:
+        a = torch.nan_to_num(grads[0][n]).double()
+        b = torch.nan_to_num(grads[1][n]).double()
+        fr = float((a - b).norm() / (a.norm() + 1e-30))
+        assert fr <= 5e-3, f"{name} {n}: saved vs recomputed relative Frobenius {fr:.3e}"
 
 
 def test_backward_sparse_case_has_empty_experts():
@@ -159,15 +188,16 @@ FULL = ["small", "medium_prefill", "medium_decode", "large_prefill", "large_pref
         "large_decode", "large_decode_zipf", "latent"]
 
 
-@pytest.mark.parametrize("name", FULL)
-def test_full_size_backward_sampled_rows(name):
+@pytest.mark.parametrize("name,saved", [(n, False) for n in FULL] + [("small", True), ("latent", True)])
+def test_full_size_backward_sampled_rows(name, saved):
     """The benchmark layers at full size: dx on sampled tokens (first, last,
     random, tokens of the rarest experts) against the oracle's backward of
     just those tokens, on the GPU's selection; expert slices of experts
-    without rows stay as given; a second backward gives the same bits."""
+    without rows stay as given; a second backward gives the same bits.
+    saved: on the forward's kept gate/up products."""
     w = W.WORKLOADS[name]
     assert _tc(w)
-    spec, inp, ws, gidx, counts, dout, g = run(w)
+    spec, inp, ws, gidx, counts, dout, g = run(w, save_gate_up=saved)
     rows = P.sample_rows(w, gidx, n=8)
     ref = O.moe_backward(inp["x"], inp, dout, w.gate, w.K, w.renormalize, w.routed_scale,
                          routing=gidx, latent_rows_bf16=bool(w.latent_dim), tokens=rows)
