@@ -309,7 +309,9 @@ moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes);
  * BF16 layers whose d, d_ff, latent_dim and shared_d_ff are multiples of 64
  * run the expert contractions on the tensor cores with BF16 operands (the
  * upstream and activation gradients rounded to BF16, FP32 sums); the others
- * on the CUDA cores in FP32.
+ * on the CUDA cores in FP32. On the tensor cores, cfg->save_gate_up = 1 takes
+ * the gate and up products the forward kept (BF16) instead of recomputing
+ * them; the forward must then have run with save_gate_up = 1 as well.
  *   ws: the forward's workspace (moe_workspace_size bytes, 256-byte aligned).
  *   bws: moe_backward_workspace_size bytes, 256-byte aligned. */
 moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights* w,
