@@ -212,6 +212,9 @@ moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* topk_idx,
  *   x [T, d] (dtype, device), out [T, d] (out_dtype, device).
  *   The routing and dispatch results stay in ws (moe_get_workspace_views).
  *   The balance bias is read, never written (use moe_quantile_bias_update).
+ *   No host synchronisation and no allocation: after a first call on the
+ *   device (which sets kernel attributes), calls can be captured into a CUDA
+ *   graph; so can moe_backward.
  * Sources: APEX-1 Math Ref Part 3 sections 12.2 and 13.2; APEX-1 docs
  * "10 - Mixture of Experts" MoEFFN.forward; kimi_k3 StableLatentMoE
  * "Grouped expert execution" and "Return to model width"; "MoE from scratch"
