@@ -54,6 +54,24 @@ def test_workspace_size_and_validation(api):
         assert ei.value.status in (api.MOE_ERR_INVALID_ARG, api.MOE_ERR_UNSUPPORTED), kw
 
 
+def test_saved_gate_up_workspace(api):
+    """save_gate_up grows the workspace by the BF16 gate and up products of every
+    routed row and shared expert (4 (T K d_ff + T S Fs) bytes, plus at most the
+    four regions' 256-byte alignment) on a layer whose backward runs on the
+    tensor cores, and nowhere else; a value other than 0 or 1 is rejected."""
+    T, K, F, S, Fs = 64, 2, 128, 1, 128
+    base = api.workspace_size(_spec(api))
+    saved = api.workspace_size(_spec(api, save_gate_up=True))
+    grow = 4 * (T * K * F + T * S * Fs)
+    assert grow <= saved - base <= grow + 4 * 256
+    for kw in (dict(dtype="f32"), dict(d_ff=96)):  # CUDA-core backward: nothing kept
+        assert api.workspace_size(_spec(api, save_gate_up=True, **kw)) == api.workspace_size(_spec(api, **kw))
+    cfg = _spec(api).config()
+    cfg.save_gate_up = 2
+    n = ctypes.c_size_t(0)
+    assert api.lib().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == api.MOE_ERR_INVALID_ARG
+
+
 def test_status_strings_and_metadata(api):
     L = api.lib()
     assert L.moe_version().decode().count(".") == 2
