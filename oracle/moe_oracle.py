@@ -29,7 +29,7 @@ Sources, cited as page title + section:
 * [BOOK-MoE] book-ai "Mixture of Experts" chapter, class ``MoELoss``:
   ``router_z_loss`` (ST-MoE z-loss).
 
-Readings where the pages are silent or disagree (each is listed in the design doc):
+Readings where the pages are silent or disagree:
 ties in top-K go to the lower expert index; slot k holds the k-th largest
 score; in the softmax modes the balance bias is added to the logits before
 the score; the quantile rank is computed in FP32 as the FP32 quantile would;
