@@ -196,11 +196,16 @@ moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const fl
  * T*K <= 65536 and E <= 256 (about 130 KB, held by every GPU that loads the
  * library until the process exits); larger calls return MOE_ERR_UNSUPPORTED.
  * The first call on each device looks up the array's device address with
- * that device current; make that first call before any stream capture.
+ * that device current; make that first call before any stream capture. The
+ * address is kept per device and context: after cudaDeviceReset (or anything
+ * else that makes a new context) the next call looks it up again, so make
+ * that call before any capture too.
  * Every call reuses the same array, so calls that overlap on the GPU (for
  * example on two streams with no ordering between them) race and corrupt
  * each other's results; order such calls on one stream. Expert ids outside
- * [0, E) are skipped and not reported. Calls no allocating function. */
+ * [0, E) are skipped, the other assignments dispatched as moe_dispatch does;
+ * the caller detects skipped ids by offsets[E] falling short of T*K by their
+ * number. Calls no allocating function. */
 moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* topk_idx,
                                 const float* topk_w, int32_t* counts, int32_t* offsets,
                                 int32_t* sorted_token, float* sorted_w, int32_t* inv,

@@ -34,11 +34,42 @@ constexpr size_t NOALLOC_WORDS =
 
 static __device__ __align__(256) int32_t g_dispatch_scratch[NOALLOC_WORDS];
 
-// Device address of the array, looked up once per device with that device
-// current (in host code the symbol is only a stand-in for the address).
+// Identity of the current context: its process-unique id (cuCtxGetId), so
+// that a context destroyed and made again (cudaDeviceReset, for one) is seen
+// as new even if its handle value comes back. Driver entry points are taken
+// through the runtime; the library does not link libcuda.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+bool current_context_id(unsigned long long* id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+        return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the array, looked up once per device and context with
+// that device current (in host code the symbol is only a stand-in for the
+// address). The lookup is redone when the device's context is not the one the
+// cached address was taken in.
 int32_t* scratch_address(cudaError_t* err) {
     static std::mutex mu;
     static int32_t* addr[64] = {};
+    static unsigned long long ctx_of[64] = {};
     int dev = 0;
     *err = cudaGetDevice(&dev);
     if (*err != cudaSuccess) return nullptr;
@@ -46,12 +77,22 @@ int32_t* scratch_address(cudaError_t* err) {
         *err = cudaErrorInvalidDevice;
         return nullptr;
     }
+    // cudaSetDevice makes the device's primary context current (and creates it
+    // if no call has yet)
+    *err = cudaSetDevice(dev);
+    if (*err != cudaSuccess) return nullptr;
+    unsigned long long ctx = 0;
+    if (!current_context_id(&ctx)) {
+        *err = cudaErrorDeviceUninitialized;
+        return nullptr;
+    }
     std::lock_guard<std::mutex> lk(mu);
-    if (addr[dev] == nullptr) {
+    if (addr[dev] == nullptr || ctx_of[dev] != ctx) {
         void* p = nullptr;
         *err = cudaGetSymbolAddress(&p, g_dispatch_scratch);
         if (*err != cudaSuccess) return nullptr;
         addr[dev] = static_cast<int32_t*>(p);
+        ctx_of[dev] = ctx;
     }
     return addr[dev];
 }

@@ -109,8 +109,14 @@ WORKLOADS: dict[str, Workload] = {
                        shared_d_ff=2048, dtype="bf16", gate=GATE_SIGMOID, latent_dim=512),
 }
 
-# The single-GPU throughput workload (the APEX-small-like layer).
-BENCH_WORKLOAD = "small"
+# The single-GPU throughput workload: the largest configuration, the
+# APEX-large-like prefill batch (T=8192, d=4096, d_ff=2048, 256 experts, top-8,
+# two shared experts).
+BENCH_WORKLOAD = "large_prefill"
+
+# Every configuration, in the order the bench reports them.
+ALL_BENCH = ["tiny_f32", "small", "medium_prefill", "medium_decode", "large_prefill",
+             "large_prefill_zipf", "large_decode", "large_decode_zipf", "latent"]
 
 
 def _seed(base: int, *parts) -> int:
@@ -143,6 +149,29 @@ def _expert_stack(n, shape, std, device, dtype, base, name) -> torch.Tensor:
     return out
 
 
+def _stack_geometry(w: Workload, which: str):
+    """(shape of one matrix, std, seed name) of an expert stack of make_inputs."""
+    de = w.d_expert
+    S, Fs = w.n_shared, w.shared_d_ff
+    geo = {
+        "W_gate": ((de, w.d_ff), 1.0 / math.sqrt(de)),
+        "W_up": ((de, w.d_ff), 1.0 / math.sqrt(de)),
+        "W_down": ((w.d_ff, de), 1.0 / math.sqrt(w.d_ff)),
+        "Ws_gate": ((w.d, Fs), 1.0 / math.sqrt(w.d) if S else 1.0),
+        "Ws_up": ((w.d, Fs), 1.0 / math.sqrt(w.d) if S else 1.0),
+        "Ws_down": ((Fs, w.d), 1.0 / math.sqrt(Fs) if S else 1.0),
+    }
+    shape, std = geo[which]
+    return shape, std, w.name + "/" + which
+
+
+def expert_matrix(w: Workload, which: str, e: int, device="cpu", seed: int = 0) -> torch.Tensor:
+    """Matrix e of the expert stack `which` (W_gate, W_up, W_down, Ws_*) alone:
+    the same values as make_inputs(w, device, seed)[which][e]."""
+    shape, std, name = _stack_geometry(w, which)
+    return _normal(shape, std, device, torch_dtype(w), seed, name, e)
+
+
 def make_bias(w: Workload, seed: int = 0) -> torch.Tensor | None:
     """Balance bias [E] FP32 on the CPU (None when the workload has none)."""
     if not w.has_bias:
@@ -160,13 +189,16 @@ def make_bias(w: Workload, seed: int = 0) -> torch.Tensor | None:
     return b
 
 
-def make_inputs(w: Workload, device="cpu", seed: int = 0, with_x: bool = True) -> dict:
+def make_inputs(w: Workload, device="cpu", seed: int = 0, with_x: bool = True,
+                routed_experts: bool = True) -> dict:
     """All tensors of one forward, row-major and contiguous.
 
     x [T, d]; W_router [d, E] FP32; bias [E] FP32 or None;
     W_gate, W_up [E, d_e, d_ff]; W_down [E, d_ff, d_e] (d_e = d, or L when latent);
     Ws_gate, Ws_up [S, d, Fs]; Ws_down [S, Fs, d];
     W_down_latent [d, L], W_up_latent [L, d] when latent.
+    routed_experts=False leaves W_gate, W_up, W_down out (expert_matrix makes
+    any one of them on its own).
     """
     dt = torch_dtype(w)
     de = w.d_expert
@@ -177,20 +209,15 @@ def make_inputs(w: Workload, device="cpu", seed: int = 0, with_x: bool = True) -
                             seed, w.name, "W_router")
     b = make_bias(w, seed)
     t["bias"] = None if b is None else b.to(device)
-    t["W_gate"] = _expert_stack(w.E, (de, w.d_ff), 1.0 / math.sqrt(de), device, dt, seed,
-                                w.name + "/W_gate")
-    t["W_up"] = _expert_stack(w.E, (de, w.d_ff), 1.0 / math.sqrt(de), device, dt, seed,
-                              w.name + "/W_up")
-    t["W_down"] = _expert_stack(w.E, (w.d_ff, de), 1.0 / math.sqrt(w.d_ff), device, dt,
-                                seed, w.name + "/W_down")
-    S, Fs = w.n_shared, w.shared_d_ff
+    names = (("W_gate", "W_up", "W_down") if routed_experts else ())
+    for which in names:
+        shape, std, name = _stack_geometry(w, which)
+        t[which] = _expert_stack(w.E, shape, std, device, dt, seed, name)
+    S = w.n_shared
     if S:
-        t["Ws_gate"] = _expert_stack(S, (w.d, Fs), 1.0 / math.sqrt(w.d), device, dt, seed,
-                                     w.name + "/Ws_gate")
-        t["Ws_up"] = _expert_stack(S, (w.d, Fs), 1.0 / math.sqrt(w.d), device, dt, seed,
-                                   w.name + "/Ws_up")
-        t["Ws_down"] = _expert_stack(S, (Fs, w.d), 1.0 / math.sqrt(Fs), device, dt, seed,
-                                     w.name + "/Ws_down")
+        for which in ("Ws_gate", "Ws_up", "Ws_down"):
+            shape, std, name = _stack_geometry(w, which)
+            t[which] = _expert_stack(S, shape, std, device, dt, seed, name)
     else:
         t["Ws_gate"] = t["Ws_up"] = t["Ws_down"] = None
     if w.latent_dim:

@@ -356,22 +356,36 @@ def moe_forward(x, params, gate, K, renormalize=False, routed_scale=1.0,
     return out, rt
 
 
-def moe_forward_sorted(x, params, gate, K, renormalize=False, routed_scale=1.0):
-    """Second formulation used only to cross-check the per-token one: group the
-    assignments with dispatch(), run each expert once on its contiguous block,
-    weight the rows, and scatter-add them back to their tokens
-    ([MoE-FS] MoELayer.forward; [K3-SLM] grouped execution semantics)."""
+def moe_forward_sorted(x, params, gate, K, renormalize=False, routed_scale=1.0,
+                       tokens=None, routing=None):
+    """Second formulation of the same layer: group the assignments with
+    dispatch(), run each expert once on its contiguous block of rows, weight
+    the rows, and scatter-add them back to their tokens ([MoE-FS]
+    MoELayer.forward; [K3-SLM] grouped execution semantics). Pinned equal to
+    the per-token form; it reads each expert's weights once, which makes
+    whole large layers affordable on the CPU.
+
+    ``tokens`` and ``routing`` work as in moe_forward: only the listed rows are
+    computed (the others are NaN), and ``routing`` = (idx [T, K], w [T, K])
+    replaces the oracle's own routing. Returns out [T, d] float64.
+    """
     xn = f64(_to_np(x))
     T = xn.shape[0]
-    rt = route(xn, _to_np(params["W_router"]), _to_np(params.get("bias")), gate, K,
+    sub = np.arange(T, dtype=np.int64) if tokens is None else np.asarray(list(tokens), np.int64)
+    rt = route(xn[sub], _to_np(params["W_router"]), _to_np(params.get("bias")), gate, K,
                renormalize, routed_scale)
+    idx, w = rt["idx"], rt["w"]
+    if routing is not None:
+        idx = np.asarray(routing[0])[sub]
+        w = f64(np.asarray(routing[1])[sub])
     E = params["W_gate"].shape[0]
-    dp = dispatch(rt["idx"], E)
+    dp = dispatch(idx, E)
     cache = _WeightCache(params)
     latent = params.get("W_down_latent") is not None
-    z = xn @ cache.get("W_down_latent") if latent else xn
+    xsub = xn[sub]
+    z = xsub @ cache.get("W_down_latent") if latent else xsub
     xs = z[dp["sorted_token"]]
-    ws = rt["w"].reshape(-1)[dp["order"]]
+    ws = w.reshape(-1)[dp["order"]]
     ys = np.zeros_like(xs)
     for e in range(E):
         a, b = dp["offsets"][e], dp["offsets"][e + 1]
@@ -383,12 +397,14 @@ def moe_forward_sorted(x, params, gate, K, renormalize=False, routed_scale=1.0):
     np.add.at(routed, dp["sorted_token"], ys)
     if latent:
         routed = routed @ cache.get("W_up_latent")
-    shared = np.zeros_like(xn)
+    shared = np.zeros_like(xsub)
     if params.get("Ws_gate") is not None:
         for s in range(params["Ws_gate"].shape[0]):
-            shared = shared + swiglu_ffn(xn, cache.get("Ws_gate", s), cache.get("Ws_up", s),
+            shared = shared + swiglu_ffn(xsub, cache.get("Ws_gate", s), cache.get("Ws_up", s),
                                          cache.get("Ws_down", s))
-    return shared + routed
+    out = np.full((T, xn.shape[1]), np.nan)
+    out[sub] = shared + routed
+    return out
 
 
 # --------------------------------------------------------------------------

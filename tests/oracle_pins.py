@@ -262,6 +262,15 @@ def pin_sorted_equals_naive(o):
         a, _ = o.moe_forward(x, p, gate, K)
         b = o.moe_forward_sorted(x, p, gate, K)
         np.testing.assert_allclose(a, b, atol=1e-12, rtol=0)
+        # a subset of rows, in any order, under an adopted selection: the same
+        # rows, NaN elsewhere
+        rows = [30, 2, 17, 5, 36]
+        idx = np.stack([rng.permutation(E)[:K] for _ in range(T)])
+        wts = rng.uniform(0.1, 1.0, size=(T, K))
+        a, _ = o.moe_forward(x, p, gate, K, tokens=rows, routing=(idx, wts))
+        b = o.moe_forward_sorted(x, p, gate, K, tokens=rows, routing=(idx, wts))
+        assert np.isnan(b[[0, 1, 3]]).all()
+        np.testing.assert_allclose(a[rows], b[rows], atol=1e-12, rtol=0)
 
 
 def pin_shared_concat_identity(o):

@@ -117,25 +117,44 @@ def run_forward(w: W.Workload, inputs, stream=None):
     return out, views, ws
 
 
-def sample_rows(w, gpu_idx, n=12, seed=0):
-    """First, last, random tokens and tokens routed to the rarest used experts."""
+def sample_rows(w, gpu_idx, offsets=None, sorted_token=None, n_even=512, n_rare=8,
+                n_tile_experts=4, seed=0):
+    """Rows for a sampled comparison: n_even evenly spaced tokens (with the
+    first and last), every token routed to the n_rare least-used experts that
+    get any, and, for n_tile_experts experts (the most and least loaded of
+    those with rows, and random others), the tokens at the first and last row
+    of each of their 128-row and 256-row tiles in the expert-sorted order."""
     rng = np.random.default_rng(seed)
     T = w.T
     rows = {0, T - 1}
-    rows.update(int(v) for v in rng.choice(T, size=min(T, n // 2), replace=False))
+    rows.update(int(v) for v in np.linspace(0, T - 1, num=min(T, n_even)).round())
     counts = np.bincount(gpu_idx.reshape(-1), minlength=w.E)
     used = np.where(counts > 0)[0]
-    rare = used[np.argsort(counts[used], kind="stable")][: max(1, n // 4)]
-    for e in rare:
-        t = int(np.where((gpu_idx == e).any(axis=1))[0][0])
-        rows.add(t)
-    return sorted(rows)[: n + 4]
+    by_load = used[np.argsort(counts[used], kind="stable")]
+    for e in by_load[:n_rare]:
+        rows.update(int(t) for t in np.where((gpu_idx == e).any(axis=1))[0])
+    if offsets is not None and sorted_token is not None and used.size:
+        pick = [int(by_load[-1]), int(by_load[0])]
+        rest = [int(e) for e in used if e not in pick]
+        if rest:
+            pick += [int(e) for e in rng.choice(rest, size=min(len(rest), n_tile_experts - 2),
+                                               replace=False)]
+        for e in pick:
+            a, b = int(offsets[e]), int(offsets[e + 1])
+            for h in (128, 256):
+                for s0 in range(a, b, h):
+                    rows.add(int(sorted_token[s0]))
+                    rows.add(int(sorted_token[min(s0 + h, b) - 1]))
+    return sorted(rows)
 
 
-def full_parity(w: W.Workload, device="cuda", sample=None):
+def full_parity(w: W.Workload, device="cuda", sample=False, record=None):
     """Forward on the GPU, then: routing bit-exact on all tokens (outside near
-    ties), dispatch bit-exact on all assignments, outputs vs the oracle on all
-    rows (sample=None) or a sampled row set."""
+    ties), dispatch bit-exact on all assignments, outputs against the oracle
+    on every row (sample=False) or on sample_rows' set (sample=True). The
+    oracle's expert-grouped form (pinned equal to its per-token form) keeps
+    whole large layers affordable. ``record``: a path that gets one JSON line
+    with the counts and errors."""
     inputs = W.make_inputs(w, device=device)
     out, views, ws = run_forward(w, inputs)
     torch.cuda.synchronize()
@@ -144,13 +163,20 @@ def full_parity(w: W.Workload, device="cuda", sample=None):
     idx, wts, near = merge_routing(w, inputs, ort, gi)
     check_routing(w, ort, views, near)
     # dispatch of the oracle's routing (GPU selection only at near ties), bit for bit
-    check_dispatch(w, idx, views["w"].detach().cpu().numpy().reshape(-1), views)
-    rows = None if sample is None else sample_rows(w, gi, n=sample)
-    ref, _ = O.moe_forward(inputs["x"], inputs, w.gate, w.K, w.renormalize, w.routed_scale,
-                           tokens=rows, routing=(idx, wts))
+    dp = check_dispatch(w, idx, views["w"].detach().cpu().numpy().reshape(-1), views)
+    rows = sample_rows(w, gi, dp["offsets"], dp["sorted_token"]) if sample else None
+    ref = O.moe_forward_sorted(inputs["x"], inputs, w.gate, w.K, w.renormalize,
+                               w.routed_scale, tokens=rows, routing=(idx, wts))
     err, rms = check_output(w, out, ref, rows)
-    res = {"near_ties": int(near.sum()), "max_err": err, "rms": rms,
-           "rows": w.T if rows is None else len(rows)}
+    res = {"workload": w.name, "T": w.T, "near_ties": int(near.sum()),
+           "near_ties_at_selection": int((ort["margin"] <= NEAR_TIE).sum()),
+           "max_err": err, "rms": rms, "max_err_over_rms": None if rms is None else err / rms,
+           "rows": w.T if rows is None else len(rows),
+           "empty_experts": int((dp["counts"] == 0).sum())}
+    if record:
+        import json
+        with open(record, "a") as f:
+            f.write(json.dumps(res) + "\n")
     del inputs, out, views, ws
     torch.cuda.empty_cache()
     return res

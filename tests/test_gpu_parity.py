@@ -1,9 +1,11 @@
 """GPU parity of the CUDA path (through the C ABI) against the CPU oracle.
 
-Small cases are compared element by element on every output row; the
-configurations at full size are compared on sampled rows, with routing and
-dispatch checked on every token. Tolerances are in tests/parity.py.
+Small cases and the configurations at full size are compared element by
+element on every output row, with routing and dispatch checked on every
+token. Tolerances are in tests/parity.py.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -134,9 +136,21 @@ FULL = ["small", "medium_prefill", "medium_decode", "large_prefill", "large_pref
 
 
 @pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled_rows(name):
-    res = P.full_parity(W.WORKLOADS[name], sample=12)
+def test_full_size_all_rows(name):
+    """Every benchmark configuration at full size, every output row against the
+    oracle (its expert-grouped form). MOE_PARITY_RECORD names a file that gets
+    one JSON line per layer (near-tie count, max error, RMS, rows)."""
+    res = P.full_parity(W.WORKLOADS[name], record=os.environ.get("MOE_PARITY_RECORD"))
     print(name, res)
+
+
+def test_sampled_rows_cover_tiles_and_rare_experts():
+    """The sampled row set used where every row would cost too much: evenly
+    spaced tokens, every token of the rarest experts, tile boundaries."""
+    w = W.WORKLOADS["large_prefill_zipf"]
+    res = P.full_parity(w, sample=True)
+    assert res["rows"] >= 512, res
+    print(res)
 
 
 # ---------------------------------------------------------------------------
