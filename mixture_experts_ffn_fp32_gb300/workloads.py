@@ -109,6 +109,16 @@ WORKLOADS: dict[str, Workload] = {
                        shared_d_ff=2048, dtype="bf16", gate=GATE_SIGMOID, latent_dim=512),
 }
 
+# Reduced copies of the large layers for profiler captures that must stay at a
+# few GB of device memory: the same widths and the same rows per expert
+# (T*K/E = 256), an eighth of the experts and tokens.
+PROFILE_CASES: dict[str, Workload] = {
+    "large_prefill_e32": replace(WORKLOADS["large_prefill"], name="large_prefill_e32", T=1024,
+                                 E=32),
+    "large_decode_e32": replace(WORKLOADS["large_decode"], name="large_decode_e32", E=32),
+}
+WORKLOADS.update(PROFILE_CASES)
+
 # The single-GPU throughput workload: the largest configuration, the
 # APEX-large-like prefill batch (T=8192, d=4096, d_ff=2048, 256 experts, top-8,
 # two shared experts).

@@ -118,12 +118,13 @@ def run_forward(w: W.Workload, inputs, stream=None):
 
 
 def sample_rows(w, gpu_idx, offsets=None, sorted_token=None, n_even=512, n_rare=8,
-                n_tile_experts=4, seed=0):
+                n_tile_experts=4, seed=0, rare_cap=None):
     """Rows for a sampled comparison: n_even evenly spaced tokens (with the
     first and last), every token routed to the n_rare least-used experts that
     get any, and, for n_tile_experts experts (the most and least loaded of
     those with rows, and random others), the tokens at the first and last row
-    of each of their 128-row and 256-row tiles in the expert-sorted order."""
+    of each of their 128-row and 256-row tiles in the expert-sorted order.
+    rare_cap: at most that many tokens of each rare expert (all if None)."""
     rng = np.random.default_rng(seed)
     T = w.T
     rows = {0, T - 1}
@@ -132,7 +133,7 @@ def sample_rows(w, gpu_idx, offsets=None, sorted_token=None, n_even=512, n_rare=
     used = np.where(counts > 0)[0]
     by_load = used[np.argsort(counts[used], kind="stable")]
     for e in by_load[:n_rare]:
-        rows.update(int(t) for t in np.where((gpu_idx == e).any(axis=1))[0])
+        rows.update(int(t) for t in np.where((gpu_idx == e).any(axis=1))[0][:rare_cap])
     if offsets is not None and sorted_token is not None and used.size:
         pick = [int(by_load[-1]), int(by_load[0])]
         rest = [int(e) for e in used if e not in pick]

@@ -224,7 +224,7 @@ def test_full_size_backward_sampled_rows(name, saved):
     w = W.WORKLOADS[name]
     assert _tc(w)
     spec, inp, ws, gidx, counts, dout, g = run(w, save_gate_up=saved)
-    rows = P.sample_rows(w, gidx, n_even=8, n_rare=2)
+    rows = P.sample_rows(w, gidx, n_even=8, n_rare=2, rare_cap=4)
     ref = O.moe_backward(inp["x"], inp, dout, w.gate, w.K, w.renormalize, w.routed_scale,
                          routing=gidx, latent_rows_bf16=bool(w.latent_dim), tokens=rows)
     got = g["dx"][rows].detach().cpu().numpy().astype(np.float64)
