@@ -57,6 +57,7 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-backward", action="store_true", help="skip the timed backward pass")
+    p.add_argument("--no-diag", action="store_true", help="skip the routing diagnostics pass")
     p.add_argument("--no-workloads", action="store_true",
                    help="skip the per-configuration block")
     p.add_argument("--workload-steps", type=int, default=10)
@@ -654,7 +655,7 @@ def run_ours(args, name):
     # pass, outside the timed forward region
     diag = None
     bwd = None
-    if world == 1:
+    if world == 1 and not args.no_diag:
         dws = api.alloc_workspace(layer.spec)
         x, Wr, b = layer.inp["x"], layer.inp["W_router"], layer.inp["bias"]
         api.routing_stats(layer.spec, x, Wr, b, ws=dws, stream=stream)
@@ -673,6 +674,7 @@ def run_ours(args, name):
                 "note": "moe_routing_stats (router + diagnostics reduction) timed alone with "
                         "CUDA events, L2 flushed before each call"}
         del dws
+    if world == 1:
         if not args.no_backward:
             bwd = time_backward(api, W, layer, dev, stream, flush, max(1, min(args.steps, 5)), pk)
 
