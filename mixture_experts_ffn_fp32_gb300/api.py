@@ -471,7 +471,8 @@ def selftest_wait_timeout(ms: int, ws: torch.Tensor, stream=None) -> int:
     return lib().moe_selftest_wait_timeout(int(ms), ws.data_ptr(), _stream(stream))
 
 
-STAGES = ["router", "latent_down", "dispatch", "gather", "gate_up", "down", "combine", "latent_up"]
+STAGES = ["router", "latent_down", "dispatch", "gather", "gate_up", "down", "combine", "latent_up",
+          "decode_fused"]
 
 
 class StageTimer:

@@ -110,24 +110,48 @@ bool router_on_tensor_cores(const moe_config& c) {
     return c.dtype == MOE_BF16 && c.E > 32 && c.E % 8 == 0 && c.d % ROUTER_CHUNK == 0;
 }
 
-// Up to 512 tokens and 128 experts the chunked FP32 router (two launches, no
-// split weights written, many CTAs even for a decode batch) is as fast as the
-// tensor-core router (three launches). With 256 experts its logit-sum kernel,
-// one warp per token over 8 experts x d/64 slices per lane, is the slower one.
-bool router_chunked(const moe_config& c) { return c.E > 32 && c.E <= 128 && c.T <= 512; }
+// Up to 512 tokens the FP32 cluster router (one launch; slices of d summed
+// through distributed shared memory) is faster than the tensor-core router
+// (three launches): up to 128 experts with W_router slices in shared memory,
+// up to 256 reading them from global memory. (Where a slice of x and
+// W_router would not fit shared memory, the chunked two-launch form runs.)
+bool router_chunked(const moe_config& c) { return c.E > 32 && c.E <= 256 && c.T <= 512; }
 
+// Partial slices of the tensor-core router: each slice is a run of whole
+// ROUTER_CHUNK-long chunks of d, and the GEMM adds a slice's chunks in FP32 in
+// its epilogue. The count minimises the chunks the busiest SM reduces (units
+// = 128-token row tiles x slices, spread over 152 SMs) plus a quarter chunk
+// per slice for writing and reading the partial logits: the 8192-token
+// layers take 2.
 int router_ksplit(int T, int d) {
-    (void)T;
-    return d / ROUTER_CHUNK;
+    const int chunks = d / ROUTER_CHUNK;
+    const int tiles = (T + TC_BM - 1) / TC_BM;
+    int best = 1;
+    double best_cost = 1e30;
+    for (int sl = 1; sl <= chunks; ++sl) {
+        const int per = (chunks + sl - 1) / sl;
+        const int real = (chunks + per - 1) / per;
+        if (real != sl) continue;
+        const int rounds = (tiles * sl + 151) / 152;
+        const double cost = static_cast<double>(rounds) * per + 0.25 * sl;
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = sl;
+        }
+    }
+    return best;
 }
 
 // The router GEMM: x [T, d] against the chunk-interleaved split weights W3
-// [3d, E]; reduction k-block kb reads x k-block (kb / 12) * 4 + kb % 4.
+// [3d, E]; reduction k-block kb reads x k-block (kb / 12) * 4 + kb % 4; each
+// chunk of 12 k-blocks (the lo, mid and hi parts of 256 rows of W_router)
+// accumulates in tensor memory on its own.
 static TcGroup router_group(const void* x, int T, int d, int E, void* w3, void* rpart) {
     TcGroup g{1, 3 * d, x, d, T, w3, nullptr, 1, E, rpart, E, 1};
     g.a_kgroup = ROUTER_CHUNK / 64;
     g.a_krep = 3;
-    g.ksplit = d / ROUTER_CHUNK;
+    g.ksplit = router_ksplit(T, d);
+    g.kchunk = 3 * ROUTER_CHUNK / 64;
     return g;
 }
 
@@ -187,6 +211,7 @@ WsLayout plan_workspace(const moe_config& c) {
     L.rpart = (tcr || chk) ? take(nsplit * T * E * 4) : 0;
     L.logits = take(T * E * 4);
     L.stats_part = take(((T + STATS_TOKENS - 1) / STATS_TOKENS) * (2 * E + 1) * 4);
+    L.dctr = take((E + 2) * 4);
     L.total = o;
     return L;
 }
@@ -195,9 +220,10 @@ WsLayout plan_workspace(const moe_config& c) {
 // Stage timing (instrumentation)
 // ---------------------------------------------------------------------------
 enum Stage { ST_ROUTE = 0, ST_LATENT_DOWN, ST_DISPATCH, ST_GATHER, ST_GATEUP, ST_DOWN, ST_COMBINE,
-             ST_LATENT_UP, ST_COUNT };
+             ST_LATENT_UP, ST_FUSED, ST_COUNT };
 static const char* kStageNames[ST_COUNT] = {"router", "latent_down", "dispatch", "gather",
-                                            "gate_up", "down", "combine", "latent_up"};
+                                            "gate_up", "down", "combine", "latent_up",
+                                            "decode_fused"};
 
 struct Timing {
     std::mutex mu;
@@ -284,6 +310,15 @@ static RouterArgs router_args(const moe_config& c, const void* x, const float* W
     return ra;
 }
 
+// A decode batch of a BF16 layer without latent projection (at most 128
+// tokens, the router in one launch) runs everything after the router in one
+// persistent launch (decode_fused.cu): two launches for the whole forward.
+static bool decode_fused(const moe_config& c) {
+    return c.dtype == MOE_BF16 && c.latent_dim == 0 && !c.save_gate_up &&
+           decode_fused_shape_ok(c.T, c.d, c.d_ff, c.E, c.K, c.n_shared, c.n_shared ? c.shared_d_ff : 0) &&
+           router_one_launch(c.T, c.d, c.E, 1);
+}
+
 // Enqueue the whole forward on s. x and out are device pointers.
 static moe_status forward_impl(const moe_config& c, const void* x, const moe_weights& w, void* out,
                                uint8_t* ws, cudaStream_t s) {
@@ -331,11 +366,37 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
     ra.margin = static_cast<float*>(P(L.margin));
     ra.top_scores = L.top_scores ? static_cast<float*>(P(L.top_scores)) : nullptr;
     ra.scores = L.scores ? static_cast<float*>(P(L.scores)) : nullptr;
+    const bool fused = decode_fused(c);
+    if (fused) {
+        ra.zero = static_cast<unsigned*>(P(L.dctr));
+        ra.nzero = E + 2;
+    }
     {
         const moe_status rs = run_router(c, ra, static_cast<const float*>(w.W_router), x, ws, L, s);
         if (rs != MOE_OK) return rs;
     }
     rec.end(ST_ROUTE);
+
+    if (fused) {
+        // 2. everything else in one launch
+        rec.begin(ST_FUSED);
+        DecodeArgs a{};
+        a.T = T; a.d = c.d; a.F = c.d_ff; a.E = E; a.K = K; a.S = S; a.Fs = S ? Fs : 0;
+        a.x = x; a.idx = idx; a.w = tw;
+        a.W_gate = w.W_gate; a.W_up = w.W_up; a.W_down = w.W_down;
+        a.Ws_gate = w.Ws_gate; a.Ws_up = w.Ws_up; a.Ws_down = w.Ws_down;
+        a.counts = da.counts; a.offsets = offsets; a.mt_prefix = mt_prefix;
+        a.sorted_token = sorted_token; a.sorted_w = sorted_w; a.inv = inv;
+        a.xs = P(L.xs); a.h = P(L.h); a.hs = S ? P(L.hs) : nullptr;
+        a.ys = static_cast<float*>(P(L.ys));
+        a.shout = S ? static_cast<float*>(P(L.shout)) : nullptr;
+        a.out = out; a.out_f32 = of32;
+        a.ctr = static_cast<unsigned*>(P(L.dctr));
+        a.err = err;
+        if ((e = launch_decode_fused(a, s)) != cudaSuccess) return cuda_status(e);
+        rec.end(ST_FUSED);
+        return MOE_OK;
+    }
 
     // 1b. latent compression z = x W_down_latent (once per token)
     const void* ex_src = x;  // rows the routed experts act on

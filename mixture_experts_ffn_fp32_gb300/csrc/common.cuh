@@ -151,6 +151,36 @@ MOE_DEV bool bounded_wait(uint32_t bar, uint32_t parity, const WaitCtx& w, bool 
     }
 }
 
+// Global counters that CTAs of one launch release to each other: the writer
+// orders its stores (generic proxy) before the async proxy and the counter,
+// the reader acquires the counter and orders it before its tensor-map copies.
+MOE_DEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+MOE_DEV unsigned ld_acquire_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+MOE_DEV void release_add_gpu(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Wait until *p >= target (bounded like bounded_wait).
+MOE_DEV bool bounded_wait_count(const unsigned* p, unsigned target, const WaitCtx& w) {
+    if (ld_acquire_gpu(p) >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (ld_acquire_gpu(p) >= target) return true;
+        if (*w.abort) return false;
+        if (globaltimer_ns() - t0 > w.timeout_ns) {
+            *w.abort = 1;
+            atomicOr(w.err, ERRBIT_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 // Same, ignoring the abort flag (used to drain copies already in flight).
 MOE_DEV bool bounded_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns, int* err) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -205,6 +235,18 @@ MOE_DEV void tma_load_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1, i
         "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
+// Row gather: four rows r0..r3 of the column box at c0 of a 2-D tensor map
+// whose box is one row high; they land as four consecutive box rows at dst
+// (swizzled by their shared-memory address like a tiled copy of 4 rows).
+MOE_DEV void tma_gather4(uint32_t dst, const CUtensorMap* map, int c0, int r0, int r1, int r2, int r3,
+                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
         : "memory");
 }
 

@@ -21,37 +21,49 @@
 namespace moe {
 namespace {
 
+// Scratch of dispatch_block_impl: NG x EMAX per-group counts and EMAX offsets.
+template <int EMAX>
+struct DispatchScratch {
+    int wcnt[DISPATCH_CHUNK / 32][EMAX];
+    int off[EMAX];
+};
+
 // idx and w are read through L2. EMAX: a multiple of 32 that is at least E.
+// The calling threads are tid = 0 .. NT-1 (whole warps, tid 0 starting a warp)
+// of a group that sync() synchronises; sc is their shared scratch.
 // write_out: write counts, offsets, mt_prefix, sorted_token, sorted_w and inv;
-// tok_local (optional): gets sorted_token too (e.g. in shared memory).
-template <int NT, int EMAX>
-MOE_DEV void dispatch_block(const int32_t* idx, const float* w, int TK, int K, int E, int bm,
-                            bool write_out, int32_t* __restrict__ counts,
-                            int32_t* __restrict__ offsets, int32_t* __restrict__ mt_prefix,
-                            int32_t* __restrict__ sorted_token, float* __restrict__ sorted_w,
-                            int32_t* __restrict__ inv, int* err, int32_t* tok_local = nullptr) {
+// tok_local / w_local / inv_local (optional): get sorted_token, sorted_w and
+// inv too (e.g. in shared memory), and off_local the E + 1 offsets.
+template <int NT, int EMAX, typename Sync>
+MOE_DEV void dispatch_block_impl(int tid, Sync sync, DispatchScratch<EMAX>& sc, const int32_t* idx,
+                                 const float* w, int TK, int K, int E, int bm, bool write_out,
+                                 int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                 int32_t* __restrict__ mt_prefix, int32_t* __restrict__ sorted_token,
+                                 float* __restrict__ sorted_w, int32_t* __restrict__ inv, int* err,
+                                 int32_t* tok_local, float* w_local = nullptr,
+                                 int32_t* inv_local = nullptr, int32_t* off_local = nullptr) {
     constexpr int ROUNDS = DISPATCH_CHUNK / NT;
     constexpr int NG = DISPATCH_CHUNK / 32;  // groups of 32 consecutive assignments
     constexpr int EPL = EMAX / 32;           // experts per lane in the scan
     static_assert(NT * ROUNDS == DISPATCH_CHUNK && EMAX % 32 == 0, "dispatch_block shape");
-    __shared__ int wcnt[NG][EMAX];
-    __shared__ int off[EMAX];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int i = threadIdx.x; i < NG * EMAX; i += NT) (&wcnt[0][0])[i] = 0;
+    auto& wcnt = sc.wcnt;
+    auto& off = sc.off;
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int i = tid; i < NG * EMAX; i += NT) (&wcnt[0][0])[i] = 0;
     // all of the thread's ids and weights in flight at once
     int ev[ROUNDS];
     float wv[ROUNDS];
 #pragma unroll
     for (int q = 0; q < ROUNDS; ++q) {
-        const int j = q * NT + threadIdx.x;
+        const int j = q * NT + tid;
         ev[q] = (j < TK) ? __ldcg(idx + j) : -1;
         wv[q] = (j < TK) ? __ldcg(w + j) : 0.0f;
     }
-    __syncthreads();
+    sync();
     int rk[ROUNDS];
 #pragma unroll
     for (int q = 0; q < ROUNDS; ++q) {
-        const int j = q * NT + threadIdx.x;
+        const int j = q * NT + tid;
         int e = ev[q];
         if (j < TK && (e < 0 || e >= E)) atomicOr(err, ERRBIT_INDEX);
         if (e < 0 || e >= E) e = -1;
@@ -60,9 +72,9 @@ MOE_DEV void dispatch_block(const int32_t* idx, const float* w, int TK, int K, i
         if (e >= 0 && rk[q] == 0) wcnt[q * (NT / 32) + warp][e] = __popc(peers);
         ev[q] = e;
     }
-    __syncthreads();
+    sync();
     // per-group exclusive prefixes and the expert totals
-    for (int x = threadIdx.x; x < EMAX; x += NT) {
+    for (int x = tid; x < EMAX; x += NT) {
         int run = 0;
         for (int g = 0; g < NG; ++g) {
             const int c = wcnt[g][x];
@@ -71,7 +83,7 @@ MOE_DEV void dispatch_block(const int32_t* idx, const float* w, int TK, int K, i
         }
         off[x] = x < E ? run : 0;
     }
-    __syncthreads();
+    sync();
     if (warp == 0) {
         // exclusive scan of the totals (and of the tile counts of both heights)
         int c[EPL], m1[EPL], m2[EPL], s = 0, s1 = 0, s2 = 0;
@@ -106,6 +118,8 @@ MOE_DEV void dispatch_block(const int32_t* idx, const float* w, int TK, int K, i
                 mt_prefix[ex] = b1;
                 mt_prefix[E + 1 + ex] = b2;
             }
+            if (off_local != nullptr && ex < E) off_local[ex] = b;
+            if (off_local != nullptr && ex == E - 1) off_local[E] = b + c[i];
             if (write_out && ex == E - 1) {
                 offsets[E] = b + c[i];
                 mt_prefix[E] = b1 + m1[i];
@@ -117,14 +131,16 @@ MOE_DEV void dispatch_block(const int32_t* idx, const float* w, int TK, int K, i
             b2 += m2[i];
         }
     }
-    __syncthreads();
+    sync();
 #pragma unroll
     for (int q = 0; q < ROUNDS; ++q) {
         const int e = ev[q];
         if (e >= 0) {
-            const int j = q * NT + threadIdx.x;
+            const int j = q * NT + tid;
             const int pos = off[e] + wcnt[q * (NT / 32) + warp][e] + rk[q];
             if (tok_local != nullptr) tok_local[pos] = j / K;
+            if (w_local != nullptr) w_local[pos] = wv[q];
+            if (inv_local != nullptr) inv_local[j] = pos;
             if (write_out) {
                 sorted_token[pos] = j / K;
                 sorted_w[pos] = wv[q];
@@ -132,6 +148,20 @@ MOE_DEV void dispatch_block(const int32_t* idx, const float* w, int TK, int K, i
             }
         }
     }
+}
+
+
+// The whole CTA (NT threads) with its own static scratch.
+template <int NT, int EMAX>
+MOE_DEV void dispatch_block(const int32_t* idx, const float* w, int TK, int K, int E, int bm,
+                            bool write_out, int32_t* __restrict__ counts,
+                            int32_t* __restrict__ offsets, int32_t* __restrict__ mt_prefix,
+                            int32_t* __restrict__ sorted_token, float* __restrict__ sorted_w,
+                            int32_t* __restrict__ inv, int* err, int32_t* tok_local = nullptr) {
+    __shared__ DispatchScratch<EMAX> sc;
+    dispatch_block_impl<NT, EMAX>(static_cast<int>(threadIdx.x), [] { __syncthreads(); }, sc, idx, w, TK,
+                                  K, E, bm, write_out, counts, offsets, mt_prefix, sorted_token,
+                                  sorted_w, inv, err, tok_local);
 }
 
 }  // namespace

@@ -92,6 +92,7 @@ struct TcParams {
     int bno;             // output columns per tile
     uint32_t idesc;      // instruction descriptor (M = 128 or 256, N = 64 * nstrip)
     int ksplit1, kbs1;   // group 1 split-K: slices and k-blocks per slice
+    int kchunk1;         // TC_PLAIN_ACC: k-blocks per tensor-memory chunk
     int E, mt1;
     const int32_t* offsets;
     const int32_t* mt_prefix;  // group 0 tiles of this kernel's rows (128, pair 256) per segment
@@ -241,7 +242,8 @@ struct UnitCopies {
 
 template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __grid_constant__ TcParams p) {
-    constexpr bool SWIGLU = MODE != TC_PLAIN;
+    constexpr bool SWIGLU = MODE == TC_SWIGLU || MODE == TC_SWIGLU_BWD;
+    static_assert(MODE != TC_PLAIN_ACC || !PAIR, "chunk accumulation runs in the single-CTA form");
     using G = Geo<PAIR>;
     constexpr int STAGES = G::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -376,49 +378,57 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
             const uint64_t bdesc0 = smem_desc_sw128(sbase + A_BYTES, STRIP_BYTES, 1024);
             for (int u = unit0; u < total && ok; u += ustep) {
                 const Unit t = decode_unit<PAIR>(u, p, total0, s_mtp, s_off);
-                if (!bounded_wait(tempty_bar(acc), acc_phase ^ 1u, wc, PAIR)) break;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
-                for (int kb = t.kb0; kb < t.kb1; kb += G::KPS) {
-                    const int nk = min(G::KPS, t.kb1 - kb);
-                    if (!bounded_wait(full_bar(stage), phase, wc, PAIR)) {
+                // one accumulator per unit; TC_PLAIN_ACC: one per chunk of kchunk1 k-blocks
+                const int kstep = MODE == TC_PLAIN_ACC ? p.kchunk1 : t.kb1 - t.kb0;
+                for (int cs = t.kb0; cs < t.kb1; cs += kstep) {
+                    const int ce = min(cs + kstep, t.kb1);
+                    if (!bounded_wait(tempty_bar(acc), acc_phase ^ 1u, wc, PAIR)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t soff = static_cast<uint64_t>(stage * G::STAGE_BYTES) >> 4;
-                    const uint32_t first = kb == t.kb0 ? 0u : 1u;  // 0: overwrite the accumulator
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
+                    for (int kb = cs; kb < ce; kb += G::KPS) {
+                        const int nk = min(G::KPS, ce - kb);
+                        if (!bounded_wait(full_bar(stage), phase, wc, PAIR)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t soff = static_cast<uint64_t>(stage * G::STAGE_BYTES) >> 4;
+                        const uint32_t first = kb == cs ? 0u : 1u;  // 0: overwrite the accumulator
 #pragma unroll
-                    for (int j = 0; j < G::KPS; ++j) {
-                        if (j < nk) {
+                        for (int j = 0; j < G::KPS; ++j) {
+                            if (j < nk) {
 #pragma unroll
-                            for (int ks = 0; ks < BK / 16; ++ks) {
-                                const uint64_t ad = adesc0 + soff + (j * G::SUB_BYTES + ks * 32) / 16;
-                                const uint64_t bd = bdesc0 + soff + (j * G::SUB_BYTES + ks * 2048) / 16;
-                                const uint32_t accum = (j != 0 || ks != 0) ? 1u : first;
-                                if (PAIR)
-                                    tc_mma_bf16_pair(d_tmem, ad, bd, p.idesc, accum);
-                                else
-                                    tc_mma_bf16(d_tmem, ad, bd, p.idesc, accum);
+                                for (int ks = 0; ks < BK / 16; ++ks) {
+                                    const uint64_t ad = adesc0 + soff + (j * G::SUB_BYTES + ks * 32) / 16;
+                                    const uint64_t bd = bdesc0 + soff + (j * G::SUB_BYTES + ks * 2048) / 16;
+                                    const uint32_t accum = (j != 0 || ks != 0) ? 1u : first;
+                                    if (PAIR)
+                                        tc_mma_bf16_pair(d_tmem, ad, bd, p.idesc, accum);
+                                    else
+                                        tc_mma_bf16(d_tmem, ad, bd, p.idesc, accum);
+                                }
                             }
                         }
+                        if (PAIR)
+                            tc_commit_pair_mc(empty_bar(stage), 3);
+                        else
+                            tc_commit(empty_bar(stage));
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
+                    if (!ok) break;
                     if (PAIR)
-                        tc_commit_pair_mc(empty_bar(stage), 3);
+                        tc_commit_pair_mc(tfull_bar(acc), 3);
                     else
-                        tc_commit(empty_bar(stage));
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                        tc_commit(tfull_bar(acc));
+                    acc ^= 1;
+                    if (acc == 0) acc_phase ^= 1u;
                 }
-                if (!ok) break;
-                if (PAIR)
-                    tc_commit_pair_mc(tfull_bar(acc), 3);
-                else
-                    tc_commit(tfull_bar(acc));
-                acc ^= 1;
-                if (acc == 0) acc_phase ^= 1u;
             }
             if (PAIR)
                 tc_commit_pair(drain_bar);
@@ -435,6 +445,71 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
         uint32_t acc_phase = 0;
         for (int u = unit0; u < total; u += ustep) {
             const Unit t = decode_unit<PAIR>(u, p, total0, s_mtp, s_off);
+            if constexpr (MODE == TC_PLAIN_ACC) {
+                // the unit's chunks, each from its own accumulator, summed in FP32 in
+                // chunk order in this thread's registers (its row, `span` columns)
+                const int span = 32 * p.nstrip;  // <= 128
+                float av[128];
+#pragma unroll
+                for (int i = 0; i < 128; ++i) av[i] = 0.0f;
+                bool okc = true;
+                for (int cs = t.kb0; cs < t.kb1; cs += p.kchunk1) {
+                    int okw = 1;
+                    if (lane == 0) okw = bounded_wait(tfull_bar(acc), acc_phase, wc) ? 1 : 0;
+                    okw = __shfl_sync(0xffffffffu, okw, 0);
+                    if (!okw) {
+                        okc = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * ACC_COLS) +
+                                        (static_cast<uint32_t>(q * 32) << 16) +
+                                        static_cast<uint32_t>(half * span);
+#pragma unroll
+                    for (int c = 0; c < 128; c += 32) {
+                        if (c < span) {
+                            uint32_t r0[16], r1[16];
+                            tc_ld_32x32b_x16(tb + c, r0);
+                            tc_ld_32x32b_x16(tb + c + 16, r1);
+                            tc_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                av[c + i] += __uint_as_float(r0[i]);
+                                av[c + 16 + i] += __uint_as_float(r1[i]);
+                            }
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty_bar(acc));
+                    acc ^= 1;
+                    if (acc == 0) acc_phase ^= 1u;
+                }
+                if (!okc) break;
+                const int valid_rows = min(BM, t.rows) - q * 32;
+                if (valid_rows > 0) {
+                    const int N = p.N[t.g];
+                    const size_t pitch = static_cast<size_t>(p.out_ld[t.g]) * 4;
+                    char* out_rows = static_cast<char*>(p.out[t.g]) +
+                                     static_cast<size_t>(t.out_row0 + q * 32) * pitch;
+#pragma unroll
+                    for (int c = 0; c < 128; c += 16) {
+                        if (c < span) {
+                            const int cc = half * span + c;
+                            const int lim = N - (t.n0 + cc);
+                            uint4 blk[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                blk[j] = make_uint4(__float_as_uint(av[c + 4 * j]), __float_as_uint(av[c + 4 * j + 1]),
+                                                    __float_as_uint(av[c + 4 * j + 2]), __float_as_uint(av[c + 4 * j + 3]));
+                            const int vch = lim > 0 ? (lim >= 16 ? 4 : lim / 4) : 0;
+                            warp_store_block(stg, blk, lane, out_rows + static_cast<size_t>(t.out_col0 + cc) * 4,
+                                             pitch, valid_rows, vch);
+                        }
+                    }
+                }
+                continue;
+            }
             int ok = 1;
             if (lane == 0) ok = bounded_wait(tfull_bar(acc), acc_phase, wc) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -751,7 +826,7 @@ int pair_slots(int dev) {
 
 template <int MODE, bool PAIR>
 cudaError_t launch_tc_t(const TcGemmArgs& a, int nstrip, int slots, cudaStream_t s) {
-    constexpr bool SWIGLU = MODE != TC_PLAIN;
+    constexpr bool SWIGLU = MODE == TC_SWIGLU || MODE == TC_SWIGLU_BWD;
     constexpr int UROWS = PAIR ? 2 * BM : BM;
     TcParams p;
     memset(&p, 0, sizeof(p));
@@ -785,6 +860,12 @@ cudaError_t launch_tc_t(const TcGemmArgs& a, int nstrip, int slots, cudaStream_t
         if (g == 1) {
             const int ks = G.ksplit > 1 ? G.ksplit : 1;
             p.kbs1 = (p.kblocks[1] + ks - 1) / ks;
+            if (MODE == TC_PLAIN_ACC) {
+                // whole chunks per slice
+                if (G.kchunk <= 0) return cudaErrorInvalidValue;
+                p.kchunk1 = G.kchunk;
+                p.kbs1 = (p.kbs1 + G.kchunk - 1) / G.kchunk * G.kchunk;
+            }
             p.ksplit1 = ks > 1 ? (p.kblocks[1] + p.kbs1 - 1) / p.kbs1 : 1;
         }
         p.rows[g] = G.rows;
@@ -826,17 +907,18 @@ cudaError_t launch_tc_t(const TcGemmArgs& a, int nstrip, int slots, cudaStream_t
     long long grid = slots;  // persistent: one CTA (pair) per slot, at most one per unit
     if (units_bound < grid) grid = units_bound;
     if (grid < 1) grid = 1;
-    if (PAIR)
+    if constexpr (PAIR)
         return launch_pdl_cluster(tc_grouped_gemm_kernel<MODE, true>,
                                   dim3(2 * static_cast<unsigned>(grid)), dim3(THREADS),
                                   Geo<true>::SMEM_BYTES, s, 2, p);
-    return launch_pdl(tc_grouped_gemm_kernel<MODE, false>, dim3(static_cast<unsigned>(grid)),
-                      dim3(THREADS), Geo<false>::SMEM_BYTES, s, p);
+    else
+        return launch_pdl(tc_grouped_gemm_kernel<MODE, false>, dim3(static_cast<unsigned>(grid)),
+                          dim3(THREADS), Geo<false>::SMEM_BYTES, s, p);
 }
 
 template <int MODE>
 cudaError_t launch_tc_s(const TcGemmArgs& a, cudaStream_t s) {
-    constexpr bool SWIGLU = MODE != TC_PLAIN;
+    constexpr bool SWIGLU = MODE == TC_SWIGLU || MODE == TC_SWIGLU_BWD;
     int dev = 0;
     cudaGetDevice(&dev);
     int nmax = 0;
@@ -853,8 +935,15 @@ cudaError_t launch_tc_s(const TcGemmArgs& a, cudaStream_t s) {
     const bool long_segments =
         !a.g[0].enabled || static_cast<long long>(a.g[0].rows) >= 512LL * (a.E > 0 ? a.E : 1);
     const bool dense_plain = MODE == TC_PLAIN && !a.g[0].enabled;
-    const int slots = (even && long_segments && !dense_plain) ? pair_slots<MODE>(dev) : 0;
-    if (slots > 0) return launch_tc_t<MODE, true>(a, nstrip, slots, s);
+    if constexpr (MODE != TC_PLAIN_ACC) {
+        const int slots = (even && long_segments && !dense_plain) ? pair_slots<MODE>(dev) : 0;
+        if (slots > 0) return launch_tc_t<MODE, true>(a, nstrip, slots, s);
+    } else {
+        (void)even;
+        (void)long_segments;
+        (void)dense_plain;
+        if (a.g[0].enabled || !a.g[1].enabled) return cudaErrorInvalidValue;
+    }
     if (!prepare_kernel<MODE, false>(dev)) return cudaErrorInvalidValue;
     return launch_tc_t<MODE, false>(a, nstrip, num_sms(), s);
 }
@@ -863,6 +952,8 @@ cudaError_t launch_tc_s(const TcGemmArgs& a, cudaStream_t s) {
 
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t s) {
     if (a.swiglu == TC_SWIGLU_BWD) return launch_tc_s<TC_SWIGLU_BWD>(a, s);
+    if (a.swiglu == TC_PLAIN && a.g[1].enabled && a.g[1].kchunk > 0)
+        return launch_tc_s<TC_PLAIN_ACC>(a, s);
     return a.swiglu ? launch_tc_s<TC_SWIGLU>(a, s) : launch_tc_s<TC_PLAIN>(a, s);
 }
 

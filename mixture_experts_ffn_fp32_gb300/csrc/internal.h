@@ -74,6 +74,7 @@ struct WsLayout {
     size_t xs, z, h, hs, ys, routed, shout, xstage, ostage, qb, w3, rpart;
     size_t ga, gu, gas, gus;  // saved gate / up products (save_gate_up): routed rows, shared
     size_t logits, stats_part;  // routing diagnostics: r [T, E], per-CTA partial sums
+    size_t dctr;                // fused decode back end: counters [E + 2]
     size_t total;
     int nchunks;
 };
@@ -99,8 +100,12 @@ struct RouterArgs {
     int* err_clear;   // if set, block 0 zeroes this error word and the dispatch ticket after
                       // it (first kernel of a forward)
     float* logits;    // if set: the raw FP32 logits r [T, E] (routing diagnostics)
+    unsigned* zero = nullptr;  // if set (one-launch routers): block 0 zeroes zero[0, nzero)
+    int nzero = 0;             //   (the fused decode back end's counters)
 };
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
+// Whether the router of this layer runs as one launch that honours RouterArgs::zero.
+bool router_one_launch(int T, int d, int E, int x_bf16);
 // Tensor-core router pieces: W3 [3, d, E] BF16 = exact split of W [d, E];
 // routing from logits summed over nsplit partial slices part [nsplit, T, E].
 cudaError_t launch_router_split(const float* W, int d, int E, void* W3, int* err_clear,
@@ -165,7 +170,12 @@ cudaError_t launch_gather_sum_split(const float* ys, const int32_t* inv, int T, 
 //   Group 1 ("dense"): S segments all over A rows [0, rows1), B = matrix s;
 //     output columns [s*N1, (s+1)*N1).
 // tc_grouped_gemm epilogues (TcGemmArgs::swiglu)
-enum { TC_PLAIN = 0, TC_SWIGLU = 1, TC_SWIGLU_BWD = 2 };
+// TC_PLAIN_ACC: the single product of group 1 (split-K slices), each slice's
+// k-range reduced in chunks of TcGroup::kchunk k-blocks: every chunk's product
+// goes through tensor memory on its own and the epilogue adds the chunks in
+// FP32, in order, before it stores the slice (the tensor-core router: short
+// accumulation chains, few partial slices).
+enum { TC_PLAIN = 0, TC_SWIGLU = 1, TC_SWIGLU_BWD = 2, TC_PLAIN_ACC = 3 };
 struct TcGroup {
     int enabled;
     int K;              // reduction length of this group
@@ -186,6 +196,8 @@ struct TcGroup {
     int b_rows = 0;     // > 0: B has b_rows rows per matrix (rows beyond read as zero)
     int ksplit = 1;     // group 1 only: split K into ksplit slices; slice s writes the partial
                         // product to out rows [s*rows, (s+1)*rows) (needs Z == 1)
+    int kchunk = 0;     // TC_PLAIN_ACC, group 1: k-blocks per chunk (each slice a whole
+                        // number of chunks)
     // TC_SWIGLU: a_out / u_out (optional, both or neither, BF16 like out): the gate
     // and up products a = A B0, u = A B1 themselves, in out's rows, columns and pitch.
     void* a_out = nullptr;
@@ -262,6 +274,30 @@ cudaError_t launch_sign_bias(int E, int N, int K, const int32_t* counts, float* 
 cudaError_t launch_wait_selftest(int* err, uint64_t timeout_ns, cudaStream_t s);
 
 // Tensor-map encoder (driver entry point, resolved once).
+// ---- fused decode back end (decode_fused.cu) ---------------------------------
+// Everything after the router of a batch of at most 128 tokens in one launch:
+// dispatch (written to counts .. inv), row gather (xs, for the backward pass),
+// gate/up (h, hs), down (ys, shout), combine (out). ctr [E + 2] must be zero
+// (the router launch zeroes it).
+struct DecodeArgs {
+    int T, d, F, E, K, S, Fs;
+    const void* x;
+    const int32_t* idx;
+    const float* w;
+    const void *W_gate, *W_up, *W_down, *Ws_gate, *Ws_up, *Ws_down;
+    int32_t *counts, *offsets, *mt_prefix, *sorted_token;
+    float* sorted_w;
+    int32_t* inv;
+    void *xs, *h, *hs;
+    float *ys, *shout;
+    void* out;
+    int out_f32;
+    unsigned* ctr;
+    int* err;
+};
+bool decode_fused_shape_ok(int T, int d, int F, int E, int K, int S, int Fs);
+cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s);
+
 bool encode_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
                  const uint64_t* strides_bytes, const uint32_t* box);
 

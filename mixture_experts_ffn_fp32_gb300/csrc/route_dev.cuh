@@ -20,6 +20,12 @@ MOE_DEV void clear_status(int* w) {
     w[1] = 0;
 }
 
+// Block `first` of a one-launch router zeroes the counters it was given.
+MOE_DEV void zero_counters(const RouterArgs& a, bool first) {
+    if (first && a.zero != nullptr)
+        for (int i = threadIdx.x; i < a.nzero; i += blockDim.x) a.zero[i] = 0u;
+}
+
 MOE_DEV float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

@@ -34,6 +34,7 @@ __global__ void __launch_bounds__(256) router_small_kernel(RouterArgs a) {
     pdl_wait();
     pdl_trigger();
     if (a.err_clear != nullptr && blockIdx.x == 0 && threadIdx.x == 0) clear_status(a.err_clear);
+    zero_counters(a, blockIdx.x == 0);
     const int E = a.E, d = a.d;
     const int t0 = blockIdx.x * 8;
     const int ntok = min(8, a.T - t0);
@@ -264,13 +265,16 @@ __global__ void __launch_bounds__(256) router_chunk_kernel(RouterArgs a, float* 
 // partial logits of the slice there, and after a cluster barrier the CTAs
 // sum the slices of their tokens in slice order straight from the peers'
 // shared memory and route them (token c + ns w in warp w of the CTA of
-// cluster rank c).
+// cluster rank c). WG (E up to 256, whose W_router slice does not fit shared
+// memory): the W_router rows are read from global memory in the FMA loop,
+// one thread per expert, eight rows' loads in flight.
 struct ClusterRouterShape {
     int ns, lenc;
+    bool wg;  // W_router read from global memory (more than 128 experts)
     size_t smem;
 };
 
-template <bool BF16, int EP>
+template <bool BF16, int EP, bool WG>
 __global__ void __launch_bounds__(256) router_cluster_kernel(RouterArgs a, int lenc, uint64_t timeout_ns) {
     extern __shared__ __align__(128) uint8_t sm[];
     constexpr int R = 256 / EP;  // parts per expert
@@ -286,8 +290,8 @@ __global__ void __launch_bounds__(256) router_cluster_kernel(RouterArgs a, int l
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm);
     uint8_t* xstage = sm + 16;
     float* xt = reinterpret_cast<float*>(xstage + xstage_bytes);  // [lenc][8]
-    float* ws = xt + 8 * lenc;                                    // [lenc][E]
-    float* part = ws + static_cast<size_t>(lenc) * E;             // [8][EP]
+    float* ws = xt + 8 * lenc;                                    // [lenc][E] (not WG)
+    float* part = ws + (WG ? 0 : static_cast<size_t>(lenc) * E);  // [8][EP]
     float* red = part + 8 * EP;                                   // [R-1][8][EP]
     __shared__ int abort_flag;
     const uint32_t b = smem_u32(bar);
@@ -300,13 +304,14 @@ __global__ void __launch_bounds__(256) router_cluster_kernel(RouterArgs a, int l
     pdl_trigger();
     if (a.err_clear != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
         clear_status(a.err_clear);
+    zero_counters(a, blockIdx.x == 0 && blockIdx.y == 0);
     __syncthreads();
     if (threadIdx.x == 0) {
-        const uint32_t wbytes = static_cast<uint32_t>(kn) * E * 4;
+        const uint32_t wbytes = WG ? 0u : static_cast<uint32_t>(kn) * E * 4;
         const uint32_t xbytes = static_cast<uint32_t>(kn) * XES;
         mbar_expect_tx(b, wbytes + xbytes * ntok);
         if (kn > 0) {
-            bulk_load(smem_u32(ws), a.W + static_cast<size_t>(k0) * E, wbytes, b);
+            if (!WG) bulk_load(smem_u32(ws), a.W + static_cast<size_t>(k0) * E, wbytes, b);
             for (int tt = 0; tt < ntok; ++tt)
                 bulk_load(smem_u32(xstage + static_cast<size_t>(tt) * lenc * XES),
                           static_cast<const uint8_t*>(a.x) +
@@ -336,7 +341,42 @@ __global__ void __launch_bounds__(256) router_cluster_kernel(RouterArgs a, int l
     float acc[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-    if (ok && e < E) {
+    if (WG && ok && e < E) {
+        const float* wg = a.W + static_cast<size_t>(k0) * E + e;
+        int k = kb;
+        for (; k + 8 <= ke; k += 8) {
+            float wv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) wv[i] = __ldg(wg + static_cast<size_t>(k + i) * E);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 x0 = *reinterpret_cast<const float4*>(xt + (k + i) * 8);
+                const float4 x1 = *reinterpret_cast<const float4*>(xt + (k + i) * 8 + 4);
+                acc[0] = fmaf(x0.x, wv[i], acc[0]);
+                acc[1] = fmaf(x0.y, wv[i], acc[1]);
+                acc[2] = fmaf(x0.z, wv[i], acc[2]);
+                acc[3] = fmaf(x0.w, wv[i], acc[3]);
+                acc[4] = fmaf(x1.x, wv[i], acc[4]);
+                acc[5] = fmaf(x1.y, wv[i], acc[5]);
+                acc[6] = fmaf(x1.z, wv[i], acc[6]);
+                acc[7] = fmaf(x1.w, wv[i], acc[7]);
+            }
+        }
+        for (; k < ke; ++k) {
+            const float wv = __ldg(wg + static_cast<size_t>(k) * E);
+            const float4 x0 = *reinterpret_cast<const float4*>(xt + k * 8);
+            const float4 x1 = *reinterpret_cast<const float4*>(xt + k * 8 + 4);
+            acc[0] = fmaf(x0.x, wv, acc[0]);
+            acc[1] = fmaf(x0.y, wv, acc[1]);
+            acc[2] = fmaf(x0.z, wv, acc[2]);
+            acc[3] = fmaf(x0.w, wv, acc[3]);
+            acc[4] = fmaf(x1.x, wv, acc[4]);
+            acc[5] = fmaf(x1.y, wv, acc[5]);
+            acc[6] = fmaf(x1.z, wv, acc[6]);
+            acc[7] = fmaf(x1.w, wv, acc[7]);
+        }
+    }
+    if (!WG && ok && e < E) {
         for (int k = kb; k < ke; ++k) {
             const float wv = ws[static_cast<size_t>(k) * E + e];
             const float4 x0 = *reinterpret_cast<const float4*>(xt + k * 8);
@@ -400,15 +440,26 @@ ClusterRouterShape cluster_router_shape(int d, int E, int x_bf16) {
     const int ns0 = std::min(8, (d + 127) / 128);
     sh.lenc = ((d + ns0 - 1) / ns0 + 15) / 16 * 16;
     sh.ns = (d + sh.lenc - 1) / sh.lenc;
-    const int EP = E <= 64 ? 64 : 128;
+    sh.wg = E > 128;
+    const int EP = E <= 64 ? 64 : (E <= 128 ? 128 : 256);
     const int R = 256 / EP;
     const size_t xes = x_bf16 ? 2 : 4;
     sh.smem = 16 + (8 * sh.lenc * xes + 15) / 16 * 16 + 8 * static_cast<size_t>(sh.lenc) * 4 +
-              static_cast<size_t>(sh.lenc) * E * 4 + 8 * EP * 4 + (R - 1) * 8 * EP * 4;
+              (sh.wg ? 0 : static_cast<size_t>(sh.lenc) * E * 4) + 8 * EP * 4 + (R - 1) * 8 * EP * 4;
     return sh;
 }
 
 constexpr size_t CLUSTER_ROUTER_SMEM_MAX = 200 * 1024;
+
+}  // namespace
+
+bool router_one_launch(int T, int d, int E, int x_bf16) {
+    if (E <= 32) return true;  // router_small_kernel
+    // the cluster router (launch_router_chunked with a workspace)
+    return E <= 256 && T <= 512 && cluster_router_shape(d, E, x_bf16).smem <= CLUSTER_ROUTER_SMEM_MAX;
+}
+
+namespace {
 
 template <bool BF16>
 cudaError_t launch_router_t(const RouterArgs& a, cudaStream_t s) {
@@ -469,24 +520,26 @@ cudaError_t launch_router_chunked(const RouterArgs& a, float* part, cudaStream_t
     if (a.err_clear != nullptr && sh.smem <= CLUSTER_ROUTER_SMEM_MAX) {
         const dim3 grid(sh.ns, (a.T + 7) / 8);
         const uint64_t to = wait_timeout_ns();
-#define MOE_RCL(B, EPV)                                                                            \
+#define MOE_RCL(B, EPV, WGV)                                                                       \
     {                                                                                              \
         static bool set = false;                                                                   \
         if (!set) {                                                                                \
-            cudaFuncSetAttribute(router_cluster_kernel<B, EPV>,                                    \
+            cudaFuncSetAttribute(router_cluster_kernel<B, EPV, WGV>,                               \
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,                      \
                                  static_cast<int>(CLUSTER_ROUTER_SMEM_MAX));                       \
             set = true;                                                                            \
         }                                                                                          \
-        return launch_pdl_cluster(router_cluster_kernel<B, EPV>, grid, dim3(256), sh.smem, s,      \
+        return launch_pdl_cluster(router_cluster_kernel<B, EPV, WGV>, grid, dim3(256), sh.smem, s, \
                                   sh.ns, a, sh.lenc, to);                                          \
     }
         if (a.x_bf16) {
-            if (a.E <= 64) MOE_RCL(true, 64)
-            MOE_RCL(true, 128)
+            if (a.E <= 64) MOE_RCL(true, 64, false)
+            if (a.E <= 128) MOE_RCL(true, 128, false)
+            MOE_RCL(true, 256, true)
         } else {
-            if (a.E <= 64) MOE_RCL(false, 64)
-            MOE_RCL(false, 128)
+            if (a.E <= 64) MOE_RCL(false, 64, false)
+            if (a.E <= 128) MOE_RCL(false, 128, false)
+            MOE_RCL(false, 256, true)
         }
 #undef MOE_RCL
     }

@@ -392,9 +392,10 @@ def test_launch_count_grows():
 
 
 def test_decode_launches_and_dirty_workspace():
-    """A decode batch routes in one cluster launch and dispatches and gathers in
-    one more; nothing in the workspace carries over between forwards, so a
-    workspace full of garbage gives the same result, bit for bit."""
+    """A decode batch routes in one cluster launch and runs everything else in
+    one more (the fused decode back end); nothing in the workspace carries over
+    between forwards, so a workspace full of garbage gives the same result, bit
+    for bit."""
     A = api()
     w = W.WORKLOADS["medium_decode"].resized(T=64, d=512, d_ff=128)
     inp = W.make_inputs(w, device="cuda")
@@ -404,8 +405,8 @@ def test_decode_launches_and_dirty_workspace():
     n0 = A.launch_count()
     o1 = A.forward(spec, inp["x"], inp, ws=ws).clone()
     torch.cuda.synchronize()
-    # router, dispatch + gather, gate/up, down, combine
-    assert A.launch_count() - n0 == 5
+    # router, fused back end
+    assert A.launch_count() - n0 == 2
     ws.fill_(0xFF)
     o2 = A.forward(spec, inp["x"], inp, ws=ws).clone()
     assert A.workspace_status(ws) == A.MOE_OK
