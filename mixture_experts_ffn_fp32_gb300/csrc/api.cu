@@ -211,7 +211,7 @@ WsLayout plan_workspace(const moe_config& c) {
     L.rpart = (tcr || chk) ? take(nsplit * T * E * 4) : 0;
     L.logits = take(T * E * 4);
     L.stats_part = take(((T + STATS_TOKENS - 1) / STATS_TOKENS) * (2 * E + 1) * 4);
-    L.dctr = take((E + 2) * 4);
+    L.dctr = take((E + 3) * 4);
     L.total = o;
     return L;
 }
@@ -369,7 +369,7 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
     const bool fused = decode_fused(c);
     if (fused) {
         ra.zero = static_cast<unsigned*>(P(L.dctr));
-        ra.nzero = E + 2;
+        ra.nzero = E + 3;
     }
     {
         const moe_status rs = run_router(c, ra, static_cast<const float*>(w.W_router), x, ws, L, s);

@@ -29,9 +29,11 @@
 // each one is bounded anyway. The counters are zeroed by the router launch
 // that precedes this one.
 //
-// Rows of a routed gate/up unit come straight from x with TMA row gathers
-// (four rows per copy); the rows also go to the gathered-row buffer for the
-// backward pass.
+// Rows of a routed gate/up unit with at most GATHER_MAX rows come straight
+// from x with TMA row gathers (four rows per copy); every CTA also copies its
+// share of the rows into the gathered-row buffer (which the backward pass
+// reads), and a heavier unit loads its rows from there as tiles once every
+// CTA has released its share (one more counter).
 #include "common.cuh"
 #include "dispatch_dev.cuh"
 #include "internal.h"
@@ -48,29 +50,41 @@ constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 512;
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
-constexpr int STAGES = 3;
 constexpr int STAGE_BYTES = A_BYTES + 4 * STRIP_BYTES;  // 48 KB
 constexpr int STG_BYTES = 32 * 64;
 constexpr int EMAXF = 256;
-constexpr int NBARS = 2 * STAGES + 4 + 2;  // full, empty, tfull x2, tempty x2, drain, dispatch
+constexpr int GATHER_MAX = 32;  // routed rows a unit gathers from x itself
+constexpr int MAX_STAGES = 4;
+constexpr int NBARS = 2 * MAX_STAGES + 4 + 2;  // full, empty, tfull x2, tempty x2, drain, dispatch
 
+// Shared memory after the 1024-aligned ring. The dispatch scratch and the
+// epilogue's staging buffers share their space (the epilogue warps use one,
+// then the other).
+template <int EMAXT>
 struct Smem {
-    // after the 1024-aligned ring
     uint64_t bars[NBARS];
     uint32_t tmem_slot;
     int abort_flag;
     int nused;
     int pad_;
-    DispatchScratch<EMAXF> disp;
+    union {
+        DispatchScratch<EMAXT> disp;
+        uint4 stg[EPI_WARPS][STG_BYTES / 16];
+    };
     int32_t tok[DISPATCH_CHUNK];   // sorted position -> token
     float wloc[DISPATCH_CHUNK];    // sorted position -> gate weight
     int32_t invl[DISPATCH_CHUNK];  // assignment t*K+k -> sorted position
-    int32_t off[EMAXF + 1];        // expert offsets
-    int32_t used[EMAXF];           // experts with rows, ascending
-    uint4 stg[EPI_WARPS][STG_BYTES / 16];
+    int32_t off[EMAXT + 1];        // expert offsets
+    int32_t used[EMAXT];           // experts with rows, ascending
 };
 
-constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + sizeof(Smem);
+// Ring stages: 4 (192 KB of weight tiles in flight).
+template <int EMAXT>
+constexpr int stages_for() { return 4; }
+template <int EMAXT>
+constexpr size_t smem_bytes() { return 1024 + stages_for<EMAXT>() * STAGE_BYTES + sizeof(Smem<EMAXT>); }
+static_assert(smem_bytes<64>() <= 227 * 1024 && smem_bytes<128>() <= 227 * 1024 &&
+              smem_bytes<256>() <= 227 * 1024, "fused decode shared memory");
 
 struct DecodeParams {
     CUtensorMap mapX;    // x [T, d], box 64 x 128 (shared experts' rows)
@@ -83,6 +97,7 @@ struct DecodeParams {
     CUtensorMap mapHs;   // hs [T, S*Fs], box 64 x 128
     CUtensorMap mapWd;   // W_down [E, F, d], 4 strips
     CUtensorMap mapSd;   // Ws_down as [1, S*Fs, d], 4 strips
+    CUtensorMap mapXs;   // gathered rows xs [T*K, d], box 64 x 128
     uint32_t idesc;
     int T, d, F, E, K, S, Fs;
     const int32_t* idx;  // router output [T, K]
@@ -98,11 +113,12 @@ struct DecodeParams {
     __nv_bfloat16* xs;
     __nv_bfloat16* h;
     __nv_bfloat16* hs;
-    float* ys;
+    float* ys;  // routed rows times their gate weight
     float* shout;
     void* out;
     int out_f32;
-    unsigned* ctr;  // [E + 2]: per-expert gate/up warps, shared gate/up warps, down warps
+    unsigned* ctr;  // [E + 3]: per-expert gate/up warps, shared gate/up warps, down warps,
+                    // gather warps
     int* err;
     unsigned long long timeout_ns;
 };
@@ -131,7 +147,8 @@ MOE_DEV Counts unit_counts(const DecodeParams& p, int nused) {
     return c;
 }
 
-MOE_DEV DUnit decode_dunit(int u, const DecodeParams& p, const Counts& c, const Smem& sm) {
+template <class SM>
+MOE_DEV DUnit decode_dunit(int u, const DecodeParams& p, const Counts& c, const SM& sm) {
     DUnit t;
     if (u < c.U1) {
         const int s = u / c.nt_gs;
@@ -186,11 +203,13 @@ MOE_DEV unsigned* unit_counter(const DecodeParams& p, const DUnit& t) {
 
 MOE_DEV void epi_bar_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
+template <int EMAXT>
 __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_constant__ DecodeParams p) {
+    constexpr int STAGES = stages_for<EMAXT>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    Smem& sm = *reinterpret_cast<Smem*>(ring + STAGES * STAGE_BYTES);
+    Smem<EMAXT>& sm = *reinterpret_cast<Smem<EMAXT>*>(ring + STAGES * STAGE_BYTES);
     const uint32_t sbase = smem_u32(ring);
     const uint32_t bar0 = smem_u32(&sm.bars[0]);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -224,6 +243,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
         tma_prefetch_map(&p.mapWu);
         tma_prefetch_map(&p.mapH);
         tma_prefetch_map(&p.mapWd);
+        tma_prefetch_map(&p.mapXs);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&sm.tmem_slot), TMEM_COLS);
@@ -245,7 +265,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
             // ---------------- TMA producer ----------------
             int stage = 0;
             uint32_t phase = 0, issued = 0, last_par = 0;
-            bool ok = true, have = false;
+            bool ok = true, have = false, gathered = false;
             Counts c = c0;
             for (int u = blockIdx.x; ok; u += gridDim.x) {
                 if (!have && u >= c.U1) {
@@ -255,6 +275,13 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
                 }
                 if (u >= (have ? c.total() : c.U1)) break;
                 const DUnit t = decode_dunit(u, p, c, sm);
+                const bool tiled = t.kind == 1 && t.rows > GATHER_MAX;  // rows from xs
+                if (tiled && !gathered) {
+                    // every CTA's share of the gathered rows is in xs
+                    if (!bounded_wait_count(p.ctr + p.E + 2, EPI_WARPS * gridDim.x, wc)) break;
+                    fence_proxy_async_global();
+                    gathered = true;
+                }
                 if (t.kind >= 2) {
                     // the hidden rows this unit reads: every epilogue warp of their units done
                     const unsigned target = EPI_WARPS * (t.kind == 2 ? c.U1 : c.nt_g);
@@ -262,7 +289,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
                     fence_proxy_async_global();
                 }
                 const int ng = (t.rows + 3) / 4;  // row gathers of a routed gate/up k-block
-                const uint32_t abytes = t.kind == 1 ? static_cast<uint32_t>(ng) * 512u : A_BYTES;
+                const uint32_t abytes = (t.kind == 1 && !tiled) ? static_cast<uint32_t>(ng) * 512u : A_BYTES;
                 for (int kb = 0; kb < t.kblocks; ++kb) {
                     if (!bounded_wait(empty_bar(stage), phase ^ 1u, wc)) {
                         ok = false;
@@ -276,6 +303,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
                         tma_load_2d(sA, &p.mapX, kc, 0, fb);
                         tma_load_4d(sB, &p.mapSg, 0, kc, t.n0 >> 6, t.z, fb);
                         tma_load_4d(sB + 2 * STRIP_BYTES, &p.mapSu, 0, kc, t.n0 >> 6, t.z, fb);
+                    } else if (tiled) {
+                        tma_load_2d(sA, &p.mapXs, kc, t.row0, fb);
+                        tma_load_4d(sB, &p.mapWg, 0, kc, t.n0 >> 6, t.z, fb);
+                        tma_load_4d(sB + 2 * STRIP_BYTES, &p.mapWu, 0, kc, t.n0 >> 6, t.z, fb);
                     } else if (t.kind == 1) {
                         for (int g = 0; g < ng; ++g) {
                             int r[4];
@@ -355,18 +386,18 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
         // ---------------- epilogue warps 2..9 ----------------
         const int tid = threadIdx.x - 64;
         // the dispatch, the same in every CTA (CTA 0 also writes it out)
-        dispatch_block_impl<256, EMAXF>(tid, [] { epi_bar_sync(); }, sm.disp, p.idx, p.w, TK, p.K, p.E,
+        dispatch_block_impl<256, EMAXT>(tid, [] { epi_bar_sync(); }, sm.disp, p.idx, p.w, TK, p.K, p.E,
                                         BM, blockIdx.x == 0, p.counts, p.offsets, p.mt_prefix,
                                         p.sorted_token, p.sorted_w, p.inv, p.err, sm.tok, sm.wloc,
                                         sm.invl, sm.off);
         epi_bar_sync();
         if (tid < 32) {
             // the experts with rows, ascending
-            int has[EMAXF / 32];
+            int has[EMAXT / 32];
             int n = 0;
 #pragma unroll
-            for (int i = 0; i < EMAXF / 32; ++i) {
-                const int e = lane * (EMAXF / 32) + i;
+            for (int i = 0; i < EMAXT / 32; ++i) {
+                const int e = lane * (EMAXT / 32) + i;
                 has[i] = (e < p.E && sm.off[e + 1] > sm.off[e]) ? 1 : 0;
                 n += has[i];
             }
@@ -378,8 +409,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
             }
             int at = incl - n;
 #pragma unroll
-            for (int i = 0; i < EMAXF / 32; ++i)
-                if (has[i]) sm.used[at++] = lane * (EMAXF / 32) + i;
+            for (int i = 0; i < EMAXT / 32; ++i)
+                if (has[i]) sm.used[at++] = lane * (EMAXT / 32) + i;
             if (lane == 31) sm.nused = incl;
         }
         epi_bar_sync();
@@ -392,6 +423,13 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
             for (int r = blockIdx.x + gridDim.x * (tid >> 5); r < TK; r += gridDim.x * EPI_WARPS) {
                 const size_t so = static_cast<size_t>(sm.tok[r]) * vpr, d0 = static_cast<size_t>(r) * vpr;
                 for (int v = lane; v < vpr; v += 32) dst[d0 + v] = __ldg(src + so + v);
+            }
+            // release this warp's rows to the tiled loads of heavier units
+            fence_proxy_async_global();
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence();
+                release_add_gpu(p.ctr + p.E + 2, 1u);
             }
         }
         const Counts c = unit_counts(p, sm.nused);
@@ -561,7 +599,8 @@ cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s) {
               map_strips(&p.mapWg, a.W_gate, a.E, a.d, a.F, 2) &&
               map_strips(&p.mapWu, a.W_up, a.E, a.d, a.F, 2) &&
               map2d(&p.mapH, a.h, TK, a.F, a.F, TC_BM) &&
-              map_strips(&p.mapWd, a.W_down, a.E, a.F, a.d, 4);
+              map_strips(&p.mapWd, a.W_down, a.E, a.F, a.d, 4) &&
+              map2d(&p.mapXs, a.xs, TK, a.d, a.d, TC_BM);
     if (ok && a.S)
         ok = map_strips(&p.mapSg, a.Ws_gate, a.S, a.d, a.Fs, 2) &&
              map_strips(&p.mapSu, a.Ws_up, a.S, a.d, a.Fs, 2) && map2d(&p.mapHs, a.hs, a.T, SF, SF, TC_BM) &&
@@ -578,16 +617,25 @@ cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s) {
     p.ys = a.ys; p.shout = a.shout; p.out = a.out; p.out_f32 = a.out_f32;
     p.ctr = a.ctr; p.err = a.err;
     p.timeout_ns = wait_timeout_ns();
-    static bool attr_set[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
-        const cudaError_t e = cudaFuncSetAttribute(decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(SMEM_BYTES));
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+    const dim3 grid(static_cast<unsigned>(num_sms()));
+#define MOE_DF(EM)                                                                                  \
+    {                                                                                               \
+        static bool attr_set[64] = {};                                                              \
+        if (!attr_set[dev]) {                                                                       \
+            const cudaError_t e = cudaFuncSetAttribute(decode_fused_kernel<EM>,                     \
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                                       static_cast<int>(smem_bytes<EM>()));         \
+            if (e != cudaSuccess) return e;                                                         \
+            attr_set[dev] = true;                                                                   \
+        }                                                                                           \
+        return launch_pdl(decode_fused_kernel<EM>, grid, dim3(THREADS), smem_bytes<EM>(), s, p);   \
     }
-    return launch_pdl(decode_fused_kernel, dim3(static_cast<unsigned>(num_sms())), dim3(THREADS), SMEM_BYTES, s, p);
+    if (a.E <= 64) MOE_DF(64)
+    if (a.E <= 128) MOE_DF(128)
+    MOE_DF(256)
+#undef MOE_DF
 }
 
 }  // namespace moe

@@ -21,12 +21,14 @@
 namespace moe {
 namespace {
 
-// Scratch of dispatch_block_impl: NG x EMAX per-group counts and EMAX offsets.
+// Scratch of dispatch_block_impl: NG x EMAX per-group counts (then their
+// prefixes: at most DISPATCH_CHUNK, so 16 bits hold them) and EMAX offsets.
 template <int EMAX>
 struct DispatchScratch {
-    int wcnt[DISPATCH_CHUNK / 32][EMAX];
+    unsigned short wcnt[DISPATCH_CHUNK / 32][EMAX];
     int off[EMAX];
 };
+static_assert(DISPATCH_CHUNK < 65536, "per-group prefixes in 16 bits");
 
 // idx and w are read through L2. EMAX: a multiple of 32 that is at least E.
 // The calling threads are tid = 0 .. NT-1 (whole warps, tid 0 starting a warp)

@@ -74,7 +74,7 @@ struct WsLayout {
     size_t xs, z, h, hs, ys, routed, shout, xstage, ostage, qb, w3, rpart;
     size_t ga, gu, gas, gus;  // saved gate / up products (save_gate_up): routed rows, shared
     size_t logits, stats_part;  // routing diagnostics: r [T, E], per-CTA partial sums
-    size_t dctr;                // fused decode back end: counters [E + 2]
+    size_t dctr;                // fused decode back end: counters [E + 3]
     size_t total;
     int nchunks;
 };
@@ -277,7 +277,7 @@ cudaError_t launch_wait_selftest(int* err, uint64_t timeout_ns, cudaStream_t s);
 // ---- fused decode back end (decode_fused.cu) ---------------------------------
 // Everything after the router of a batch of at most 128 tokens in one launch:
 // dispatch (written to counts .. inv), row gather (xs, for the backward pass),
-// gate/up (h, hs), down (ys, shout), combine (out). ctr [E + 2] must be zero
+// gate/up (h, hs), down (ys, shout), combine (out). ctr [E + 3] must be zero
 // (the router launch zeroes it).
 struct DecodeArgs {
     int T, d, F, E, K, S, Fs;

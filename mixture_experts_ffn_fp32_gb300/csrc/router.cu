@@ -266,8 +266,11 @@ __global__ void __launch_bounds__(256) router_chunk_kernel(RouterArgs a, float* 
 // sum the slices of their tokens in slice order straight from the peers'
 // shared memory and route them (token c + ns w in warp w of the CTA of
 // cluster rank c). WG (E up to 256, whose W_router slice does not fit shared
-// memory): the W_router rows are read from global memory in the FMA loop,
-// one thread per expert, eight rows' loads in flight.
+// memory): the slice streams through a ring of three 32-row chunks in shared
+// memory (bulk copies, one thread per expert consuming each row).
+constexpr int WG_ROWS = 32;  // W_router rows per streamed chunk (WG)
+constexpr int WG_BUFS = 3;
+
 struct ClusterRouterShape {
     int ns, lenc;
     bool wg;  // W_router read from global memory (more than 128 experts)
@@ -287,17 +290,19 @@ __global__ void __launch_bounds__(256) router_cluster_kernel(RouterArgs a, int l
     const int kn = max(0, min(lenc, d - k0));
     const int ntok = min(8, a.T - t0);
     const int xstage_bytes = (8 * lenc * XES + 15) / 16 * 16;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sm);
-    uint8_t* xstage = sm + 16;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm);  // [0]: x and W slice; [1..]: WG ring
+    uint8_t* xstage = sm + 64;
     float* xt = reinterpret_cast<float*>(xstage + xstage_bytes);  // [lenc][8]
-    float* ws = xt + 8 * lenc;                                    // [lenc][E] (not WG)
-    float* part = ws + (WG ? 0 : static_cast<size_t>(lenc) * E);  // [8][EP]
+    float* ws = xt + 8 * lenc;  // [lenc][E]; WG: the ring [WG_BUFS][WG_ROWS][EP]
+    float* part = ws + (WG ? static_cast<size_t>(WG_BUFS) * WG_ROWS * EP : static_cast<size_t>(lenc) * E);
     float* red = part + 8 * EP;                                   // [R-1][8][EP]
     __shared__ int abort_flag;
     const uint32_t b = smem_u32(bar);
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(b, 1);
+        if (WG)
+            for (int i = 0; i < WG_BUFS; ++i) mbar_init(b + 8u * (1 + i), 1);
         fence_mbarrier_init();
     }
     pdl_wait();
@@ -317,6 +322,17 @@ __global__ void __launch_bounds__(256) router_cluster_kernel(RouterArgs a, int l
                           static_cast<const uint8_t*>(a.x) +
                               (static_cast<size_t>(t0 + tt) * d + k0) * XES,
                           xbytes, b);
+        }
+        if (WG) {
+            // the first chunks of the W_router slice
+            const int nch = (kn + WG_ROWS - 1) / WG_ROWS;
+            for (int i = 0; i < WG_BUFS && i < nch; ++i) {
+                const int rows = min(WG_ROWS, kn - i * WG_ROWS);
+                const uint32_t bytes = static_cast<uint32_t>(rows) * E * 4;
+                mbar_expect_tx(b + 8u * (1 + i), bytes);
+                bulk_load(smem_u32(ws + static_cast<size_t>(i) * WG_ROWS * EP),
+                          a.W + static_cast<size_t>(k0 + i * WG_ROWS) * E, bytes, b + 8u * (1 + i));
+            }
         }
     }
     // the routing warps' bias values, loaded while the copies are in flight
@@ -341,39 +357,50 @@ __global__ void __launch_bounds__(256) router_cluster_kernel(RouterArgs a, int l
     float acc[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-    if (WG && ok && e < E) {
-        const float* wg = a.W + static_cast<size_t>(k0) * E + e;
-        int k = kb;
-        for (; k + 8 <= ke; k += 8) {
-            float wv[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) wv[i] = __ldg(wg + static_cast<size_t>(k + i) * E);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 x0 = *reinterpret_cast<const float4*>(xt + (k + i) * 8);
-                const float4 x1 = *reinterpret_cast<const float4*>(xt + (k + i) * 8 + 4);
-                acc[0] = fmaf(x0.x, wv[i], acc[0]);
-                acc[1] = fmaf(x0.y, wv[i], acc[1]);
-                acc[2] = fmaf(x0.z, wv[i], acc[2]);
-                acc[3] = fmaf(x0.w, wv[i], acc[3]);
-                acc[4] = fmaf(x1.x, wv[i], acc[4]);
-                acc[5] = fmaf(x1.y, wv[i], acc[5]);
-                acc[6] = fmaf(x1.z, wv[i], acc[6]);
-                acc[7] = fmaf(x1.w, wv[i], acc[7]);
+    if (WG) {
+        // stream the slice: chunk i in buffer i % WG_BUFS, refilled with chunk
+        // i + WG_BUFS once every thread has used it; rows in order, as above
+        const int nch = (kn + WG_ROWS - 1) / WG_ROWS;
+        bool okc = ok;
+        int consumed = 0;
+        for (int i = 0; i < nch; ++i) {
+            const int buf = i % WG_BUFS;
+            if (okc) okc = bounded_wait(b + 8u * (1 + buf), static_cast<uint32_t>((i / WG_BUFS) & 1), wc);
+            if (okc) consumed = i + 1;
+            const int rows = min(WG_ROWS, kn - i * WG_ROWS);
+            if (okc && e < E) {
+                const float* wb = ws + static_cast<size_t>(buf) * WG_ROWS * EP;
+                for (int r0 = 0; r0 < rows; ++r0) {
+                    const float wv = wb[r0 * E + e];
+                    const int k = i * WG_ROWS + r0;
+                    const float4 x0 = *reinterpret_cast<const float4*>(xt + k * 8);
+                    const float4 x1 = *reinterpret_cast<const float4*>(xt + k * 8 + 4);
+                    acc[0] = fmaf(x0.x, wv, acc[0]);
+                    acc[1] = fmaf(x0.y, wv, acc[1]);
+                    acc[2] = fmaf(x0.z, wv, acc[2]);
+                    acc[3] = fmaf(x0.w, wv, acc[3]);
+                    acc[4] = fmaf(x1.x, wv, acc[4]);
+                    acc[5] = fmaf(x1.y, wv, acc[5]);
+                    acc[6] = fmaf(x1.z, wv, acc[6]);
+                    acc[7] = fmaf(x1.w, wv, acc[7]);
+                }
+            }
+            __syncthreads();
+            if (threadIdx.x == 0 && i + WG_BUFS < nch && !abort_flag) {
+                const int j = i + WG_BUFS;
+                const int rj = min(WG_ROWS, kn - j * WG_ROWS);
+                const uint32_t bytes = static_cast<uint32_t>(rj) * E * 4;
+                mbar_expect_tx(b + 8u * (1 + buf), bytes);
+                bulk_load(smem_u32(ws + static_cast<size_t>(buf) * WG_ROWS * EP),
+                          a.W + static_cast<size_t>(k0 + j * WG_ROWS) * E, bytes, b + 8u * (1 + buf));
             }
         }
-        for (; k < ke; ++k) {
-            const float wv = __ldg(wg + static_cast<size_t>(k) * E);
-            const float4 x0 = *reinterpret_cast<const float4*>(xt + k * 8);
-            const float4 x1 = *reinterpret_cast<const float4*>(xt + k * 8 + 4);
-            acc[0] = fmaf(x0.x, wv, acc[0]);
-            acc[1] = fmaf(x0.y, wv, acc[1]);
-            acc[2] = fmaf(x0.z, wv, acc[2]);
-            acc[3] = fmaf(x0.w, wv, acc[3]);
-            acc[4] = fmaf(x1.x, wv, acc[4]);
-            acc[5] = fmaf(x1.y, wv, acc[5]);
-            acc[6] = fmaf(x1.z, wv, acc[6]);
-            acc[7] = fmaf(x1.w, wv, acc[7]);
+        // copies issued and never waited for (a wait gave up) land before the exit
+        if (threadIdx.x == 0 && consumed < nch) {
+            const int issued = abort_flag ? min(nch, consumed + WG_BUFS) : nch;
+            for (int i = consumed; i < issued; ++i)
+                bounded_drain(b + 8u * (1 + i % WG_BUFS), static_cast<uint32_t>((i / WG_BUFS) & 1),
+                              timeout_ns, a.err_clear);
         }
     }
     if (!WG && ok && e < E) {
@@ -444,8 +471,9 @@ ClusterRouterShape cluster_router_shape(int d, int E, int x_bf16) {
     const int EP = E <= 64 ? 64 : (E <= 128 ? 128 : 256);
     const int R = 256 / EP;
     const size_t xes = x_bf16 ? 2 : 4;
-    sh.smem = 16 + (8 * sh.lenc * xes + 15) / 16 * 16 + 8 * static_cast<size_t>(sh.lenc) * 4 +
-              (sh.wg ? 0 : static_cast<size_t>(sh.lenc) * E * 4) + 8 * EP * 4 + (R - 1) * 8 * EP * 4;
+    sh.smem = 64 + (8 * sh.lenc * xes + 15) / 16 * 16 + 8 * static_cast<size_t>(sh.lenc) * 4 +
+              (sh.wg ? static_cast<size_t>(WG_BUFS) * WG_ROWS * EP * 4 : static_cast<size_t>(sh.lenc) * E * 4) +
+              8 * EP * 4 + (R - 1) * 8 * EP * 4;
     return sh;
 }
 

@@ -116,6 +116,9 @@ PROFILE_CASES: dict[str, Workload] = {
     "large_prefill_e32": replace(WORKLOADS["large_prefill"], name="large_prefill_e32", T=1024,
                                  E=32),
     "large_decode_e32": replace(WORKLOADS["large_decode"], name="large_decode_e32", E=32),
+    # the 128-token, 256-expert router of the large decode batch, with narrow experts
+    "decode_e256_router": replace(WORKLOADS["large_decode"], name="decode_e256_router", d_ff=128,
+                                  shared_d_ff=128),
 }
 WORKLOADS.update(PROFILE_CASES)
 
