@@ -129,9 +129,14 @@ MOE_DEV Unit decode_unit(int u, const TcParams& p, int total0, const int* s_mtp,
     const int BNO = p.bno;
     Unit t;
     if (u < total0) {
+        // An expert's units are consecutive. Single CTA: its row tiles innermost,
+        // so the units reading one weight strip (one column tile) are neighbours,
+        // and the CTAs that take them (neighbours too) read the strip at about the
+        // same time: all but the first find it in L2 (large prefill: 23 % -> 7.5 %
+        // weight re-reads). Pair: its column tiles innermost (measured faster
+        // there: segments of many row tiles keep their weights in L2 anyway).
         const int nt = p.nt[0];
         const int mt = u / nt;
-        const int n = u - mt * nt;
         int lo = 0, hi = p.E;  // s_mtp[lo] <= mt < s_mtp[hi]
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
@@ -140,7 +145,16 @@ MOE_DEV Unit decode_unit(int u, const TcParams& p, int total0, const int* s_mtp,
             else
                 hi = mid;
         }
-        const int m = mt - s_mtp[lo];
+        int n, m;
+        if (PAIR) {
+            n = u - mt * nt;
+            m = mt - s_mtp[lo];
+        } else {
+            const int me = s_mtp[lo + 1] - s_mtp[lo];  // row tiles of expert lo (>= 1)
+            const int l = u - s_mtp[lo] * nt;
+            n = l / me;
+            m = l - n * me;
+        }
         t.g = 0;
         t.row0 = s_off[lo] + m * UROWS;
         t.rows = min(UROWS, s_off[lo + 1] - t.row0);
