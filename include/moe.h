@@ -220,6 +220,10 @@ moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* topk_idx,
  *   No host synchronisation and no allocation: after a first call on the
  *   device (which sets kernel attributes), calls can be captured into a CUDA
  *   graph; so can moe_backward.
+ *   The grouped GEMMs pick their tile form from the shapes; the environment
+ *   variable MOE_GEMM_FORM, read at each call, overrides the choice for tests
+ *   and tuning ("rows": row-tile forms only; "tokens": the token-column form
+ *   wherever the product allows it). Every form gives the same bits.
  * Sources: APEX-1 Math Ref Part 3 sections 12.2 and 13.2; APEX-1 docs
  * "10 - Mixture of Experts" MoEFFN.forward; kimi_k3 StableLatentMoE
  * "Grouped expert execution" and "Return to model width"; "MoE from scratch"

@@ -37,6 +37,8 @@
 //
 // Every wait is bounded (see common.cuh): on timeout the CTA stops, drains
 // its copies and MMAs, frees TMEM and flags the error word.
+#include <cstdlib>
+
 #include "common.cuh"
 #include "internal.h"
 #include "warp_stage.cuh"
@@ -763,6 +765,369 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
     }
 }
 
+// ---------------------------------------------------------------------------
+// Token-column form (CTA pair). The weights are the MMA's A operand: M = 256
+// output features, 128 rows of A in each CTA, read MN-major straight from the
+// [Z, K, N] weights (the same 64-column strips as the row-tile forms). The
+// unit's tokens are its B operand: N = the unit's token count rounded up to
+// 16 (at most 256), the first half in the even CTA, read K-major from the
+// row-major activations. A segment of n rows thus costs n rounded up to 16
+// MMA columns instead of whole 128- or 256-row tiles.
+//
+// Units: a segment of n rows is cut into ceil(n / 256) token tiles of nearly
+// equal size (the 256-row tile counts of the dispatch); each unit covers 128
+// output features per CTA. SwiGLU: gate and up of those features, two MMAs
+// into two 256-column accumulators that take all of tensor memory, a stage
+// of 48 KB (16 KB of token rows, 32 KB of weights: twice the tensor work of
+// the single-CTA row-tile form per byte), 4 stages; the epilogue of a unit
+// runs before the MMAs of the next, while the copies of the next run ahead.
+// Plain: one MMA into one of two 256-column accumulators, so that the
+// epilogue of a unit overlaps the MMAs of the next; a stage of 32 KB, 6
+// stages. An expert's token tiles are innermost, so the CTA pairs that share
+// a weight tile run side by side.
+//
+// An accumulator holds features on its lanes and tokens on its columns; the
+// epilogue warps transpose 32 x 32 (BF16) or 16 x 32 (FP32) blocks through
+// their staging buffers so that the stores stay row-major. Same per-element
+// arithmetic as the row-tile epilogues, and the tensor core's sums do not
+// depend on which operand is A: the outputs equal the row-tile forms' bit
+// for bit (measured).
+// ---------------------------------------------------------------------------
+constexpr int SW_TOK = 256;  // tokens per unit at most
+constexpr int SW_FPC = 128;  // output features of one CTA per unit
+
+template <bool SWIGLU>
+struct TGeo {
+    static constexpr int STAGES = SWIGLU ? 4 : 6;
+    static constexpr int WSTRIPS = SWIGLU ? 4 : 2;  // weight strips per stage
+    static constexpr int STAGE_BYTES = A_BYTES + WSTRIPS * STRIP_BYTES;
+    static constexpr int NACC = SWIGLU ? 1 : 2;     // accumulators (TMEM: 512 columns)
+    static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+    static constexpr int NBARS = 2 * STAGES + 2 * NACC + 1;
+    static constexpr int MISC_OFF = BAR_OFF + 8 * NBARS;
+    static constexpr int SCHED_OFF = ((MISC_OFF + 16) + 15) / 16 * 16;
+    static constexpr int STG_OFF = (SCHED_OFF + 2 * (MAXE + 1) * 4 + 127) / 128 * 128;
+    static constexpr int SMEM_BYTES = STG_OFF + EPI_WARPS * STG_BYTES + 1024;
+    static_assert(SMEM_BYTES <= 227 * 1024, "token-column shared memory");
+};
+
+struct SUnit {
+    int g, row0, n, zb, f0, out_col0;
+};
+
+MOE_DEV SUnit decode_sunit(int u, const TcParams& p, int total0, const int* s_mtp2, const int* s_off) {
+    SUnit t;
+    if (u < total0) {
+        const int nt = p.nt[0];
+        const int mt = u / nt;
+        int lo = 0, hi = p.E;  // s_mtp2[lo] <= mt < s_mtp2[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_mtp2[mid] <= mt)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        const int me = s_mtp2[lo + 1] - s_mtp2[lo];  // token tiles of expert lo (>= 1)
+        const int l = u - s_mtp2[lo] * nt;
+        const int n = l / me, m = l - n * me;
+        const long long rows = s_off[lo + 1] - s_off[lo];
+        const int r0 = static_cast<int>(m * rows / me), r1 = static_cast<int>((m + 1) * rows / me);
+        t.g = 0;
+        t.row0 = s_off[lo] + r0;
+        t.n = r1 - r0;
+        t.zb = lo;
+        t.f0 = n * p.bno;
+        t.out_col0 = t.f0;
+    } else {
+        const int u1 = u - total0;
+        const int m = u1 % p.mt1;
+        const int rest = u1 / p.mt1;
+        const int n = rest % p.nt[1];
+        const int s = rest / p.nt[1];
+        const long long rows = p.rows[1];
+        const int r0 = static_cast<int>(m * rows / p.mt1), r1 = static_cast<int>((m + 1) * rows / p.mt1);
+        t.g = 1;
+        t.row0 = r0;
+        t.n = r1 - r0;
+        t.zb = s;
+        t.f0 = n * p.bno;
+        t.out_col0 = s * p.N[1] + t.f0;
+    }
+    return t;
+}
+
+template <bool SWIGLU>
+__global__ void __launch_bounds__(THREADS, 1) tc_token_pair_kernel(const __grid_constant__ TcParams p) {
+    using G = TGeo<SWIGLU>;
+    constexpr int STAGES = G::STAGES;
+    constexpr int NACC = G::NACC;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + G::BAR_OFF;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + NACC + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * NACC);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::MISC_OFF);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + G::MISC_OFF + 4);
+    int* s_mtp = reinterpret_cast<int*>(smem + G::SCHED_OFF);
+    int* s_off = s_mtp + (MAXE + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int unit0 = static_cast<int>(blockIdx.x >> 1);
+    const int ustep = static_cast<int>(gridDim.x >> 1);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < NACC; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 2 * EPI_WARPS);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        for (int g = 0; g < 2; ++g) {
+            if (!p.enabled[g]) continue;
+            tma_prefetch_map(&p.mapA[g]);
+            tma_prefetch_map(&p.mapB0[g]);
+            if (SWIGLU) tma_prefetch_map(&p.mapB1[g]);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    // everything above overlaps the previous kernel; its outputs are read below
+    pdl_wait();
+    pdl_trigger();
+    if (p.enabled[0]) {
+        for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
+            s_mtp[i] = p.mt_prefix[i];
+            s_off[i] = p.offsets[i];
+        }
+    }
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total0 = p.enabled[0] ? s_mtp[p.E] * p.nt[0] : 0;
+    const int total = total0 + (p.enabled[1] ? p.mt1 * p.Z[1] * p.nt[1] : 0);
+    const WaitCtx wc{p.err, abort_flag, p.timeout_ns};
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer (both CTAs) ----------------
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, last_par = 0;
+            bool ok = true;
+            for (int u = unit0; u < total && ok; u += ustep) {
+                const SUnit t = decode_sunit(u, p, total0, s_mtp, s_off);
+                const int nh = ((t.n + 15) & ~15) >> 1;  // token columns held by each CTA
+                const int arow = t.row0 + rank * nh;
+                const int fc = t.f0 + SW_FPC * rank;   // this CTA's first output feature
+                const CUtensorMap* mA = &p.mapA[t.g];
+                const CUtensorMap* mB0 = &p.mapB0[t.g];
+                const CUtensorMap* mB1 = &p.mapB1[t.g];
+                const bool wide = p.b_wide[t.g] != 0;
+                for (int kb = 0; kb < p.kblocks[t.g]; ++kb) {
+                    if (!bounded_wait(empty_bar(stage), phase ^ 1u, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sX = sbase + stage * G::STAGE_BYTES;
+                    const uint32_t sW = sX + A_BYTES;
+                    const uint32_t fb = map_shared_rank(full_bar(stage), 0);
+                    if (rank == 0) mbar_expect_tx(full_bar(stage), 2 * G::STAGE_BYTES);
+                    const int kc = kb * BK;
+                    tma_load_2d_pair(sX, mA, kc, arow, fb);
+                    if (wide) {
+                        tma_load_4d_pair(sW, mB0, 0, kc, fc >> 6, t.zb, fb);
+                        if (SWIGLU) tma_load_4d_pair(sW + 2 * STRIP_BYTES, mB1, 0, kc, fc >> 6, t.zb, fb);
+                    } else {
+                        tma_load_3d_pair(sW, mB0, fc, kc, t.zb, fb);
+                        tma_load_3d_pair(sW + STRIP_BYTES, mB0, fc + 64, kc, t.zb, fb);
+                        if (SWIGLU) {
+                            tma_load_3d_pair(sW + 2 * STRIP_BYTES, mB1, fc, kc, t.zb, fb);
+                            tma_load_3d_pair(sW + 3 * STRIP_BYTES, mB1, fc + 64, kc, t.zb, fb);
+                        }
+                    }
+                    issued |= 1u << stage;
+                    last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // every copy this thread issued has landed before the CTA can exit
+            for (int s = 0; s < STAGES; ++s)
+                if ((issued >> s) & 1u)
+                    bounded_drain(rank == 0 ? full_bar(s) : empty_bar(s), (last_par >> s) & 1u,
+                                  p.timeout_ns, p.err);
+        }
+    } else if (warp == 1 && rank == 1) {
+        // the odd CTA of a pair issues no MMAs
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer (even CTA) ----------------
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            // token rows: K-major B; weight strips: MN-major A (8 KB between
+            // 64-feature strips, 1 KB between 8-row k groups)
+            const uint64_t bdesc0 = smem_desc_sw128(sbase, 16, 1024);
+            const uint64_t adesc0 = smem_desc_sw128(sbase + A_BYTES, STRIP_BYTES, 1024);
+            const uint32_t idesc0 = idesc_bf16_f32(2 * BM, 0, 0) | (1u << 15);  // A MN-major
+            for (int u = unit0; u < total && ok; u += ustep) {
+                const SUnit t = decode_sunit(u, p, total0, s_mtp, s_off);
+                const uint32_t idesc = idesc0 | (static_cast<uint32_t>(((t.n + 15) & ~15) >> 3) << 17);
+                if (!bounded_wait(tempty_bar(acc), acc_phase ^ 1u, wc, true)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 256);
+                for (int kb = 0; kb < p.kblocks[t.g]; ++kb) {
+                    if (!bounded_wait(full_bar(stage), phase, wc, true)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t soff = static_cast<uint64_t>(stage * G::STAGE_BYTES) >> 4;
+#pragma unroll
+                    for (int ks = 0; ks < BK / 16; ++ks) {
+                        const uint64_t bd = bdesc0 + soff + (ks * 32) / 16;
+                        const uint32_t accum = (kb != 0 || ks != 0) ? 1u : 0u;
+                        // SwiGLU: gate strips into columns 0-255, up strips into 256-511
+#pragma unroll
+                        for (int j = 0; j < (SWIGLU ? 2 : 1); ++j) {
+                            const uint64_t ad = adesc0 + soff + (j * 2 * STRIP_BYTES + ks * 2048) / 16;
+                            tc_mma_bf16_pair(d_tmem + static_cast<uint32_t>(256 * j), ad, bd, idesc, accum);
+                        }
+                    }
+                    tc_commit_pair_mc(empty_bar(stage), 3);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit_pair_mc(tfull_bar(acc), 3);
+                if (++acc == NACC) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            tc_commit_pair(drain_bar);
+            bounded_drain(drain_bar, 0, p.timeout_ns, p.err);
+        }
+    } else {
+        // ---------------- epilogue warps 2..9 (both CTAs) ----------------
+        const int q = warp & 3;            // TMEM lane quarter: features 32q .. 32q + 31
+        const int half = (warp - 2) >> 2;  // token columns [128 half, 128 half + 128)
+        uint4* stg = reinterpret_cast<uint4*>(smem + G::STG_OFF + (warp - 2) * STG_BYTES);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int u = unit0; u < total; u += ustep) {
+            const SUnit t = decode_sunit(u, p, total0, s_mtp, s_off);
+            int ok = 1;
+            if (lane == 0) ok = bounded_wait(tfull_bar(acc), acc_phase, wc) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * 256) + (static_cast<uint32_t>(q * 32) << 16);
+            const int N = p.N[t.g];
+            const int fl = SW_FPC * rank + 32 * q;  // this warp's first feature in the unit
+            const int lim = N - (t.f0 + fl);
+            const int c0 = 128 * half;
+            if (SWIGLU) {
+                const size_t pitch = static_cast<size_t>(p.out_ld[t.g]) * 2;
+                const int vch = lim <= 0 ? 0 : (lim >= 32 ? 4 : lim / 8);
+                char* base = static_cast<char*>(p.out[t.g]) + static_cast<size_t>(t.out_col0 + fl) * 2;
+                const int c1 = min(c0 + 128, t.n);
+#pragma unroll 1
+                for (int c = c0; c < c1; c += 32) {
+                    uint32_t g0[16], g1[16], u0[16], u1[16];
+                    tc_ld_32x32b_x16(tb + c, g0);
+                    tc_ld_32x32b_x16(tb + c + 16, g1);
+                    tc_ld_32x32b_x16(tb + 256 + c, u0);
+                    tc_ld_32x32b_x16(tb + 256 + c + 16, u1);
+                    tc_wait_ld();
+                    float h[32];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float ga = __uint_as_float(g0[i]), gb = __uint_as_float(g1[i]);
+                        h[i] = __fdividef(ga, 1.0f + __expf(-ga)) * __uint_as_float(u0[i]);
+                        h[16 + i] = __fdividef(gb, 1.0f + __expf(-gb)) * __uint_as_float(u1[i]);
+                    }
+                    warp_stage_bf16_column(stg, lane, h);
+                    warp_flush_block(stg, lane, base + static_cast<size_t>(t.row0 + c) * pitch, pitch,
+                                     t.n - c, vch);
+                }
+            } else {
+                const size_t pitch = static_cast<size_t>(p.out_ld[t.g]) * 4;
+                const int vch = lim <= 0 ? 0 : (lim >= 32 ? 8 : lim / 4);
+                char* base = static_cast<char*>(p.out[t.g]) + static_cast<size_t>(t.out_col0 + fl) * 4;
+                // the row scales of this warp's 128 tokens, lane l holding tokens c0 + 32 j + l
+                float rs[4];
+                const bool scale = t.g == 0 && p.rowscale0 != nullptr;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int ti = c0 + 32 * j + lane;
+                    rs[j] = (scale && ti < t.n) ? p.rowscale0[t.row0 + ti] : 1.0f;
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int c = c0 + 16 * i;
+                    if (c < t.n) {
+                        uint32_t r[16];
+                        tc_ld_32x32b_x16(tb + c, r);
+                        tc_wait_ld();
+                        float v[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            v[e] = __shfl_sync(0xffffffffu, rs[i >> 1], 16 * (i & 1) + e) * __uint_as_float(r[e]);
+                        warp_store_f32_columns(stg, lane, v, base + static_cast<size_t>(t.row0 + c) * pitch, pitch,
+                                               t.n - c, vch);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (rank == 1)
+                    mbar_arrive_remote(map_shared_rank(tempty_bar(acc), 0));
+                else
+                    mbar_arrive(tempty_bar(acc));
+            }
+            if (++acc == NACC) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    // no CTA of the pair leaves while the other may still touch its shared
+    // memory, barriers or tensor memory
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
 bool make_A_map(CUtensorMap* m, const void* A, int rows, int K, int lda) {
     // K: the columns of A the reduction reads
     const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rows)};
@@ -930,6 +1295,122 @@ cudaError_t launch_tc_t(const TcGemmArgs& a, int nstrip, int slots, cudaStream_t
                           dim3(THREADS), Geo<false>::SMEM_BYTES, s, p);
 }
 
+// The token-column CTA-pair form (tc_token_pair_kernel).
+template <bool SWIGLU>
+bool prepare_token_kernel(int dev) {
+    static bool attr_set[64] = {};
+    if (dev < 0 || dev >= 64) return false;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(tc_token_pair_kernel<SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 TGeo<SWIGLU>::SMEM_BYTES) != cudaSuccess)
+            return false;
+        attr_set[dev] = true;
+    }
+    return true;
+}
+
+template <bool SWIGLU>
+int token_pair_slots(int dev) {
+    static int cache[64] = {};
+    if (dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int n = -1;
+        if (prepare_token_kernel<SWIGLU>(dev)) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2 * static_cast<unsigned>(num_sms()));
+            cfg.blockDim = dim3(THREADS);
+            cfg.dynamicSmemBytes = TGeo<SWIGLU>::SMEM_BYTES;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int c = 0;
+            if (cudaOccupancyMaxActiveClusters(&c, tc_token_pair_kernel<SWIGLU>, &cfg) == cudaSuccess && c > 0)
+                n = c;
+            else
+                cudaGetLastError();  // clear a failed query
+        }
+        cache[dev] = n;
+    }
+    return cache[dev] > 0 ? cache[dev] : 0;
+}
+
+// Whether a forward launch takes the token-column form: the SwiGLU or the
+// plain product (FP32 output, no addend), no k remaps or split, no gate/up
+// products kept, and routed segments of 128 to 511 rows on average, where
+// the row-tile forms would run single-CTA 128-row tiles that pad each
+// segment by 64 rows on average. Shorter segments leave the pair's 256 MMA
+// rows of weights for few tokens; from 512 rows on the row-tile CTA pair,
+// whose epilogue overlaps the next tile, measured faster (medium prefill
+// gate/up 1116 against 1198 us). The environment variable MOE_GEMM_FORM
+// overrides the choice for tests and tuning: "rows" never takes the token
+// form, "tokens" takes it whenever the product allows it.
+template <int MODE>
+bool token_form_ok(const TcGemmArgs& a) {
+    if (MODE != TC_SWIGLU && MODE != TC_PLAIN) return false;
+    if (a.addend != nullptr || !a.g[0].enabled || a.mt_prefix == nullptr) return false;
+    for (int g = 0; g < 2; ++g) {
+        const TcGroup& G = a.g[g];
+        if (!G.enabled) continue;
+        if (G.a_kmod || G.b_kmod || G.a_kgroup || G.ksplit > 1 || G.a_out != nullptr ||
+            (G.b_rows && G.b_rows != G.K))
+            return false;
+        if (MODE == TC_PLAIN && G.out_f32 != 1) return false;
+        if (MODE == TC_SWIGLU && G.out_f32 != 0) return false;
+    }
+    const char* e = getenv("MOE_GEMM_FORM");
+    if (e != nullptr && e[0] == 'r') return false;
+    if (e != nullptr && e[0] == 't') return true;
+    const long long E = a.E > 0 ? a.E : 1;
+    return a.g[0].rows >= 128LL * E && a.g[0].rows < 512LL * E;
+}
+
+template <bool SWIGLU>
+cudaError_t launch_token_t(const TcGemmArgs& a, int slots, cudaStream_t s) {
+    TcParams p;
+    memset(&p, 0, sizeof(p));
+    p.bno = 2 * SW_FPC;  // output features of a pair per unit
+    const int strips = 2;  // 64-column strips per matrix and CTA
+    long long units_bound = 0;
+    for (int g = 0; g < 2; ++g) {
+        const TcGroup& G = a.g[g];
+        p.enabled[g] = G.enabled;
+        if (!G.enabled) continue;
+        if (!make_A_map(&p.mapA[g], G.A, G.rows, G.K, G.lda)) return cudaErrorInvalidValue;
+        p.b_wide[g] = G.N % 64 == 0 && make_B_strip_map(&p.mapB0[g], G.B0, G.Z, G.K, G.N, strips) &&
+                      (!SWIGLU || make_B_strip_map(&p.mapB1[g], G.B1, G.Z, G.K, G.N, strips));
+        if (!p.b_wide[g]) {
+            if (!make_B_map(&p.mapB0[g], G.B0, G.Z, G.K, G.N)) return cudaErrorInvalidValue;
+            if (SWIGLU && !make_B_map(&p.mapB1[g], G.B1, G.Z, G.K, G.N)) return cudaErrorInvalidValue;
+        }
+        p.kblocks[g] = (G.K + BK - 1) / BK;
+        p.rows[g] = G.rows;
+        p.N[g] = G.N;
+        p.nt[g] = (G.N + p.bno - 1) / p.bno;
+        p.Z[g] = G.Z;
+        p.out[g] = G.out;
+        p.out_ld[g] = G.out_ld;
+        p.out_f32[g] = G.out_f32;
+        const long long mt = (G.rows + SW_TOK - 1) / SW_TOK;
+        units_bound += g == 0 ? (mt + a.E) * p.nt[0] : mt * G.Z * p.nt[1];
+    }
+    p.E = a.E;
+    p.mt1 = a.g[1].enabled ? (a.g[1].rows + SW_TOK - 1) / SW_TOK : 0;
+    p.offsets = a.offsets;
+    p.mt_prefix = a.mt_prefix + a.E + 1;  // tiles of 256 rows per expert
+    p.rowscale0 = a.rowscale0;
+    p.err = a.err;
+    p.timeout_ns = wait_timeout_ns();
+    long long grid = slots;
+    if (units_bound < grid) grid = units_bound;
+    if (grid < 1) grid = 1;
+    return launch_pdl_cluster(tc_token_pair_kernel<SWIGLU>, dim3(2 * static_cast<unsigned>(grid)),
+                              dim3(THREADS), TGeo<SWIGLU>::SMEM_BYTES, s, 2, p);
+}
+
 template <int MODE>
 cudaError_t launch_tc_s(const TcGemmArgs& a, cudaStream_t s) {
     constexpr bool SWIGLU = MODE == TC_SWIGLU || MODE == TC_SWIGLU_BWD;
@@ -949,6 +1430,12 @@ cudaError_t launch_tc_s(const TcGemmArgs& a, cudaStream_t s) {
     const bool long_segments =
         !a.g[0].enabled || static_cast<long long>(a.g[0].rows) >= 512LL * (a.E > 0 ? a.E : 1);
     const bool dense_plain = MODE == TC_PLAIN && !a.g[0].enabled;
+    if constexpr (MODE == TC_SWIGLU || MODE == TC_PLAIN) {
+        if (token_form_ok<MODE>(a)) {
+            const int slots = token_pair_slots<MODE == TC_SWIGLU>(dev);
+            if (slots > 0) return launch_token_t<MODE == TC_SWIGLU>(a, slots, s);
+        }
+    }
     if constexpr (MODE != TC_PLAIN_ACC) {
         const int slots = (even && long_segments && !dense_plain) ? pair_slots<MODE>(dev) : 0;
         if (slots > 0) return launch_tc_t<MODE, true>(a, nstrip, slots, s);

@@ -29,6 +29,55 @@ MOE_DEV void warp_store_block(uint4* stg, const uint4 (&v)[4], int lane, char* r
     __syncwarp();
 }
 
+// The global half of warp_store_block, for a block already in the staging
+// buffer in its swizzled layout (chunk c of row r at 16-byte slot
+// r * 4 + (c ^ ((r >> 1) & 3))).
+MOE_DEV void warp_flush_block(const uint4* stg, int lane, char* row0, size_t pitch, int valid_rows,
+                              int valid_chunks) {
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int row = 8 * i + (lane >> 2);
+        const int ch = lane & 3;
+        const uint4 w = stg[row * 4 + (ch ^ ((row >> 1) & 3))];
+        if (row < valid_rows && ch < valid_chunks)
+            *reinterpret_cast<uint4*>(row0 + row * pitch + ch * 16) = w;
+    }
+    __syncwarp();
+}
+
+// Column `lane` of a 32-row x 32-column BF16 block into the staging buffer in
+// warp_flush_block's layout: v[i] is row i.
+MOE_DEV void warp_stage_bf16_column(uint4* stg, int lane, const float (&v)[32]) {
+    unsigned short* b = reinterpret_cast<unsigned short*>(stg);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const __nv_bfloat16 h = __float2bfloat16_rn(v[i]);
+        b[(i * 4 + ((lane >> 3) ^ ((i >> 1) & 3))) * 8 + (lane & 7)] = *reinterpret_cast<const unsigned short*>(&h);
+    }
+}
+
+// A 16-row x 32-column FP32 block, column `lane` from v (v[i] is row i),
+// stored row-major (128 bytes per row) from the staging buffer: every store
+// instruction moves 4 rows x 128 contiguous bytes. Rows >= valid_rows and
+// 16-byte chunks >= valid_chunks are not written.
+MOE_DEV void warp_store_f32_columns(uint4* stg, int lane, const float (&v)[16], char* row0, size_t pitch,
+                                    int valid_rows, int valid_chunks) {
+    float* f = reinterpret_cast<float*>(stg);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) f[i * 32 + lane] = v[i];
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int idx = lane + 32 * k;
+        const int row = idx >> 3, ch = idx & 7;
+        const uint4 w = stg[idx];
+        if (row < valid_rows && ch < valid_chunks)
+            *reinterpret_cast<uint4*>(row0 + row * pitch + ch * 16) = w;
+    }
+    __syncwarp();
+}
+
 // Loads the block in two steps, so that the global loads can be in flight
 // while other work runs: warp_load_issue reads it row-major (rows >=
 // valid_rows as zeros) into w, warp_load_finish turns w into the lane = row
