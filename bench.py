@@ -390,6 +390,16 @@ def time_oracle(name: str, tokens: list, pool, workers: int, seed: int = 0) -> d
 # GPU arm
 # ---------------------------------------------------------------------------
 
+def gemm_kernel_name(w) -> str:
+    """The grouped GEMM kernel the forward's gate/up launch takes: the
+    token-column CTA pair where routed segments average 128 to 511 rows (the
+    library's rule, MOE_GEMM_FORM overriding it), else the row-tile kernel."""
+    form = os.environ.get("MOE_GEMM_FORM", "")
+    rows, E = w.T * w.K, w.E
+    token = form.startswith("t") or (not form.startswith("r") and 128 * E <= rows < 512 * E)
+    return "tc_token_pair_kernel<SwiGLU>" if token else "tc_grouped_gemm_kernel<SwiGLU>"
+
+
 def gate_up_roofline(w, gu_ms, counts, pk, name):
     """The grouped gate/up launch against the roof that bounds it: tensor on
     prefill batches, HBM (weight streaming) on decode batches, FP32 FFMA for
@@ -407,12 +417,12 @@ def gate_up_roofline(w, gu_ms, counts, pk, name):
                 "peak_source": "FP32 FFMA: 152 SMs x 128 lanes x 2 FLOP x max SM clock",
                 "flops_per_launch": gu_flops}
     elif hbm:
-        roof = {"kernel": "tc_grouped_gemm_kernel<SwiGLU> (gate_up)", "bound": "hbm",
+        roof = {"kernel": gemm_kernel_name(w) + " (gate_up)", "bound": "hbm",
                 "achieved": gu_bytes / (gu_ms / 1e3) / 1e9 if ok else None,
                 "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "peak_source": f"{pk['source']} HBM copy", "bytes_per_launch": gu_bytes}
     else:
-        roof = {"kernel": "tc_grouped_gemm_kernel<SwiGLU> (gate_up)", "bound": "tensor",
+        roof = {"kernel": gemm_kernel_name(w) + " (gate_up)", "bound": "tensor",
                 "achieved": gu_flops / (gu_ms / 1e3) / 1e12 if ok else None,
                 "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                 "peak_source": f"{pk['source']} bf16 burst", "flops_per_launch": gu_flops}
