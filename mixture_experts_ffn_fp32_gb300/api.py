@@ -472,7 +472,7 @@ def selftest_wait_timeout(ms: int, ws: torch.Tensor, stream=None) -> int:
 
 
 STAGES = ["router", "latent_down", "dispatch", "gather", "gate_up", "down", "combine", "latent_up",
-          "decode_fused"]
+          "decode_fused", "route_dispatch_gather"]
 
 
 class StageTimer:

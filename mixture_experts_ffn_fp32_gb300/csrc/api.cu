@@ -212,6 +212,9 @@ WsLayout plan_workspace(const moe_config& c) {
     L.logits = take(T * E * 4);
     L.stats_part = take(((T + STATS_TOKENS - 1) / STATS_TOKENS) * (2 * E + 1) * 4);
     L.dctr = take((E + 3) * 4);
+    const bool fsw = bf && c.latent_dim == 0 && E <= 8 && TK > 1024 && TK <= DISPATCH_WIDE_MAX;
+    L.fs_tags = fsw ? take(FRONT_SMALL_MAX_CTAS * 128) : 0;
+    L.fs_cnt = fsw ? take(FRONT_SMALL_MAX_CTAS * 8 * 4) : 0;
     L.total = o;
     return L;
 }
@@ -220,10 +223,10 @@ WsLayout plan_workspace(const moe_config& c) {
 // Stage timing (instrumentation)
 // ---------------------------------------------------------------------------
 enum Stage { ST_ROUTE = 0, ST_LATENT_DOWN, ST_DISPATCH, ST_GATHER, ST_GATEUP, ST_DOWN, ST_COMBINE,
-             ST_LATENT_UP, ST_FUSED, ST_COUNT };
+             ST_LATENT_UP, ST_FUSED, ST_FRONT, ST_COUNT };
 static const char* kStageNames[ST_COUNT] = {"router", "latent_down", "dispatch", "gather",
                                             "gate_up", "down", "combine", "latent_up",
-                                            "decode_fused"};
+                                            "decode_fused", "route_dispatch_gather"};
 
 struct Timing {
     std::mutex mu;
@@ -358,7 +361,6 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
     da.ticket = err + 1;
 
     // 1. router (with the dispatch, for a decode batch)
-    rec.begin(ST_ROUTE);
     RouterArgs ra = router_args(c, x, static_cast<const float*>(w.W_router),
                                 static_cast<const float*>(w.bias));
     ra.idx = idx;
@@ -371,11 +373,21 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
         ra.zero = static_cast<unsigned*>(P(L.dctr));
         ra.nzero = E + 3;
     }
-    {
+    // few experts, a prefill batch: router, dispatch and row gather in one launch
+    const bool front = !fused && L.fs_tags != 0 && front_small_ok(T, c.d, E, K);
+    if (front) {
+        rec.begin(ST_FRONT);
+        ra.err_clear = err;
+        if ((e = launch_front_small(ra, da, P(L.xs), static_cast<unsigned long long*>(P(L.fs_tags)),
+                                    static_cast<int*>(P(L.fs_cnt)), s)) != cudaSuccess)
+            return cuda_status(e);
+        rec.end(ST_FRONT);
+    } else {
+        rec.begin(ST_ROUTE);
         const moe_status rs = run_router(c, ra, static_cast<const float*>(w.W_router), x, ws, L, s);
         if (rs != MOE_OK) return rs;
+        rec.end(ST_ROUTE);
     }
-    rec.end(ST_ROUTE);
 
     if (fused) {
         // 2. everything else in one launch
@@ -413,11 +425,14 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
 
     // 2. dispatch (BF16 batches of up to DISPATCH_WIDE_MAX assignments: with the row
     //    gather, one launch)
-    rec.begin(ST_DISPATCH);
+    // (a stage without a launch records no events: its time is nil)
     const bool dg1 = bf && L.nchunks == 1;
     const bool dgw = bf && !dg1 && TK <= DISPATCH_WIDE_MAX;
-    const bool dg = dg1 || dgw;
-    if (dg1) {
+    const bool dg = dg1 || dgw || front;
+    if (!front) rec.begin(ST_DISPATCH);
+    if (front) {
+        // done by the front-end launch
+    } else if (dg1) {
         if ((e = launch_dispatch_gather(da, ex_src, de * 2, P(L.xs), s)) != cudaSuccess)
             return cuda_status(e);
     } else if (dgw) {
@@ -426,16 +441,18 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
     } else if ((e = launch_dispatch(da, s, nullptr)) != cudaSuccess) {
         return cuda_status(e);
     }
-    rec.end(ST_DISPATCH);
+    if (!front) rec.end(ST_DISPATCH);
 
     if (bf) {
         float* ys = static_cast<float*>(P(L.ys));
         float* shout = S ? static_cast<float*>(P(L.shout)) : nullptr;
         // 3. gather the routed rows into expert order
-        rec.begin(ST_GATHER);
-        if (!dg && (e = launch_gather_rows(ex_src, sorted_token, TK, de * 2, P(L.xs), s)) != cudaSuccess)
-            return cuda_status(e);
-        rec.end(ST_GATHER);
+        if (!dg) {
+            rec.begin(ST_GATHER);
+            if ((e = launch_gather_rows(ex_src, sorted_token, TK, de * 2, P(L.xs), s)) != cudaSuccess)
+                return cuda_status(e);
+            rec.end(ST_GATHER);
+        }
 
         // 4. gate/up with the SiLU(gate) * up epilogue: routed experts (group 0, on the
         //    sorted rows) and shared experts (group 1, on x) in one launch

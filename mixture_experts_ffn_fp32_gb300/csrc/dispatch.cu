@@ -674,6 +674,18 @@ cudaError_t launch_gather_sum(const float* ys, const int32_t* inv, int T, int K,
                                  inv, T, K, cols, addend, out)                                   \
                     : launch_pdl(gather_sum_kernel<false, KM, NB>, ysplit(NB), dim3(256), 0, s, ys, \
                                  inv, T, K, cols, addend, out)
+    // Many tokens: one 256-column batch per warp, the batches of a token on
+    // separate CTAs, so that few registers keep every warp resident (NB > 1
+    // holds more loads per lane in flight, for batches of few tokens).
+    const int batches1 = (cols + 255) / 256;
+    if (K <= 4 && static_cast<long long>(T) * batches1 >= 64LL * num_sms()) {
+        const dim3 g1(blocks, static_cast<unsigned>(batches1));
+        if (K <= 2)
+            return out_bf16 ? launch_pdl(gather_sum_kernel<true, 2, 1>, g1, dim3(256), 0, s, ys, inv, T, K, cols, addend, out)
+                            : launch_pdl(gather_sum_kernel<false, 2, 1>, g1, dim3(256), 0, s, ys, inv, T, K, cols, addend, out);
+        return out_bf16 ? launch_pdl(gather_sum_kernel<true, 4, 1>, g1, dim3(256), 0, s, ys, inv, T, K, cols, addend, out)
+                        : launch_pdl(gather_sum_kernel<false, 4, 1>, g1, dim3(256), 0, s, ys, inv, T, K, cols, addend, out);
+    }
     if (K <= 2) MOE_GS(2, 4);
     if (K <= 4) MOE_GS(4, 2);
     if (K <= 8) MOE_GS(8, 1);

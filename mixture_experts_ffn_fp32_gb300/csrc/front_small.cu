@@ -1,0 +1,348 @@
+// K1+K2 in one launch for prefill batches of a BF16 layer with few experts
+// (E <= 8, 1024 < T*K <= 16384, no latent projection): router, dispatch and
+// row gather. It replaces the router launch and the dispatch-and-gather
+// launch, whose dispatch every CTA recomputed from all T*K assignments.
+//
+// What it computes is exactly what those two launches compute (same logits
+// bit for bit, same routing, same integer dispatch):
+//   r[t, :] = x[t, :] W_router (FP32), the gate rule's top-K (APEX-1
+//   Mathematical Reference Part 3 section 13.1; "MoE from scratch"
+//   MoELayer.forward), then the stable counting sort of the T*K (token, slot)
+//   assignments by expert (kimi_k3 StableLatentMoE "Grouped expert
+//   execution": tokens of one expert in token order) and xs[pos] = x[token].
+//
+// Shape: one CTA per SM at most, launched cooperatively (all CTAs resident at
+// once). CTA b routes a contiguous block of tokens, so its assignments are a
+// contiguous range of the (token, slot) order:
+//   1. its tokens' x rows into shared memory with every load in flight, one
+//      warp per token (lane l takes the d-index pairs 2l + 64m in increasing m,
+//      the fused multiply-adds of the standalone router in the same order,
+//      then the same butterfly and the same per-token routing);
+//   2. its per-expert counts into its slot of a global table, then its tag
+//      (the launch's %gridid, unique per launch in a context) with release
+//      order; every CTA waits, with a time limit, until all tags carry this
+//      launch's id - a grid barrier that needs no zeroed memory, so a dirty
+//      workspace and graph replays are fine;
+//   3. expert totals, the CTA's prefix per expert (counts of the CTAs before
+//      it), offsets and tile prefixes (CTA 0 writes them), ranks inside the
+//      range (warp match), sorted_token / sorted_w / inv, and the rows copied
+//      into xs from shared memory.
+#include "common.cuh"
+#include "internal.h"
+#include "route_dev.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int FS_THREADS = 512;
+constexpr int FS_WARPS = FS_THREADS / 32;
+constexpr size_t FS_SMEM_MAX = 190 * 1024;  // dynamic; the static arrays take up to ~31 KB
+constexpr int FS_MAX_G = 256;  // blocks at most (one per SM)
+// tags one 128-byte line apart, so that the polls of all blocks spread over
+// many L2 lines instead of queueing on a few
+constexpr int FS_TAG_STRIDE = 16;
+
+MOE_DEV unsigned long long grid_id() {
+    unsigned long long g;
+    asm volatile("mov.u64 %0, %%gridid;" : "=l"(g));
+    return g;
+}
+
+MOE_DEV void st_release_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+MOE_DEV unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Acquire side of the tags: after relaxed loads saw every tag, this fence
+// orders them before the loads of the counts (release-acquire through a fence).
+MOE_DEV void fence_acquire_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+template <int EP>
+__global__ void __launch_bounds__(FS_THREADS, 1) front_small_kernel(RouterArgs ra, DispatchArgs da, int tpc,
+                                                                    void* __restrict__ xs,
+                                                                    unsigned long long* __restrict__ tags,
+                                                                    int* __restrict__ cnt,
+                                                                    uint64_t timeout_ns) {
+    extern __shared__ __align__(16) uint8_t xsm[];
+    __shared__ int s_cnt[EP], s_base[EP], s_rank[FS_WARPS][EP];
+    __shared__ int s_pos[FS_WARPS * 32], s_tok[FS_WARPS * 32], s_ids[FS_WARPS * 32];
+    __shared__ float s_logit[FS_WARPS * 32 * EP];  // the block's logits (tpc <= FS_WARPS * 32)
+    __shared__ int s_ok;
+    __shared__ int s_all[FS_MAX_G * EP];  // every block's counts
+    pdl_wait();
+    pdl_trigger();
+    const int b = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (ra.err_clear != nullptr && b == 0 && threadIdx.x == 0) clear_status(ra.err_clear);
+    const int E = ra.E, K = ra.K, d = ra.d, T = ra.T;
+    const int t0 = min(T, b * tpc), t1 = min(T, t0 + tpc);
+    const int nt = t1 - t0;
+    if (threadIdx.x < EP) s_cnt[threadIdx.x] = 0;
+    for (int i = threadIdx.x; i < FS_WARPS * EP; i += FS_THREADS) (&s_rank[0][0])[i] = 0;
+
+    // 1. stage the block's x rows and W_router (EP columns, zero beyond E) with
+    //    every load in flight, then route: warp w takes tokens w and w + 16
+    //    together (the W_router values it reads serve both)
+    const int xbytes = nt * d * 2;
+    float* wsm = reinterpret_cast<float*>(xsm + ((tpc * d * 2 + 15) & ~15));
+    {
+        // up to 8 x pieces and 8 W_router values per thread in flight per round
+        // (one round for the small layer) before any of them is stored
+        const int nvec = xbytes / 16, nw = d * EP;
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(ra.x) +
+                                                          static_cast<size_t>(t0) * d);
+        uint4* dst = reinterpret_cast<uint4*>(xsm);
+        const int n = nvec > nw ? nvec : nw;
+        for (int base = threadIdx.x; base < n; base += 8 * FS_THREADS) {
+            uint4 xv[8];
+            float wv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int q = base + u * FS_THREADS;
+                if (q < nvec) xv[u] = __ldg(src + q);
+                wv[u] = 0.0f;
+                if (q < nw) {
+                    const int k = q / EP, e = q - k * EP;
+                    if (e < E) wv[u] = __ldg(ra.W + static_cast<size_t>(k) * E + e);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int q = base + u * FS_THREADS;
+                if (q < nvec) dst[q] = xv[u];
+                if (q < nw) wsm[q] = wv[u];
+            }
+        }
+    }
+    __syncthreads();
+    for (int i = warp; i < nt; i += 2 * FS_WARPS) {
+        const int i2 = i + FS_WARPS;
+        const bool two = i2 < nt;
+        const uint32_t* xa = reinterpret_cast<const uint32_t*>(xsm) + static_cast<size_t>(i) * (d >> 1);
+        const uint32_t* xb = reinterpret_cast<const uint32_t*>(xsm) + static_cast<size_t>(two ? i2 : i) * (d >> 1);
+        float acc[EP], acc2[EP];
+#pragma unroll
+        for (int e = 0; e < EP; ++e) acc[e] = acc2[e] = 0.0f;
+        // lane l: d-index pairs k = 2 l + 64 m, m increasing (the standalone
+        // router's order), one fused multiply-add chain per expert
+        for (int k = 2 * lane; k < d; k += 64) {
+            const uint32_t va = xa[k >> 1], vb = xb[k >> 1];
+            const float a0 = bf16_lo(va), a1 = bf16_hi(va), b0 = bf16_lo(vb), b1 = bf16_hi(vb);
+            // rows k and k + 1 of W_router: 2 EP contiguous floats, 16-byte loads
+            const float4* w4 = reinterpret_cast<const float4*>(wsm + static_cast<size_t>(k) * EP);
+            float wr0[EP], wr1[EP];
+#pragma unroll
+            for (int e = 0; e < EP; e += 4) {
+                const float4 p0 = w4[e / 4], p1 = w4[EP / 4 + e / 4];
+                wr0[e] = p0.x; wr0[e + 1] = p0.y; wr0[e + 2] = p0.z; wr0[e + 3] = p0.w;
+                wr1[e] = p1.x; wr1[e + 1] = p1.y; wr1[e + 2] = p1.z; wr1[e + 3] = p1.w;
+            }
+#pragma unroll
+            for (int e = 0; e < EP; ++e) {
+                acc[e] = fmaf(a1, wr1[e], fmaf(a0, wr0[e], acc[e]));
+                acc2[e] = fmaf(b1, wr1[e], fmaf(b0, wr0[e], acc2[e]));
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < EP; ++e) {
+            acc[e] = warp_sum(acc[e]);
+            acc2[e] = warp_sum(acc2[e]);
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int e = 0; e < EP; ++e) s_logit[i * EP + e] = acc[e];
+        }
+        if (lane == 1 && two) {
+#pragma unroll
+            for (int e = 0; e < EP; ++e) s_logit[i2 * EP + e] = acc2[e];
+        }
+    }
+    __syncthreads();
+    // one thread per token: the per-token routing is a serial chain, so all of
+    // the block's tokens take it side by side
+    if (threadIdx.x < nt) {
+        float r[EP];
+#pragma unroll
+        for (int e = 0; e < EP; ++e) r[e] = s_logit[threadIdx.x * EP + e];
+        route_token_seq<EP>(r, t0 + threadIdx.x, ra, s_ids + threadIdx.x * K);
+    }
+    __syncthreads();  // the block's ids are in s_ids
+
+    // 2. the block's counts and tag; wait for every block's
+    const int j0 = t0 * K, j1 = t1 * K;
+    for (int j = threadIdx.x; j < j1 - j0; j += FS_THREADS) {
+        const int e = s_ids[j];
+        if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+    }
+    __syncthreads();
+    const unsigned long long gid = grid_id();
+    if (threadIdx.x == 0) {
+        // the counts, then the tag with release order (same thread)
+#pragma unroll
+        for (int e = 0; e < EP; ++e) cnt[static_cast<size_t>(b) * EP + e] = s_cnt[e];
+        st_release_u64(tags + FS_TAG_STRIDE * b, gid);
+    }
+    if (warp == 0) {
+        // lane l watches tags l, l + 32, ... (all of its loads in flight each round)
+        bool ok = true;
+        const uint64_t start = globaltimer_ns();
+        uint32_t pending = 0;  // bit q: tag lane + 32 q not yet this launch's
+        for (int q = 0; q < 32 && lane + 32 * q < G; ++q) pending |= 1u << q;
+        while (pending) {
+            uint32_t still = 0;
+            for (int q = 0; q < 32; ++q)
+                if ((pending >> q) & 1u)
+                    if (ld_relaxed_u64(tags + FS_TAG_STRIDE * (lane + 32 * q)) != gid) still |= 1u << q;
+            pending = still;
+            if (pending) {
+                if (globaltimer_ns() - start > timeout_ns) {
+                    ok = false;
+                    break;
+                }
+                __nanosleep(128);  // fewer polls on the tags' lines while the writers arrive
+            }
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        fence_acquire_gpu();  // the tags seen order the counts read below
+        if (lane == 0) {
+            s_ok = ok ? 1 : 0;
+            if (!ok) atomicOr(da.err, ERRBIT_TIMEOUT);
+        }
+    }
+    __syncthreads();
+    if (!s_ok) return;
+
+    // 3. totals, offsets, the block's base per expert; ranks; rows
+    for (int i = threadIdx.x; i < G * EP; i += FS_THREADS) s_all[i] = __ldcg(cnt + i);
+    __syncthreads();
+    if (warp < EP) {
+        // warp e: the total of expert e and its count in the blocks before this one
+        int tot = 0, pre = 0;
+        if (warp < E)
+            for (int i = lane; i < G; i += 32) {
+                const int c = s_all[i * EP + warp];
+                tot += c;
+                pre += i < b ? c : 0;
+            }
+        tot = __reduce_add_sync(0xffffffffu, tot);
+        pre = __reduce_add_sync(0xffffffffu, pre);
+        if (lane == 0) {
+            s_cnt[warp] = tot;
+            s_base[warp] = pre;
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int tot = lane < E ? s_cnt[lane] : 0;
+        const int pre = lane < E ? s_base[lane] : 0;
+        const int bm = da.bm;
+        const int m1 = (tot + bm - 1) / bm, m2 = (tot + 2 * bm - 1) / (2 * bm);
+        int x = tot, x1 = m1, x2 = m2;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            const int y1 = __shfl_up_sync(0xffffffffu, x1, o);
+            const int y2 = __shfl_up_sync(0xffffffffu, x2, o);
+            if (lane >= o) {
+                x += y;
+                x1 += y1;
+                x2 += y2;
+            }
+        }
+        if (lane < E) {
+            s_base[lane] = x - tot + pre;
+            if (b == 0) {
+                da.counts[lane] = tot;
+                da.offsets[lane] = x - tot;
+                da.mt_prefix[lane] = x1 - m1;
+                da.mt_prefix[E + 1 + lane] = x2 - m2;
+                if (lane == E - 1) {
+                    da.offsets[E] = x;
+                    da.mt_prefix[E] = x1;
+                    da.mt_prefix[2 * E + 1] = x2;
+                }
+            }
+        }
+    }
+    {
+        const int j = j0 + 32 * warp + lane;
+        const bool mine = j < j1;
+        int e = mine ? s_ids[j - j0] : -1;
+        if (e < 0 || e >= E) e = -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        if (e >= 0 && rank == 0) s_rank[warp][e] = __popc(peers);
+        __syncthreads();
+        if (mine) {
+            int pos = -1;
+            if (e >= 0) {
+                pos = s_base[e] + rank;
+                for (int w = 0; w < warp; ++w) pos += s_rank[w][e];
+                da.sorted_token[pos] = j / K;
+                da.sorted_w[pos] = ra.w[j];
+                da.inv[j] = pos;
+            }
+            s_pos[j - j0] = pos;
+            s_tok[j - j0] = j / K - t0;
+        }
+    }
+    __syncthreads();
+    const int vpr = d / 8;  // 16-byte pieces per row
+    const uint4* rows = reinterpret_cast<const uint4*>(xsm);
+    uint4* out = static_cast<uint4*>(xs);
+    for (int r = warp; r < j1 - j0; r += FS_WARPS) {
+        const int pos = s_pos[r];
+        if (pos < 0) continue;
+        const uint4* sr = rows + static_cast<size_t>(s_tok[r]) * vpr;
+        uint4* dr = out + static_cast<size_t>(pos) * vpr;
+        for (int v = lane; v < vpr; v += 32) dr[v] = sr[v];
+    }
+}
+
+// Dynamic shared memory: the block's x rows, then W_router as [d, 8] FP32.
+size_t front_small_smem(int tpc, int d) {
+    return ((static_cast<size_t>(tpc) * d * 2 + 15) & ~static_cast<size_t>(15)) + static_cast<size_t>(d) * 8 * 4;
+}
+
+}  // namespace
+
+bool front_small_ok(int T, int d, int E, int K) {
+    const long long TK = static_cast<long long>(T) * K;
+    if (E < 1 || E > 8 || K < 1 || TK <= 1024 || TK > DISPATCH_WIDE_MAX || d % 8) return false;
+    const int G = num_sms() < FS_MAX_G ? num_sms() : FS_MAX_G;
+    const int tpc = (T + G - 1) / G;
+    return tpc * K <= FS_WARPS * 32 && front_small_smem(tpc, d) <= FS_SMEM_MAX;
+}
+
+cudaError_t launch_front_small(const RouterArgs& ra, const DispatchArgs& da, void* xs,
+                               unsigned long long* tags, int* cnt, cudaStream_t s) {
+    if (!front_small_ok(ra.T, ra.d, ra.E, ra.K) || !ra.x_bf16) return cudaErrorInvalidValue;
+    const int G0 = num_sms() < FS_MAX_G ? num_sms() : FS_MAX_G;
+    const int tpc = (ra.T + G0 - 1) / G0;
+    const int G = (ra.T + tpc - 1) / tpc;
+    const size_t smem = front_small_smem(tpc, ra.d);
+    static bool attr_set[64][2] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int which = ra.E <= 4 ? 0 : 1;
+    if (dev >= 0 && dev < 64 && !attr_set[dev][which]) {
+        const cudaError_t e = which == 0
+            ? cudaFuncSetAttribute(front_small_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(FS_SMEM_MAX))
+            : cudaFuncSetAttribute(front_small_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(FS_SMEM_MAX));
+        if (e != cudaSuccess) return e;
+        attr_set[dev][which] = true;
+    }
+    const uint64_t tmo = wait_timeout_ns();
+    return which == 0
+        ? launch_pdl_coop(front_small_kernel<4>, dim3(G), dim3(FS_THREADS), smem, s, ra, da, tpc, xs, tags, cnt, tmo)
+        : launch_pdl_coop(front_small_kernel<8>, dim3(G), dim3(FS_THREADS), smem, s, ra, da, tpc, xs, tags, cnt, tmo);
+}
+
+}  // namespace moe

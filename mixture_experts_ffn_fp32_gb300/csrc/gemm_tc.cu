@@ -680,15 +680,33 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
             } else {
                 float rs = 1.0f;
                 if (t.g == 0 && p.rowscale0 != nullptr && lane < valid_rows) rs = p.rowscale0[orow];
-                const float* arow = (t.g == 1 && p.addend != nullptr && lane < valid_rows)
-                                        ? p.addend + orow * static_cast<size_t>(p.add_ld)
-                                        : nullptr;
+                // the addend's rows of this warp, read row-major (8 rows x 64 contiguous
+                // bytes per load instruction) before the accumulator is waited for, then
+                // turned into the lane = row layout through the staging buffer
+                const bool add = t.g == 1 && p.addend != nullptr;
+                const size_t apitch = static_cast<size_t>(p.add_ld) * 4;
+                const char* add_rows = add ? reinterpret_cast<const char*>(p.addend) +
+                                                 static_cast<size_t>(my_out0 + q * 32) * apitch
+                                           : nullptr;
+                auto add_issue = [&](uint4 (&w)[4], int col) {
+                    const int lim = N - (t.n0 + col);  // valid columns from col
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int row = 8 * i + (lane >> 2), ch = lane & 3;
+                        w[i] = make_uint4(0u, 0u, 0u, 0u);
+                        if (row < valid_rows && 4 * ch + 4 <= lim)
+                            w[i] = *reinterpret_cast<const uint4*>(
+                                add_rows + row * apitch + static_cast<size_t>(t.out_col0 + col) * 4 + ch * 16);
+                    }
+                };
                 const int span = 32 * p.nstrip;  // this warp's columns: [half * span, +span)
                 // blocks of 64 bytes per row: 16 FP32 or 32 BF16 columns
                 const int bc = of32 ? 16 : 32;
 #pragma unroll 1
                 for (int c = half * span; c < half * span + span; c += bc) {
                     float v[32];
+                    uint4 aw[4];
+                    if (add) add_issue(aw, c);
                     uint32_t r0[16], r1[16];
                     tc_ld_32x32b_x16(tb + c, r0);
                     if (!of32) tc_ld_32x32b_x16(tb + c + 16, r1);
@@ -699,17 +717,25 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
                         v[16 + i] = of32 ? 0.0f : rs * __uint_as_float(r1[i]);
                     }
                     const int lim = N - (t.n0 + c);
-                    if (arow != nullptr && lim > 0) {
-                        const float* ap = arow + t.out_col0 + c;
-                        const int n = lim < bc ? lim : bc;
+                    if (add) {
+                        uint4 av[4];
+                        warp_load_finish(stg, aw, av, lane);
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4) {
-                            if (i < n) {
-                                const float4 a4 = *reinterpret_cast<const float4*>(ap + i);
-                                v[i] += a4.x;
-                                v[i + 1] += a4.y;
-                                v[i + 2] += a4.z;
-                                v[i + 3] += a4.w;
+                        for (int j = 0; j < 4; ++j) {
+                            v[4 * j] += __uint_as_float(av[j].x);
+                            v[4 * j + 1] += __uint_as_float(av[j].y);
+                            v[4 * j + 2] += __uint_as_float(av[j].z);
+                            v[4 * j + 3] += __uint_as_float(av[j].w);
+                        }
+                        if (!of32) {
+                            add_issue(aw, c + 16);
+                            warp_load_finish(stg, aw, av, lane);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                v[16 + 4 * j] += __uint_as_float(av[j].x);
+                                v[16 + 4 * j + 1] += __uint_as_float(av[j].y);
+                                v[16 + 4 * j + 2] += __uint_as_float(av[j].z);
+                                v[16 + 4 * j + 3] += __uint_as_float(av[j].w);
                             }
                         }
                     }

@@ -54,6 +54,35 @@ cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, 
     note_launch();
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
+// The same as a cooperative launch (every CTA resident at once; the grid must
+// fit the device). Programmatic serialisation is requested too; where the
+// runtime refuses the pair, the launch goes without it (decided once).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_coop(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t s, Args&&... args) {
+    static int with_pdl = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = with_pdl ? 2 : 1;
+    note_launch();
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    if (e != cudaSuccess && with_pdl) {
+        cudaGetLastError();
+        with_pdl = 0;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    }
+    return e;
+}
 // Wait limit of device-side bounded waits, in ns.
 uint64_t wait_timeout_ns();
 // Number of SMs of the current device (cached per device).
@@ -75,6 +104,7 @@ struct WsLayout {
     size_t ga, gu, gas, gus;  // saved gate / up products (save_gate_up): routed rows, shared
     size_t logits, stats_part;  // routing diagnostics: r [T, E], per-CTA partial sums
     size_t dctr;                // fused decode back end: counters [E + 3]
+    size_t fs_tags, fs_cnt;     // one-launch front end (front_small.cu): CTA tags, CTA counts
     size_t total;
     int nchunks;
 };
@@ -148,6 +178,15 @@ cudaError_t launch_dispatch_gather(const DispatchArgs& a, const void* src, int r
 constexpr int DISPATCH_WIDE_MAX = 16384;
 cudaError_t launch_dispatch_gather_wide(const DispatchArgs& a, const void* src, int row_bytes,
                                         void* dst, cudaStream_t s);
+
+// Router, dispatch and row gather in one cooperative launch (front_small.cu)
+// for BF16 x, E <= 8, 1024 < T*K <= DISPATCH_WIDE_MAX. tags: FRONT_SMALL_MAX_CTAS
+// 128-byte lines (one 64-bit tag each), cnt: FRONT_SMALL_MAX_CTAS * 8 ints of
+// scratch (no initial state needed).
+constexpr int FRONT_SMALL_MAX_CTAS = 256;
+bool front_small_ok(int T, int d, int E, int K);
+cudaError_t launch_front_small(const RouterArgs& ra, const DispatchArgs& da, void* xs,
+                               unsigned long long* tags, int* cnt, cudaStream_t s);
 
 // dst[r, :] = src[rowidx[r], :] for r < rows, row_bytes a multiple of 16.
 cudaError_t launch_gather_rows(const void* src, const int32_t* rowidx, int rows, int row_bytes,

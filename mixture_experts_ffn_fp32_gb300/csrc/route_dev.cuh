@@ -98,36 +98,46 @@ MOE_DEV void route_token_warp(const float (&r)[J], const float (&bj)[J], int t, 
     for (int j = 0; j < J; ++j)
         if (!(c[j] == c[j])) c[j] = -INFINITY;
 
+    // Selection of the nsel largest candidates (ties: the lower expert id), one
+    // per step: every lane keeps its best remaining candidate as an
+    // order-preserving 32-bit key (-0 counted as +0, so equal values give equal
+    // keys); the warp's largest key and, among the lanes holding it, the
+    // lowest expert id come from two warp reductions; the winning lane then
+    // finds its next best. The same choice as comparing (value, id) pairs.
     const int nsel = (K < E) ? K + 1 : K;
-    uint32_t taken = 0;
+    uint32_t key[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const uint32_t u = __float_as_uint(c[j] + 0.0f);
+        key[j] = (lane + 32 * j < E) ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
+    }
+    // best remaining candidate of this lane (the lowest j among equal keys)
+    auto head = [&](uint32_t& hk, uint32_t& he) {
+        hk = 0u;
+        he = 0xffffffffu;
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+            if (key[j] > hk) {
+                hk = key[j];
+                he = static_cast<uint32_t>(lane + 32 * j);
+            }
+    };
+    uint32_t hk, he;
+    head(hk, he);
     float my_val = 0.0f;
     int my_idx = 0;
     for (int it = 0; it < nsel; ++it) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < J; ++j) {
-            const int e = lane + 32 * j;
-            if (e < E && !((taken >> j) & 1u)) {
-                if (c[j] > bv || (c[j] == bv && e < bi)) {
-                    bv = c[j];
-                    bi = e;
-                }
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        if (lane == (bi & 31)) taken |= 1u << (bi >> 5);
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, hk);
+        const uint32_t me = __reduce_min_sync(0xffffffffu, hk == mk ? he : 0xffffffffu);
         if (lane == it) {
-            my_val = bv;
-            my_idx = bi;
+            my_val = __uint_as_float((mk & 0x80000000u) ? (mk & 0x7fffffffu) : ~mk);
+            my_idx = static_cast<int>(me);
+        }
+        if (he == me) {
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+                if (static_cast<uint32_t>(lane + 32 * j) == me) key[j] = 0u;
+            head(hk, he);
         }
     }
 
@@ -182,8 +192,9 @@ MOE_DEV void route_token_warp(const float (&r)[J], int t, const RouterArgs& a) {
 // Routes token t in one thread from all E logits in r[0..E-1] (E <= EP <= 8):
 // the same selection, ranking and weights as route_token_warp, for small E
 // where one lane is cheaper than the warp-wide search.
+// ids_out (optional): the K expert ids once more, ids_out[k].
 template <int EP>
-MOE_DEV void route_token_seq(const float (&r)[EP], int t, const RouterArgs& a) {
+MOE_DEV void route_token_seq(const float (&r)[EP], int t, const RouterArgs& a, int* ids_out = nullptr) {
     const int E = a.E, K = a.K;
     if (a.logits != nullptr) {
 #pragma unroll
@@ -242,56 +253,67 @@ MOE_DEV void route_token_seq(const float (&r)[EP], int t, const RouterArgs& a) {
             rank[e] = n;
         }
     }
-    auto slot = [&](int k, float& v, int& id, float& sgv) {
-        v = 0.0f;
-        id = 0;
-        sgv = 0.0f;
+    // the experts in rank order, built once (slot k: the expert of rank k; a
+    // slot no expert reaches holds zeros)
+    float ov[EP + 1], osg[EP + 1];
+    int oid[EP + 1];
 #pragma unroll
-        for (int e = 0; e < EP; ++e)
-            if (rank[e] == k) {
-                v = c[e];
-                id = e;
-                sgv = sg[e];
-            }
-    };
-    float v0, sg0;
-    int id0;
-    slot(0, v0, id0, sg0);
+    for (int k = 0; k <= EP; ++k) {
+        ov[k] = 0.0f;
+        osg[k] = 0.0f;
+        oid[k] = 0;
+    }
+#pragma unroll
+    for (int k = 0; k < EP; ++k) {
+        float v = 0.0f, g = 0.0f;
+        int id = 0;
+#pragma unroll
+        for (int e = 0; e < EP; ++e) {
+            const bool m = rank[e] == k;
+            v = m ? c[e] : v;
+            g = m ? sg[e] : g;
+            id = m ? e : id;
+        }
+        ov[k] = v;
+        osg[k] = g;
+        oid[k] = id;
+    }
+    const float v0 = ov[0];
+    float ex[EP];
     float sum = 0.0f;
 #pragma unroll
     for (int k = 0; k < EP; ++k) {
+        ex[k] = 0.0f;
         if (k < K) {
-            float v, sgv;
-            int id;
-            slot(k, v, id, sgv);
-            sum += a.gate == MOE_GATE_SOFTMAX_TOPK ? expf(v - v0)
-                   : a.gate == MOE_GATE_SOFTMAX_ALL_RENORM ? v : sgv;
+            ex[k] = a.gate == MOE_GATE_SOFTMAX_TOPK ? expf(ov[k] - v0)
+                    : a.gate == MOE_GATE_SOFTMAX_ALL_RENORM ? ov[k] : osg[k];
+            sum += ex[k];
         }
     }
     const bool normalise = a.gate != MOE_GATE_SIGMOID || a.renorm;
 #pragma unroll
     for (int k = 0; k < EP + 1; ++k) {
         if (k <= K && k < E) {
-            float v, sgv;
-            int id;
-            slot(k, v, id, sgv);
             if (k < K) {
-                float wk = a.gate == MOE_GATE_SOFTMAX_TOPK ? expf(v - v0)
-                           : a.gate == MOE_GATE_SOFTMAX_ALL_RENORM ? v : sgv;
+                float wk = ex[k < EP ? k : 0];
                 if (normalise) wk = wk / sum;
                 if (a.gate == MOE_GATE_SIGMOID) wk *= a.scale;
-                a.idx[static_cast<size_t>(t) * K + k] = id;
+                a.idx[static_cast<size_t>(t) * K + k] = oid[k];
                 a.w[static_cast<size_t>(t) * K + k] = wk;
+                if (ids_out != nullptr) ids_out[k] = oid[k];
             }
             if (a.top_scores != nullptr && a.gate == MOE_GATE_SIGMOID)
-                a.top_scores[static_cast<size_t>(t) * (K + 1) + k] = v;
+                a.top_scores[static_cast<size_t>(t) * (K + 1) + k] = ov[k];
         }
     }
     if (a.margin != nullptr) {
-        float vK1, vK, sgv;
-        int id;
-        slot(K - 1, vK1, id, sgv);
-        slot(K, vK, id, sgv);
+        // the values of rank K - 1 and K (zero where no expert has rank K)
+        float vK1 = 0.0f, vK = 0.0f;
+#pragma unroll
+        for (int e = 0; e < EP; ++e) {
+            vK1 = rank[e] == K - 1 ? c[e] : vK1;
+            vK = rank[e] == K ? c[e] : vK;
+        }
         a.margin[t] = (K < E) ? (vK1 - vK) : INFINITY;
     }
 }
