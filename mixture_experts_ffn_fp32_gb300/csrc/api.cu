@@ -445,6 +445,7 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
 
     if (bf) {
         float* ys = static_cast<float*>(P(L.ys));
+        int ys_f24 = 0;  // routed rows stored in the 24-bit blocked layout (ys24)
         float* shout = S ? static_cast<float*>(P(L.shout)) : nullptr;
         // 3. gather the routed rows into expert order
         if (!dg) {
@@ -484,6 +485,9 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
             if (S) g.g[1] = TcGroup{1, SF, P(L.hs), SF, T, w.Ws_down, nullptr, 1, c.d, shout, c.d, 1};
             g.E = E; g.offsets = offsets; g.mt_prefix = mt_prefix; g.swiglu = 0;
             g.rowscale0 = sorted_w; g.err = err;
+            // routed rows in the 24-bit blocked layout where the launch's form writes it
+            g.f24_ok = c.latent_dim == 0;
+            g.used_f24 = &ys_f24;
             if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
         }
         rec.end(ST_DOWN);
@@ -491,7 +495,8 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
         // 6. deterministic combine of the K routed rows of each token (+ shared)
         rec.begin(ST_COMBINE);
         if (!c.latent_dim) {
-            if ((e = launch_gather_sum(ys, inv, T, K, de, shout, out, !of32, s)) != cudaSuccess)
+            if ((e = ys_f24 ? launch_gather_sum_f24(ys, inv, T, K, de, shout, out, !of32, s)
+                            : launch_gather_sum(ys, inv, T, K, de, shout, out, !of32, s)) != cudaSuccess)
                 return cuda_status(e);
             rec.end(ST_COMBINE);
         } else {

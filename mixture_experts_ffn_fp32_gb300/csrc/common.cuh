@@ -419,4 +419,16 @@ MOE_DEV uint32_t pack_bf16x2(float lo, float hi) {
 MOE_DEV float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 MOE_DEV float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// 24-bit storage of an FP32 value: rounded to nearest (ties to even) at 16
+// significant bits and kept as the float's top 24 bits, returned as
+// (hi16 << 8) | lo8. Infinities pass through, a NaN stays a NaN, a finite
+// value that rounds past the largest float becomes an infinity (IEEE
+// rounding). f24_to_f32 puts the 24 bits back exactly.
+MOE_DEV uint32_t f32_to_f24(float v) {
+    const uint32_t u = __float_as_uint(v);
+    if ((u & 0x7F800000u) == 0x7F800000u) return (u >> 8) | ((u & 0x007FFFFFu) ? 0x4000u : 0u);
+    return (u + 0x7Fu + ((u >> 8) & 1u)) >> 8;
+}
+MOE_DEV float f24_to_f32(uint32_t hi16, uint32_t lo8) { return __uint_as_float((hi16 << 16) | (lo8 << 8)); }
+
 MOE_DEV float silu_f(float a) { return a / (1.0f + __expf(-a)); }

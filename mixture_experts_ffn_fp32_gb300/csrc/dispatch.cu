@@ -549,6 +549,79 @@ __global__ void __launch_bounds__(256) gather_sum_kernel(const float* __restrict
     }
 }
 
+// The combine with the routed rows in the 24-bit blocked layout (ys24): one
+// warp per (token, 256-column block), a lane's 8 columns being 16 bytes of
+// high parts and 8 of low parts in each routed row. Every row's raw parts are
+// loaded before the first is converted, and they are summed as they are put
+// back (exactly), in the same order as the FP32 combine.
+template <bool OUT_BF16, int KMAX>
+__global__ void __launch_bounds__(256) gather_sum_f24_kernel(const uint8_t* __restrict__ ys24,
+                                                             const int32_t* __restrict__ inv, int T,
+                                                             int K, int cols,
+                                                             const float* __restrict__ addend,
+                                                             void* __restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (t >= T) return;
+    const int lane = threadIdx.x & 31;
+    int pos[KMAX];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) pos[k] = (k < K) ? inv[static_cast<size_t>(t) * K + k] : 0;
+    const size_t pitch = static_cast<size_t>(cols) * 3;
+    for (int cb = blockIdx.y * YS24_BLOCK; cb < cols; cb += gridDim.y * YS24_BLOCK) {
+        const int c0 = cb + lane * 8;
+        const size_t boff = static_cast<size_t>(cb / YS24_BLOCK) * (3 * YS24_BLOCK);
+        uint4 h[KMAX];
+        uint2 l[KMAX];
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k) {
+            if (k < K) {
+                const uint8_t* blk = ys24 + static_cast<size_t>(pos[k]) * pitch + boff;
+                h[k] = __ldg(reinterpret_cast<const uint4*>(blk + 16 * lane));
+                l[k] = __ldg(reinterpret_cast<const uint2*>(blk + 2 * YS24_BLOCK + 8 * lane));
+            }
+        }
+        float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+        if (addend != nullptr) {
+            const float* p = addend + static_cast<size_t>(t) * cols + c0;
+            a0 = __ldg(reinterpret_cast<const float4*>(p));
+            a1 = __ldg(reinterpret_cast<const float4*>(p + 4));
+        }
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k) {
+            if (k < K) {
+                acc[0] += f24_to_f32(h[k].x & 0xFFFFu, l[k].x & 0xFFu);
+                acc[1] += f24_to_f32(h[k].x >> 16, (l[k].x >> 8) & 0xFFu);
+                acc[2] += f24_to_f32(h[k].y & 0xFFFFu, (l[k].x >> 16) & 0xFFu);
+                acc[3] += f24_to_f32(h[k].y >> 16, l[k].x >> 24);
+                acc[4] += f24_to_f32(h[k].z & 0xFFFFu, l[k].y & 0xFFu);
+                acc[5] += f24_to_f32(h[k].z >> 16, (l[k].y >> 8) & 0xFFu);
+                acc[6] += f24_to_f32(h[k].w & 0xFFFFu, (l[k].y >> 16) & 0xFFu);
+                acc[7] += f24_to_f32(h[k].w >> 16, l[k].y >> 24);
+            }
+        }
+        if (addend != nullptr) {
+            acc[0] += a0.x; acc[1] += a0.y; acc[2] += a0.z; acc[3] += a0.w;
+            acc[4] += a1.x; acc[5] += a1.y; acc[6] += a1.z; acc[7] += a1.w;
+        }
+        const size_t o = static_cast<size_t>(t) * cols + c0;
+        if (OUT_BF16) {
+            uint4 v;
+            v.x = pack_bf16x2(acc[0], acc[1]);
+            v.y = pack_bf16x2(acc[2], acc[3]);
+            v.z = pack_bf16x2(acc[4], acc[5]);
+            v.w = pack_bf16x2(acc[6], acc[7]);
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + o) = v;
+        } else {
+            float* q = static_cast<float*>(out) + o;
+            *reinterpret_cast<float4*>(q) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            *reinterpret_cast<float4*>(q + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+    }
+}
+
 // gather_sum stored as a BF16 hi/lo pair (see launch_gather_sum_split).
 __global__ void __launch_bounds__(256) gather_sum_split_kernel(const float* __restrict__ ys,
                                                                const int32_t* __restrict__ inv,
@@ -657,6 +730,27 @@ cudaError_t launch_gather_rows(const void* src, const int32_t* rowidx, int rows,
     const int blocks = (rows * 32 + 255) / 256;
     return launch_pdl(gather_rows_kernel, dim3(blocks), dim3(256), 0, s,
                       static_cast<const uint4*>(src), rowidx, rows, vpr, static_cast<uint4*>(dst));
+}
+
+cudaError_t launch_gather_sum_f24(const void* ys24, const int32_t* inv, int T, int K, int cols,
+                                  const float* addend, void* out, int out_bf16, cudaStream_t s) {
+    if (cols % YS24_BLOCK || K > 16) return cudaErrorInvalidValue;
+    const int blocks = (T * 32 + 255) / 256;
+    // the blocks of a token on separate CTAs when that keeps every SM busy
+    const int batches = cols / YS24_BLOCK;
+    const int want = (2 * num_sms() + blocks - 1) / blocks;
+    const dim3 g(blocks, static_cast<unsigned>(batches < want ? batches : (want > 0 ? want : 1)));
+    const uint8_t* y = static_cast<const uint8_t*>(ys24);
+#define MOE_GS24(KM)                                                                                  \
+    return out_bf16 ? launch_pdl(gather_sum_f24_kernel<true, KM>, g, dim3(256), 0, s, y, inv, T, K,    \
+                                 cols, addend, out)                                                  \
+                    : launch_pdl(gather_sum_f24_kernel<false, KM>, g, dim3(256), 0, s, y, inv, T, K,   \
+                                 cols, addend, out)
+    if (K <= 2) MOE_GS24(2);
+    if (K <= 4) MOE_GS24(4);
+    if (K <= 8) MOE_GS24(8);
+    MOE_GS24(16);
+#undef MOE_GS24
 }
 
 cudaError_t launch_gather_sum(const float* ys, const int32_t* inv, int T, int K, int cols,

@@ -1100,9 +1100,15 @@ __global__ void __launch_bounds__(THREADS, 1) tc_token_pair_kernel(const __grid_
                                      t.n - c, vch);
                 }
             } else {
-                const size_t pitch = static_cast<size_t>(p.out_ld[t.g]) * 4;
+                // FP32 rows, or the 24-bit blocked layout (a 256-feature pair unit is one block)
+                const bool f24 = p.out_f32[t.g] == 2;
+                const size_t pitch = static_cast<size_t>(p.out_ld[t.g]) * (f24 ? 3 : 4);
                 const int vch = lim <= 0 ? 0 : (lim >= 32 ? 8 : lim / 4);
-                char* base = static_cast<char*>(p.out[t.g]) + static_cast<size_t>(t.out_col0 + fl) * 4;
+                const int col = t.out_col0 + fl;
+                const size_t blk = static_cast<size_t>(col / YS24_BLOCK) * (3 * YS24_BLOCK);
+                const size_t hi_off = blk + 2 * (col % YS24_BLOCK), lo_off = blk + 2 * YS24_BLOCK + col % YS24_BLOCK;
+                char* rows0 = static_cast<char*>(p.out[t.g]);
+                char* base = rows0 + static_cast<size_t>(col) * 4;
                 // the row scales of this warp's 128 tokens, lane l holding tokens c0 + 32 j + l
                 float rs[4];
                 const bool scale = t.g == 0 && p.rowscale0 != nullptr;
@@ -1122,8 +1128,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_token_pair_kernel(const __grid_
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
                             v[e] = __shfl_sync(0xffffffffu, rs[i >> 1], 16 * (i & 1) + e) * __uint_as_float(r[e]);
-                        warp_store_f32_columns(stg, lane, v, base + static_cast<size_t>(t.row0 + c) * pitch, pitch,
-                                               t.n - c, vch);
+                        if (f24)
+                            warp_store_f24_columns(stg, lane, v, rows0 + static_cast<size_t>(t.row0 + c) * pitch, pitch,
+                                                   t.n - c, hi_off, lo_off);
+                        else
+                            warp_store_f32_columns(stg, lane, v, base + static_cast<size_t>(t.row0 + c) * pitch,
+                                                   pitch, t.n - c, vch);
                     }
                 }
             }
@@ -1420,6 +1430,8 @@ cudaError_t launch_token_t(const TcGemmArgs& a, int slots, cudaStream_t s) {
         p.out[g] = G.out;
         p.out_ld[g] = G.out_ld;
         p.out_f32[g] = G.out_f32;
+        // routed rows of a plain product in the 24-bit blocked layout, where allowed
+        if (!SWIGLU && g == 0 && a.f24_ok && G.out_f32 == 1 && G.N % YS24_BLOCK == 0) p.out_f32[g] = 2;
         const long long mt = (G.rows + SW_TOK - 1) / SW_TOK;
         units_bound += g == 0 ? (mt + a.E) * p.nt[0] : mt * G.Z * p.nt[1];
     }
@@ -1433,6 +1445,7 @@ cudaError_t launch_token_t(const TcGemmArgs& a, int slots, cudaStream_t s) {
     long long grid = slots;
     if (units_bound < grid) grid = units_bound;
     if (grid < 1) grid = 1;
+    if (a.used_f24 != nullptr) *a.used_f24 = p.enabled[0] && p.out_f32[0] == 2 ? 1 : 0;
     return launch_pdl_cluster(tc_token_pair_kernel<SWIGLU>, dim3(2 * static_cast<unsigned>(grid)),
                               dim3(THREADS), TGeo<SWIGLU>::SMEM_BYTES, s, 2, p);
 }
@@ -1478,6 +1491,7 @@ cudaError_t launch_tc_s(const TcGemmArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t s) {
+    if (a.used_f24 != nullptr) *a.used_f24 = 0;  // set by the token-column launch where it applies
     if (a.swiglu == TC_SWIGLU_BWD) return launch_tc_s<TC_SWIGLU_BWD>(a, s);
     if (a.swiglu == TC_PLAIN && a.g[1].enabled && a.g[1].kchunk > 0)
         return launch_tc_s<TC_PLAIN_ACC>(a, s);

@@ -196,6 +196,9 @@ cudaError_t launch_gather_rows(const void* src, const int32_t* rowidx, int rows,
 // last), stored BF16 or FP32. ys and addend are FP32; addend may be NULL.
 cudaError_t launch_gather_sum(const float* ys, const int32_t* inv, int T, int K, int cols,
                               const float* addend, void* out, int out_bf16, cudaStream_t s);
+// The same with the routed rows in the 24-bit blocked layout (ys24; cols % 256 == 0).
+cudaError_t launch_gather_sum_f24(const void* ys24, const int32_t* inv, int T, int K, int cols,
+                                  const float* addend, void* out, int out_bf16, cudaStream_t s);
 // Same sum, stored as two BF16 parts hi = bf16(v), lo = bf16(v - hi) in
 // out2 [T, 2*cols_pad]: hi in columns [0, cols), lo in [cols_pad, cols_pad + cols),
 // zeros elsewhere (hi + lo carries ~16 significant bits of v).
@@ -269,8 +272,19 @@ struct TcGemmArgs {
     const float* addend;         // group 1: add addend[r, col] (FP32 [rows1, add_ld])
     int add_ld;
     int* err;
+    // Group 0 of a plain product with FP32 output may instead be stored in the
+    // 24-bit blocked layout (ys24 below) where the launch takes a form that
+    // writes it: f24_ok allows it, *used_f24 (if set) tells whether it did.
+    int f24_ok = 0;
+    int* used_f24 = nullptr;
 };
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t s);
+
+// The 24-bit blocked row layout of routed rows (ys24): each row of N columns
+// (N % 256 == 0) is N / 256 blocks of 768 bytes; block b holds columns
+// 256 b .. 256 b + 255 as 256 16-bit high parts, then 256 8-bit low parts
+// (f32_to_f24). Row pitch 3 N bytes.
+constexpr int YS24_BLOCK = 256;
 
 // ---- FP32 SIMT grouped GEMM (same groups, FP32 everywhere) ----------------
 struct SimtGroup {

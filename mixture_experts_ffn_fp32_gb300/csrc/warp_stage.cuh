@@ -78,6 +78,34 @@ MOE_DEV void warp_store_f32_columns(uint4* stg, int lane, const float (&v)[16], 
     __syncwarp();
 }
 
+// The same 16 x 32 block in the 24-bit blocked layout (f32_to_f24): per row,
+// 32 16-bit high parts at hi_off and 32 8-bit low parts at lo_off (byte
+// offsets from the row's start); rows >= valid_rows are not written.
+MOE_DEV void warp_store_f24_columns(uint4* stg, int lane, const float (&v)[16], char* row0, size_t pitch,
+                                    int valid_rows, size_t hi_off, size_t lo_off) {
+    unsigned short* h = reinterpret_cast<unsigned short*>(stg);          // [16][32], 1 KB
+    unsigned char* l = reinterpret_cast<unsigned char*>(stg) + 1024;     // [16][32], 512 bytes
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t f = f32_to_f24(v[i]);
+        h[i * 32 + lane] = static_cast<unsigned short>(f >> 8);
+        l[i * 32 + lane] = static_cast<unsigned char>(f & 0xFFu);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int idx = lane + 32 * k, row = idx >> 2, ch = idx & 3;
+        if (row < valid_rows)
+            *reinterpret_cast<uint4*>(row0 + row * pitch + hi_off + ch * 16) = stg[idx];
+    }
+    {
+        const int row = lane >> 1, ch = lane & 1;
+        if (row < valid_rows)
+            *reinterpret_cast<uint4*>(row0 + row * pitch + lo_off + ch * 16) = stg[64 + lane];
+    }
+    __syncwarp();
+}
+
 // Loads the block in two steps, so that the global loads can be in flight
 // while other work runs: warp_load_issue reads it row-major (rows >=
 // valid_rows as zeros) into w, warp_load_finish turns w into the lane = row
