@@ -200,7 +200,8 @@ WsLayout plan_workspace(const moe_config& c) {
     L.ys = take(TK * de * 4);  // FP32: the K routed rows are summed before one final rounding
     // latent routed sum as a BF16 hi/lo pair, each part padded to a multiple of 64 columns
     L.routed = c.latent_dim ? take(T * 2 * static_cast<size_t>(latent_pad(c.latent_dim)) * 2) : 0;
-    L.shout = c.n_shared ? take(T * c.d * 4) : 0;  // FP32 shared-expert output
+    // FP32 shared-expert output (latent layers add the shared product inside the up-projection)
+    L.shout = (c.n_shared && !c.latent_dim) ? take(T * c.d * 4) : 0;
     L.xstage = take(T * c.d * es);
     L.ostage = take(T * c.d * (c.out_dtype == MOE_BF16 ? 2 : 4));
     L.qb = take(E * 4);
@@ -212,9 +213,12 @@ WsLayout plan_workspace(const moe_config& c) {
     L.logits = take(T * E * 4);
     L.stats_part = take(((T + STATS_TOKENS - 1) / STATS_TOKENS) * (2 * E + 1) * 4);
     L.dctr = take((E + 3) * 4);
+    // one-launch front end (E <= 8) or one-launch dispatch (larger batches): CTA tags
+    // and per-CTA count tables
     const bool fsw = bf && c.latent_dim == 0 && E <= 8 && TK > 1024 && TK <= DISPATCH_WIDE_MAX;
-    L.fs_tags = fsw ? take(FRONT_SMALL_MAX_CTAS * 128) : 0;
-    L.fs_cnt = fsw ? take(FRONT_SMALL_MAX_CTAS * 8 * 4) : 0;
+    const bool dow = bf && E <= 256 && TK > DISPATCH_WIDE_MAX && TK <= 1024ull * DISPATCH_ONEPASS_MAX_CTAS;
+    L.fs_tags = (fsw || dow) ? take(FRONT_SMALL_MAX_CTAS * 128) : 0;
+    L.fs_cnt = (fsw || dow) ? take(static_cast<size_t>(DISPATCH_ONEPASS_MAX_CTAS) * (E > 8 ? E : 8) * 4) : 0;
     L.total = o;
     return L;
 }
@@ -428,10 +432,16 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
     // (a stage without a launch records no events: its time is nil)
     const bool dg1 = bf && L.nchunks == 1;
     const bool dgw = bf && !dg1 && TK <= DISPATCH_WIDE_MAX;
-    const bool dg = dg1 || dgw || front;
+    const bool onepass = bf && !dg1 && !dgw && L.fs_tags != 0 && dispatch_onepass_ok(T, K, E);
+    const bool dg = dg1 || dgw || front || onepass;
     if (!front) rec.begin(ST_DISPATCH);
     if (front) {
         // done by the front-end launch
+    } else if (onepass) {
+        if ((e = launch_dispatch_gather_onepass(da, ex_src, de * 2, P(L.xs),
+                                                static_cast<unsigned long long*>(P(L.fs_tags)),
+                                                static_cast<int*>(P(L.fs_cnt)), s)) != cudaSuccess)
+            return cuda_status(e);
     } else if (dg1) {
         if ((e = launch_dispatch_gather(da, ex_src, de * 2, P(L.xs), s)) != cudaSuccess)
             return cuda_status(e);
@@ -446,7 +456,7 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
     if (bf) {
         float* ys = static_cast<float*>(P(L.ys));
         int ys_f24 = 0;  // routed rows stored in the 24-bit blocked layout (ys24)
-        float* shout = S ? static_cast<float*>(P(L.shout)) : nullptr;
+        float* shout = L.shout ? static_cast<float*>(P(L.shout)) : nullptr;
         // 3. gather the routed rows into expert order
         if (!dg) {
             rec.begin(ST_GATHER);
@@ -482,7 +492,9 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
         {
             TcGemmArgs g{};
             g.g[0] = TcGroup{1, c.d_ff, P(L.h), c.d_ff, TK, w.W_down, nullptr, E, de, ys, de, 1};
-            if (S) g.g[1] = TcGroup{1, SF, P(L.hs), SF, T, w.Ws_down, nullptr, 1, c.d, shout, c.d, 1};
+            // (latent layers: the shared experts' down product joins the up-projection below)
+            if (S && !c.latent_dim)
+                g.g[1] = TcGroup{1, SF, P(L.hs), SF, T, w.Ws_down, nullptr, 1, c.d, shout, c.d, 1};
             g.E = E; g.offsets = offsets; g.mt_prefix = mt_prefix; g.swiglu = 0;
             g.rowscale0 = sorted_w; g.err = err;
             // routed rows in the 24-bit blocked layout where the launch's form writes it
@@ -508,13 +520,20 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
             rec.end(ST_COMBINE);
             rec.begin(ST_LATENT_UP);
             TcGemmArgs g{};
+            // out = [routed hi | routed lo] [W_up_latent; W_up_latent] + hs Ws_down: the
+            // shared experts' down product as a second reduction segment of the same
+            // accumulation (no FP32 shared output written and read back)
             g.g[1] = TcGroup{1, 2 * Lp, P(L.routed), 2 * Lp, T, w.W_up_latent, nullptr, 1, c.d, out,
                              c.d, of32};
             g.g[1].b_kmod = Lp;
             g.g[1].b_rows = de;
+            if (S) {
+                g.g[1].A2 = P(L.hs);
+                g.g[1].lda2 = SF;
+                g.g[1].B2 = w.Ws_down;
+                g.g[1].K2 = SF;
+            }
             g.swiglu = 0; g.err = err;
-            g.addend = shout;
-            g.add_ld = c.d;
             if ((e = launch_tc_gemm(g, s)) != cudaSuccess) return cuda_status(e);
             rec.end(ST_LATENT_UP);
         }

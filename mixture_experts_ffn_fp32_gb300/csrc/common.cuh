@@ -166,6 +166,61 @@ MOE_DEV void release_add_gpu(unsigned* p, unsigned v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Grid barrier without initial state (one-launch kernels whose CTAs are all
+// resident): every CTA stores this launch's %gridid (unique per launch in a
+// context) into its own tag with release order and waits until every tag
+// carries it. Tags sit one per 128-byte line.
+constexpr int GRID_TAG_STRIDE = 16;  // 64-bit words between tags
+
+MOE_DEV unsigned long long grid_launch_id() {
+    unsigned long long g;
+    asm volatile("mov.u64 %0, %%gridid;" : "=l"(g));
+    return g;
+}
+
+MOE_DEV void st_release_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+MOE_DEV unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+MOE_DEV void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// Called by one whole warp of each CTA after the CTA's tag was stored: polls
+// tags lane, lane + 32, ... (relaxed loads, short sleeps between rounds), then
+// an acquire fence. False when timeout_ns ran out (the error word gets
+// ERRBIT_TIMEOUT).
+MOE_DEV bool grid_tags_wait(const unsigned long long* tags, int ntags, unsigned long long gid,
+                            uint64_t timeout_ns, int* err) {
+    const int lane = threadIdx.x & 31;
+    bool ok = true;
+    const uint64_t start = globaltimer_ns();
+    uint32_t pending = 0;
+    for (int q = 0; q < 32 && lane + 32 * q < ntags; ++q) pending |= 1u << q;
+    while (pending) {
+        uint32_t still = 0;
+        for (int q = 0; q < 32; ++q)
+            if ((pending >> q) & 1u)
+                if (ld_relaxed_u64(tags + GRID_TAG_STRIDE * (lane + 32 * q)) != gid) still |= 1u << q;
+        pending = still;
+        if (pending) {
+            if (globaltimer_ns() - start > timeout_ns) {
+                ok = false;
+                break;
+            }
+            __nanosleep(128);
+        }
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    fence_acq_rel_gpu();
+    if (!ok && lane == 0) atomicOr(err, ERRBIT_TIMEOUT);
+    return ok;
+}
+
 // Wait until *p >= target (bounded like bounded_wait).
 MOE_DEV bool bounded_wait_count(const unsigned* p, unsigned target, const WaitCtx& w) {
     if (ld_acquire_gpu(p) >= target) return true;

@@ -38,29 +38,6 @@ constexpr int FS_THREADS = 512;
 constexpr int FS_WARPS = FS_THREADS / 32;
 constexpr size_t FS_SMEM_MAX = 190 * 1024;  // dynamic; the static arrays take up to ~31 KB
 constexpr int FS_MAX_G = 256;  // blocks at most (one per SM)
-// tags one 128-byte line apart, so that the polls of all blocks spread over
-// many L2 lines instead of queueing on a few
-constexpr int FS_TAG_STRIDE = 16;
-
-MOE_DEV unsigned long long grid_id() {
-    unsigned long long g;
-    asm volatile("mov.u64 %0, %%gridid;" : "=l"(g));
-    return g;
-}
-
-MOE_DEV void st_release_u64(unsigned long long* p, unsigned long long v) {
-    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-MOE_DEV unsigned long long ld_relaxed_u64(const unsigned long long* p) {
-    unsigned long long v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Acquire side of the tags: after relaxed loads saw every tag, this fence
-// orders them before the loads of the counts (release-acquire through a fence).
-MOE_DEV void fence_acquire_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 template <int EP>
 __global__ void __launch_bounds__(FS_THREADS, 1) front_small_kernel(RouterArgs ra, DispatchArgs da, int tpc,
@@ -180,39 +157,16 @@ __global__ void __launch_bounds__(FS_THREADS, 1) front_small_kernel(RouterArgs r
         if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
     }
     __syncthreads();
-    const unsigned long long gid = grid_id();
+    const unsigned long long gid = grid_launch_id();
     if (threadIdx.x == 0) {
         // the counts, then the tag with release order (same thread)
 #pragma unroll
         for (int e = 0; e < EP; ++e) cnt[static_cast<size_t>(b) * EP + e] = s_cnt[e];
-        st_release_u64(tags + FS_TAG_STRIDE * b, gid);
+        st_release_u64(tags + GRID_TAG_STRIDE * b, gid);
     }
     if (warp == 0) {
-        // lane l watches tags l, l + 32, ... (all of its loads in flight each round)
-        bool ok = true;
-        const uint64_t start = globaltimer_ns();
-        uint32_t pending = 0;  // bit q: tag lane + 32 q not yet this launch's
-        for (int q = 0; q < 32 && lane + 32 * q < G; ++q) pending |= 1u << q;
-        while (pending) {
-            uint32_t still = 0;
-            for (int q = 0; q < 32; ++q)
-                if ((pending >> q) & 1u)
-                    if (ld_relaxed_u64(tags + FS_TAG_STRIDE * (lane + 32 * q)) != gid) still |= 1u << q;
-            pending = still;
-            if (pending) {
-                if (globaltimer_ns() - start > timeout_ns) {
-                    ok = false;
-                    break;
-                }
-                __nanosleep(128);  // fewer polls on the tags' lines while the writers arrive
-            }
-        }
-        ok = __all_sync(0xffffffffu, ok);
-        fence_acquire_gpu();  // the tags seen order the counts read below
-        if (lane == 0) {
-            s_ok = ok ? 1 : 0;
-            if (!ok) atomicOr(da.err, ERRBIT_TIMEOUT);
-        }
+        const bool ok = grid_tags_wait(tags, G, gid, timeout_ns, da.err);
+        if (lane == 0) s_ok = ok ? 1 : 0;
     }
     __syncthreads();
     if (!s_ok) return;

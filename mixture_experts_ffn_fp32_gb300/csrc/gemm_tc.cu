@@ -95,6 +95,10 @@ struct TcParams {
     uint32_t idesc;      // instruction descriptor (M = 128 or 256, N = 64 * nstrip)
     int ksplit1, kbs1;   // group 1 split-K: slices and k-blocks per slice
     int kchunk1;         // TC_PLAIN_ACC: k-blocks per tensor-memory chunk
+    // group 1, single-CTA plain: a second reduction segment (TcGroup::A2/B2)
+    // from k-block kseg2 on (0: none)
+    CUtensorMap mapA2, mapB2;
+    int kseg2, b2_wide;
     int E, mt1;
     const int32_t* offsets;
     const int32_t* mt_prefix;  // group 0 tiles of this kernel's rows (128, pair 256) per segment
@@ -207,8 +211,16 @@ struct UnitCopies {
     int akm, bkm, akg, akr;   // k-block remaps (0: none)
     int arow, nb, zb, bstrips;
     bool loadA, wide;
+    const CUtensorMap* mA2;   // second reduction segment (group 1, single-CTA plain): from k-block kbs2
+    const CUtensorMap* mB2;
+    int kbs2;
+    bool wide2;
 
     MOE_DEV UnitCopies(const TcParams& p, const Unit& t, int rank, int bstrips_) {
+        mA2 = &p.mapA2;
+        mB2 = &p.mapB2;
+        kbs2 = (t.g == 1 && p.kseg2 > 0) ? p.kseg2 : 0x7fffffff;
+        wide2 = p.b2_wide != 0;
         mA = &p.mapA[t.g];
         mB0 = (PAIR && SWIGLU && rank) ? &p.mapB1[t.g] : &p.mapB0[t.g];
         mB1 = &p.mapB1[t.g];
@@ -226,6 +238,17 @@ struct UnitCopies {
     }
 
     MOE_DEV void issue(int kb, uint32_t sA, uint32_t sB, uint32_t bar) const {
+        if (!PAIR && !SWIGLU && kb >= kbs2) {
+            // second segment: A2 [rows, K2] against B2 [1, K2, N], no remaps
+            const int kc2 = (kb - kbs2) * BK;
+            tma_load_2d(sA, mA2, kc2, arow, bar);
+            if (wide2) {
+                tma_load_4d(sB, mB2, 0, kc2, nb >> 6, 0, bar);
+            } else {
+                for (int j = 0; j < bstrips; ++j) tma_load_3d(sB + j * STRIP_BYTES, mB2, nb + 64 * j, kc2, 0, bar);
+            }
+            return;
+        }
         const int kc = kb * BK;
         int kca = akm ? kc % akm : kc;
         if (akg) kca = ((kb / (akg * akr)) * akg + kb % akg) * BK;
@@ -303,6 +326,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_grouped_gemm_kernel(const __gri
             tma_prefetch_map(&p.mapA[g]);
             tma_prefetch_map(&p.mapB0[g]);
             if (SWIGLU) tma_prefetch_map(&p.mapB1[g]);
+        }
+        if (p.kseg2 > 0) {
+            tma_prefetch_map(&p.mapA2);
+            tma_prefetch_map(&p.mapB2);
         }
     }
     if (warp == 1) {
@@ -1268,6 +1295,16 @@ cudaError_t launch_tc_t(const TcGemmArgs& a, int nstrip, int slots, cudaStream_t
             if (SWIGLU && !make_B_map(&p.mapB1[g], G.B1, G.Z, KB, G.N)) return cudaErrorInvalidValue;
         }
         p.kblocks[g] = (G.K + BK - 1) / BK;
+        if (G.A2 != nullptr) {
+            // a second reduction segment: group 1 of a single-CTA plain launch, whole k-blocks
+            if (g != 1 || PAIR || MODE != TC_PLAIN || G.K % BK || G.ksplit > 1 || G.K2 <= 0 || G.Z != 1)
+                return cudaErrorInvalidValue;
+            if (!make_A_map(&p.mapA2, G.A2, G.rows, G.K2, G.lda2)) return cudaErrorInvalidValue;
+            p.b2_wide = G.N % 64 == 0 && make_B_strip_map(&p.mapB2, G.B2, 1, G.K2, G.N, strips);
+            if (!p.b2_wide && !make_B_map(&p.mapB2, G.B2, 1, G.K2, G.N)) return cudaErrorInvalidValue;
+            p.kseg2 = p.kblocks[g];
+            p.kblocks[g] += (G.K2 + BK - 1) / BK;
+        }
         p.a_kmod[g] = G.a_kmod;
         p.b_kmod[g] = G.b_kmod;
         p.a_kgroup[g] = G.a_kgroup;

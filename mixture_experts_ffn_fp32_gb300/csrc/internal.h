@@ -184,6 +184,15 @@ cudaError_t launch_dispatch_gather_wide(const DispatchArgs& a, const void* src, 
 // 128-byte lines (one 64-bit tag each), cnt: FRONT_SMALL_MAX_CTAS * 8 ints of
 // scratch (no initial state needed).
 constexpr int FRONT_SMALL_MAX_CTAS = 256;
+
+// Dispatch and row gather in one cooperative launch (dispatch_onepass.cu) for
+// DISPATCH_WIDE_MAX < T*K <= 1024 * CTAs, E <= 256. tags: as for the front end
+// (DISPATCH_ONEPASS_MAX_CTAS 128-byte lines), cnt: DISPATCH_ONEPASS_MAX_CTAS * E
+// ints of scratch (no initial state needed).
+constexpr int DISPATCH_ONEPASS_MAX_CTAS = 256;
+bool dispatch_onepass_ok(int T, int K, int E);
+cudaError_t launch_dispatch_gather_onepass(const DispatchArgs& a, const void* src, int row_bytes, void* dst,
+                                           unsigned long long* tags, int* cnt, cudaStream_t s);
 bool front_small_ok(int T, int d, int E, int K);
 cudaError_t launch_front_small(const RouterArgs& ra, const DispatchArgs& da, void* xs,
                                unsigned long long* tags, int* cnt, cudaStream_t s);
@@ -240,6 +249,13 @@ struct TcGroup {
                         // product to out rows [s*rows, (s+1)*rows) (needs Z == 1)
     int kchunk = 0;     // TC_PLAIN_ACC, group 1: k-blocks per chunk (each slice a whole
                         // number of chunks)
+    // A second reduction segment (group 1 of a plain product, Z == 1, K a multiple
+    // of 64): out += A2 [rows, K2] (pitch lda2) times B2 [K2, N], accumulated with
+    // the first segment's product in one pass (the remaps above apply to the first).
+    const void* A2 = nullptr;
+    int lda2 = 0;
+    const void* B2 = nullptr;
+    int K2 = 0;
     // TC_SWIGLU: a_out / u_out (optional, both or neither, BF16 like out): the gate
     // and up products a = A B0, u = A B1 themselves, in out's rows, columns and pitch.
     void* a_out = nullptr;

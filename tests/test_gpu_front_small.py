@@ -92,3 +92,43 @@ def test_front_small_replays_in_a_graph(A):
         torch.cuda.synchronize()
         assert torch.equal(out.view(torch.int32), ref.view(torch.int32))
     assert A.workspace_status(ws) == A.MOE_OK
+
+
+# Larger prefill batches (16384 < T*K <= 1024 per SM): the dispatch and the row
+# gather in one cooperative launch with the same launch-id grid barrier.
+ONEPASS = {
+    "e64_k8": _wl("s_7", T=2500, d=256, d_ff=128, E=64, K=8, skew=1.2),
+    "e256_k6_ragged": _wl("s_8", T=3001, d=320, d_ff=64, E=256, K=6, n_shared=0, shared_d_ff=0),
+    "e8_k4_latent": _wl("s_9", T=4500, d=256, d_ff=128, E=8, K=4, gate="sigmoid", latent_dim=128),
+}
+
+
+@pytest.mark.parametrize("name", list(ONEPASS))
+def test_onepass_dispatch_equals_two_launch_dispatch(A, name):
+    w = ONEPASS[name]
+    assert 16384 < w.T * w.K <= 1024 * torch.cuda.get_device_properties(0).multi_processor_count
+    inp = W.make_inputs(w, device="cuda")
+    spec = A.LayerSpec.of(w)
+    ws = A.alloc_workspace(spec)
+    ws.fill_(0x3C)  # no initial state is needed
+    out = A.forward(spec, inp["x"], inp, ws=ws).clone()
+    assert A.workspace_status(ws) == A.MOE_OK
+    v = A.workspace_views(spec, ws)
+    dsp = A.dispatch(spec, v["idx"].clone(), v["w"].clone())
+    for k in ("counts", "offsets", "sorted_token", "inv"):
+        assert torch.equal(v[k].reshape(-1), dsp[k].reshape(-1)), k
+    assert torch.equal(v["sorted_w"].view(torch.int32), dsp["sorted_w"].view(torch.int32))
+    # replayed in a graph: the same bits
+    o2 = torch.empty_like(out)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        A.forward(spec, inp["x"], inp, out=o2, ws=ws, stream=s)
+    for _ in range(2):
+        o2.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(o2.view(torch.int32), out.view(torch.int32))
+    res = P.full_parity(w)
+    print(name, res)
