@@ -90,7 +90,7 @@ def swiglu_ffn(x, W_gate, W_up, W_down):
 
 def rank_experts(c):
     """Expert ids ordered by score descending; among equal scores the lower
-    expert id comes first (the tie-break this build fixes)."""
+    expert id comes first (the tie-break the library and this oracle share)."""
     c = f64(c)
     return np.argsort(-c, axis=-1, kind="stable")
 
