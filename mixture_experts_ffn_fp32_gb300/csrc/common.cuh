@@ -190,34 +190,25 @@ MOE_DEV unsigned long long ld_relaxed_u64(const unsigned long long* p) {
 
 MOE_DEV void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
-// Called by one whole warp of each CTA after the CTA's tag was stored: polls
-// tags lane, lane + 32, ... (relaxed loads, short sleeps between rounds), then
-// an acquire fence. False when timeout_ns ran out (the error word gets
-// ERRBIT_TIMEOUT).
-MOE_DEV bool grid_tags_wait(const unsigned long long* tags, int ntags, unsigned long long gid,
-                            uint64_t timeout_ns, int* err) {
-    const int lane = threadIdx.x & 31;
+// Called by every thread of each CTA once the CTA's tag was stored (ntags <=
+// blockDim.x): thread i watches tag i (relaxed loads), the CTA combines the
+// outcomes, and an acquire fence orders the tags seen before the loads that
+// follow. False when timeout_ns ran out (the error word gets ERRBIT_TIMEOUT).
+MOE_DEV bool grid_tags_wait_cta(const unsigned long long* tags, int ntags, unsigned long long gid,
+                                uint64_t timeout_ns, int* err) {
     bool ok = true;
-    const uint64_t start = globaltimer_ns();
-    uint32_t pending = 0;
-    for (int q = 0; q < 32 && lane + 32 * q < ntags; ++q) pending |= 1u << q;
-    while (pending) {
-        uint32_t still = 0;
-        for (int q = 0; q < 32; ++q)
-            if ((pending >> q) & 1u)
-                if (ld_relaxed_u64(tags + GRID_TAG_STRIDE * (lane + 32 * q)) != gid) still |= 1u << q;
-        pending = still;
-        if (pending) {
+    if (static_cast<int>(threadIdx.x) < ntags) {
+        const uint64_t start = globaltimer_ns();
+        while (ld_relaxed_u64(tags + GRID_TAG_STRIDE * threadIdx.x) != gid) {
             if (globaltimer_ns() - start > timeout_ns) {
                 ok = false;
                 break;
             }
-            __nanosleep(128);
         }
     }
-    ok = __all_sync(0xffffffffu, ok);
+    ok = __syncthreads_and(ok) != 0;
     fence_acq_rel_gpu();
-    if (!ok && lane == 0) atomicOr(err, ERRBIT_TIMEOUT);
+    if (!ok && threadIdx.x == 0) atomicOr(err, ERRBIT_TIMEOUT);
     return ok;
 }
 

@@ -41,7 +41,6 @@ __global__ void __launch_bounds__(DO_THREADS, 1) dispatch_onepass_kernel(Dispatc
     __shared__ int s_base[EMAX];
     __shared__ int s_wtot[8][3];
     __shared__ int s_pos[DO_THREADS], s_tok[DO_THREADS];
-    __shared__ int s_ok;
     pdl_wait();
     pdl_trigger();
     const int b = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
@@ -77,12 +76,7 @@ __global__ void __launch_bounds__(DO_THREADS, 1) dispatch_onepass_kernel(Dispatc
     __syncthreads();
     const unsigned long long gid = grid_launch_id();
     if (threadIdx.x == 0) st_release_u64(tags + GRID_TAG_STRIDE * b, gid);
-    if (warp == 0) {
-        const bool ok = grid_tags_wait(tags, G, gid, timeout_ns, a.err);
-        if (lane == 0) s_ok = ok ? 1 : 0;
-    }
-    __syncthreads();
-    if (!s_ok) return;
+    if (!grid_tags_wait_cta(tags, G, gid, timeout_ns, a.err)) return;
 
     // 3. expert totals and the counts of the CTAs before this one
     {

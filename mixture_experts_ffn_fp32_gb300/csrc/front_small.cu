@@ -49,7 +49,6 @@ __global__ void __launch_bounds__(FS_THREADS, 1) front_small_kernel(RouterArgs r
     __shared__ int s_cnt[EP], s_base[EP], s_rank[FS_WARPS][EP];
     __shared__ int s_pos[FS_WARPS * 32], s_tok[FS_WARPS * 32], s_ids[FS_WARPS * 32];
     __shared__ float s_logit[FS_WARPS * 32 * EP];  // the block's logits (tpc <= FS_WARPS * 32)
-    __shared__ int s_ok;
     __shared__ int s_all[FS_MAX_G * EP];  // every block's counts
     pdl_wait();
     pdl_trigger();
@@ -107,6 +106,7 @@ __global__ void __launch_bounds__(FS_THREADS, 1) front_small_kernel(RouterArgs r
         for (int e = 0; e < EP; ++e) acc[e] = acc2[e] = 0.0f;
         // lane l: d-index pairs k = 2 l + 64 m, m increasing (the standalone
         // router's order), one fused multiply-add chain per expert
+#pragma unroll 4
         for (int k = 2 * lane; k < d; k += 64) {
             const uint32_t va = xa[k >> 1], vb = xb[k >> 1];
             const float a0 = bf16_lo(va), a1 = bf16_hi(va), b0 = bf16_lo(vb), b1 = bf16_hi(vb);
@@ -164,12 +164,7 @@ __global__ void __launch_bounds__(FS_THREADS, 1) front_small_kernel(RouterArgs r
         for (int e = 0; e < EP; ++e) cnt[static_cast<size_t>(b) * EP + e] = s_cnt[e];
         st_release_u64(tags + GRID_TAG_STRIDE * b, gid);
     }
-    if (warp == 0) {
-        const bool ok = grid_tags_wait(tags, G, gid, timeout_ns, da.err);
-        if (lane == 0) s_ok = ok ? 1 : 0;
-    }
-    __syncthreads();
-    if (!s_ok) return;
+    if (!grid_tags_wait_cta(tags, G, gid, timeout_ns, da.err)) return;
 
     // 3. totals, offsets, the block's base per expert; ranks; rows
     for (int i = threadIdx.x; i < G * EP; i += FS_THREADS) s_all[i] = __ldcg(cnt + i);
