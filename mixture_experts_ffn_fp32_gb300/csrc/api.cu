@@ -208,17 +208,21 @@ WsLayout plan_workspace(const moe_config& c) {
     const bool chk = router_chunked(c);
     const bool tcr = router_on_tensor_cores(c) && !chk;
     L.w3 = tcr ? take(3 * static_cast<size_t>(c.d) * E * 2) : 0;
-    const size_t nsplit = chk ? router_chunked_nsplit(c.d, c.E) : router_ksplit(c.T, c.d);
+    // (decode batches: the one-launch decode router's partials, at most 32 slices)
+    const bool rdec = chk && c.T <= 128 && c.E > 128;
+    size_t nsplit = chk ? router_chunked_nsplit(c.d, c.E) : router_ksplit(c.T, c.d);
+    if (rdec && nsplit < 32) nsplit = 32;
     L.rpart = (tcr || chk) ? take(nsplit * T * E * 4) : 0;
     L.logits = take(T * E * 4);
     L.stats_part = take(((T + STATS_TOKENS - 1) / STATS_TOKENS) * (2 * E + 1) * 4);
     L.dctr = take((E + 3) * 4);
-    // one-launch front end (E <= 8) or one-launch dispatch (larger batches): CTA tags
-    // and per-CTA count tables
+    // one-launch front end (E <= 8), one-launch dispatch (larger batches) or decode
+    // router: CTA tag lines (the front end's count words), the dispatch's per-CTA
+    // count table
     const bool fsw = bf && c.latent_dim == 0 && E <= 8 && TK > 1024 && TK <= DISPATCH_WIDE_MAX;
     const bool dow = bf && E <= 256 && TK > DISPATCH_WIDE_MAX && TK <= 1024ull * DISPATCH_ONEPASS_MAX_CTAS;
-    L.fs_tags = (fsw || dow) ? take(FRONT_SMALL_MAX_CTAS * 128) : 0;
-    L.fs_cnt = (fsw || dow) ? take(static_cast<size_t>(DISPATCH_ONEPASS_MAX_CTAS) * (E > 8 ? E : 8) * 4) : 0;
+    L.fs_tags = (fsw || dow || rdec) ? take(FRONT_SMALL_MAX_CTAS * 128) : 0;
+    L.fs_cnt = dow ? take(static_cast<size_t>(DISPATCH_ONEPASS_MAX_CTAS) * (E > 8 ? E : 8) * 4) : 0;
     L.total = o;
     return L;
 }
@@ -286,8 +290,12 @@ static moe_status check_weights(const moe_config& c, const moe_weights* w) {
 static moe_status run_router(const moe_config& c, RouterArgs ra, const float* W_router,
                              const void* x, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
     if (ws != nullptr) ra.err_clear = reinterpret_cast<int*>(ws + L.err);
-    if (ws != nullptr && router_chunked(c))
+    if (ws != nullptr && router_chunked(c)) {
+        if (L.fs_tags != 0 && router_decode_ok(c.T, c.d, c.E, ra.x_bf16))
+            return cuda_status(launch_router_decode(ra, reinterpret_cast<float*>(ws + L.rpart),
+                                                    reinterpret_cast<unsigned long long*>(ws + L.fs_tags), s));
         return cuda_status(launch_router_chunked(ra, reinterpret_cast<float*>(ws + L.rpart), s));
+    }
     if (ws != nullptr && router_on_tensor_cores(c)) {
         ra.err_clear = nullptr;
         int* err = reinterpret_cast<int*>(ws + L.err);
@@ -382,8 +390,8 @@ static moe_status forward_impl(const moe_config& c, const void* x, const moe_wei
     if (front) {
         rec.begin(ST_FRONT);
         ra.err_clear = err;
-        if ((e = launch_front_small(ra, da, P(L.xs), static_cast<unsigned long long*>(P(L.fs_tags)),
-                                    static_cast<int*>(P(L.fs_cnt)), s)) != cudaSuccess)
+        if ((e = launch_front_small(ra, da, P(L.xs), static_cast<unsigned long long*>(P(L.fs_tags)), s)) !=
+            cudaSuccess)
             return cuda_status(e);
         rec.end(ST_FRONT);
     } else {

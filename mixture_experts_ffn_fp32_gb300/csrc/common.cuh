@@ -212,6 +212,17 @@ MOE_DEV bool grid_tags_wait_cta(const unsigned long long* tags, int ntags, unsig
     return ok;
 }
 
+// Asynchronous copies global -> shared (cp.async; 16 bytes: both addresses
+// 16-byte aligned, 4 bytes: 4-byte aligned), all completed by cp_async_wait_all
+// in the issuing thread (a __syncthreads then publishes them to the CTA).
+MOE_DEV void cp_async_16(void* sdst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sdst)), "l"(gsrc) : "memory");
+}
+MOE_DEV void cp_async_4(void* sdst, const void* gsrc) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(sdst)), "l"(gsrc) : "memory");
+}
+MOE_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Wait until *p >= target (bounded like bounded_wait).
 MOE_DEV bool bounded_wait_count(const unsigned* p, unsigned target, const WaitCtx& w) {
     if (ld_acquire_gpu(p) >= target) return true;

@@ -18,15 +18,16 @@
 //      warp per token (lane l takes the d-index pairs 2l + 64m in increasing m,
 //      the fused multiply-adds of the standalone router in the same order,
 //      then the same butterfly and the same per-token routing);
-//   2. its per-expert counts into its slot of a global table, then its tag
-//      (the launch's %gridid, unique per launch in a context) with release
-//      order; every CTA waits, with a time limit, until all tags carry this
-//      launch's id - a grid barrier that needs no zeroed memory, so a dirty
-//      workspace and graph replays are fine;
+//   2. ranks inside the range (warp match) and the CTA's per-expert counts,
+//      published as count words: each 64-bit word holds two experts' counts
+//      (10 bits each) under a 44-bit tag taken from the launch's %gridid
+//      (unique per launch in a context), stored with release order; every CTA
+//      waits, with a time limit, until all words carry this launch's tag - a
+//      grid barrier that needs no zeroed memory (a dirty workspace and graph
+//      replays are fine) and whose polls bring the counts along;
 //   3. expert totals, the CTA's prefix per expert (counts of the CTAs before
-//      it), offsets and tile prefixes (CTA 0 writes them), ranks inside the
-//      range (warp match), sorted_token / sorted_w / inv, and the rows copied
-//      into xs from shared memory.
+//      it), offsets and tile prefixes (CTA 0 writes them), sorted_token /
+//      sorted_w / inv, and the rows copied into xs from shared memory.
 #include "common.cuh"
 #include "internal.h"
 #include "route_dev.cuh"
@@ -39,15 +40,50 @@ constexpr int FS_WARPS = FS_THREADS / 32;
 constexpr size_t FS_SMEM_MAX = 190 * 1024;  // dynamic; the static arrays take up to ~31 KB
 constexpr int FS_MAX_G = 256;  // blocks at most (one per SM)
 
+// The count words' tag: 44 bits of the launch id, never zero (a zeroed word
+// never passes for a launch's).
+MOE_DEV unsigned long long fs_tag(unsigned long long gid) { return ((gid << 1) | 1ULL) & ((1ULL << 44) - 1); }
+
+// Every thread of each CTA, once the CTA's count words were stored: the G * EP/2
+// words (word q of CTA i: counts of experts 2q and 2q + 1 in bits 0-9 and 10-19)
+// are watched with relaxed loads until they carry this launch's tag, and their
+// counts go to s_all[i * EP + expert]. The counts travel inside the watched
+// words, so no other memory needs ordering. False when timeout_ns ran out (the
+// error word gets ERRBIT_TIMEOUT).
+template <int EP>
+MOE_DEV bool fs_wait_counts(const unsigned long long* tags, int G, unsigned long long tag, uint64_t timeout_ns,
+                            int* err, int* s_all) {
+    constexpr int NW = EP / 2;
+    bool ok = true;
+    const uint64_t start = globaltimer_ns();
+    for (int i = threadIdx.x; i < G * NW && ok; i += FS_THREADS) {
+        const int blk = i / NW, q = i - blk * NW;
+        const unsigned long long* p = tags + GRID_TAG_STRIDE * blk + q;
+        unsigned long long v = ld_relaxed_u64(p);
+        while ((v >> 20) != tag) {
+            if (globaltimer_ns() - start > timeout_ns) {
+                ok = false;
+                break;
+            }
+            v = ld_relaxed_u64(p);
+        }
+        s_all[blk * EP + 2 * q] = static_cast<int>(v & 1023u);
+        s_all[blk * EP + 2 * q + 1] = static_cast<int>((v >> 10) & 1023u);
+    }
+    ok = __syncthreads_and(ok) != 0;
+    if (!ok && threadIdx.x == 0) atomicOr(err, ERRBIT_TIMEOUT);
+    return ok;
+}
+
 template <int EP>
 __global__ void __launch_bounds__(FS_THREADS, 1) front_small_kernel(RouterArgs ra, DispatchArgs da, int tpc,
                                                                     void* __restrict__ xs,
                                                                     unsigned long long* __restrict__ tags,
-                                                                    int* __restrict__ cnt,
                                                                     uint64_t timeout_ns) {
     extern __shared__ __align__(16) uint8_t xsm[];
-    __shared__ int s_cnt[EP], s_base[EP], s_rank[FS_WARPS][EP];
+    __shared__ int s_base[EP], s_rank[FS_WARPS][EP];
     __shared__ int s_pos[FS_WARPS * 32], s_tok[FS_WARPS * 32], s_ids[FS_WARPS * 32];
+    __shared__ float s_wt[FS_WARPS * 32];  // the block's gate weights, in (token, slot) order
     __shared__ float s_logit[FS_WARPS * 32 * EP];  // the block's logits (tpc <= FS_WARPS * 32)
     __shared__ int s_all[FS_MAX_G * EP];  // every block's counts
     pdl_wait();
@@ -58,7 +94,6 @@ __global__ void __launch_bounds__(FS_THREADS, 1) front_small_kernel(RouterArgs r
     const int E = ra.E, K = ra.K, d = ra.d, T = ra.T;
     const int t0 = min(T, b * tpc), t1 = min(T, t0 + tpc);
     const int nt = t1 - t0;
-    if (threadIdx.x < EP) s_cnt[threadIdx.x] = 0;
     for (int i = threadIdx.x; i < FS_WARPS * EP; i += FS_THREADS) (&s_rank[0][0])[i] = 0;
 
     // 1. stage the block's x rows and W_router (EP columns, zero beyond E) with
@@ -146,49 +181,58 @@ __global__ void __launch_bounds__(FS_THREADS, 1) front_small_kernel(RouterArgs r
         float r[EP];
 #pragma unroll
         for (int e = 0; e < EP; ++e) r[e] = s_logit[threadIdx.x * EP + e];
-        route_token_seq<EP>(r, t0 + threadIdx.x, ra, s_ids + threadIdx.x * K);
+        route_token_seq<EP>(r, t0 + threadIdx.x, ra, s_ids + threadIdx.x * K, s_wt + threadIdx.x * K);
     }
-    __syncthreads();  // the block's ids are in s_ids
+    __syncthreads();  // the block's ids and gate weights are in shared memory
 
-    // 2. the block's counts and tag; wait for every block's
+    // 2. ranks inside the block's range (one assignment per thread: tpc * K <=
+    //    FS_THREADS), the block's counts as count words; wait for every block's
     const int j0 = t0 * K, j1 = t1 * K;
-    for (int j = threadIdx.x; j < j1 - j0; j += FS_THREADS) {
-        const int e = s_ids[j];
-        if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
-    }
+    const int j = j0 + static_cast<int>(threadIdx.x);
+    const bool mine = j < j1;
+    int e = mine ? s_ids[threadIdx.x] : -1;
+    if (e < 0 || e >= E) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (e >= 0 && rank == 0) s_rank[warp][e] = __popc(peers);
     __syncthreads();
-    const unsigned long long gid = grid_launch_id();
-    if (threadIdx.x == 0) {
-        // the counts, then the tag with release order (same thread)
+    const unsigned long long tag = fs_tag(grid_launch_id());
+    if (threadIdx.x < EP / 2) {
+        const int e0 = 2 * static_cast<int>(threadIdx.x);
+        unsigned long long c0 = 0, c1 = 0;
 #pragma unroll
-        for (int e = 0; e < EP; ++e) cnt[static_cast<size_t>(b) * EP + e] = s_cnt[e];
-        st_release_u64(tags + GRID_TAG_STRIDE * b, gid);
-    }
-    if (!grid_tags_wait_cta(tags, G, gid, timeout_ns, da.err)) return;
-
-    // 3. totals, offsets, the block's base per expert; ranks; rows
-    for (int i = threadIdx.x; i < G * EP; i += FS_THREADS) s_all[i] = __ldcg(cnt + i);
-    __syncthreads();
-    if (warp < EP) {
-        // warp e: the total of expert e and its count in the blocks before this one
-        int tot = 0, pre = 0;
-        if (warp < E)
-            for (int i = lane; i < G; i += 32) {
-                const int c = s_all[i * EP + warp];
-                tot += c;
-                pre += i < b ? c : 0;
-            }
-        tot = __reduce_add_sync(0xffffffffu, tot);
-        pre = __reduce_add_sync(0xffffffffu, pre);
-        if (lane == 0) {
-            s_cnt[warp] = tot;
-            s_base[warp] = pre;
+        for (int w = 0; w < FS_WARPS; ++w) {
+            c0 += static_cast<unsigned>(s_rank[w][e0]);
+            c1 += static_cast<unsigned>(s_rank[w][e0 + 1]);
         }
+        st_release_u64(tags + GRID_TAG_STRIDE * b + threadIdx.x, (tag << 20) | (c1 << 10) | c0);
     }
-    __syncthreads();
+    if (!fs_wait_counts<EP>(tags, G, tag, timeout_ns, da.err, s_all)) return;
+
+    // 3. warp 0: every expert's total and its count in the blocks before this
+    //    one, the scan into offsets and tile prefixes, the block's base per expert
     if (warp == 0) {
-        const int tot = lane < E ? s_cnt[lane] : 0;
-        const int pre = lane < E ? s_base[lane] : 0;
+        int tot_e[EP], pre_e[EP];
+#pragma unroll
+        for (int x = 0; x < EP; ++x) tot_e[x] = pre_e[x] = 0;
+        for (int i = lane; i < G; i += 32) {
+#pragma unroll
+            for (int x = 0; x < EP; ++x) {
+                const int c = s_all[i * EP + x];
+                tot_e[x] += c;
+                pre_e[x] += i < b ? c : 0;
+            }
+        }
+        int tot = 0, pre = 0;
+#pragma unroll
+        for (int x = 0; x < EP; ++x) {
+            const int tx = __reduce_add_sync(0xffffffffu, tot_e[x]);
+            const int px = __reduce_add_sync(0xffffffffu, pre_e[x]);
+            if (lane == x && x < E) {
+                tot = tx;
+                pre = px;
+            }
+        }
         const int bm = da.bm;
         const int m1 = (tot + bm - 1) / bm, m2 = (tot + 2 * bm - 1) / (2 * bm);
         int x = tot, x1 = m1, x2 = m2;
@@ -218,27 +262,18 @@ __global__ void __launch_bounds__(FS_THREADS, 1) front_small_kernel(RouterArgs r
             }
         }
     }
-    {
-        const int j = j0 + 32 * warp + lane;
-        const bool mine = j < j1;
-        int e = mine ? s_ids[j - j0] : -1;
-        if (e < 0 || e >= E) e = -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
-        const int rank = __popc(peers & ((1u << lane) - 1u));
-        if (e >= 0 && rank == 0) s_rank[warp][e] = __popc(peers);
-        __syncthreads();
-        if (mine) {
-            int pos = -1;
-            if (e >= 0) {
-                pos = s_base[e] + rank;
-                for (int w = 0; w < warp; ++w) pos += s_rank[w][e];
-                da.sorted_token[pos] = j / K;
-                da.sorted_w[pos] = ra.w[j];
-                da.inv[j] = pos;
-            }
-            s_pos[j - j0] = pos;
-            s_tok[j - j0] = j / K - t0;
+    __syncthreads();
+    if (mine) {
+        int pos = -1;
+        if (e >= 0) {
+            pos = s_base[e] + rank;
+            for (int w = 0; w < warp; ++w) pos += s_rank[w][e];
+            da.sorted_token[pos] = j / K;
+            da.sorted_w[pos] = s_wt[threadIdx.x];
+            da.inv[j] = pos;
         }
+        s_pos[threadIdx.x] = pos;
+        s_tok[threadIdx.x] = j / K - t0;
     }
     __syncthreads();
     const int vpr = d / 8;  // 16-byte pieces per row
@@ -269,7 +304,7 @@ bool front_small_ok(int T, int d, int E, int K) {
 }
 
 cudaError_t launch_front_small(const RouterArgs& ra, const DispatchArgs& da, void* xs,
-                               unsigned long long* tags, int* cnt, cudaStream_t s) {
+                               unsigned long long* tags, cudaStream_t s) {
     if (!front_small_ok(ra.T, ra.d, ra.E, ra.K) || !ra.x_bf16) return cudaErrorInvalidValue;
     const int G0 = num_sms() < FS_MAX_G ? num_sms() : FS_MAX_G;
     const int tpc = (ra.T + G0 - 1) / G0;
@@ -290,8 +325,8 @@ cudaError_t launch_front_small(const RouterArgs& ra, const DispatchArgs& da, voi
     }
     const uint64_t tmo = wait_timeout_ns();
     return which == 0
-        ? launch_pdl_coop(front_small_kernel<4>, dim3(G), dim3(FS_THREADS), smem, s, ra, da, tpc, xs, tags, cnt, tmo)
-        : launch_pdl_coop(front_small_kernel<8>, dim3(G), dim3(FS_THREADS), smem, s, ra, da, tpc, xs, tags, cnt, tmo);
+        ? launch_pdl_coop(front_small_kernel<4>, dim3(G), dim3(FS_THREADS), smem, s, ra, da, tpc, xs, tags, tmo)
+        : launch_pdl_coop(front_small_kernel<8>, dim3(G), dim3(FS_THREADS), smem, s, ra, da, tpc, xs, tags, tmo);
 }
 
 }  // namespace moe

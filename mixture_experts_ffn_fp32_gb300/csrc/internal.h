@@ -104,7 +104,7 @@ struct WsLayout {
     size_t ga, gu, gas, gus;  // saved gate / up products (save_gate_up): routed rows, shared
     size_t logits, stats_part;  // routing diagnostics: r [T, E], per-CTA partial sums
     size_t dctr;                // fused decode back end: counters [E + 3]
-    size_t fs_tags, fs_cnt;     // one-launch front end (front_small.cu): CTA tags, CTA counts
+    size_t fs_tags, fs_cnt;     // one-launch front end / dispatch: CTA tag lines, CTA counts (dispatch)
     size_t total;
     int nchunks;
 };
@@ -144,6 +144,13 @@ cudaError_t launch_route_from_logits(const float* part, int nsplit, const Router
                                      cudaStream_t s);
 // Tensor-core router used when x is BF16, E > 32, E % 8 == 0 and d % ROUTER_CHUNK == 0.
 bool router_on_tensor_cores(const moe_config& c);
+// Decode batches (T <= 128, 128 < E <= 256, d a multiple of 8 (BF16 x) or 4):
+// one cooperative launch reading W_router once (router.cu); part: [S, T, E]
+// FP32 (S = router_decode_slices), tags: FRONT_SMALL_MAX_CTAS 128-byte lines
+// (no initial state needed); a.err_clear must be set.
+bool router_decode_ok(int T, int d, int E, int x_bf16);
+int router_decode_slices(int T, int d, int E);
+cudaError_t launch_router_decode(const RouterArgs& a, float* part, unsigned long long* tags, cudaStream_t s);
 // Few tokens and E > 32: FP32 partial logits per 256-long slice of d on many
 // CTAs, summed and routed by route_from_logits (needs a workspace's rpart).
 bool router_chunked(const moe_config& c);
@@ -181,13 +188,13 @@ cudaError_t launch_dispatch_gather_wide(const DispatchArgs& a, const void* src, 
 
 // Router, dispatch and row gather in one cooperative launch (front_small.cu)
 // for BF16 x, E <= 8, 1024 < T*K <= DISPATCH_WIDE_MAX. tags: FRONT_SMALL_MAX_CTAS
-// 128-byte lines (one 64-bit tag each), cnt: FRONT_SMALL_MAX_CTAS * 8 ints of
-// scratch (no initial state needed).
+// 128-byte lines, each CTA's count words at the start of its line (no initial
+// state needed).
 constexpr int FRONT_SMALL_MAX_CTAS = 256;
 
 // Dispatch and row gather in one cooperative launch (dispatch_onepass.cu) for
-// DISPATCH_WIDE_MAX < T*K <= 1024 * CTAs, E <= 256. tags: as for the front end
-// (DISPATCH_ONEPASS_MAX_CTAS 128-byte lines), cnt: DISPATCH_ONEPASS_MAX_CTAS * E
+// DISPATCH_WIDE_MAX < T*K <= 1024 * CTAs, E <= 256. tags: DISPATCH_ONEPASS_MAX_CTAS
+// 128-byte lines (one 64-bit tag each), cnt: DISPATCH_ONEPASS_MAX_CTAS * E
 // ints of scratch (no initial state needed).
 constexpr int DISPATCH_ONEPASS_MAX_CTAS = 256;
 bool dispatch_onepass_ok(int T, int K, int E);
@@ -195,7 +202,7 @@ cudaError_t launch_dispatch_gather_onepass(const DispatchArgs& a, const void* sr
                                            unsigned long long* tags, int* cnt, cudaStream_t s);
 bool front_small_ok(int T, int d, int E, int K);
 cudaError_t launch_front_small(const RouterArgs& ra, const DispatchArgs& da, void* xs,
-                               unsigned long long* tags, int* cnt, cudaStream_t s);
+                               unsigned long long* tags, cudaStream_t s);
 
 // dst[r, :] = src[rowidx[r], :] for r < rows, row_bytes a multiple of 16.
 cudaError_t launch_gather_rows(const void* src, const int32_t* rowidx, int rows, int row_bytes,

@@ -192,9 +192,11 @@ MOE_DEV void route_token_warp(const float (&r)[J], int t, const RouterArgs& a) {
 // Routes token t in one thread from all E logits in r[0..E-1] (E <= EP <= 8):
 // the same selection, ranking and weights as route_token_warp, for small E
 // where one lane is cheaper than the warp-wide search.
-// ids_out (optional): the K expert ids once more, ids_out[k].
+// ids_out, w_out (optional): the K expert ids and gate weights once more,
+// ids_out[k] and w_out[k].
 template <int EP>
-MOE_DEV void route_token_seq(const float (&r)[EP], int t, const RouterArgs& a, int* ids_out = nullptr) {
+MOE_DEV void route_token_seq(const float (&r)[EP], int t, const RouterArgs& a, int* ids_out = nullptr,
+                             float* w_out = nullptr) {
     const int E = a.E, K = a.K;
     if (a.logits != nullptr) {
 #pragma unroll
@@ -301,6 +303,7 @@ MOE_DEV void route_token_seq(const float (&r)[EP], int t, const RouterArgs& a, i
                 a.idx[static_cast<size_t>(t) * K + k] = oid[k];
                 a.w[static_cast<size_t>(t) * K + k] = wk;
                 if (ids_out != nullptr) ids_out[k] = oid[k];
+                if (w_out != nullptr) w_out[k] = wk;
             }
             if (a.top_scores != nullptr && a.gate == MOE_GATE_SIGMOID)
                 a.top_scores[static_cast<size_t>(t) * (K + 1) + k] = ov[k];

@@ -479,10 +479,272 @@ ClusterRouterShape cluster_router_shape(int d, int E, int x_bf16) {
 
 constexpr size_t CLUSTER_ROUTER_SMEM_MAX = 200 * 1024;
 
+// Decode batches (T <= 128, 128 < E <= 256, where the cluster router would
+// stream its W_router slices through a ring) in one cooperative launch that
+// reads W_router once: CTA (s, eb) holds the d-slice s of every token's x row
+// and the 32 W_router columns of expert block eb in shared memory and forms
+// the partial logits of all tokens for those 32 experts (FP32 FMA chains over
+// the slice in increasing d); the partials go to global memory, then every
+// CTA stores its tag (the launch's %gridid, release order) and waits, with a
+// time limit, for all tags (no zeroed memory needed); CTA c then routes tokens
+// c, c + G, ...: each expert's logit is the sum of its slices' partials in
+// slice order. (The cluster router re-reads W_router once per 8-token block.)
+// The slices arrive by asynchronous 16-byte copies (one memory round trip, no
+// registers held); x is then transposed to [k][token] FP32. Thread layout of
+// the partial phase: warp w takes tokens 16 (w % WT) .. +15 over part w / WT
+// of the slice; lane l the 4 tokens 16 (w % WT) + 4 (l >> 3) .. and the 4
+// experts 4 (l & 7) .., so each k costs two 16-byte shared loads for 16 FMAs.
+// Parts of a slice are added in part order.
+constexpr int RD_THREADS = 512;
+constexpr int RD_WARPS = RD_THREADS / 32;
+constexpr int RD_EB = 32;    // experts per CTA
+constexpr int RD_TMAX = 128;  // tokens
+constexpr int RD_MAX_SLICES = 32;
+constexpr size_t RD_SMEM_MAX = 210 * 1024;
+
+// Row stride (elements) of the staged x slice [token][k]: 16-byte aligned
+// rows whose 16-byte chunks start in different bank groups for 8 consecutive
+// tokens (an odd number of chunks per row).
+__host__ __device__ __forceinline__ int router_decode_xs(int lens, bool bf16) {
+    const int per = bf16 ? 8 : 4;  // elements per 16-byte chunk
+    return ((lens / per) % 2 == 0) ? lens + per : lens;
+}
+
+struct RouterDecodeShape {
+    int neb, S, lens, G, tt, wt, kp;
+    size_t smem;
+};
+
+RouterDecodeShape router_decode_shape(int T, int d, int E, bool bf16) {
+    RouterDecodeShape sh{};
+    sh.neb = (E + RD_EB - 1) / RD_EB;
+    sh.tt = (T + 15) / 16 * 16;
+    sh.wt = sh.tt / 16;
+    sh.kp = sh.wt > 0 ? RD_WARPS / sh.wt : 1;
+    const int G0 = std::min(num_sms(), FRONT_SMALL_MAX_CTAS);
+    const int s0 = std::max(1, std::min(RD_MAX_SLICES, G0 / std::max(1, sh.neb)));
+    sh.lens = ((d + s0 - 1) / s0 + 7) / 8 * 8;
+    sh.S = (d + sh.lens - 1) / sh.lens;
+    sh.G = sh.S * sh.neb;
+    const size_t stage = static_cast<size_t>(sh.tt) * router_decode_xs(sh.lens, bf16) * (bf16 ? 2 : 4);
+    const size_t red = static_cast<size_t>(sh.kp - 1) * sh.wt * 32 * 16 * 4;
+    sh.smem = static_cast<size_t>(sh.lens) * (RD_EB + sh.tt) * 4 + std::max(stage, red);
+    return sh;
+}
+
+template <bool BF16, int EP>
+__global__ void __launch_bounds__(RD_THREADS, 1) router_decode_kernel(RouterArgs a, int S, int lens, int tt, int wt,
+                                                                      int kp, float* __restrict__ part,
+                                                                      unsigned long long* __restrict__ tags,
+                                                                      uint64_t timeout_ns) {
+    extern __shared__ __align__(16) float rsm[];
+    __shared__ float s_r[EP];
+    constexpr int J = EP / 32;
+    constexpr int ES = BF16 ? 2 : 4;  // x element bytes
+    constexpr int XV = 16 / ES;       // x elements per 16-byte chunk
+    pdl_wait();
+    pdl_trigger();
+    const int b = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
+    const int T = a.T, E = a.E, d = a.d;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (a.err_clear != nullptr && b == 0 && threadIdx.x == 0) clear_status(a.err_clear);
+    zero_counters(a, b == 0);
+    const int sl = b % S, eb = b / S;
+    const int k0 = sl * lens, kn = max(0, min(lens, d - k0));  // kn: a multiple of 8
+    const int e0 = eb * RD_EB;
+    const int xs = router_decode_xs(lens, BF16);
+    float* ws = rsm;                                     // [lens][32] W_router columns e0 ..
+    float* xt = ws + static_cast<size_t>(lens) * RD_EB;  // [lens][tt] x as FP32
+    uint8_t* xst = reinterpret_cast<uint8_t*>(xt + static_cast<size_t>(lens) * tt);  // [tt][xs] staged x
+    float* red = reinterpret_cast<float*>(xst);  // [kp - 1][wt][32][16], once the staged x is used
+
+    // 1. the slice of W_router and of every token's x row
+    if (E % 4 == 0) {
+        for (int q = threadIdx.x; q < kn * 8; q += RD_THREADS) {
+            const int k = q >> 3, c4 = q & 7, e = e0 + 4 * c4;
+            float* dst = ws + k * RD_EB + 4 * c4;
+            if (e < E)
+                cp_async_16(dst, a.W + static_cast<size_t>(k0 + k) * E + e);
+            else
+                *reinterpret_cast<float4*>(dst) = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+    } else {
+        for (int q = threadIdx.x; q < kn * RD_EB; q += RD_THREADS) {
+            const int k = q >> 5, c = q & 31, e = e0 + c;
+            float* dst = ws + k * RD_EB + c;
+            if (e < E)
+                cp_async_4(dst, a.W + static_cast<size_t>(k0 + k) * E + e);
+            else
+                *dst = 0.0f;
+        }
+    }
+    const int npc = kn / XV;  // 16-byte chunks per token
+    // chunk pc of token t: threads take consecutive tokens for one chunk (the
+    // first (RD_THREADS / tt) * tt threads)
+    const int cstep = RD_THREADS / tt;
+    const bool stager = static_cast<int>(threadIdx.x) < cstep * tt;
+    for (int pc = stager ? threadIdx.x / tt : npc; pc < npc; pc += cstep) {
+        const int t = threadIdx.x % tt;
+        uint8_t* dst = xst + (static_cast<size_t>(t) * xs + pc * XV) * ES;
+        if (t < T)
+            cp_async_16(dst, static_cast<const uint8_t*>(a.x) + (static_cast<size_t>(t) * d + k0 + pc * XV) * ES);
+        else
+            *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    // x to [k][token] FP32 (16-byte chunk reads, consecutive tokens per warp)
+    for (int pc = stager ? threadIdx.x / tt : npc; pc < npc; pc += cstep) {
+        const int t = threadIdx.x % tt;
+        const uint4 v = *reinterpret_cast<const uint4*>(xst + (static_cast<size_t>(t) * xs + pc * XV) * ES);
+        float f[XV];
+        if (BF16) {
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                f[2 * i] = bf16_lo(w4[i]);
+                f[(2 * i + 1) % XV] = bf16_hi(w4[i]);
+            }
+        } else {
+            f[0] = __uint_as_float(v.x);
+            f[1 % XV] = __uint_as_float(v.y);
+            f[2 % XV] = __uint_as_float(v.z);
+            f[3 % XV] = __uint_as_float(v.w);
+        }
+#pragma unroll
+        for (int i = 0; i < XV; ++i) xt[static_cast<size_t>(pc * XV + i) * tt + t] = f[i];
+    }
+    __syncthreads();
+
+    // 2. partial logits of the slice: 4 tokens x 4 experts per thread
+    const int pp = warp / wt, wtok = warp - pp * wt;
+    const int eg = lane & 7, tg = lane >> 3;
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+    if (pp < kp) {
+        const int kper = (kn + kp - 1) / kp;
+        const int kb = min(kn, pp * kper), ke = min(kn, kb + kper);
+        const float* wr = ws + eg * 4;
+        const float* xr = xt + wtok * 16 + tg * 4;
+#pragma unroll 4
+        for (int k = kb; k < ke; ++k) {
+            const float4 w0 = *reinterpret_cast<const float4*>(wr + k * RD_EB);
+            const float4 x0 = *reinterpret_cast<const float4*>(xr + static_cast<size_t>(k) * tt);
+            const float xa[4] = {x0.x, x0.y, x0.z, x0.w}, wa[4] = {w0.x, w0.y, w0.z, w0.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xa[i], wa[j], acc[i][j]);
+        }
+        if (pp > 0) {
+            float4* rp = reinterpret_cast<float4*>(red + ((static_cast<size_t>(pp - 1) * wt + wtok) * 32 + lane) * 16);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) rp[i] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        }
+    }
+    if (kp > 1) __syncthreads();
+    if (pp == 0) {
+        for (int q = 1; q < kp; ++q) {
+            const float4* rp =
+                reinterpret_cast<const float4*>(red + ((static_cast<size_t>(q - 1) * wt + wtok) * 32 + lane) * 16);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 v = rp[i];
+                acc[i][0] += v.x;
+                acc[i][1] += v.y;
+                acc[i][2] += v.z;
+                acc[i][3] += v.w;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int t = wtok * 16 + tg * 4 + i;
+            if (t < T) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int e = e0 + eg * 4 + j;
+                    if (e < E) part[(static_cast<size_t>(sl) * T + t) * E + e] = acc[i][j];
+                }
+            }
+        }
+    }
+    __syncthreads();
+    const unsigned long long gid = grid_launch_id();
+    if (threadIdx.x == 0) {
+        __threadfence();  // the CTA's partials (ordered by the barrier above) before the tag
+        st_release_u64(tags + GRID_TAG_STRIDE * b, gid);
+    }
+    if (!grid_tags_wait_cta(tags, G, gid, timeout_ns, a.err_clear)) return;
+
+    // 3. route tokens b, b + G, ...: expert e's logit in thread e, its slices
+    //    summed in slice order
+    for (int t = b; t < T; t += G) {
+        if (static_cast<int>(threadIdx.x) < EP) {
+            const int e = threadIdx.x;
+            float r = 0.0f;
+            if (e < E) {
+                float v[RD_MAX_SLICES];
+#pragma unroll
+                for (int q = 0; q < RD_MAX_SLICES; ++q)
+                    v[q] = q < S ? __ldcg(part + (static_cast<size_t>(q) * T + t) * E + e) : 0.0f;
+#pragma unroll
+                for (int q = 0; q < RD_MAX_SLICES; ++q)
+                    if (q < S) r += v[q];
+            }
+            s_r[e] = r;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            float rl[J];
+#pragma unroll
+            for (int j = 0; j < J; ++j) rl[j] = s_r[lane + 32 * j];
+            route_token_warp<J>(rl, t, a);
+        }
+        __syncthreads();
+    }
+}
+
 }  // namespace
+
+bool router_decode_ok(int T, int d, int E, int x_bf16) {
+    // up to 128 experts the cluster router holds its W_router slices in shared
+    // memory and sums them over a cluster barrier: faster than the grid barrier
+    if (T < 1 || T > RD_TMAX || E <= 128 || E > 256 || d % 16) return false;
+    const RouterDecodeShape sh = router_decode_shape(T, d, E, x_bf16 != 0);
+    return sh.G <= std::min(num_sms(), FRONT_SMALL_MAX_CTAS) && sh.S <= RD_MAX_SLICES && sh.smem <= RD_SMEM_MAX;
+}
+
+int router_decode_slices(int T, int d, int E) { return router_decode_shape(T, d, E, true).S; }
+
+cudaError_t launch_router_decode(const RouterArgs& a, float* part, unsigned long long* tags, cudaStream_t s) {
+    if (!router_decode_ok(a.T, a.d, a.E, a.x_bf16) || a.err_clear == nullptr || tags == nullptr)
+        return cudaErrorInvalidValue;
+    const RouterDecodeShape sh = router_decode_shape(a.T, a.d, a.E, a.x_bf16 != 0);
+    const uint64_t to = wait_timeout_ns();
+#define MOE_RD(B, EPV)                                                                                 \
+    {                                                                                                  \
+        static bool set = false;                                                                       \
+        if (!set) {                                                                                    \
+            const cudaError_t ea = cudaFuncSetAttribute(router_decode_kernel<B, EPV>,                  \
+                                                        cudaFuncAttributeMaxDynamicSharedMemorySize,   \
+                                                        static_cast<int>(RD_SMEM_MAX));                \
+            if (ea != cudaSuccess) return ea;                                                          \
+            set = true;                                                                                \
+        }                                                                                              \
+        return launch_pdl_coop(router_decode_kernel<B, EPV>, dim3(sh.G), dim3(RD_THREADS), sh.smem, s, a, \
+                               sh.S, sh.lens, sh.tt, sh.wt, sh.kp, part, tags, to);                    \
+    }
+    if (a.x_bf16) MOE_RD(true, 256)
+    MOE_RD(false, 256)
+#undef MOE_RD
+}
 
 bool router_one_launch(int T, int d, int E, int x_bf16) {
     if (E <= 32) return true;  // router_small_kernel
+    if (router_decode_ok(T, d, E, x_bf16)) return true;  // router_decode_kernel (with a workspace)
     // the cluster router (launch_router_chunked with a workspace)
     return E <= 256 && T <= 512 && cluster_router_shape(d, E, x_bf16).smem <= CLUSTER_ROUTER_SMEM_MAX;
 }

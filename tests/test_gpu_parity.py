@@ -187,13 +187,16 @@ def test_route(gate, E, K, dtype, d, with_ws):
 @pytest.mark.parametrize("gate,E,K", [("softmax_topk", 64, 8), ("softmax_topk", 256, 8),
                                       ("sigmoid", 128, 8), ("softmax_all_renorm", 100, 7),
                                       ("softmax_topk", 33, 16), ("sigmoid", 120, 4)])
-@pytest.mark.parametrize("dtype,d,T", [("bf16", 272, 200), ("f32", 1024, 64), ("bf16", 4096, 1)])
+@pytest.mark.parametrize("dtype,d,T", [("bf16", 272, 200), ("f32", 1024, 64), ("bf16", 4096, 1),
+                                       ("bf16", 4096, 128), ("bf16", 2048, 64), ("f32", 112, 33)])
 def test_route_few_tokens(gate, E, K, dtype, d, T):
-    """Up to 512 tokens with 32 < E <= 128 and a workspace: the FP32 cluster
-    router (partial logits per slice of d, at most 8 slices, summed in slice
-    order through distributed shared memory), including ragged last slices and
-    a single token; slices too wide for shared memory (E = 128, d = 4096) take
-    the two-launch chunked router; E = 256 takes the tensor-core or tiled router."""
+    """Few tokens with 32 < E <= 256 and a workspace. Up to 128 tokens and more
+    than 128 experts: the one-launch decode router (every CTA one slice of d for
+    32 experts and all tokens, partials summed in slice order after a grid
+    barrier), with ragged last slices, token counts that leave warps idle, a
+    single token and the 128-token, 4096-wide, 256-expert batch; otherwise the
+    FP32 cluster router (slices summed in slice order through distributed shared
+    memory)."""
     A = api()
     w = W.Workload("r", T=T, d=d, d_ff=16, E=E, K=K, n_shared=0, shared_d_ff=0, dtype=dtype,
                    gate=gate, bias_std=0.02, skew=0.5 if gate != "sigmoid" else 0.0)
