@@ -222,8 +222,9 @@ moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* topk_idx,
  *   graph; so can moe_backward.
  *   The grouped GEMMs pick their tile form from the shapes; the environment
  *   variable MOE_GEMM_FORM, read at each call, overrides the choice for tests
- *   and tuning ("rows": row-tile forms only; "tokens": the token-column form
- *   wherever the product allows it). The forms give the same bits except
+ *   and tuning ("rows": row-tile forms only; "single": single-CTA row tiles
+ *   only; "tokens": the token-column form wherever the product allows it).
+ *   The forms give the same bits except
  *   that the token-column down product stores its routed rows rounded to 16
  *   significant bits (a relative error of at most 2^-17 per routed row).
  * Sources: APEX-1 Math Ref Part 3 sections 12.2 and 13.2; APEX-1 docs

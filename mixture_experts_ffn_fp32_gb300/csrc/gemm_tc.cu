@@ -1435,7 +1435,7 @@ bool token_form_ok(const TcGemmArgs& a) {
         if (MODE == TC_SWIGLU && G.out_f32 != 0) return false;
     }
     const char* e = getenv("MOE_GEMM_FORM");
-    if (e != nullptr && e[0] == 'r') return false;
+    if (e != nullptr && (e[0] == 'r' || e[0] == 's')) return false;
     if (e != nullptr && e[0] == 't') return true;
     const long long E = a.E > 0 ? a.E : 1;
     return a.g[0].rows >= 128LL * E && a.g[0].rows < 512LL * E;
@@ -1503,8 +1503,10 @@ cudaError_t launch_tc_s(const TcGemmArgs& a, cudaStream_t s) {
     // down and up projections, the router) measured faster in the single-CTA
     // form (latent up projection 69 -> 60 us).
     const bool even = SWIGLU || nstrip % 2 == 0;
+    const char* form = getenv("MOE_GEMM_FORM");  // 's': single-CTA row tiles (tests, tuning)
     const bool long_segments =
-        !a.g[0].enabled || static_cast<long long>(a.g[0].rows) >= 512LL * (a.E > 0 ? a.E : 1);
+        (form == nullptr || form[0] != 's') &&
+        (!a.g[0].enabled || static_cast<long long>(a.g[0].rows) >= 512LL * (a.E > 0 ? a.E : 1));
     const bool dense_plain = MODE == TC_PLAIN && !a.g[0].enabled;
     if constexpr (MODE == TC_SWIGLU || MODE == TC_PLAIN) {
         if (token_form_ok<MODE>(a)) {
