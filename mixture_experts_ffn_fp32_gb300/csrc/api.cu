@@ -157,6 +157,9 @@ static TcGroup router_group(const void* x, int T, int d, int E, void* w3, void* 
 
 static int latent_pad(int L) { return (L + 63) / 64 * 64; }
 
+static_assert(GRID_EPOCH_LINE >= FRONT_SMALL_MAX_CTAS && GRID_EPOCH_LINE >= DISPATCH_ONEPASS_MAX_CTAS,
+              "the grid barrier's epoch line follows every CTA's tag line");
+
 WsLayout plan_workspace(const moe_config& c) {
     WsLayout L;
     memset(&L, 0, sizeof(L));
@@ -221,7 +224,7 @@ WsLayout plan_workspace(const moe_config& c) {
     // count table
     const bool fsw = bf && c.latent_dim == 0 && E <= 8 && TK > 1024 && TK <= DISPATCH_WIDE_MAX;
     const bool dow = bf && E <= 256 && TK > DISPATCH_WIDE_MAX && TK <= 1024ull * DISPATCH_ONEPASS_MAX_CTAS;
-    L.fs_tags = (fsw || dow || rdec) ? take(FRONT_SMALL_MAX_CTAS * 128) : 0;
+    L.fs_tags = (fsw || dow || rdec) ? take((GRID_EPOCH_LINE + 1) * 128) : 0;  // + the epoch line
     L.fs_cnt = dow ? take(static_cast<size_t>(DISPATCH_ONEPASS_MAX_CTAS) * (E > 8 ? E : 8) * 4) : 0;
     L.total = o;
     return L;

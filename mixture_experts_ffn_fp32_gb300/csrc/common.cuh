@@ -167,16 +167,12 @@ MOE_DEV void release_add_gpu(unsigned* p, unsigned v) {
 }
 
 // Grid barrier without initial state (one-launch kernels whose CTAs are all
-// resident): every CTA stores this launch's %gridid (unique per launch in a
-// context) into its own tag with release order and waits until every tag
-// carries it. Tags sit one per 128-byte line.
+// resident): every CTA stores this launch's tag (grid_epoch_tag: unique per
+// launch on a workspace, graph replays included) into its own tag with
+// release order and waits until every tag carries it. Tags sit one per
+// 128-byte line; the epoch word sits on line GRID_EPOCH_LINE.
 constexpr int GRID_TAG_STRIDE = 16;  // 64-bit words between tags
-
-MOE_DEV unsigned long long grid_launch_id() {
-    unsigned long long g;
-    asm volatile("mov.u64 %0, %%gridid;" : "=l"(g));
-    return g;
-}
+constexpr int GRID_EPOCH_LINE = 256;  // the epoch word's line, after 256 CTAs' tag lines
 
 MOE_DEV void st_release_u64(unsigned long long* p, unsigned long long v) {
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
@@ -189,6 +185,18 @@ MOE_DEV unsigned long long ld_relaxed_u64(const unsigned long long* p) {
 }
 
 MOE_DEV void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// The grid barrier's tag for this launch: one more than the epoch word that
+// the previous launch on the same workspace left there (read after
+// griddepcontrol.wait, so that launch has completed). Once every CTA has
+// read the word - after the barrier - CTA 0 stores the new value back
+// (grid_epoch_store), so each launch, eager or a replay of a captured graph
+// (whose launch parameters never change), waits for tags no earlier launch
+// wrote, and the tags need no zeroing.
+MOE_DEV unsigned long long grid_epoch_tag(const unsigned long long* epoch) { return ld_relaxed_u64(epoch) + 1ull; }
+MOE_DEV void grid_epoch_store(unsigned long long* epoch, unsigned long long tag) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) st_release_u64(epoch, tag);
+}
 
 // Called by every thread of each CTA once the CTA's tag was stored (ntags <=
 // blockDim.x): thread i watches tag i (relaxed loads), the CTA combines the

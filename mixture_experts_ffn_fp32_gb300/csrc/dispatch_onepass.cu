@@ -13,8 +13,8 @@
 //   1. each thread reads one assignment's expert id; warp match gives its rank
 //      among the warp's equal ids and the warp's count per expert;
 //   2. the CTA's count per expert goes to its row of a global table, then its
-//      tag (this launch's %gridid, release order); every CTA waits, with a time
-//      limit, until all tags carry this launch's id - no zeroed memory needed;
+//      tag (this launch's epoch tag, release order); every CTA waits, with a
+//      time limit, until all tags carry it - no zeroed memory needed;
 //   3. each CTA sums the table (its expert totals, and the counts of the CTAs
 //      before it), scans the totals into offsets and tile prefixes (CTA 0
 //      writes them), places its assignments (offset + earlier CTAs + earlier
@@ -43,6 +43,9 @@ __global__ void __launch_bounds__(DO_THREADS, 1) dispatch_onepass_kernel(Dispatc
     __shared__ int s_pos[DO_THREADS], s_tok[DO_THREADS];
     pdl_wait();
     pdl_trigger();
+    // this launch's tag (every thread reads the epoch before any CTA can pass the barrier)
+    unsigned long long* epoch = tags + GRID_TAG_STRIDE * GRID_EPOCH_LINE;
+    const unsigned long long gid = grid_epoch_tag(epoch);
     const int b = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int TK = a.T * a.K, E = a.E;
@@ -74,9 +77,10 @@ __global__ void __launch_bounds__(DO_THREADS, 1) dispatch_onepass_kernel(Dispatc
     }
     __threadfence();  // each writer orders its counts before the tag below
     __syncthreads();
-    const unsigned long long gid = grid_launch_id();
     if (threadIdx.x == 0) st_release_u64(tags + GRID_TAG_STRIDE * b, gid);
-    if (!grid_tags_wait_cta(tags, G, gid, timeout_ns, a.err)) return;
+    const bool okb = grid_tags_wait_cta(tags, G, gid, timeout_ns, a.err);
+    grid_epoch_store(epoch, gid);  // every CTA has read the epoch by now
+    if (!okb) return;
 
     // 3. expert totals and the counts of the CTAs before this one
     {

@@ -20,11 +20,12 @@
 //      then the same butterfly and the same per-token routing);
 //   2. ranks inside the range (warp match) and the CTA's per-expert counts,
 //      published as count words: each 64-bit word holds two experts' counts
-//      (10 bits each) under a 44-bit tag taken from the launch's %gridid
-//      (unique per launch in a context), stored with release order; every CTA
-//      waits, with a time limit, until all words carry this launch's tag - a
-//      grid barrier that needs no zeroed memory (a dirty workspace and graph
-//      replays are fine) and whose polls bring the counts along;
+//      (10 bits each) under a 44-bit tag taken from this launch's epoch tag
+//      (one more than the workspace's epoch word, which CTA 0 advances after
+//      the barrier), stored with release order; every CTA waits, with a time
+//      limit, until all words carry this launch's tag - a grid barrier that
+//      needs no zeroed memory (a dirty workspace and graph replays are fine)
+//      and whose polls bring the counts along;
 //   3. expert totals, the CTA's prefix per expert (counts of the CTAs before
 //      it), offsets and tile prefixes (CTA 0 writes them), sorted_token /
 //      sorted_w / inv, and the rows copied into xs from shared memory.
@@ -40,9 +41,9 @@ constexpr int FS_WARPS = FS_THREADS / 32;
 constexpr size_t FS_SMEM_MAX = 190 * 1024;  // dynamic; the static arrays take up to ~31 KB
 constexpr int FS_MAX_G = 256;  // blocks at most (one per SM)
 
-// The count words' tag: 44 bits of the launch id, never zero (a zeroed word
-// never passes for a launch's).
-MOE_DEV unsigned long long fs_tag(unsigned long long gid) { return ((gid << 1) | 1ULL) & ((1ULL << 44) - 1); }
+// The count words' tag: 44 bits of the launch's epoch tag, never zero (a
+// zeroed word never passes for a launch's).
+MOE_DEV unsigned long long fs_tag(unsigned long long ep) { return ((ep << 1) | 1ULL) & ((1ULL << 44) - 1); }
 
 // Every thread of each CTA, once the CTA's count words were stored: the G * EP/2
 // words (word q of CTA i: counts of experts 2q and 2q + 1 in bits 0-9 and 10-19)
@@ -88,6 +89,9 @@ __global__ void __launch_bounds__(FS_THREADS, 1) front_small_kernel(RouterArgs r
     __shared__ int s_all[FS_MAX_G * EP];  // every block's counts
     pdl_wait();
     pdl_trigger();
+    // this launch's tag (every thread reads the epoch before any CTA can pass the barrier)
+    unsigned long long* epoch = tags + GRID_TAG_STRIDE * GRID_EPOCH_LINE;
+    const unsigned long long ep = grid_epoch_tag(epoch);
     const int b = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (ra.err_clear != nullptr && b == 0 && threadIdx.x == 0) clear_status(ra.err_clear);
@@ -196,7 +200,7 @@ __global__ void __launch_bounds__(FS_THREADS, 1) front_small_kernel(RouterArgs r
     const int rank = __popc(peers & ((1u << lane) - 1u));
     if (e >= 0 && rank == 0) s_rank[warp][e] = __popc(peers);
     __syncthreads();
-    const unsigned long long tag = fs_tag(grid_launch_id());
+    const unsigned long long tag = fs_tag(ep);
     if (threadIdx.x < EP / 2) {
         const int e0 = 2 * static_cast<int>(threadIdx.x);
         unsigned long long c0 = 0, c1 = 0;
@@ -207,7 +211,9 @@ __global__ void __launch_bounds__(FS_THREADS, 1) front_small_kernel(RouterArgs r
         }
         st_release_u64(tags + GRID_TAG_STRIDE * b + threadIdx.x, (tag << 20) | (c1 << 10) | c0);
     }
-    if (!fs_wait_counts<EP>(tags, G, tag, timeout_ns, da.err, s_all)) return;
+    const bool okb = fs_wait_counts<EP>(tags, G, tag, timeout_ns, da.err, s_all);
+    grid_epoch_store(epoch, ep);  // every CTA has read the epoch by now
+    if (!okb) return;
 
     // 3. warp 0: every expert's total and its count in the blocks before this
     //    one, the scan into offsets and tile prefixes, the block's base per expert

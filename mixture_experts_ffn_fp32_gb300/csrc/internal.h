@@ -147,7 +147,7 @@ bool router_on_tensor_cores(const moe_config& c);
 // Decode batches (T <= 128, 128 < E <= 256, d a multiple of 8 (BF16 x) or 4):
 // one cooperative launch reading W_router once (router.cu); part: [S, T, E]
 // FP32 (S = router_decode_slices), tags: FRONT_SMALL_MAX_CTAS 128-byte lines
-// (no initial state needed); a.err_clear must be set.
+// and the epoch line (no initial state needed); a.err_clear must be set.
 bool router_decode_ok(int T, int d, int E, int x_bf16);
 int router_decode_slices(int T, int d, int E);
 cudaError_t launch_router_decode(const RouterArgs& a, float* part, unsigned long long* tags, cudaStream_t s);
@@ -188,13 +188,13 @@ cudaError_t launch_dispatch_gather_wide(const DispatchArgs& a, const void* src, 
 
 // Router, dispatch and row gather in one cooperative launch (front_small.cu)
 // for BF16 x, E <= 8, 1024 < T*K <= DISPATCH_WIDE_MAX. tags: FRONT_SMALL_MAX_CTAS
-// 128-byte lines, each CTA's count words at the start of its line (no initial
-// state needed).
+// 128-byte lines, each CTA's count words at the start of its line, then the
+// epoch line (no initial state needed).
 constexpr int FRONT_SMALL_MAX_CTAS = 256;
 
 // Dispatch and row gather in one cooperative launch (dispatch_onepass.cu) for
 // DISPATCH_WIDE_MAX < T*K <= 1024 * CTAs, E <= 256. tags: DISPATCH_ONEPASS_MAX_CTAS
-// 128-byte lines (one 64-bit tag each), cnt: DISPATCH_ONEPASS_MAX_CTAS * E
+// 128-byte lines (one 64-bit tag each) and the epoch line, cnt: DISPATCH_ONEPASS_MAX_CTAS * E
 // ints of scratch (no initial state needed).
 constexpr int DISPATCH_ONEPASS_MAX_CTAS = 256;
 bool dispatch_onepass_ok(int T, int K, int E);

@@ -485,8 +485,8 @@ constexpr size_t CLUSTER_ROUTER_SMEM_MAX = 200 * 1024;
 // and the 32 W_router columns of expert block eb in shared memory and forms
 // the partial logits of all tokens for those 32 experts (FP32 FMA chains over
 // the slice in increasing d); the partials go to global memory, then every
-// CTA stores its tag (the launch's %gridid, release order) and waits, with a
-// time limit, for all tags (no zeroed memory needed); CTA c then routes tokens
+// CTA stores its tag (this launch's epoch tag, release order) and waits, with
+// a time limit, for all tags (no zeroed memory needed); CTA c then routes tokens
 // c, c + G, ...: each expert's logit is the sum of its slices' partials in
 // slice order. (The cluster router re-reads W_router once per 8-token block.)
 // The slices arrive by asynchronous 16-byte copies (one memory round trip, no
@@ -544,6 +544,9 @@ __global__ void __launch_bounds__(RD_THREADS, 1) router_decode_kernel(RouterArgs
     constexpr int XV = 16 / ES;       // x elements per 16-byte chunk
     pdl_wait();
     pdl_trigger();
+    // this launch's tag (every thread reads the epoch before any CTA can pass the barrier)
+    unsigned long long* epoch = tags + GRID_TAG_STRIDE * GRID_EPOCH_LINE;
+    const unsigned long long gid = grid_epoch_tag(epoch);
     const int b = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
     const int T = a.T, E = a.E, d = a.d;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -672,12 +675,13 @@ __global__ void __launch_bounds__(RD_THREADS, 1) router_decode_kernel(RouterArgs
         }
     }
     __syncthreads();
-    const unsigned long long gid = grid_launch_id();
     if (threadIdx.x == 0) {
         __threadfence();  // the CTA's partials (ordered by the barrier above) before the tag
         st_release_u64(tags + GRID_TAG_STRIDE * b, gid);
     }
-    if (!grid_tags_wait_cta(tags, G, gid, timeout_ns, a.err_clear)) return;
+    const bool okb = grid_tags_wait_cta(tags, G, gid, timeout_ns, a.err_clear);
+    grid_epoch_store(epoch, gid);  // every CTA has read the epoch by now
+    if (!okb) return;
 
     // 3. route tokens b, b + G, ...: expert e's logit in thread e, its slices
     //    summed in slice order

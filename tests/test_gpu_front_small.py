@@ -92,6 +92,16 @@ def test_front_small_replays_in_a_graph(A):
         torch.cuda.synchronize()
         assert torch.equal(out.view(torch.int32), ref.view(torch.int32))
     assert A.workspace_status(ws) == A.MOE_OK
+    # new tokens in place: every replay routes and counts them anew (a replay
+    # must not pass the grid barrier on the previous replay's tags)
+    for seed in (3, 4, 5):
+        gen = torch.Generator(device="cuda").manual_seed(seed)
+        inp["x"].copy_(torch.randn(w.T, w.d, device="cuda", generator=gen).to(inp["x"].dtype))
+        g.replay()
+        torch.cuda.synchronize()
+        ref2 = A.forward(spec, inp["x"], inp, ws=A.alloc_workspace(spec))
+        assert torch.equal(out.view(torch.int32), ref2.view(torch.int32)), seed
+    assert A.workspace_status(ws) == A.MOE_OK
 
 
 # Larger prefill batches (16384 < T*K <= 1024 per SM): the dispatch and the row
@@ -130,5 +140,15 @@ def test_onepass_dispatch_equals_two_launch_dispatch(A, name):
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(o2.view(torch.int32), out.view(torch.int32))
+    # new tokens in place: the replay follows them
+    for seed in (3, 4):
+        gen = torch.Generator(device="cuda").manual_seed(seed)
+        src = inp["x"]
+        src.copy_(torch.randn(src.shape, device="cuda", generator=gen).to(src.dtype))
+        g.replay()
+        torch.cuda.synchronize()
+        ref2 = A.forward(spec, inp["x"], inp, ws=A.alloc_workspace(spec))
+        assert torch.equal(o2.view(torch.int32), ref2.view(torch.int32)), seed
+    assert A.workspace_status(ws) == A.MOE_OK
     res = P.full_parity(w)
     print(name, res)

@@ -62,6 +62,19 @@ def test_decode_router_dirty_workspace_and_graph(A, name):
         assert torch.equal(gr["idx"], g0["idx"])
         assert torch.equal(gr["w"].view(torch.int32), g0["w"].view(torch.int32))
     assert A.workspace_status(ws) == A.MOE_OK
+    # new tokens in place: each replay routes them anew (a replay must not pass
+    # the grid barrier on the previous replay's tags and partials)
+    x0 = inp["x"].clone()
+    for seed in (3, 4, 5):
+        gen = torch.Generator(device="cuda").manual_seed(seed)
+        inp["x"].copy_(torch.randn(inp["x"].shape, device="cuda", generator=gen).to(inp["x"].dtype))
+        graph.replay()
+        torch.cuda.synchronize()
+        e = A.route(spec, inp["x"], inp["W_router"], inp["bias"], ws=A.alloc_workspace(spec))
+        assert torch.equal(gr["idx"], e["idx"]), seed
+        assert torch.equal(gr["w"].view(torch.int32), e["w"].view(torch.int32)), seed
+    assert A.workspace_status(ws) == A.MOE_OK
+    inp["x"].copy_(x0)
     ort = P.oracle_routing(w, inp)
     near = ort["min_gap"] <= P.NEAR_TIE
     P.check_routing(w, ort, g0, near)
