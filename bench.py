@@ -158,6 +158,22 @@ def backward_flops(w) -> float:
     return f
 
 
+def backward_bytes(w, counts=None) -> float:
+    """Algorithmic HBM bytes of the backward: x, the upstream gradient (FP32)
+    and the weights of the experts that got tokens (+ shared, router, latent
+    projections) read once; dx and every weight gradient written once in FP32
+    (the gradients of experts without tokens are not written)."""
+    es = 4 if w.dtype == "f32" else 2
+    de = w.latent_dim or w.d
+    used = w.E if counts is None else int(sum(1 for c in counts if c > 0))
+    wts = used * 3 * de * w.d_ff + w.n_shared * 3 * w.d * w.shared_d_ff
+    lat = 2 * w.d * w.latent_dim if w.latent_dim else 0
+    b = (wts + lat) * (es + 4)          # weights read, their gradients written
+    b += w.d * w.E * (4 + 4)            # router weights read, gradient written
+    b += w.T * w.d * (es + 4 + 4)       # x and the upstream gradient read, dx written
+    return float(b)
+
+
 def layer_bytes(w, counts=None) -> float:
     """Algorithmic HBM bytes of one forward: weights of the experts that get
     tokens + shared + router weights + x read + out written (FP32 out)."""
@@ -581,6 +597,9 @@ def time_backward(api, W, layer, dev, stream, flush, n_bw, pk):
     f_re, b_re = run(layer.spec)
     bfl = backward_flops(w)
     bpk = pk["bf16_tflops"] if tc else pk["fp32_tflops"]
+    counts, _ = layer.routing_summary()
+    t_flop = bfl / (bpk * 1e12) * 1e3
+    t_hbm = backward_bytes(w, counts) / (pk["hbm_gbs"] * 1e9) * 1e3
     if tc:
         f_sv, bms = run(api.LayerSpec.of(w, save_gate_up=True))
     else:
@@ -588,6 +607,14 @@ def time_backward(api, W, layer, dev, stream, flush, n_bw, pk):
     return {"ms": bms, "tflops": bfl / (bms / 1e3) / 1e12, "flops_per_step": bfl,
             "bound": "tensor" if tc else "alu", "peak": bpk, "unit": "TFLOP/s",
             "frac": bfl / (bms / 1e3) / 1e12 / bpk,
+            "layer_roofline": {"t_flop_ms": t_flop, "t_hbm_ms": t_hbm,
+                               "bound": ("tensor" if tc else "alu") if t_flop >= t_hbm else "hbm",
+                               "frac": max(t_flop, t_hbm) / bms,
+                               "bytes_per_step": backward_bytes(w, counts),
+                               "note": "max(FLOPs / peak, algorithmic bytes / HBM copy rate) over the "
+                                       "backward's time; the bytes read x, the upstream gradient and "
+                                       "the used experts' weights once and write dx and every weight "
+                                       "gradient (FP32) once"},
             "forward_ms": f_sv, "training_step_ms": f_sv + bms,
             "recompute": {"ms": b_re, "forward_ms": f_re, "training_step_ms": f_re + b_re},
             "note": ("moe_backward (all gradients) after a forward on the same workspace; "
