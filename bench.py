@@ -196,9 +196,14 @@ def layer_roofline(w, ms, counts, pk) -> dict:
     t_flop = w.flops() / (fpk * 1e12)
     t_hbm = layer_bytes(w, counts) / (pk["hbm_gbs"] * 1e9)
     bound = ("alu" if f32 else "tensor") if t_flop >= t_hbm else "hbm"
-    return {"t_flop_ms": t_flop * 1e3, "t_hbm_ms": t_hbm * 1e3, "bound": bound,
-            "frac": max(t_flop, t_hbm) * 1e3 / ms, "peak_source": pk["source"],
-            "flop_peak": "FP32 FFMA" if f32 else "BF16 burst"}
+    r = {"t_flop_ms": t_flop * 1e3, "t_hbm_ms": t_hbm * 1e3, "bound": bound,
+         "frac": max(t_flop, t_hbm) * 1e3 / ms, "peak_source": pk["source"],
+         "flop_peak": "FP32 FFMA" if f32 else "BF16 burst"}
+    sus = pk.get("bf16_tflops_sustained")
+    if not f32 and sus:
+        # against the BF16 rate sustained for seconds under the power cap
+        r["frac_of_sustained"] = max(w.flops() / (sus * 1e12), t_hbm) * 1e3 / ms
+    return r
 
 
 def kernel_source_hash() -> str:
@@ -443,6 +448,11 @@ def gate_up_roofline(w, gu_ms, counts, pk, name):
                 "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                 "peak_source": f"{pk['source']} bf16 burst", "flops_per_launch": gu_flops}
     roof["frac"] = roof["achieved"] / roof["peak"] if roof["achieved"] else None
+    sus = pk.get("bf16_tflops_sustained")
+    if roof["bound"] == "tensor" and sus and roof["achieved"]:
+        # the same launch against the cuBLAS rate sustained for seconds under the power cap
+        roof["peak_sustained"] = sus
+        roof["frac_of_sustained"] = roof["achieved"] / sus
     traffic, note = profiled_traffic(name)
     roof["traffic"] = traffic
     if note:
